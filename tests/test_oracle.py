@@ -1,0 +1,270 @@
+"""Pins of the fp64 oracle to facts other than itself.
+
+The pages print no worked attention example (no inputs with outputs), so the
+oracle is pinned by: central finite differences of its own loss, closed forms
+(a hand-derived two-token case, uniform attention, T = 1, constant V),
+invariants (softmax rows sum to one, causality, GQA as repeated-KV MHA) and a
+library special case (PyTorch's fp64 CPU scaled_dot_product_attention with
+autograd).  Each test names the kind of mistake it is there to catch.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+def _case(seed, B, T, Hq, Hkv, D):
+    rng = np.random.default_rng(seed)
+    return (_rand(rng, B, T, Hq, D), _rand(rng, B, T, Hkv, D), _rand(rng, B, T, Hkv, D),
+            _rand(rng, B, T, Hq, D))
+
+
+def _rel(a, b, floor=1e-300):
+    """max |a - b| relative to max |b| (or to `floor` when b is all ~0)."""
+    return float(np.max(np.abs(a - b)) / max(floor, np.max(np.abs(b))))
+
+
+# ------------------------------------------------------------ closed forms
+def test_hand_derived_two_tokens():
+    """T=2, D=1, scale=1, q=(1,2), k=(1,-1), v=(3,5), dO=(0.5,-1.5).
+
+    Row 0 sees only key 0: LSE_0 = 1, O_0 = 3.  Row 1 has scores (2, -2):
+    with p = 1/(1+e^4) = P_11, LSE_1 = ln(e^2 + e^-2), O_1 = 3 + 2p.
+    Backward: dS_00 = 0, dS_10 = P_10 P_11 dO_1 (v_0 - v_1) = 3p(1-p) = -dS_11,
+    so dQ = (0, 6p(1-p)), dK = (6p(1-p), -6p(1-p)),
+    dV = (0.5 - 1.5(1-p), -1.5p).  Catches sign, transposition and masking
+    mistakes in every formula of the backward.
+    """
+    q = np.array([1.0, 2.0]).reshape(1, 2, 1, 1)
+    k = np.array([1.0, -1.0]).reshape(1, 2, 1, 1)
+    v = np.array([3.0, 5.0]).reshape(1, 2, 1, 1)
+    do = np.array([0.5, -1.5]).reshape(1, 2, 1, 1)
+    p = 1.0 / (1.0 + math.exp(4.0))
+    o, lse = oracle.attn_fwd(q, k, v, 1.0, True)
+    np.testing.assert_allclose(o.reshape(-1), [3.0, 3.0 + 2.0 * p], rtol=1e-15, atol=0)
+    np.testing.assert_allclose(lse.reshape(-1), [1.0, math.log(math.exp(2) + math.exp(-2))],
+                               rtol=1e-15)
+    dq, dk, dv, delta, worst = oracle.attn_bwd(q, k, v, do, 1.0, True)
+    s = 6.0 * p * (1.0 - p)
+    np.testing.assert_allclose(dq.reshape(-1), [0.0, s], rtol=1e-13, atol=1e-16)
+    np.testing.assert_allclose(dk.reshape(-1), [s, -s], rtol=1e-13)
+    np.testing.assert_allclose(dv.reshape(-1), [0.5 - 1.5 * (1.0 - p), -1.5 * p], rtol=1e-14)
+    np.testing.assert_allclose(delta.reshape(-1), [0.5 * 3.0, -1.5 * (3.0 + 2.0 * p)], rtol=1e-15)
+    assert worst < 1e-14
+
+
+def test_uniform_attention_when_q_is_zero():
+    """Q = 0 makes every visible score 0: P_ij = 1/(i+1), LSE_i = ln(i+1),
+    O_i = mean(V_0..V_i).  Catches an off-by-one in the causal range."""
+    B, T, Hq, Hkv, D = 2, 9, 4, 2, 5
+    _, k, v, _ = _case(1, B, T, Hq, Hkv, D)
+    q = np.zeros((B, T, Hq, D))
+    o, lse = oracle.attn_fwd(q, k, v, 0.3, True)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            for i in range(T):
+                assert abs(lse[b, h, i] - math.log(i + 1)) < 1e-14
+                ref = v[b, : i + 1, g, :].mean(axis=0)
+                np.testing.assert_allclose(o[b, i, h], ref, rtol=1e-13, atol=1e-14)
+    p = oracle.attn_probs(q, k, 1, 3, 0.3, True)
+    for i in range(T):
+        np.testing.assert_allclose(p[i, : i + 1], 1.0 / (i + 1), rtol=1e-14)
+
+
+def test_single_token():
+    """T = 1: O = V_0 and LSE = scale * q.k_0 (a one-term softmax)."""
+    q, k, v, _ = _case(2, 3, 1, 6, 3, 7)
+    o, lse = oracle.attn_fwd(q, k, v, 0.4, True)
+    for b in range(3):
+        for h in range(6):
+            g = h // 2
+            np.testing.assert_allclose(o[b, 0, h], v[b, 0, g], rtol=1e-15)
+            assert abs(lse[b, h, 0] - 0.4 * float(q[b, 0, h] @ k[b, 0, g])) < 1e-14
+
+
+def test_constant_v_rows():
+    """Every V row equal to v: O_i = v; then D_i = dO_i.v = dP_ij for every j,
+    so dS = 0 and dQ = dK = 0.  Catches a wrong D_i or a missing P factor."""
+    B, T, Hq, Hkv, D = 1, 11, 3, 1, 6
+    q, k, _, do = _case(3, B, T, Hq, Hkv, D)
+    vrow = np.linspace(-1.0, 2.0, D)
+    v = np.broadcast_to(vrow, (B, T, Hkv, D)).copy()
+    o, _ = oracle.attn_fwd(q, k, v, 0.5, True)
+    np.testing.assert_allclose(o, np.broadcast_to(vrow, o.shape), rtol=1e-15, atol=1e-15)
+    dq, dk, dv, _, _ = oracle.attn_bwd(q, k, v, do, 0.5, True)
+    assert np.max(np.abs(dq)) < 1e-14
+    assert np.max(np.abs(dk)) < 1e-14
+    assert np.max(np.abs(dv)) > 0.1
+
+
+# ------------------------------------------------------------ invariants
+@pytest.mark.parametrize("causal", [True, False])
+def test_softmax_rows_sum_to_one_and_mask(causal):
+    q, k, _, _ = _case(4, 2, 13, 4, 2, 8)
+    for b in range(2):
+        for h in range(4):
+            p = oracle.attn_probs(q, k, b, h, 0.35, causal)
+            assert np.max(np.abs(p.sum(axis=1) - 1.0)) <= 1e-12
+            assert np.all(p >= 0)
+            if causal:
+                assert np.all(p[np.triu_indices(13, 1)] == 0.0)
+            else:
+                assert np.all(p > 0)
+
+
+def test_causality_is_exact():
+    """Perturbing keys/values after position i leaves O_i and LSE_i
+    bit-identical.  Catches a mask that lets a later key leak in."""
+    B, T, Hq, Hkv, D = 2, 17, 4, 2, 8
+    q, k, v, _ = _case(5, B, T, Hq, Hkv, D)
+    o, lse = oracle.attn_fwd(q, k, v, 0.25, True)
+    for i0 in (0, 5, 16):
+        k2, v2 = k.copy(), v.copy()
+        rng = np.random.default_rng(i0)
+        k2[:, i0 + 1:] += rng.standard_normal(k2[:, i0 + 1:].shape) * 3
+        v2[:, i0 + 1:] -= rng.standard_normal(v2[:, i0 + 1:].shape) * 3
+        o2, lse2 = oracle.attn_fwd(q, k2, v2, 0.25, True)
+        assert np.array_equal(o2[:, : i0 + 1], o[:, : i0 + 1])
+        assert np.array_equal(lse2[:, :, : i0 + 1], lse[:, :, : i0 + 1])
+        if i0 < T - 1:
+            assert not np.array_equal(o2[:, i0 + 1:], o[:, i0 + 1:])
+
+
+@pytest.mark.parametrize("G", [2, 3])
+def test_gqa_is_repeated_kv_mha(G):
+    """GQA with group size G equals MHA with each KV head repeated G times
+    (query head h reads KV head h // G); dK/dV are the sums of the MHA
+    gradients over the group.  Catches a wrong head mapping (e.g. h % Hkv)."""
+    B, T, Hkv, D = 2, 10, 2, 4
+    Hq = Hkv * G
+    q, k, v, do = _case(6 + G, B, T, Hq, Hkv, D)
+    kr, vr = np.repeat(k, G, axis=2), np.repeat(v, G, axis=2)
+    o, lse = oracle.attn_fwd(q, k, v, 0.6, True)
+    o_m, lse_m = oracle.attn_fwd(q, kr, vr, 0.6, True)
+    assert np.array_equal(o, o_m) and np.array_equal(lse, lse_m)
+    dq, dk, dv, _, _ = oracle.attn_bwd(q, k, v, do, 0.6, True)
+    dq_m, dk_m, dv_m, _, _ = oracle.attn_bwd(q, kr, vr, do, 0.6, True)
+    np.testing.assert_allclose(dq, dq_m, rtol=1e-13, atol=1e-15)
+    dk_sum = dk_m.reshape(B, T, Hkv, G, D).sum(axis=3)
+    dv_sum = dv_m.reshape(B, T, Hkv, G, D).sum(axis=3)
+    assert _rel(dk, dk_sum) <= 1e-13
+    assert _rel(dv, dv_sum) <= 1e-13
+
+
+def test_delta_forms_agree():
+    """D_i = dO_i.O_i equals sum_j P_ij dP_ij (softmax Jacobian identity)."""
+    q, k, v, do = _case(9, 2, 33, 6, 2, 16)
+    *_, worst = oracle.attn_bwd(q, k, v, do, 0.25, True)
+    assert worst <= 1e-12
+
+
+# ------------------------------------------------------------ finite differences
+@pytest.mark.parametrize("causal", [True, False])
+def test_finite_differences(causal):
+    """Central differences of L = sum(dO * O) with h = 1e-6 in every entry of
+    Q, K and V match the closed-form dQ, dK, dV.  Catches any dropped term,
+    wrong sign or missing scale in the backward."""
+    B, T, Hq, Hkv, D = 1, 5, 2, 1, 3
+    q, k, v, do = _case(10, B, T, Hq, Hkv, D)
+    scale = 0.7
+    dq, dk, dv, _, _ = oracle.attn_bwd(q, k, v, do, scale, causal)
+
+    def loss(q_, k_, v_):
+        o, _ = oracle.attn_fwd(q_, k_, v_, scale, causal)
+        return float(np.sum(do * o))
+
+    h = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            fd[idx] = (loss(**{kk + "_": vv for kk, vv in args_p.items()}) -
+                       loss(**{kk + "_": vv for kk, vv in args_m.items()})) / (2 * h)
+        assert np.max(np.abs(fd - grad)) <= 1e-6 * max(1.0, np.max(np.abs(grad))), name
+
+
+# ------------------------------------------------------------ library special case
+def _torch_ref(q, k, v, do, scale, causal):
+    G = q.shape[2] // k.shape[2]
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64).permute(0, 2, 1, 3).contiguous()
+                  .requires_grad_(True) for x in (q, k, v))
+    kr = tk.repeat_interleave(G, dim=1)
+    vr = tv.repeat_interleave(G, dim=1)
+    o = torch.nn.functional.scaled_dot_product_attention(tq, kr, vr, is_causal=causal,
+                                                         scale=scale)
+    tdo = torch.tensor(do, dtype=torch.float64).permute(0, 2, 1, 3)
+    o.backward(tdo)
+    s = (tq @ kr.transpose(-1, -2)) * scale
+    if causal:
+        T = q.shape[1]
+        s = s.masked_fill(torch.triu(torch.ones(T, T, dtype=torch.bool), 1), float("-inf"))
+    lse = torch.logsumexp(s, dim=-1)
+    f = lambda t: t.detach().permute(0, 2, 1, 3).numpy()
+    return f(o), lse.detach().numpy(), f(tq.grad), f(tk.grad), f(tv.grad)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("shape", [(2, 37, 6, 2, 16), (1, 64, 4, 4, 32), (1, 1, 2, 1, 8)])
+def test_matches_torch_sdpa_fp64(shape, causal):
+    B, T, Hq, Hkv, D = shape
+    q, k, v, do = _case(11, *shape)
+    scale = 1.0 / math.sqrt(D)
+    o_r, lse_r, dq_r, dk_r, dv_r = _torch_ref(q, k, v, do, scale, causal)
+    o, lse = oracle.attn_fwd(q, k, v, scale, causal)
+    dq, dk, dv, _, _ = oracle.attn_bwd(q, k, v, do, scale, causal)
+    # With T = 1 the exact dQ and dK are 0 (one-term softmax); torch leaves
+    # ~1e-17 of rounding there, so the relative measure gets a floor of 1.
+    assert _rel(o, o_r) <= 1e-12
+    assert _rel(lse, lse_r) <= 1e-12
+    assert _rel(dq, dq_r, floor=1.0) <= 1e-12
+    assert _rel(dk, dk_r, floor=1.0) <= 1e-12
+    assert _rel(dv, dv_r) <= 1e-12
+
+
+# ------------------------------------------------------------ sampled rows, determinism
+def test_sampled_rows_match_full_oracle():
+    B, T, Hq, Hkv, D = 2, 40, 6, 2, 8
+    q, k, v, do = _case(12, B, T, Hq, Hkv, D)
+    for causal in (True, False):
+        o, lse = oracle.attn_fwd(q, k, v, 0.3, causal)
+        dq, dk, dv, _, _ = oracle.attn_bwd(q, k, v, do, 0.3, causal)
+        rows = [(0, 0, 0), (1, 5, 39), (0, 3, 17), (1, 2, 1)]
+        o_r, lse_r, dq_r = oracle.attn_rows(q, k, v, do, rows, 0.3, causal)
+        for s, (b, h, i) in enumerate(rows):
+            assert np.array_equal(o_r[s], o[b, i, h])
+            assert lse_r[s] == lse[b, h, i]
+            np.testing.assert_allclose(dq_r[s], dq[b, i, h], rtol=1e-12, atol=1e-15)
+        js = [0, 7, 39]
+        dk_r, dv_r = oracle.kv_rows(q, k, v, do, 1, 1, js, 0.3, causal)
+        for s, j in enumerate(js):
+            np.testing.assert_allclose(dk_r[s], dk[1, j, 1], rtol=1e-12, atol=1e-15)
+            np.testing.assert_allclose(dv_r[s], dv[1, j, 1], rtol=1e-12, atol=1e-15)
+
+
+def test_oracle_is_deterministic():
+    q, k, v, do = _case(13, 2, 50, 4, 2, 8)
+    a = oracle.attn_bwd(q, k, v, do, 0.3, True)
+    b = oracle.attn_bwd(q, k, v, do, 0.3, True)
+    for x, y in zip(a[:4], b[:4]):
+        assert x.tobytes() == y.tobytes()
+
+
+def test_bf16_widening_is_exact():
+    vals = torch.tensor([0.0, -0.0, 1.0, -2.5, 3.140625, 1e-30, 65280.0, float("inf")],
+                        dtype=torch.bfloat16)
+    bits = vals.view(torch.int16).numpy().view(np.uint16)
+    got = oracle.bf16_bits_to_f64(bits)
+    np.testing.assert_array_equal(got, vals.to(torch.float64).numpy())
