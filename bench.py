@@ -1,0 +1,513 @@
+"""Benchmark: causal GQA flash attention forward + backward on GB300.
+
+One step = the whole hot path on one batch: attn_fwd (Q K^T, online softmax,
+P V, LSE), then attn_bwd (Delta, dK/dV, dQ).  Default workload: one attention
+layer of the 16-layer d_model-768 GQA model at batch 4 x 1024 tokens
+(B=4, T=1024, Hq=12, Hkv=4, D=64, bf16), seeded synthetic inputs.
+
+Prints one JSON line.  `value` is algorithmic causal fwd+bwd TFLOPS
+(fwd = 2*B*Hq*T^2*D, fwd+bwd = 3.5x fwd) over all ranks; inputs are resident
+in HBM and rotate over enough sets that each step reads them from DRAM, not
+L2.  `e2e` is the same metric through the public API with host buffers
+(pinned host -> device copies of Q, K, V, dO and device -> host copies of O,
+LSE, dQ, dK, dV inside the timed region).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload page3]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
+
+With N > 1 (torchrun, one process per GPU) every rank runs its own replica of
+the workload (independent problems, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from deterministic_attention_gb300.inputs import WORKLOADS, workload_inputs  # noqa: E402
+
+METRIC = "causal attn fwd+bwd TFLOPS & % of GB300 BF16 peak; bitwise run-to-run repro"
+L2_BYTES = 129 * 2 ** 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {"bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ distributed
+def _dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"detattn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.remove(self.path)
+        if not rows:
+            return None
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max((float(r[2]) for r in rows if r[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ GPU arm
+class Problem:
+    """One replica's device buffers (several rotating sets) and the step."""
+
+    def __init__(self, w, n_sets, device):
+        import deterministic_attention_gb300 as da
+        self.da, self.w = da, w
+        B, T, Hq, Hkv, D = w.shape
+        q, k, v, do = workload_inputs(w)
+        self.host_in = [t.pin_memory() for t in (q, k, v, do)]
+        self.sets = []
+        for s in range(n_sets):
+            ins = [t.to(device) for t in (q, k, v, do)]
+            outs = dict(o=torch.empty_like(ins[0]), dq=torch.empty_like(ins[0]),
+                        dk=torch.empty_like(ins[1]), dv=torch.empty_like(ins[2]),
+                        lse=torch.empty((B, Hq, T), dtype=torch.float32, device=device),
+                        ws=torch.empty((max(16, da.workspace_bytes(*w.shape)),),
+                                       dtype=torch.uint8, device=device))
+            self.sets.append((ins, outs))
+        self.scale = w.softmax_scale
+
+    def set_bytes(self):
+        ins, outs = self.sets[0]
+        return sum(t.numel() * t.element_size() for t in list(ins) + list(outs.values()))
+
+    def step(self, s):
+        """fwd + bwd on set s (the four kernels of the hot path)."""
+        for which in ("fwd", "delta", "dkdv", "dq"):
+            self.kernel(which, s)
+
+    def kernel(self, which, s):
+        """One kernel of the step on set s (for per-kernel timing)."""
+        da = self.da
+        (q, k, v, do), o = self.sets[s % len(self.sets)]
+        delta = o["ws"][: 4 * o["lse"].numel()].view(torch.float32).view(o["lse"].shape)
+        if which == "fwd":
+            da.attn_fwd(q, k, v, scale=self.scale, out=o["o"], lse=o["lse"])
+        elif which == "delta":
+            da.attn_bwd_delta(o["o"], do, delta)
+        elif which == "dkdv":
+            da.attn_bwd_dkdv(q, k, v, o["lse"], delta, do, scale=self.scale, dk=o["dk"], dv=o["dv"])
+        else:
+            da.attn_bwd_dq(q, k, v, o["lse"], delta, do, scale=self.scale, dq=o["dq"])
+
+    def step_api(self, s):
+        """The public two-call API (attn_fwd + attn_bwd)."""
+        da = self.da
+        (q, k, v, do), o = self.sets[s % len(self.sets)]
+        da.attn_fwd(q, k, v, scale=self.scale, out=o["o"], lse=o["lse"])
+        da.attn_bwd(q, k, v, o["o"], o["lse"], do, scale=self.scale, dq=o["dq"], dk=o["dk"],
+                    dv=o["dv"], workspace=o["ws"])
+
+    def digests(self, s):
+        _, o = self.sets[s % len(self.sets)]
+        return tuple(hashlib.sha256(o[n].contiguous().view(torch.uint8).cpu().numpy().tobytes())
+                     .hexdigest() for n in ("o", "lse", "dq", "dk", "dv"))
+
+
+def _traffic_from_profiles(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if
+    the summary was taken on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, _, v = line.strip()[2:].partition(":")
+            vals[k.strip()] = v.strip().strip("`")
+    src = vals.get("source_sha256")
+    want = _kernel_source_sha()
+    if not src or src != want:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def _kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    cs = os.path.join(ROOT, "deterministic_attention_gb300", "csrc")
+    for f in ("sm103_ptx.cuh", "attn_launch.h", "attn_fwd.cu", "attn_bwd.cu"):
+        h.update(open(os.path.join(cs, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def _graph_time(fn, n_calls, replays):
+    """Captures `n_calls` calls of fn(i) in one CUDA graph, replays it
+    `replays` times and returns the average device ms per call (CUDA events
+    on the replay stream)."""
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for i in range(n_calls):  # warm up outside capture (kernel attributes, descriptors)
+            fn(i)
+    torch.cuda.current_stream().wait_stream(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n_calls):
+            fn(i)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (replays * n_calls), g
+
+
+def run_gpu_arm(args, world, rank):
+    import deterministic_attention_gb300 as da
+    da.build()
+    w = WORKLOADS[args.workload]
+    B, T, Hq, Hkv, D = w.shape
+    dev = torch.device("cuda", torch.cuda.current_device())
+    probe = Problem(w, 1, dev)
+    per_set = probe.set_bytes()
+    del probe
+    n_sets = max(1, math.ceil(1.5 * L2_BYTES / per_set))
+    P = Problem(w, n_sets, dev)
+
+    # Gate: finite outputs and bitwise-identical repeats before anything is timed.
+    ref = None
+    repro_runs = 20
+    for r in range(repro_runs):
+        P.step_api(0)
+        torch.cuda.synchronize()
+        d = P.digests(0)
+        ref = ref or d
+        if d != ref:
+            raise SystemExit(json.dumps({"error": "outputs differ between identical runs"}))
+    _, o0 = P.sets[0]
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        if not torch.isfinite(o0[n].float()).all():
+            raise SystemExit(json.dumps({"error": f"non-finite {n}"}))
+    da.check_status()
+
+    for i in range(args.warmup):
+        P.step(i)
+    torch.cuda.synchronize()
+
+    # Timed region: the K steps (fwd + Delta + dK/dV + dQ) replayed from one
+    # CUDA graph holding one step per rotating input set.
+    replays = max(1, math.ceil(args.steps / n_sets))
+    K = replays * n_sets
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.25)
+    _barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    step_ms, graph = _graph_time(P.step, n_sets, replays)
+    wall = time.perf_counter() - t0
+    _barrier(world)
+    clocks = sampler.stop()
+    da.check_status()
+    ms_step = _max_over_ranks(step_ms, world)
+
+    # Each kernel alone, K launches from a graph, for the per-kernel roofline.
+    kernels = {"attn_fwd": lambda i: P.kernel("fwd", i), "attn_bwd_delta": lambda i: P.kernel("delta", i),
+               "attn_bwd_dkdv": lambda i: P.kernel("dkdv", i), "attn_bwd_dq": lambda i: P.kernel("dq", i)}
+    per_kernel_ms = {}
+    for n, fn in kernels.items():
+        per_kernel_ms[n], _ = _graph_time(fn, n_sets, replays)
+
+    # The same steps launched one by one on the stream (no graph).
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    evs[0].record()
+    for i in range(K):
+        P.step_api(i)
+    evs[1].record()
+    torch.cuda.synchronize()
+    stream_ms = evs[0].elapsed_time(evs[1]) / K
+
+    flops = w.fwd_bwd_flops()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    peaks = _peaks()
+    peak = peaks["bf16_tflops"]
+    # Algorithmic work per launch of each kernel: per (b, h) head, forward
+    # 2 T^2 D flops (QK^T, PV over the causal half), dK/dV 4 T^2 D (S, dP, dV,
+    # dK), dQ T^2 D (the dQ product; its S/dP recompute is not counted).
+    heads = B * Hq
+    kflops = {"attn_fwd": 2.0 * heads * T * T * D, "attn_bwd_dkdv": 4.0 * heads * T * T * D,
+              "attn_bwd_dq": 1.0 * heads * T * T * D}
+    delta_bytes = B * T * Hq * D * 2 * 2 + B * Hq * T * 4
+    top = max(per_kernel_ms, key=per_kernel_ms.get)
+    if top == "attn_bwd_delta":
+        ach = delta_bytes / (per_kernel_ms[top] * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        ach = kflops[top] / (per_kernel_ms[top] * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = top
+    roof["peak_source"] = f"{peaks['source']} (burst)"
+    roof["traffic"] = _traffic_from_profiles(top, args.workload)
+    kernel_rates = {n: (kflops[n] / (v * 1e-3) / 1e12 if n in kflops
+                        else delta_bytes / (v * 1e-3) / 1e9) for n, v in per_kernel_ms.items()}
+
+    # End to end through the public API with host buffers.
+    hin = P.host_in
+    ins, outs = P.sets[0]
+    houts = {n: torch.empty(outs[n].shape, dtype=outs[n].dtype, pin_memory=True)
+             for n in ("o", "lse", "dq", "dk", "dv")}
+    n_e2e = max(3, min(K, 200))
+    h2d = sum(t.numel() * t.element_size() for t in hin)
+    d2h = sum(t.numel() * t.element_size() for t in houts.values())
+
+    def e2e_step():
+        for dst, src in zip(ins, hin):
+            dst.copy_(src, non_blocking=True)
+        P.step_api(0)
+        for n, h in houts.items():
+            h.copy_(outs[n], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n_e2e):
+        e2e_step()
+    b.record()
+    torch.cuda.synchronize()
+    e2e_ms = _max_over_ranks(a.elapsed_time(b) / n_e2e, world)
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+           "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, budget_s=args.cpu_budget)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "T": T, "Hq": Hq, "Hkv": Hkv, "D": D,
+                   "causal": True, "scale": w.softmax_scale, "seed": w.seed,
+                   "dout_std": w.dout_std,
+                   "l2": f"{n_sets} rotating input/output sets of {per_set / 2**20:.1f} MiB "
+                         f"({n_sets * per_set / 2**20:.0f} MiB vs 129 MiB L2)",
+                   "launch": f"CUDA graph of {n_sets} steps x 4 kernels, replayed {replays}x",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "flop_convention": "fwd 2*B*Hq*T^2*D (causal half), fwd+bwd 3.5x fwd"},
+        "pct_of_peak": value / world / peak,
+        "fwd_tflops": world * w.fwd_flops() / (per_kernel_ms["attn_fwd"] * 1e-3) / 1e12,
+        "stream_launch": {"value": world * flops / (stream_ms * 1e-3) / 1e12, "ms_per_step": stream_ms},
+        "kernels_ms": per_kernel_ms,
+        "kernel_rates": kernel_rates,
+        "roofline": roof,
+        "repro": {"runs": repro_runs, "sha256_identical": True},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": 4 * K,
+        "wall_s_timed": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ CPU oracle
+def _oracle_sample(w, T_s, n_groups):
+    """fp64 inputs of a bounded sample: batch 0, KV groups 0..n_groups-1 (all
+    their query heads), the first T_s positions (a causal prefix is itself a
+    complete causal problem)."""
+    import oracle
+    from deterministic_attention_gb300.inputs import bf16_bits
+    q, k, v, do = workload_inputs(w)
+    G = w.Hq // w.Hkv
+    sl = lambda t, hs: t[:1, :T_s, hs].contiguous()
+    qs = sl(q, slice(0, n_groups * G))
+    ks, vs = sl(k, slice(0, n_groups)), sl(v, slice(0, n_groups))
+    dos = sl(do, slice(0, n_groups * G))
+    f = lambda t: oracle.bf16_bits_to_f64(bf16_bits(t)).reshape(tuple(t.shape))
+    return tuple(f(t) for t in (qs, ks, vs, dos))
+
+
+def _oracle_step(w, xs):
+    import oracle
+    q, k, v, do = xs
+    oracle.attn_fwd(q, k, v, w.softmax_scale, True)
+    oracle.attn_bwd(q, k, v, do, w.softmax_scale, True)
+
+
+def cpu_baseline(w, budget_s=20.0):
+    """The oracle as it stands, on host cores, on a bounded sample."""
+    import oracle
+    G = w.Hq // w.Hkv
+    xs = _oracle_sample(w, w.T, 1)
+    t0 = time.perf_counter()
+    _oracle_step(w, xs)
+    one = time.perf_counter() - t0
+    n_groups = max(1, min(w.Hkv, int(budget_s / max(one, 1e-3))))
+    xs = _oracle_sample(w, w.T, n_groups)
+    t0 = time.perf_counter()
+    _oracle_step(w, xs)
+    dt = time.perf_counter() - t0
+    flops = 3.5 * 2.0 * n_groups * G * w.T * w.T * w.D
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"batch 0, KV heads 0..{n_groups - 1} with their {n_groups * G} query heads, "
+                      f"all T={w.T} positions: fwd + bwd in fp64"}
+
+
+def run_reference_arm(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = WORKLOADS[args.workload]
+    G = w.Hq // w.Hkv
+    # Size the per-step sample (a causal prefix of one KV group) so the whole
+    # run stays within a few minutes.
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    T_s = w.T
+    while True:
+        xs = _oracle_sample(w, T_s, 1)
+        t0 = time.perf_counter()
+        _oracle_step(w, xs)
+        one = time.perf_counter() - t0
+        if one <= budget or T_s <= 16:
+            break
+        T_s = max(16, int(T_s / math.sqrt(one / budget) * 0.9))
+    for _ in range(args.warmup):
+        _oracle_step(w, xs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(w, xs)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    flops = 3.5 * 2.0 * G * T_s * T_s * w.D
+    value = flops / dt / 1e12
+    sample = (f"per step: batch 0, KV head 0 with its {G} query heads, causal prefix of "
+              f"T={T_s} of {w.T} positions, fwd + bwd in fp64")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                   "causal": True},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="page3", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank = _dist_init()
+    try:
+        if args.impl == "reference":
+            run_reference_arm(args, world, rank)
+        else:
+            run_gpu_arm(args, world, rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,683 @@
+// Deterministic flash-attention backward for sm_103a: Delta preprocess,
+// dK/dV kernel and dQ kernel.
+//
+// RustingBrain vs PyTorch/TensorFlow page, "Step 2: fused flash attention"
+// (the backward is fused too) and "Where the time goes now" (the dK/dV kernel
+// flash_attention_dkv recomputes the probabilities and dominates the
+// backward).  oxide-train README, "The trainer is not bit-identical to itself
+// after step 1": gradients summed with atomics change from run to run.  Here
+// every output element is written once, by the one block that owns its tile,
+// after a reduction whose order is fixed:
+//   * Delta_i = sum_d dO_id O_id       one warp per 32 rows, fixed shuffle tree
+//   * dK_j, dV_j                       one block per (b, KV head, 128-key tile);
+//                                      query heads of the group in ascending
+//                                      order, query tiles ascending, all summed
+//                                      in the block's TMEM accumulators
+//   * dQ_i                             one block per (b, query head, 128-query
+//                                      tile); key tiles ascending
+// The probabilities are recomputed from LSE: P = exp2(S * scale * log2e -
+// LSE * log2e), dS = P * (dP - Delta).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_launch.h"
+#include "sm103_ptx.cuh"
+
+namespace detattn {
+
+__device__ unsigned int g_bwd_status;
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kThreads = 192;
+
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
+
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
+  return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
+// ============================================================== Delta
+// One warp per (b, h, 32 consecutive rows).  Each row of D bf16 is split in
+// 16-byte chunks over D/8 lanes; a lane forms its 8 products in order, the
+// lanes of a row are combined by a fixed xor-shuffle tree, and lane t stores
+// row t of the group (coalesced).
+template <int D>
+__global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
+  constexpr int kCpr = D / 8;        // 16-byte chunks per row
+  constexpr int kRpi = 32 / kCpr;    // rows per warp iteration
+  constexpr int kIters = 32 / kRpi;
+  const int lane = threadIdx.x & 31;
+  const long unit = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int tchunks = (a.T + 31) / 32;
+  const long units = static_cast<long>(a.B) * a.Hq * tchunks;
+  if (unit >= units) return;
+  const int tc = static_cast<int>(unit % tchunks);
+  const int bh = static_cast<int>(unit / tchunks);
+  const int b = bh / a.Hq, h = bh % a.Hq;
+  const int i0 = tc * 32;
+  const uint4* O = static_cast<const uint4*>(a.o);
+  const uint4* dO = static_cast<const uint4*>(a.dout);
+  float res[kIters];
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int i = i0 + it * kRpi + lane / kCpr;
+    const int c = lane % kCpr;
+    float acc = 0.f;
+    if (i < a.T) {
+      const size_t off = ((static_cast<size_t>(b) * a.T + i) * a.Hq + h) * kCpr + c;
+      const uint4 x = O[off], y = dO[off];
+      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 xf = bf16x2_to_float2(xs[k]), yf = bf16x2_to_float2(ys[k]);
+        acc = fmaf(xf.x, yf.x, acc);
+        acc = fmaf(xf.y, yf.y, acc);
+      }
+    }
+#pragma unroll
+    for (int s = kCpr / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    res[it] = acc;
+  }
+  float mine = 0.f;
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const float v = __shfl_sync(0xffffffffu, res[it], (lane % kRpi) * kCpr);
+    if (lane / kRpi == it) mine = v;
+  }
+  const int i = i0 + lane;
+  if (i < a.T) a.delta[(static_cast<size_t>(b) * a.Hq + h) * a.T + i] = mine;
+}
+
+// ============================================================== dK / dV
+// Block = (b, KV head, 128-key tile).  Warp 0 loads K, V once and then the
+// (Q, dO, LSE, Delta) of 64-row query tiles of every query head in the group;
+// warp 1 issues S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and
+// dK += dS^T Q with P^T and dS^T read from TMEM; warps 2..5 (thread r = key
+// row r) turn S^T, dP^T into P^T, dS^T.
+template <int D>
+struct DkvCfg {
+  static constexpr int kAtoms = D / 64;
+  static constexpr int kKvBytes = kTileN * 128 * kAtoms;    // 128 keys x D
+  static constexpr int kQBytes = kDkvTileM * 128 * kAtoms;  // 64 queries x D
+  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kStageBytes = 2 * kQBytes + 1024;    // Q, dO, then LSE/Delta rows
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kKvBytes;
+  static constexpr int kOffStage = 2 * kKvBytes;
+  static constexpr int kSmemBytes = kOffStage + kStages * kStageBytes + 1024;
+  static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;
+  static constexpr uint32_t kColS = 0;        // S^T fp32 [128 x 64]; P^T bf16 over cols 0..31
+  static constexpr uint32_t kColDP = 64;      // dP^T fp32; dS^T bf16 over cols 64..95
+  static constexpr uint32_t kColDV = 128;     // dV accumulator, D cols
+  static constexpr uint32_t kColDK = 128 + D; // dK accumulator, D cols
+};
+
+enum : int { kDkvBarKV = 0, kDkvBarQFull = 1, kDkvBarQEmpty = 4, kDkvBarS = 7, kDkvBarP = 8,
+             kDkvBarAcc = 9, kDkvBarDrain = 10, kDkvNumBars = 11 };
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
+    attn_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
+                     const BwdArgs a) {
+  using C = DkvCfg<D>;
+  constexpr int NS = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kDkvNumBars];
+  __shared__ uint32_t tmem_slot;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Key tiles near the start of the sequence see the most query tiles under
+  // the causal mask: hand those out first.
+  const int nt = static_cast<int>(blockIdx.x) / a.BH;
+  const int bg = static_cast<int>(blockIdx.x) % a.BH;
+  const int b = bg / a.Hkv, g = bg % a.Hkv;
+  const int G = a.Hq / a.Hkv;
+  const int n0 = nt * kTileN;
+  const int m_begin = a.causal ? n0 / kDkvTileM : 0;
+  const int m_end = (a.T + kDkvTileM - 1) / kDkvTileM;
+  const int per_head = m_end - m_begin;
+  const int n_it = G * per_head;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sK = s0 + C::kOffK, sV = s0 + C::kOffV;
+  auto stage_base = [&](int s) { return s0 + C::kOffStage + s * C::kStageBytes; };
+  auto stage_rows = [&](int s) {  // float lse2[64], delta[64]
+    return reinterpret_cast<float*>(smem + C::kOffStage + s * C::kStageBytes + 2 * C::kQBytes);
+  };
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kDkvBarKV), 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(bar(kDkvBarQFull + s), 1);
+      mbar_init(bar(kDkvBarQEmpty + s), 1);
+    }
+    mbar_init(bar(kDkvBarS), 1);
+    mbar_init(bar(kDkvBarP), 4);
+    mbar_init(bar(kDkvBarAcc), 1);
+    mbar_init(bar(kDkvBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&mQ);
+    tma_prefetch_desc(&mK);
+    tma_prefetch_desc(&mV);
+    tma_prefetch_desc(&mdO);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint64_t wait_ns = a.wait_ns;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (whole warp)
+    int last[3] = {-1, -1, -1};
+    if (lane == 0) {
+      mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * C::kKvBytes);
+      for (int at = 0; at < C::kAtoms; ++at) {
+        tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, g, n0, b);
+        tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, g, n0, b);
+      }
+    }
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % NS;
+      const uint32_t ph = (it / NS) & 1;
+      const int h = g * G + it / per_head;
+      const int i0 = (m_begin + it % per_head) * kDkvTileM;
+      if (it >= NS) {
+        ok = warp_all(mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns));
+        if (!ok) break;
+      }
+      float* rows = stage_rows(s);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int c = lane + 32 * k;
+        const int i = i0 + c;
+        float l2 = INFINITY, dl = 0.f;  // rows past T: P = exp2(-inf) = 0
+        if (i < a.T) {
+          const size_t off = (static_cast<size_t>(b) * a.Hq + h) * a.T + i;
+          l2 = a.lse[off] * kLog2e;
+          dl = a.delta[off];
+        }
+        rows[c] = l2;
+        rows[64 + c] = dl;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const uint32_t st = stage_base(s);
+        mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * C::kQBytes);
+        for (int at = 0; at < C::kAtoms; ++at) {
+          tma_load_4d(st + at * (kDkvTileM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h, i0, b);
+          tma_load_4d(st + C::kQBytes + at * (kDkvTileM * 128), &mdO, bar(kDkvBarQFull + s),
+                      at * 64, h, i0, b);
+        }
+      }
+      last[s] = it;
+    }
+    if (!ok && lane == 0) {
+      mbar_wait(bar(kDkvBarKV), 0, wait_ns);
+      for (int s = 0; s < NS; ++s)
+        if (last[s] >= 0) mbar_wait(bar(kDkvBarQFull + s), (last[s] / NS) & 1, wait_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
+      const uint32_t tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
+      constexpr uint32_t kIdS = idesc_bf16(kTileN, kDkvTileM, false, false);
+      constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
+      ok = mbar_wait(bar(kDkvBarKV), 0, wait_ns);
+      tc_fence_after();
+      for (int it = 0; it < n_it && ok; ++it) {
+        const int s = it % NS;
+        const uint32_t ph = (it / NS) & 1;
+        const uint32_t sQ = stage_base(s), sdO = stage_base(s) + C::kQBytes;
+        if (!(ok = mbar_wait(bar(kDkvBarQFull + s), ph, wait_ns))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
+          const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
+          mma_ss(tS, sdesc_sw128(sK + okv, 16, 1024), sdesc_sw128(sQ + oq, 16, 1024), kIdS, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
+          const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
+          mma_ss(tDP, sdesc_sw128(sV + okv, 16, 1024), sdesc_sw128(sdO + oq, 16, 1024), kIdS,
+                 ks > 0);
+        }
+        mma_commit(bar(kDkvBarS));
+        if (!(ok = mbar_wait(bar(kDkvBarP), it & 1, wait_ns))) break;
+        tc_fence_after();
+        // Accumulate over the 64 queries of this tile, 16 at a time.
+#pragma unroll
+        for (int ks = 0; ks < kDkvTileM / 16; ++ks) {
+          const uint32_t acc = (it > 0 || ks > 0) ? 1u : 0u;
+          mma_ts(tDV, tS + ks * 8, sdesc_sw128(sdO + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
+          mma_ts(tDK, tDP + ks * 8, sdesc_sw128(sQ + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
+        }
+        mma_commit(bar(kDkvBarQEmpty + s));
+      }
+      mma_commit(bar(kDkvBarAcc));
+      mma_commit(bar(kDkvBarDrain));
+      mbar_wait(bar(kDkvBarDrain), 0, wait_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ P^T / dS^T warps
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int krow = n0 + r;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = a.scale_log2;
+    for (int it = 0; it < n_it; ++it) {
+      const int s = it % NS;
+      const int i0 = (m_begin + it % per_head) * kDkvTileM;
+      ok = warp_all(mbar_wait(bar(kDkvBarS), it & 1, wait_ns));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[2][32], dp[2][32];
+      tmem_ld32_nowait(tl + C::kColS, sv[0]);
+      tmem_ld32_nowait(tl + C::kColS + 32, sv[1]);
+      tmem_ld32_nowait(tl + C::kColDP, dp[0]);
+      tmem_ld32_nowait(tl + C::kColDP + 32, dp[1]);
+      tmem_wait_ld();
+      reg_fence32(sv[0]);
+      reg_fence32(sv[1]);
+      reg_fence32(dp[0]);
+      reg_fence32(dp[1]);
+      const float* rows = stage_rows(s);
+      // Causal: query i0 + c sees key krow iff c >= krow - i0.
+      const int cmin = a.causal ? (krow - i0) : -1;
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int c2 = 0; c2 < 32; ++c2) {
+        float pv[2], dsv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 2 * c2 + e;
+          const float sval = __uint_as_float(sv[c >> 5][c & 31]);
+          float p = ex2_approx(fmaf(sval, sl2, -rows[c]));
+          if (c < cmin) p = 0.f;
+          pv[e] = p;
+          dsv[e] = p * (__uint_as_float(dp[c >> 5][c & 31]) - rows[64 + c]);
+        }
+        pk[c2] = pack_bf16x2(pv[0], pv[1]);
+        dk[c2] = pack_bf16x2(dsv[0], dsv[1]);
+      }
+      tmem_st32_nowait(tl + C::kColS, pk);
+      tmem_st32_nowait(tl + C::kColDP, dk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDkvBarP));
+    }
+    if (ok) ok = warp_all(mbar_wait(bar(kDkvBarAcc), 0, wait_ns));
+    if (ok) {
+      tc_fence_after();
+      const bool live = krow < a.T;
+      const size_t rbase = ((static_cast<size_t>(b) * a.T + krow) * a.Hkv + g) * D;
+      __nv_bfloat16* dvrow = static_cast<__nv_bfloat16*>(a.dv) + rbase;
+      __nv_bfloat16* dkrow = static_cast<__nv_bfloat16*>(a.dk) + rbase;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+        const float mul = which == 0 ? 1.f : a.scale;
+        __nv_bfloat16* dst_row = which == 0 ? dvrow : dkrow;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tl + col + c * 32, v);
+          uint32_t pkd[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  if (!ok) atomicOr(&g_bwd_status, 2u);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ============================================================== dQ
+// Block = (b, query head, 128-query tile).  Warp 0 loads Q, dO once and the
+// K, V of 64-key tiles 0..diagonal in ascending order; warp 1 issues
+// S = Q K^T, dP = dO V^T and dQ += dS K with dS read from TMEM; warps 2..5
+// (thread r = query row r) form P and dS.
+template <int D>
+struct DqCfg {
+  static constexpr int kAtoms = D / 64;
+  static constexpr int kQBytes = kTileM * 128 * kAtoms;     // 128 queries x D
+  static constexpr int kKvBytes = kDqTileN * 128 * kAtoms;  // 64 keys x D
+  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffdO = kQBytes;
+  static constexpr int kOffK = 2 * kQBytes;
+  static constexpr int kOffV = kOffK + kStages * kKvBytes;
+  static constexpr int kSmemBytes = kOffV + kStages * kKvBytes + 1024;
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kColS = 0;    // S fp32 [128 x 64]; dS bf16 over cols 0..31
+  static constexpr uint32_t kColDP = 64;  // dP fp32 [128 x 64]
+  static constexpr uint32_t kColDQ = 128; // dQ accumulator, D cols
+};
+
+enum : int { kDqBarQ = 0, kDqBarKFull = 1, kDqBarVFull = 4, kDqBarKEmpty = 7, kDqBarVEmpty = 10,
+             kDqBarS = 13, kDqBarDS = 14, kDqBarAcc = 15, kDqBarDrain = 16, kDqNumBars = 17 };
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                   const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
+                   const BwdArgs a) {
+  using C = DqCfg<D>;
+  constexpr int NS = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kDqNumBars];
+  __shared__ uint32_t tmem_slot;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = a.n_tiles - 1 - static_cast<int>(blockIdx.x) / a.BH;
+  const int bh = static_cast<int>(blockIdx.x) % a.BH;
+  const int b = bh / a.Hq, h = bh % a.Hq;
+  const int hkv = h / (a.Hq / a.Hkv);
+  const int m0 = mt * kTileM;
+  const int kv_tiles = (a.T + kDqTileN - 1) / kDqTileN;
+  const int n_kv = a.causal ? min(kv_tiles, (m0 + kTileM) / kDqTileN) : kv_tiles;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sQ = s0 + C::kOffQ, sdO = s0 + C::kOffdO;
+  const uint32_t sK0 = s0 + C::kOffK, sV0 = s0 + C::kOffV;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kDqBarQ), 1);
+    for (int s = 0; s < 3; ++s) {
+      mbar_init(bar(kDqBarKFull + s), 1);
+      mbar_init(bar(kDqBarVFull + s), 1);
+      mbar_init(bar(kDqBarKEmpty + s), 1);
+      mbar_init(bar(kDqBarVEmpty + s), 1);
+    }
+    mbar_init(bar(kDqBarS), 1);
+    mbar_init(bar(kDqBarDS), 4);
+    mbar_init(bar(kDqBarAcc), 1);
+    mbar_init(bar(kDqBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&mQ);
+    tma_prefetch_desc(&mK);
+    tma_prefetch_desc(&mV);
+    tma_prefetch_desc(&mdO);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint64_t wait_ns = a.wait_ns;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int last_k[3] = {-1, -1, -1}, last_v[3] = {-1, -1, -1};
+      mbar_arrive_expect_tx(bar(kDqBarQ), 2 * C::kQBytes);
+      for (int at = 0; at < C::kAtoms; ++at) {
+        tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kDqBarQ), at * 64, h, m0, b);
+        tma_load_4d(sdO + at * (kTileM * 128), &mdO, bar(kDqBarQ), at * 64, h, m0, b);
+      }
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % NS;
+        const uint32_t ph = (j / NS) & 1;
+        if (j >= NS && !(ok = mbar_wait(bar(kDqBarKEmpty + s), ph ^ 1, wait_ns))) break;
+        mbar_arrive_expect_tx(bar(kDqBarKFull + s), C::kKvBytes);
+        for (int at = 0; at < C::kAtoms; ++at)
+          tma_load_4d(sK0 + s * C::kKvBytes + at * (kDqTileN * 128), &mK, bar(kDqBarKFull + s),
+                      at * 64, hkv, j * kDqTileN, b);
+        last_k[s] = j;
+        if (j >= NS && !(ok = mbar_wait(bar(kDqBarVEmpty + s), ph ^ 1, wait_ns))) break;
+        mbar_arrive_expect_tx(bar(kDqBarVFull + s), C::kKvBytes);
+        for (int at = 0; at < C::kAtoms; ++at)
+          tma_load_4d(sV0 + s * C::kKvBytes + at * (kDqTileN * 128), &mV, bar(kDqBarVFull + s),
+                      at * 64, hkv, j * kDqTileN, b);
+        last_v[s] = j;
+      }
+      if (!ok) {
+        mbar_wait(bar(kDqBarQ), 0, wait_ns);
+        for (int s = 0; s < NS; ++s) {
+          if (last_k[s] >= 0) mbar_wait(bar(kDqBarKFull + s), (last_k[s] / NS) & 1, wait_ns);
+          if (last_v[s] >= 0) mbar_wait(bar(kDqBarVFull + s), (last_v[s] / NS) & 1, wait_ns);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ;
+      constexpr uint32_t kIdS = idesc_bf16(kTileM, kDqTileN, false, false);
+      constexpr uint32_t kIdDQ = idesc_bf16(kTileM, D, false, true);
+      ok = mbar_wait(bar(kDqBarQ), 0, wait_ns);
+      tc_fence_after();
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int s = j % NS;
+        const uint32_t ph = (j / NS) & 1;
+        const uint32_t sK = sK0 + s * C::kKvBytes, sV = sV0 + s * C::kKvBytes;
+        if (!(ok = mbar_wait(bar(kDqBarKFull + s), ph, wait_ns))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
+          const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
+          mma_ss(tS, sdesc_sw128(sQ + oq, 16, 1024), sdesc_sw128(sK + okv, 16, 1024), kIdS, ks > 0);
+        }
+        if (!(ok = mbar_wait(bar(kDqBarVFull + s), ph, wait_ns))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
+          const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
+          mma_ss(tDP, sdesc_sw128(sdO + oq, 16, 1024), sdesc_sw128(sV + okv, 16, 1024), kIdS,
+                 ks > 0);
+        }
+        mma_commit(bar(kDqBarS));
+        mma_commit(bar(kDqBarVEmpty + s));
+        if (!(ok = mbar_wait(bar(kDqBarDS), j & 1, wait_ns))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kDqTileN / 16; ++ks)
+          mma_ts(tDQ, tS + ks * 8, sdesc_sw128(sK + ks * 2048, kDqTileN * 128, 1024), kIdDQ,
+                 (j > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(bar(kDqBarKEmpty + s));
+      }
+      mma_commit(bar(kDqBarAcc));
+      mma_commit(bar(kDqBarDrain));
+      mbar_wait(bar(kDqBarDrain), 0, wait_ns);
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qrow = m0 + r;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = a.scale_log2;
+    float lse2 = INFINITY, dl = 0.f;  // rows past T: P = 0, dS = 0
+    if (qrow < a.T) {
+      const size_t off = (static_cast<size_t>(b) * a.Hq + h) * a.T + qrow;
+      lse2 = a.lse[off] * kLog2e;
+      dl = a.delta[off];
+    }
+    for (int j = 0; j < n_kv; ++j) {
+      ok = warp_all(mbar_wait(bar(kDqBarS), j & 1, wait_ns));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[2][32], dp[2][32];
+      tmem_ld32_nowait(tl + C::kColS, sv[0]);
+      tmem_ld32_nowait(tl + C::kColS + 32, sv[1]);
+      tmem_ld32_nowait(tl + C::kColDP, dp[0]);
+      tmem_ld32_nowait(tl + C::kColDP + 32, dp[1]);
+      tmem_wait_ld();
+      reg_fence32(sv[0]);
+      reg_fence32(sv[1]);
+      reg_fence32(dp[0]);
+      reg_fence32(dp[1]);
+      const int kv0 = j * kDqTileN;
+      // key kv0 + c visible iff c <= lim
+      const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
+      uint32_t dsk[32];
+#pragma unroll
+      for (int c2 = 0; c2 < 32; ++c2) {
+        float dsv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int c = 2 * c2 + e;
+          float p = ex2_approx(fmaf(__uint_as_float(sv[c >> 5][c & 31]), sl2, -lse2));
+          if (c > lim) p = 0.f;
+          dsv[e] = p * (__uint_as_float(dp[c >> 5][c & 31]) - dl);
+        }
+        dsk[c2] = pack_bf16x2(dsv[0], dsv[1]);
+      }
+      tmem_st32_nowait(tl + C::kColS, dsk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDqBarDS));
+    }
+    if (ok) ok = warp_all(mbar_wait(bar(kDqBarAcc), 0, wait_ns));
+    if (ok) {
+      tc_fence_after();
+      const bool live = qrow < a.T;
+      __nv_bfloat16* dqrow = static_cast<__nv_bfloat16*>(a.dq) +
+                             ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tl + C::kColDQ + c * 32, v);
+        uint32_t pkd[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * a.scale,
+                               __uint_as_float(v[2 * i + 1]) * a.scale);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(dqrow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  if (!ok) atomicOr(&g_bwd_status, 4u);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <typename K>
+cudaError_t set_smem_once(K kernel, int bytes, bool* done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !done[dev]) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
+                          cudaStream_t st) {
+  static bool done[64] = {};
+  cudaError_t e = set_smem_once(attn_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  attn_dkdv_kernel<D><<<grid, kThreads, DkvCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                        const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
+                        cudaStream_t st) {
+  static bool done[64] = {};
+  cudaError_t e = set_smem_once(attn_dq_kernel<D>, DqCfg<D>::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  attn_dq_kernel<D><<<grid, kThreads, DqCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st) {
+  const long units = static_cast<long>(a.B) * a.Hq * ((a.T + 31) / 32);
+  const int grid = static_cast<int>((units + 7) / 8);
+  if (a.D == 64)
+    attn_delta_kernel<64><<<grid, 256, 0, st>>>(a);
+  else
+    attn_delta_kernel<128><<<grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                        const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
+                        cudaStream_t st) {
+  return D == 64 ? launch_dkdv_t<64>(grid, mq, mk, mv, mdo, a, st)
+                 : launch_dkdv_t<128>(grid, mq, mk, mv, mdo, a, st);
+}
+
+cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                      const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
+                      cudaStream_t st) {
+  return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, a, st)
+                 : launch_dq_t<128>(grid, mq, mk, mv, mdo, a, st);
+}
+
+cudaError_t take_bwd_status(cudaStream_t st, unsigned* out) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_bwd_status, sizeof(v), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && v)
+    e = cudaMemcpyToSymbolAsync(g_bwd_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  *out = v;
+  return e;
+}
+
+}  // namespace detattn

@@ -1,0 +1,335 @@
+// Fused causal grouped-query flash-attention forward for sm_103a.
+//
+// RustingBrain vs PyTorch/TensorFlow page, "Step 2: fused flash attention":
+// one fused kernel replaces the causal softmax kernels and never writes the
+// [seq_len, seq_len] score matrix.  "Step 1" names the per-row logsumexp the
+// forward hands to the backward.
+//
+// One thread block owns one 128-row query tile of one (batch, query head) and
+// walks the key/value tiles 0..diagonal in ascending order:
+//   warp 0      TMA producer: Q once, then K_j / V_j into a ring of stages
+//   warp 1      tcgen05 issuer: S = Q K_j^T into TMEM, then O += P V_j with P
+//               read from TMEM (bf16, written over S by the softmax warps)
+//   warps 2..5  softmax: thread r owns query row r (TMEM lane r); online
+//               softmax in base 2 with a lazily moved row maximum, P to TMEM,
+//               O rescaled in TMEM when the maximum moves, epilogue O / l and
+//               LSE = ln2 * (m + log2 l)
+// Two blocks share an SM (256 TMEM columns each), so one block's softmax
+// overlaps the other's matrix multiplies.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_launch.h"
+#include "sm103_ptx.cuh"
+
+namespace detattn {
+
+__device__ unsigned int g_fwd_status;
+
+namespace {
+
+constexpr int kThreads = 192;
+// The row maximum used in the exponent is only moved when the true maximum
+// exceeds it by more than 2^8; until then P <= 256, which bf16 and the fp32
+// accumulators hold exactly as well.  The final O / l and LSE are exact for
+// any value of the stale maximum.
+constexpr float kRescaleLog2 = 8.0f;
+
+template <int D>
+struct Cfg {
+  static constexpr int kAtoms = D / 64;                   // 128-byte swizzle atoms per row
+  static constexpr int kTileBytes = kTileM * 128 * kAtoms;  // 128 rows x D bf16
+  static constexpr int kStages = (D == 64) ? 2 : 1;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kColS = 0;    // S (fp32, 128 cols); P (bf16 pairs) over cols 0..63
+  static constexpr uint32_t kColO = 128;  // O accumulator, D cols
+};
+
+enum : int { kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKEmpty = 5, kBarVEmpty = 7,
+             kBarS = 9, kBarP = 10, kBarO = 11, kBarDrain = 12, kNumBars = 13 };
+
+__device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                    const __grid_constant__ CUtensorMap mV, const FwdArgs a) {
+  using C = Cfg<D>;
+  constexpr int NS = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ uint32_t tmem_slot;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Heaviest query tiles (most key tiles under the causal mask) are handed out first.
+  const int mt = a.n_m - 1 - static_cast<int>(blockIdx.x) / a.BHq;
+  const int bh = static_cast<int>(blockIdx.x) % a.BHq;
+  const int b = bh / a.Hq, h = bh % a.Hq;
+  const int hkv = h / (a.Hq / a.Hkv);
+  const int m0 = mt * kTileM;
+  const int n_kv = a.causal ? (mt + 1) : (a.T + kTileN - 1) / kTileN;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sQ = smem_u32(smem) + C::kOffQ;
+  const uint32_t sK0 = smem_u32(smem) + C::kOffK;
+  const uint32_t sV0 = smem_u32(smem) + C::kOffV;
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQ), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
+    }
+    mbar_init(bar(kBarS), 1);
+    mbar_init(bar(kBarP), 4);
+    mbar_init(bar(kBarO), 1);
+    mbar_init(bar(kBarDrain), 1);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&mQ);
+    tma_prefetch_desc(&mK);
+    tma_prefetch_desc(&mV);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint64_t wait_ns = a.wait_ns;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
+      mbar_arrive_expect_tx(bar(kBarQ), C::kTileBytes);
+      for (int at = 0; at < C::kAtoms; ++at)
+        tma_load_4d(sQ + at * 16384, &mQ, bar(kBarQ), at * 64, h, m0, b);
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % NS;
+        const uint32_t ph = (j / NS) & 1;
+        if (j >= NS && !(ok = mbar_wait(bar(kBarKEmpty + s), ph ^ 1, wait_ns))) break;
+        mbar_arrive_expect_tx(bar(kBarKFull + s), C::kTileBytes);
+        for (int at = 0; at < C::kAtoms; ++at)
+          tma_load_4d(sK0 + s * C::kTileBytes + at * 16384, &mK, bar(kBarKFull + s), at * 64, hkv,
+                      j * kTileN, b);
+        last_k[s] = j;
+        if (j >= NS && !(ok = mbar_wait(bar(kBarVEmpty + s), ph ^ 1, wait_ns))) break;
+        mbar_arrive_expect_tx(bar(kBarVFull + s), C::kTileBytes);
+        for (int at = 0; at < C::kAtoms; ++at)
+          tma_load_4d(sV0 + s * C::kTileBytes + at * 16384, &mV, bar(kBarVFull + s), at * 64, hkv,
+                      j * kTileN, b);
+        last_v[s] = j;
+      }
+      if (!ok) {
+        // Let every copy already issued land before the block's shared memory goes away.
+        mbar_wait(bar(kBarQ), 0, wait_ns);
+        for (int s = 0; s < NS; ++s) {
+          if (last_k[s] >= 0) mbar_wait(bar(kBarKFull + s), (last_k[s] / NS) & 1, wait_ns);
+          if (last_v[s] >= 0) mbar_wait(bar(kBarVFull + s), (last_v[s] / NS) & 1, wait_ns);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t tS = tmem + C::kColS, tO = tmem + C::kColO;
+      constexpr uint32_t kIdQK = idesc_bf16(kTileM, kTileN, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, false, true);
+      ok = mbar_wait(bar(kBarQ), 0, wait_ns);
+      tc_fence_after();
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int s = j % NS;
+        const uint32_t ph = (j / NS) & 1;
+        const uint32_t sK = sK0 + s * C::kTileBytes, sV = sV0 + s * C::kTileBytes;
+        if (!(ok = mbar_wait(bar(kBarKFull + s), ph, wait_ns))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(tS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdQK,
+                 ks > 0);
+        }
+        mma_commit(bar(kBarS));
+        mma_commit(bar(kBarKEmpty + s));
+        if (!(ok = mbar_wait(bar(kBarP), j & 1, wait_ns))) break;
+        if (!(ok = mbar_wait(bar(kBarVFull + s), ph, wait_ns))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < kTileN / 16; ++ks)
+          mma_ts(tO, tS + ks * 8, sdesc_sw128(sV + ks * 2048, 16384, 1024), kIdPV,
+                 (j > 0 || ks > 0) ? 1u : 0u);
+        mma_commit(bar(kBarVEmpty + s));
+        mma_commit(bar(kBarO));
+      }
+      // Every issued MMA must finish before TMEM is released.
+      mma_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, wait_ns);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int r = quarter * 32 + lane;
+    const int qrow = m0 + r;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = a.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = warp_all(mbar_wait(bar(kBarS), j & 1, wait_ns));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tl + C::kColS + c * 32, sr[c]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+
+      const int kv0 = j * kTileN;
+      const bool need_mask = a.causal ? (j == n_kv - 1) : (kv0 + kTileN > a.T);
+      if (need_mask) {
+        const int lim = a.causal ? (qrow - kv0) : (a.T - 1 - kv0);  // key columns c <= lim visible
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+      const float m_new = mx * sl2;
+      float alpha = 1.f;
+      bool moved = false;
+      if (m_new > m_run + kRescaleLog2) {
+        alpha = ex2_approx(m_run - m_new);
+        m_run = m_new;
+        moved = true;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      float rowsum = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]), sl2, -m_use));
+        const float p1 =
+            ex2_approx(fmaf(__uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), sl2, -m_use));
+        rowsum += p0;
+        rowsum += p1;
+        pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
+      }
+      tmem_st32_nowait(tl + C::kColS, pk[0]);
+      tmem_st32_nowait(tl + C::kColS + 32, pk[1]);
+      tmem_wait_st();
+      if (j > 0 && __any_sync(0xffffffffu, moved)) {
+        // O holds sum over earlier tiles scaled by the old maximum: wait for the
+        // last P V to land, then rescale O in TMEM.
+        ok = warp_all(mbar_wait(bar(kBarO), (j - 1) & 1, wait_ns));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tl + C::kColO + c * 32, ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32_nowait(tl + C::kColO + c * 32, ov);
+        }
+        tmem_wait_st();
+      }
+      l_run = l_run * alpha + rowsum;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarP));
+    }
+    if (ok) ok = warp_all(mbar_wait(bar(kBarO), (n_kv - 1) & 1, wait_ns));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l_run;
+      const bool live = qrow < a.T;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
+                            ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tl + C::kColO + c * 32, ov);
+        uint32_t pkd[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                               __uint_as_float(ov[2 * i + 1]) * inv_l);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+        }
+      }
+      if (live)
+        a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + qrow] =
+            (m_run + log2f(l_run)) * 0.69314718055994530942f;
+    }
+  }
+
+  if (!ok) atomicOr(&g_fwd_status, 1u);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                         const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
+  const int smem = Cfg<D>::kSmemBytes;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  attn_fwd_kernel<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                       const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
+  return D == 64 ? launch_fwd_t<64>(grid, mq, mk, mv, a, st)
+                 : launch_fwd_t<128>(grid, mq, mk, mv, a, st);
+}
+
+cudaError_t take_fwd_status(cudaStream_t st, unsigned* out) {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_fwd_status, sizeof(v), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && v)
+    e = cudaMemcpyToSymbolAsync(g_fwd_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  *out = v;
+  return e;
+}
+
+}  // namespace detattn

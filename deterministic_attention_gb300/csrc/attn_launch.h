@@ -1,0 +1,64 @@
+// Internal interface between the C-ABI host layer and the kernel translation
+// units: argument blocks and launch functions.  Not part of the public API.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace detattn {
+
+constexpr int kTileM = 128;     // query rows per forward / dQ tile
+constexpr int kTileN = 128;     // key rows per forward KV tile and per dK/dV tile
+constexpr int kDqTileN = 64;    // key rows per dQ-kernel KV tile
+constexpr int kDkvTileM = 64;   // query rows per dK/dV-kernel Q tile
+
+struct FwdArgs {
+  void* o;               // bf16 [B, T, Hq, D]
+  float* lse;            // fp32 [B, Hq, T]
+  int T, Hq, Hkv;
+  int n_m;               // query tiles per (b, h)
+  int BHq;               // B * Hq
+  int causal;
+  float scale_log2;      // scale * log2(e)
+  unsigned long long wait_ns;
+};
+
+struct DeltaArgs {
+  const void* o;         // bf16 [B, T, Hq, D]
+  const void* dout;      // bf16 [B, T, Hq, D]
+  float* delta;          // fp32 [B, Hq, T]
+  int B, T, Hq, D;
+};
+
+struct BwdArgs {
+  const float* lse;      // fp32 [B, Hq, T]
+  const float* delta;    // fp32 [B, Hq, T]
+  void* dq;              // bf16 [B, T, Hq, D]   (dQ kernel)
+  void* dk;              // bf16 [B, T, Hkv, D]  (dK/dV kernel)
+  void* dv;
+  int T, Hq, Hkv;
+  int n_tiles;           // tiles per (b, head) along T
+  int BH;                // B * Hq (dQ) or B * Hkv (dK/dV)
+  int causal;
+  float scale;
+  float scale_log2;
+  unsigned long long wait_ns;
+};
+
+// Each returns the launch error (cudaSuccess when the kernel was queued).
+cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                       const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st);
+cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st);
+cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                        const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
+                        cudaStream_t st);
+cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                      const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
+                      cudaStream_t st);
+
+// Read-and-clear of the device status words the kernels set when a bounded
+// wait runs out (synchronous on `st`).  Returns the OR of the words.
+cudaError_t take_fwd_status(cudaStream_t st, unsigned* out);
+cudaError_t take_bwd_status(cudaStream_t st, unsigned* out);
+
+}  // namespace detattn

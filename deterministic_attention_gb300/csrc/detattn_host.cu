@@ -1,0 +1,326 @@
+// C-ABI host layer of libdetattn: argument validation, TMA descriptor
+// encoding and kernel launches.  Declarations and contracts: include/detattn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+
+#include "../../include/detattn.h"
+#include "attn_launch.h"
+
+using namespace detattn;
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+thread_local char g_err[512] = "";
+unsigned long long g_wait_ns = 1000000000ull;  // 1 s per bounded wait
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+int ok_status() {
+  g_err[0] = '\0';
+  return DETATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by all entry points.  Sets *empty for B*T == 0.
+int check_shape(int B, int T, int Hq, int Hkv, int D, bool* empty) {
+  if (B < 0 || T < 0) return fail(DETATTN_ERR_SHAPE, "B=%d T=%d must be >= 0", B, T);
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return fail(DETATTN_ERR_SHAPE, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  if (D != 64 && D != 128) return fail(DETATTN_ERR_HEADDIM, "D=%d: only 64 and 128", D);
+  // Grid and index limits: tiles per launch and elements per tensor.
+  const double tiles = static_cast<double>(B) * Hq * ((T + 63) / 64);
+  const double elems = static_cast<double>(B) * T * Hq * D;
+  if (tiles > 2.0e9 || elems > 1.0e12 || T > (1 << 30))
+    return fail(DETATTN_ERR_SHAPE, "problem too large (B=%d T=%d Hq=%d)", B, T, Hq);
+  *empty = (B == 0 || T == 0);
+  return DETATTN_OK;
+}
+
+int check_scale(float scale, int causal) {
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(DETATTN_ERR_SCALE, "scale=%g must be finite and > 0", static_cast<double>(scale));
+  if (causal != 0 && causal != 1) return fail(DETATTN_ERR_SCALE, "causal=%d must be 0 or 1", causal);
+  return DETATTN_OK;
+}
+
+int check_ptrs(std::initializer_list<std::pair<const void*, const char*>> ps) {
+  for (const auto& p : ps)
+    if (p.first == nullptr) return fail(DETATTN_ERR_NULL, "%s is NULL", p.second);
+  for (const auto& p : ps)
+    if (!aligned16(p.first)) return fail(DETATTN_ERR_ALIGN, "%s is not 16-byte aligned", p.second);
+  return DETATTN_OK;
+}
+
+// ------------------------------------------------------------ device checks
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_err = cudaSuccess;
+
+int check_device() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  static int arch_ok[64] = {};  // 0 unknown, 1 ok, 2 wrong arch
+  if (dev >= 64 || arch_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess)
+      return fail(DETATTN_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    const int v = (major == 10 && minor == 3) ? 1 : 2;
+    if (dev < 64) arch_ok[dev] = v;
+    if (v == 2)
+      return fail(DETATTN_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                  major, minor);
+  } else if (arch_ok[dev] == 2) {
+    return fail(DETATTN_ERR_ARCH, "device %d is not sm_103", dev);
+  }
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    g_encode_err = cudaGetDriverEntryPointByVersion(
+        "cuTensorMapEncodeTiled", reinterpret_cast<void**>(&g_encode), 12000, cudaEnableDefault, &q);
+    if (g_encode_err == cudaSuccess && q != cudaDriverEntryPointSuccess)
+      g_encode_err = cudaErrorNotSupported;
+  });
+  if (g_encode_err != cudaSuccess || g_encode == nullptr)
+    return fail(DETATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable: %s",
+                cudaGetErrorString(g_encode_err));
+  return DETATTN_OK;
+}
+
+// Tensor map over a bf16 [B, T, H, D] tensor whose box is `rows` consecutive
+// positions t of one (b, h) and 64 columns of d (one 128-byte swizzle atom).
+// Rows past T read as zero.
+int encode_rows(CUtensorMap* m, const void* ptr, int B, int T, int H, int D, int rows,
+                const char* what) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                           static_cast<cuuint64_t>(T) * H * D * 2};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DETATTN_ERR_CUDA, "tensor map for %s: CUresult %d", what, (int)r);
+  return DETATTN_OK;
+}
+
+int launched(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+  return ok_status();
+}
+
+float log2e_times(float scale) { return scale * 1.4426950408889634f; }
+
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
+             int Hq, int Hkv, int D, float scale, int causal, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  int rc;
+  if ((rc = encode_rows(&mq, q, B, T, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
+  FwdArgs a{};
+  a.o = o;
+  a.lse = lse;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.n_m = (T + kTileM - 1) / kTileM;
+  a.BHq = B * Hq;
+  a.causal = causal;
+  a.scale_log2 = log2e_times(scale);
+  a.wait_ns = g_wait_ns;
+  return launched(launch_fwd(D, a.n_m * a.BHq, mq, mk, mv, a, st), "attn_fwd");
+}
+
+int delta_impl(const void* o, const void* dout, float* delta, int B, int T, int Hq, int D,
+               cudaStream_t st) {
+  DeltaArgs a{o, dout, delta, B, T, Hq, D};
+  return launched(launch_delta(a, st), "attn_bwd_delta");
+}
+
+BwdArgs bwd_args(const float* lse, const float* delta, int T, int Hq, int Hkv, float scale,
+                 int causal) {
+  BwdArgs a{};
+  a.lse = lse;
+  a.delta = delta;
+  a.T = T;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.causal = causal;
+  a.scale = scale;
+  a.scale_log2 = log2e_times(scale);
+  a.wait_ns = g_wait_ns;
+  return a;
+}
+
+int dkdv_impl(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+              const void* dout, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
+              float scale, int causal, cudaStream_t st) {
+  CUtensorMap mq, mk, mv, mdo;
+  int rc;
+  if ((rc = encode_rows(&mq, q, B, T, Hq, D, kDkvTileM, "q")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mdo, dout, B, T, Hq, D, kDkvTileM, "dout")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
+  BwdArgs a = bwd_args(lse, delta, T, Hq, Hkv, scale, causal);
+  a.dk = dk;
+  a.dv = dv;
+  a.n_tiles = (T + kTileN - 1) / kTileN;
+  a.BH = B * Hkv;
+  return launched(launch_dkdv(D, a.n_tiles * a.BH, mq, mk, mv, mdo, a, st), "attn_bwd_dkdv");
+}
+
+int dq_impl(const void* q, const void* k, const void* v, const float* lse, const float* delta,
+            const void* dout, void* dq, int B, int T, int Hq, int Hkv, int D, float scale,
+            int causal, cudaStream_t st) {
+  CUtensorMap mq, mk, mv, mdo;
+  int rc;
+  if ((rc = encode_rows(&mq, q, B, T, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mdo, dout, B, T, Hq, D, kTileM, "dout")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kDqTileN, "k")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kDqTileN, "v")) != DETATTN_OK) return rc;
+  BwdArgs a = bwd_args(lse, delta, T, Hq, Hkv, scale, causal);
+  a.dq = dq;
+  a.n_tiles = (T + kTileM - 1) / kTileM;
+  a.BH = B * Hq;
+  return launched(launch_dq(D, a.n_tiles * a.BH, mq, mk, mv, mdo, a, st), "attn_bwd_dq");
+}
+
+size_t delta_bytes(int B, int T, int Hq) {
+  const size_t n = static_cast<size_t>(B) * Hq * T * sizeof(float);
+  return (n + 255) & ~static_cast<size_t>(255);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
+             int Hq, int Hkv, int D, float scale, int causal, void* stream) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, Hkv, D, &empty)) != DETATTN_OK) return rc;
+  if ((rc = check_scale(scale, causal)) != DETATTN_OK) return rc;
+  if (empty) return ok_status();
+  if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}})) != DETATTN_OK)
+    return rc;
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  return fwd_impl(q, k, v, o, lse, B, T, Hq, Hkv, D, scale, causal,
+                  static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
+  bool empty = false;
+  if (check_shape(B, T, Hq, Hkv, D, &empty) != DETATTN_OK || empty) return 0;
+  return delta_bytes(B, T, Hq);
+}
+
+int attn_bwd_delta(const void* o, const void* dout, float* delta, int B, int T, int Hq, int D,
+                   void* stream) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, 1, D, &empty)) != DETATTN_OK) return rc;
+  if (empty) return ok_status();
+  if ((rc = check_ptrs({{o, "o"}, {dout, "dout"}, {delta, "delta"}})) != DETATTN_OK) return rc;
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  return delta_impl(o, dout, delta, B, T, Hq, D, static_cast<cudaStream_t>(stream));
+}
+
+int attn_bwd_dkdv(const void* q, const void* k, const void* v, const float* lse,
+                  const float* delta, const void* dout, void* dk, void* dv, int B, int T, int Hq,
+                  int Hkv, int D, float scale, int causal, void* stream) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, Hkv, D, &empty)) != DETATTN_OK) return rc;
+  if ((rc = check_scale(scale, causal)) != DETATTN_OK) return rc;
+  if (empty) return ok_status();
+  if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {lse, "lse"}, {delta, "delta"},
+                        {dout, "dout"}, {dk, "dk"}, {dv, "dv"}})) != DETATTN_OK)
+    return rc;
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  return dkdv_impl(q, k, v, lse, delta, dout, dk, dv, B, T, Hq, Hkv, D, scale, causal,
+                   static_cast<cudaStream_t>(stream));
+}
+
+int attn_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
+                const float* delta, const void* dout, void* dq, int B, int T, int Hq, int Hkv,
+                int D, float scale, int causal, void* stream) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, Hkv, D, &empty)) != DETATTN_OK) return rc;
+  if ((rc = check_scale(scale, causal)) != DETATTN_OK) return rc;
+  if (empty) return ok_status();
+  if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {lse, "lse"}, {delta, "delta"},
+                        {dout, "dout"}, {dq, "dq"}})) != DETATTN_OK)
+    return rc;
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  return dq_impl(q, k, v, lse, delta, dout, dq, B, T, Hq, Hkv, D, scale, causal,
+                 static_cast<cudaStream_t>(stream));
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, void* workspace,
+             size_t workspace_bytes, int B, int T, int Hq, int Hkv, int D, float scale,
+             int causal, void* stream) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, Hkv, D, &empty)) != DETATTN_OK) return rc;
+  if ((rc = check_scale(scale, causal)) != DETATTN_OK) return rc;
+  if (empty) return ok_status();
+  if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {dout, "dout"},
+                        {dq, "dq"}, {dk, "dk"}, {dv, "dv"}})) != DETATTN_OK)
+    return rc;
+  if (workspace == nullptr || workspace_bytes < delta_bytes(B, T, Hq))
+    return fail(DETATTN_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu%s",
+                delta_bytes(B, T, Hq), workspace_bytes, workspace ? "" : " (NULL)");
+  if (!aligned16(workspace)) return fail(DETATTN_ERR_ALIGN, "workspace is not 16-byte aligned");
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* delta = static_cast<float*>(workspace);
+  if ((rc = delta_impl(o, dout, delta, B, T, Hq, D, st)) != DETATTN_OK) return rc;
+  if ((rc = dkdv_impl(q, k, v, lse, delta, dout, dk, dv, B, T, Hq, Hkv, D, scale, causal, st)) !=
+      DETATTN_OK)
+    return rc;
+  return dq_impl(q, k, v, lse, delta, dout, dq, B, T, Hq, Hkv, D, scale, causal, st);
+}
+
+int detattn_check_status(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned f = 0, b = 0;
+  cudaError_t e = take_fwd_status(st, &f);
+  if (e == cudaSuccess) e = take_bwd_status(st, &b);
+  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (f | b)
+    return fail(DETATTN_ERR_DEVICE_TIMEOUT,
+                "a kernel gave up on a pipeline wait (fwd flags %u, bwd flags %u)", f, b);
+  return ok_status();
+}
+
+void detattn_set_wait_limit_ns(unsigned long long ns) {
+  if (ns < 1000000ull) ns = 1000000ull;
+  if (ns > 60000000000ull) ns = 60000000000ull;
+  g_wait_ns = ns;
+}
+
+const char* detattn_last_error(void) { return g_err; }
+
+int detattn_version(void) { return kVersion; }
+
+}  // extern "C"

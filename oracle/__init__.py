@@ -62,6 +62,8 @@ def _load():
         lib.oracle_attn_rows.restype = None
         lib.oracle_kv_rows.argtypes = [dp, dp, dp, dp, i, i, i, ip, dp, dp, i, i, i, i, i, d, i]
         lib.oracle_kv_rows.restype = None
+        lib.oracle_rowdot.argtypes = [dp, dp, dp, i, i, i, i]
+        lib.oracle_rowdot.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i
         _lib = lib
@@ -120,6 +122,15 @@ def attn_bwd(q, k, v, dout, scale: float, causal: bool = True):
     worst = _load().oracle_attn_bwd(_dp(q), _dp(k), _dp(v), _dp(dout), _dp(dq), _dp(dk), _dp(dv),
                                     _dp(delta), B, T, Hq, Hkv, D, float(scale), int(bool(causal)))
     return dq, dk, dv, delta, worst
+
+
+def rowdot(o, dout):
+    """Delta [B,H,T] = sum_d dout * o for given o, dout [B,T,H,D]."""
+    o, dout = _f64(o), _f64(dout)
+    B, T, H, D = o.shape
+    delta = np.empty((B, H, T), dtype=np.float64)
+    _load().oracle_rowdot(_dp(o), _dp(dout), _dp(delta), B, T, H, D)
+    return delta
 
 
 def attn_probs(q, k, b: int, h: int, scale: float, causal: bool = True):

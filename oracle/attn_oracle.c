@@ -151,6 +151,15 @@ double oracle_attn_bwd(const double* q, const double* k, const double* v, const 
   return worst;
 }
 
+void oracle_rowdot(const double* o, const double* dout, double* delta, int B, int T, int H, int D) {
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h)
+      for (int i = 0; i < T; ++i)
+        delta[((size_t)b * H + h) * T + i] =
+            dot(dout + row_off(b, i, h, T, H, D), o + row_off(b, i, h, T, H, D), D);
+}
+
 void oracle_attn_probs(const double* q, const double* k, double* p, int b, int h, int B, int T,
                        int Hq, int Hkv, int D, double scale, int causal) {
   (void)B;

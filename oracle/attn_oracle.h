@@ -71,6 +71,10 @@ void oracle_kv_rows(const double* q, const double* k, const double* v, const dou
                     int g, int nj, const int* js, double* dk_rows, double* dv_rows, int B, int T,
                     int Hq, int Hkv, int D, double scale, int causal);
 
+/* delta[b, h, i] = sum_d dout[b, i, h, d] * o[b, i, h, d] for a given o
+ * (the rowsum that the backward's first step forms from the stored output). */
+void oracle_rowdot(const double* o, const double* dout, double* delta, int B, int T, int H, int D);
+
 /* Number of OpenMP threads the oracle uses. */
 int oracle_num_threads(void);
 

@@ -159,6 +159,14 @@ def test_gqa_is_repeated_kv_mha(G):
     assert _rel(dv, dv_sum) <= 1e-13
 
 
+def test_rowdot_is_the_backward_delta():
+    """The standalone rowsum of dO * O equals the D_i the backward forms."""
+    q, k, v, do = _case(14, 2, 21, 4, 2, 8)
+    o, _ = oracle.attn_fwd(q, k, v, 0.3, True)
+    *_, delta, _ = oracle.attn_bwd(q, k, v, do, 0.3, True)
+    np.testing.assert_allclose(oracle.rowdot(o, do), delta, rtol=1e-13, atol=1e-15)
+
+
 def test_delta_forms_agree():
     """D_i = dO_i.O_i equals sum_j P_ij dP_ij (softmax Jacobian identity)."""
     q, k, v, do = _case(9, 2, 33, 6, 2, 16)
