@@ -145,8 +145,7 @@ class Problem:
             outs = dict(o=torch.empty_like(ins[0]), dq=torch.empty_like(ins[0]),
                         dk=torch.empty_like(ins[1]), dv=torch.empty_like(ins[2]),
                         lse=torch.empty((B, Hq, T), dtype=torch.float32, device=device),
-                        ws=torch.empty((max(16, da.workspace_bytes(*w.shape)),),
-                                       dtype=torch.uint8, device=device))
+                        ws=da.new_workspace(*w.shape, device=device))
             self.sets.append((ins, outs))
         self.scale = w.softmax_scale
 
@@ -163,15 +162,14 @@ class Problem:
         """One kernel of the step on set s (for per-kernel timing)."""
         da = self.da
         (q, k, v, do), o = self.sets[s % len(self.sets)]
-        delta = o["ws"][: 4 * o["lse"].numel()].view(torch.float32).view(o["lse"].shape)
         if which == "fwd":
             da.attn_fwd(q, k, v, scale=self.scale, out=o["o"], lse=o["lse"])
         elif which == "delta":
-            da.attn_bwd_delta(o["o"], do, delta)
+            da.attn_bwd_delta(o["o"], do, o["lse"], o["ws"])
         elif which == "dkdv":
-            da.attn_bwd_dkdv(q, k, v, o["lse"], delta, do, scale=self.scale, dk=o["dk"], dv=o["dv"])
+            da.attn_bwd_dkdv(q, k, v, do, o["ws"], scale=self.scale, dk=o["dk"], dv=o["dv"])
         else:
-            da.attn_bwd_dq(q, k, v, o["lse"], delta, do, scale=self.scale, dq=o["dq"])
+            da.attn_bwd_dq(q, k, v, do, o["ws"], scale=self.scale, dq=o["dq"])
 
     def step_api(self, s):
         """The public two-call API (attn_fwd + attn_bwd)."""
@@ -319,7 +317,7 @@ def run_gpu_arm(args, world, rank):
     heads = B * Hq
     kflops = {"attn_fwd": 2.0 * heads * T * T * D, "attn_bwd_dkdv": 4.0 * heads * T * T * D,
               "attn_bwd_dq": 1.0 * heads * T * T * D}
-    delta_bytes = B * T * Hq * D * 2 * 2 + B * Hq * T * 4
+    delta_bytes = B * T * Hq * D * 2 * 2 + B * Hq * T * (4 + 8)
     top = max(per_kernel_ms, key=per_kernel_ms.get)
     if top == "attn_bwd_delta":
         ach = delta_bytes / (per_kernel_ms[top] * 1e-3) / 1e9

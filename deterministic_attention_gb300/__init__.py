@@ -21,7 +21,8 @@ import torch
 from .build import LIB as _LIB_PATH, build  # noqa: F401
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_delta", "attn_bwd_dkdv", "attn_bwd_dq",
-           "workspace_bytes", "check_status", "set_wait_limit_ns", "last_error", "lib",
+           "workspace_bytes", "check_status", "set_wait_limit_ns", "selftest_wait_timeout",
+           "set_dkdv_split", "new_workspace", "rowstats_view", "last_error", "lib",
            "DetAttnError", "STATUS", "header_symbols", "build"]
 
 STATUS = {0: "DETATTN_OK", -1: "DETATTN_ERR_NULL", -2: "DETATTN_ERR_ALIGN",
@@ -55,10 +56,16 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
     L.attn_bwd_workspace_bytes.restype = sz
     L.attn_bwd.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
-    L.attn_bwd_delta.argtypes = [vp, vp, fp, i, i, i, i, vp]
-    L.attn_bwd_dkdv.argtypes = [vp, vp, vp, fp, fp, vp, vp, vp, i, i, i, i, i, f, i, vp]
-    L.attn_bwd_dq.argtypes = [vp, vp, vp, fp, fp, vp, vp, i, i, i, i, i, f, i, vp]
+    L.attn_bwd_delta.argtypes = [vp, vp, fp, vp, sz, i, i, i, i, vp]
+    L.attn_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, sz, vp, vp, i, i, i, i, i, f, i, vp]
+    L.attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, sz, vp, i, i, i, i, i, f, i, vp]
     L.detattn_check_status.argtypes = [vp]
+    L.detattn_diag_exp2.argtypes = [vp, vp, vp, vp, i, vp]
+    L.detattn_diag_exp2.restype = i
+    L.detattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
+    L.detattn_selftest_wait_timeout.restype = i
+    L.detattn_set_dkdv_split.argtypes = [i]
+    L.detattn_set_dkdv_split.restype = i
     L.detattn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     L.detattn_set_wait_limit_ns.restype = None
     L.detattn_last_error.argtypes = []
@@ -155,9 +162,8 @@ def attn_bwd(q, k, v, o, lse, dout, scale=None, causal=True, dq=None, dk=None, d
     _need(dq, "dq", bf, (B, T, Hq, D))
     _need(dk, "dk", bf, (B, T, Hkv, D))
     _need(dv, "dv", bf, (B, T, Hkv, D))
-    nbytes = workspace_bytes(B, T, Hq, Hkv, D)
     if workspace is None:
-        workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=q.device)
+        workspace = new_workspace(B, T, Hq, Hkv, D, q.device)
     rc = lib().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
                         _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(), B, T, Hq, Hkv, D,
                         _scale(scale, D), int(bool(causal)), _stream())
@@ -165,39 +171,74 @@ def attn_bwd(q, k, v, o, lse, dout, scale=None, causal=True, dq=None, dk=None, d
     return dq, dk, dv
 
 
-def attn_bwd_delta(o, dout, delta=None):
+def new_workspace(B, T, Hq, Hkv, D, device="cuda"):
+    """A device workspace of attn_bwd_workspace_bytes (uint8)."""
+    return torch.empty((max(16, workspace_bytes(B, T, Hq, Hkv, D)),), dtype=torch.uint8,
+                       device=device)
+
+
+def rowstats_view(workspace, B, T, Hq):
+    """The workspace's row statistics as fp32 [B, Hq, Tp, 2]:
+    [..., 0] = -LSE*log2(e), [..., 1] = -Delta (see include/detattn.h)."""
+    Tp = (T + 127) // 128 * 128
+    return workspace[: B * Hq * Tp * 8].view(torch.float32).view(B, Hq, Tp, 2)
+
+
+def attn_bwd_delta(o, dout, lse, workspace):
+    """Backward step 1: row statistics (from o, dout, lse) into `workspace`."""
     B, T, Hq, D = o.shape
-    delta = torch.empty((B, Hq, T), dtype=torch.float32, device=o.device) if delta is None else delta
     _need(o, "o", torch.bfloat16, (B, T, Hq, D))
     _need(dout, "dout", torch.bfloat16, (B, T, Hq, D))
-    _need(delta, "delta", torch.float32, (B, Hq, T))
-    _check(lib().attn_bwd_delta(_ptr(o), _ptr(dout), _ptr(delta), B, T, Hq, D, _stream()),
-           "attn_bwd_delta")
-    return delta
+    _need(lse, "lse", torch.float32, (B, Hq, T))
+    _check(lib().attn_bwd_delta(_ptr(o), _ptr(dout), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                B, T, Hq, D, _stream()), "attn_bwd_delta")
+    return workspace
 
 
-def attn_bwd_dkdv(q, k, v, lse, delta, dout, scale=None, causal=True, dk=None, dv=None):
+def attn_bwd_dkdv(q, k, v, dout, workspace, scale=None, causal=True, dk=None, dv=None):
+    """Backward step 2: dk, dv from the row statistics in `workspace`."""
     B, T, Hq, Hkv, D = _dims(q, k)
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    _check(lib().attn_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(dout),
-                               _ptr(dk), _ptr(dv), B, T, Hq, Hkv, D, _scale(scale, D),
-                               int(bool(causal)), _stream()), "attn_bwd_dkdv")
+    _check(lib().attn_bwd_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(workspace),
+                               workspace.numel(), _ptr(dk), _ptr(dv), B, T, Hq, Hkv, D,
+                               _scale(scale, D), int(bool(causal)), _stream()), "attn_bwd_dkdv")
     return dk, dv
 
 
-def attn_bwd_dq(q, k, v, lse, delta, dout, scale=None, causal=True, dq=None):
+def attn_bwd_dq(q, k, v, dout, workspace, scale=None, causal=True, dq=None):
+    """Backward step 3: dq from the row statistics in `workspace`."""
     B, T, Hq, Hkv, D = _dims(q, k)
     dq = torch.empty_like(q) if dq is None else dq
-    _check(lib().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(delta), _ptr(dout),
-                             _ptr(dq), B, T, Hq, Hkv, D, _scale(scale, D), int(bool(causal)),
-                             _stream()), "attn_bwd_dq")
+    _check(lib().attn_bwd_dq(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(workspace),
+                             workspace.numel(), _ptr(dq), B, T, Hq, Hkv, D, _scale(scale, D),
+                             int(bool(causal)), _stream()), "attn_bwd_dq")
     return dq
 
 
 def check_status():
     """Synchronises the current stream and raises if a kernel timed out."""
     _check(lib().detattn_check_status(_stream()), "detattn_check_status")
+
+
+def diag_exp2(x):
+    """(poly, poly pair form, special-function unit) 2^x of a float32 CUDA tensor."""
+    _need(x, "x", torch.float32, tuple(x.shape))
+    ys = [torch.empty_like(x) for _ in range(3)]
+    _check(lib().detattn_diag_exp2(_ptr(x), _ptr(ys[0]), _ptr(ys[1]), _ptr(ys[2]), x.numel(),
+                                   _stream()), "detattn_diag_exp2")
+    return tuple(ys)
+
+
+def selftest_wait_timeout(limit_ns: int = 50_000_000):
+    """Runs the device-side bounded-wait self-test (see include/detattn.h)."""
+    _check(lib().detattn_selftest_wait_timeout(int(limit_ns), _stream()),
+           "detattn_selftest_wait_timeout")
+
+
+def set_dkdv_split(blocks_per_key_tile: int):
+    """Forces the dK/dV split (1, 2, 4, 8) or restores automatic (0)."""
+    _check(lib().detattn_set_dkdv_split(int(blocks_per_key_tile)), "detattn_set_dkdv_split")
 
 
 def set_wait_limit_ns(ns: int):

@@ -24,6 +24,7 @@
 #include <cstdint>
 
 #include "attn_launch.h"
+#include "exp2_poly.cuh"
 #include "sm103_ptx.cuh"
 
 namespace detattn {
@@ -34,6 +35,12 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kThreads = 192;
+// Of every 8 consecutive pairs of probabilities, this many take 2^x from the
+// FMA-pipe polynomial instead of the special-function unit.
+#ifndef DETATTN_BWD_POLY_OF8
+#define DETATTN_BWD_POLY_OF8 2
+#endif
+constexpr int kPolyOf8 = DETATTN_BWD_POLY_OF8;
 
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
@@ -42,10 +49,11 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
 }
 
 // ============================================================== Delta
-// One warp per (b, h, 32 consecutive rows).  Each row of D bf16 is split in
-// 16-byte chunks over D/8 lanes; a lane forms its 8 products in order, the
-// lanes of a row are combined by a fixed xor-shuffle tree, and lane t stores
-// row t of the group (coalesced).
+// One warp per (b, h, 32 consecutive positions).  Each row of D bf16 is split
+// in 16-byte chunks over D/8 lanes; a lane issues all its loads first, forms
+// its 8 products per chunk in order, the lanes of a row are combined by a
+// fixed xor-shuffle tree, and lane t stores the (-LSE*log2e, -Delta) pair of
+// position t (coalesced).  Positions T..Tp-1 get (-inf, -0).
 template <int D>
 __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
   constexpr int kCpr = D / 8;        // 16-byte chunks per row
@@ -53,7 +61,7 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
   constexpr int kIters = 32 / kRpi;
   const int lane = threadIdx.x & 31;
   const long unit = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int tchunks = (a.T + 31) / 32;
+  const int tchunks = a.Tp / 32;
   const long units = static_cast<long>(a.B) * a.Hq * tchunks;
   if (unit >= units) return;
   const int tc = static_cast<int>(unit % tchunks);
@@ -62,35 +70,39 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
   const int i0 = tc * 32;
   const uint4* O = static_cast<const uint4*>(a.o);
   const uint4* dO = static_cast<const uint4*>(a.dout);
-  float res[kIters];
+  const int mine_i = i0 + lane;
+  const float lse = mine_i < a.T ? a.lse[static_cast<size_t>(bh) * a.T + mine_i] : 0.f;
+  uint4 xo[kIters], xd[kIters];
 #pragma unroll
   for (int it = 0; it < kIters; ++it) {
     const int i = i0 + it * kRpi + lane / kCpr;
-    const int c = lane % kCpr;
-    float acc = 0.f;
+    xo[it] = make_uint4(0u, 0u, 0u, 0u);
+    xd[it] = xo[it];
     if (i < a.T) {
-      const size_t off = ((static_cast<size_t>(b) * a.T + i) * a.Hq + h) * kCpr + c;
-      const uint4 x = O[off], y = dO[off];
-      const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 xf = bf16x2_to_float2(xs[k]), yf = bf16x2_to_float2(ys[k]);
-        acc = fmaf(xf.x, yf.x, acc);
-        acc = fmaf(xf.y, yf.y, acc);
-      }
+      const size_t off = ((static_cast<size_t>(b) * a.T + i) * a.Hq + h) * kCpr + lane % kCpr;
+      xo[it] = O[off];
+      xd[it] = dO[off];
     }
-#pragma unroll
-    for (int s = kCpr / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    res[it] = acc;
   }
   float mine = 0.f;
 #pragma unroll
   for (int it = 0; it < kIters; ++it) {
-    const float v = __shfl_sync(0xffffffffu, res[it], (lane % kRpi) * kCpr);
+    const uint32_t xs[4] = {xo[it].x, xo[it].y, xo[it].z, xo[it].w};
+    const uint32_t ys[4] = {xd[it].x, xd[it].y, xd[it].z, xd[it].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 xf = bf16x2_to_float2(xs[k]), yf = bf16x2_to_float2(ys[k]);
+      acc = fmaf(xf.x, yf.x, acc);
+      acc = fmaf(xf.y, yf.y, acc);
+    }
+#pragma unroll
+    for (int s = kCpr / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    const float v = __shfl_sync(0xffffffffu, acc, (lane % kRpi) * kCpr);
     if (lane / kRpi == it) mine = v;
   }
-  const int i = i0 + lane;
-  if (i < a.T) a.delta[(static_cast<size_t>(b) * a.Hq + h) * a.T + i] = mine;
+  a.rowstats[static_cast<size_t>(bh) * a.Tp + mine_i] =
+      mine_i < a.T ? make_float2(-lse * kLog2e, -mine) : make_float2(-INFINITY, -0.f);
 }
 
 // ============================================================== dK / dV
@@ -117,6 +129,9 @@ struct DkvCfg {
   static constexpr uint32_t kColDK = 128 + D; // dK accumulator, D cols
 };
 
+static_assert(kTileN * 2 * 64 * 4 <= DkvCfg<64>::kSmemBytes - 1024, "dK/dV partials fit");
+static_assert(kTileN * 2 * 128 * 4 <= DkvCfg<128>::kSmemBytes - 1024, "dK/dV partials fit");
+
 enum : int { kDkvBarKV = 0, kDkvBarQFull = 1, kDkvBarQEmpty = 4, kDkvBarS = 7, kDkvBarP = 8,
              kDkvBarAcc = 9, kDkvBarDrain = 10, kDkvNumBars = 11 };
 
@@ -125,37 +140,50 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                      const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
                      const BwdArgs a) {
-  using C = DkvCfg<D>;
-  constexpr int NS = C::kStages;
+  using Cf = DkvCfg<D>;
+  constexpr int NS = Cf::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[kDkvNumBars];
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // A cluster of C blocks shares one key tile: the tile's (head, query tile)
+  // items, in ascending order, are cut into C contiguous chunks; block r sums
+  // chunk r in its TMEM, and the C partial sums are added in rank order.
+  const int C = a.cluster;
+  const int crank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int tile = static_cast<int>(blockIdx.x) / C;
   // Key tiles near the start of the sequence see the most query tiles under
   // the causal mask: hand those out first.
-  const int nt = static_cast<int>(blockIdx.x) / a.BH;
-  const int bg = static_cast<int>(blockIdx.x) % a.BH;
+  const int nt = tile / a.BH;
+  const int bg = tile % a.BH;
   const int b = bg / a.Hkv, g = bg % a.Hkv;
   const int G = a.Hq / a.Hkv;
   const int n0 = nt * kTileN;
   const int m_begin = a.causal ? n0 / kDkvTileM : 0;
   const int m_end = (a.T + kDkvTileM - 1) / kDkvTileM;
   const int per_head = m_end - m_begin;
-  const int n_it = G * per_head;
+  const int n_all = G * per_head;
+  const int it_lo = static_cast<int>(static_cast<long>(crank) * n_all / C);
+  const int n_it = static_cast<int>(static_cast<long>(crank + 1) * n_all / C) - it_lo;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t s0 = smem_u32(smem);
-  const uint32_t sK = s0 + C::kOffK, sV = s0 + C::kOffV;
-  auto stage_base = [&](int s) { return s0 + C::kOffStage + s * C::kStageBytes; };
-  auto stage_rows = [&](int s) {  // float lse2[64], delta[64]
-    return reinterpret_cast<float*>(smem + C::kOffStage + s * C::kStageBytes + 2 * C::kQBytes);
+  const uint32_t sK = s0 + Cf::kOffK, sV = s0 + Cf::kOffV;
+  auto stage_base = [&](int s) { return s0 + Cf::kOffStage + s * Cf::kStageBytes; };
+  auto stage_rows = [&](int s) {  // 64 pairs (-LSE*log2e, -Delta)
+    return reinterpret_cast<float*>(smem + Cf::kOffStage + s * Cf::kStageBytes + 2 * Cf::kQBytes);
   };
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  // Byte offset of 16-byte chunk `chunk` of partial-sum row `row` (2D floats
+  // per row, chunks XOR-swizzled by row % 8 against bank conflicts).
+  auto partial_off = [](int row, int chunk) {
+    return static_cast<uint32_t>(row * (2 * D * 4) + ((chunk ^ (row & 7)) * 16));
+  };
 
   if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+    tmem_alloc(smem_u32(&tmem_slot), Cf::kTmemCols);
     tmem_relinquish();
     tc_fence_before();
   }
@@ -187,46 +215,35 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     // ------------------------------------------------------------ producer (whole warp)
     int last[3] = {-1, -1, -1};
     if (lane == 0) {
-      mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * C::kKvBytes);
-      for (int at = 0; at < C::kAtoms; ++at) {
+      mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * Cf::kKvBytes);
+      for (int at = 0; at < Cf::kAtoms; ++at) {
         tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, g, n0, b);
         tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, g, n0, b);
       }
     }
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it % NS;
-      const uint32_t ph = (it / NS) & 1;
+    for (int li = 0; li < n_it; ++li) {
+      const int it = it_lo + li;
+      const int s = li % NS;
+      const uint32_t ph = (li / NS) & 1;
       const int h = g * G + it / per_head;
       const int i0 = (m_begin + it % per_head) * kDkvTileM;
-      if (it >= NS) {
+      if (li >= NS) {
         ok = warp_all(mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns));
         if (!ok) break;
       }
-      float* rows = stage_rows(s);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int c = lane + 32 * k;
-        const int i = i0 + c;
-        float l2 = INFINITY, dl = 0.f;  // rows past T: P = exp2(-inf) = 0
-        if (i < a.T) {
-          const size_t off = (static_cast<size_t>(b) * a.Hq + h) * a.T + i;
-          l2 = a.lse[off] * kLog2e;
-          dl = a.delta[off];
-        }
-        rows[c] = l2;
-        rows[64 + c] = dl;
-      }
-      __syncwarp();
       if (lane == 0) {
         const uint32_t st = stage_base(s);
-        mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * C::kQBytes);
-        for (int at = 0; at < C::kAtoms; ++at) {
+        mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + kDkvTileM * 8);
+        for (int at = 0; at < Cf::kAtoms; ++at) {
           tma_load_4d(st + at * (kDkvTileM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h, i0, b);
-          tma_load_4d(st + C::kQBytes + at * (kDkvTileM * 128), &mdO, bar(kDkvBarQFull + s),
+          tma_load_4d(st + Cf::kQBytes + at * (kDkvTileM * 128), &mdO, bar(kDkvBarQFull + s),
                       at * 64, h, i0, b);
         }
+        bulk_load(st + 2 * Cf::kQBytes,
+                  a.rowstats + (static_cast<size_t>(b) * a.Hq + h) * a.Tp + i0, kDkvTileM * 8,
+                  bar(kDkvBarQFull + s));
       }
-      last[s] = it;
+      last[s] = li;
     }
     if (!ok && lane == 0) {
       mbar_wait(bar(kDkvBarKV), 0, wait_ns);
@@ -236,16 +253,16 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP;
-      const uint32_t tDV = tmem + C::kColDV, tDK = tmem + C::kColDK;
+      const uint32_t tS = tmem + Cf::kColS, tDP = tmem + Cf::kColDP;
+      const uint32_t tDV = tmem + Cf::kColDV, tDK = tmem + Cf::kColDK;
       constexpr uint32_t kIdS = idesc_bf16(kTileN, kDkvTileM, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
       ok = mbar_wait(bar(kDkvBarKV), 0, wait_ns);
       tc_fence_after();
-      for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it % NS;
-        const uint32_t ph = (it / NS) & 1;
-        const uint32_t sQ = stage_base(s), sdO = stage_base(s) + C::kQBytes;
+      for (int li = 0; li < n_it && ok; ++li) {
+        const int s = li % NS;
+        const uint32_t ph = (li / NS) & 1;
+        const uint32_t sQ = stage_base(s), sdO = stage_base(s) + Cf::kQBytes;
         if (!(ok = mbar_wait(bar(kDkvBarQFull + s), ph, wait_ns))) break;
         tc_fence_after();
 #pragma unroll
@@ -262,12 +279,12 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
                  ks > 0);
         }
         mma_commit(bar(kDkvBarS));
-        if (!(ok = mbar_wait(bar(kDkvBarP), it & 1, wait_ns))) break;
+        if (!(ok = mbar_wait(bar(kDkvBarP), li & 1, wait_ns))) break;
         tc_fence_after();
         // Accumulate over the 64 queries of this tile, 16 at a time.
 #pragma unroll
         for (int ks = 0; ks < kDkvTileM / 16; ++ks) {
-          const uint32_t acc = (it > 0 || ks > 0) ? 1u : 0u;
+          const uint32_t acc = (li > 0 || ks > 0) ? 1u : 0u;
           mma_ts(tDV, tS + ks * 8, sdesc_sw128(sdO + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
           mma_ts(tDK, tDP + ks * 8, sdesc_sw128(sQ + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
         }
@@ -284,17 +301,18 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     const int krow = n0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it % NS;
+    for (int li = 0; li < n_it; ++li) {
+      const int it = it_lo + li;
+      const int s = li % NS;
       const int i0 = (m_begin + it % per_head) * kDkvTileM;
-      ok = warp_all(mbar_wait(bar(kDkvBarS), it & 1, wait_ns));
+      ok = warp_all(mbar_wait(bar(kDkvBarS), li & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
       uint32_t sv[2][32], dp[2][32];
-      tmem_ld32_nowait(tl + C::kColS, sv[0]);
-      tmem_ld32_nowait(tl + C::kColS + 32, sv[1]);
-      tmem_ld32_nowait(tl + C::kColDP, dp[0]);
-      tmem_ld32_nowait(tl + C::kColDP + 32, dp[1]);
+      tmem_ld32_nowait(tl + Cf::kColS, sv[0]);
+      tmem_ld32_nowait(tl + Cf::kColS + 32, sv[1]);
+      tmem_ld32_nowait(tl + Cf::kColDP, dp[0]);
+      tmem_ld32_nowait(tl + Cf::kColDP + 32, dp[1]);
       tmem_wait_ld();
       reg_fence32(sv[0]);
       reg_fence32(sv[1]);
@@ -304,30 +322,72 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       // Causal: query i0 + c sees key krow iff c >= krow - i0.
       const int cmin = a.causal ? (krow - i0) : -1;
       uint32_t pk[32], dk[32];
+      const uint64_t sl2x2 = f2_make(sl2, sl2);
+      const float4* st4 = reinterpret_cast<const float4*>(rows);  // 2 positions per float4
+      const bool need_mask = cmin > 0;
 #pragma unroll
       for (int c2 = 0; c2 < 32; ++c2) {
-        float pv[2], dsv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 2 * c2 + e;
-          const float sval = __uint_as_float(sv[c >> 5][c & 31]);
-          float p = ex2_approx(fmaf(sval, sl2, -rows[c]));
-          if (c < cmin) p = 0.f;
-          pv[e] = p;
-          dsv[e] = p * (__uint_as_float(dp[c >> 5][c & 31]) - rows[64 + c]);
+        const int c = 2 * c2;
+        const float4 rs = st4[c2];  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
+        const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c >> 5][c & 31]),
+                                          __uint_as_float(sv[c >> 5][(c + 1) & 31])), sl2x2,
+                                  f2_make(rs.x, rs.z));
+        float x0, x1, p0, p1;
+        f2_split(x, x0, x1);
+        if ((c2 & 7) < kPolyOf8) {
+          exp2_poly2(x0, x1, p0, p1);
+        } else {
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
         }
-        pk[c2] = pack_bf16x2(pv[0], pv[1]);
-        dk[c2] = pack_bf16x2(dsv[0], dsv[1]);
+        if (need_mask) {
+          if (c < cmin) p0 = 0.f;
+          if (c + 1 < cmin) p1 = 0.f;
+        }
+        const uint64_t dpm = f2_add(f2_make(__uint_as_float(dp[c >> 5][c & 31]),
+                                            __uint_as_float(dp[c >> 5][(c + 1) & 31])),
+                                    f2_make(rs.y, rs.w));
+        float d0, d1;
+        f2_split(f2_mul(f2_make(p0, p1), dpm), d0, d1);
+        pk[c2] = pack_bf16x2(p0, p1);
+        dk[c2] = pack_bf16x2(d0, d1);
       }
-      tmem_st32_nowait(tl + C::kColS, pk);
-      tmem_st32_nowait(tl + C::kColDP, dk);
+      tmem_st32_nowait(tl + Cf::kColS, pk);
+      tmem_st32_nowait(tl + Cf::kColDP, dk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kDkvBarP));
     }
     if (ok) ok = warp_all(mbar_wait(bar(kDkvBarAcc), 0, wait_ns));
-    if (ok) {
+    if (ok && C > 1) {
+      // Partial sums to this block's shared memory (fp32, row r = key row r,
+      // [dV | dK] = 2D floats per row, 16-byte chunks XOR-swizzled by r % 8).
+      tc_fence_after();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? Cf::kColDV : Cf::kColDK;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          if (n_it > 0) {
+            tmem_ld32(tl + col + c * 32, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0u;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int chunk = (which * D + c * 32) / 4 + i;
+            st_shared_f4(s0 + partial_off(r, chunk),
+                         make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+          }
+        }
+      }
+    }
+    if (ok && C == 1) {
       tc_fence_after();
       const bool live = krow < a.T;
       const size_t rbase = ((static_cast<size_t>(b) * a.T + krow) * a.Hkv + g) * D;
@@ -335,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       __nv_bfloat16* dkrow = static_cast<__nv_bfloat16*>(a.dk) + rbase;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? C::kColDV : C::kColDK;
+        const uint32_t col = which == 0 ? Cf::kColDV : Cf::kColDK;
         const float mul = which == 0 ? 1.f : a.scale;
         __nv_bfloat16* dst_row = which == 0 ? dvrow : dkrow;
 #pragma unroll
@@ -357,13 +417,54 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     }
   }
 
+  if (C > 1) {
+    // Every block of the cluster reaches both barriers (no early exit; all
+    // waits above are bounded), so the cluster barrier always completes.
+    __syncwarp();
+    cluster_sync();
+    if (warp >= 2) {
+      // Block `crank` owns key rows [crank*R, (crank+1)*R) of the tile: it adds
+      // the C partial sums in rank order and stores bf16 dV, dK (dK * scale).
+      const int R = kTileN / C;
+      constexpr int kCpr = 2 * D / 8;  // 8-float output chunks per row ([dV | dK])
+      const int ct = static_cast<int>(threadIdx.x) - 64;
+      for (int e = ct; e < R * kCpr; e += 128) {
+        const int rl = e / kCpr, oc = e % kCpr;
+        const int row = crank * R + rl;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        for (int src = 0; src < C; ++src) {
+          const uint32_t base = map_shared_rank(s0, static_cast<uint32_t>(src));
+          const float4 x = ld_shared_cluster_f4(base + partial_off(row, 2 * oc));
+          const float4 y = ld_shared_cluster_f4(base + partial_off(row, 2 * oc + 1));
+          acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
+          acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
+        }
+        const bool is_dk = oc * 8 >= D;
+        const float mul = is_dk ? a.scale : 1.f;
+        const int col = oc * 8 - (is_dk ? D : 0);
+        const int krow_out = n0 + row;
+        if (krow_out < a.T) {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_dk ? a.dk : a.dv) +
+                               ((static_cast<size_t>(b) * a.T + krow_out) * a.Hkv + g) * D + col;
+          *reinterpret_cast<uint4*>(dst) =
+              make_uint4(pack_bf16x2(acc[0] * mul, acc[1] * mul), pack_bf16x2(acc[2] * mul, acc[3] * mul),
+                         pack_bf16x2(acc[4] * mul, acc[5] * mul), pack_bf16x2(acc[6] * mul, acc[7] * mul));
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();
+  }
+
   if (!ok) atomicOr(&g_bwd_status, 2u);
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc(tmem, Cf::kTmemCols);
   }
 }
 
@@ -530,12 +631,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int qrow = m0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
-    float lse2 = INFINITY, dl = 0.f;  // rows past T: P = 0, dS = 0
-    if (qrow < a.T) {
-      const size_t off = (static_cast<size_t>(b) * a.Hq + h) * a.T + qrow;
-      lse2 = a.lse[off] * kLog2e;
-      dl = a.delta[off];
-    }
+    // (-LSE*log2e, -Delta) of this row; rows past T read (-inf, -0): P = 0.
+    const float2 rstat = a.rowstats[(static_cast<size_t>(b) * a.Hq + h) * a.Tp + qrow];
     for (int j = 0; j < n_kv; ++j) {
       ok = warp_all(mbar_wait(bar(kDqBarS), j & 1, wait_ns));
       if (!ok) break;
@@ -554,17 +651,31 @@ __global__ void __launch_bounds__(kThreads, 2)
       // key kv0 + c visible iff c <= lim
       const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
       uint32_t dsk[32];
+      const uint64_t sl2x2 = f2_make(sl2, sl2), neg_l = f2_make(rstat.x, rstat.x);
+      const uint64_t neg_d = f2_make(rstat.y, rstat.y);
+      const bool need_mask = a.causal ? (kv0 + kDqTileN - 1 > m0) : (kv0 + kDqTileN > a.T);
 #pragma unroll
       for (int c2 = 0; c2 < 32; ++c2) {
-        float dsv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int c = 2 * c2 + e;
-          float p = ex2_approx(fmaf(__uint_as_float(sv[c >> 5][c & 31]), sl2, -lse2));
-          if (c > lim) p = 0.f;
-          dsv[e] = p * (__uint_as_float(dp[c >> 5][c & 31]) - dl);
+        const int c = 2 * c2;
+        const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c >> 5][c & 31]),
+                                          __uint_as_float(sv[c >> 5][(c + 1) & 31])), sl2x2, neg_l);
+        float x0, x1, p0, p1;
+        f2_split(x, x0, x1);
+        if ((c2 & 7) < kPolyOf8) {
+          exp2_poly2(x0, x1, p0, p1);
+        } else {
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
         }
-        dsk[c2] = pack_bf16x2(dsv[0], dsv[1]);
+        if (need_mask) {
+          if (c > lim) p0 = 0.f;
+          if (c + 1 > lim) p1 = 0.f;
+        }
+        const uint64_t dpm = f2_add(f2_make(__uint_as_float(dp[c >> 5][c & 31]),
+                                            __uint_as_float(dp[c >> 5][(c + 1) & 31])), neg_d);
+        float d0, d1;
+        f2_split(f2_mul(f2_make(p0, p1), dpm), d0, d1);
+        dsk[c2] = pack_bf16x2(d0, d1);
       }
       tmem_st32_nowait(tl + C::kColS, dsk);
       tmem_wait_st();
@@ -607,6 +718,18 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// Failure-detection self-test: one thread waits, with the same bounded wait
+// the attention kernels use, on an mbarrier that nothing arrives on.  The wait
+// runs out, the kernel records the timeout in the status word and returns; no
+// asynchronous copy or MMA is in flight, so nothing else needs draining.
+__global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  fence_barrier_init();
+  if (!mbar_wait(smem_u32(&bar), 0, limit_ns)) atomicOr(&g_bwd_status, 8u);
+}
+
 template <typename K>
 cudaError_t set_smem_once(K kernel, int bytes, bool* done) {
   int dev = 0;
@@ -627,7 +750,24 @@ cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk
   static bool done[64] = {};
   cudaError_t e = set_smem_once(attn_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
-  attn_dkdv_kernel<D><<<grid, kThreads, DkvCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
+  if (a.cluster <= 1) {
+    attn_dkdv_kernel<D><<<grid, kThreads, DkvCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = DkvCfg<D>::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_dkdv_kernel<D>, mq, mk, mv, mdo, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -645,7 +785,7 @@ cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
 }  // namespace
 
 cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st) {
-  const long units = static_cast<long>(a.B) * a.Hq * ((a.T + 31) / 32);
+  const long units = static_cast<long>(a.B) * a.Hq * (a.Tp / 32);
   const int grid = static_cast<int>((units + 7) / 8);
   if (a.D == 64)
     attn_delta_kernel<64><<<grid, 256, 0, st>>>(a);
@@ -666,6 +806,37 @@ cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap&
                       cudaStream_t st) {
   return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, a, st)
                  : launch_dq_t<128>(grid, mq, mk, mv, mdo, a, st);
+}
+
+// Diagnostic: the kernels' 2^x forms on n inputs (polynomial scalar form,
+// polynomial pair form, special-function unit).
+__global__ void exp2_diag_kernel(const float* x, float* y_poly, float* y_pair, float* y_sfu,
+                                 int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const float x0 = x[i], x1 = (i + 1 < n) ? x[i + 1] : 0.f;
+  float p0, p1;
+  exp2_poly2(x0, x1, p0, p1);
+  y_poly[i] = exp2_poly(x0);
+  y_pair[i] = p0;
+  y_sfu[i] = ex2_approx(x0);
+  if (i + 1 < n) {
+    y_poly[i + 1] = exp2_poly(x1);
+    y_pair[i + 1] = p1;
+    y_sfu[i + 1] = ex2_approx(x1);
+  }
+}
+
+cudaError_t launch_exp2_diag(const float* x, float* y_poly, float* y_pair, float* y_sfu, int n,
+                             cudaStream_t st) {
+  const int pairs = (n + 1) / 2;
+  exp2_diag_kernel<<<(pairs + 255) / 256, 256, 0, st>>>(x, y_poly, y_pair, y_sfu, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t st) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t take_bwd_status(cudaStream_t st, unsigned* out) {

@@ -23,6 +23,7 @@
 #include <cstdint>
 
 #include "attn_launch.h"
+#include "exp2_poly.cuh"
 #include "sm103_ptx.cuh"
 
 namespace detattn {
@@ -37,6 +38,12 @@ constexpr int kThreads = 192;
 // accumulators hold exactly as well.  The final O / l and LSE are exact for
 // any value of the stale maximum.
 constexpr float kRescaleLog2 = 8.0f;
+// Of every 8 consecutive pairs of scores, this many take 2^x from the FMA-pipe
+// polynomial instead of the special-function unit, to balance the two.
+#ifndef DETATTN_FWD_POLY_OF8
+#define DETATTN_FWD_POLY_OF8 2
+#endif
+constexpr int kPolyOf8 = DETATTN_FWD_POLY_OF8;
 
 template <int D>
 struct Cfg {
@@ -210,7 +217,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c >> 5][c & 31]));
+      for (int c = 0; c < 64; ++c)
+        mx = fmax3(mx, __uint_as_float(sr[c >> 4][(2 * c) & 31]),
+                   __uint_as_float(sr[c >> 4][(2 * c + 1) & 31]));
       const float m_new = mx * sl2;
       float alpha = 1.f;
       bool moved = false;
@@ -220,19 +229,34 @@ __global__ void __launch_bounds__(kThreads, 2)
         moved = true;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      float rowsum = 0.f;
-      uint32_t pk[2][32];
+      const int lim = need_mask ? (a.causal ? (qrow - kv0) : (a.T - 1 - kv0)) : 1 << 30;
+      const uint64_t sl2x2 = f2_make(sl2, sl2), neg_m = f2_make(-m_use, -m_use);
+      uint64_t sum2 = f2_make(0.f, 0.f);  // two running partial row sums
+      // P in four chunks of 32 scores (16 packed bf16 pairs each), stored to
+      // TMEM over the S columns already consumed.
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[(2 * c) >> 5][(2 * c) & 31]), sl2, -m_use));
-        const float p1 =
-            ex2_approx(fmaf(__uint_as_float(sr[(2 * c + 1) >> 5][(2 * c + 1) & 31]), sl2, -m_use));
-        rowsum += p0;
-        rowsum += p1;
-        pk[c >> 5][c & 31] = pack_bf16x2(p0, p1);
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = ch * 16 + i;  // pair index: scores 2c, 2c+1
+          const uint64_t x = f2_fma(f2_make(__uint_as_float(sr[ch][2 * i]),
+                                            __uint_as_float(sr[ch][2 * i + 1])), sl2x2, neg_m);
+          float x0, x1, p0, p1;
+          f2_split(x, x0, x1);
+          if ((c & 7) < kPolyOf8) {
+            exp2_poly2(x0, x1, p0, p1);
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
+          if (2 * c > lim) p0 = 0.f;  // masked keys contribute exactly zero
+          if (2 * c + 1 > lim) p1 = 0.f;
+          sum2 = f2_add(sum2, f2_make(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16_nowait(tl + C::kColS + ch * 16, pk);
       }
-      tmem_st32_nowait(tl + C::kColS, pk[0]);
-      tmem_st32_nowait(tl + C::kColS + 32, pk[1]);
       tmem_wait_st();
       if (j > 0 && __any_sync(0xffffffffu, moved)) {
         // O holds sum over earlier tiles scaled by the old maximum: wait for the
@@ -250,7 +274,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         tmem_wait_st();
       }
-      l_run = l_run * alpha + rowsum;
+      float sum_lo, sum_hi;
+      f2_split(sum2, sum_lo, sum_hi);
+      l_run = l_run * alpha + (sum_lo + sum_hi);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarP));

@@ -23,22 +23,30 @@ struct FwdArgs {
   unsigned long long wait_ns;
 };
 
+// Row statistics of the backward, in the caller's workspace: for every (b, h)
+// and every position t < Tp = T rounded up to 128, the pair
+// (-LSE * log2(e), -Delta); positions t >= T hold (-inf, -0) so padded query
+// rows contribute exactly nothing.  Both are stored negated because the
+// kernels add them: x = S * scale * log2(e) + (-LSE * log2 e), dP + (-Delta).
+inline int padded_T(int T) { return (T + 127) / 128 * 128; }
+
 struct DeltaArgs {
   const void* o;         // bf16 [B, T, Hq, D]
   const void* dout;      // bf16 [B, T, Hq, D]
-  float* delta;          // fp32 [B, Hq, T]
-  int B, T, Hq, D;
+  const float* lse;      // fp32 [B, Hq, T]
+  float2* rowstats;      // [B * Hq, Tp] pairs
+  int B, T, Tp, Hq, D;
 };
 
 struct BwdArgs {
-  const float* lse;      // fp32 [B, Hq, T]
-  const float* delta;    // fp32 [B, Hq, T]
+  const float2* rowstats;  // [B * Hq, Tp] pairs written by the Delta step
   void* dq;              // bf16 [B, T, Hq, D]   (dQ kernel)
   void* dk;              // bf16 [B, T, Hkv, D]  (dK/dV kernel)
   void* dv;
-  int T, Hq, Hkv;
+  int T, Tp, Hq, Hkv;
   int n_tiles;           // tiles per (b, head) along T
   int BH;                // B * Hq (dQ) or B * Hkv (dK/dV)
+  int cluster;           // dK/dV: blocks sharing one key tile (1, 2, 4 or 8)
   int causal;
   float scale;
   float scale_log2;
@@ -55,6 +63,13 @@ cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMa
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                       cudaStream_t st);
+
+// Launches a one-thread kernel whose bounded wait on a never-completed
+// mbarrier runs out after limit_ns (sets the timeout bit, then returns).
+cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream_t st);
+
+cudaError_t launch_exp2_diag(const float* x, float* y_poly, float* y_pair, float* y_sfu, int n,
+                             cudaStream_t st);
 
 // Read-and-clear of the device status words the kernels set when a bounded
 // wait runs out (synchronous on `st`).  Returns the OR of the words.

@@ -20,6 +20,7 @@ namespace {
 constexpr int kVersion = 10000;  // 1.0.0
 thread_local char g_err[512] = "";
 unsigned long long g_wait_ns = 1000000000ull;  // 1 s per bounded wait
+int g_dkdv_split = 0;                           // 0: automatic
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -149,18 +150,17 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   return launched(launch_fwd(D, a.n_m * a.BHq, mq, mk, mv, a, st), "attn_fwd");
 }
 
-int delta_impl(const void* o, const void* dout, float* delta, int B, int T, int Hq, int D,
-               cudaStream_t st) {
-  DeltaArgs a{o, dout, delta, B, T, Hq, D};
+int delta_impl(const void* o, const void* dout, const float* lse, void* workspace, int B, int T,
+               int Hq, int D, cudaStream_t st) {
+  DeltaArgs a{o, dout, lse, static_cast<float2*>(workspace), B, T, padded_T(T), Hq, D};
   return launched(launch_delta(a, st), "attn_bwd_delta");
 }
 
-BwdArgs bwd_args(const float* lse, const float* delta, int T, int Hq, int Hkv, float scale,
-                 int causal) {
+BwdArgs bwd_args(const void* workspace, int T, int Hq, int Hkv, float scale, int causal) {
   BwdArgs a{};
-  a.lse = lse;
-  a.delta = delta;
+  a.rowstats = static_cast<const float2*>(workspace);
   a.T = T;
+  a.Tp = padded_T(T);
   a.Hq = Hq;
   a.Hkv = Hkv;
   a.causal = causal;
@@ -170,8 +170,43 @@ BwdArgs bwd_args(const float* lse, const float* delta, int T, int Hq, int Hkv, f
   return a;
 }
 
-int dkdv_impl(const void* q, const void* k, const void* v, const float* lse, const float* delta,
-              const void* dout, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
+int sm_count(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  static int cached[64] = {};
+  if (e == cudaSuccess && dev < 64 && cached[dev] > 0) {
+    *out = cached[dev];
+    return DETATTN_OK;
+  }
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
+  if (dev < 64) cached[dev] = *out;
+  return DETATTN_OK;
+}
+
+// Blocks per key tile in the dK/dV kernel.  A key tile's work is G query heads
+// times the query tiles at or after it (causal), so the first tiles carry the
+// most.  The tile is split over C = 1, 2, 4 or 8 blocks (a cluster) until its
+// largest share is no more than 1.5x the average work per resident block.
+// The split depends only on the shape and the SM count, so the summation
+// order, and with it every output bit, is fixed for a given problem and GPU.
+int dkdv_cluster_size(int B, int T, int Hq, int Hkv, int D, int causal, int sms) {
+  const int G = Hq / Hkv;
+  const int n_tiles = (T + kTileN - 1) / kTileN;
+  const int m_end = (T + kDkvTileM - 1) / kDkvTileM;
+  double total = 0.0;
+  for (int nt = 0; nt < n_tiles; ++nt) total += m_end - (causal ? nt * kTileN / kDkvTileM : 0);
+  total *= static_cast<double>(B) * Hkv * G;
+  const double max_items = static_cast<double>(G) * m_end;
+  const double slots = static_cast<double>(sms) * (D == 64 ? 2 : 1);
+  const double avg = total / slots;
+  int c = 1;
+  while (c < 8 && max_items / c > 1.5 * avg && 2 * c <= max_items) c *= 2;
+  return c;
+}
+
+int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
+              const void* workspace, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
               float scale, int causal, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdo;
   int rc;
@@ -179,33 +214,44 @@ int dkdv_impl(const void* q, const void* k, const void* v, const float* lse, con
   if ((rc = encode_rows(&mdo, dout, B, T, Hq, D, kDkvTileM, "dout")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
-  BwdArgs a = bwd_args(lse, delta, T, Hq, Hkv, scale, causal);
+  BwdArgs a = bwd_args(workspace, T, Hq, Hkv, scale, causal);
   a.dk = dk;
   a.dv = dv;
   a.n_tiles = (T + kTileN - 1) / kTileN;
   a.BH = B * Hkv;
-  return launched(launch_dkdv(D, a.n_tiles * a.BH, mq, mk, mv, mdo, a, st), "attn_bwd_dkdv");
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
+  a.cluster = g_dkdv_split > 0 ? g_dkdv_split : dkdv_cluster_size(B, T, Hq, Hkv, D, causal, sms);
+  return launched(launch_dkdv(D, a.n_tiles * a.BH * a.cluster, mq, mk, mv, mdo, a, st),
+                  "attn_bwd_dkdv");
 }
 
-int dq_impl(const void* q, const void* k, const void* v, const float* lse, const float* delta,
-            const void* dout, void* dq, int B, int T, int Hq, int Hkv, int D, float scale,
-            int causal, cudaStream_t st) {
+int dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
+            void* dq, int B, int T, int Hq, int Hkv, int D, float scale, int causal,
+            cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdo;
   int rc;
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mdo, dout, B, T, Hq, D, kTileM, "dout")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kDqTileN, "k")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kDqTileN, "v")) != DETATTN_OK) return rc;
-  BwdArgs a = bwd_args(lse, delta, T, Hq, Hkv, scale, causal);
+  BwdArgs a = bwd_args(workspace, T, Hq, Hkv, scale, causal);
   a.dq = dq;
   a.n_tiles = (T + kTileM - 1) / kTileM;
   a.BH = B * Hq;
   return launched(launch_dq(D, a.n_tiles * a.BH, mq, mk, mv, mdo, a, st), "attn_bwd_dq");
 }
 
-size_t delta_bytes(int B, int T, int Hq) {
-  const size_t n = static_cast<size_t>(B) * Hq * T * sizeof(float);
-  return (n + 255) & ~static_cast<size_t>(255);
+size_t rowstat_bytes(int B, int T, int Hq) {
+  return static_cast<size_t>(B) * Hq * padded_T(T) * sizeof(float2);
+}
+
+int check_workspace(const void* ws, size_t bytes, int B, int T, int Hq) {
+  if (ws == nullptr || bytes < rowstat_bytes(B, T, Hq))
+    return fail(DETATTN_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu%s",
+                rowstat_bytes(B, T, Hq), bytes, ws ? "" : " (NULL)");
+  if (!aligned16(ws)) return fail(DETATTN_ERR_ALIGN, "workspace is not 16-byte aligned");
+  return DETATTN_OK;
 }
 
 }  // namespace
@@ -229,49 +275,51 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
   bool empty = false;
   if (check_shape(B, T, Hq, Hkv, D, &empty) != DETATTN_OK || empty) return 0;
-  return delta_bytes(B, T, Hq);
+  return rowstat_bytes(B, T, Hq);
 }
 
-int attn_bwd_delta(const void* o, const void* dout, float* delta, int B, int T, int Hq, int D,
-                   void* stream) {
+int attn_bwd_delta(const void* o, const void* dout, const float* lse, void* workspace,
+                   size_t workspace_bytes, int B, int T, int Hq, int D, void* stream) {
   bool empty = false;
   int rc;
   if ((rc = check_shape(B, T, Hq, 1, D, &empty)) != DETATTN_OK) return rc;
   if (empty) return ok_status();
-  if ((rc = check_ptrs({{o, "o"}, {dout, "dout"}, {delta, "delta"}})) != DETATTN_OK) return rc;
+  if ((rc = check_ptrs({{o, "o"}, {dout, "dout"}, {lse, "lse"}})) != DETATTN_OK) return rc;
+  if ((rc = check_workspace(workspace, workspace_bytes, B, T, Hq)) != DETATTN_OK) return rc;
   if ((rc = check_device()) != DETATTN_OK) return rc;
-  return delta_impl(o, dout, delta, B, T, Hq, D, static_cast<cudaStream_t>(stream));
+  return delta_impl(o, dout, lse, workspace, B, T, Hq, D, static_cast<cudaStream_t>(stream));
 }
 
-int attn_bwd_dkdv(const void* q, const void* k, const void* v, const float* lse,
-                  const float* delta, const void* dout, void* dk, void* dv, int B, int T, int Hq,
-                  int Hkv, int D, float scale, int causal, void* stream) {
+int attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout,
+                  const void* workspace, size_t workspace_bytes, void* dk, void* dv, int B, int T,
+                  int Hq, int Hkv, int D, float scale, int causal, void* stream) {
   bool empty = false;
   int rc;
   if ((rc = check_shape(B, T, Hq, Hkv, D, &empty)) != DETATTN_OK) return rc;
   if ((rc = check_scale(scale, causal)) != DETATTN_OK) return rc;
   if (empty) return ok_status();
-  if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {lse, "lse"}, {delta, "delta"},
-                        {dout, "dout"}, {dk, "dk"}, {dv, "dv"}})) != DETATTN_OK)
+  if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {dout, "dout"}, {dk, "dk"}, {dv, "dv"}})) !=
+      DETATTN_OK)
     return rc;
+  if ((rc = check_workspace(workspace, workspace_bytes, B, T, Hq)) != DETATTN_OK) return rc;
   if ((rc = check_device()) != DETATTN_OK) return rc;
-  return dkdv_impl(q, k, v, lse, delta, dout, dk, dv, B, T, Hq, Hkv, D, scale, causal,
+  return dkdv_impl(q, k, v, dout, workspace, dk, dv, B, T, Hq, Hkv, D, scale, causal,
                    static_cast<cudaStream_t>(stream));
 }
 
-int attn_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
-                const float* delta, const void* dout, void* dq, int B, int T, int Hq, int Hkv,
-                int D, float scale, int causal, void* stream) {
+int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout,
+                const void* workspace, size_t workspace_bytes, void* dq, int B, int T, int Hq,
+                int Hkv, int D, float scale, int causal, void* stream) {
   bool empty = false;
   int rc;
   if ((rc = check_shape(B, T, Hq, Hkv, D, &empty)) != DETATTN_OK) return rc;
   if ((rc = check_scale(scale, causal)) != DETATTN_OK) return rc;
   if (empty) return ok_status();
-  if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {lse, "lse"}, {delta, "delta"},
-                        {dout, "dout"}, {dq, "dq"}})) != DETATTN_OK)
+  if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {dout, "dout"}, {dq, "dq"}})) != DETATTN_OK)
     return rc;
+  if ((rc = check_workspace(workspace, workspace_bytes, B, T, Hq)) != DETATTN_OK) return rc;
   if ((rc = check_device()) != DETATTN_OK) return rc;
-  return dq_impl(q, k, v, lse, delta, dout, dq, B, T, Hq, Hkv, D, scale, causal,
+  return dq_impl(q, k, v, dout, workspace, dq, B, T, Hq, Hkv, D, scale, causal,
                  static_cast<cudaStream_t>(stream));
 }
 
@@ -287,18 +335,14 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {dout, "dout"},
                         {dq, "dq"}, {dk, "dk"}, {dv, "dv"}})) != DETATTN_OK)
     return rc;
-  if (workspace == nullptr || workspace_bytes < delta_bytes(B, T, Hq))
-    return fail(DETATTN_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu%s",
-                delta_bytes(B, T, Hq), workspace_bytes, workspace ? "" : " (NULL)");
-  if (!aligned16(workspace)) return fail(DETATTN_ERR_ALIGN, "workspace is not 16-byte aligned");
+  if ((rc = check_workspace(workspace, workspace_bytes, B, T, Hq)) != DETATTN_OK) return rc;
   if ((rc = check_device()) != DETATTN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  float* delta = static_cast<float*>(workspace);
-  if ((rc = delta_impl(o, dout, delta, B, T, Hq, D, st)) != DETATTN_OK) return rc;
-  if ((rc = dkdv_impl(q, k, v, lse, delta, dout, dk, dv, B, T, Hq, Hkv, D, scale, causal, st)) !=
+  if ((rc = delta_impl(o, dout, lse, workspace, B, T, Hq, D, st)) != DETATTN_OK) return rc;
+  if ((rc = dkdv_impl(q, k, v, dout, workspace, dk, dv, B, T, Hq, Hkv, D, scale, causal, st)) !=
       DETATTN_OK)
     return rc;
-  return dq_impl(q, k, v, lse, delta, dout, dq, B, T, Hq, Hkv, D, scale, causal, st);
+  return dq_impl(q, k, v, dout, workspace, dq, B, T, Hq, Hkv, D, scale, causal, st);
 }
 
 int detattn_check_status(void* stream) {
@@ -310,6 +354,37 @@ int detattn_check_status(void* stream) {
   if (f | b)
     return fail(DETATTN_ERR_DEVICE_TIMEOUT,
                 "a kernel gave up on a pipeline wait (fwd flags %u, bwd flags %u)", f, b);
+  return ok_status();
+}
+
+int detattn_diag_exp2(const float* x, float* y_poly, float* y_pair, float* y_sfu, int n,
+                      void* stream) {
+  int rc;
+  if (n < 0) return fail(DETATTN_ERR_SHAPE, "n=%d", n);
+  if (n == 0) return ok_status();
+  if ((rc = check_ptrs({{x, "x"}, {y_poly, "y_poly"}, {y_pair, "y_pair"}, {y_sfu, "y_sfu"}})) !=
+      DETATTN_OK)
+    return rc;
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  return launched(launch_exp2_diag(x, y_poly, y_pair, y_sfu, n, static_cast<cudaStream_t>(stream)),
+                  "detattn_diag_exp2");
+}
+
+int detattn_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+  int rc;
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  if (limit_ns < 1000000ull) limit_ns = 1000000ull;
+  if (limit_ns > 10000000000ull) limit_ns = 10000000000ull;
+  return launched(launch_wait_timeout_selftest(limit_ns, static_cast<cudaStream_t>(stream)),
+                  "detattn_selftest_wait_timeout");
+}
+
+int detattn_set_dkdv_split(int blocks_per_key_tile) {
+  if (blocks_per_key_tile != 0 && blocks_per_key_tile != 1 && blocks_per_key_tile != 2 &&
+      blocks_per_key_tile != 4 && blocks_per_key_tile != 8)
+    return fail(DETATTN_ERR_SHAPE, "dK/dV split %d: must be 0 (automatic), 1, 2, 4 or 8",
+                blocks_per_key_tile);
+  g_dkdv_split = blocks_per_key_tile;
   return ok_status();
 }
 

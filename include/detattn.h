@@ -20,6 +20,7 @@
  *   k, v, dk, dv   : bf16 [B, T, Hkv, D]
  *   lse            : fp32 [B, Hq, T]   natural-log logsumexp of the scaled scores
  *   workspace      : caller-owned device scratch of attn_bwd_workspace_bytes()
+ *                    (row statistics of the backward; layout below)
  *
  * Conventions shared by every entry point:
  *   - Pointers are device pointers, 16-byte aligned.  The caller owns every
@@ -68,44 +69,83 @@ typedef enum {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
              int Hq, int Hkv, int D, float scale, int causal, void* stream);
 
-/* Bytes of device workspace attn_bwd needs (Delta, fp32 [B,Hq,T], rounded up
- * to 256 bytes).  Returns 0 for an empty or invalid shape. */
+/* Bytes of device workspace the backward needs: B * Hq * Tp * 8 with
+ * Tp = T rounded up to a multiple of 128.  Returns 0 for an empty or invalid
+ * shape.
+ *
+ * Workspace layout (written by attn_bwd_delta, read by attn_bwd_dkdv and
+ * attn_bwd_dq): row statistics, one (float, float) pair per (b, h, t),
+ * pairs ordered [b][h][t] with t < Tp:
+ *   pair.x = -LSE[b,h,t] * log2(e),   pair.y = -Delta[b,h,t]
+ *   Delta[b,h,t] = sum_d dout[b,t,h,d] * o[b,t,h,d]   (fp32, fixed order)
+ * and (-inf, -0) for t >= T.  Stored negated and in base 2 because the
+ * kernels add them: P = exp2(S*scale*log2(e) + pair.x), dS = P (dP + pair.y). */
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
 
 /* Backward.  Given q, k, v, the forward's o and lse, and dout, writes dq, dk,
  * dv (bf16).  Runs attn_bwd_delta, attn_bwd_dkdv and attn_bwd_dq in that
- * order on `stream`.  `workspace` (>= attn_bwd_workspace_bytes) holds Delta.
- * Passage: "Step 2: fused flash attention" and "Where the time goes now"
- * (the flash_attention_dkv kernel) on the RustingBrain page. */
+ * order on `stream`.  `workspace` (>= attn_bwd_workspace_bytes, 16-byte
+ * aligned, caller-owned, contents on entry irrelevant) holds the row
+ * statistics.  Passage: "Step 2: fused flash attention" and "Where the time
+ * goes now" (the flash_attention_dkv kernel) on the RustingBrain page. */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dout, void* dq, void* dk, void* dv, void* workspace,
              size_t workspace_bytes, int B, int T, int Hq, int Hkv, int D, float scale,
              int causal, void* stream);
 
-/* Backward step 1 alone: delta [B,Hq,T] fp32 = rowsum(dout * o), summed in a
- * fixed order.  (Implied by recomputing P from the logsumexp in "Step 1" of
- * the RustingBrain page.) */
-int attn_bwd_delta(const void* o, const void* dout, float* delta, int B, int T, int Hq, int D,
-                   void* stream);
+/* Backward step 1 alone: writes the workspace row statistics (layout above)
+ * from o, dout and lse; Delta is the rowsum of dout * o summed in a fixed
+ * order.  (Implied by recomputing P from the logsumexp, "Step 1" of the
+ * RustingBrain page.) */
+int attn_bwd_delta(const void* o, const void* dout, const float* lse, void* workspace,
+                   size_t workspace_bytes, int B, int T, int Hq, int D, void* stream);
 
-/* Backward step 2 alone: dk, dv for every KV tile, summing the query heads of
- * the GQA group inside the tile in ascending head order ("Where the time goes
- * now": flash_attention_dkv).  `delta` is the output of attn_bwd_delta. */
-int attn_bwd_dkdv(const void* q, const void* k, const void* v, const float* lse,
-                  const float* delta, const void* dout, void* dk, void* dv, int B, int T, int Hq,
-                  int Hkv, int D, float scale, int causal, void* stream);
+/* Backward step 2 alone: dk, dv for every 128-key tile, summing the query
+ * heads of the GQA group inside the tile in ascending head order ("Where the
+ * time goes now": flash_attention_dkv).  `workspace` holds the row statistics
+ * of attn_bwd_delta. */
+int attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout,
+                  const void* workspace, size_t workspace_bytes, void* dk, void* dv, int B, int T,
+                  int Hq, int Hkv, int D, float scale, int causal, void* stream);
 
-/* Backward step 3 alone: dq, reduced over KV tiles in ascending order by the
- * single block that owns the query tile (no atomics). */
-int attn_bwd_dq(const void* q, const void* k, const void* v, const float* lse,
-                const float* delta, const void* dout, void* dq, int B, int T, int Hq, int Hkv,
-                int D, float scale, int causal, void* stream);
+/* Backward step 3 alone: dq, reduced over key tiles in ascending order by the
+ * single block that owns the 128-query tile (no atomics). */
+int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout,
+                const void* workspace, size_t workspace_bytes, void* dq, int B, int T, int Hq,
+                int Hkv, int D, float scale, int causal, void* stream);
 
 /* Synchronises `stream`, then reads and clears the device-side status word
  * that kernels set when a pipeline wait runs out (a bounded wait, default
  * limit 1 s).  Returns DETATTN_OK, DETATTN_ERR_DEVICE_TIMEOUT or
  * DETATTN_ERR_CUDA. */
 int detattn_check_status(void* stream);
+
+/* Diagnostic for accuracy tests: evaluates on n device floats x the three
+ * ways the kernels form 2^x -- the FMA-pipe polynomial (Cody-Waite range
+ * reduction plus a fitted cubic, max relative error 7.5e-5, inputs clamped at
+ * -126), the same polynomial in its paired f32x2 form, and the special-function
+ * unit's ex2.approx -- into y_poly, y_pair and y_sfu.  Not tied to a passage
+ * of the method. */
+int detattn_diag_exp2(const float* x, float* y_poly, float* y_pair, float* y_sfu, int n,
+                      void* stream);
+
+/* Failure-detection self-test.  Launches a one-thread kernel on `stream`
+ * that waits, with the same bounded wait the attention kernels use, on a
+ * barrier nothing ever completes; after `limit_ns` (clamped to [1 ms, 10 s])
+ * it gives up, records a timeout in the device status word and returns, so
+ * the context stays usable.  A following detattn_check_status() returns
+ * DETATTN_ERR_DEVICE_TIMEOUT (and clears the word).  Not tied to a passage of
+ * the method: it exists to test the timeout path without faulting a GPU. */
+int detattn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+/* Tuning knob: number of thread blocks that share one 128-key tile in the
+ * dK/dV step (1, 2, 4 or 8; 0 = automatic, the default).  The blocks split
+ * the tile's (query head, query tile) items into contiguous chunks and add
+ * their partial sums in a fixed order, so results stay bitwise reproducible
+ * for a given setting; different settings round differently.  Automatic
+ * picks from the shape and the SM count only.  Host-side, per process.
+ * Returns DETATTN_OK or DETATTN_ERR_SHAPE for another value. */
+int detattn_set_dkdv_split(int blocks_per_key_tile);
 
 /* Sets the per-wait time limit used by kernels launched afterwards, in
  * nanoseconds (clamped to [1 ms, 60 s]).  Host-side setting, per process. */

@@ -24,6 +24,14 @@ def test_exports_every_declared_symbol(L):
         assert hasattr(L, n), n
 
 
+def test_dkdv_split_knob_validates(L):
+    for ok in (0, 1, 2, 4, 8):
+        assert L.detattn_set_dkdv_split(ok) == 0
+    for bad in (-1, 3, 16):
+        assert L.detattn_set_dkdv_split(bad) == -3
+    assert L.detattn_set_dkdv_split(0) == 0
+
+
 def test_version(L):
     assert L.detattn_version() == 10000
 
@@ -55,8 +63,9 @@ def test_empty_problem_is_ok_without_device(L):
 
 
 def test_workspace_bytes(L):
-    assert L.attn_bwd_workspace_bytes(4, 1024, 12, 4, 64) == 4 * 12 * 1024 * 4
-    assert L.attn_bwd_workspace_bytes(1, 3, 1, 1, 64) == 256
+    assert L.attn_bwd_workspace_bytes(4, 1024, 12, 4, 64) == 4 * 12 * 1024 * 8
+    assert L.attn_bwd_workspace_bytes(1, 3, 1, 1, 64) == 128 * 8
+    assert L.attn_bwd_workspace_bytes(2, 129, 3, 1, 128) == 2 * 3 * 256 * 8
     assert L.attn_bwd_workspace_bytes(1, 3, 3, 2, 64) == 0
     assert L.attn_bwd_workspace_bytes(0, 3, 2, 1, 64) == 0
 
@@ -75,9 +84,12 @@ def test_bwd_rejects(L):
     assert call(ws=BAD) == -2
     assert call(D=80) == -4
     assert call(Hq=5, Hkv=2) == -3
-    assert L.attn_bwd_dq(P, P, P, P, P, P, None, 1, 128, 2, 1, 64, 0.125, 1, None) == -1
-    assert L.attn_bwd_dkdv(P, P, P, P, P, P, P, BAD, 1, 128, 2, 1, 64, 0.125, 1, None) == -2
-    assert L.attn_bwd_delta(P, P, None, 1, 128, 2, 64, None) == -1
+    assert L.attn_bwd_dq(P, P, P, P, P, 1 << 20, None, 1, 128, 2, 1, 64, 0.125, 1, None) == -1
+    assert L.attn_bwd_dq(P, P, P, P, P, 100, P, 1, 128, 2, 1, 64, 0.125, 1, None) == -9
+    assert L.attn_bwd_dkdv(P, P, P, P, P, 1 << 20, P, BAD, 1, 128, 2, 1, 64, 0.125, 1, None) == -2
+    assert L.attn_bwd_dkdv(P, P, P, P, None, 1 << 20, P, P, 1, 128, 2, 1, 64, 0.125, 1, None) == -9
+    assert L.attn_bwd_delta(P, P, None, P, 1 << 20, 1, 128, 2, 64, None) == -1
+    assert L.attn_bwd_delta(P, P, P, BAD, 1 << 20, 1, 128, 2, 64, None) == -2
 
 
 def test_python_binding_refuses_cpu_tensors(L):

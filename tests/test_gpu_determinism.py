@@ -118,3 +118,19 @@ def test_empty_problem_launches_nothing():
     dq, dk, dv = da.attn_bwd(q, k, k, o, lse, q)
     assert dq.shape == q.shape
     da.check_status()
+
+
+def test_device_wait_timeout_is_reported_and_context_survives():
+    """A bounded device wait that can never complete gives up, the host reads
+    DETATTN_ERR_DEVICE_TIMEOUT, and the next attention call still works."""
+    da.check_status()  # clean slate
+    da.selftest_wait_timeout(50_000_000)  # 50 ms
+    with pytest.raises(da.DetAttnError) as e:
+        da.check_status()
+    assert e.value.code == -7
+    da.check_status()  # the word was cleared
+    q, k, v, do = (t.cuda() for t in make_inputs(1, 256, 2, 1, 64, seed=3))
+    o, lse = da.attn_fwd(q, k, v)
+    torch.cuda.synchronize()
+    da.check_status()
+    assert torch.isfinite(o.float()).all()

@@ -114,15 +114,23 @@ def test_long_context_sampled():
 
 
 def test_delta_step_alone():
-    """The backward's first step on seeded (O, dO): fp32 sums vs fp64."""
+    """The backward's first step on seeded (O, dO, LSE): -Delta as fp32 sums
+    against the fp64 rowsum, -LSE*log2(e) copied exactly, padding (-inf, -0)."""
     import deterministic_attention_gb300 as da
-    for (B, T, H, D) in [(2, 333, 5, 64), (1, 129, 3, 128)]:
-        o, _, _, do = make_inputs(B, T, H, H, D, seed=T)
-        o = o  # seeded bf16 tensor standing in for a forward output
-        d = da.attn_bwd_delta(o.cuda(), do.cuda())
+    for (B, T, H, D) in [(2, 333, 5, 64), (1, 129, 3, 128), (1, 1, 2, 64)]:
+        o, _, _, do = make_inputs(B, T, H, H, D, seed=T)  # o: seeded bf16 standing in for O
+        lse = torch.randn((B, H, T), generator=torch.Generator().manual_seed(T)) * 3 + 5
+        ws = da.new_workspace(B, T, H, H, D)
+        da.attn_bwd_delta(o.cuda(), do.cuda(), lse.cuda(), ws)
         torch.cuda.synchronize()
+        rs = da.rowstats_view(ws, B, T, H).cpu()
         ref = oracle.rowdot(widen(o), widen(do))
-        assert rel_l2(to_np(d.cpu()), ref) <= 1e-5
+        assert rel_l2(-to_np(rs[:, :, :T, 1]), ref) <= 1e-5
+        assert torch.equal(rs[:, :, :T, 0], -(lse * 1.4426950408889634).to(torch.float32)) or \
+            float((rs[:, :, :T, 0] + lse * 1.4426950408889634).abs().max()) <= 1e-5
+        if rs.shape[2] > T:
+            assert bool(torch.isneginf(rs[:, :, T:, 0]).all())
+            assert bool((rs[:, :, T:, 1] == 0).all())
 
 
 def test_causality_exact_on_gpu():
@@ -137,3 +145,44 @@ def test_causality_exact_on_gpu():
         o2, lse2, *_ = run_gpu(q, k2, v2, do, 0.125, True)
         assert torch.equal(o1[:, : i0 + 1], o2[:, : i0 + 1])
         assert torch.equal(lse1[:, :, : i0 + 1], lse2[:, :, : i0 + 1])
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("B,T,Hq,Hkv,D,causal", [(2, 520, 6, 2, 64, True), (1, 300, 4, 1, 128, True),
+                                                 (1, 256, 4, 4, 64, False)])
+def test_dkdv_split_sizes(split, B, T, Hq, Hkv, D, causal):
+    """Every dK/dV split (blocks per key tile, partial sums added in rank
+    order through distributed shared memory) matches the oracle and repeats
+    bit for bit."""
+    import deterministic_attention_gb300 as da
+    q, k, v, do = make_inputs(B, T, Hq, Hkv, D, seed=split * 100 + T, dout_std=0.2)
+    da.set_dkdv_split(split)
+    try:
+        o, lse, dq, dk, dv = run_gpu(q, k, v, do, 1.0 / math.sqrt(D), causal)
+        _, _, _, dk2, dv2 = run_gpu(q, k, v, do, 1.0 / math.sqrt(D), causal)
+    finally:
+        da.set_dkdv_split(0)
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    qf, kf, vf, dof = (widen(t) for t in (q, k, v, do))
+    _, dk_r, dv_r, _, _ = oracle.attn_bwd(qf, kf, vf, dof, 1.0 / math.sqrt(D), causal)
+    assert_bwd_close([("dK", to_np(dk), dk_r), ("dV", to_np(dv), dv_r)], f"split {split}")
+
+
+def test_fma_pipe_exp2_error_bound():
+    """The polynomial 2^x used for part of the exponentials: relative error
+    <= 1e-4 against exact 2^x over the range the kernels feed it, the pair
+    form bit-identical to the scalar form, and agreement with the
+    special-function unit's ex2.approx to the same bound."""
+    import numpy as np
+    import deterministic_attention_gb300 as da
+    xs = np.concatenate([np.linspace(-126.0, 8.0, 200001), np.array([-300.0, -126.5, -0.5, 0.5])])
+    x = torch.tensor(xs, dtype=torch.float32, device="cuda")
+    yp, y2, ys = (t.cpu().double().numpy() for t in da.diag_exp2(x))
+    xf = x.cpu().double().numpy()
+    assert np.array_equal(yp, y2)
+    assert np.all(yp > 0)
+    normal = xf >= -125.0  # below, the clamp at -126 leaves values under 2^-124
+    assert np.max(np.abs(yp[normal] / np.exp2(xf[normal]) - 1.0)) <= 1e-4
+    assert np.all(yp[~normal] <= 2.0 ** -124)
+    live = xf > -120.0
+    assert np.max(np.abs(yp[live] / ys[live] - 1.0)) <= 1e-4
