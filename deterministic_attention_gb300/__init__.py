@@ -56,6 +56,8 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd_workspace_bytes.argtypes = [i, i, i, i, i]
     L.attn_bwd_workspace_bytes.restype = sz
     L.attn_bwd.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
+    L.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    L.attn_bwd_noalloc.restype = i
     L.attn_bwd_delta.argtypes = [vp, vp, fp, vp, sz, i, i, i, i, vp]
     L.attn_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, sz, vp, vp, i, i, i, i, i, f, i, vp]
     L.attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, sz, vp, i, i, i, i, i, f, i, vp]

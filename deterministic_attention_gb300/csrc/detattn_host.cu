@@ -254,6 +254,36 @@ int check_workspace(const void* ws, size_t bytes, int B, int T, int Hq) {
   return DETATTN_OK;
 }
 
+// ------------------------------------------------------------ built-in scratch
+// Row statistics for attn_bwd_noalloc: a file-scope device array, so callers
+// that cannot allocate device memory still get the backward.  Every GPU that
+// loads this library holds it (8 MiB) until the process exits.  In host code
+// the name is only a host-side stand-in; its device address comes from
+// cudaGetSymbolAddress, looked up once per device with that device current.
+constexpr size_t kNoallocMaxPairs = size_t(1) << 20;
+static __device__ __align__(256) float2 g_noalloc_rowstats[kNoallocMaxPairs];
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  static void* cached[64] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 64 && cached[dev] != nullptr) {
+    *out = cached[dev];
+    return DETATTN_OK;
+  }
+  void* ptr = nullptr;
+  e = cudaGetSymbolAddress(&ptr, g_noalloc_rowstats);
+  if (e != cudaSuccess || ptr == nullptr)
+    return fail(DETATTN_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch: %s",
+                cudaGetErrorString(e));
+  if (dev < 64) cached[dev] = ptr;
+  *out = ptr;
+  return DETATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -343,6 +373,34 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
       DETATTN_OK)
     return rc;
   return dq_impl(q, k, v, dout, workspace, dq, B, T, Hq, Hkv, D, scale, causal, st);
+}
+
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, int B, int T, int Hq,
+                     int Hkv, int D, float scale, int causal, void* stream) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, Hkv, D, &empty)) != DETATTN_OK) return rc;
+  if ((rc = check_scale(scale, causal)) != DETATTN_OK) return rc;
+  if (empty) return ok_status();
+  const size_t pairs = static_cast<size_t>(B) * Hq * padded_T(T);
+  if (pairs > kNoallocMaxPairs)
+    return fail(DETATTN_ERR_WORKSPACE,
+                "attn_bwd_noalloc: B*Hq*Tp = %zu row-statistic pairs (Tp = T rounded up to 128) "
+                "exceeds the built-in scratch of %zu pairs; use attn_bwd with a workspace",
+                pairs, kNoallocMaxPairs);
+  if ((rc = check_ptrs({{q, "q"}, {k, "k"}, {v, "v"}, {o, "o"}, {lse, "lse"}, {dout, "dout"},
+                        {dq, "dq"}, {dk, "dk"}, {dv, "dv"}})) != DETATTN_OK)
+    return rc;
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  void* ws = nullptr;
+  if ((rc = noalloc_scratch(&ws)) != DETATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, st)) != DETATTN_OK) return rc;
+  if ((rc = dkdv_impl(q, k, v, dout, ws, dk, dv, B, T, Hq, Hkv, D, scale, causal, st)) !=
+      DETATTN_OK)
+    return rc;
+  return dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, st);
 }
 
 int detattn_check_status(void* stream) {

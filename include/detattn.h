@@ -93,6 +93,29 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              size_t workspace_bytes, int B, int T, int Hq, int Hkv, int D, float scale,
              int causal, void* stream);
 
+/* Backward without a caller workspace, for callers that cannot allocate
+ * device memory: for example a plug-in whose host application gives it no
+ * allocator, or code inside a framework whose device memory is all owned by
+ * its own pooled allocator, where a stray cudaMalloc can fail or fragment the
+ * pool.  Same arguments, results and errors as attn_bwd minus the workspace.
+ * The method has no counterpart of this on the pages; it is an interface
+ * convenience.
+ *
+ * The row statistics live in an 8 MiB array built into the library (every
+ * GPU that loads the library holds it until the process exits), so
+ * B * Hq * Tp must not exceed 1,048,576 (Tp = T rounded up to 128); larger
+ * problems return DETATTN_ERR_WORKSPACE without launching anything.  This
+ * call never allocates memory.  Its first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call shares the one
+ * array: each call overwrites all the statistics it reads before reading
+ * them, so nothing needs to start at zero, but calls that overlap on the GPU
+ * (on different streams, or different host threads without ordering) race
+ * on it and must not be issued. */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                     const void* dout, void* dq, void* dk, void* dv, int B, int T, int Hq,
+                     int Hkv, int D, float scale, int causal, void* stream);
+
 /* Backward step 1 alone: writes the workspace row statistics (layout above)
  * from o, dout and lse; Delta is the rowsum of dout * o summed in a fixed
  * order.  (Implied by recomputing P from the logsumexp, "Step 1" of the
