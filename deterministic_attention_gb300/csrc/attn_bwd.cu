@@ -34,11 +34,11 @@ __device__ unsigned int g_bwd_status;
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA issuer, 8 compute warps
 // Of every 8 consecutive pairs of probabilities, this many take 2^x from the
 // FMA-pipe polynomial instead of the special-function unit.
 #ifndef DETATTN_BWD_POLY_OF8
-#define DETATTN_BWD_POLY_OF8 2
+#define DETATTN_BWD_POLY_OF8 0
 #endif
 constexpr int kPolyOf8 = DETATTN_BWD_POLY_OF8;
 
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       mbar_init(bar(kDkvBarQEmpty + s), 1);
     }
     mbar_init(bar(kDkvBarS), 1);
-    mbar_init(bar(kDkvBarP), 4);
+    mbar_init(bar(kDkvBarP), 8);
     mbar_init(bar(kDkvBarAcc), 1);
     mbar_init(bar(kDkvBarDrain), 1);
     fence_barrier_init();
@@ -282,11 +282,14 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         if (!(ok = mbar_wait(bar(kDkvBarP), li & 1, wait_ns))) break;
         tc_fence_after();
         // Accumulate over the 64 queries of this tile, 16 at a time.
+        // P^T / dS^T of queries 16ks..16ks+15: half ks/2 wrote its 32 queries as
+        // 16 packed columns at the start of its own 32 S^T / dP^T columns.
 #pragma unroll
         for (int ks = 0; ks < kDkvTileM / 16; ++ks) {
           const uint32_t acc = (li > 0 || ks > 0) ? 1u : 0u;
-          mma_ts(tDV, tS + ks * 8, sdesc_sw128(sdO + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
-          mma_ts(tDK, tDP + ks * 8, sdesc_sw128(sQ + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
+          const uint32_t pc = (ks >> 1) * 32 + (ks & 1) * 8;
+          mma_ts(tDV, tS + pc, sdesc_sw128(sdO + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
+          mma_ts(tDK, tDP + pc, sdesc_sw128(sQ + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
         }
         mma_commit(bar(kDkvBarQEmpty + s));
       }
@@ -296,42 +299,43 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     }
   } else {
     // ------------------------------------------------------------ P^T / dS^T warps
+    // Eight warps: warps w and w+4 share TMEM lane quarter (w & 3), i.e. the
+    // same 32 key rows; half 0 takes query columns 0..31 of the tile, half 1
+    // columns 32..63.  Each half writes its P^T / dS^T (bf16 pairs) over the
+    // first 16 of its own 32 S^T / dP^T columns.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int krow = n0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tS = tl + Cf::kColS + half * 32, tDP = tl + Cf::kColDP + half * 32;
     const float sl2 = a.scale_log2;
     for (int li = 0; li < n_it; ++li) {
       const int it = it_lo + li;
       const int s = li % NS;
-      const int i0 = (m_begin + it % per_head) * kDkvTileM;
+      const int i0 = (m_begin + it % per_head) * kDkvTileM + half * 32;  // this half's first query
       ok = warp_all(mbar_wait(bar(kDkvBarS), li & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sv[2][32], dp[2][32];
-      tmem_ld32_nowait(tl + Cf::kColS, sv[0]);
-      tmem_ld32_nowait(tl + Cf::kColS + 32, sv[1]);
-      tmem_ld32_nowait(tl + Cf::kColDP, dp[0]);
-      tmem_ld32_nowait(tl + Cf::kColDP + 32, dp[1]);
+      uint32_t sv[32], dp[32];
+      tmem_ld32_nowait(tS, sv);
+      tmem_ld32_nowait(tDP, dp);
       tmem_wait_ld();
-      reg_fence32(sv[0]);
-      reg_fence32(sv[1]);
-      reg_fence32(dp[0]);
-      reg_fence32(dp[1]);
-      const float* rows = stage_rows(s);
+      reg_fence32(sv);
+      reg_fence32(dp);
       // Causal: query i0 + c sees key krow iff c >= krow - i0.
       const int cmin = a.causal ? (krow - i0) : -1;
-      uint32_t pk[32], dk[32];
-      const uint64_t sl2x2 = f2_make(sl2, sl2);
-      const float4* st4 = reinterpret_cast<const float4*>(rows);  // 2 positions per float4
       const bool need_mask = cmin > 0;
+      uint32_t pk[16], dk[16];
+      const uint64_t sl2x2 = f2_make(sl2, sl2);
+      // (-lse2, -delta) of this half's 32 queries, two per float4.
+      const float4* st4 = reinterpret_cast<const float4*>(stage_rows(s)) + half * 16;
 #pragma unroll
-      for (int c2 = 0; c2 < 32; ++c2) {
+      for (int c2 = 0; c2 < 16; ++c2) {
         const int c = 2 * c2;
         const float4 rs = st4[c2];  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
-        const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c >> 5][c & 31]),
-                                          __uint_as_float(sv[c >> 5][(c + 1) & 31])), sl2x2,
-                                  f2_make(rs.x, rs.z));
+        const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                  sl2x2, f2_make(rs.x, rs.z));
         float x0, x1, p0, p1;
         f2_split(x, x0, x1);
         if ((c2 & 7) < kPolyOf8) {
@@ -344,16 +348,15 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
           if (c < cmin) p0 = 0.f;
           if (c + 1 < cmin) p1 = 0.f;
         }
-        const uint64_t dpm = f2_add(f2_make(__uint_as_float(dp[c >> 5][c & 31]),
-                                            __uint_as_float(dp[c >> 5][(c + 1) & 31])),
+        const uint64_t dpm = f2_add(f2_make(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
                                     f2_make(rs.y, rs.w));
         float d0, d1;
         f2_split(f2_mul(f2_make(p0, p1), dpm), d0, d1);
         pk[c2] = pack_bf16x2(p0, p1);
         dk[c2] = pack_bf16x2(d0, d1);
       }
-      tmem_st32_nowait(tl + Cf::kColS, pk);
-      tmem_st32_nowait(tl + Cf::kColDP, dk);
+      tmem_st16_nowait(tS, pk);
+      tmem_st16_nowait(tDP, dk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -369,7 +372,8 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? Cf::kColDV : Cf::kColDK;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int c = half * (D / 64) + cc;  // this half's 32-column chunks
           uint32_t v[32];
           if (n_it > 0) {
             tmem_ld32(tl + col + c * 32, v);
@@ -399,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         const float mul = which == 0 ? 1.f : a.scale;
         __nv_bfloat16* dst_row = which == 0 ? dvrow : dkrow;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int c = half * (D / 64) + cc;
           uint32_t v[32];
           tmem_ld32(tl + col + c * 32, v);
           uint32_t pkd[16];
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       const int R = kTileN / C;
       constexpr int kCpr = 2 * D / 8;  // 8-float output chunks per row ([dV | dK])
       const int ct = static_cast<int>(threadIdx.x) - 64;
-      for (int e = ct; e < R * kCpr; e += 128) {
+      for (int e = ct; e < R * kCpr; e += 256) {
         const int rl = e / kCpr, oc = e % kCpr;
         const int row = crank * R + rl;
         float acc[8];
@@ -534,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(bar(kDqBarVEmpty + s), 1);
     }
     mbar_init(bar(kDqBarS), 1);
-    mbar_init(bar(kDqBarDS), 4);
+    mbar_init(bar(kDqBarDS), 8);
     mbar_init(bar(kDqBarAcc), 1);
     mbar_init(bar(kDqBarDrain), 1);
     fence_barrier_init();
@@ -615,9 +620,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         mma_commit(bar(kDqBarVEmpty + s));
         if (!(ok = mbar_wait(bar(kDqBarDS), j & 1, wait_ns))) break;
         tc_fence_after();
+        // dS of keys 16ks..16ks+15: half ks/2 wrote its 32 keys as 16 packed
+        // columns at the start of its own 32 S columns.
 #pragma unroll
         for (int ks = 0; ks < kDqTileN / 16; ++ks)
-          mma_ts(tDQ, tS + ks * 8, sdesc_sw128(sK + ks * 2048, kDqTileN * 128, 1024), kIdDQ,
+          mma_ts(tDQ, tS + (ks >> 1) * 32 + (ks & 1) * 8,
+                 sdesc_sw128(sK + ks * 2048, kDqTileN * 128, 1024), kIdDQ,
                  (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(bar(kDqBarKEmpty + s));
       }
@@ -626,10 +634,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_wait(bar(kDqBarDrain), 0, wait_ns);
     }
   } else {
+    // Eight warps: warps w and w+4 share TMEM lane quarter (w & 3), i.e. the
+    // same 32 query rows; half 0 takes key columns 0..31 of the tile, half 1
+    // columns 32..63.  Each half writes its dS (bf16 pairs) over the first 16
+    // of its own 32 S columns.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int qrow = m0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tS = tl + C::kColS + half * 32, tDP = tl + C::kColDP + half * 32;
     const float sl2 = a.scale_log2;
     // (-LSE*log2e, -Delta) of this row; rows past T read (-inf, -0): P = 0.
     const float2 rstat = a.rowstats[(static_cast<size_t>(b) * a.Hq + h) * a.Tp + qrow];
@@ -637,28 +651,24 @@ __global__ void __launch_bounds__(kThreads, 2)
       ok = warp_all(mbar_wait(bar(kDqBarS), j & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sv[2][32], dp[2][32];
-      tmem_ld32_nowait(tl + C::kColS, sv[0]);
-      tmem_ld32_nowait(tl + C::kColS + 32, sv[1]);
-      tmem_ld32_nowait(tl + C::kColDP, dp[0]);
-      tmem_ld32_nowait(tl + C::kColDP + 32, dp[1]);
+      uint32_t sv[32], dp[32];
+      tmem_ld32_nowait(tS, sv);
+      tmem_ld32_nowait(tDP, dp);
       tmem_wait_ld();
-      reg_fence32(sv[0]);
-      reg_fence32(sv[1]);
-      reg_fence32(dp[0]);
-      reg_fence32(dp[1]);
-      const int kv0 = j * kDqTileN;
+      reg_fence32(sv);
+      reg_fence32(dp);
+      const int kv0 = j * kDqTileN + half * 32;  // key of this half's first column
       // key kv0 + c visible iff c <= lim
       const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
-      uint32_t dsk[32];
+      uint32_t dsk[16];
       const uint64_t sl2x2 = f2_make(sl2, sl2), neg_l = f2_make(rstat.x, rstat.x);
       const uint64_t neg_d = f2_make(rstat.y, rstat.y);
-      const bool need_mask = a.causal ? (kv0 + kDqTileN - 1 > m0) : (kv0 + kDqTileN > a.T);
+      const bool need_mask = a.causal ? (kv0 + 31 > m0) : (kv0 + 32 > a.T);
 #pragma unroll
-      for (int c2 = 0; c2 < 32; ++c2) {
+      for (int c2 = 0; c2 < 16; ++c2) {
         const int c = 2 * c2;
-        const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c >> 5][c & 31]),
-                                          __uint_as_float(sv[c >> 5][(c + 1) & 31])), sl2x2, neg_l);
+        const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
+                                  sl2x2, neg_l);
         float x0, x1, p0, p1;
         f2_split(x, x0, x1);
         if ((c2 & 7) < kPolyOf8) {
@@ -671,13 +681,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (c > lim) p0 = 0.f;
           if (c + 1 > lim) p1 = 0.f;
         }
-        const uint64_t dpm = f2_add(f2_make(__uint_as_float(dp[c >> 5][c & 31]),
-                                            __uint_as_float(dp[c >> 5][(c + 1) & 31])), neg_d);
+        const uint64_t dpm = f2_add(f2_make(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
+                                    neg_d);
         float d0, d1;
         f2_split(f2_mul(f2_make(p0, p1), dpm), d0, d1);
         dsk[c2] = pack_bf16x2(d0, d1);
       }
-      tmem_st32_nowait(tl + C::kColS, dsk);
+      tmem_st16_nowait(tS, dsk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -690,7 +700,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       __nv_bfloat16* dqrow = static_cast<__nv_bfloat16*>(a.dq) +
                              ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = half * (D / 64) + cc;  // this half's 32-column chunks of dQ
         uint32_t v[32];
         tmem_ld32(tl + C::kColDQ + c * 32, v);
         uint32_t pkd[16];

@@ -32,7 +32,7 @@ __device__ unsigned int g_fwd_status;
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
 // The row maximum used in the exponent is only moved when the true maximum
 // exceeds it by more than 2^8; until then P <= 256, which bf16 and the fp32
 // accumulators hold exactly as well.  The final O / l and LSE are exact for
@@ -41,7 +41,7 @@ constexpr float kRescaleLog2 = 8.0f;
 // Of every 8 consecutive pairs of scores, this many take 2^x from the FMA-pipe
 // polynomial instead of the special-function unit, to balance the two.
 #ifndef DETATTN_FWD_POLY_OF8
-#define DETATTN_FWD_POLY_OF8 2
+#define DETATTN_FWD_POLY_OF8 0
 #endif
 constexpr int kPolyOf8 = DETATTN_FWD_POLY_OF8;
 
@@ -55,7 +55,8 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 256;
-  static constexpr uint32_t kColS = 0;    // S (fp32, 128 cols); P (bf16 pairs) over cols 0..63
+  static constexpr uint32_t kColS = 0;    // S (fp32, 128 cols); P (bf16 pairs) of keys
+                                          // 64h..64h+63 over cols 64h..64h+31
   static constexpr uint32_t kColO = 128;  // O accumulator, D cols
 };
 
@@ -63,6 +64,10 @@ enum : int { kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKEmpty = 5, kBarVEmpty
              kBarS = 9, kBarP = 10, kBarO = 11, kBarDrain = 12, kNumBars = 13 };
 
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -73,6 +78,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_slot;
+  __shared__ float red_max[2][2][kTileM];  // [tile parity][half][row] partial maxima
+  __shared__ float red_l[2][kTileM];       // [half][row] partial row sums
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Heaviest query tiles (most key tiles under the causal mask) are handed out first.
@@ -104,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(bar(kBarVEmpty + s), 1);
     }
     mbar_init(bar(kBarS), 1);
-    mbar_init(bar(kBarP), 4);
+    mbar_init(bar(kBarP), 8);
     mbar_init(bar(kBarO), 1);
     mbar_init(bar(kBarDrain), 1);
     fence_barrier_init();
@@ -177,10 +184,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!(ok = mbar_wait(bar(kBarP), j & 1, wait_ns))) break;
         if (!(ok = mbar_wait(bar(kBarVFull + s), ph, wait_ns))) break;
         tc_fence_after();
+        // P of keys 16ks..16ks+15: half ks/4 wrote its 64 keys as 32 packed
+        // columns at the start of its own 64 S columns.
 #pragma unroll
         for (int ks = 0; ks < kTileN / 16; ++ks)
-          mma_ts(tO, tS + ks * 8, sdesc_sw128(sV + ks * 2048, 16384, 1024), kIdPV,
-                 (j > 0 || ks > 0) ? 1u : 0u);
+          mma_ts(tO, tS + (ks >> 2) * 64 + (ks & 3) * 8, sdesc_sw128(sV + ks * 2048, 16384, 1024),
+                 kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(bar(kBarVEmpty + s));
         mma_commit(bar(kBarO));
       }
@@ -190,36 +199,50 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
   } else {
     // ------------------------------------------------------------ softmax warps
+    // Eight warps: warps w and w+4 share TMEM lane quarter (w & 3), i.e. the
+    // same 32 query rows; "half" 0 takes key columns 0..63, half 1 64..127.
+    // The two halves of a row trade their partial row maxima through shared
+    // memory (one 64-thread named barrier per tile); the row sums stay split
+    // until the epilogue.  Each half writes its P over its own S columns, so
+    // the halves never touch each other's TMEM columns.
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int qrow = m0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t tS = tl + C::kColS + half * 64;  // this half's 64 score columns
     const float sl2 = a.scale_log2;
+    const uint32_t pair_bar = 1 + quarter;          // named barrier of the two halves
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < n_kv; ++j) {
       ok = warp_all(mbar_wait(bar(kBarS), j & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tl + C::kColS + c * 32, sr[c]);
+      uint32_t sr[2][32];
+      tmem_ld32_nowait(tS, sr[0]);
+      tmem_ld32_nowait(tS + 32, sr[1]);
       tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence32(sr[c]);
+      reg_fence32(sr[0]);
+      reg_fence32(sr[1]);
 
-      const int kv0 = j * kTileN;
-      const bool need_mask = a.causal ? (j == n_kv - 1) : (kv0 + kTileN > a.T);
+      const int kv0 = j * kTileN + half * 64;  // key of this half's first column
+      const bool need_mask = a.causal ? (j == n_kv - 1) : (j * kTileN + kTileN > a.T);
+      const int lim = need_mask ? (a.causal ? (qrow - kv0) : (a.T - 1 - kv0)) : (1 << 30);
       if (need_mask) {
-        const int lim = a.causal ? (qrow - kv0) : (a.T - 1 - kv0);  // key columns c <= lim visible
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // Partial maximum over 64 columns in four independent chains.
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 64; ++c)
-        mx = fmax3(mx, __uint_as_float(sr[c >> 4][(2 * c) & 31]),
-                   __uint_as_float(sr[c >> 4][(2 * c + 1) & 31]));
+      for (int c = 0; c < 32; ++c)
+        mx4[c & 3] = fmax3(mx4[c & 3], __uint_as_float(sr[c >> 4][(2 * c) & 31]),
+                           __uint_as_float(sr[c >> 4][(2 * c + 1) & 31]));
+      const float mx_half = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      red_max[j & 1][half][r] = mx_half;
+      named_barrier_sync(pair_bar, 64);
+      const float mx = fmaxf(red_max[j & 1][0][r], red_max[j & 1][1][r]);
       const float m_new = mx * sl2;
       float alpha = 1.f;
       bool moved = false;
@@ -229,17 +252,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         moved = true;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      const int lim = need_mask ? (a.causal ? (qrow - kv0) : (a.T - 1 - kv0)) : 1 << 30;
       const uint64_t sl2x2 = f2_make(sl2, sl2), neg_m = f2_make(-m_use, -m_use);
-      uint64_t sum2 = f2_make(0.f, 0.f);  // two running partial row sums
-      // P in four chunks of 32 scores (16 packed bf16 pairs each), stored to
-      // TMEM over the S columns already consumed.
+      uint64_t sum2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};  // four partial sums
+      // P in two chunks of 32 scores (16 packed bf16 pairs each), stored over
+      // this half's first 32 S columns (already read).
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < 2; ++ch) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int c = ch * 16 + i;  // pair index: scores 2c, 2c+1
+          const int c = ch * 16 + i;  // pair index within the half: columns 2c, 2c+1
           const uint64_t x = f2_fma(f2_make(__uint_as_float(sr[ch][2 * i]),
                                             __uint_as_float(sr[ch][2 * i + 1])), sl2x2, neg_m);
           float x0, x1, p0, p1;
@@ -250,48 +272,56 @@ __global__ void __launch_bounds__(kThreads, 2)
             p0 = ex2_approx(x0);
             p1 = ex2_approx(x1);
           }
-          if (2 * c > lim) p0 = 0.f;  // masked keys contribute exactly zero
-          if (2 * c + 1 > lim) p1 = 0.f;
-          sum2 = f2_add(sum2, f2_make(p0, p1));
+          if (need_mask) {  // masked keys contribute exactly zero
+            if (2 * c > lim) p0 = 0.f;
+            if (2 * c + 1 > lim) p1 = 0.f;
+          }
+          sum2[i & 1] = f2_add(sum2[i & 1], f2_make(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tmem_st16_nowait(tl + C::kColS + ch * 16, pk);
+        tmem_st16_nowait(tS + ch * 16, pk);
       }
       tmem_wait_st();
       if (j > 0 && __any_sync(0xffffffffu, moved)) {
-        // O holds sum over earlier tiles scaled by the old maximum: wait for the
-        // last P V to land, then rescale O in TMEM.
+        // O holds the sum over earlier tiles scaled by the old maximum: wait for
+        // the last P V to land, then rescale this half's O columns in TMEM.
         ok = warp_all(mbar_wait(bar(kBarO), (j - 1) & 1, wait_ns));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
           uint32_t ov[32];
-          tmem_ld32(tl + C::kColO + c * 32, ov);
+          const uint32_t col = C::kColO + half * (D / 2) + c * 32;
+          tmem_ld32(tl + col, ov);
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32_nowait(tl + C::kColO + c * 32, ov);
+          tmem_st32_nowait(tl + col, ov);
         }
         tmem_wait_st();
       }
-      float sum_lo, sum_hi;
-      f2_split(sum2, sum_lo, sum_hi);
-      l_run = l_run * alpha + (sum_lo + sum_hi);
+      float s0, s1, s2, s3;
+      f2_split(sum2[0], s0, s1);
+      f2_split(sum2[1], s2, s3);
+      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarP));
     }
     if (ok) ok = warp_all(mbar_wait(bar(kBarO), (n_kv - 1) & 1, wait_ns));
+    // Row sum = half 0's part + half 1's part, in that order.
+    red_l[half][r] = l_run;
+    named_barrier_sync(pair_bar, 64);
     if (ok) {
       tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      const float l_tot = red_l[0][r] + red_l[1][r];
+      const float inv_l = 1.f / l_tot;
       const bool live = qrow < a.T;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
-                            ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * D;
+                            ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * D + half * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t ov[32];
-        tmem_ld32(tl + C::kColO + c * 32, ov);
+        tmem_ld32(tl + C::kColO + half * (D / 2) + c * 32, ov);
         uint32_t pkd[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -304,9 +334,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
         }
       }
-      if (live)
+      if (live && half == 0)
         a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + qrow] =
-            (m_run + log2f(l_run)) * 0.69314718055994530942f;
+            (m_run + log2f(l_tot)) * 0.69314718055994530942f;
     }
   }
 
