@@ -257,26 +257,32 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       const uint32_t tDV = tmem + Cf::kColDV, tDK = tmem + Cf::kColDK;
       constexpr uint32_t kIdS = idesc_bf16(kTileN, kDkvTileM, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
+      // Operand descriptors built once; the loops only add constant offsets.
+      const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
+      const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);  // Q as K-major B
+      const uint64_t dQm0 = sdesc_sw128(stage_base(0), kDkvTileM * 128, 1024);  // Q as MN-major B
       ok = mbar_wait(bar(kDkvBarKV), 0, wait_ns);
       tc_fence_after();
       for (int li = 0; li < n_it && ok; ++li) {
         const int s = li % NS;
         const uint32_t ph = (li / NS) & 1;
-        const uint32_t sQ = stage_base(s), sdO = stage_base(s) + Cf::kQBytes;
+        const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
+        const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
+        const uint64_t dQm = desc_add(dQm0, s * Cf::kStageBytes);
+        const uint64_t ddOm = desc_add(dQm, Cf::kQBytes);
         if (!(ok = mbar_wait(bar(kDkvBarQFull + s), ph, wait_ns))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
           const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-          mma_ss(tS, sdesc_sw128(sK + okv, 16, 1024), sdesc_sw128(sQ + oq, 16, 1024), kIdS, ks > 0);
+          mma_ss(tS, desc_add(dK, okv), desc_add(dQk, oq), kIdS, ks > 0);
         }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
           const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-          mma_ss(tDP, sdesc_sw128(sV + okv, 16, 1024), sdesc_sw128(sdO + oq, 16, 1024), kIdS,
-                 ks > 0);
+          mma_ss(tDP, desc_add(dV, okv), desc_add(ddOk, oq), kIdS, ks > 0);
         }
         mma_commit(bar(kDkvBarS));
         if (!(ok = mbar_wait(bar(kDkvBarP), li & 1, wait_ns))) break;
@@ -288,8 +294,8 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         for (int ks = 0; ks < kDkvTileM / 16; ++ks) {
           const uint32_t acc = (li > 0 || ks > 0) ? 1u : 0u;
           const uint32_t pc = (ks >> 1) * 32 + (ks & 1) * 8;
-          mma_ts(tDV, tS + pc, sdesc_sw128(sdO + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
-          mma_ts(tDK, tDP + pc, sdesc_sw128(sQ + ks * 2048, kDkvTileM * 128, 1024), kIdAcc, acc);
+          mma_ts(tDV, tS + pc, desc_add(ddOm, ks * 2048), kIdAcc, acc);
+          mma_ts(tDK, tDP + pc, desc_add(dQm, ks * 2048), kIdAcc, acc);
         }
         mma_commit(bar(kDkvBarQEmpty + s));
       }
@@ -593,19 +599,24 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ;
       constexpr uint32_t kIdS = idesc_bf16(kTileM, kDqTileN, false, false);
       constexpr uint32_t kIdDQ = idesc_bf16(kTileM, D, false, true);
+      // Operand descriptors built once; the loops only add constant offsets.
+      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), ddO = sdesc_sw128(sdO, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024), dV0 = sdesc_sw128(sV0, 16, 1024);
+      const uint64_t dKm0 = sdesc_sw128(sK0, kDqTileN * 128, 1024);  // K as MN-major B
       ok = mbar_wait(bar(kDqBarQ), 0, wait_ns);
       tc_fence_after();
       for (int j = 0; j < n_kv && ok; ++j) {
         const int s = j % NS;
         const uint32_t ph = (j / NS) & 1;
-        const uint32_t sK = sK0 + s * C::kKvBytes, sV = sV0 + s * C::kKvBytes;
+        const uint64_t dK = desc_add(dK0, s * C::kKvBytes), dV = desc_add(dV0, s * C::kKvBytes);
+        const uint64_t dKm = desc_add(dKm0, s * C::kKvBytes);
         if (!(ok = mbar_wait(bar(kDqBarKFull + s), ph, wait_ns))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
           const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
-          mma_ss(tS, sdesc_sw128(sQ + oq, 16, 1024), sdesc_sw128(sK + okv, 16, 1024), kIdS, ks > 0);
+          mma_ss(tS, desc_add(dQ, oq), desc_add(dK, okv), kIdS, ks > 0);
         }
         if (!(ok = mbar_wait(bar(kDqBarVFull + s), ph, wait_ns))) break;
         tc_fence_after();
@@ -613,8 +624,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
           const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
-          mma_ss(tDP, sdesc_sw128(sdO + oq, 16, 1024), sdesc_sw128(sV + okv, 16, 1024), kIdS,
-                 ks > 0);
+          mma_ss(tDP, desc_add(ddO, oq), desc_add(dV, okv), kIdS, ks > 0);
         }
         mma_commit(bar(kDqBarS));
         mma_commit(bar(kDqBarVEmpty + s));
@@ -624,8 +634,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // columns at the start of its own 32 S columns.
 #pragma unroll
         for (int ks = 0; ks < kDqTileN / 16; ++ks)
-          mma_ts(tDQ, tS + (ks >> 1) * 32 + (ks & 1) * 8,
-                 sdesc_sw128(sK + ks * 2048, kDqTileN * 128, 1024), kIdDQ,
+          mma_ts(tDQ, tS + (ks >> 1) * 32 + (ks & 1) * 8, desc_add(dKm, ks * 2048), kIdDQ,
                  (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(bar(kDqBarKEmpty + s));
       }

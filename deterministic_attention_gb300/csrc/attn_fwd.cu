@@ -165,19 +165,23 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t tS = tmem + C::kColS, tO = tmem + C::kColO;
       constexpr uint32_t kIdQK = idesc_bf16(kTileM, kTileN, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, false, true);
+      // Operand descriptors built once; the loops only add constant offsets.
+      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(sV0, 16384, 1024);
       ok = mbar_wait(bar(kBarQ), 0, wait_ns);
       tc_fence_after();
       for (int j = 0; j < n_kv && ok; ++j) {
         const int s = j % NS;
         const uint32_t ph = (j / NS) & 1;
-        const uint32_t sK = sK0 + s * C::kTileBytes, sV = sV0 + s * C::kTileBytes;
+        const uint64_t dK = desc_add(dK0, s * C::kTileBytes), dV = desc_add(dV0, s * C::kTileBytes);
         if (!(ok = mbar_wait(bar(kBarKFull + s), ph, wait_ns))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(tS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), kIdQK,
-                 ks > 0);
+          constexpr uint32_t kAtom = 16384;
+          const uint32_t off = (ks >> 2) * kAtom + (ks & 3) * 32;
+          mma_ss(tS, desc_add(dQ, off), desc_add(dK, off), kIdQK, ks > 0);
         }
         mma_commit(bar(kBarS));
         mma_commit(bar(kBarKEmpty + s));
@@ -188,8 +192,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         // columns at the start of its own 64 S columns.
 #pragma unroll
         for (int ks = 0; ks < kTileN / 16; ++ks)
-          mma_ts(tO, tS + (ks >> 2) * 64 + (ks & 3) * 8, sdesc_sw128(sV + ks * 2048, 16384, 1024),
-                 kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+          mma_ts(tO, tS + (ks >> 2) * 64 + (ks & 3) * 8, desc_add(dV, ks * 2048), kIdPV,
+                 (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(bar(kBarVEmpty + s));
         mma_commit(bar(kBarO));
       }

@@ -163,6 +163,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// A descriptor moved by `bytes` (a multiple of 16): the start-address field
+// holds address / 16 in its low bits, and shared-memory addresses stay below
+// 2^18, so the add never carries out of the field.  Descriptors are built once
+// per buffer and advanced with this single add in the issue loops: the MMA
+// issue rate is then set by the tensor core rather than by the issuing
+// thread's dependent integer arithmetic.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+  return d + static_cast<uint64_t>(bytes >> 4);
+}
+
 // TMEM loads/stores, 32 lanes x 32-bit shape: thread i of the warp reads lane
 // (lane base + i), N consecutive columns.  Each helper waits for completion
 // inside the same asm statement, so the registers are valid on return.
