@@ -6,16 +6,18 @@
 // forward hands to the backward.
 //
 // One thread block owns one 128-row query tile of one (batch, query head) and
-// walks the key/value tiles 0..diagonal in ascending order:
+// walks 64-key tiles 0..diagonal in ascending order:
 //   warp 0      TMA producer: Q once, then K_j / V_j into a ring of stages
-//   warp 1      tcgen05 issuer: S = Q K_j^T into TMEM, then O += P V_j with P
-//               read from TMEM (bf16, written over S by the softmax warps)
-//   warps 2..5  softmax: thread r owns query row r (TMEM lane r); online
-//               softmax in base 2 with a lazily moved row maximum, P to TMEM,
-//               O rescaled in TMEM when the maximum moves, epilogue O / l and
-//               LSE = ln2 * (m + log2 l)
-// Two blocks share an SM (256 TMEM columns each), so one block's softmax
-// overlaps the other's matrix multiplies.
+//   warp 1      tcgen05 issuer, one key tile ahead of the softmax: S_{j+1} =
+//               Q K_{j+1}^T goes into the other of two TMEM score buffers while
+//               the softmax works on S_j; then O += P_j V_j with P_j read from
+//               TMEM (bf16, written over S_j by the softmax warps)
+//   warps 2..9  softmax: two threads per query row (TMEM lane), each taking 32
+//               of the tile's 64 keys; online softmax in base 2 with a lazily
+//               moved row maximum, P to TMEM, O rescaled in TMEM when the
+//               maximum moves, epilogue O / l and LSE = ln2 * (m + log2 l)
+// Two blocks share an SM (256 TMEM columns each), so one block's prologue and
+// epilogue overlap the other's main loop.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -33,13 +35,14 @@ __device__ unsigned int g_fwd_status;
 namespace {
 
 constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
+constexpr int kBN = kFwdTileN;  // keys per tile (64)
 // The row maximum used in the exponent is only moved when the true maximum
 // exceeds it by more than 2^8; until then P <= 256, which bf16 and the fp32
 // accumulators hold exactly as well.  The final O / l and LSE are exact for
 // any value of the stale maximum.
 constexpr float kRescaleLog2 = 8.0f;
 // Of every 8 consecutive pairs of scores, this many take 2^x from the FMA-pipe
-// polynomial instead of the special-function unit, to balance the two.
+// polynomial instead of the special-function unit.
 #ifndef DETATTN_FWD_POLY_OF8
 #define DETATTN_FWD_POLY_OF8 0
 #endif
@@ -47,27 +50,40 @@ constexpr int kPolyOf8 = DETATTN_FWD_POLY_OF8;
 
 template <int D>
 struct Cfg {
-  static constexpr int kAtoms = D / 64;                   // 128-byte swizzle atoms per row
-  static constexpr int kTileBytes = kTileM * 128 * kAtoms;  // 128 rows x D bf16
-  static constexpr int kStages = (D == 64) ? 2 : 1;
+  static constexpr int kAtoms = D / 64;                  // 128-byte swizzle atoms per row
+  static constexpr int kQBytes = kTileM * 128 * kAtoms;  // 128 rows x D bf16
+  static constexpr int kKvBytes = kBN * 128 * kAtoms;    // 64 rows x D bf16
+  static constexpr int kStages = (D == 64) ? 4 : 2;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kSmemBytes = kOffV + kStages * kTileBytes + 1024;  // + alignment slack
+  static constexpr int kOffK = kQBytes;
+  static constexpr int kOffV = kOffK + kStages * kKvBytes;
+  static constexpr int kSmemBytes = kOffV + kStages * kKvBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 256;
-  static constexpr uint32_t kColS = 0;    // S (fp32, 128 cols); P (bf16 pairs) of keys
-                                          // 64h..64h+63 over cols 64h..64h+31
+  // Two score buffers of 64 fp32 columns (buffer b at 64 b).  The softmax
+  // thread of half h owns columns 32h..32h+31 of a buffer and writes its 32
+  // bf16 P values, packed in pairs, over the first 16 of them.
+  static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO = 128;  // O accumulator, D cols
 };
 
-enum : int { kBarQ = 0, kBarKFull = 1, kBarVFull = 3, kBarKEmpty = 5, kBarVEmpty = 7,
-             kBarS = 9, kBarP = 10, kBarO = 11, kBarDrain = 12, kNumBars = 13 };
+constexpr int kMaxStages = 4;
+enum : int {
+  kBarQ = 0,
+  kBarKFull = 1,
+  kBarVFull = kBarKFull + kMaxStages,
+  kBarKEmpty = kBarVFull + kMaxStages,
+  kBarVEmpty = kBarKEmpty + kMaxStages,
+  kBarS = kBarVEmpty + kMaxStages,  // [2]: score buffer b holds S_j
+  kBarP = kBarS + 2,                // [2]: softmax wrote P_j over buffer b
+  kBarO = kBarP + 2,                // one arrival per finished O += P V
+  kBarOFinal = kBarO + 1,           // the last O += P V has finished
+  kBarDrain = kBarOFinal + 1,
+  kBarPair = kBarDrain + 1,         // [4]: the two softmax halves of a lane quarter
+  kNumBars = kBarPair + 4
+};
 
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
-__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -88,7 +104,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int b = bh / a.Hq, h = bh % a.Hq;
   const int hkv = h / (a.Hq / a.Hkv);
   const int m0 = mt * kTileM;
-  const int n_kv = a.causal ? (mt + 1) : (a.T + kTileN - 1) / kTileN;
+  const int kv_tiles = (a.T + kBN - 1) / kBN;
+  const int n_kv = a.causal ? min(kv_tiles, (m0 + kTileM) / kBN) : kv_tiles;
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -104,16 +121,20 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ), 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
       mbar_init(bar(kBarVFull + s), 1);
       mbar_init(bar(kBarKEmpty + s), 1);
       mbar_init(bar(kBarVEmpty + s), 1);
     }
-    mbar_init(bar(kBarS), 1);
-    mbar_init(bar(kBarP), 8);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarS + i), 1);
+      mbar_init(bar(kBarP + i), 8);
+    }
     mbar_init(bar(kBarO), 1);
+    mbar_init(bar(kBarOFinal), 1);
     mbar_init(bar(kBarDrain), 1);
+    for (int qq = 0; qq < 4; ++qq) mbar_init(bar(kBarPair + qq), 64);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -130,24 +151,25 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int last_k[2] = {-1, -1}, last_v[2] = {-1, -1};
-      mbar_arrive_expect_tx(bar(kBarQ), C::kTileBytes);
+      int last_k[kMaxStages], last_v[kMaxStages];
+      for (int s = 0; s < kMaxStages; ++s) last_k[s] = last_v[s] = -1;
+      mbar_arrive_expect_tx(bar(kBarQ), C::kQBytes);
       for (int at = 0; at < C::kAtoms; ++at)
-        tma_load_4d(sQ + at * 16384, &mQ, bar(kBarQ), at * 64, h, m0, b);
+        tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kBarQ), at * 64, h, m0, b);
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % NS;
         const uint32_t ph = (j / NS) & 1;
         if (j >= NS && !(ok = mbar_wait(bar(kBarKEmpty + s), ph ^ 1, wait_ns))) break;
-        mbar_arrive_expect_tx(bar(kBarKFull + s), C::kTileBytes);
+        mbar_arrive_expect_tx(bar(kBarKFull + s), C::kKvBytes);
         for (int at = 0; at < C::kAtoms; ++at)
-          tma_load_4d(sK0 + s * C::kTileBytes + at * 16384, &mK, bar(kBarKFull + s), at * 64, hkv,
-                      j * kTileN, b);
+          tma_load_4d(sK0 + s * C::kKvBytes + at * (kBN * 128), &mK, bar(kBarKFull + s), at * 64,
+                      hkv, j * kBN, b);
         last_k[s] = j;
         if (j >= NS && !(ok = mbar_wait(bar(kBarVEmpty + s), ph ^ 1, wait_ns))) break;
-        mbar_arrive_expect_tx(bar(kBarVFull + s), C::kTileBytes);
+        mbar_arrive_expect_tx(bar(kBarVFull + s), C::kKvBytes);
         for (int at = 0; at < C::kAtoms; ++at)
-          tma_load_4d(sV0 + s * C::kTileBytes + at * 16384, &mV, bar(kBarVFull + s), at * 64, hkv,
-                      j * kTileN, b);
+          tma_load_4d(sV0 + s * C::kKvBytes + at * (kBN * 128), &mV, bar(kBarVFull + s), at * 64,
+                      hkv, j * kBN, b);
         last_v[s] = j;
       }
       if (!ok) {
@@ -162,91 +184,103 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t tS = tmem + C::kColS, tO = tmem + C::kColO;
-      constexpr uint32_t kIdQK = idesc_bf16(kTileM, kTileN, false, false);
+      constexpr uint32_t kIdQK = idesc_bf16(kTileM, kBN, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, false, true);
       // Operand descriptors built once; the loops only add constant offsets.
       const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(sV0, 16384, 1024);
+      const uint64_t dV0 = sdesc_sw128(sV0, kBN * 128, 1024);
+      // S_j = Q K_j^T into score buffer j & 1.
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j % NS;
+        if (!mbar_wait(bar(kBarKFull + s), (j / NS) & 1, wait_ns)) return false;
+        tc_fence_after();
+        const uint64_t dK = desc_add(dK0, s * C::kKvBytes);
+        const uint32_t tS = tmem + C::kColS + (j & 1) * kBN;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          mma_ss(tS, desc_add(dQ, (ks >> 2) * (kTileM * 128) + (ks & 3) * 32),
+                 desc_add(dK, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), kIdQK, ks > 0);
+        mma_commit(bar(kBarS + (j & 1)));
+        mma_commit(bar(kBarKEmpty + s));
+        return true;
+      };
       ok = mbar_wait(bar(kBarQ), 0, wait_ns);
       tc_fence_after();
+      if (ok && n_kv > 0) ok = issue_qk(0);
       for (int j = 0; j < n_kv && ok; ++j) {
+        // One tile ahead: S_{j+1} lands in the other buffer while the softmax
+        // works on S_j.  That buffer last held P_{j-1}, whose P V was issued
+        // in the previous iteration (tcgen05 operations run in issue order).
+        if (j + 1 < n_kv && !(ok = issue_qk(j + 1))) break;
         const int s = j % NS;
-        const uint32_t ph = (j / NS) & 1;
-        const uint64_t dK = desc_add(dK0, s * C::kTileBytes), dV = desc_add(dV0, s * C::kTileBytes);
-        if (!(ok = mbar_wait(bar(kBarKFull + s), ph, wait_ns))) break;
+        if (!(ok = mbar_wait(bar(kBarP + (j & 1)), (j >> 1) & 1, wait_ns))) break;
+        if (!(ok = mbar_wait(bar(kBarVFull + s), (j / NS) & 1, wait_ns))) break;
         tc_fence_after();
+        const uint64_t dV = desc_add(dV0, s * C::kKvBytes);
+        const uint32_t tP = tmem + C::kColS + (j & 1) * kBN;
+        // P of keys 16ks..16ks+15: half ks/2 wrote its 32 keys as 16 packed
+        // columns at the start of its own 32 score columns.
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          constexpr uint32_t kAtom = 16384;
-          const uint32_t off = (ks >> 2) * kAtom + (ks & 3) * 32;
-          mma_ss(tS, desc_add(dQ, off), desc_add(dK, off), kIdQK, ks > 0);
-        }
-        mma_commit(bar(kBarS));
-        mma_commit(bar(kBarKEmpty + s));
-        if (!(ok = mbar_wait(bar(kBarP), j & 1, wait_ns))) break;
-        if (!(ok = mbar_wait(bar(kBarVFull + s), ph, wait_ns))) break;
-        tc_fence_after();
-        // P of keys 16ks..16ks+15: half ks/4 wrote its 64 keys as 32 packed
-        // columns at the start of its own 64 S columns.
-#pragma unroll
-        for (int ks = 0; ks < kTileN / 16; ++ks)
-          mma_ts(tO, tS + (ks >> 2) * 64 + (ks & 3) * 8, desc_add(dV, ks * 2048), kIdPV,
-                 (j > 0 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          mma_ts(tmem + C::kColO, tP + (ks >> 1) * 32 + (ks & 1) * 8, desc_add(dV, ks * 2048),
+                 kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
         mma_commit(bar(kBarVEmpty + s));
         mma_commit(bar(kBarO));
       }
+      // The epilogue waits on its own barrier: with the issuer a tile ahead,
+      // the per-tile O barrier can trail the softmax by two phases there,
+      // which a parity wait cannot tell apart.
+      mma_commit(bar(kBarOFinal));
       // Every issued MMA must finish before TMEM is released.
       mma_commit(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, wait_ns);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    // Eight warps: warps w and w+4 share TMEM lane quarter (w & 3), i.e. the
-    // same 32 query rows; "half" 0 takes key columns 0..63, half 1 64..127.
-    // The two halves of a row trade their partial row maxima through shared
-    // memory (one 64-thread named barrier per tile); the row sums stay split
-    // until the epilogue.  Each half writes its P over its own S columns, so
-    // the halves never touch each other's TMEM columns.
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    // Warps w and w+4 share TMEM lane quarter (w & 3), i.e. the same 32 query
+    // rows; half 0 takes keys 0..31 of each tile, half 1 keys 32..63.  The two
+    // halves of a row trade partial row maxima through shared memory, meeting
+    // at an mbarrier of the pair (64 arrivals, bounded wait) once per tile;
+    // the row sums stay split until the epilogue.
+    const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int qrow = m0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t tS = tl + C::kColS + half * 64;  // this half's 64 score columns
     const float sl2 = a.scale_log2;
-    const uint32_t pair_bar = 1 + quarter;          // named barrier of the two halves
+    const uint32_t pair_bar = bar(kBarPair + quarter);  // the two halves of these rows
     float m_run = -INFINITY, l_run = 0.f;
     for (int j = 0; j < n_kv; ++j) {
-      ok = warp_all(mbar_wait(bar(kBarS), j & 1, wait_ns));
+      ok = warp_all(mbar_wait(bar(kBarS + (j & 1)), (j >> 1) & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sr[2][32];
-      tmem_ld32_nowait(tS, sr[0]);
-      tmem_ld32_nowait(tS + 32, sr[1]);
+      const uint32_t tS = tl + C::kColS + (j & 1) * kBN + half * 32;  // this half's columns
+      uint32_t sr[32];
+      tmem_ld32_nowait(tS, sr);
       tmem_wait_ld();
-      reg_fence32(sr[0]);
-      reg_fence32(sr[1]);
+      reg_fence32(sr);
 
-      const int kv0 = j * kTileN + half * 64;  // key of this half's first column
-      const bool need_mask = a.causal ? (j == n_kv - 1) : (j * kTileN + kTileN > a.T);
-      const int lim = need_mask ? (a.causal ? (qrow - kv0) : (a.T - 1 - kv0)) : (1 << 30);
+      const int kv0 = j * kBN + half * 32;  // key of this thread's first column
+      const bool need_mask = a.causal ? (kv0 + 31 > m0) : (kv0 + 32 > a.T);
+      const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c > lim) sr[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < 32; ++c)
+          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      // Partial maximum over 64 columns in four independent chains.
+      // Partial maximum over 32 columns in four independent chains.
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        mx4[c & 3] = fmax3(mx4[c & 3], __uint_as_float(sr[c >> 4][(2 * c) & 31]),
-                           __uint_as_float(sr[c >> 4][(2 * c + 1) & 31]));
-      const float mx_half = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      red_max[j & 1][half][r] = mx_half;
-      named_barrier_sync(pair_bar, 64);
+      for (int c = 0; c < 16; ++c)
+        mx4[c & 3] = fmax3(mx4[c & 3], __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+      red_max[j & 1][half][r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      mbar_arrive(pair_bar);
+      ok = warp_all(mbar_wait(pair_bar, j & 1, wait_ns));
+      if (!ok) break;
       const float mx = fmaxf(red_max[j & 1][0][r], red_max[j & 1][1][r]);
+      // A row may see no key in this tile (the half-tile past its diagonal):
+      // mx = -inf leaves the running maximum alone and every P zero.
       const float m_new = mx * sl2;
       float alpha = 1.f;
       bool moved = false;
@@ -258,37 +292,33 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
       const uint64_t sl2x2 = f2_make(sl2, sl2), neg_m = f2_make(-m_use, -m_use);
       uint64_t sum2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};  // four partial sums
-      // P in two chunks of 32 scores (16 packed bf16 pairs each), stored over
-      // this half's first 32 S columns (already read).
+      uint32_t pk[16];
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = ch * 16 + i;  // pair index within the half: columns 2c, 2c+1
-          const uint64_t x = f2_fma(f2_make(__uint_as_float(sr[ch][2 * i]),
-                                            __uint_as_float(sr[ch][2 * i + 1])), sl2x2, neg_m);
-          float x0, x1, p0, p1;
-          f2_split(x, x0, x1);
-          if ((c & 7) < kPolyOf8) {
-            exp2_poly2(x0, x1, p0, p1);
-          } else {
-            p0 = ex2_approx(x0);
-            p1 = ex2_approx(x1);
-          }
-          if (need_mask) {  // masked keys contribute exactly zero
-            if (2 * c > lim) p0 = 0.f;
-            if (2 * c + 1 > lim) p1 = 0.f;
-          }
-          sum2[i & 1] = f2_add(sum2[i & 1], f2_make(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+      for (int i = 0; i < 16; ++i) {
+        const uint64_t x = f2_fma(f2_make(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                                  sl2x2, neg_m);
+        float x0, x1, p0, p1;
+        f2_split(x, x0, x1);
+        if ((i & 7) < kPolyOf8) {
+          exp2_poly2(x0, x1, p0, p1);
+        } else {
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
         }
-        tmem_st16_nowait(tS + ch * 16, pk);
+        if (need_mask) {  // masked keys contribute exactly zero
+          if (2 * i > lim) p0 = 0.f;
+          if (2 * i + 1 > lim) p1 = 0.f;
+        }
+        sum2[i & 1] = f2_add(sum2[i & 1], f2_make(p0, p1));
+        pk[i] = pack_bf16x2(p0, p1);
       }
+      tmem_st16_nowait(tS, pk);
       tmem_wait_st();
       if (j > 0 && __any_sync(0xffffffffu, moved)) {
         // O holds the sum over earlier tiles scaled by the old maximum: wait for
         // the last P V to land, then rescale this half's O columns in TMEM.
+        // (S_j was committed after P_{j-2} V, so the O barrier is at most one
+        // phase behind here and the parity wait is exact.)
         ok = warp_all(mbar_wait(bar(kBarO), (j - 1) & 1, wait_ns));
         if (!ok) break;
         tc_fence_after();
@@ -309,12 +339,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarP));
+      if (lane == 0) mbar_arrive(bar(kBarP + (j & 1)));
     }
-    if (ok) ok = warp_all(mbar_wait(bar(kBarO), (n_kv - 1) & 1, wait_ns));
+    if (ok) ok = warp_all(mbar_wait(bar(kBarOFinal), 0, wait_ns));
     // Row sum = half 0's part + half 1's part, in that order.
     red_l[half][r] = l_run;
-    named_barrier_sync(pair_bar, 64);
+    mbar_arrive(pair_bar);
+    if (ok) ok = warp_all(mbar_wait(pair_bar, n_kv & 1, wait_ns));
     if (ok) {
       tc_fence_after();
       const float l_tot = red_l[0][r] + red_l[1][r];

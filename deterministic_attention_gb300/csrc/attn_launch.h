@@ -8,7 +8,8 @@
 namespace detattn {
 
 constexpr int kTileM = 128;     // query rows per forward / dQ tile
-constexpr int kTileN = 128;     // key rows per forward KV tile and per dK/dV tile
+constexpr int kTileN = 128;     // key rows per dK/dV tile
+constexpr int kFwdTileN = 64;   // key rows per forward KV tile
 constexpr int kDqTileN = 64;    // key rows per dQ-kernel KV tile
 constexpr int kDkvTileM = 64;   // query rows per dK/dV-kernel Q tile
 
