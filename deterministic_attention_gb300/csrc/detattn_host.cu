@@ -134,8 +134,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   CUtensorMap mq, mk, mv;
   int rc;
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
-  if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
-  if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kFwdTileN, "k")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kFwdTileN, "v")) != DETATTN_OK) return rc;
   FwdArgs a{};
   a.o = o;
   a.lse = lse;
