@@ -34,7 +34,6 @@ __device__ unsigned int g_bwd_status;
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kThreads = 320;  // producer, MMA issuer, 8 compute warps
 // Of every 8 consecutive pairs of probabilities, this many take 2^x from the
 // FMA-pipe polynomial instead of the special-function unit.
 #ifndef DETATTN_BWD_POLY_OF8
@@ -106,37 +105,51 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
 }
 
 // ============================================================== dK / dV
-// Block = (b, KV head, 128-key tile).  Warp 0 loads K, V once and then the
-// (Q, dO, LSE, Delta) of 64-row query tiles of every query head in the group;
-// warp 1 issues S^T = K Q^T and dP^T = V dO^T, then dV += P^T dO and
-// dK += dS^T Q with P^T and dS^T read from TMEM; warps 2..5 (thread r = key
-// row r) turn S^T, dP^T into P^T, dS^T.
+// Block = (b, KV head, 128-key tile), or one of C blocks of a cluster sharing
+// that tile.  Warp 0 loads K, V once and then the (Q, dO, row statistics) of
+// 64-row query tiles of every query head in the group; warp 1 issues, one
+// query tile ahead, S^T = K Q^T and dP^T = V dO^T into the other of two TMEM
+// buffers, then dV += P^T dO and dK += dS^T Q with P^T and dS^T read from
+// TMEM; warps 2..17 turn S^T, dP^T into P^T, dS^T (four threads per key row,
+// 16 queries each).
+constexpr int kBwdThreads = 576;  // producer, MMA issuer, 16 compute warps
+constexpr int kComputeWarps = 16;
+
 template <int D>
 struct DkvCfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kKvBytes = kTileN * 128 * kAtoms;    // 128 keys x D
   static constexpr int kQBytes = kDkvTileM * 128 * kAtoms;  // 64 queries x D
-  static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr int kStageBytes = 2 * kQBytes + 1024;    // Q, dO, then LSE/Delta rows
+  static constexpr int kStages = (D == 64) ? 4 : 3;
+  static constexpr int kStageBytes = 2 * kQBytes + 1024;    // Q, dO, then row statistics
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kKvBytes;
   static constexpr int kOffStage = 2 * kKvBytes;
   static constexpr int kSmemBytes = kOffStage + kStages * kStageBytes + 1024;
-  static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;
-  static constexpr uint32_t kColS = 0;        // S^T fp32 [128 x 64]; P^T bf16 over cols 0..31
-  static constexpr uint32_t kColDP = 64;      // dP^T fp32; dS^T bf16 over cols 64..95
-  static constexpr uint32_t kColDV = 128;     // dV accumulator, D cols
-  static constexpr uint32_t kColDK = 128 + D; // dK accumulator, D cols
+  static constexpr uint32_t kTmemCols = 512;
+  // Buffer b (b = 0, 1): S^T at 128 b, dP^T at 128 b + 64 (64 fp32 columns
+  // each, one per query); the compute thread of group g writes its 16 P^T
+  // (dS^T) values as 8 packed bf16 pairs over columns 16g..16g+7 of S^T (dP^T).
+  static constexpr uint32_t kColDV = 256;      // dV accumulator, D cols
+  static constexpr uint32_t kColDK = 256 + D;  // dK accumulator, D cols
 };
-
 static_assert(kTileN * 2 * 64 * 4 <= DkvCfg<64>::kSmemBytes - 1024, "dK/dV partials fit");
 static_assert(kTileN * 2 * 128 * 4 <= DkvCfg<128>::kSmemBytes - 1024, "dK/dV partials fit");
 
-enum : int { kDkvBarKV = 0, kDkvBarQFull = 1, kDkvBarQEmpty = 4, kDkvBarS = 7, kDkvBarP = 8,
-             kDkvBarAcc = 9, kDkvBarDrain = 10, kDkvNumBars = 11 };
+constexpr int kDkvMaxStages = 4;
+enum : int {
+  kDkvBarKV = 0,
+  kDkvBarQFull = 1,
+  kDkvBarQEmpty = kDkvBarQFull + kDkvMaxStages,
+  kDkvBarS = kDkvBarQEmpty + kDkvMaxStages,  // [2]
+  kDkvBarP = kDkvBarS + 2,                   // [2]
+  kDkvBarAcc = kDkvBarP + 2,
+  kDkvBarDrain = kDkvBarAcc + 1,
+  kDkvNumBars = kDkvBarDrain + 1
+};
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                      const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
                      const BwdArgs a) {
@@ -189,12 +202,14 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(bar(kDkvBarKV), 1);
-    for (int s = 0; s < 3; ++s) {
+    for (int s = 0; s < kDkvMaxStages; ++s) {
       mbar_init(bar(kDkvBarQFull + s), 1);
       mbar_init(bar(kDkvBarQEmpty + s), 1);
     }
-    mbar_init(bar(kDkvBarS), 1);
-    mbar_init(bar(kDkvBarP), 8);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kDkvBarS + i), 1);
+      mbar_init(bar(kDkvBarP + i), kComputeWarps);
+    }
     mbar_init(bar(kDkvBarAcc), 1);
     mbar_init(bar(kDkvBarDrain), 1);
     fence_barrier_init();
@@ -212,26 +227,22 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
   bool ok = true;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer (whole warp)
-    int last[3] = {-1, -1, -1};
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
+      int last[kDkvMaxStages];
+      for (int s = 0; s < kDkvMaxStages; ++s) last[s] = -1;
       mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * Cf::kKvBytes);
       for (int at = 0; at < Cf::kAtoms; ++at) {
         tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, g, n0, b);
         tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, g, n0, b);
       }
-    }
-    for (int li = 0; li < n_it; ++li) {
-      const int it = it_lo + li;
-      const int s = li % NS;
-      const uint32_t ph = (li / NS) & 1;
-      const int h = g * G + it / per_head;
-      const int i0 = (m_begin + it % per_head) * kDkvTileM;
-      if (li >= NS) {
-        ok = warp_all(mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns));
-        if (!ok) break;
-      }
-      if (lane == 0) {
+      for (int li = 0; li < n_it; ++li) {
+        const int it = it_lo + li;
+        const int s = li % NS;
+        const uint32_t ph = (li / NS) & 1;
+        const int h = g * G + it / per_head;
+        const int i0 = (m_begin + it % per_head) * kDkvTileM;
+        if (li >= NS && !(ok = mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns))) break;
         const uint32_t st = stage_base(s);
         mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + kDkvTileM * 8);
         for (int at = 0; at < Cf::kAtoms; ++at) {
@@ -242,36 +253,32 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         bulk_load(st + 2 * Cf::kQBytes,
                   a.rowstats + (static_cast<size_t>(b) * a.Hq + h) * a.Tp + i0, kDkvTileM * 8,
                   bar(kDkvBarQFull + s));
+        last[s] = li;
       }
-      last[s] = li;
-    }
-    if (!ok && lane == 0) {
-      mbar_wait(bar(kDkvBarKV), 0, wait_ns);
-      for (int s = 0; s < NS; ++s)
-        if (last[s] >= 0) mbar_wait(bar(kDkvBarQFull + s), (last[s] / NS) & 1, wait_ns);
+      if (!ok) {
+        mbar_wait(bar(kDkvBarKV), 0, wait_ns);
+        for (int s = 0; s < NS; ++s)
+          if (last[s] >= 0) mbar_wait(bar(kDkvBarQFull + s), (last[s] / NS) & 1, wait_ns);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t tS = tmem + Cf::kColS, tDP = tmem + Cf::kColDP;
       const uint32_t tDV = tmem + Cf::kColDV, tDK = tmem + Cf::kColDK;
       constexpr uint32_t kIdS = idesc_bf16(kTileN, kDkvTileM, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
       // Operand descriptors built once; the loops only add constant offsets.
       const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
-      const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);  // Q as K-major B
-      const uint64_t dQm0 = sdesc_sw128(stage_base(0), kDkvTileM * 128, 1024);  // Q as MN-major B
-      ok = mbar_wait(bar(kDkvBarKV), 0, wait_ns);
-      tc_fence_after();
-      for (int li = 0; li < n_it && ok; ++li) {
+      const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);                 // K-major B
+      const uint64_t dQm0 = sdesc_sw128(stage_base(0), kDkvTileM * 128, 1024);  // MN-major B
+      // S^T, dP^T of item li into buffer li & 1.
+      auto issue_st = [&](int li) -> bool {
         const int s = li % NS;
-        const uint32_t ph = (li / NS) & 1;
+        if (!mbar_wait(bar(kDkvBarQFull + s), (li / NS) & 1, wait_ns)) return false;
+        tc_fence_after();
         const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
         const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
-        const uint64_t dQm = desc_add(dQm0, s * Cf::kStageBytes);
-        const uint64_t ddOm = desc_add(dQm, Cf::kQBytes);
-        if (!(ok = mbar_wait(bar(kDkvBarQFull + s), ph, wait_ns))) break;
-        tc_fence_after();
+        const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
@@ -284,18 +291,29 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
           const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
           mma_ss(tDP, desc_add(dV, okv), desc_add(ddOk, oq), kIdS, ks > 0);
         }
-        mma_commit(bar(kDkvBarS));
-        if (!(ok = mbar_wait(bar(kDkvBarP), li & 1, wait_ns))) break;
+        mma_commit(bar(kDkvBarS + (li & 1)));
+        return true;
+      };
+      ok = mbar_wait(bar(kDkvBarKV), 0, wait_ns);
+      tc_fence_after();
+      if (ok && n_it > 0) ok = issue_st(0);
+      for (int li = 0; li < n_it && ok; ++li) {
+        // One item ahead: S^T, dP^T of item li+1 land in the other buffer while
+        // the compute warps work on item li.
+        if (li + 1 < n_it && !(ok = issue_st(li + 1))) break;
+        const int s = li % NS;
+        if (!(ok = mbar_wait(bar(kDkvBarP + (li & 1)), (li >> 1) & 1, wait_ns))) break;
         tc_fence_after();
-        // Accumulate over the 64 queries of this tile, 16 at a time.
-        // P^T / dS^T of queries 16ks..16ks+15: half ks/2 wrote its 32 queries as
-        // 16 packed columns at the start of its own 32 S^T / dP^T columns.
+        const uint64_t dQm = desc_add(dQm0, s * Cf::kStageBytes);
+        const uint64_t ddOm = desc_add(dQm, Cf::kQBytes);
+        const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
+        // P^T / dS^T of queries 16ks..16ks+15: group ks wrote them as 8 packed
+        // columns at the start of its 16 S^T / dP^T columns.
 #pragma unroll
         for (int ks = 0; ks < kDkvTileM / 16; ++ks) {
           const uint32_t acc = (li > 0 || ks > 0) ? 1u : 0u;
-          const uint32_t pc = (ks >> 1) * 32 + (ks & 1) * 8;
-          mma_ts(tDV, tS + pc, desc_add(ddOm, ks * 2048), kIdAcc, acc);
-          mma_ts(tDK, tDP + pc, desc_add(dQm, ks * 2048), kIdAcc, acc);
+          mma_ts(tDV, tS + ks * 16, desc_add(ddOm, ks * 2048), kIdAcc, acc);
+          mma_ts(tDK, tDP + ks * 16, desc_add(dQm, ks * 2048), kIdAcc, acc);
         }
         mma_commit(bar(kDkvBarQEmpty + s));
       }
@@ -305,39 +323,38 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     }
   } else {
     // ------------------------------------------------------------ P^T / dS^T warps
-    // Eight warps: warps w and w+4 share TMEM lane quarter (w & 3), i.e. the
-    // same 32 key rows; half 0 takes query columns 0..31 of the tile, half 1
-    // columns 32..63.  Each half writes its P^T / dS^T (bf16 pairs) over the
-    // first 16 of its own 32 S^T / dP^T columns.
+    // Warps w, w+4, w+8, w+12 share TMEM lane quarter (w & 3), i.e. the same
+    // 32 key rows; group grp = (w - 2) / 4 takes queries 16 grp..16 grp+15 of
+    // each 64-query item.
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int krow = n0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t tS = tl + Cf::kColS + half * 32, tDP = tl + Cf::kColDP + half * 32;
     const float sl2 = a.scale_log2;
     for (int li = 0; li < n_it; ++li) {
       const int it = it_lo + li;
       const int s = li % NS;
-      const int i0 = (m_begin + it % per_head) * kDkvTileM + half * 32;  // this half's first query
-      ok = warp_all(mbar_wait(bar(kDkvBarS), li & 1, wait_ns));
+      const int i0 = (m_begin + it % per_head) * kDkvTileM + grp * 16;  // this group's first query
+      ok = warp_all(mbar_wait(bar(kDkvBarS + (li & 1)), (li >> 1) & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sv[32], dp[32];
-      tmem_ld32_nowait(tS, sv);
-      tmem_ld32_nowait(tDP, dp);
+      const uint32_t tS = tl + (li & 1) * 128 + grp * 16, tDP = tS + 64;
+      uint32_t sv[16], dp[16];
+      tmem_ld16_nowait(tS, sv);
+      tmem_ld16_nowait(tDP, dp);
       tmem_wait_ld();
-      reg_fence32(sv);
-      reg_fence32(dp);
+      reg_fence16(sv);
+      reg_fence16(dp);
       // Causal: query i0 + c sees key krow iff c >= krow - i0.
       const int cmin = a.causal ? (krow - i0) : -1;
       const bool need_mask = cmin > 0;
-      uint32_t pk[16], dk[16];
+      uint32_t pk[8], dk[8];
       const uint64_t sl2x2 = f2_make(sl2, sl2);
-      // (-lse2, -delta) of this half's 32 queries, two per float4.
-      const float4* st4 = reinterpret_cast<const float4*>(stage_rows(s)) + half * 16;
+      // (-lse2, -delta) of this group's 16 queries, two per float4.
+      const float4* st4 = reinterpret_cast<const float4*>(stage_rows(s)) + grp * 8;
 #pragma unroll
-      for (int c2 = 0; c2 < 16; ++c2) {
+      for (int c2 = 0; c2 < 8; ++c2) {
         const int c = 2 * c2;
         const float4 rs = st4[c2];  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
         const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
@@ -361,35 +378,37 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         pk[c2] = pack_bf16x2(p0, p1);
         dk[c2] = pack_bf16x2(d0, d1);
       }
-      tmem_st16_nowait(tS, pk);
-      tmem_st16_nowait(tDP, dk);
+      tmem_st8_nowait(tS, pk);
+      tmem_st8_nowait(tDP, dk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDkvBarP));
+      if (lane == 0) mbar_arrive(bar(kDkvBarP + (li & 1)));
     }
     if (ok) ok = warp_all(mbar_wait(bar(kDkvBarAcc), 0, wait_ns));
     if (ok && C > 1) {
       // Partial sums to this block's shared memory (fp32, row r = key row r,
-      // [dV | dK] = 2D floats per row, 16-byte chunks XOR-swizzled by r % 8).
+      // [dV | dK] = 2D floats per row, 16-byte chunks XOR-swizzled by r % 8);
+      // group grp writes columns grp*D/4 .. of both.
       tc_fence_after();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? Cf::kColDV : Cf::kColDK;
+        const uint32_t col = (which == 0 ? Cf::kColDV : Cf::kColDK) + grp * (D / 4);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
-          const int c = half * (D / 64) + cc;  // this half's 32-column chunks
-          uint32_t v[32];
+          uint32_t v[16];
           if (n_it > 0) {
-            tmem_ld32(tl + col + c * 32, v);
+            tmem_ld16_nowait(tl + col + cc * 16, v);
+            tmem_wait_ld();
+            reg_fence16(v);
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0u;
+            for (int i = 0; i < 16; ++i) v[i] = 0u;
           }
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int chunk = (which * D + c * 32) / 4 + i;
+          for (int i = 0; i < 4; ++i) {
+            const int chunk = (which * D + grp * (D / 4) + cc * 16) / 4 + i;
             st_shared_f4(s0 + partial_off(r, chunk),
                          make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
@@ -401,27 +420,26 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       tc_fence_after();
       const bool live = krow < a.T;
       const size_t rbase = ((static_cast<size_t>(b) * a.T + krow) * a.Hkv + g) * D;
-      __nv_bfloat16* dvrow = static_cast<__nv_bfloat16*>(a.dv) + rbase;
-      __nv_bfloat16* dkrow = static_cast<__nv_bfloat16*>(a.dk) + rbase;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = which == 0 ? Cf::kColDV : Cf::kColDK;
+        const uint32_t col = (which == 0 ? Cf::kColDV : Cf::kColDK) + grp * (D / 4);
         const float mul = which == 0 ? 1.f : a.scale;
-        __nv_bfloat16* dst_row = which == 0 ? dvrow : dkrow;
+        __nv_bfloat16* dst_row =
+            static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + rbase + grp * (D / 4);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
-          const int c = half * (D / 64) + cc;
-          uint32_t v[32];
-          tmem_ld32(tl + col + c * 32, v);
-          uint32_t pkd[16];
+          uint32_t v[16];
+          tmem_ld16_nowait(tl + col + cc * 16, v);
+          tmem_wait_ld();
+          reg_fence16(v);
+          uint32_t pkd[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
+          for (int i = 0; i < 8; ++i)
             pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
           if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+            uint4* dst = reinterpret_cast<uint4*>(dst_row + cc * 16);
+            dst[0] = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
+            dst[1] = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
           }
         }
       }
@@ -439,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       const int R = kTileN / C;
       constexpr int kCpr = 2 * D / 8;  // 8-float output chunks per row ([dV | dK])
       const int ct = static_cast<int>(threadIdx.x) - 64;
-      for (int e = ct; e < R * kCpr; e += 256) {
+      for (int e = ct; e < R * kCpr; e += kComputeWarps * 32) {
         const int rl = e / kCpr, oc = e % kCpr;
         const int row = crank * R + rl;
         float acc[8];
@@ -480,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
 }
 
 // ============================================================== dQ
+constexpr int kDqThreads = 320;  // producer, MMA issuer, 8 compute warps
 // Block = (b, query head, 128-query tile).  Warp 0 loads Q, dO once and the
 // K, V of 64-key tiles 0..diagonal in ascending order; warp 1 issues
 // S = Q K^T, dP = dO V^T and dQ += dS K with dS read from TMEM; warps 2..5
@@ -505,7 +524,7 @@ enum : int { kDqBarQ = 0, kDqBarKFull = 1, kDqBarVFull = 4, kDqBarKEmpty = 7, kD
              kDqBarS = 13, kDqBarDS = 14, kDqBarAcc = 15, kDqBarDrain = 16, kDqNumBars = 17 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kDqThreads, 2)
     attn_dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
                    const BwdArgs a) {
@@ -771,12 +790,12 @@ cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk
   cudaError_t e = set_smem_once(attn_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   if (a.cluster <= 1) {
-    attn_dkdv_kernel<D><<<grid, kThreads, DkvCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
+    attn_dkdv_kernel<D><<<grid, kBwdThreads, DkvCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kBwdThreads);
   cfg.dynamicSmemBytes = DkvCfg<D>::kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -798,7 +817,7 @@ cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
   static bool done[64] = {};
   cudaError_t e = set_smem_once(attn_dq_kernel<D>, DqCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
-  attn_dq_kernel<D><<<grid, kThreads, DqCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
+  attn_dq_kernel<D><<<grid, kDqThreads, DqCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
   return cudaGetLastError();
 }
 

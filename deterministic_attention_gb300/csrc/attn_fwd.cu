@@ -13,11 +13,15 @@
 //               the softmax works on S_j; then O += P_j V_j with P_j read from
 //               TMEM (bf16, written over S_j by the softmax warps)
 //   warps 2..9  softmax: two threads per query row (TMEM lane), each taking 32
-//               of the tile's 64 keys; online softmax in base 2 with a lazily
-//               moved row maximum, P to TMEM, O rescaled in TMEM when the
-//               maximum moves, epilogue O / l and LSE = ln2 * (m + log2 l)
-// Two blocks share an SM (256 TMEM columns each), so one block's prologue and
-// epilogue overlap the other's main loop.
+//               of the tile's 64 keys, each with its own running maximum, row
+//               sum and O accumulator (P of keys 0..31 of every tile goes to
+//               O_0, of keys 32..63 to O_1); online softmax in base 2 with a
+//               lazily moved maximum, P to TMEM, O_h rescaled in TMEM when its
+//               maximum moves.  The epilogue merges the two halves once:
+//               O = (O_0 2^(m_0-M) + O_1 2^(m_1-M)) / (l_0 2^(m_0-M) + l_1 2^(m_1-M)),
+//               M = max(m_0, m_1), LSE = ln2 * (M + log2 L).
+// For D = 64 two blocks share an SM (256 TMEM columns each), so one block's
+// prologue and epilogue overlap the other's main loop.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -58,12 +62,12 @@ struct Cfg {
   static constexpr int kOffK = kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKvBytes;
   static constexpr int kSmemBytes = kOffV + kStages * kKvBytes + 1024;  // + alignment slack
-  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;
   // Two score buffers of 64 fp32 columns (buffer b at 64 b).  The softmax
   // thread of half h owns columns 32h..32h+31 of a buffer and writes its 32
   // bf16 P values, packed in pairs, over the first 16 of them.
   static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColO = 128;  // O accumulator, D cols
+  static constexpr uint32_t kColO = 128;  // O_h accumulator at 128 + D h, D cols each
 };
 
 constexpr int kMaxStages = 4;
@@ -86,7 +90,7 @@ __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffff
 
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const FwdArgs a) {
   using C = Cfg<D>;
@@ -94,8 +98,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[kNumBars];
   __shared__ uint32_t tmem_slot;
-  __shared__ float red_max[2][2][kTileM];  // [tile parity][half][row] partial maxima
-  __shared__ float red_l[2][kTileM];       // [half][row] partial row sums
+  __shared__ float red_m[2][kTileM];  // [half][row] final running maxima (log2 units)
+  __shared__ float red_l[2][kTileM];  // [half][row] final row sums
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Heaviest query tiles (most key tiles under the causal mask) are handed out first.
@@ -219,12 +223,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_after();
         const uint64_t dV = desc_add(dV0, s * C::kKvBytes);
         const uint32_t tP = tmem + C::kColS + (j & 1) * kBN;
-        // P of keys 16ks..16ks+15: half ks/2 wrote its 32 keys as 16 packed
-        // columns at the start of its own 32 score columns.
+        // O_h += P_h V_h over the 32 keys of half h: half h wrote them as 16
+        // packed columns at the start of its own 32 score columns.
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks)
-          mma_ts(tmem + C::kColO, tP + (ks >> 1) * 32 + (ks & 1) * 8, desc_add(dV, ks * 2048),
-                 kIdPV, (j > 0 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const int hh = ks >> 1;
+          mma_ts(tmem + C::kColO + hh * D, tP + hh * 32 + (ks & 1) * 8, desc_add(dV, ks * 2048),
+                 kIdPV, (j > 0 || (ks & 1)) ? 1u : 0u);
+        }
         mma_commit(bar(kBarVEmpty + s));
         mma_commit(bar(kBarO));
       }
@@ -239,10 +245,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else {
     // ------------------------------------------------------------ softmax warps
     // Warps w and w+4 share TMEM lane quarter (w & 3), i.e. the same 32 query
-    // rows; half 0 takes keys 0..31 of each tile, half 1 keys 32..63.  The two
-    // halves of a row trade partial row maxima through shared memory, meeting
-    // at an mbarrier of the pair (64 arrivals, bounded wait) once per tile;
-    // the row sums stay split until the epilogue.
+    // rows; half 0 takes keys 0..31 of each tile, half 1 keys 32..63.  Each
+    // half runs its own online softmax into its own accumulator O_h; the two
+    // meet once, in the epilogue, at an mbarrier of the pair (64 arrivals,
+    // bounded wait).
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
@@ -269,18 +275,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int c = 0; c < 32; ++c)
           if (c > lim) sr[c] = __float_as_uint(-INFINITY);
       }
-      // Partial maximum over 32 columns in four independent chains.
+      // Maximum over this half's 32 columns in four independent chains.
       float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 16; ++c)
         mx4[c & 3] = fmax3(mx4[c & 3], __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
-      red_max[j & 1][half][r] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      mbar_arrive(pair_bar);
-      ok = warp_all(mbar_wait(pair_bar, j & 1, wait_ns));
-      if (!ok) break;
-      const float mx = fmaxf(red_max[j & 1][0][r], red_max[j & 1][1][r]);
-      // A row may see no key in this tile (the half-tile past its diagonal):
-      // mx = -inf leaves the running maximum alone and every P zero.
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      // A half-row may see no key in this tile (past its diagonal): mx = -inf
+      // leaves the running maximum alone and every P zero.
       const float m_new = mx * sl2;
       float alpha = 1.f;
       bool moved = false;
@@ -315,17 +317,17 @@ __global__ void __launch_bounds__(kThreads, 2)
       tmem_st16_nowait(tS, pk);
       tmem_wait_st();
       if (j > 0 && __any_sync(0xffffffffu, moved)) {
-        // O holds the sum over earlier tiles scaled by the old maximum: wait for
-        // the last P V to land, then rescale this half's O columns in TMEM.
-        // (S_j was committed after P_{j-2} V, so the O barrier is at most one
-        // phase behind here and the parity wait is exact.)
+        // O_h holds the sum over earlier tiles scaled by the old maximum: wait
+        // for the last P V to land, then rescale O_h in TMEM.  (S_j was
+        // committed after P_{j-2} V, so the O barrier is at most one phase
+        // behind here and the parity wait is exact.)
         ok = warp_all(mbar_wait(bar(kBarO), (j - 1) & 1, wait_ns));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
-          const uint32_t col = C::kColO + half * (D / 2) + c * 32;
+          const uint32_t col = C::kColO + half * D + c * 32;
           tmem_ld32(tl + col, ov);
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
@@ -342,26 +344,35 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (lane == 0) mbar_arrive(bar(kBarP + (j & 1)));
     }
     if (ok) ok = warp_all(mbar_wait(bar(kBarOFinal), 0, wait_ns));
-    // Row sum = half 0's part + half 1's part, in that order.
+    // Merge the two halves: M = max(m_0, m_1), f_h = 2^(m_h - M),
+    // L = l_0 f_0 + l_1 f_1 (half 0 first), O = (O_0 f_0 + O_1 f_1) / L.
+    red_m[half][r] = m_run;
     red_l[half][r] = l_run;
     mbar_arrive(pair_bar);
-    if (ok) ok = warp_all(mbar_wait(pair_bar, n_kv & 1, wait_ns));
+    if (ok) ok = warp_all(mbar_wait(pair_bar, 0, wait_ns));
     if (ok) {
       tc_fence_after();
-      const float l_tot = red_l[0][r] + red_l[1][r];
+      const float m0v = red_m[0][r], m1v = red_m[1][r];
+      const float M = fmaxf(m0v, m1v);  // finite: key 0 is visible to every row
+      const float f0 = ex2_approx(m0v - M), f1 = ex2_approx(m1v - M);
+      const float l_tot = red_l[0][r] * f0 + red_l[1][r] * f1;
       const float inv_l = 1.f / l_tot;
+      const float w0 = f0 * inv_l, w1 = f1 * inv_l;
       const bool live = qrow < a.T;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
                             ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * D + half * (D / 2);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        uint32_t ov[32];
-        tmem_ld32(tl + C::kColO + half * (D / 2) + c * 32, ov);
+        uint32_t o0[32], o1[32];
+        const uint32_t col = half * (D / 2) + c * 32;
+        tmem_ld32(tl + C::kColO + col, o0);
+        tmem_ld32(tl + C::kColO + D + col, o1);
         uint32_t pkd[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
-                               __uint_as_float(ov[2 * i + 1]) * inv_l);
+          pkd[i] = pack_bf16x2(
+              fmaf(__uint_as_float(o0[2 * i]), w0, __uint_as_float(o1[2 * i]) * w1),
+              fmaf(__uint_as_float(o0[2 * i + 1]), w0, __uint_as_float(o1[2 * i + 1]) * w1));
         if (live) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
@@ -371,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (live && half == 0)
         a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + qrow] =
-            (m_run + log2f(l_tot)) * 0.69314718055994530942f;
+            (M + log2f(l_tot)) * 0.69314718055994530942f;
     }
   }
 

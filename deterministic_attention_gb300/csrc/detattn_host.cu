@@ -198,7 +198,7 @@ int dkdv_cluster_size(int B, int T, int Hq, int Hkv, int D, int causal, int sms)
   for (int nt = 0; nt < n_tiles; ++nt) total += m_end - (causal ? nt * kTileN / kDkvTileM : 0);
   total *= static_cast<double>(B) * Hkv * G;
   const double max_items = static_cast<double>(G) * m_end;
-  const double slots = static_cast<double>(sms) * (D == 64 ? 2 : 1);
+  const double slots = static_cast<double>(sms);  // one dK/dV block per SM
   const double avg = total / slots;
   int c = 1;
   while (c < 8 && max_items / c > 1.5 * avg && 2 * c <= max_items) c *= 2;
