@@ -154,9 +154,9 @@ class Problem:
         return sum(t.numel() * t.element_size() for t in list(ins) + list(outs.values()))
 
     def step(self, s):
-        """fwd + bwd on set s (the four kernels of the hot path)."""
-        for which in ("fwd", "delta", "dkdv", "dq"):
-            self.kernel(which, s)
+        """fwd + bwd on set s through the public API: attn_fwd, then attn_bwd
+        (Delta, then dK/dV and dQ on two streams)."""
+        self.step_api(s)
 
     def kernel(self, which, s):
         """One kernel of the step on set s (for per-kernel timing)."""
@@ -375,7 +375,8 @@ def run_gpu_arm(args, world, rank):
                    "dout_std": w.dout_std,
                    "l2": f"{n_sets} rotating input/output sets of {per_set / 2**20:.1f} MiB "
                          f"({n_sets * per_set / 2**20:.0f} MiB vs 129 MiB L2)",
-                   "launch": f"CUDA graph of {n_sets} steps x 4 kernels, replayed {replays}x",
+                   "launch": f"CUDA graph of {n_sets} steps (attn_fwd + attn_bwd, 4 kernels each), "
+                             f"replayed {replays}x",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "flop_convention": "fwd 2*B*Hq*T^2*D (causal half), fwd+bwd 3.5x fwd"},
         "pct_of_peak": value / world / peak,

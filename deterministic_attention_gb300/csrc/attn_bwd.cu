@@ -132,6 +132,12 @@ struct DkvCfg {
   // (dS^T) values as 8 packed bf16 pairs over columns 16g..16g+7 of S^T (dP^T).
   static constexpr uint32_t kColDV = 256;      // dV accumulator, D cols
   static constexpr uint32_t kColDK = 256 + D;  // dK accumulator, D cols
+  // For D = 64 the block's K and V tiles also live in TMEM (as packed bf16
+  // pairs, D/2 columns each), so S^T = K Q^T and dP^T = V dO^T read only Q / dO
+  // from shared memory.  For D = 128 TMEM is full and they stay in SMEM.
+  static constexpr bool kKvInTmem = (D == 64);
+  static constexpr uint32_t kColK = 256 + 2 * D;
+  static constexpr uint32_t kColV = kColK + D / 2;
 };
 static_assert(kTileN * 2 * 64 * 4 <= DkvCfg<64>::kSmemBytes - 1024, "dK/dV partials fit");
 static_assert(kTileN * 2 * 128 * 4 <= DkvCfg<128>::kSmemBytes - 1024, "dK/dV partials fit");
@@ -145,7 +151,8 @@ enum : int {
   kDkvBarP = kDkvBarS + 2,                   // [2]
   kDkvBarAcc = kDkvBarP + 2,
   kDkvBarDrain = kDkvBarAcc + 1,
-  kDkvNumBars = kDkvBarDrain + 1
+  kDkvBarKvTmem = kDkvBarDrain + 1,  // compute warps copied K, V into TMEM
+  kDkvNumBars = kDkvBarKvTmem + 1
 };
 
 template <int D>
@@ -212,6 +219,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(bar(kDkvBarAcc), 1);
     mbar_init(bar(kDkvBarDrain), 1);
+    mbar_init(bar(kDkvBarKvTmem), kComputeWarps);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -283,18 +291,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
           const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-          mma_ss(tS, desc_add(dK, okv), desc_add(dQk, oq), kIdS, ks > 0);
+          if (Cf::kKvInTmem)
+            mma_ts(tS, tmem + Cf::kColK + ks * 8, desc_add(dQk, oq), kIdS, ks > 0);
+          else
+            mma_ss(tS, desc_add(dK, okv), desc_add(dQk, oq), kIdS, ks > 0);
         }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
           const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-          mma_ss(tDP, desc_add(dV, okv), desc_add(ddOk, oq), kIdS, ks > 0);
+          if (Cf::kKvInTmem)
+            mma_ts(tDP, tmem + Cf::kColV + ks * 8, desc_add(ddOk, oq), kIdS, ks > 0);
+          else
+            mma_ss(tDP, desc_add(dV, okv), desc_add(ddOk, oq), kIdS, ks > 0);
         }
         mma_commit(bar(kDkvBarS + (li & 1)));
         return true;
       };
       ok = mbar_wait(bar(kDkvBarKV), 0, wait_ns);
+      if (ok && Cf::kKvInTmem) ok = mbar_wait(bar(kDkvBarKvTmem), 0, wait_ns);
       tc_fence_after();
       if (ok && n_it > 0) ok = issue_st(0);
       for (int li = 0; li < n_it && ok; ++li) {
@@ -332,7 +347,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int krow = n0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
-    for (int li = 0; li < n_it; ++li) {
+    if (Cf::kKvInTmem) {
+      // K and V rows r into TMEM as the A operand of S^T and dP^T: this
+      // thread copies elements 16 grp..16 grp+15 (two 16-byte chunks of the
+      // 128-byte-swizzled tile row) as 8 packed pairs.
+      ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
+      if (ok) {
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t base = (which == 0 ? sK : sV) + r * 128;
+          uint32_t v8[8];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint4 x = ld_shared_u4(base + (((2 * grp + c) ^ (r & 7)) * 16));
+            v8[4 * c] = x.x;
+            v8[4 * c + 1] = x.y;
+            v8[4 * c + 2] = x.z;
+            v8[4 * c + 3] = x.w;
+          }
+          tmem_st8_nowait(tl + (which == 0 ? Cf::kColK : Cf::kColV) + grp * 8, v8);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDkvBarKvTmem));
+    }
+    for (int li = 0; li < n_it && ok; ++li) {
       const int it = it_lo + li;
       const int s = li % NS;
       const int i0 = (m_begin + it % per_head) * kDkvTileM + grp * 16;  // this group's first query
@@ -352,11 +393,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t pk[8], dk[8];
       const uint64_t sl2x2 = f2_make(sl2, sl2);
       // (-lse2, -delta) of this group's 16 queries, two per float4.
-      const float4* st4 = reinterpret_cast<const float4*>(stage_rows(s)) + grp * 8;
+      const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * 8 * 16;
 #pragma unroll
       for (int c2 = 0; c2 < 8; ++c2) {
         const int c = 2 * c2;
-        const float4 rs = st4[c2];  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
+        const float4 rs = ld_shared_f4(st4 + c2 * 16);  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
         const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
                                   sl2x2, f2_make(rs.x, rs.z));
         float x0, x1, p0, p1;

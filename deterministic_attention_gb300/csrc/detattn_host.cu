@@ -254,6 +254,62 @@ int check_workspace(const void* ws, size_t bytes, int B, int T, int Hq) {
   return DETATTN_OK;
 }
 
+// ------------------------------------------------------------ side stream
+// attn_bwd runs dK/dV and dQ, which both need only the Delta step's output,
+// on two streams: dQ on a per-device side stream forked from the caller's
+// stream after Delta and joined back before attn_bwd returns.  The two grids
+// then fill each other's idle SMs.  Stream capture records the fork and join
+// as graph edges.  The side stream and events are created on first use.
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+int side_stream(SideStream** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  static SideStream per_dev[64];
+  static std::mutex mu;
+  if (dev >= 64) return fail(DETATTN_ERR_CUDA, "device index %d too large", dev);
+  std::lock_guard<std::mutex> lock(mu);
+  SideStream& ss = per_dev[dev];
+  if (ss.stream == nullptr) {
+    e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      ss = SideStream{};
+      return fail(DETATTN_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
+    }
+  }
+  *out = &ss;
+  return DETATTN_OK;
+}
+
+// Delta, then dK/dV on `st` and dQ on the side stream.
+int bwd_steps(const void* q, const void* k, const void* v, const void* o, const float* lse,
+              const void* dout, void* dq, void* dk, void* dv, void* ws, int B, int T, int Hq,
+              int Hkv, int D, float scale, int causal, cudaStream_t st) {
+  int rc;
+  if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, st)) != DETATTN_OK) return rc;
+  SideStream* ss = nullptr;
+  if ((rc = side_stream(&ss)) != DETATTN_OK) return rc;
+  cudaError_t e = cudaEventRecord(ss->fork, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->fork, 0);
+  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "fork: %s", cudaGetErrorString(e));
+  if ((rc = dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, ss->stream)) !=
+      DETATTN_OK)
+    return rc;
+  if ((rc = dkdv_impl(q, k, v, dout, ws, dk, dv, B, T, Hq, Hkv, D, scale, causal, st)) !=
+      DETATTN_OK)
+    return rc;
+  e = cudaEventRecord(ss->join, ss->stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->join, 0);
+  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "join: %s", cudaGetErrorString(e));
+  return ok_status();
+}
+
 // ------------------------------------------------------------ built-in scratch
 // Row statistics for attn_bwd_noalloc: a file-scope device array, so callers
 // that cannot allocate device memory still get the backward.  Every GPU that
@@ -367,12 +423,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
     return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, B, T, Hq)) != DETATTN_OK) return rc;
   if ((rc = check_device()) != DETATTN_OK) return rc;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if ((rc = delta_impl(o, dout, lse, workspace, B, T, Hq, D, st)) != DETATTN_OK) return rc;
-  if ((rc = dkdv_impl(q, k, v, dout, workspace, dk, dv, B, T, Hq, Hkv, D, scale, causal, st)) !=
-      DETATTN_OK)
-    return rc;
-  return dq_impl(q, k, v, dout, workspace, dq, B, T, Hq, Hkv, D, scale, causal, st);
+  return bwd_steps(q, k, v, o, lse, dout, dq, dk, dv, workspace, B, T, Hq, Hkv, D, scale, causal,
+                   static_cast<cudaStream_t>(stream));
 }
 
 int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -83,8 +83,11 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
 
 /* Backward.  Given q, k, v, the forward's o and lse, and dout, writes dq, dk,
- * dv (bf16).  Runs attn_bwd_delta, attn_bwd_dkdv and attn_bwd_dq in that
- * order on `stream`.  `workspace` (>= attn_bwd_workspace_bytes, 16-byte
+ * dv (bf16).  Runs attn_bwd_delta on `stream`, then attn_bwd_dkdv on `stream`
+ * and attn_bwd_dq concurrently on a library-owned side stream (forked from
+ * `stream` after the Delta step with an event and joined back before the call
+ * returns; created on the first call per device), so all work is ordered
+ * after earlier work on `stream` and later work on `stream` sees the results.  `workspace` (>= attn_bwd_workspace_bytes, 16-byte
  * aligned, caller-owned, contents on entry irrelevant) holds the row
  * statistics.  Passage: "Step 2: fused flash attention" and "Where the time
  * goes now" (the flash_attention_dkv kernel) on the RustingBrain page. */
