@@ -271,7 +271,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (MMA issue is warp-collective); every
+    // wait is made warp-uniform so the warp stays converged.
+    {
       const uint32_t tDV = tmem + Cf::kColDV, tDK = tmem + Cf::kColDK;
       constexpr uint32_t kIdS = idesc_bf16(kTileN, kDkvTileM, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // S^T, dP^T of item li into buffer li & 1.
       auto issue_st = [&](int li) -> bool {
         const int s = li % NS;
-        if (!mbar_wait(bar(kDkvBarQFull + s), (li / NS) & 1, wait_ns)) return false;
+        if (!warp_all(mbar_wait(bar(kDkvBarQFull + s), (li / NS) & 1, wait_ns))) return false;
         tc_fence_after();
         const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
         const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
@@ -308,8 +310,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mma_commit(bar(kDkvBarS + (li & 1)));
         return true;
       };
-      ok = mbar_wait(bar(kDkvBarKV), 0, wait_ns);
-      if (ok && Cf::kKvInTmem) ok = mbar_wait(bar(kDkvBarKvTmem), 0, wait_ns);
+      ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
+      if (ok && Cf::kKvInTmem) ok = warp_all(mbar_wait(bar(kDkvBarKvTmem), 0, wait_ns));
       tc_fence_after();
       if (ok && n_it > 0) ok = issue_st(0);
       for (int li = 0; li < n_it && ok; ++li) {
@@ -317,7 +319,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // the compute warps work on item li.
         if (li + 1 < n_it && !(ok = issue_st(li + 1))) break;
         const int s = li % NS;
-        if (!(ok = mbar_wait(bar(kDkvBarP + (li & 1)), (li >> 1) & 1, wait_ns))) break;
+        if (!(ok = warp_all(mbar_wait(bar(kDkvBarP + (li & 1)), (li >> 1) & 1, wait_ns)))) break;
         tc_fence_after();
         const uint64_t dQm = desc_add(dQm0, s * Cf::kStageBytes);
         const uint64_t ddOm = desc_add(dQm, Cf::kQBytes);
@@ -334,7 +336,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       mma_commit(bar(kDkvBarAcc));
       mma_commit(bar(kDkvBarDrain));
-      mbar_wait(bar(kDkvBarDrain), 0, wait_ns);
+      warp_all(mbar_wait(bar(kDkvBarDrain), 0, wait_ns));
     }
   } else {
     // ------------------------------------------------------------ P^T / dS^T warps
@@ -655,7 +657,9 @@ __global__ void __launch_bounds__(kDqThreads, 2)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    // MMA issuer: the whole warp runs the loop (MMA issue is warp-collective);
+    // every wait is made warp-uniform so the warp stays converged.
+    {
       const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ;
       constexpr uint32_t kIdS = idesc_bf16(kTileM, kDqTileN, false, false);
       constexpr uint32_t kIdDQ = idesc_bf16(kTileM, D, false, true);
@@ -663,14 +667,14 @@ __global__ void __launch_bounds__(kDqThreads, 2)
       const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), ddO = sdesc_sw128(sdO, 16, 1024);
       const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024), dV0 = sdesc_sw128(sV0, 16, 1024);
       const uint64_t dKm0 = sdesc_sw128(sK0, kDqTileN * 128, 1024);  // K as MN-major B
-      ok = mbar_wait(bar(kDqBarQ), 0, wait_ns);
+      ok = warp_all(mbar_wait(bar(kDqBarQ), 0, wait_ns));
       tc_fence_after();
       for (int j = 0; j < n_kv && ok; ++j) {
         const int s = j % NS;
         const uint32_t ph = (j / NS) & 1;
         const uint64_t dK = desc_add(dK0, s * C::kKvBytes), dV = desc_add(dV0, s * C::kKvBytes);
         const uint64_t dKm = desc_add(dKm0, s * C::kKvBytes);
-        if (!(ok = mbar_wait(bar(kDqBarKFull + s), ph, wait_ns))) break;
+        if (!(ok = warp_all(mbar_wait(bar(kDqBarKFull + s), ph, wait_ns)))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -678,7 +682,7 @@ __global__ void __launch_bounds__(kDqThreads, 2)
           const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
           mma_ss(tS, desc_add(dQ, oq), desc_add(dK, okv), kIdS, ks > 0);
         }
-        if (!(ok = mbar_wait(bar(kDqBarVFull + s), ph, wait_ns))) break;
+        if (!(ok = warp_all(mbar_wait(bar(kDqBarVFull + s), ph, wait_ns)))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -688,7 +692,7 @@ __global__ void __launch_bounds__(kDqThreads, 2)
         }
         mma_commit(bar(kDqBarS));
         mma_commit(bar(kDqBarVEmpty + s));
-        if (!(ok = mbar_wait(bar(kDqBarDS), j & 1, wait_ns))) break;
+        if (!(ok = warp_all(mbar_wait(bar(kDqBarDS), j & 1, wait_ns)))) break;
         tc_fence_after();
         // dS of keys 16ks..16ks+15: half ks/2 wrote its 32 keys as 16 packed
         // columns at the start of its own 32 S columns.
@@ -700,7 +704,7 @@ __global__ void __launch_bounds__(kDqThreads, 2)
       }
       mma_commit(bar(kDqBarAcc));
       mma_commit(bar(kDqBarDrain));
-      mbar_wait(bar(kDqBarDrain), 0, wait_ns);
+      warp_all(mbar_wait(bar(kDqBarDrain), 0, wait_ns));
     }
   } else {
     // Eight warps: warps w and w+4 share TMEM lane quarter (w & 3), i.e. the

@@ -187,7 +187,9 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (MMA issue is warp-collective); every
+    // wait is made warp-uniform so the warp stays converged.
+    {
       constexpr uint32_t kIdQK = idesc_bf16(kTileM, kBN, false, false);
       constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, false, true);
       // Operand descriptors built once; the loops only add constant offsets.
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       // S_j = Q K_j^T into score buffer j & 1.
       auto issue_qk = [&](int j) -> bool {
         const int s = j % NS;
-        if (!mbar_wait(bar(kBarKFull + s), (j / NS) & 1, wait_ns)) return false;
+        if (!warp_all(mbar_wait(bar(kBarKFull + s), (j / NS) & 1, wait_ns))) return false;
         tc_fence_after();
         const uint64_t dK = desc_add(dK0, s * C::kKvBytes);
         const uint32_t tS = tmem + C::kColS + (j & 1) * kBN;
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         mma_commit(bar(kBarKEmpty + s));
         return true;
       };
-      ok = mbar_wait(bar(kBarQ), 0, wait_ns);
+      ok = warp_all(mbar_wait(bar(kBarQ), 0, wait_ns));
       tc_fence_after();
       if (ok && n_kv > 0) ok = issue_qk(0);
       for (int j = 0; j < n_kv && ok; ++j) {
@@ -218,8 +220,8 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         // in the previous iteration (tcgen05 operations run in issue order).
         if (j + 1 < n_kv && !(ok = issue_qk(j + 1))) break;
         const int s = j % NS;
-        if (!(ok = mbar_wait(bar(kBarP + (j & 1)), (j >> 1) & 1, wait_ns))) break;
-        if (!(ok = mbar_wait(bar(kBarVFull + s), (j / NS) & 1, wait_ns))) break;
+        if (!(ok = warp_all(mbar_wait(bar(kBarP + (j & 1)), (j >> 1) & 1, wait_ns)))) break;
+        if (!(ok = warp_all(mbar_wait(bar(kBarVFull + s), (j / NS) & 1, wait_ns)))) break;
         tc_fence_after();
         const uint64_t dV = desc_add(dV0, s * C::kKvBytes);
         const uint32_t tP = tmem + C::kColS + (j & 1) * kBN;
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       mma_commit(bar(kBarOFinal));
       // Every issued MMA must finish before TMEM is released.
       mma_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, wait_ns);
+      warp_all(mbar_wait(bar(kBarDrain), 0, wait_ns));
     }
   } else {
     // ------------------------------------------------------------ softmax warps
