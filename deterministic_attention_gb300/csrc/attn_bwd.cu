@@ -393,19 +393,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int cmin = a.causal ? (krow - i0) : -1;
       const bool need_mask = cmin > 0;
       uint32_t pk[8], dk[8];
-      const uint64_t sl2x2 = f2_make(sl2, sl2);
       // (-lse2, -delta) of this group's 16 queries, two per float4.
       const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * 8 * 16;
 #pragma unroll
       for (int c2 = 0; c2 < 8; ++c2) {
         const int c = 2 * c2;
         const float4 rs = ld_shared_f4(st4 + c2 * 16);  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
-        const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
-                                  sl2x2, f2_make(rs.x, rs.z));
-        float x0, x1, p0, p1;
-        f2_split(x, x0, x1);
+        const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rs.x);
+        const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rs.z);
+        float p0, p1;
         if ((c2 & 7) < kPolyOf8) {
-          exp2_poly2(x0, x1, p0, p1);
+          p0 = exp2_poly(x0);
+          p1 = exp2_poly(x1);
         } else {
           p0 = ex2_approx(x0);
           p1 = ex2_approx(x1);
@@ -414,10 +413,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (c < cmin) p0 = 0.f;
           if (c + 1 < cmin) p1 = 0.f;
         }
-        const uint64_t dpm = f2_add(f2_make(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
-                                    f2_make(rs.y, rs.w));
-        float d0, d1;
-        f2_split(f2_mul(f2_make(p0, p1), dpm), d0, d1);
+        const float d0 = p0 * (__uint_as_float(dp[c]) + rs.y);
+        const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rs.w);
         pk[c2] = pack_bf16x2(p0, p1);
         dk[c2] = pack_bf16x2(d0, d1);
       }
@@ -561,10 +558,18 @@ struct DqCfg {
   static constexpr uint32_t kColS = 0;    // S fp32 [128 x 64]; dS bf16 over cols 0..31
   static constexpr uint32_t kColDP = 64;  // dP fp32 [128 x 64]
   static constexpr uint32_t kColDQ = 128; // dQ accumulator, D cols
+  // For D = 64 the block's Q and dO tiles also live in TMEM (packed bf16
+  // pairs, 32 columns each), so S = Q K^T and dP = dO V^T read only K / V from
+  // shared memory: an N = 64 MMA with both operands in shared memory is bound
+  // by shared-memory bandwidth (48 clocks against 32 for the math).
+  static constexpr bool kQInTmem = (D == 64);
+  static constexpr uint32_t kColQ = 192;
+  static constexpr uint32_t kColdO = 224;
 };
 
 enum : int { kDqBarQ = 0, kDqBarKFull = 1, kDqBarVFull = 4, kDqBarKEmpty = 7, kDqBarVEmpty = 10,
-             kDqBarS = 13, kDqBarDS = 14, kDqBarAcc = 15, kDqBarDrain = 16, kDqNumBars = 17 };
+             kDqBarS = 13, kDqBarDS = 14, kDqBarAcc = 15, kDqBarDrain = 16, kDqBarQTmem = 17,
+             kDqNumBars = 18 };
 
 template <int D>
 __global__ void __launch_bounds__(kDqThreads, 2)
@@ -610,6 +615,7 @@ __global__ void __launch_bounds__(kDqThreads, 2)
     mbar_init(bar(kDqBarDS), 8);
     mbar_init(bar(kDqBarAcc), 1);
     mbar_init(bar(kDqBarDrain), 1);
+    mbar_init(bar(kDqBarQTmem), 8);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -668,6 +674,7 @@ __global__ void __launch_bounds__(kDqThreads, 2)
       const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024), dV0 = sdesc_sw128(sV0, 16, 1024);
       const uint64_t dKm0 = sdesc_sw128(sK0, kDqTileN * 128, 1024);  // K as MN-major B
       ok = warp_all(mbar_wait(bar(kDqBarQ), 0, wait_ns));
+      if (ok && C::kQInTmem) ok = warp_all(mbar_wait(bar(kDqBarQTmem), 0, wait_ns));
       tc_fence_after();
       for (int j = 0; j < n_kv && ok; ++j) {
         const int s = j % NS;
@@ -680,7 +687,10 @@ __global__ void __launch_bounds__(kDqThreads, 2)
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
           const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
-          mma_ss(tS, desc_add(dQ, oq), desc_add(dK, okv), kIdS, ks > 0);
+          if (C::kQInTmem)
+            mma_ts(tS, tmem + C::kColQ + ks * 8, desc_add(dK, okv), kIdS, ks > 0);
+          else
+            mma_ss(tS, desc_add(dQ, oq), desc_add(dK, okv), kIdS, ks > 0);
         }
         if (!(ok = warp_all(mbar_wait(bar(kDqBarVFull + s), ph, wait_ns)))) break;
         tc_fence_after();
@@ -688,7 +698,10 @@ __global__ void __launch_bounds__(kDqThreads, 2)
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
           const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
-          mma_ss(tDP, desc_add(ddO, oq), desc_add(dV, okv), kIdS, ks > 0);
+          if (C::kQInTmem)
+            mma_ts(tDP, tmem + C::kColdO + ks * 8, desc_add(dV, okv), kIdS, ks > 0);
+          else
+            mma_ss(tDP, desc_add(ddO, oq), desc_add(dV, okv), kIdS, ks > 0);
         }
         mma_commit(bar(kDqBarS));
         mma_commit(bar(kDqBarVEmpty + s));
@@ -720,7 +733,33 @@ __global__ void __launch_bounds__(kDqThreads, 2)
     const float sl2 = a.scale_log2;
     // (-LSE*log2e, -Delta) of this row; rows past T read (-inf, -0): P = 0.
     const float2 rstat = a.rowstats[(static_cast<size_t>(b) * a.Hq + h) * a.Tp + qrow];
-    for (int j = 0; j < n_kv; ++j) {
+    if (C::kQInTmem) {
+      // Q and dO row r into TMEM as the A operands of S and dP: this warp
+      // copies elements 32 half..32 half+31 (four 16-byte chunks of the
+      // 128-byte-swizzled tile row) as 16 packed pairs.
+      ok = warp_all(mbar_wait(bar(kDqBarQ), 0, wait_ns));
+      if (ok) {
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t base = (which == 0 ? sQ : sdO) + r * 128;
+          uint32_t v16[16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 x = ld_shared_u4(base + (((4 * half + c) ^ (r & 7)) * 16));
+            v16[4 * c] = x.x;
+            v16[4 * c + 1] = x.y;
+            v16[4 * c + 2] = x.z;
+            v16[4 * c + 3] = x.w;
+          }
+          tmem_st16_nowait(tl + (which == 0 ? C::kColQ : C::kColdO) + half * 16, v16);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDqBarQTmem));
+    }
+    for (int j = 0; j < n_kv && ok; ++j) {
       ok = warp_all(mbar_wait(bar(kDqBarS), j & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
@@ -734,18 +773,16 @@ __global__ void __launch_bounds__(kDqThreads, 2)
       // key kv0 + c visible iff c <= lim
       const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
       uint32_t dsk[16];
-      const uint64_t sl2x2 = f2_make(sl2, sl2), neg_l = f2_make(rstat.x, rstat.x);
-      const uint64_t neg_d = f2_make(rstat.y, rstat.y);
       const bool need_mask = a.causal ? (kv0 + 31 > m0) : (kv0 + 32 > a.T);
 #pragma unroll
       for (int c2 = 0; c2 < 16; ++c2) {
         const int c = 2 * c2;
-        const uint64_t x = f2_fma(f2_make(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])),
-                                  sl2x2, neg_l);
-        float x0, x1, p0, p1;
-        f2_split(x, x0, x1);
+        const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rstat.x);
+        const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rstat.x);
+        float p0, p1;
         if ((c2 & 7) < kPolyOf8) {
-          exp2_poly2(x0, x1, p0, p1);
+          p0 = exp2_poly(x0);
+          p1 = exp2_poly(x1);
         } else {
           p0 = ex2_approx(x0);
           p1 = ex2_approx(x1);
@@ -754,10 +791,8 @@ __global__ void __launch_bounds__(kDqThreads, 2)
           if (c > lim) p0 = 0.f;
           if (c + 1 > lim) p1 = 0.f;
         }
-        const uint64_t dpm = f2_add(f2_make(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])),
-                                    neg_d);
-        float d0, d1;
-        f2_split(f2_mul(f2_make(p0, p1), dpm), d0, d1);
+        const float d0 = p0 * (__uint_as_float(dp[c]) + rstat.y);
+        const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rstat.y);
         dsk[c2] = pack_bf16x2(d0, d1);
       }
       tmem_st16_nowait(tS, dsk);
