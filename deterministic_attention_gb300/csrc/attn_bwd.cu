@@ -289,23 +289,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
         const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
         const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
+        if (Cf::kKvInTmem) {
+          // K = 64 = D: four steps over the packed K / V columns and the
+          // 32-byte K-major slices of Q / dO.
+          const uint32_t aK = tmem + Cf::kColK, aV = tmem + Cf::kColV;
+          mma_ts_x4(tS, aK, aK + 8, aK + 16, aK + 24, dQk, desc_add(dQk, 32), desc_add(dQk, 64),
+                    desc_add(dQk, 96), kIdS, 0u);
+          mma_ts_x4(tDP, aV, aV + 8, aV + 16, aV + 24, ddOk, desc_add(ddOk, 32), desc_add(ddOk, 64),
+                    desc_add(ddOk, 96), kIdS, 0u);
+        } else {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
-          const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-          if (Cf::kKvInTmem)
-            mma_ts(tS, tmem + Cf::kColK + ks * 8, desc_add(dQk, oq), kIdS, ks > 0);
-          else
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
+            const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
             mma_ss(tS, desc_add(dK, okv), desc_add(dQk, oq), kIdS, ks > 0);
-        }
+          }
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
-          const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-          if (Cf::kKvInTmem)
-            mma_ts(tDP, tmem + Cf::kColV + ks * 8, desc_add(ddOk, oq), kIdS, ks > 0);
-          else
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
+            const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
             mma_ss(tDP, desc_add(dV, okv), desc_add(ddOk, oq), kIdS, ks > 0);
+          }
         }
         mma_commit(bar(kDkvBarS + (li & 1)));
         return true;
@@ -326,12 +330,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
         // P^T / dS^T of queries 16ks..16ks+15: group ks wrote them as 8 packed
         // columns at the start of its 16 S^T / dP^T columns.
-#pragma unroll
-        for (int ks = 0; ks < kDkvTileM / 16; ++ks) {
-          const uint32_t acc = (li > 0 || ks > 0) ? 1u : 0u;
-          mma_ts(tDV, tS + ks * 16, desc_add(ddOm, ks * 2048), kIdAcc, acc);
-          mma_ts(tDK, tDP + ks * 16, desc_add(dQm, ks * 2048), kIdAcc, acc);
-        }
+        static_assert(kDkvTileM == 64, "the dV / dK issue below takes 4 query steps");
+        mma_ts_x4(tDV, tS, tS + 16, tS + 32, tS + 48, ddOm, desc_add(ddOm, 2048),
+                  desc_add(ddOm, 4096), desc_add(ddOm, 6144), kIdAcc, li > 0 ? 1u : 0u);
+        mma_ts_x4(tDK, tDP, tDP + 16, tDP + 32, tDP + 48, dQm, desc_add(dQm, 2048),
+                  desc_add(dQm, 4096), desc_add(dQm, 6144), kIdAcc, li > 0 ? 1u : 0u);
         mma_commit(bar(kDkvBarQEmpty + s));
       }
       mma_commit(bar(kDkvBarAcc));
@@ -683,25 +686,31 @@ __global__ void __launch_bounds__(kDqThreads, 2)
         const uint64_t dKm = desc_add(dKm0, s * C::kKvBytes);
         if (!(ok = warp_all(mbar_wait(bar(kDqBarKFull + s), ph, wait_ns)))) break;
         tc_fence_after();
+        if (C::kQInTmem) {
+          const uint32_t aQ = tmem + C::kColQ;
+          mma_ts_x4(tS, aQ, aQ + 8, aQ + 16, aQ + 24, dK, desc_add(dK, 32), desc_add(dK, 64),
+                    desc_add(dK, 96), kIdS, 0u);
+        } else {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
-          const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
-          if (C::kQInTmem)
-            mma_ts(tS, tmem + C::kColQ + ks * 8, desc_add(dK, okv), kIdS, ks > 0);
-          else
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
+            const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
             mma_ss(tS, desc_add(dQ, oq), desc_add(dK, okv), kIdS, ks > 0);
+          }
         }
         if (!(ok = warp_all(mbar_wait(bar(kDqBarVFull + s), ph, wait_ns)))) break;
         tc_fence_after();
+        if (C::kQInTmem) {
+          const uint32_t adO = tmem + C::kColdO;
+          mma_ts_x4(tDP, adO, adO + 8, adO + 16, adO + 24, dV, desc_add(dV, 32), desc_add(dV, 64),
+                    desc_add(dV, 96), kIdS, 0u);
+        } else {
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
-          const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
-          if (C::kQInTmem)
-            mma_ts(tDP, tmem + C::kColdO + ks * 8, desc_add(dV, okv), kIdS, ks > 0);
-          else
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
+            const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
             mma_ss(tDP, desc_add(ddO, oq), desc_add(dV, okv), kIdS, ks > 0);
+          }
         }
         mma_commit(bar(kDqBarS));
         mma_commit(bar(kDqBarVEmpty + s));
@@ -709,10 +718,9 @@ __global__ void __launch_bounds__(kDqThreads, 2)
         tc_fence_after();
         // dS of keys 16ks..16ks+15: half ks/2 wrote its 32 keys as 16 packed
         // columns at the start of its own 32 S columns.
-#pragma unroll
-        for (int ks = 0; ks < kDqTileN / 16; ++ks)
-          mma_ts(tDQ, tS + (ks >> 1) * 32 + (ks & 1) * 8, desc_add(dKm, ks * 2048), kIdDQ,
-                 (j > 0 || ks > 0) ? 1u : 0u);
+        static_assert(kDqTileN == 64, "the dQ issue below takes 4 key steps");
+        mma_ts_x4(tDQ, tS, tS + 8, tS + 32, tS + 40, dKm, desc_add(dKm, 2048), desc_add(dKm, 4096),
+                  desc_add(dKm, 6144), kIdDQ, j > 0 ? 1u : 0u);
         mma_commit(bar(kDqBarKEmpty + s));
       }
       mma_commit(bar(kDqBarAcc));

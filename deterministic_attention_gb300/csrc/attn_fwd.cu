@@ -204,9 +204,11 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         const uint64_t dK = desc_add(dK0, s * C::kKvBytes);
         const uint32_t tS = tmem + C::kColS + (j & 1) * kBN;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          mma_ss(tS, desc_add(dQ, (ks >> 2) * (kTileM * 128) + (ks & 3) * 32),
-                 desc_add(dK, (ks >> 2) * (kBN * 128) + (ks & 3) * 32), kIdQK, ks > 0);
+        for (int g = 0; g < D / 64; ++g) {  // K = 64 per group of four steps
+          const uint64_t q = desc_add(dQ, g * (kTileM * 128)), k = desc_add(dK, g * (kBN * 128));
+          mma_ss_x4(tS, q, desc_add(q, 32), desc_add(q, 64), desc_add(q, 96), k, desc_add(k, 32),
+                    desc_add(k, 64), desc_add(k, 96), kIdQK, g > 0 ? 1u : 0u);
+        }
         mma_commit(bar(kBarS + (j & 1)));
         mma_commit(bar(kBarKEmpty + s));
         return true;
@@ -227,12 +229,12 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         const uint32_t tP = tmem + C::kColS + (j & 1) * kBN;
         // O_h += P_h V_h over the 32 keys of half h: half h wrote them as 16
         // packed columns at the start of its own 32 score columns.
+        static_assert(kBN == 64, "the P V issue below takes 2 steps per half");
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const int hh = ks >> 1;
-          mma_ts(tmem + C::kColO + hh * D, tP + hh * 32 + (ks & 1) * 8, desc_add(dV, ks * 2048),
-                 kIdPV, (j > 0 || (ks & 1)) ? 1u : 0u);
-        }
+        for (int hh = 0; hh < 2; ++hh)
+          mma_ts_x2(tmem + C::kColO + hh * D, tP + hh * 32, tP + hh * 32 + 8,
+                    desc_add(dV, (2 * hh) * 2048), desc_add(dV, (2 * hh + 1) * 2048), kIdPV,
+                    j > 0 ? 1u : 0u);
         mma_commit(bar(kBarVEmpty + s));
         mma_commit(bar(kBarO));
       }
