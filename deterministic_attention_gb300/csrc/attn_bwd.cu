@@ -107,13 +107,18 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
 // ============================================================== dK / dV
 // Block = (b, KV head, 128-key tile), or one of C blocks of a cluster sharing
 // that tile.  Warp 0 loads K, V once and then the (Q, dO, row statistics) of
-// 64-row query tiles of every query head in the group; warp 1 issues, one
-// query tile ahead, S^T = K Q^T and dP^T = V dO^T into the other of two TMEM
-// buffers, then dV += P^T dO and dK += dS^T Q with P^T and dS^T read from
-// TMEM; warps 2..17 turn S^T, dP^T into P^T, dS^T (four threads per key row,
-// 16 queries each).
-constexpr int kBwdThreads = 576;  // producer, MMA issuer, 16 compute warps
+// 64-row query tiles of every query head in the group; warp 1 issues
+// S^T = K Q^T and dP^T = V dO^T into two alternating TMEM buffers; warps
+// 2..17 turn S^T, dP^T into P^T, dS^T (four threads per key row, 16 queries
+// each); warp 18 issues dV += P^T dO and dK += dS^T Q with P^T and dS^T read
+// from TMEM.  With the two MMA streams in separate warps, S^T of the next
+// query tile is issued while the element-wise warps still work on this one,
+// without waiting behind the accumulate step: each issuing warp shares its
+// scheduler with four busy element-wise warps, so a single issuer running
+// both streams in turn was the critical path.
+constexpr int kBwdThreads = 608;  // producer, S issuer, 16 compute warps, dV/dK issuer
 constexpr int kComputeWarps = 16;
+constexpr int kDkvAccWarp = 2 + kComputeWarps;
 
 template <int D>
 struct DkvCfg {
@@ -152,7 +157,9 @@ enum : int {
   kDkvBarAcc = kDkvBarP + 2,
   kDkvBarDrain = kDkvBarAcc + 1,
   kDkvBarKvTmem = kDkvBarDrain + 1,  // compute warps copied K, V into TMEM
-  kDkvNumBars = kDkvBarKvTmem + 1
+  kDkvBarFree = kDkvBarKvTmem + 1,   // [2] dV, dK of the buffer's last item done
+  kDkvBarDrainAcc = kDkvBarFree + 2,
+  kDkvNumBars = kDkvBarDrainAcc + 1
 };
 
 template <int D>
@@ -220,6 +227,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(kDkvBarAcc), 1);
     mbar_init(bar(kDkvBarDrain), 1);
     mbar_init(bar(kDkvBarKvTmem), kComputeWarps);
+    mbar_init(bar(kDkvBarFree + 0), 1);
+    mbar_init(bar(kDkvBarFree + 1), 1);
+    mbar_init(bar(kDkvBarDrainAcc), 1);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -270,77 +280,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ S^T / dP^T issuer
     // The whole warp runs this loop (MMA issue is warp-collective); every
     // wait is made warp-uniform so the warp stays converged.
-    {
-      const uint32_t tDV = tmem + Cf::kColDV, tDK = tmem + Cf::kColDK;
-      constexpr uint32_t kIdS = idesc_bf16(kTileN, kDkvTileM, false, false);
-      constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
-      // Operand descriptors built once; the loops only add constant offsets.
-      const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
-      const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);                 // K-major B
-      const uint64_t dQm0 = sdesc_sw128(stage_base(0), kDkvTileM * 128, 1024);  // MN-major B
-      // S^T, dP^T of item li into buffer li & 1.
-      auto issue_st = [&](int li) -> bool {
-        const int s = li % NS;
-        if (!warp_all(mbar_wait(bar(kDkvBarQFull + s), (li / NS) & 1, wait_ns))) return false;
-        tc_fence_after();
-        const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
-        const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
-        const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
-        if (Cf::kKvInTmem) {
-          // K = 64 = D: four steps over the packed K / V columns and the
-          // 32-byte K-major slices of Q / dO.
-          const uint32_t aK = tmem + Cf::kColK, aV = tmem + Cf::kColV;
-          mma_ts_x4(tS, aK, aK + 8, aK + 16, aK + 24, dQk, desc_add(dQk, 32), desc_add(dQk, 64),
-                    desc_add(dQk, 96), kIdS, 0u);
-          mma_ts_x4(tDP, aV, aV + 8, aV + 16, aV + 24, ddOk, desc_add(ddOk, 32), desc_add(ddOk, 64),
-                    desc_add(ddOk, 96), kIdS, 0u);
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
-            const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-            mma_ss(tS, desc_add(dK, okv), desc_add(dQk, oq), kIdS, ks > 0);
-          }
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
-            const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-            mma_ss(tDP, desc_add(dV, okv), desc_add(ddOk, oq), kIdS, ks > 0);
-          }
-        }
-        mma_commit(bar(kDkvBarS + (li & 1)));
-        return true;
-      };
-      ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
-      if (ok && Cf::kKvInTmem) ok = warp_all(mbar_wait(bar(kDkvBarKvTmem), 0, wait_ns));
+    constexpr uint32_t kIdS = idesc_bf16(kTileN, kDkvTileM, false, false);
+    // Operand descriptors built once; the loop only adds constant offsets.
+    const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
+    const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);  // K-major B
+    ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
+    if (ok && Cf::kKvInTmem) ok = warp_all(mbar_wait(bar(kDkvBarKvTmem), 0, wait_ns));
+    tc_fence_after();
+    for (int li = 0; li < n_it && ok; ++li) {
+      const int s = li % NS;
+      // Buffer li & 1 last held item li - 2: its dV, dK must have read P^T,
+      // dS^T before S^T, dP^T of item li overwrite them.
+      if (li >= 2 && !(ok = warp_all(mbar_wait(bar(kDkvBarFree + (li & 1)), ((li - 2) >> 1) & 1,
+                                               wait_ns))))
+        break;
+      if (!(ok = warp_all(mbar_wait(bar(kDkvBarQFull + s), (li / NS) & 1, wait_ns)))) break;
       tc_fence_after();
-      if (ok && n_it > 0) ok = issue_st(0);
-      for (int li = 0; li < n_it && ok; ++li) {
-        // One item ahead: S^T, dP^T of item li+1 land in the other buffer while
-        // the compute warps work on item li.
-        if (li + 1 < n_it && !(ok = issue_st(li + 1))) break;
-        const int s = li % NS;
-        if (!(ok = warp_all(mbar_wait(bar(kDkvBarP + (li & 1)), (li >> 1) & 1, wait_ns)))) break;
-        tc_fence_after();
-        const uint64_t dQm = desc_add(dQm0, s * Cf::kStageBytes);
-        const uint64_t ddOm = desc_add(dQm, Cf::kQBytes);
-        const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
-        // P^T / dS^T of queries 16ks..16ks+15: group ks wrote them as 8 packed
-        // columns at the start of its 16 S^T / dP^T columns.
-        static_assert(kDkvTileM == 64, "the dV / dK issue below takes 4 query steps");
-        mma_ts_x4(tDV, tS, tS + 16, tS + 32, tS + 48, ddOm, desc_add(ddOm, 2048),
-                  desc_add(ddOm, 4096), desc_add(ddOm, 6144), kIdAcc, li > 0 ? 1u : 0u);
-        mma_ts_x4(tDK, tDP, tDP + 16, tDP + 32, tDP + 48, dQm, desc_add(dQm, 2048),
-                  desc_add(dQm, 4096), desc_add(dQm, 6144), kIdAcc, li > 0 ? 1u : 0u);
-        mma_commit(bar(kDkvBarQEmpty + s));
+      const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
+      const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
+      const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
+      if (Cf::kKvInTmem) {
+        // K = 64 = D: four steps over the packed K / V columns and the
+        // 32-byte K-major slices of Q / dO.
+        const uint32_t aK = tmem + Cf::kColK, aV = tmem + Cf::kColV;
+        mma_ts_x4(tS, aK, aK + 8, aK + 16, aK + 24, dQk, desc_add(dQk, 32), desc_add(dQk, 64),
+                  desc_add(dQk, 96), kIdS, 0u);
+        mma_ts_x4(tDP, aV, aV + 8, aV + 16, aV + 24, ddOk, desc_add(ddOk, 32), desc_add(ddOk, 64),
+                  desc_add(ddOk, 96), kIdS, 0u);
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
+          const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
+          mma_ss(tS, desc_add(dK, okv), desc_add(dQk, oq), kIdS, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
+          const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
+          mma_ss(tDP, desc_add(dV, okv), desc_add(ddOk, oq), kIdS, ks > 0);
+        }
       }
-      mma_commit(bar(kDkvBarAcc));
-      mma_commit(bar(kDkvBarDrain));
-      warp_all(mbar_wait(bar(kDkvBarDrain), 0, wait_ns));
+      mma_commit(bar(kDkvBarS + (li & 1)));
     }
+    // Every issued MMA must finish before TMEM is released.
+    mma_commit(bar(kDkvBarDrain));
+    warp_all(mbar_wait(bar(kDkvBarDrain), 0, wait_ns));
+  } else if (warp == kDkvAccWarp) {
+    // ------------------------------------------------------------ dV / dK issuer
+    constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
+    const uint32_t tDV = tmem + Cf::kColDV, tDK = tmem + Cf::kColDK;
+    const uint64_t dQm0 = sdesc_sw128(stage_base(0), kDkvTileM * 128, 1024);  // MN-major B
+    for (int li = 0; li < n_it && ok; ++li) {
+      const int s = li % NS;
+      if (!(ok = warp_all(mbar_wait(bar(kDkvBarP + (li & 1)), (li >> 1) & 1, wait_ns)))) break;
+      tc_fence_after();
+      const uint64_t dQm = desc_add(dQm0, s * Cf::kStageBytes);
+      const uint64_t ddOm = desc_add(dQm, Cf::kQBytes);
+      const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
+      // P^T / dS^T of queries 16ks..16ks+15: group ks wrote them as 8 packed
+      // columns at the start of its 16 S^T / dP^T columns.
+      static_assert(kDkvTileM == 64, "the dV / dK issue below takes 4 query steps");
+      mma_ts_x4(tDV, tS, tS + 16, tS + 32, tS + 48, ddOm, desc_add(ddOm, 2048),
+                desc_add(ddOm, 4096), desc_add(ddOm, 6144), kIdAcc, li > 0 ? 1u : 0u);
+      mma_ts_x4(tDK, tDP, tDP + 16, tDP + 32, tDP + 48, dQm, desc_add(dQm, 2048),
+                desc_add(dQm, 4096), desc_add(dQm, 6144), kIdAcc, li > 0 ? 1u : 0u);
+      // Both MMA streams of item li have read stage s (the S^T stream
+      // finished before the element-wise warps released P): free it, and the
+      // TMEM buffer.
+      mma_commit(bar(kDkvBarQEmpty + s));
+      mma_commit(bar(kDkvBarFree + (li & 1)));
+    }
+    mma_commit(bar(kDkvBarAcc));
+    mma_commit(bar(kDkvBarDrainAcc));
+    warp_all(mbar_wait(bar(kDkvBarDrainAcc), 0, wait_ns));
   } else {
     // ------------------------------------------------------------ P^T / dS^T warps
     // Warps w, w+4, w+8, w+12 share TMEM lane quarter (w & 3), i.e. the same
@@ -352,11 +368,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int krow = n0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
+    // K, V must have landed before anything below: for D = 64 they are
+    // copied into TMEM, and the cluster epilogue reuses their shared memory
+    // for partial sums (a block with no query items reaches it at once, and a
+    // late K/V copy would overwrite the sums).
+    ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
     if (Cf::kKvInTmem) {
       // K and V rows r into TMEM as the A operand of S^T and dP^T: this
       // thread copies elements 16 grp..16 grp+15 (two 16-byte chunks of the
       // 128-byte-swizzled tile row) as 8 packed pairs.
-      ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
       if (ok) {
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
@@ -494,7 +514,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // waits above are bounded), so the cluster barrier always completes.
     __syncwarp();
     cluster_sync();
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 2 + kComputeWarps) {
       // Block `crank` owns key rows [crank*R, (crank+1)*R) of the tile: it adds
       // the C partial sums in rank order and stores bf16 dV, dK (dK * scale).
       const int R = kTileN / C;
