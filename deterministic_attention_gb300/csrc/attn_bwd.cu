@@ -254,12 +254,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, g, n0, b);
         tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, g, n0, b);
       }
+      int h = g * G + (n_it > 0 ? it_lo / per_head : 0);
+      int m_idx = n_it > 0 ? it_lo % per_head : 0;
       for (int li = 0; li < n_it; ++li) {
-        const int it = it_lo + li;
         const int s = li % NS;
         const uint32_t ph = (li / NS) & 1;
-        const int h = g * G + it / per_head;
-        const int i0 = (m_begin + it % per_head) * kDkvTileM;
+        const int i0 = (m_begin + m_idx) * kDkvTileM;
         if (li >= NS && !(ok = mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns))) break;
         const uint32_t st = stage_base(s);
         mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + kDkvTileM * 8);
@@ -272,6 +272,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                   a.rowstats + (static_cast<size_t>(b) * a.Hq + h) * a.Tp + i0, kDkvTileM * 8,
                   bar(kDkvBarQFull + s));
         last[s] = li;
+        if (++m_idx == per_head) {
+          m_idx = 0;
+          ++h;
+        }
       }
       if (!ok) {
         mbar_wait(bar(kDkvBarKV), 0, wait_ns);
@@ -398,10 +402,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kDkvBarKvTmem));
     }
+    int m_idx = n_it > 0 ? it_lo % per_head : 0;  // query tile of item li within its head
     for (int li = 0; li < n_it && ok; ++li) {
-      const int it = it_lo + li;
       const int s = li % NS;
-      const int i0 = (m_begin + it % per_head) * kDkvTileM + grp * 16;  // this group's first query
+      const int i0 = (m_begin + m_idx) * kDkvTileM + grp * 16;  // this group's first query
+      if (++m_idx == per_head) m_idx = 0;
       ok = warp_all(mbar_wait(bar(kDkvBarS + (li & 1)), (li >> 1) & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
