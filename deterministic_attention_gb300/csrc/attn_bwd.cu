@@ -106,43 +106,53 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
 
 // ============================================================== dK / dV
 // Block = (b, KV head, 128-key tile), or one of C blocks of a cluster sharing
-// that tile.  Warp 0 loads K, V once and then the (Q, dO, row statistics) of
-// 64-row query tiles of every query head in the group; warp 1 issues
-// S^T = K Q^T and dP^T = V dO^T into two alternating TMEM buffers; warps
-// 2..17 turn S^T, dP^T into P^T, dS^T (four threads per key row, 16 queries
-// each); warp 18 issues dV += P^T dO and dK += dS^T Q with P^T and dS^T read
-// from TMEM.  With the two MMA streams in separate warps, S^T of the next
-// query tile is issued while the element-wise warps still work on this one,
-// without waiting behind the accumulate step: each issuing warp shares its
-// scheduler with four busy element-wise warps, so a single issuer running
-// both streams in turn was the critical path.
+// that tile.  The work is a sequence of items, one per (query head of the
+// group, query tile of TM rows at or after the key tile); TM = 128 for
+// D = 64 and 64 for D = 128.
+//   warp 0     loads K, V once, then each item's Q, dO tiles and row statistics
+//              into a ring of shared-memory stages;
+//   warp 1     issues S^T = K Q^T and dP^T = V dO^T into one TMEM buffer, as
+//              soon as the element-wise warps hold the previous item's in
+//              registers;
+//   warps 2-17 turn S^T, dP^T into P^T, dS^T (four threads per key row, TM/4
+//              queries each) and store them, as packed bf16, into a separate
+//              TMEM buffer;
+//   warp 18    issues dV += P^T dO and dK += dS^T Q from that buffer.
+// With the two MMA streams in separate warps and S^T, dP^T released early, the
+// next item's scores are computed while the element-wise warps still work on
+// this one: each issuing warp shares its scheduler with four busy
+// element-wise warps, and any step that waits behind another lands on the
+// critical path.
 constexpr int kBwdThreads = 608;  // producer, S issuer, 16 compute warps, dV/dK issuer
 constexpr int kComputeWarps = 16;
 constexpr int kDkvAccWarp = 2 + kComputeWarps;
 
 template <int D>
 struct DkvCfg {
+  static constexpr int kTM = dkdv_tile_m(D);   // query rows per item
+  static constexpr int kQG = kTM / 4;          // queries per element-wise thread
   static constexpr int kAtoms = D / 64;
-  static constexpr int kKvBytes = kTileN * 128 * kAtoms;    // 128 keys x D
-  static constexpr int kQBytes = kDkvTileM * 128 * kAtoms;  // 64 queries x D
+  static constexpr int kKvBytes = kTileN * 128 * kAtoms;  // 128 keys x D
+  static constexpr int kQBytes = kTM * 128 * kAtoms;      // TM queries x D
   static constexpr int kStages = (D == 64) ? 4 : 3;
-  static constexpr int kStageBytes = 2 * kQBytes + 1024;    // Q, dO, then row statistics
+  static constexpr int kStageBytes = 2 * kQBytes + 1024;  // Q, dO, then TM row statistics
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kKvBytes;
   static constexpr int kOffStage = 2 * kKvBytes;
   static constexpr int kSmemBytes = kOffStage + kStages * kStageBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // Buffer b (b = 0, 1): S^T at 128 b, dP^T at 128 b + 64 (64 fp32 columns
-  // each, one per query); the compute thread of group g writes its 16 P^T
-  // (dS^T) values as 8 packed bf16 pairs over columns 16g..16g+7 of S^T (dP^T).
-  static constexpr uint32_t kColDV = 256;      // dV accumulator, D cols
-  static constexpr uint32_t kColDK = 256 + D;  // dK accumulator, D cols
-  // For D = 64 the block's K and V tiles also live in TMEM (as packed bf16
-  // pairs, D/2 columns each), so S^T = K Q^T and dP^T = V dO^T read only Q / dO
-  // from shared memory.  For D = 128 TMEM is full and they stay in SMEM.
-  static constexpr bool kKvInTmem = (D == 64);
-  static constexpr uint32_t kColK = 256 + 2 * D;
-  static constexpr uint32_t kColV = kColK + D / 2;
+  // S^T at 0 and dP^T at TM (TM fp32 columns each, one per query).  P^T and
+  // dS^T of item li go to buffer li % kNumPB at kColPB + TM * buffer: P^T as
+  // packed bf16 pairs over TM/2 columns (two queries per column), dS^T over
+  // the next TM/2; group g writes columns g*TM/8 .. of each.
+  static constexpr int kNumPB = (D == 64) ? 1 : 2;
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColDP = kTM;
+  static constexpr uint32_t kColPB = 2 * kTM;
+  static constexpr uint32_t kColDV = kColPB + kNumPB * kTM;  // dV accumulator, D cols
+  static constexpr uint32_t kColDK = kColDV + D;             // dK accumulator, D cols
+  static_assert(kColDK + D <= kTmemCols, "TMEM layout");
+  static_assert(kTM * 8 <= 1024, "row statistics fit their stage slot");
 };
 static_assert(kTileN * 2 * 64 * 4 <= DkvCfg<64>::kSmemBytes - 1024, "dK/dV partials fit");
 static_assert(kTileN * 2 * 128 * 4 <= DkvCfg<128>::kSmemBytes - 1024, "dK/dV partials fit");
@@ -152,15 +162,34 @@ enum : int {
   kDkvBarKV = 0,
   kDkvBarQFull = 1,
   kDkvBarQEmpty = kDkvBarQFull + kDkvMaxStages,
-  kDkvBarS = kDkvBarQEmpty + kDkvMaxStages,  // [2]
-  kDkvBarP = kDkvBarS + 2,                   // [2]
-  kDkvBarAcc = kDkvBarP + 2,
+  kDkvBarS = kDkvBarQEmpty + kDkvMaxStages,  // S^T, dP^T of the current item landed
+  kDkvBarSFree = kDkvBarS + 1,               // element-wise warps hold them in registers
+  kDkvBarP = kDkvBarSFree + 1,               // [2] P^T, dS^T of the buffer's item written
+  kDkvBarFree = kDkvBarP + 2,                // [2] dV, dK of the buffer's item done
+  kDkvBarAcc = kDkvBarFree + 2,
   kDkvBarDrain = kDkvBarAcc + 1,
-  kDkvBarKvTmem = kDkvBarDrain + 1,  // compute warps copied K, V into TMEM
-  kDkvBarFree = kDkvBarKvTmem + 1,   // [2] dV, dK of the buffer's last item done
-  kDkvBarDrainAcc = kDkvBarFree + 2,
+  kDkvBarDrainAcc = kDkvBarDrain + 1,
   kDkvNumBars = kDkvBarDrainAcc + 1
 };
+
+// TMEM columns [taddr, taddr + N) of this warp's 32 lanes into v (N = 16, 32).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&v)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 16) tmem_ld16_nowait(taddr, v);
+  else tmem_ld32_nowait(taddr, v);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&v)[N]) {
+  static_assert(N == 8 || N == 16, "8 or 16 columns");
+  if constexpr (N == 8) tmem_st8_nowait(taddr, v);
+  else tmem_st16_nowait(taddr, v);
+}
+template <int N>
+__device__ __forceinline__ void reg_fence_cols(uint32_t (&v)[N]) {
+  if constexpr (N == 16) reg_fence16(v);
+  else reg_fence32(v);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -169,6 +198,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      const BwdArgs a) {
   using Cf = DkvCfg<D>;
   constexpr int NS = Cf::kStages;
+  constexpr int TM = Cf::kTM;
+  constexpr int QG = Cf::kQG;
+  constexpr int NPB = Cf::kNumPB;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[kDkvNumBars];
   __shared__ uint32_t tmem_slot;
@@ -187,8 +219,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int b = bg / a.Hkv, g = bg % a.Hkv;
   const int G = a.Hq / a.Hkv;
   const int n0 = nt * kTileN;
-  const int m_begin = a.causal ? n0 / kDkvTileM : 0;
-  const int m_end = (a.T + kDkvTileM - 1) / kDkvTileM;
+  const int m_begin = a.causal ? n0 / TM : 0;
+  const int m_end = (a.T + TM - 1) / TM;
   const int per_head = m_end - m_begin;
   const int n_all = G * per_head;
   const int it_lo = static_cast<int>(static_cast<long>(crank) * n_all / C);
@@ -199,9 +231,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sK = s0 + Cf::kOffK, sV = s0 + Cf::kOffV;
   auto stage_base = [&](int s) { return s0 + Cf::kOffStage + s * Cf::kStageBytes; };
-  auto stage_rows = [&](int s) {  // 64 pairs (-LSE*log2e, -Delta)
-    return reinterpret_cast<float*>(smem + Cf::kOffStage + s * Cf::kStageBytes + 2 * Cf::kQBytes);
-  };
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
   // Byte offset of 16-byte chunk `chunk` of partial-sum row `row` (2D floats
   // per row, chunks XOR-swizzled by row % 8 against bank conflicts).
@@ -220,15 +249,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(kDkvBarQFull + s), 1);
       mbar_init(bar(kDkvBarQEmpty + s), 1);
     }
+    mbar_init(bar(kDkvBarS), 1);
+    mbar_init(bar(kDkvBarSFree), kComputeWarps);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kDkvBarS + i), 1);
       mbar_init(bar(kDkvBarP + i), kComputeWarps);
+      mbar_init(bar(kDkvBarFree + i), 1);
     }
     mbar_init(bar(kDkvBarAcc), 1);
     mbar_init(bar(kDkvBarDrain), 1);
-    mbar_init(bar(kDkvBarKvTmem), kComputeWarps);
-    mbar_init(bar(kDkvBarFree + 0), 1);
-    mbar_init(bar(kDkvBarFree + 1), 1);
     mbar_init(bar(kDkvBarDrainAcc), 1);
     fence_barrier_init();
   }
@@ -259,17 +287,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int li = 0; li < n_it; ++li) {
         const int s = li % NS;
         const uint32_t ph = (li / NS) & 1;
-        const int i0 = (m_begin + m_idx) * kDkvTileM;
+        const int i0 = (m_begin + m_idx) * TM;
         if (li >= NS && !(ok = mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns))) break;
         const uint32_t st = stage_base(s);
-        mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + kDkvTileM * 8);
+        mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + TM * 8);
         for (int at = 0; at < Cf::kAtoms; ++at) {
-          tma_load_4d(st + at * (kDkvTileM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h, i0, b);
-          tma_load_4d(st + Cf::kQBytes + at * (kDkvTileM * 128), &mdO, bar(kDkvBarQFull + s),
-                      at * 64, h, i0, b);
+          tma_load_4d(st + at * (TM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h, i0, b);
+          tma_load_4d(st + Cf::kQBytes + at * (TM * 128), &mdO, bar(kDkvBarQFull + s), at * 64,
+                      h, i0, b);
         }
         bulk_load(st + 2 * Cf::kQBytes,
-                  a.rowstats + (static_cast<size_t>(b) * a.Hq + h) * a.Tp + i0, kDkvTileM * 8,
+                  a.rowstats + (static_cast<size_t>(b) * a.Hq + h) * a.Tp + i0, TM * 8,
                   bar(kDkvBarQFull + s));
         last[s] = li;
         if (++m_idx == per_head) {
@@ -287,48 +315,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ S^T / dP^T issuer
     // The whole warp runs this loop (MMA issue is warp-collective); every
     // wait is made warp-uniform so the warp stays converged.
-    constexpr uint32_t kIdS = idesc_bf16(kTileN, kDkvTileM, false, false);
+    constexpr uint32_t kIdS = idesc_bf16(kTileN, TM, false, false);
     // Operand descriptors built once; the loop only adds constant offsets.
     const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
     const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);  // K-major B
+    const uint32_t tS = tmem + Cf::kColS, tDP = tmem + Cf::kColDP;
     ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
-    if (ok && Cf::kKvInTmem) ok = warp_all(mbar_wait(bar(kDkvBarKvTmem), 0, wait_ns));
     tc_fence_after();
     for (int li = 0; li < n_it && ok; ++li) {
       const int s = li % NS;
-      // Buffer li & 1 last held item li - 2: its dV, dK must have read P^T,
-      // dS^T before S^T, dP^T of item li overwrite them.
-      if (li >= 2 && !(ok = warp_all(mbar_wait(bar(kDkvBarFree + (li & 1)), ((li - 2) >> 1) & 1,
-                                               wait_ns))))
-        break;
+      // The element-wise warps must hold S^T, dP^T of item li - 1 in
+      // registers before those of item li overwrite them.
+      if (li >= 1 && !(ok = warp_all(mbar_wait(bar(kDkvBarSFree), (li - 1) & 1, wait_ns)))) break;
       if (!(ok = warp_all(mbar_wait(bar(kDkvBarQFull + s), (li / NS) & 1, wait_ns)))) break;
       tc_fence_after();
       const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
       const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
-      const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
-      if (Cf::kKvInTmem) {
-        // K = 64 = D: four steps over the packed K / V columns and the
-        // 32-byte K-major slices of Q / dO.
-        const uint32_t aK = tmem + Cf::kColK, aV = tmem + Cf::kColV;
-        mma_ts_x4(tS, aK, aK + 8, aK + 16, aK + 24, dQk, desc_add(dQk, 32), desc_add(dQk, 64),
-                  desc_add(dQk, 96), kIdS, 0u);
-        mma_ts_x4(tDP, aV, aV + 8, aV + 16, aV + 24, ddOk, desc_add(ddOk, 32), desc_add(ddOk, 64),
-                  desc_add(ddOk, 96), kIdS, 0u);
-      } else {
+      // K = D in groups of 64 (one 128-byte swizzle atom): four 32-byte steps.
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
-          const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-          mma_ss(tS, desc_add(dK, okv), desc_add(dQk, oq), kIdS, ks > 0);
-        }
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t okv = (ks >> 2) * (kTileN * 128) + (ks & 3) * 32;
-          const uint32_t oq = (ks >> 2) * (kDkvTileM * 128) + (ks & 3) * 32;
-          mma_ss(tDP, desc_add(dV, okv), desc_add(ddOk, oq), kIdS, ks > 0);
-        }
+      for (int at = 0; at < Cf::kAtoms; ++at) {
+        const uint64_t k = desc_add(dK, at * (kTileN * 128)), q = desc_add(dQk, at * (TM * 128));
+        mma_ss_x4(tS, k, desc_add(k, 32), desc_add(k, 64), desc_add(k, 96), q, desc_add(q, 32),
+                  desc_add(q, 64), desc_add(q, 96), kIdS, at > 0 ? 1u : 0u);
       }
-      mma_commit(bar(kDkvBarS + (li & 1)));
+#pragma unroll
+      for (int at = 0; at < Cf::kAtoms; ++at) {
+        const uint64_t v = desc_add(dV, at * (kTileN * 128)), o = desc_add(ddOk, at * (TM * 128));
+        mma_ss_x4(tDP, v, desc_add(v, 32), desc_add(v, 64), desc_add(v, 96), o, desc_add(o, 32),
+                  desc_add(o, 64), desc_add(o, 96), kIdS, at > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(kDkvBarS));
     }
     // Every issued MMA must finish before TMEM is released.
     mma_commit(bar(kDkvBarDrain));
@@ -337,26 +353,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ dV / dK issuer
     constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
     const uint32_t tDV = tmem + Cf::kColDV, tDK = tmem + Cf::kColDK;
-    const uint64_t dQm0 = sdesc_sw128(stage_base(0), kDkvTileM * 128, 1024);  // MN-major B
+    // Q, dO as MN-major B operands: 16 queries per 2048-byte step, the
+    // 64-column blocks of D = 128 TM * 128 bytes apart.
+    const uint64_t dQm0 = sdesc_sw128(stage_base(0), TM * 128, 1024);
     for (int li = 0; li < n_it && ok; ++li) {
       const int s = li % NS;
-      if (!(ok = warp_all(mbar_wait(bar(kDkvBarP + (li & 1)), (li >> 1) & 1, wait_ns)))) break;
+      const int pb = li % NPB;
+      if (!(ok = warp_all(mbar_wait(bar(kDkvBarP + pb), (li / NPB) & 1, wait_ns)))) break;
       tc_fence_after();
       const uint64_t dQm = desc_add(dQm0, s * Cf::kStageBytes);
       const uint64_t ddOm = desc_add(dQm, Cf::kQBytes);
-      const uint32_t tS = tmem + (li & 1) * 128, tDP = tS + 64;
-      // P^T / dS^T of queries 16ks..16ks+15: group ks wrote them as 8 packed
-      // columns at the start of its 16 S^T / dP^T columns.
-      static_assert(kDkvTileM == 64, "the dV / dK issue below takes 4 query steps");
-      mma_ts_x4(tDV, tS, tS + 16, tS + 32, tS + 48, ddOm, desc_add(ddOm, 2048),
-                desc_add(ddOm, 4096), desc_add(ddOm, 6144), kIdAcc, li > 0 ? 1u : 0u);
-      mma_ts_x4(tDK, tDP, tDP + 16, tDP + 32, tDP + 48, dQm, desc_add(dQm, 2048),
-                desc_add(dQm, 4096), desc_add(dQm, 6144), kIdAcc, li > 0 ? 1u : 0u);
+      // P^T / dS^T of queries 16ks..16ks+15: 8 packed columns at 8ks.
+      const uint32_t tP = tmem + Cf::kColPB + pb * TM, tDS = tP + TM / 2;
+#pragma unroll
+      for (int q4 = 0; q4 < TM / 64; ++q4) {
+        const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
+        const uint32_t p = tP + q4 * 32;
+        const uint64_t o = desc_add(ddOm, q4 * 8192);
+        mma_ts_x4(tDV, p, p + 8, p + 16, p + 24, o, desc_add(o, 2048), desc_add(o, 4096),
+                  desc_add(o, 6144), kIdAcc, acc);
+      }
+#pragma unroll
+      for (int q4 = 0; q4 < TM / 64; ++q4) {
+        const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
+        const uint32_t p = tDS + q4 * 32;
+        const uint64_t q = desc_add(dQm, q4 * 8192);
+        mma_ts_x4(tDK, p, p + 8, p + 16, p + 24, q, desc_add(q, 2048), desc_add(q, 4096),
+                  desc_add(q, 6144), kIdAcc, acc);
+      }
       // Both MMA streams of item li have read stage s (the S^T stream
       // finished before the element-wise warps released P): free it, and the
-      // TMEM buffer.
+      // P^T / dS^T buffer.
       mma_commit(bar(kDkvBarQEmpty + s));
-      mma_commit(bar(kDkvBarFree + (li & 1)));
+      mma_commit(bar(kDkvBarFree + pb));
     }
     mma_commit(bar(kDkvBarAcc));
     mma_commit(bar(kDkvBarDrainAcc));
@@ -364,67 +393,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else {
     // ------------------------------------------------------------ P^T / dS^T warps
     // Warps w, w+4, w+8, w+12 share TMEM lane quarter (w & 3), i.e. the same
-    // 32 key rows; group grp = (w - 2) / 4 takes queries 16 grp..16 grp+15 of
-    // each 64-query item.
+    // 32 key rows; group grp = (w - 2) / 4 takes queries QG grp..QG grp+QG-1
+    // of each item.
     const int quarter = warp & 3;
     const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     const int krow = n0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
-    // K, V must have landed before anything below: for D = 64 they are
-    // copied into TMEM, and the cluster epilogue reuses their shared memory
-    // for partial sums (a block with no query items reaches it at once, and a
-    // late K/V copy would overwrite the sums).
+    // K, V must have landed before the cluster epilogue reuses their shared
+    // memory for partial sums (a block with no items reaches it at once).
     ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
-    if (Cf::kKvInTmem) {
-      // K and V rows r into TMEM as the A operand of S^T and dP^T: this
-      // thread copies elements 16 grp..16 grp+15 (two 16-byte chunks of the
-      // 128-byte-swizzled tile row) as 8 packed pairs.
-      if (ok) {
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t base = (which == 0 ? sK : sV) + r * 128;
-          uint32_t v8[8];
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint4 x = ld_shared_u4(base + (((2 * grp + c) ^ (r & 7)) * 16));
-            v8[4 * c] = x.x;
-            v8[4 * c + 1] = x.y;
-            v8[4 * c + 2] = x.z;
-            v8[4 * c + 3] = x.w;
-          }
-          tmem_st8_nowait(tl + (which == 0 ? Cf::kColK : Cf::kColV) + grp * 8, v8);
-        }
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDkvBarKvTmem));
-    }
     int m_idx = n_it > 0 ? it_lo % per_head : 0;  // query tile of item li within its head
     for (int li = 0; li < n_it && ok; ++li) {
       const int s = li % NS;
-      const int i0 = (m_begin + m_idx) * kDkvTileM + grp * 16;  // this group's first query
+      const int pb = li % NPB;
+      const int i0 = (m_begin + m_idx) * TM + grp * QG;  // this group's first query
       if (++m_idx == per_head) m_idx = 0;
-      ok = warp_all(mbar_wait(bar(kDkvBarS + (li & 1)), (li >> 1) & 1, wait_ns));
+      ok = warp_all(mbar_wait(bar(kDkvBarS), li & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tS = tl + (li & 1) * 128 + grp * 16, tDP = tS + 64;
-      uint32_t sv[16], dp[16];
-      tmem_ld16_nowait(tS, sv);
-      tmem_ld16_nowait(tDP, dp);
+      uint32_t sv[QG], dp[QG];
+      tmem_ld_cols<QG>(tl + Cf::kColS + grp * QG, sv);
+      tmem_ld_cols<QG>(tl + Cf::kColDP + grp * QG, dp);
       tmem_wait_ld();
-      reg_fence16(sv);
-      reg_fence16(dp);
+      reg_fence_cols<QG>(sv);
+      reg_fence_cols<QG>(dp);
+      // S^T, dP^T are in registers: the next item's may overwrite them.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDkvBarSFree));
       // Causal: query i0 + c sees key krow iff c >= krow - i0.
       const int cmin = a.causal ? (krow - i0) : -1;
       const bool need_mask = cmin > 0;
-      uint32_t pk[8], dk[8];
-      // (-lse2, -delta) of this group's 16 queries, two per float4.
-      const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * 8 * 16;
+      uint32_t pk[QG / 2], dk[QG / 2];
+      // (-lse2, -delta) of this group's queries, two per float4.
+      const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * QG * 8;
 #pragma unroll
-      for (int c2 = 0; c2 < 8; ++c2) {
+      for (int c2 = 0; c2 < QG / 2; ++c2) {
         const int c = 2 * c2;
         const float4 rs = ld_shared_f4(st4 + c2 * 16);  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
         const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rs.x);
@@ -446,12 +452,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         pk[c2] = pack_bf16x2(p0, p1);
         dk[c2] = pack_bf16x2(d0, d1);
       }
-      tmem_st8_nowait(tS, pk);
-      tmem_st8_nowait(tDP, dk);
+      // P^T / dS^T buffer pb last held item li - NPB: its dV, dK must have
+      // read it.
+      if (li >= NPB) {
+        ok = warp_all(mbar_wait(bar(kDkvBarFree + pb), ((li - NPB) / NPB) & 1, wait_ns));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      const uint32_t tP = tl + Cf::kColPB + pb * TM + grp * (QG / 2);
+      tmem_st_cols<QG / 2>(tP, pk);
+      tmem_st_cols<QG / 2>(tP + TM / 2, dk);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDkvBarP + (li & 1)));
+      if (lane == 0) mbar_arrive(bar(kDkvBarP + pb));
     }
     if (ok) ok = warp_all(mbar_wait(bar(kDkvBarAcc), 0, wait_ns));
     if (ok && C > 1) {

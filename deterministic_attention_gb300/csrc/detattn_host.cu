@@ -193,9 +193,10 @@ int sm_count(int* out) {
 int dkdv_cluster_size(int B, int T, int Hq, int Hkv, int D, int causal, int sms) {
   const int G = Hq / Hkv;
   const int n_tiles = (T + kTileN - 1) / kTileN;
-  const int m_end = (T + kDkvTileM - 1) / kDkvTileM;
+  const int tm = dkdv_tile_m(D);
+  const int m_end = (T + tm - 1) / tm;
   double total = 0.0;
-  for (int nt = 0; nt < n_tiles; ++nt) total += m_end - (causal ? nt * kTileN / kDkvTileM : 0);
+  for (int nt = 0; nt < n_tiles; ++nt) total += m_end - (causal ? nt * kTileN / tm : 0);
   total *= static_cast<double>(B) * Hkv * G;
   const double max_items = static_cast<double>(G) * m_end;
   const double slots = static_cast<double>(sms);  // one dK/dV block per SM
@@ -210,8 +211,8 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
               float scale, int causal, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdo;
   int rc;
-  if ((rc = encode_rows(&mq, q, B, T, Hq, D, kDkvTileM, "q")) != DETATTN_OK) return rc;
-  if ((rc = encode_rows(&mdo, dout, B, T, Hq, D, kDkvTileM, "dout")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mq, q, B, T, Hq, D, dkdv_tile_m(D), "q")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mdo, dout, B, T, Hq, D, dkdv_tile_m(D), "dout")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
   BwdArgs a = bwd_args(workspace, T, Hq, Hkv, scale, causal);
