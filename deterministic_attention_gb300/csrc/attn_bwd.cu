@@ -271,6 +271,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = tmem_slot;
   const uint64_t wait_ns = a.wait_ns;
   bool ok = true;
+  // The element-wise threads' share of the finished dV, dK accumulators
+  // (zero for a block without items), kept for the cluster epilogue.
+  uint32_t part_v[D / 4], part_k[D / 4];
+#pragma unroll
+  for (int i = 0; i < D / 4; ++i) part_v[i] = part_k[i] = 0u;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -468,94 +473,83 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (lane == 0) mbar_arrive(bar(kDkvBarP + pb));
     }
     if (ok) ok = warp_all(mbar_wait(bar(kDkvBarAcc), 0, wait_ns));
-    if (ok && C > 1) {
-      // Partial sums to this block's shared memory (fp32, row r = key row r,
-      // [dV | dK] = 2D floats per row, 16-byte chunks XOR-swizzled by r % 8);
-      // group grp writes columns grp*D/4 .. of both.
+    // This thread's share of key row r: D/4 columns of dV and of dK.
+    if (ok && n_it > 0) {
       tc_fence_after();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = (which == 0 ? Cf::kColDV : Cf::kColDK) + grp * (D / 4);
-#pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          uint32_t v[16];
-          if (n_it > 0) {
-            tmem_ld16_nowait(tl + col + cc * 16, v);
-            tmem_wait_ld();
-            reg_fence16(v);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = 0u;
-          }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int chunk = (which * D + grp * (D / 4) + cc * 16) / 4 + i;
-            st_shared_f4(s0 + partial_off(r, chunk),
-                         make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
-          }
-        }
-      }
+      tmem_ld_cols<D / 4>(tl + Cf::kColDV + grp * (D / 4), part_v);
+      tmem_ld_cols<D / 4>(tl + Cf::kColDK + grp * (D / 4), part_k);
+      tmem_wait_ld();
+      reg_fence_cols<D / 4>(part_v);
+      reg_fence_cols<D / 4>(part_k);
     }
-    if (ok && C == 1) {
-      tc_fence_after();
-      const bool live = krow < a.T;
-      const size_t rbase = ((static_cast<size_t>(b) * a.T + krow) * a.Hkv + g) * D;
+    if (ok && C == 1 && krow < a.T) {
+      const size_t rbase = ((static_cast<size_t>(b) * a.T + krow) * a.Hkv + g) * D + grp * (D / 4);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t col = (which == 0 ? Cf::kColDV : Cf::kColDK) + grp * (D / 4);
+        const uint32_t* v = which == 0 ? part_v : part_k;
         const float mul = which == 0 ? 1.f : a.scale;
-        __nv_bfloat16* dst_row =
-            static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + rbase + grp * (D / 4);
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + rbase);
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          uint32_t v[16];
-          tmem_ld16_nowait(tl + col + cc * 16, v);
-          tmem_wait_ld();
-          reg_fence16(v);
-          uint32_t pkd[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * mul, __uint_as_float(v[2 * i + 1]) * mul);
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(dst_row + cc * 16);
-            dst[0] = make_uint4(pkd[0], pkd[1], pkd[2], pkd[3]);
-            dst[1] = make_uint4(pkd[4], pkd[5], pkd[6], pkd[7]);
-          }
-        }
+        for (int i = 0; i < D / 32; ++i)
+          dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i]) * mul, __uint_as_float(v[8 * i + 1]) * mul),
+                              pack_bf16x2(__uint_as_float(v[8 * i + 2]) * mul, __uint_as_float(v[8 * i + 3]) * mul),
+                              pack_bf16x2(__uint_as_float(v[8 * i + 4]) * mul, __uint_as_float(v[8 * i + 5]) * mul),
+                              pack_bf16x2(__uint_as_float(v[8 * i + 6]) * mul, __uint_as_float(v[8 * i + 7]) * mul));
       }
     }
   }
 
   if (C > 1) {
-    // Every block of the cluster reaches both barriers (no early exit; all
-    // waits above are bounded), so the cluster barrier always completes.
+    // Block `crank` owns key rows [crank R, (crank + 1) R) of the tile.  Every
+    // block writes its partial sums of the rows block p owns into p's shared
+    // memory (slot crank: rows crank R .. of a [C R rows][dV | dK] fp32
+    // array, 16-byte chunks XOR-swizzled by row % 8); p then adds its C slots
+    // in rank order and stores bf16 dV, dK (dK * scale).  The first cluster
+    // barrier makes sure p is past its main loop (its shared memory is free),
+    // the second that every slot has landed.  Every block of the cluster
+    // reaches both (no early exit; all waits above are bounded).
+    const int R = kTileN / C;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     cluster_sync();
     if (warp >= 2 && warp < 2 + kComputeWarps) {
-      // Block `crank` owns key rows [crank*R, (crank+1)*R) of the tile: it adds
-      // the C partial sums in rank order and stores bf16 dV, dK (dK * scale).
-      const int R = kTileN / C;
+      const int r = (warp & 3) * 32 + lane;
+      const int grp = (warp - 2) >> 2;
+      const int p = r / R;
+      const uint32_t dst = map_shared_rank(s0, static_cast<uint32_t>(p));
+      const int row = crank * R + (r - p * R);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t* v = which == 0 ? part_v : part_k;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          const int chunk = (which * D + grp * (D / 4)) / 4 + i;
+          st_shared_cluster_f4(dst + partial_off(row, chunk),
+                               make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                           __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();
+    if (warp >= 2 && warp < 2 + kComputeWarps) {
       constexpr int kCpr = 2 * D / 8;  // 8-float output chunks per row ([dV | dK])
       const int ct = static_cast<int>(threadIdx.x) - 64;
       for (int e = ct; e < R * kCpr; e += kComputeWarps * 32) {
         const int rl = e / kCpr, oc = e % kCpr;
-        const int row = crank * R + rl;
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
         for (int src = 0; src < C; ++src) {
-          const uint32_t base = map_shared_rank(s0, static_cast<uint32_t>(src));
-          const float4 x = ld_shared_cluster_f4(base + partial_off(row, 2 * oc));
-          const float4 y = ld_shared_cluster_f4(base + partial_off(row, 2 * oc + 1));
+          const float4 x = ld_shared_f4(s0 + partial_off(src * R + rl, 2 * oc));
+          const float4 y = ld_shared_f4(s0 + partial_off(src * R + rl, 2 * oc + 1));
           acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
           acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
         }
         const bool is_dk = oc * 8 >= D;
         const float mul = is_dk ? a.scale : 1.f;
         const int col = oc * 8 - (is_dk ? D : 0);
-        const int krow_out = n0 + row;
+        const int krow_out = n0 + crank * R + rl;
         if (krow_out < a.T) {
           __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_dk ? a.dk : a.dv) +
                                ((static_cast<size_t>(b) * a.T + krow_out) * a.Hkv + g) * D + col;
@@ -565,8 +559,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       }
     }
-    __syncwarp();
-    cluster_sync();
   }
 
   if (!ok) atomicOr(&g_bwd_status, 2u);

@@ -363,6 +363,13 @@ __device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
                : "memory");
   return v;
 }
+// Store to shared memory of another block of the cluster (`addr` from
+// map_shared_rank).  Made visible to that block by the next cluster barrier.
+__device__ __forceinline__ void st_shared_cluster_f4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
+}
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
