@@ -139,7 +139,12 @@ struct DkvCfg {
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kKvBytes;
   static constexpr int kOffStage = 2 * kKvBytes;
-  static constexpr int kSmemBytes = kOffStage + kStages * kStageBytes + 1024;
+  // D = 64 gathers cluster partial sums by bulk copies into a region of its
+  // own: up to 7/8 of the 128 rows of [dV | dK] fp32 (512 bytes per row).
+  static constexpr bool kBulkEpi = (D == 64);
+  static constexpr int kOffRecv = kOffStage + kStages * kStageBytes;
+  static constexpr int kRecvBytes = kBulkEpi ? (kTileN - kTileN / 8) * 2 * D * 4 : 0;
+  static constexpr int kSmemBytes = kOffRecv + kRecvBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // S^T at 0 and dP^T at TM (TM fp32 columns each, one per query).  P^T and
   // dS^T of item li go to buffer li % kNumPB at kColPB + TM * buffer: P^T as
@@ -169,7 +174,8 @@ enum : int {
   kDkvBarAcc = kDkvBarFree + 2,
   kDkvBarDrain = kDkvBarAcc + 1,
   kDkvBarDrainAcc = kDkvBarDrain + 1,
-  kDkvNumBars = kDkvBarDrainAcc + 1
+  kDkvBarRecv = kDkvBarDrainAcc + 1,  // the cluster peers' partial sums landed
+  kDkvNumBars = kDkvBarRecv + 1
 };
 
 // TMEM columns [taddr, taddr + N) of this warp's 32 lanes into v (N = 16, 32).
@@ -258,6 +264,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar(kDkvBarAcc), 1);
     mbar_init(bar(kDkvBarDrain), 1);
     mbar_init(bar(kDkvBarDrainAcc), 1);
+    mbar_init(bar(kDkvBarRecv), 1);
+    // The C - 1 peers each send the R = 128 / C rows this block owns.
+    if (Cf::kBulkEpi && C > 1)
+      mbar_arrive_expect_tx(bar(kDkvBarRecv), (C - 1) * (kTileN / C) * 2 * D * 4);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -267,6 +277,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&mdO);
   }
   __syncthreads();
+  // Peers may send into this block's shared memory (and its mbarrier) once
+  // this arrival is matched by their wait, long before it is needed.
+  if (C > 1) cluster_arrive();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const uint64_t wait_ns = a.wait_ns;
@@ -482,6 +495,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       reg_fence_cols<D / 4>(part_v);
       reg_fence_cols<D / 4>(part_k);
     }
+    if (Cf::kBulkEpi && C > 1 && r / (kTileN / C) != crank) {
+      // Partial sums of rows another block owns: staged in row order over the
+      // (now idle) K / V / stage memory, rows [p R, (p + 1) R) contiguous for
+      // block p, 16-byte chunks XOR-swizzled by row % 8.
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t* v = which == 0 ? part_v : part_k;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) {
+          const int chunk = (which * D + grp * (D / 4)) / 4 + i;
+          st_shared_f4(s0 + partial_off(r, chunk),
+                       make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+        }
+      }
+    }
     if (ok && C == 1 && krow < a.T) {
       const size_t rbase = ((static_cast<size_t>(b) * a.T + krow) * a.Hkv + g) * D + grp * (D / 4);
 #pragma unroll
@@ -499,8 +528,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   }
 
-  if (C > 1) {
-    // Block `crank` owns key rows [crank R, (crank + 1) R) of the tile.  Every
+  if (Cf::kBulkEpi && C > 1) {
+    // Block `crank` owns key rows [crank R, (crank + 1) R) of the tile.  Each
+    // peer's staged rows for it arrive by one bulk copy into slot j (j = src,
+    // or src - 1 above crank) of this block's receive region; the owner
+    // threads then add the C partial sums in rank order (their own from
+    // registers) and store bf16 dV, dK (dK * scale).  The final cluster
+    // barrier keeps every block alive until the copies reading its staged
+    // rows have completed.
+    const int R = kTileN / C;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    cluster_wait();
+    if (threadIdx.x == 64) {
+      for (int p = 0; p < C; ++p) {
+        if (p == crank) continue;
+        const int j = crank < p ? crank : crank - 1;
+        bulk_copy_to_peer(map_shared_rank(s0 + Cf::kOffRecv + j * R * 2 * D * 4, p),
+                          s0 + p * R * 2 * D * 4, R * 2 * D * 4,
+                          map_shared_rank(bar(kDkvBarRecv), p));
+      }
+    }
+    if (warp >= 2 && warp < 2 + kComputeWarps) {
+      const int r = (warp & 3) * 32 + lane;
+      const int grp = (warp - 2) >> 2;
+      // Whole warps wait (R may be 16: half a warp owns rows).
+      const bool got = warp_all(mbar_wait(bar(kDkvBarRecv), 0, wait_ns));
+      if (!got) ok = false;
+      if (r / R == crank) {
+        const int rl = r - crank * R;
+        float acc_v[D / 4], acc_k[D / 4];
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) acc_v[i] = acc_k[i] = 0.f;
+        for (int src = 0; src < C; ++src) {
+          if (src == crank) {
+#pragma unroll
+            for (int i = 0; i < D / 4; ++i) {
+              acc_v[i] += __uint_as_float(part_v[i]);
+              acc_k[i] += __uint_as_float(part_k[i]);
+            }
+          } else {
+            const int j = src < crank ? src : src - 1;
+            const uint32_t slot = s0 + Cf::kOffRecv + j * R * 2 * D * 4;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+              const float4 x = ld_shared_f4(slot + partial_off(rl, (grp * (D / 4)) / 4 + i));
+              const float4 y = ld_shared_f4(slot + partial_off(rl, (D + grp * (D / 4)) / 4 + i));
+              acc_v[4 * i] += x.x; acc_v[4 * i + 1] += x.y; acc_v[4 * i + 2] += x.z; acc_v[4 * i + 3] += x.w;
+              acc_k[4 * i] += y.x; acc_k[4 * i + 1] += y.y; acc_k[4 * i + 2] += y.z; acc_k[4 * i + 3] += y.w;
+            }
+          }
+        }
+        const int krow_out = n0 + r;
+        if (got && krow_out < a.T) {
+          const size_t rbase =
+              ((static_cast<size_t>(b) * a.T + krow_out) * a.Hkv + g) * D + grp * (D / 4);
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const float* v = which == 0 ? acc_v : acc_k;
+            const float mul = which == 0 ? 1.f : a.scale;
+            uint4* dst = reinterpret_cast<uint4*>(
+                static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + rbase);
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i)
+              dst[i] = make_uint4(pack_bf16x2(v[8 * i] * mul, v[8 * i + 1] * mul),
+                                  pack_bf16x2(v[8 * i + 2] * mul, v[8 * i + 3] * mul),
+                                  pack_bf16x2(v[8 * i + 4] * mul, v[8 * i + 5] * mul),
+                                  pack_bf16x2(v[8 * i + 6] * mul, v[8 * i + 7] * mul));
+          }
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync();
+  } else if (C > 1) {
+    // (D = 128) Block `crank` owns key rows [crank R, (crank + 1) R) of the tile.  Every
     // block writes its partial sums of the rows block p owns into p's shared
     // memory (slot crank: rows crank R .. of a [C R rows][dV | dK] fp32
     // array, 16-byte chunks XOR-swizzled by row % 8); p then adds its C slots
@@ -511,6 +613,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int R = kTileN / C;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
+    cluster_wait();  // matches the arrival after setup
     cluster_sync();
     if (warp >= 2 && warp < 2 + kComputeWarps) {
       const int r = (warp & 3) * 32 + lane;
