@@ -105,24 +105,43 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
 }
 
 // ============================================================== dK / dV
-// Block = (b, KV head, 128-key tile), or one of C blocks of a cluster sharing
-// that tile.  The work is a sequence of items, one per (query head of the
-// group, query tile of TM rows at or after the key tile); TM = 128 for
-// D = 64 and 64 for D = 128.
-//   warp 0     loads K, V once, then each item's Q, dO tiles and row statistics
-//              into a ring of shared-memory stages;
+// Persistent: the grid is n_groups clusters of C blocks, all resident.  Key
+// tiles (b, KV head, 128 keys), heaviest first under the causal mask, are
+// dealt to the clusters in snake order (round r: tiles r*NG .. r*NG + NG - 1,
+// reversed in odd rounds), and a cluster's C blocks split each of its tiles:
+// the tile's items -- one per (query head of the group, query tile of TM rows
+// at or after the key tile), TM = 128 for D = 64 and 64 for D = 128 -- are cut
+// into C contiguous chunks, and block r sums chunk r.  The split and the deal
+// depend only on the shape and the SM count, so every output bit is fixed for
+// a given problem and GPU.
+//   warp 0     loads each tile's K, V (once the previous tile's S^T MMAs are
+//              done with them), then each item's Q, dO tiles and row
+//              statistics into a ring of shared-memory stages;
 //   warp 1     issues S^T = K Q^T and dP^T = V dO^T into one TMEM buffer, as
 //              soon as the element-wise warps hold the previous item's in
 //              registers;
 //   warps 2-17 turn S^T, dP^T into P^T, dS^T (four threads per key row, TM/4
 //              queries each) and store them, as packed bf16, into a separate
-//              TMEM buffer;
+//              TMEM buffer; after a tile's last item they read its dV, dK
+//              accumulators and write them out;
 //   warp 18    issues dV += P^T dO and dK += dS^T Q from that buffer.
 // With the two MMA streams in separate warps and S^T, dP^T released early, the
 // next item's scores are computed while the element-wise warps still work on
 // this one: each issuing warp shares its scheduler with four busy
 // element-wise warps, and any step that waits behind another lands on the
-// critical path.
+// critical path.  Tiles follow one another without a break in the pipeline:
+// the next tile's loads and S^T MMAs start while this one's accumulators are
+// being written out.
+//
+// Cluster partial sums (C > 1): block p owns key rows [p R, (p + 1) R) of
+// the tile, R = 128 / C.  Each block sends the partial sums of rows other
+// blocks own with asynchronous 16-byte stores into the owner's receive
+// region (slot j = sender rank, minus one above the owner), completing on the
+// owner's receive mbarrier; the owner adds the C partial sums in rank order
+// (its own from registers) and stores bf16 dV, dK (dK * scale).  Before a
+// sender reuses a receive region for the next tile it waits until the owner
+// has read it (each owner warp arrives, remotely, on the senders' "region
+// free" mbarrier).
 constexpr int kBwdThreads = 608;  // producer, S issuer, 16 compute warps, dV/dK issuer
 constexpr int kComputeWarps = 16;
 constexpr int kDkvAccWarp = 2 + kComputeWarps;
@@ -134,20 +153,20 @@ struct DkvCfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kKvBytes = kTileN * 128 * kAtoms;  // 128 keys x D
   static constexpr int kQBytes = kTM * 128 * kAtoms;      // TM queries x D
-  static constexpr int kStages = (D == 64) ? 4 : 3;
+  static constexpr int kStages = (D == 64) ? 4 : 2;
   static constexpr int kStageBytes = 2 * kQBytes + 1024;  // Q, dO, then TM row statistics
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kKvBytes;
   static constexpr int kOffStage = 2 * kKvBytes;
-  // D = 64 gathers cluster partial sums by bulk copies into a region of its
-  // own: up to 7/8 of the 128 rows of [dV | dK] fp32 (512 bytes per row).
-  static constexpr bool kBulkEpi = (D == 64);
+  // Receive region for cluster partial sums: (C - 1) R rows of [dV | dK] fp32.
+  static constexpr int kMaxCluster = (D == 64) ? 8 : 2;
+  static constexpr int kRowBytes = 2 * D * 4;
   static constexpr int kOffRecv = kOffStage + kStages * kStageBytes;
-  static constexpr int kRecvBytes = kBulkEpi ? (kTileN - kTileN / 8) * 2 * D * 4 : 0;
+  static constexpr int kRecvBytes = (kTileN - kTileN / kMaxCluster) * kRowBytes;
   static constexpr int kSmemBytes = kOffRecv + kRecvBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
   // S^T at 0 and dP^T at TM (TM fp32 columns each, one per query).  P^T and
-  // dS^T of item li go to buffer li % kNumPB at kColPB + TM * buffer: P^T as
+  // dS^T of item gi go to buffer gi % kNumPB at kColPB + TM * buffer: P^T as
   // packed bf16 pairs over TM/2 columns (two queries per column), dS^T over
   // the next TM/2; group g writes columns g*TM/8 .. of each.
   static constexpr int kNumPB = (D == 64) ? 1 : 2;
@@ -158,24 +177,26 @@ struct DkvCfg {
   static constexpr uint32_t kColDK = kColDV + D;             // dK accumulator, D cols
   static_assert(kColDK + D <= kTmemCols, "TMEM layout");
   static_assert(kTM * 8 <= 1024, "row statistics fit their stage slot");
+  static_assert(kSmemBytes + 512 <= 227 * 1024, "shared memory per block (with the static part)");
 };
-static_assert(kTileN * 2 * 64 * 4 <= DkvCfg<64>::kSmemBytes - 1024, "dK/dV partials fit");
-static_assert(kTileN * 2 * 128 * 4 <= DkvCfg<128>::kSmemBytes - 1024, "dK/dV partials fit");
 
 constexpr int kDkvMaxStages = 4;
 enum : int {
-  kDkvBarKV = 0,
-  kDkvBarQFull = 1,
+  kDkvBarKV = 0,                             // this tile's K, V landed
+  kDkvBarKVFree = 1,                         // the previous tile's S^T MMAs are done with K, V
+  kDkvBarQFull = 2,
   kDkvBarQEmpty = kDkvBarQFull + kDkvMaxStages,
   kDkvBarS = kDkvBarQEmpty + kDkvMaxStages,  // S^T, dP^T of the current item landed
   kDkvBarSFree = kDkvBarS + 1,               // element-wise warps hold them in registers
   kDkvBarP = kDkvBarSFree + 1,               // [2] P^T, dS^T of the buffer's item written
   kDkvBarFree = kDkvBarP + 2,                // [2] dV, dK of the buffer's item done
-  kDkvBarAcc = kDkvBarFree + 2,
-  kDkvBarDrain = kDkvBarAcc + 1,
+  kDkvBarAcc = kDkvBarFree + 2,              // this tile's dV, dK complete
+  kDkvBarAccFree = kDkvBarAcc + 1,           // element-wise warps hold them in registers
+  kDkvBarDrain = kDkvBarAccFree + 1,
   kDkvBarDrainAcc = kDkvBarDrain + 1,
-  kDkvBarRecv = kDkvBarDrainAcc + 1,  // the cluster peers' partial sums landed
-  kDkvNumBars = kDkvBarRecv + 1
+  kDkvBarRecv = kDkvBarDrainAcc + 1,         // the peers' partial sums of this tile landed
+  kDkvBarRegionFree = kDkvBarRecv + 1,       // every peer has read this block's previous sums
+  kDkvNumBars = kDkvBarRegionFree + 1
 };
 
 // TMEM columns [taddr, taddr + N) of this warp's 32 lanes into v (N = 16, 32).
@@ -197,6 +218,13 @@ __device__ __forceinline__ void reg_fence_cols(uint32_t (&v)[N]) {
   else reg_fence32(v);
 }
 
+// One key tile of the dK/dV work, as one block of its cluster sees it.
+struct DkvTile {
+  int b, g, n0;
+  int m_begin, per_head;  // first query tile, query tiles per head
+  int it_lo, n_it;        // this block's chunk of the tile's G * per_head items
+};
+
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
@@ -212,25 +240,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __shared__ uint32_t tmem_slot;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // A cluster of C blocks shares one key tile: the tile's (head, query tile)
-  // items, in ascending order, are cut into C contiguous chunks; block r sums
-  // chunk r in its TMEM, and the C partial sums are added in rank order.
   const int C = a.cluster;
   const int crank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int tile = static_cast<int>(blockIdx.x) / C;
-  // Key tiles near the start of the sequence see the most query tiles under
-  // the causal mask: hand those out first.
-  const int nt = tile / a.BH;
-  const int bg = tile % a.BH;
-  const int b = bg / a.Hkv, g = bg % a.Hkv;
+  const int group = static_cast<int>(blockIdx.x) / C;
+  const int NG = a.n_groups;
+  const int n_tiles_all = a.n_tiles * a.BH;
   const int G = a.Hq / a.Hkv;
-  const int n0 = nt * kTileN;
-  const int m_begin = a.causal ? n0 / TM : 0;
   const int m_end = (a.T + TM - 1) / TM;
-  const int per_head = m_end - m_begin;
-  const int n_all = G * per_head;
-  const int it_lo = static_cast<int>(static_cast<long>(crank) * n_all / C);
-  const int n_it = static_cast<int>(static_cast<long>(crank + 1) * n_all / C) - it_lo;
+  const int R = kTileN / C;
+  // Tile of this cluster's kt-th turn, or -1 past its last.
+  auto tile_of = [&](int kt) {
+    const int t = kt * NG + ((kt & 1) ? NG - 1 - group : group);
+    return t < n_tiles_all ? t : -1;
+  };
+  auto tile_info = [&](int t) {
+    DkvTile ti;
+    const int nt = t / a.BH, bg = t % a.BH;
+    ti.b = bg / a.Hkv;
+    ti.g = bg % a.Hkv;
+    ti.n0 = nt * kTileN;
+    ti.m_begin = a.causal ? ti.n0 / TM : 0;
+    ti.per_head = m_end - ti.m_begin;
+    const int n_all = G * ti.per_head;
+    ti.it_lo = static_cast<int>(static_cast<long>(crank) * n_all / C);
+    ti.n_it = static_cast<int>(static_cast<long>(crank + 1) * n_all / C) - ti.it_lo;
+    return ti;
+  };
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -238,11 +273,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t sK = s0 + Cf::kOffK, sV = s0 + Cf::kOffV;
   auto stage_base = [&](int s) { return s0 + Cf::kOffStage + s * Cf::kStageBytes; };
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
-  // Byte offset of 16-byte chunk `chunk` of partial-sum row `row` (2D floats
-  // per row, chunks XOR-swizzled by row % 8 against bank conflicts).
-  auto partial_off = [](int row, int chunk) {
-    return static_cast<uint32_t>(row * (2 * D * 4) + ((chunk ^ (row & 7)) * 16));
+  // Byte offset of 16-byte chunk `chunk` of row `row` of a receive slot
+  // ([dV | dK] fp32 per row, chunks XOR-swizzled by row % 8).
+  auto slot_off = [](int row, int chunk) {
+    return static_cast<uint32_t>(row * Cf::kRowBytes + ((chunk ^ (row & 7)) * 16));
   };
+  const uint32_t recv_bytes = static_cast<uint32_t>((C - 1) * R * Cf::kRowBytes);
 
   if (warp == 1) {
     tmem_alloc(smem_u32(&tmem_slot), Cf::kTmemCols);
@@ -251,6 +287,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(bar(kDkvBarKV), 1);
+    mbar_init(bar(kDkvBarKVFree), 1);
     for (int s = 0; s < kDkvMaxStages; ++s) {
       mbar_init(bar(kDkvBarQFull + s), 1);
       mbar_init(bar(kDkvBarQEmpty + s), 1);
@@ -262,12 +299,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(kDkvBarFree + i), 1);
     }
     mbar_init(bar(kDkvBarAcc), 1);
+    mbar_init(bar(kDkvBarAccFree), kComputeWarps);
     mbar_init(bar(kDkvBarDrain), 1);
     mbar_init(bar(kDkvBarDrainAcc), 1);
     mbar_init(bar(kDkvBarRecv), 1);
-    // The C - 1 peers each send the R = 128 / C rows this block owns.
-    if (Cf::kBulkEpi && C > 1)
-      mbar_arrive_expect_tx(bar(kDkvBarRecv), (C - 1) * (kTileN / C) * 2 * D * 4);
+    mbar_init(bar(kDkvBarRegionFree), kComputeWarps * (C > 1 ? C - 1 : 1));
+    // The first tile's partial sums may arrive any time from now on.
+    if (C > 1) mbar_arrive_expect_tx(bar(kDkvBarRecv), recv_bytes);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -277,54 +315,60 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tma_prefetch_desc(&mdO);
   }
   __syncthreads();
-  // Peers may send into this block's shared memory (and its mbarrier) once
-  // this arrival is matched by their wait, long before it is needed.
-  if (C > 1) cluster_arrive();
+  // Peers' remote stores and arrivals target this block's mbarriers: they must
+  // be initialised first.
+  if (C > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const uint64_t wait_ns = a.wait_ns;
   bool ok = true;
-  // The element-wise threads' share of the finished dV, dK accumulators
-  // (zero for a block without items), kept for the cluster epilogue.
-  uint32_t part_v[D / 4], part_k[D / 4];
-#pragma unroll
-  for (int i = 0; i < D / 4; ++i) part_v[i] = part_k[i] = 0u;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int last[kDkvMaxStages];
       for (int s = 0; s < kDkvMaxStages; ++s) last[s] = -1;
-      mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * Cf::kKvBytes);
-      for (int at = 0; at < Cf::kAtoms; ++at) {
-        tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, g, n0, b);
-        tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, g, n0, b);
-      }
-      int h = g * G + (n_it > 0 ? it_lo / per_head : 0);
-      int m_idx = n_it > 0 ? it_lo % per_head : 0;
-      for (int li = 0; li < n_it; ++li) {
-        const int s = li % NS;
-        const uint32_t ph = (li / NS) & 1;
-        const int i0 = (m_begin + m_idx) * TM;
-        if (li >= NS && !(ok = mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns))) break;
-        const uint32_t st = stage_base(s);
-        mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + TM * 8);
+      int last_kv = -1;
+      int gi = 0;  // items loaded so far, over all tiles
+      for (int kt = 0; ok; ++kt) {
+        const int t = tile_of(kt);
+        if (t < 0) break;
+        const DkvTile ti = tile_info(t);
+        // K, V of the previous tile must no longer be read.
+        if (kt > 0 && !(ok = mbar_wait(bar(kDkvBarKVFree), (kt - 1) & 1, wait_ns))) break;
+        mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * Cf::kKvBytes);
         for (int at = 0; at < Cf::kAtoms; ++at) {
-          tma_load_4d(st + at * (TM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h, i0, b);
-          tma_load_4d(st + Cf::kQBytes + at * (TM * 128), &mdO, bar(kDkvBarQFull + s), at * 64,
-                      h, i0, b);
+          tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, ti.g, ti.n0, ti.b);
+          tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, ti.g, ti.n0, ti.b);
         }
-        bulk_load(st + 2 * Cf::kQBytes,
-                  a.rowstats + (static_cast<size_t>(b) * a.Hq + h) * a.Tp + i0, TM * 8,
-                  bar(kDkvBarQFull + s));
-        last[s] = li;
-        if (++m_idx == per_head) {
-          m_idx = 0;
-          ++h;
+        last_kv = kt;
+        int h = ti.g * G + (ti.n_it > 0 ? ti.it_lo / ti.per_head : 0);
+        int m_idx = ti.n_it > 0 ? ti.it_lo % ti.per_head : 0;
+        for (int li = 0; li < ti.n_it; ++li, ++gi) {
+          const int s = gi % NS;
+          const uint32_t ph = (gi / NS) & 1;
+          const int i0 = (ti.m_begin + m_idx) * TM;
+          if (gi >= NS && !(ok = mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns))) break;
+          const uint32_t st = stage_base(s);
+          mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + TM * 8);
+          for (int at = 0; at < Cf::kAtoms; ++at) {
+            tma_load_4d(st + at * (TM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h, i0, ti.b);
+            tma_load_4d(st + Cf::kQBytes + at * (TM * 128), &mdO, bar(kDkvBarQFull + s), at * 64,
+                        h, i0, ti.b);
+          }
+          bulk_load(st + 2 * Cf::kQBytes,
+                    a.rowstats + (static_cast<size_t>(ti.b) * a.Hq + h) * a.Tp + i0, TM * 8,
+                    bar(kDkvBarQFull + s));
+          last[s] = gi;
+          if (++m_idx == ti.per_head) {
+            m_idx = 0;
+            ++h;
+          }
         }
       }
       if (!ok) {
-        mbar_wait(bar(kDkvBarKV), 0, wait_ns);
+        // Copies still in flight must land before the block may exit.
+        if (last_kv >= 0) mbar_wait(bar(kDkvBarKV), last_kv & 1, wait_ns);
         for (int s = 0; s < NS; ++s)
           if (last[s] >= 0) mbar_wait(bar(kDkvBarQFull + s), (last[s] / NS) & 1, wait_ns);
       }
@@ -338,31 +382,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
     const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);  // K-major B
     const uint32_t tS = tmem + Cf::kColS, tDP = tmem + Cf::kColDP;
-    ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
-    tc_fence_after();
-    for (int li = 0; li < n_it && ok; ++li) {
-      const int s = li % NS;
-      // The element-wise warps must hold S^T, dP^T of item li - 1 in
-      // registers before those of item li overwrite them.
-      if (li >= 1 && !(ok = warp_all(mbar_wait(bar(kDkvBarSFree), (li - 1) & 1, wait_ns)))) break;
-      if (!(ok = warp_all(mbar_wait(bar(kDkvBarQFull + s), (li / NS) & 1, wait_ns)))) break;
+    int gi = 0;
+    for (int kt = 0; ok; ++kt) {
+      const int t = tile_of(kt);
+      if (t < 0) break;
+      const DkvTile ti = tile_info(t);
+      if (!(ok = warp_all(mbar_wait(bar(kDkvBarKV), kt & 1, wait_ns)))) break;
       tc_fence_after();
-      const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
-      const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
-      // K = D in groups of 64 (one 128-byte swizzle atom): four 32-byte steps.
+      for (int li = 0; li < ti.n_it; ++li, ++gi) {
+        const int s = gi % NS;
+        // The element-wise warps must hold S^T, dP^T of the previous item in
+        // registers before those of this one overwrite them.
+        if (gi >= 1 && !(ok = warp_all(mbar_wait(bar(kDkvBarSFree), (gi - 1) & 1, wait_ns)))) break;
+        if (!(ok = warp_all(mbar_wait(bar(kDkvBarQFull + s), (gi / NS) & 1, wait_ns)))) break;
+        tc_fence_after();
+        const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
+        const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
+        // K = D in groups of 64 (one 128-byte swizzle atom): four 32-byte steps.
 #pragma unroll
-      for (int at = 0; at < Cf::kAtoms; ++at) {
-        const uint64_t k = desc_add(dK, at * (kTileN * 128)), q = desc_add(dQk, at * (TM * 128));
-        mma_ss_x4(tS, k, desc_add(k, 32), desc_add(k, 64), desc_add(k, 96), q, desc_add(q, 32),
-                  desc_add(q, 64), desc_add(q, 96), kIdS, at > 0 ? 1u : 0u);
-      }
+        for (int at = 0; at < Cf::kAtoms; ++at) {
+          const uint64_t k = desc_add(dK, at * (kTileN * 128)), q = desc_add(dQk, at * (TM * 128));
+          mma_ss_x4(tS, k, desc_add(k, 32), desc_add(k, 64), desc_add(k, 96), q, desc_add(q, 32),
+                    desc_add(q, 64), desc_add(q, 96), kIdS, at > 0 ? 1u : 0u);
+        }
 #pragma unroll
-      for (int at = 0; at < Cf::kAtoms; ++at) {
-        const uint64_t v = desc_add(dV, at * (kTileN * 128)), o = desc_add(ddOk, at * (TM * 128));
-        mma_ss_x4(tDP, v, desc_add(v, 32), desc_add(v, 64), desc_add(v, 96), o, desc_add(o, 32),
-                  desc_add(o, 64), desc_add(o, 96), kIdS, at > 0 ? 1u : 0u);
+        for (int at = 0; at < Cf::kAtoms; ++at) {
+          const uint64_t v = desc_add(dV, at * (kTileN * 128)), o = desc_add(ddOk, at * (TM * 128));
+          mma_ss_x4(tDP, v, desc_add(v, 32), desc_add(v, 64), desc_add(v, 96), o, desc_add(o, 32),
+                    desc_add(o, 64), desc_add(o, 96), kIdS, at > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kDkvBarS));
       }
-      mma_commit(bar(kDkvBarS));
+      if (!ok) break;
+      // K, V of this tile are free once these MMAs complete.
+      mma_commit(bar(kDkvBarKVFree));
     }
     // Every issued MMA must finish before TMEM is released.
     mma_commit(bar(kDkvBarDrain));
@@ -374,294 +427,248 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Q, dO as MN-major B operands: 16 queries per 2048-byte step, the
     // 64-column blocks of D = 128 TM * 128 bytes apart.
     const uint64_t dQm0 = sdesc_sw128(stage_base(0), TM * 128, 1024);
-    for (int li = 0; li < n_it && ok; ++li) {
-      const int s = li % NS;
-      const int pb = li % NPB;
-      if (!(ok = warp_all(mbar_wait(bar(kDkvBarP + pb), (li / NPB) & 1, wait_ns)))) break;
-      tc_fence_after();
-      const uint64_t dQm = desc_add(dQm0, s * Cf::kStageBytes);
-      const uint64_t ddOm = desc_add(dQm, Cf::kQBytes);
-      // P^T / dS^T of queries 16ks..16ks+15: 8 packed columns at 8ks.
-      const uint32_t tP = tmem + Cf::kColPB + pb * TM, tDS = tP + TM / 2;
+    int gi = 0;
+    for (int kt = 0; ok; ++kt) {
+      const int t = tile_of(kt);
+      if (t < 0) break;
+      const DkvTile ti = tile_info(t);
+      // The element-wise warps must have read the previous tile's sums before
+      // this tile's first MMA overwrites them -- and before this tile's
+      // completion is signalled at all: a tile without items here signals at
+      // once, and two completions ahead of the readers would alias the
+      // parity they wait on.
+      if (kt > 0 && !(ok = warp_all(mbar_wait(bar(kDkvBarAccFree), (kt - 1) & 1, wait_ns)))) break;
+      for (int li = 0; li < ti.n_it; ++li, ++gi) {
+        const int s = gi % NS;
+        const int pb = gi % NPB;
+        if (!(ok = warp_all(mbar_wait(bar(kDkvBarP + pb), (gi / NPB) & 1, wait_ns)))) break;
+        tc_fence_after();
+        const uint64_t dQm = desc_add(dQm0, s * Cf::kStageBytes);
+        const uint64_t ddOm = desc_add(dQm, Cf::kQBytes);
+        // P^T / dS^T of queries 16ks..16ks+15: 8 packed columns at 8ks.
+        const uint32_t tP = tmem + Cf::kColPB + pb * TM, tDS = tP + TM / 2;
 #pragma unroll
-      for (int q4 = 0; q4 < TM / 64; ++q4) {
-        const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
-        const uint32_t p = tP + q4 * 32;
-        const uint64_t o = desc_add(ddOm, q4 * 8192);
-        mma_ts_x4(tDV, p, p + 8, p + 16, p + 24, o, desc_add(o, 2048), desc_add(o, 4096),
-                  desc_add(o, 6144), kIdAcc, acc);
-      }
+        for (int q4 = 0; q4 < TM / 64; ++q4) {
+          const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
+          const uint32_t p = tP + q4 * 32;
+          const uint64_t o = desc_add(ddOm, q4 * 8192);
+          mma_ts_x4(tDV, p, p + 8, p + 16, p + 24, o, desc_add(o, 2048), desc_add(o, 4096),
+                    desc_add(o, 6144), kIdAcc, acc);
+        }
 #pragma unroll
-      for (int q4 = 0; q4 < TM / 64; ++q4) {
-        const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
-        const uint32_t p = tDS + q4 * 32;
-        const uint64_t q = desc_add(dQm, q4 * 8192);
-        mma_ts_x4(tDK, p, p + 8, p + 16, p + 24, q, desc_add(q, 2048), desc_add(q, 4096),
-                  desc_add(q, 6144), kIdAcc, acc);
+        for (int q4 = 0; q4 < TM / 64; ++q4) {
+          const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
+          const uint32_t p = tDS + q4 * 32;
+          const uint64_t q = desc_add(dQm, q4 * 8192);
+          mma_ts_x4(tDK, p, p + 8, p + 16, p + 24, q, desc_add(q, 2048), desc_add(q, 4096),
+                    desc_add(q, 6144), kIdAcc, acc);
+        }
+        // Both MMA streams of item gi have read stage s (the S^T stream
+        // finished before the element-wise warps released P): free it, and the
+        // P^T / dS^T buffer.
+        mma_commit(bar(kDkvBarQEmpty + s));
+        mma_commit(bar(kDkvBarFree + pb));
       }
-      // Both MMA streams of item li have read stage s (the S^T stream
-      // finished before the element-wise warps released P): free it, and the
-      // P^T / dS^T buffer.
-      mma_commit(bar(kDkvBarQEmpty + s));
-      mma_commit(bar(kDkvBarFree + pb));
+      if (!ok) break;
+      mma_commit(bar(kDkvBarAcc));  // this tile's sums (at once when it has no items)
     }
-    mma_commit(bar(kDkvBarAcc));
     mma_commit(bar(kDkvBarDrainAcc));
     warp_all(mbar_wait(bar(kDkvBarDrainAcc), 0, wait_ns));
   } else {
     // ------------------------------------------------------------ P^T / dS^T warps
     // Warps w, w+4, w+8, w+12 share TMEM lane quarter (w & 3), i.e. the same
     // 32 key rows; group grp = (w - 2) / 4 takes queries QG grp..QG grp+QG-1
-    // of each item.
+    // of each item, and columns grp D/4 .. of dV, dK in the tile epilogue.
     const int quarter = warp & 3;
     const int grp = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
-    const int krow = n0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
-    // K, V must have landed before the cluster epilogue reuses their shared
-    // memory for partial sums (a block with no items reaches it at once).
-    ok = warp_all(mbar_wait(bar(kDkvBarKV), 0, wait_ns));
-    int m_idx = n_it > 0 ? it_lo % per_head : 0;  // query tile of item li within its head
-    for (int li = 0; li < n_it && ok; ++li) {
-      const int s = li % NS;
-      const int pb = li % NPB;
-      const int i0 = (m_begin + m_idx) * TM + grp * QG;  // this group's first query
-      if (++m_idx == per_head) m_idx = 0;
-      ok = warp_all(mbar_wait(bar(kDkvBarS), li & 1, wait_ns));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sv[QG], dp[QG];
-      tmem_ld_cols<QG>(tl + Cf::kColS + grp * QG, sv);
-      tmem_ld_cols<QG>(tl + Cf::kColDP + grp * QG, dp);
-      tmem_wait_ld();
-      reg_fence_cols<QG>(sv);
-      reg_fence_cols<QG>(dp);
-      // S^T, dP^T are in registers: the next item's may overwrite them.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDkvBarSFree));
-      // Causal: query i0 + c sees key krow iff c >= krow - i0.
-      const int cmin = a.causal ? (krow - i0) : -1;
-      const bool need_mask = cmin > 0;
-      uint32_t pk[QG / 2], dk[QG / 2];
-      // (-lse2, -delta) of this group's queries, two per float4.
-      const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * QG * 8;
-#pragma unroll
-      for (int c2 = 0; c2 < QG / 2; ++c2) {
-        const int c = 2 * c2;
-        const float4 rs = ld_shared_f4(st4 + c2 * 16);  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
-        const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rs.x);
-        const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rs.z);
-        float p0, p1;
-        if ((c2 & 7) < kPolyOf8) {
-          p0 = exp2_poly(x0);
-          p1 = exp2_poly(x1);
-        } else {
-          p0 = ex2_approx(x0);
-          p1 = ex2_approx(x1);
-        }
-        if (need_mask) {
-          if (c < cmin) p0 = 0.f;
-          if (c + 1 < cmin) p1 = 0.f;
-        }
-        const float d0 = p0 * (__uint_as_float(dp[c]) + rs.y);
-        const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rs.w);
-        pk[c2] = pack_bf16x2(p0, p1);
-        dk[c2] = pack_bf16x2(d0, d1);
-      }
-      // P^T / dS^T buffer pb last held item li - NPB: its dV, dK must have
-      // read it.
-      if (li >= NPB) {
-        ok = warp_all(mbar_wait(bar(kDkvBarFree + pb), ((li - NPB) / NPB) & 1, wait_ns));
+    const int owner = r / R;  // block of the cluster that stores key row r
+    int gi = 0;
+    for (int kt = 0; ok; ++kt) {
+      const int t = tile_of(kt);
+      if (t < 0) break;
+      const DkvTile ti = tile_info(t);
+      const int krow = ti.n0 + r;
+      int m_idx = ti.n_it > 0 ? ti.it_lo % ti.per_head : 0;  // query tile of the item in its head
+      for (int li = 0; li < ti.n_it && ok; ++li, ++gi) {
+        const int s = gi % NS;
+        const int pb = gi % NPB;
+        const int i0 = (ti.m_begin + m_idx) * TM + grp * QG;  // this group's first query
+        if (++m_idx == ti.per_head) m_idx = 0;
+        ok = warp_all(mbar_wait(bar(kDkvBarS), gi & 1, wait_ns));
         if (!ok) break;
         tc_fence_after();
+        uint32_t sv[QG], dp[QG];
+        tmem_ld_cols<QG>(tl + Cf::kColS + grp * QG, sv);
+        tmem_ld_cols<QG>(tl + Cf::kColDP + grp * QG, dp);
+        tmem_wait_ld();
+        reg_fence_cols<QG>(sv);
+        reg_fence_cols<QG>(dp);
+        // S^T, dP^T are in registers: the next item's may overwrite them.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kDkvBarSFree));
+        // Causal: query i0 + c sees key krow iff c >= krow - i0.
+        const int cmin = a.causal ? (krow - i0) : -1;
+        const bool need_mask = cmin > 0;
+        uint32_t pk[QG / 2], dk[QG / 2];
+        // (-lse2, -delta) of this group's queries, two per float4.
+        const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * QG * 8;
+#pragma unroll
+        for (int c2 = 0; c2 < QG / 2; ++c2) {
+          const int c = 2 * c2;
+          const float4 rs = ld_shared_f4(st4 + c2 * 16);  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
+          const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rs.x);
+          const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rs.z);
+          float p0, p1;
+          if ((c2 & 7) < kPolyOf8) {
+            p0 = exp2_poly(x0);
+            p1 = exp2_poly(x1);
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
+          if (need_mask) {
+            if (c < cmin) p0 = 0.f;
+            if (c + 1 < cmin) p1 = 0.f;
+          }
+          const float d0 = p0 * (__uint_as_float(dp[c]) + rs.y);
+          const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rs.w);
+          pk[c2] = pack_bf16x2(p0, p1);
+          dk[c2] = pack_bf16x2(d0, d1);
+        }
+        // P^T / dS^T buffer pb last held item gi - NPB: its dV, dK must have
+        // read it.
+        if (gi >= NPB) {
+          ok = warp_all(mbar_wait(bar(kDkvBarFree + pb), ((gi - NPB) / NPB) & 1, wait_ns));
+          if (!ok) break;
+          tc_fence_after();
+        }
+        const uint32_t tP = tl + Cf::kColPB + pb * TM + grp * (QG / 2);
+        tmem_st_cols<QG / 2>(tP, pk);
+        tmem_st_cols<QG / 2>(tP + TM / 2, dk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kDkvBarP + pb));
       }
-      const uint32_t tP = tl + Cf::kColPB + pb * TM + grp * (QG / 2);
-      tmem_st_cols<QG / 2>(tP, pk);
-      tmem_st_cols<QG / 2>(tP + TM / 2, dk);
-      tmem_wait_st();
+      if (!ok) break;
+
+      // ---------------------------------------------------------- tile epilogue
+      // This thread's share of key row r: D/4 columns of dV and of dK (zero
+      // for a block without items in the tile).
+      ok = warp_all(mbar_wait(bar(kDkvBarAcc), kt & 1, wait_ns));
+      if (!ok) break;
+      uint32_t part_v[D / 4], part_k[D / 4];
+      if (ti.n_it > 0) {
+        tc_fence_after();
+        tmem_ld_cols<D / 4>(tl + Cf::kColDV + grp * (D / 4), part_v);
+        tmem_ld_cols<D / 4>(tl + Cf::kColDK + grp * (D / 4), part_k);
+        tmem_wait_ld();
+        reg_fence_cols<D / 4>(part_v);
+        reg_fence_cols<D / 4>(part_k);
+      } else {
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) part_v[i] = part_k[i] = 0u;
+      }
+      // The next tile's first dV, dK MMA may overwrite the accumulators.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDkvBarP + pb));
-    }
-    if (ok) ok = warp_all(mbar_wait(bar(kDkvBarAcc), 0, wait_ns));
-    // This thread's share of key row r: D/4 columns of dV and of dK.
-    if (ok && n_it > 0) {
-      tc_fence_after();
-      tmem_ld_cols<D / 4>(tl + Cf::kColDV + grp * (D / 4), part_v);
-      tmem_ld_cols<D / 4>(tl + Cf::kColDK + grp * (D / 4), part_k);
-      tmem_wait_ld();
-      reg_fence_cols<D / 4>(part_v);
-      reg_fence_cols<D / 4>(part_k);
-    }
-    if (Cf::kBulkEpi && C > 1 && r / (kTileN / C) != crank) {
-      // Partial sums of rows another block owns: staged in row order over the
-      // (now idle) K / V / stage memory, rows [p R, (p + 1) R) contiguous for
-      // block p, 16-byte chunks XOR-swizzled by row % 8.
+      if (lane == 0) mbar_arrive(bar(kDkvBarAccFree));
+
+      if (C > 1) {
+        // Rows another block owns: to its receive region, once it has read
+        // the previous tile's.
+        if (kt > 0) {
+          ok = warp_all(mbar_wait(bar(kDkvBarRegionFree), (kt - 1) & 1, wait_ns));
+          if (!ok) break;
+        }
+        if (owner != crank) {
+          const int j = crank < owner ? crank : crank - 1;
+          const int row = j * R + (r - owner * R);
+          const uint32_t dst = map_shared_rank(s0 + Cf::kOffRecv, static_cast<uint32_t>(owner));
+          const uint32_t rbar = map_shared_rank(bar(kDkvBarRecv), static_cast<uint32_t>(owner));
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t* v = which == 0 ? part_v : part_k;
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t* v = which == 0 ? part_v : part_k;
 #pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-          const int chunk = (which * D + grp * (D / 4)) / 4 + i;
-          st_shared_f4(s0 + partial_off(r, chunk),
-                       make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+            for (int i = 0; i < D / 16; ++i) {
+              const int chunk = (which * D + grp * (D / 4)) / 4 + i;
+              st_async_f4(dst + slot_off(row, chunk),
+                          make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                          rbar);
+            }
+          }
+        }
+        // Own rows: this block's sums, then the peers' in rank order.
+        ok = warp_all(mbar_wait(bar(kDkvBarRecv), kt & 1, wait_ns));
+        if (!ok) break;
+        // Arm the receive mbarrier for the next tile's sums.  Peers send them
+        // only after every warp here has signalled (below, after this arm in
+        // program order), and until then the barrier cannot move past the
+        // phase the other warps are still checking.
+        if (warp == 2 && lane == 0 && tile_of(kt + 1) >= 0)
+          mbar_arrive_expect_tx(bar(kDkvBarRecv), recv_bytes);
+        if (owner == crank) {
+          const int rl = r - crank * R;
+          for (int src = 0; src < C; ++src) {
+            if (src == crank) continue;
+            const int j = src < crank ? src : src - 1;
+            const uint32_t slot = s0 + Cf::kOffRecv;
+            const int row = j * R + rl;
+#pragma unroll
+            for (int i = 0; i < D / 16; ++i) {
+              const float4 x = ld_shared_f4(slot + slot_off(row, (grp * (D / 4)) / 4 + i));
+              const float4 y = ld_shared_f4(slot + slot_off(row, (D + grp * (D / 4)) / 4 + i));
+              part_v[4 * i] = __float_as_uint(__uint_as_float(part_v[4 * i]) + x.x);
+              part_v[4 * i + 1] = __float_as_uint(__uint_as_float(part_v[4 * i + 1]) + x.y);
+              part_v[4 * i + 2] = __float_as_uint(__uint_as_float(part_v[4 * i + 2]) + x.z);
+              part_v[4 * i + 3] = __float_as_uint(__uint_as_float(part_v[4 * i + 3]) + x.w);
+              part_k[4 * i] = __float_as_uint(__uint_as_float(part_k[4 * i]) + y.x);
+              part_k[4 * i + 1] = __float_as_uint(__uint_as_float(part_k[4 * i + 1]) + y.y);
+              part_k[4 * i + 2] = __float_as_uint(__uint_as_float(part_k[4 * i + 2]) + y.z);
+              part_k[4 * i + 3] = __float_as_uint(__uint_as_float(part_k[4 * i + 3]) + y.w);
+            }
+          }
+        }
+        // This block's receive region is read: the peers may send the next
+        // tile's sums.
+        __syncwarp();
+        if (lane == 0) {
+          for (int p = 0; p < C; ++p)
+            if (p != crank)
+              mbar_arrive_remote(map_shared_rank(bar(kDkvBarRegionFree), static_cast<uint32_t>(p)));
         }
       }
-    }
-    if (ok && C == 1 && krow < a.T) {
-      const size_t rbase = ((static_cast<size_t>(b) * a.T + krow) * a.Hkv + g) * D + grp * (D / 4);
+      if (owner == crank && krow < a.T) {
+        const size_t rbase =
+            ((static_cast<size_t>(ti.b) * a.T + krow) * a.Hkv + ti.g) * D + grp * (D / 4);
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t* v = which == 0 ? part_v : part_k;
-        const float mul = which == 0 ? 1.f : a.scale;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + rbase);
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t* v = which == 0 ? part_v : part_k;
+          const float mul = which == 0 ? 1.f : a.scale;
+          uint4* dst = reinterpret_cast<uint4*>(
+              static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + rbase);
+          auto f = [&](int i) { return __uint_as_float(v[i]) * mul; };
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i)
-          dst[i] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * i]) * mul, __uint_as_float(v[8 * i + 1]) * mul),
-                              pack_bf16x2(__uint_as_float(v[8 * i + 2]) * mul, __uint_as_float(v[8 * i + 3]) * mul),
-                              pack_bf16x2(__uint_as_float(v[8 * i + 4]) * mul, __uint_as_float(v[8 * i + 5]) * mul),
-                              pack_bf16x2(__uint_as_float(v[8 * i + 6]) * mul, __uint_as_float(v[8 * i + 7]) * mul));
+          for (int i = 0; i < D / 32; ++i)
+            dst[i] = make_uint4(pack_bf16x2(f(8 * i), f(8 * i + 1)), pack_bf16x2(f(8 * i + 2), f(8 * i + 3)),
+                                pack_bf16x2(f(8 * i + 4), f(8 * i + 5)),
+                                pack_bf16x2(f(8 * i + 6), f(8 * i + 7)));
+        }
       }
     }
   }
 
-  if (Cf::kBulkEpi && C > 1) {
-    // Block `crank` owns key rows [crank R, (crank + 1) R) of the tile.  Each
-    // peer's staged rows for it arrive by one bulk copy into slot j (j = src,
-    // or src - 1 above crank) of this block's receive region; the owner
-    // threads then add the C partial sums in rank order (their own from
-    // registers) and store bf16 dV, dK (dK * scale).  The final cluster
-    // barrier keeps every block alive until the copies reading its staged
-    // rows have completed.
-    const int R = kTileN / C;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncthreads();
-    cluster_wait();
-    if (threadIdx.x == 64) {
-      for (int p = 0; p < C; ++p) {
-        if (p == crank) continue;
-        const int j = crank < p ? crank : crank - 1;
-        bulk_copy_to_peer(map_shared_rank(s0 + Cf::kOffRecv + j * R * 2 * D * 4, p),
-                          s0 + p * R * 2 * D * 4, R * 2 * D * 4,
-                          map_shared_rank(bar(kDkvBarRecv), p));
-      }
-    }
-    if (warp >= 2 && warp < 2 + kComputeWarps) {
-      const int r = (warp & 3) * 32 + lane;
-      const int grp = (warp - 2) >> 2;
-      // Whole warps wait (R may be 16: half a warp owns rows).
-      const bool got = warp_all(mbar_wait(bar(kDkvBarRecv), 0, wait_ns));
-      if (!got) ok = false;
-      if (r / R == crank) {
-        const int rl = r - crank * R;
-        float acc_v[D / 4], acc_k[D / 4];
-#pragma unroll
-        for (int i = 0; i < D / 4; ++i) acc_v[i] = acc_k[i] = 0.f;
-        for (int src = 0; src < C; ++src) {
-          if (src == crank) {
-#pragma unroll
-            for (int i = 0; i < D / 4; ++i) {
-              acc_v[i] += __uint_as_float(part_v[i]);
-              acc_k[i] += __uint_as_float(part_k[i]);
-            }
-          } else {
-            const int j = src < crank ? src : src - 1;
-            const uint32_t slot = s0 + Cf::kOffRecv + j * R * 2 * D * 4;
-#pragma unroll
-            for (int i = 0; i < D / 16; ++i) {
-              const float4 x = ld_shared_f4(slot + partial_off(rl, (grp * (D / 4)) / 4 + i));
-              const float4 y = ld_shared_f4(slot + partial_off(rl, (D + grp * (D / 4)) / 4 + i));
-              acc_v[4 * i] += x.x; acc_v[4 * i + 1] += x.y; acc_v[4 * i + 2] += x.z; acc_v[4 * i + 3] += x.w;
-              acc_k[4 * i] += y.x; acc_k[4 * i + 1] += y.y; acc_k[4 * i + 2] += y.z; acc_k[4 * i + 3] += y.w;
-            }
-          }
-        }
-        const int krow_out = n0 + r;
-        if (got && krow_out < a.T) {
-          const size_t rbase =
-              ((static_cast<size_t>(b) * a.T + krow_out) * a.Hkv + g) * D + grp * (D / 4);
-#pragma unroll
-          for (int which = 0; which < 2; ++which) {
-            const float* v = which == 0 ? acc_v : acc_k;
-            const float mul = which == 0 ? 1.f : a.scale;
-            uint4* dst = reinterpret_cast<uint4*>(
-                static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + rbase);
-#pragma unroll
-            for (int i = 0; i < D / 32; ++i)
-              dst[i] = make_uint4(pack_bf16x2(v[8 * i] * mul, v[8 * i + 1] * mul),
-                                  pack_bf16x2(v[8 * i + 2] * mul, v[8 * i + 3] * mul),
-                                  pack_bf16x2(v[8 * i + 4] * mul, v[8 * i + 5] * mul),
-                                  pack_bf16x2(v[8 * i + 6] * mul, v[8 * i + 7] * mul));
-          }
-        }
-      }
-    }
+  // No block may exit while a peer can still store into its shared memory or
+  // arrive on its mbarriers: every block reaches this barrier (no early exit;
+  // all waits above are bounded).
+  if (C > 1) {
     __syncwarp();
     cluster_sync();
-  } else if (C > 1) {
-    // (D = 128) Block `crank` owns key rows [crank R, (crank + 1) R) of the tile.  Every
-    // block writes its partial sums of the rows block p owns into p's shared
-    // memory (slot crank: rows crank R .. of a [C R rows][dV | dK] fp32
-    // array, 16-byte chunks XOR-swizzled by row % 8); p then adds its C slots
-    // in rank order and stores bf16 dV, dK (dK * scale).  The first cluster
-    // barrier makes sure p is past its main loop (its shared memory is free),
-    // the second that every slot has landed.  Every block of the cluster
-    // reaches both (no early exit; all waits above are bounded).
-    const int R = kTileN / C;
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncwarp();
-    cluster_wait();  // matches the arrival after setup
-    cluster_sync();
-    if (warp >= 2 && warp < 2 + kComputeWarps) {
-      const int r = (warp & 3) * 32 + lane;
-      const int grp = (warp - 2) >> 2;
-      const int p = r / R;
-      const uint32_t dst = map_shared_rank(s0, static_cast<uint32_t>(p));
-      const int row = crank * R + (r - p * R);
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t* v = which == 0 ? part_v : part_k;
-#pragma unroll
-        for (int i = 0; i < D / 16; ++i) {
-          const int chunk = (which * D + grp * (D / 4)) / 4 + i;
-          st_shared_cluster_f4(dst + partial_off(row, chunk),
-                               make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                           __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
-        }
-      }
-    }
-    __syncwarp();
-    cluster_sync();
-    if (warp >= 2 && warp < 2 + kComputeWarps) {
-      constexpr int kCpr = 2 * D / 8;  // 8-float output chunks per row ([dV | dK])
-      const int ct = static_cast<int>(threadIdx.x) - 64;
-      for (int e = ct; e < R * kCpr; e += kComputeWarps * 32) {
-        const int rl = e / kCpr, oc = e % kCpr;
-        float acc[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        for (int src = 0; src < C; ++src) {
-          const float4 x = ld_shared_f4(s0 + partial_off(src * R + rl, 2 * oc));
-          const float4 y = ld_shared_f4(s0 + partial_off(src * R + rl, 2 * oc + 1));
-          acc[0] += x.x; acc[1] += x.y; acc[2] += x.z; acc[3] += x.w;
-          acc[4] += y.x; acc[5] += y.y; acc[6] += y.z; acc[7] += y.w;
-        }
-        const bool is_dk = oc * 8 >= D;
-        const float mul = is_dk ? a.scale : 1.f;
-        const int col = oc * 8 - (is_dk ? D : 0);
-        const int krow_out = n0 + crank * R + rl;
-        if (krow_out < a.T) {
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(is_dk ? a.dk : a.dv) +
-                               ((static_cast<size_t>(b) * a.T + krow_out) * a.Hkv + g) * D + col;
-          *reinterpret_cast<uint4*>(dst) =
-              make_uint4(pack_bf16x2(acc[0] * mul, acc[1] * mul), pack_bf16x2(acc[2] * mul, acc[3] * mul),
-                         pack_bf16x2(acc[4] * mul, acc[5] * mul), pack_bf16x2(acc[6] * mul, acc[7] * mul));
-        }
-      }
-    }
   }
 
   if (!ok) atomicOr(&g_bwd_status, 2u);
@@ -1005,6 +1012,25 @@ cudaError_t set_smem_once(K kernel, int bytes, bool* done) {
 }
 
 template <int D>
+cudaError_t dkdv_max_clusters_t(int c, int* out) {
+  static bool done[64] = {};
+  cudaError_t e = set_smem_once(attn_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(c));
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = DkvCfg<D>::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, attn_dkdv_kernel<D>, &cfg);
+}
+
+template <int D>
 cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                           cudaStream_t st) {
@@ -1061,6 +1087,14 @@ cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMa
   return D == 64 ? launch_dkdv_t<64>(grid, mq, mk, mv, mdo, a, st)
                  : launch_dkdv_t<128>(grid, mq, mk, mv, mdo, a, st);
 }
+
+cudaError_t dkdv_max_clusters(int D, int c, int* out) {
+  *out = 0;
+  if (D == 64) return dkdv_max_clusters_t<64>(c, out);
+  if (D == 128) return dkdv_max_clusters_t<128>(c, out);
+  return cudaErrorInvalidValue;
+}
+int dkdv_max_cluster_size(int D) { return D == 64 ? DkvCfg<64>::kMaxCluster : DkvCfg<128>::kMaxCluster; }
 
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,

@@ -51,6 +51,7 @@ struct BwdArgs {
   int n_tiles;           // tiles per (b, head) along T
   int BH;                // B * Hq (dQ) or B * Hkv (dK/dV)
   int cluster;           // dK/dV: blocks sharing one key tile (1, 2, 4 or 8)
+  int n_groups;          // dK/dV: resident clusters (persistent), each walking its key tiles
   int causal;
   float scale;
   float scale_log2;
@@ -61,6 +62,10 @@ struct BwdArgs {
 cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st);
 cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st);
+// Clusters of c blocks of the dK/dV kernel that can be resident at once on the
+// current device (c = 1: blocks), and the largest c the kernel supports.
+cudaError_t dkdv_max_clusters(int D, int c, int* out);
+int dkdv_max_cluster_size(int D);
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                         cudaStream_t st);

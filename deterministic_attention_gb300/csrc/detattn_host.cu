@@ -184,26 +184,60 @@ int sm_count(int* out) {
   return DETATTN_OK;
 }
 
-// Blocks per key tile in the dK/dV kernel.  A key tile's work is G query heads
-// times the query tiles at or after it (causal), so the first tiles carry the
-// most.  The tile is split over C = 1, 2, 4 or 8 blocks (a cluster) until its
-// largest share is no more than 1.5x the average work per resident block.
-// The split depends only on the shape and the SM count, so the summation
-// order, and with it every output bit, is fixed for a given problem and GPU.
-int dkdv_cluster_size(int B, int T, int Hq, int Hkv, int D, int causal, int sms) {
+// Shape of the persistent dK/dV launch: C blocks per key tile (a cluster) and
+// NG resident clusters, dealt the key tiles (heaviest first) in snake order.
+// C is the power of two (up to the kernel's limit for D) that minimises the
+// largest per-block load of that deal, counting a tile's K/V reload and
+// epilogue as two items; NG is every cluster of C blocks that can be resident
+// at once (at most one per tile).  Both depend only on the shape and the
+// device, so the summation order, and with it every output bit, is fixed for
+// a given problem and GPU.  `forced_c` > 0 takes that C (capped at the limit).
+int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int forced_c,
+                  int* c_out, int* ng_out) {
   const int G = Hq / Hkv;
   const int n_tiles = (T + kTileN - 1) / kTileN;
+  const int BH = B * Hkv;
   const int tm = dkdv_tile_m(D);
   const int m_end = (T + tm - 1) / tm;
-  double total = 0.0;
-  for (int nt = 0; nt < n_tiles; ++nt) total += m_end - (causal ? nt * kTileN / tm : 0);
-  total *= static_cast<double>(B) * Hkv * G;
-  const double max_items = static_cast<double>(G) * m_end;
-  const double slots = static_cast<double>(sms);  // one dK/dV block per SM
-  const double avg = total / slots;
-  int c = 1;
-  while (c < 8 && max_items / c > 1.5 * avg && 2 * c <= max_items) c *= 2;
-  return c;
+  const long total = static_cast<long>(n_tiles) * BH;
+  const int cmax = dkdv_max_cluster_size(D);
+  double best = 0.0;
+  *c_out = 0;
+  *ng_out = 0;
+  for (int c = 1; c <= cmax; c *= 2) {
+    if (forced_c > 0 && c != (forced_c < cmax ? forced_c : cmax)) continue;
+    int resident = sms;
+    if (c > 1) {
+      cudaError_t e = dkdv_max_clusters(D, c, &resident);
+      if (e != cudaSuccess) {
+        return fail(DETATTN_ERR_CUDA, "attn_bwd_dkdv: cluster occupancy query: %s",
+                    cudaGetErrorString(e));
+      }
+    }
+    if (resident < 1) continue;
+    const long ng = total < resident ? total : resident;
+    double worst = 0.0;
+    for (long k = 0; k < ng; ++k) {
+      double load = 0.0;
+      for (long kt = 0;; ++kt) {
+        const long t = kt * ng + ((kt & 1) ? ng - 1 - k : k);
+        if (t >= total) break;
+        const int nt = static_cast<int>(t / BH);
+        const int items = G * (m_end - (causal ? nt * kTileN / tm : 0));
+        load += (items + c - 1) / c + 2;
+      }
+      if (load > worst) worst = load;
+    }
+    if (*c_out == 0 || worst < best - 1e-9) {
+      best = worst;
+      *c_out = c;
+      *ng_out = static_cast<int>(ng);
+    }
+  }
+  if (*c_out == 0) {
+    return fail(DETATTN_ERR_CUDA, "attn_bwd_dkdv: no resident cluster shape for D = %d", D);
+  }
+  return DETATTN_OK;
 }
 
 int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
@@ -222,9 +256,10 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
   a.BH = B * Hkv;
   int sms = 0;
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
-  a.cluster = g_dkdv_split > 0 ? g_dkdv_split : dkdv_cluster_size(B, T, Hq, Hkv, D, causal, sms);
-  return launched(launch_dkdv(D, a.n_tiles * a.BH * a.cluster, mq, mk, mv, mdo, a, st),
-                  "attn_bwd_dkdv");
+  if ((rc = dkdv_schedule(B, T, Hq, Hkv, D, causal, sms, g_dkdv_split, &a.cluster, &a.n_groups)) !=
+      DETATTN_OK)
+    return rc;
+  return launched(launch_dkdv(D, a.n_groups * a.cluster, mq, mk, mv, mdo, a, st), "attn_bwd_dkdv");
 }
 
 int dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,

@@ -369,6 +369,21 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, ui
       "r"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// Asynchronous 16-byte store into shared memory of a block of the cluster
+// (`addr`, `bar` from map_shared_rank); completes as 16 transaction bytes on
+// that block's mbarrier `bar`, which also makes the data visible to it.
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float4 v, uint32_t bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(addr),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
+      : "memory");
+}
+// Arrival on an mbarrier of a block of the cluster (`bar` from map_shared_rank),
+// releasing this thread's prior memory operations at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
 // Address of the same shared-memory offset in block `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;

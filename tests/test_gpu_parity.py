@@ -168,6 +168,34 @@ def test_dkdv_split_sizes(split, B, T, Hq, Hkv, D, causal):
     assert_bwd_close([("dK", to_np(dk), dk_r), ("dV", to_np(dv), dv_r)], f"split {split}")
 
 
+@pytest.mark.parametrize("split,D", [(1, 64), (2, 64), (4, 64), (8, 64), (2, 128)])
+def test_dkdv_clusters_walk_several_tiles(split, D):
+    """The persistent dK/dV launch with more key tiles than resident clusters:
+    every cluster walks several tiles, the last ones small enough that some
+    blocks of a cluster get no items of them.  Sampled key rows of early and
+    late tiles match the oracle, and the whole result repeats bit for bit."""
+    import deterministic_attention_gb300 as da
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T, Hq, Hkv = 1024, 3, 1
+    B = max(2, -(-5 * sms // (2 * split * (T // 128))))  # about 2.5 tiles per cluster
+    q, k, v, do = make_inputs(B, T, Hq, Hkv, D, seed=77 + split + D, dout_std=0.2)
+    scale = 1.0 / math.sqrt(D)
+    da.set_dkdv_split(split)
+    try:
+        _, _, _, dk, dv = run_gpu(q, k, v, do, scale, True)
+        _, _, _, dk2, dv2 = run_gpu(q, k, v, do, scale, True)
+    finally:
+        da.set_dkdv_split(0)
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    js = [0, 131, 640, 897, 1023]
+    for b in (0, B - 1):
+        qf, kf, vf, dof = (widen(t[b:b + 1]) for t in (q, k, v, do))
+        dk_r, dv_r = oracle.kv_rows(qf, kf, vf, dof, 0, 0, js, scale, True)
+        got_k = to_np(dk[b:b + 1, js, 0])[0]
+        got_v = to_np(dv[b:b + 1, js, 0])[0]
+        assert_bwd_close([("dK", got_k, dk_r), ("dV", got_v, dv_r)], f"split {split} D {D} b {b}")
+
+
 def test_fma_pipe_exp2_error_bound():
     """The polynomial 2^x used for part of the exponentials: relative error
     <= 1e-4 against exact 2^x over the range the kernels feed it, the pair
