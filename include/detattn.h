@@ -165,11 +165,13 @@ int detattn_diag_exp2(const float* x, float* y_poly, float* y_pair, float* y_sfu
 int detattn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
 
 /* Tuning knob: number of thread blocks that share one 128-key tile in the
- * dK/dV step (1, 2, 4 or 8; 0 = automatic, the default).  The blocks split
- * the tile's (query head, query tile) items into contiguous chunks and add
- * their partial sums in a fixed order, so results stay bitwise reproducible
- * for a given setting; different settings round differently.  Automatic
- * picks from the shape and the SM count only.  Host-side, per process.
+ * dK/dV step (1, 2, 4 or 8; 0 = automatic, the default; at D = 128 values
+ * above 2 act as 2).  The blocks of such a cluster split the tile's (query
+ * head, query tile) items into contiguous chunks and add their partial sums
+ * in a fixed order, so results stay bitwise reproducible for a given
+ * setting; different settings round differently.  Automatic picks from the
+ * shape and the device's resident-cluster count only.  Host-side, per
+ * process.
  * Returns DETATTN_OK or DETATTN_ERR_SHAPE for another value. */
 int detattn_set_dkdv_split(int blocks_per_key_tile);
 
