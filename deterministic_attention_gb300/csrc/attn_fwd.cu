@@ -266,13 +266,30 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tS = tl + C::kColS + (j & 1) * kBN + half * 32;  // this half's columns
+      const int kv0 = j * kBN + half * 32;  // key of this thread's first column
+      // This warp's 32 rows against this half's 32 keys, decided for the
+      // whole warp: every key after every row (or past T) -- P is zero and
+      // the running maximum and sum stay as they are; every key visible -- no
+      // mask.
+      const int row0 = m0 + quarter * 32;
+      const bool all_masked = (a.causal && row0 + 31 < kv0) || kv0 >= a.T;
+      const bool need_mask = (a.causal && kv0 + 31 > row0) || kv0 + 32 > a.T;
+      if (all_masked) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = 0u;
+        tmem_st16_nowait(tS, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarP + (j & 1)));
+        continue;
+      }
       uint32_t sr[32];
       tmem_ld32_nowait(tS, sr);
       tmem_wait_ld();
       reg_fence32(sr);
 
-      const int kv0 = j * kBN + half * 32;  // key of this thread's first column
-      const bool need_mask = a.causal ? (kv0 + 31 > m0) : (kv0 + 32 > a.T);
       const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
       if (need_mask) {
 #pragma unroll
