@@ -5,9 +5,14 @@
 // [seq_len, seq_len] score matrix.  "Step 1" names the per-row logsumexp the
 // forward hands to the backward.
 //
-// One thread block owns one 128-row query tile of one (batch, query head) and
-// walks 64-key tiles 0..diagonal in ascending order:
-//   warp 0      TMA producer: Q once, then K_j / V_j into a ring of stages
+// Work unit: one 128-row query tile of one (batch, query head), walking
+// 64-key tiles 0..diagonal in ascending order.  The kernel is persistent: a
+// block holds NP pipelines (two at D = 64, one at D = 128), each with its own
+// warps, shared memory, mbarriers and TMEM columns, and each pipeline works
+// through the list of units the host dealt it (heaviest first, balanced per
+// SM, so the two pipelines of a block finish together).  Per pipeline:
+//   warp 0      TMA producer: each unit's Q (once the previous unit's Q K^T
+//               MMAs are done with Q), then K_j / V_j into a ring of stages
 //   warp 1      tcgen05 issuer, one key tile ahead of the softmax: S_{j+1} =
 //               Q K_{j+1}^T goes into the other of two TMEM score buffers while
 //               the softmax works on S_j; then O += P_j V_j with P_j read from
@@ -17,11 +22,10 @@
 //               sum and O accumulator (P of keys 0..31 of every tile goes to
 //               O_0, of keys 32..63 to O_1); online softmax in base 2 with a
 //               lazily moved maximum, P to TMEM, O_h rescaled in TMEM when its
-//               maximum moves.  The epilogue merges the two halves once:
+//               maximum moves.  Each unit's epilogue merges the two halves:
 //               O = (O_0 2^(m_0-M) + O_1 2^(m_1-M)) / (l_0 2^(m_0-M) + l_1 2^(m_1-M)),
 //               M = max(m_0, m_1), LSE = ln2 * (M + log2 L).
-// For D = 64 two blocks share an SM (256 TMEM columns each), so one block's
-// prologue and epilogue overlap the other's main loop.
+// The next unit's first scores are computed while this unit's epilogue runs.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -38,7 +42,8 @@ __device__ unsigned int g_fwd_status;
 
 namespace {
 
-constexpr int kThreads = 320;  // producer, MMA issuer, 8 softmax warps
+constexpr int kPipeWarps = 10;  // producer, MMA issuer, 8 softmax warps
+constexpr int kPipeThreads = kPipeWarps * 32;
 constexpr int kBN = kFwdTileN;  // keys per tile (64)
 // The row maximum used in the exponent is only moved when the true maximum
 // exceeds it by more than 2^8; until then P <= 256, which bf16 and the fp32
@@ -61,8 +66,11 @@ struct Cfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKvBytes;
-  static constexpr int kSmemBytes = kOffV + kStages * kKvBytes + 1024;  // + alignment slack
-  static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;
+  static constexpr int kPipeBytes = kOffV + kStages * kKvBytes;  // one pipeline (multiple of 1024)
+  static constexpr int NP = fwd_pipes_per_block(D);
+  static constexpr int kSmemBytes = NP * kPipeBytes + 1024;     // + alignment slack
+  static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;  // per pipeline
+  static_assert(kPipeBytes % 1024 == 0, "pipelines keep the 1024-byte swizzle alignment");
   // Two score buffers of 64 fp32 columns (buffer b at 64 b).  The softmax
   // thread of half h owns columns 32h..32h+31 of a buffer and writes its 32
   // bf16 P values, packed in pairs, over the first 16 of them.
@@ -83,47 +91,76 @@ enum : int {
   kBarOFinal = kBarO + 1,           // the last O += P V has finished
   kBarDrain = kBarOFinal + 1,
   kBarPair = kBarDrain + 1,         // [4]: the two softmax halves of a lane quarter
-  kNumBars = kBarPair + 4
+  kBarQFree = kBarPair + 4,         // the unit's Q K^T MMAs are done with Q
+  kBarOFree = kBarQFree + 1,        // the unit's epilogue has read O
+  kNumBars = kBarOFree + 1
 };
 
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
+__global__ void __launch_bounds__(kPipeThreads * fwd_pipes_per_block(D), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-                    const __grid_constant__ CUtensorMap mV, const FwdArgs a) {
+                    const __grid_constant__ CUtensorMap mV, const FwdArgs a,
+                    const __grid_constant__ FwdSched sched) {
   using C = Cfg<D>;
   constexpr int NS = C::kStages;
+  constexpr int NP = C::NP;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[kNumBars];
+  __shared__ __align__(8) uint64_t bars_all[NP][kNumBars];
   __shared__ uint32_t tmem_slot;
-  __shared__ float red_m[2][kTileM];  // [half][row] final running maxima (log2 units)
-  __shared__ float red_l[2][kTileM];  // [half][row] final row sums
+  __shared__ float red_m_all[NP][2][kTileM];  // [pipe][half][row] final running maxima (log2 units)
+  __shared__ float red_l_all[NP][2][kTileM];  // [pipe][half][row] final row sums
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Heaviest query tiles (most key tiles under the causal mask) are handed out first.
-  const int mt = a.n_m - 1 - static_cast<int>(blockIdx.x) / a.BHq;
-  const int bh = static_cast<int>(blockIdx.x) % a.BHq;
-  const int b = bh / a.Hq, h = bh % a.Hq;
-  const int hkv = h / (a.Hq / a.Hkv);
-  const int m0 = mt * kTileM;
+  const int pipe = static_cast<int>(threadIdx.x) / kPipeThreads;
+  const int warp = (static_cast<int>(threadIdx.x) >> 5) % kPipeWarps;  // role within the pipeline
+  const int lane = threadIdx.x & 31;
+  const int gwarp = static_cast<int>(threadIdx.x) >> 5;               // TMEM lane quarter: gwarp & 3
+  const int pipe_id = static_cast<int>(blockIdx.x) * NP + pipe;
   const int kv_tiles = (a.T + kBN - 1) / kBN;
-  const int n_kv = a.causal ? min(kv_tiles, (m0 + kTileM) / kBN) : kv_tiles;
+  // This pipeline's units: u_of(k) for k = 0 .. n_units - 1.
+  int first = pipe_id, n_units;
+  if (sched.n_listed > 0) {
+    first = sched.start[pipe_id];
+    n_units = sched.start[pipe_id + 1] - first;
+  } else {
+    const int total = a.n_m * a.BHq;
+    n_units = pipe_id < total ? (total - 1 - pipe_id) / sched.n_pipes + 1 : 0;
+  }
+  auto u_of = [&](int k) {
+    return sched.n_listed > 0 ? static_cast<int>(sched.unit[first + k]) : first + k * sched.n_pipes;
+  };
+  struct Unit { int b, h, hkv, m0, n_kv; };
+  auto unit_info = [&](int u) {
+    Unit t;
+    const int mt = a.n_m - 1 - u / a.BHq;
+    const int bh = u % a.BHq;
+    t.b = bh / a.Hq;
+    t.h = bh % a.Hq;
+    t.hkv = t.h / (a.Hq / a.Hkv);
+    t.m0 = mt * kTileM;
+    t.n_kv = a.causal ? min(kv_tiles, (t.m0 + kTileM) / kBN) : kv_tiles;
+    return t;
+  };
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sQ = smem_u32(smem) + C::kOffQ;
-  const uint32_t sK0 = smem_u32(smem) + C::kOffK;
-  const uint32_t sV0 = smem_u32(smem) + C::kOffV;
+  const uint32_t sP = smem_u32(smem) + pipe * C::kPipeBytes;
+  const uint32_t sQ = sP + C::kOffQ;
+  const uint32_t sK0 = sP + C::kOffK;
+  const uint32_t sV0 = sP + C::kOffV;
+  uint64_t* bars = bars_all[pipe];
+  float (*red_m)[kTileM] = red_m_all[pipe];
+  float (*red_l)[kTileM] = red_l_all[pipe];
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+  if (threadIdx.x < 32) {
+    tmem_alloc(smem_u32(&tmem_slot), NP * C::kTmemCols);
     tmem_relinquish();
     tc_fence_before();
   }
-  if (threadIdx.x == 0) {
+  if (warp == 1 && lane == 0) {  // each pipeline's MMA warp sets up its own barriers
     mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(bar(kBarKFull + s), 1);
@@ -139,6 +176,8 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     mbar_init(bar(kBarOFinal), 1);
     mbar_init(bar(kBarDrain), 1);
     for (int qq = 0; qq < 4; ++qq) mbar_init(bar(kBarPair + qq), 64);
+    mbar_init(bar(kBarQFree), 1);
+    mbar_init(bar(kBarOFree), 8);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -148,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_slot;
+  const uint32_t tmem = tmem_slot + pipe * C::kTmemCols;
   const uint64_t wait_ns = a.wait_ns;
   bool ok = true;
 
@@ -157,28 +196,36 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     if (lane == 0) {
       int last_k[kMaxStages], last_v[kMaxStages];
       for (int s = 0; s < kMaxStages; ++s) last_k[s] = last_v[s] = -1;
-      mbar_arrive_expect_tx(bar(kBarQ), C::kQBytes);
-      for (int at = 0; at < C::kAtoms; ++at)
-        tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kBarQ), at * 64, h, m0, b);
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % NS;
-        const uint32_t ph = (j / NS) & 1;
-        if (j >= NS && !(ok = mbar_wait(bar(kBarKEmpty + s), ph ^ 1, wait_ns))) break;
-        mbar_arrive_expect_tx(bar(kBarKFull + s), C::kKvBytes);
+      int last_q = -1;
+      int gj = 0;  // key tiles loaded so far, over all units
+      for (int ku = 0; ku < n_units && ok; ++ku) {
+        const Unit t = unit_info(u_of(ku));
+        // The previous unit's Q K^T MMAs must be done with Q.
+        if (ku > 0 && !(ok = mbar_wait(bar(kBarQFree), (ku - 1) & 1, wait_ns))) break;
+        mbar_arrive_expect_tx(bar(kBarQ), C::kQBytes);
         for (int at = 0; at < C::kAtoms; ++at)
-          tma_load_4d(sK0 + s * C::kKvBytes + at * (kBN * 128), &mK, bar(kBarKFull + s), at * 64,
-                      hkv, j * kBN, b);
-        last_k[s] = j;
-        if (j >= NS && !(ok = mbar_wait(bar(kBarVEmpty + s), ph ^ 1, wait_ns))) break;
-        mbar_arrive_expect_tx(bar(kBarVFull + s), C::kKvBytes);
-        for (int at = 0; at < C::kAtoms; ++at)
-          tma_load_4d(sV0 + s * C::kKvBytes + at * (kBN * 128), &mV, bar(kBarVFull + s), at * 64,
-                      hkv, j * kBN, b);
-        last_v[s] = j;
+          tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kBarQ), at * 64, t.h, t.m0, t.b);
+        last_q = ku;
+        for (int j = 0; j < t.n_kv; ++j, ++gj) {
+          const int s = gj % NS;
+          const uint32_t ph = (gj / NS) & 1;
+          if (gj >= NS && !(ok = mbar_wait(bar(kBarKEmpty + s), ph ^ 1, wait_ns))) break;
+          mbar_arrive_expect_tx(bar(kBarKFull + s), C::kKvBytes);
+          for (int at = 0; at < C::kAtoms; ++at)
+            tma_load_4d(sK0 + s * C::kKvBytes + at * (kBN * 128), &mK, bar(kBarKFull + s), at * 64,
+                        t.hkv, j * kBN, t.b);
+          last_k[s] = gj;
+          if (gj >= NS && !(ok = mbar_wait(bar(kBarVEmpty + s), ph ^ 1, wait_ns))) break;
+          mbar_arrive_expect_tx(bar(kBarVFull + s), C::kKvBytes);
+          for (int at = 0; at < C::kAtoms; ++at)
+            tma_load_4d(sV0 + s * C::kKvBytes + at * (kBN * 128), &mV, bar(kBarVFull + s), at * 64,
+                        t.hkv, j * kBN, t.b);
+          last_v[s] = gj;
+        }
       }
       if (!ok) {
         // Let every copy already issued land before the block's shared memory goes away.
-        mbar_wait(bar(kBarQ), 0, wait_ns);
+        if (last_q >= 0) mbar_wait(bar(kBarQ), last_q & 1, wait_ns);
         for (int s = 0; s < NS; ++s) {
           if (last_k[s] >= 0) mbar_wait(bar(kBarKFull + s), (last_k[s] / NS) & 1, wait_ns);
           if (last_v[s] >= 0) mbar_wait(bar(kBarVFull + s), (last_v[s] / NS) & 1, wait_ns);
@@ -189,44 +236,51 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this loop (MMA issue is warp-collective); every
     // wait is made warp-uniform so the warp stays converged.
-    {
-      constexpr uint32_t kIdQK = idesc_bf16(kTileM, kBN, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, false, true);
-      // Operand descriptors built once; the loops only add constant offsets.
-      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
-      const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(sV0, kBN * 128, 1024);
-      // S_j = Q K_j^T into score buffer j & 1.
-      auto issue_qk = [&](int j) -> bool {
-        const int s = j % NS;
-        if (!warp_all(mbar_wait(bar(kBarKFull + s), (j / NS) & 1, wait_ns))) return false;
-        tc_fence_after();
-        const uint64_t dK = desc_add(dK0, s * C::kKvBytes);
-        const uint32_t tS = tmem + C::kColS + (j & 1) * kBN;
-#pragma unroll
-        for (int g = 0; g < D / 64; ++g) {  // K = 64 per group of four steps
-          const uint64_t q = desc_add(dQ, g * (kTileM * 128)), k = desc_add(dK, g * (kBN * 128));
-          mma_ss_x4(tS, q, desc_add(q, 32), desc_add(q, 64), desc_add(q, 96), k, desc_add(k, 32),
-                    desc_add(k, 64), desc_add(k, 96), kIdQK, g > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(kBarS + (j & 1)));
-        mma_commit(bar(kBarKEmpty + s));
-        return true;
-      };
-      ok = warp_all(mbar_wait(bar(kBarQ), 0, wait_ns));
+    constexpr uint32_t kIdQK = idesc_bf16(kTileM, kBN, false, false);
+    constexpr uint32_t kIdPV = idesc_bf16(kTileM, D, false, true);
+    // Operand descriptors built once; the loops only add constant offsets.
+    const uint64_t dQ = sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(sV0, kBN * 128, 1024);
+    // S of global key tile gj = Q K^T into score buffer gj & 1.
+    auto issue_qk = [&](int gj) -> bool {
+      const int s = gj % NS;
+      if (!warp_all(mbar_wait(bar(kBarKFull + s), (gj / NS) & 1, wait_ns))) return false;
       tc_fence_after();
-      if (ok && n_kv > 0) ok = issue_qk(0);
-      for (int j = 0; j < n_kv && ok; ++j) {
+      const uint64_t dK = desc_add(dK0, s * C::kKvBytes);
+      const uint32_t tS = tmem + C::kColS + (gj & 1) * kBN;
+#pragma unroll
+      for (int g = 0; g < D / 64; ++g) {  // K = 64 per group of four steps
+        const uint64_t q = desc_add(dQ, g * (kTileM * 128)), k = desc_add(dK, g * (kBN * 128));
+        mma_ss_x4(tS, q, desc_add(q, 32), desc_add(q, 64), desc_add(q, 96), k, desc_add(k, 32),
+                  desc_add(k, 64), desc_add(k, 96), kIdQK, g > 0 ? 1u : 0u);
+      }
+      mma_commit(bar(kBarS + (gj & 1)));
+      mma_commit(bar(kBarKEmpty + s));
+      return true;
+    };
+    int gj = 0;
+    for (int ku = 0; ku < n_units && ok; ++ku) {
+      const Unit t = unit_info(u_of(ku));
+      if (!(ok = warp_all(mbar_wait(bar(kBarQ), ku & 1, wait_ns)))) break;
+      tc_fence_after();
+      if (t.n_kv > 0 && !(ok = issue_qk(gj))) break;
+      for (int j = 0; j < t.n_kv && ok; ++j, ++gj) {
         // One tile ahead: S_{j+1} lands in the other buffer while the softmax
         // works on S_j.  That buffer last held P_{j-1}, whose P V was issued
         // in the previous iteration (tcgen05 operations run in issue order).
-        if (j + 1 < n_kv && !(ok = issue_qk(j + 1))) break;
-        const int s = j % NS;
-        if (!(ok = warp_all(mbar_wait(bar(kBarP + (j & 1)), (j >> 1) & 1, wait_ns)))) break;
-        if (!(ok = warp_all(mbar_wait(bar(kBarVFull + s), (j / NS) & 1, wait_ns)))) break;
+        if (j + 1 < t.n_kv && !(ok = issue_qk(gj + 1))) break;
+        const int s = gj % NS;
+        if (!(ok = warp_all(mbar_wait(bar(kBarP + (gj & 1)), (gj >> 1) & 1, wait_ns)))) break;
+        if (!(ok = warp_all(mbar_wait(bar(kBarVFull + s), (gj / NS) & 1, wait_ns)))) break;
+        // The previous unit's epilogue must have read O before this unit's
+        // first P V overwrites it.
+        if (j == 0 && ku > 0 &&
+            !(ok = warp_all(mbar_wait(bar(kBarOFree), (ku - 1) & 1, wait_ns))))
+          break;
         tc_fence_after();
         const uint64_t dV = desc_add(dV0, s * C::kKvBytes);
-        const uint32_t tP = tmem + C::kColS + (j & 1) * kBN;
+        const uint32_t tP = tmem + C::kColS + (gj & 1) * kBN;
         // O_h += P_h V_h over the 32 keys of half h: half h wrote them as 16
         // packed columns at the start of its own 32 score columns.
         static_assert(kBN == 64, "the P V issue below takes 2 steps per half");
@@ -238,140 +292,148 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
         mma_commit(bar(kBarVEmpty + s));
         mma_commit(bar(kBarO));
       }
-      // The epilogue waits on its own barrier: with the issuer a tile ahead,
-      // the per-tile O barrier can trail the softmax by two phases there,
-      // which a parity wait cannot tell apart.
+      if (!ok) break;
+      // Q may be replaced once these MMAs finish; the epilogue waits on its
+      // own barrier (with the issuer a tile ahead, the per-tile O barrier can
+      // trail the softmax by two phases there, which a parity wait cannot
+      // tell apart).
+      mma_commit(bar(kBarQFree));
       mma_commit(bar(kBarOFinal));
-      // Every issued MMA must finish before TMEM is released.
-      mma_commit(bar(kBarDrain));
-      warp_all(mbar_wait(bar(kBarDrain), 0, wait_ns));
     }
+    // Every issued MMA must finish before TMEM is released.
+    mma_commit(bar(kBarDrain));
+    warp_all(mbar_wait(bar(kBarDrain), 0, wait_ns));
   } else {
     // ------------------------------------------------------------ softmax warps
-    // Warps w and w+4 share TMEM lane quarter (w & 3), i.e. the same 32 query
-    // rows; half 0 takes keys 0..31 of each tile, half 1 keys 32..63.  Each
-    // half runs its own online softmax into its own accumulator O_h; the two
-    // meet once, in the epilogue, at an mbarrier of the pair (64 arrivals,
-    // bounded wait).
-    const int quarter = warp & 3;
+    // Warps w and w+4 of a pipeline share a TMEM lane quarter, i.e. the same
+    // 32 query rows; half 0 takes keys 0..31 of each tile, half 1 keys 32..63.
+    // Each half runs its own online softmax into its own accumulator O_h; the
+    // two meet once per unit, in the epilogue, at an mbarrier of the pair (64
+    // arrivals, bounded wait).
+    const int quarter = gwarp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
-    const int qrow = m0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
     const uint32_t pair_bar = bar(kBarPair + quarter);  // the two halves of these rows
-    float m_run = -INFINITY, l_run = 0.f;
-    for (int j = 0; j < n_kv; ++j) {
-      ok = warp_all(mbar_wait(bar(kBarS + (j & 1)), (j >> 1) & 1, wait_ns));
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t tS = tl + C::kColS + (j & 1) * kBN + half * 32;  // this half's columns
-      const int kv0 = j * kBN + half * 32;  // key of this thread's first column
-      // This warp's 32 rows against this half's 32 keys, decided for the
-      // whole warp: every key after every row (or past T) -- P is zero and
-      // the running maximum and sum stay as they are; every key visible -- no
-      // mask.
-      const int row0 = m0 + quarter * 32;
-      const bool all_masked = (a.causal && row0 + 31 < kv0) || kv0 >= a.T;
-      const bool need_mask = (a.causal && kv0 + 31 > row0) || kv0 + 32 > a.T;
-      if (all_masked) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = 0u;
-        tmem_st16_nowait(tS, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarP + (j & 1)));
-        continue;
-      }
-      uint32_t sr[32];
-      tmem_ld32_nowait(tS, sr);
-      tmem_wait_ld();
-      reg_fence32(sr);
-
-      const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-      }
-      // Maximum over this half's 32 columns in four independent chains.
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        mx4[c & 3] = fmax3(mx4[c & 3], __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      // A half-row may see no key in this tile (past its diagonal): mx = -inf
-      // leaves the running maximum alone and every P zero.
-      const float m_new = mx * sl2;
-      float alpha = 1.f;
-      bool moved = false;
-      if (m_new > m_run + kRescaleLog2) {
-        alpha = ex2_approx(m_run - m_new);
-        m_run = m_new;
-        moved = true;
-      }
-      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      const uint64_t sl2x2 = f2_make(sl2, sl2), neg_m = f2_make(-m_use, -m_use);
-      uint64_t sum2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};  // four partial sums
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint64_t x = f2_fma(f2_make(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
-                                  sl2x2, neg_m);
-        float x0, x1, p0, p1;
-        f2_split(x, x0, x1);
-        if ((i & 7) < kPolyOf8) {
-          exp2_poly2(x0, x1, p0, p1);
-        } else {
-          p0 = ex2_approx(x0);
-          p1 = ex2_approx(x1);
-        }
-        if (need_mask) {  // masked keys contribute exactly zero
-          if (2 * i > lim) p0 = 0.f;
-          if (2 * i + 1 > lim) p1 = 0.f;
-        }
-        sum2[i & 1] = f2_add(sum2[i & 1], f2_make(p0, p1));
-        pk[i] = pack_bf16x2(p0, p1);
-      }
-      tmem_st16_nowait(tS, pk);
-      tmem_wait_st();
-      if (j > 0 && __any_sync(0xffffffffu, moved)) {
-        // O_h holds the sum over earlier tiles scaled by the old maximum: wait
-        // for the last P V to land, then rescale O_h in TMEM.  (S_j was
-        // committed after P_{j-2} V, so the O barrier is at most one phase
-        // behind here and the parity wait is exact.)
-        ok = warp_all(mbar_wait(bar(kBarO), (j - 1) & 1, wait_ns));
+    int gj = 0;
+    for (int ku = 0; ku < n_units && ok; ++ku) {
+      const Unit t = unit_info(u_of(ku));
+      const int qrow = t.m0 + r;
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < t.n_kv; ++j, ++gj) {
+        ok = warp_all(mbar_wait(bar(kBarS + (gj & 1)), (gj >> 1) & 1, wait_ns));
         if (!ok) break;
         tc_fence_after();
+        const uint32_t tS = tl + C::kColS + (gj & 1) * kBN + half * 32;  // this half's columns
+        const int kv0 = j * kBN + half * 32;  // key of this thread's first column
+        // This warp's 32 rows against this half's 32 keys, decided for the
+        // whole warp: every key after every row (or past T) -- P is zero and
+        // the running maximum and sum stay as they are; every key visible --
+        // no mask.
+        const int row0 = t.m0 + quarter * 32;
+        const bool all_masked = (a.causal && row0 + 31 < kv0) || kv0 >= a.T;
+        const bool need_mask = (a.causal && kv0 + 31 > row0) || kv0 + 32 > a.T;
+        if (all_masked) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          const uint32_t col = C::kColO + half * D + c * 32;
-          tmem_ld32(tl + col, ov);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tmem_st32_nowait(tl + col, ov);
+          for (int i = 0; i < 16; ++i) pk[i] = 0u;
+          tmem_st16_nowait(tS, pk);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarP + (gj & 1)));
+          continue;
         }
+        uint32_t sr[32];
+        tmem_ld32_nowait(tS, sr);
+        tmem_wait_ld();
+        reg_fence32(sr);
+
+        const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
+        if (need_mask) {
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (c > lim) sr[c] = __float_as_uint(-INFINITY);
+        }
+        // Maximum over this half's 32 columns in four independent chains.
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          mx4[c & 3] = fmax3(mx4[c & 3], __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        // A half-row may see no key in this tile (past its diagonal): mx = -inf
+        // leaves the running maximum alone and every P zero.
+        const float m_new = mx * sl2;
+        float alpha = 1.f;
+        bool moved = false;
+        if (m_new > m_run + kRescaleLog2) {
+          alpha = ex2_approx(m_run - m_new);
+          m_run = m_new;
+          moved = true;
+        }
+        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+        const uint64_t sl2x2 = f2_make(sl2, sl2), neg_m = f2_make(-m_use, -m_use);
+        uint64_t sum2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};  // four partial sums
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t x = f2_fma(f2_make(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                                    sl2x2, neg_m);
+          float x0, x1, p0, p1;
+          f2_split(x, x0, x1);
+          if ((i & 7) < kPolyOf8) {
+            exp2_poly2(x0, x1, p0, p1);
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
+          if (need_mask) {  // masked keys contribute exactly zero
+            if (2 * i > lim) p0 = 0.f;
+            if (2 * i + 1 > lim) p1 = 0.f;
+          }
+          sum2[i & 1] = f2_add(sum2[i & 1], f2_make(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16_nowait(tS, pk);
         tmem_wait_st();
+        if (j > 0 && __any_sync(0xffffffffu, moved)) {
+          // O_h holds the sum over earlier tiles scaled by the old maximum:
+          // wait for the last P V to land, then rescale O_h in TMEM.  (S of
+          // tile gj was committed after P_{gj-2} V, so the O barrier is at
+          // most one phase behind here and the parity wait is exact.)
+          ok = warp_all(mbar_wait(bar(kBarO), (gj - 1) & 1, wait_ns));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            const uint32_t col = C::kColO + half * D + c * 32;
+            tmem_ld32(tl + col, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32_nowait(tl + col, ov);
+          }
+          tmem_wait_st();
+        }
+        float s0, s1, s2, s3;
+        f2_split(sum2[0], s0, s1);
+        f2_split(sum2[1], s2, s3);
+        l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarP + (gj & 1)));
       }
-      float s0, s1, s2, s3;
-      f2_split(sum2[0], s0, s1);
-      f2_split(sum2[1], s2, s3);
-      l_run = l_run * alpha + ((s0 + s1) + (s2 + s3));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarP + (j & 1)));
-    }
-    if (ok) ok = warp_all(mbar_wait(bar(kBarOFinal), 0, wait_ns));
-    // Merge the two halves: M = max(m_0, m_1), f_h = 2^(m_h - M),
-    // L = l_0 f_0 + l_1 f_1 (half 0 first), O = (O_0 f_0 + O_1 f_1) / L.
-    red_m[half][r] = m_run;
-    red_l[half][r] = l_run;
-    mbar_arrive(pair_bar);
-    if (ok) ok = warp_all(mbar_wait(pair_bar, 0, wait_ns));
-    if (ok) {
+      if (!ok) break;
+      ok = warp_all(mbar_wait(bar(kBarOFinal), ku & 1, wait_ns));
+      if (!ok) break;
+      // Merge the two halves: M = max(m_0, m_1), f_h = 2^(m_h - M),
+      // L = l_0 f_0 + l_1 f_1 (half 0 first), O = (O_0 f_0 + O_1 f_1) / L.
+      red_m[half][r] = m_run;
+      red_l[half][r] = l_run;
+      mbar_arrive(pair_bar);
+      ok = warp_all(mbar_wait(pair_bar, ku & 1, wait_ns));
+      if (!ok) break;
       tc_fence_after();
       const float m0v = red_m[0][r], m1v = red_m[1][r];
       const float M = fmaxf(m0v, m1v);  // finite: key 0 is visible to every row
@@ -381,45 +443,49 @@ __global__ void __launch_bounds__(kThreads, D == 64 ? 2 : 1)
       const float w0 = f0 * inv_l, w1 = f1 * inv_l;
       const bool live = qrow < a.T;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
-                            ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * D + half * (D / 2);
+                            ((static_cast<size_t>(t.b) * a.T + qrow) * a.Hq + t.h) * D + half * (D / 2);
+      uint32_t pkd[D / 4];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         uint32_t o0[32], o1[32];
         const uint32_t col = half * (D / 2) + c * 32;
         tmem_ld32(tl + C::kColO + col, o0);
         tmem_ld32(tl + C::kColO + D + col, o1);
-        uint32_t pkd[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pkd[i] = pack_bf16x2(
+          pkd[16 * c + i] = pack_bf16x2(
               fmaf(__uint_as_float(o0[2 * i]), w0, __uint_as_float(o1[2 * i]) * w1),
               fmaf(__uint_as_float(o0[2 * i + 1]), w0, __uint_as_float(o1[2 * i + 1]) * w1));
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
-        }
       }
-      if (live && half == 0)
-        a.lse[(static_cast<size_t>(b) * a.Hq + h) * a.T + qrow] =
-            (M + log2f(l_tot)) * 0.69314718055994530942f;
+      // O is in registers: the next unit's first P V may overwrite it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarOFree));
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i)
+          dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+        if (half == 0)
+          a.lse[(static_cast<size_t>(t.b) * a.Hq + t.h) * a.T + qrow] =
+              (M + log2f(l_tot)) * 0.69314718055994530942f;
+      }
     }
   }
 
   if (!ok) atomicOr(&g_fwd_status, 1u);
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
+  if (threadIdx.x < 32) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc(tmem_slot, NP * C::kTmemCols);
   }
 }
 
 template <int D>
 cudaError_t launch_fwd_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                         const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
+                         const CUtensorMap& mv, const FwdArgs& a, const FwdSched& sched,
+                         cudaStream_t st) {
   const int smem = Cfg<D>::kSmemBytes;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -431,16 +497,17 @@ cudaError_t launch_fwd_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  attn_fwd_kernel<D><<<grid, kThreads, smem, st>>>(mq, mk, mv, a);
+  attn_fwd_kernel<D><<<grid, kPipeThreads * Cfg<D>::NP, smem, st>>>(mq, mk, mv, a, sched);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st) {
-  return D == 64 ? launch_fwd_t<64>(grid, mq, mk, mv, a, st)
-                 : launch_fwd_t<128>(grid, mq, mk, mv, a, st);
+                       const CUtensorMap& mv, const FwdArgs& a, const FwdSched& sched,
+                       cudaStream_t st) {
+  return D == 64 ? launch_fwd_t<64>(grid, mq, mk, mv, a, sched, st)
+                 : launch_fwd_t<128>(grid, mq, mk, mv, a, sched, st);
 }
 
 cudaError_t take_fwd_status(cudaStream_t st, unsigned* out) {

@@ -16,6 +16,22 @@ constexpr int kDqTileN = 64;    // key rows per dQ-kernel KV tile
 // 64 at D = 128 (TMEM must also hold the larger dV, dK accumulators).
 constexpr int dkdv_tile_m(int D) { return D == 64 ? 128 : 64; }
 
+// Static deal of forward work units to persistent pipelines.  Unit u (in
+// heaviest-first order) is query tile n_m - 1 - u / BHq of (b, h) = u % BHq.
+// Pipeline i takes units unit[start[i]] .. unit[start[i + 1] - 1]; with
+// n_listed == 0 it takes units i, i + n_pipes, i + 2 n_pipes, ... instead.
+constexpr int kFwdMaxPipes = 320;
+constexpr int kFwdMaxListed = 1024;
+struct FwdSched {
+  int n_pipes;
+  int n_listed;
+  uint16_t start[kFwdMaxPipes + 1];
+  uint16_t unit[kFwdMaxListed];
+};
+// Pipelines per forward block: two at D = 64 (256 TMEM columns each), one at
+// D = 128.
+constexpr int fwd_pipes_per_block(int D) { return D == 64 ? 2 : 1; }
+
 struct FwdArgs {
   void* o;               // bf16 [B, T, Hq, D]
   float* lse;            // fp32 [B, Hq, T]
@@ -60,7 +76,8 @@ struct BwdArgs {
 
 // Each returns the launch error (cudaSuccess when the kernel was queued).
 cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const FwdArgs& a, cudaStream_t st);
+                       const CUtensorMap& mv, const FwdArgs& a, const FwdSched& sched,
+                       cudaStream_t st);
 cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st);
 // Clusters of c blocks of the dK/dV kernel that can be resident at once on the
 // current device (c = 1: blocks), and the largest c the kernel supports.

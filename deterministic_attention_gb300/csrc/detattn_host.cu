@@ -4,11 +4,13 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+#include <vector>
 
 #include "../../include/detattn.h"
 #include "attn_launch.h"
@@ -129,6 +131,56 @@ int launched(cudaError_t e, const char* what) {
 
 float log2e_times(float scale) { return scale * 1.4426950408889634f; }
 
+int sm_count(int* out);
+
+// Deal of the forward's work units to persistent pipelines (see FwdSched).
+// Heaviest first, each unit goes to the block with the least work so far and
+// within it to the pipeline with the least: the pipelines of one block share
+// an SM, so it is the block totals that must balance.  A unit's work counts
+// its key tiles plus two for its Q load and epilogue.  Beyond the size of the
+// listed form, units are dealt round-robin (many units balance by number).
+// Built on the host from the shape and the SM count only; cached.
+void fwd_schedule(int D, int B, int T, int Hq, int causal, int sms, FwdSched* out, int* grid) {
+  const int NP = fwd_pipes_per_block(D);
+  const int n_m = (T + kTileM - 1) / kTileM;
+  const int BHq = B * Hq;
+  const long units = static_cast<long>(n_m) * BHq;
+  const int kv_tiles = (T + kFwdTileN - 1) / kFwdTileN;
+  long blocks = (units + NP - 1) / NP;
+  if (blocks > sms) blocks = sms;
+  if (blocks < 1) blocks = 1;
+  const int pipes = static_cast<int>(blocks) * NP;
+  out->n_pipes = pipes;
+  *grid = static_cast<int>(blocks);
+  if (units > kFwdMaxListed || pipes > kFwdMaxPipes) {
+    out->n_listed = 0;
+    return;
+  }
+  std::vector<double> block_load(blocks, 0.0), pipe_load(pipes, 0.0);
+  std::vector<std::vector<uint16_t>> lists(pipes);
+  for (long u = 0; u < units; ++u) {
+    const int mt = n_m - 1 - static_cast<int>(u / BHq);
+    const int n_kv = causal ? std::min(kv_tiles, (mt * kTileM + kTileM) / kFwdTileN) : kv_tiles;
+    const double w = n_kv + 2.0;
+    long bi = 0;
+    for (long i = 1; i < blocks; ++i)
+      if (block_load[i] < block_load[bi]) bi = i;
+    int pi = static_cast<int>(bi) * NP;
+    for (int k = 1; k < NP; ++k)
+      if (pipe_load[bi * NP + k] < pipe_load[pi]) pi = static_cast<int>(bi) * NP + k;
+    block_load[bi] += w;
+    pipe_load[pi] += w;
+    lists[pi].push_back(static_cast<uint16_t>(u));
+  }
+  int n = 0;
+  for (int i = 0; i < pipes; ++i) {
+    out->start[i] = static_cast<uint16_t>(n);
+    for (uint16_t u : lists[i]) out->unit[n++] = u;
+  }
+  out->start[pipes] = static_cast<uint16_t>(n);
+  out->n_listed = n;
+}
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
              int Hq, int Hkv, int D, float scale, int causal, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
@@ -147,7 +199,26 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.causal = causal;
   a.scale_log2 = log2e_times(scale);
   a.wait_ns = g_wait_ns;
-  return launched(launch_fwd(D, a.n_m * a.BHq, mq, mk, mv, a, st), "attn_fwd");
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
+  // The schedule depends only on (D, B, T, Hq, causal, SMs): keep the last one.
+  static std::mutex mu;
+  static int key[6] = {-1, -1, -1, -1, -1, -1};
+  static FwdSched sched;
+  static int grid = 0;
+  FwdSched sc;
+  int g;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    const int want[6] = {D, B, T, Hq, causal, sms};
+    if (!std::equal(want, want + 6, key)) {
+      fwd_schedule(D, B, T, Hq, causal, sms, &sched, &grid);
+      std::copy(want, want + 6, key);
+    }
+    sc = sched;
+    g = grid;
+  }
+  return launched(launch_fwd(D, g, mq, mk, mv, a, sc, st), "attn_fwd");
 }
 
 int delta_impl(const void* o, const void* dout, const float* lse, void* workspace, int B, int T,
