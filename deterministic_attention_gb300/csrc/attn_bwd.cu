@@ -682,11 +682,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ============================================================== dQ
-constexpr int kDqThreads = 320;  // producer, MMA issuer, 8 compute warps
-// Block = (b, query head, 128-query tile).  Warp 0 loads Q, dO once and the
-// K, V of 64-key tiles 0..diagonal in ascending order; warp 1 issues
-// S = Q K^T, dP = dO V^T and dQ += dS K with dS read from TMEM; warps 2..5
-// (thread r = query row r) form P and dS.
+// Work unit: one 128-query tile of one (b, query head), over 64-key tiles
+// 0..diagonal in ascending order.  Persistent like the forward: a block holds
+// NP pipelines (two at D = 64, one at D = 128), each with its own warps,
+// shared memory, mbarriers and TMEM columns, working through the units the
+// host dealt it.  Per pipeline, warp 0 loads each unit's Q, dO and the K, V
+// ring; warp 1 issues S = Q K^T, dP = dO V^T and dQ += dS K with dS read from
+// TMEM; warps 2..9 (two threads per query row, one per 32-key half) form P
+// and dS and, at the unit's end, write dQ.
+constexpr int kDqPipeWarps = 10;  // producer, MMA issuer, 8 compute warps
+constexpr int kDqPipeThreads = kDqPipeWarps * 32;
 template <int D>
 struct DqCfg {
   static constexpr int kAtoms = D / 64;
@@ -697,57 +702,86 @@ struct DqCfg {
   static constexpr int kOffdO = kQBytes;
   static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKvBytes;
-  static constexpr int kSmemBytes = kOffV + kStages * kKvBytes + 1024;
-  static constexpr uint32_t kTmemCols = 256;
+  static constexpr int kPipeBytes = kOffV + kStages * kKvBytes;  // multiple of 1024
+  static constexpr int NP = qtile_pipes_per_block(D);
+  static constexpr int kSmemBytes = NP * kPipeBytes + 1024;
+  static constexpr uint32_t kTmemCols = 256;  // per pipeline (D = 64: 2 x 256)
   static constexpr uint32_t kColS = 0;    // S fp32 [128 x 64]; dS bf16 over cols 0..31
   static constexpr uint32_t kColDP = 64;  // dP fp32 [128 x 64]
   static constexpr uint32_t kColDQ = 128; // dQ accumulator, D cols
-  // For D = 64 the block's Q and dO tiles also live in TMEM (packed bf16
+  // For D = 64 the unit's Q and dO tiles also live in TMEM (packed bf16
   // pairs, 32 columns each), so S = Q K^T and dP = dO V^T read only K / V from
   // shared memory: an N = 64 MMA with both operands in shared memory is bound
   // by shared-memory bandwidth (48 clocks against 32 for the math).
   static constexpr bool kQInTmem = (D == 64);
   static constexpr uint32_t kColQ = 192;
   static constexpr uint32_t kColdO = 224;
+  static_assert(kPipeBytes % 1024 == 0, "pipelines keep the 1024-byte swizzle alignment");
+  static_assert(D == 64 || NP == 1, "D = 128 needs a block's whole TMEM");
 };
 
 enum : int { kDqBarQ = 0, kDqBarKFull = 1, kDqBarVFull = 4, kDqBarKEmpty = 7, kDqBarVEmpty = 10,
              kDqBarS = 13, kDqBarDS = 14, kDqBarAcc = 15, kDqBarDrain = 16, kDqBarQTmem = 17,
-             kDqNumBars = 18 };
+             kDqBarQUsed = 18,   // the unit's S, dP MMAs are done (Q, dO no longer read)
+             kDqBarAccFree = 19, // the unit's epilogue has read dQ
+             kDqNumBars = 20 };
 
 template <int D>
-__global__ void __launch_bounds__(kDqThreads, 2)
+__global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
-                   const BwdArgs a) {
+                   const BwdArgs a, const __grid_constant__ QTileSched sched) {
   using C = DqCfg<D>;
   constexpr int NS = C::kStages;
+  constexpr int NP = C::NP;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars[kDqNumBars];
+  __shared__ __align__(8) uint64_t bars_all[NP][kDqNumBars];
   __shared__ uint32_t tmem_slot;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = a.n_tiles - 1 - static_cast<int>(blockIdx.x) / a.BH;
-  const int bh = static_cast<int>(blockIdx.x) % a.BH;
-  const int b = bh / a.Hq, h = bh % a.Hq;
-  const int hkv = h / (a.Hq / a.Hkv);
-  const int m0 = mt * kTileM;
+  const int pipe = static_cast<int>(threadIdx.x) / kDqPipeThreads;
+  const int warp = (static_cast<int>(threadIdx.x) >> 5) % kDqPipeWarps;  // role within the pipeline
+  const int lane = threadIdx.x & 31;
+  const int gwarp = static_cast<int>(threadIdx.x) >> 5;                  // TMEM lane quarter: gwarp & 3
+  const int pipe_id = static_cast<int>(blockIdx.x) * NP + pipe;
   const int kv_tiles = (a.T + kDqTileN - 1) / kDqTileN;
-  const int n_kv = a.causal ? min(kv_tiles, (m0 + kTileM) / kDqTileN) : kv_tiles;
+  int first = pipe_id, n_units;
+  if (sched.n_listed > 0) {
+    first = sched.start[pipe_id];
+    n_units = sched.start[pipe_id + 1] - first;
+  } else {
+    const int total = a.n_tiles * a.BH;
+    n_units = pipe_id < total ? (total - 1 - pipe_id) / sched.n_pipes + 1 : 0;
+  }
+  auto u_of = [&](int k) {
+    return sched.n_listed > 0 ? static_cast<int>(sched.unit[first + k]) : first + k * sched.n_pipes;
+  };
+  struct Unit { int b, h, hkv, m0, n_kv; };
+  auto unit_info = [&](int u) {
+    Unit t;
+    const int mt = a.n_tiles - 1 - u / a.BH;
+    const int bh = u % a.BH;
+    t.b = bh / a.Hq;
+    t.h = bh % a.Hq;
+    t.hkv = t.h / (a.Hq / a.Hkv);
+    t.m0 = mt * kTileM;
+    t.n_kv = a.causal ? min(kv_tiles, (t.m0 + kTileM) / kDqTileN) : kv_tiles;
+    return t;
+  };
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t s0 = smem_u32(smem);
+  const uint32_t s0 = smem_u32(smem) + pipe * C::kPipeBytes;
   const uint32_t sQ = s0 + C::kOffQ, sdO = s0 + C::kOffdO;
   const uint32_t sK0 = s0 + C::kOffK, sV0 = s0 + C::kOffV;
+  uint64_t* bars = bars_all[pipe];
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
-  if (warp == 1) {
-    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
+  if (threadIdx.x < 32) {
+    tmem_alloc(smem_u32(&tmem_slot), NP * C::kTmemCols);
     tmem_relinquish();
     tc_fence_before();
   }
-  if (threadIdx.x == 0) {
+  if (warp == 1 && lane == 0) {  // each pipeline's MMA warp sets up its own barriers
     mbar_init(bar(kDqBarQ), 1);
     for (int s = 0; s < 3; ++s) {
       mbar_init(bar(kDqBarKFull + s), 1);
@@ -760,6 +794,8 @@ __global__ void __launch_bounds__(kDqThreads, 2)
     mbar_init(bar(kDqBarAcc), 1);
     mbar_init(bar(kDqBarDrain), 1);
     mbar_init(bar(kDqBarQTmem), 8);
+    mbar_init(bar(kDqBarQUsed), 1);
+    mbar_init(bar(kDqBarAccFree), 8);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -770,36 +806,47 @@ __global__ void __launch_bounds__(kDqThreads, 2)
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_slot;
+  const uint32_t tmem = tmem_slot + pipe * C::kTmemCols;
   const uint64_t wait_ns = a.wait_ns;
   bool ok = true;
 
   if (warp == 0) {
     if (lane == 0) {
       int last_k[3] = {-1, -1, -1}, last_v[3] = {-1, -1, -1};
-      mbar_arrive_expect_tx(bar(kDqBarQ), 2 * C::kQBytes);
-      for (int at = 0; at < C::kAtoms; ++at) {
-        tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kDqBarQ), at * 64, h, m0, b);
-        tma_load_4d(sdO + at * (kTileM * 128), &mdO, bar(kDqBarQ), at * 64, h, m0, b);
-      }
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % NS;
-        const uint32_t ph = (j / NS) & 1;
-        if (j >= NS && !(ok = mbar_wait(bar(kDqBarKEmpty + s), ph ^ 1, wait_ns))) break;
-        mbar_arrive_expect_tx(bar(kDqBarKFull + s), C::kKvBytes);
-        for (int at = 0; at < C::kAtoms; ++at)
-          tma_load_4d(sK0 + s * C::kKvBytes + at * (kDqTileN * 128), &mK, bar(kDqBarKFull + s),
-                      at * 64, hkv, j * kDqTileN, b);
-        last_k[s] = j;
-        if (j >= NS && !(ok = mbar_wait(bar(kDqBarVEmpty + s), ph ^ 1, wait_ns))) break;
-        mbar_arrive_expect_tx(bar(kDqBarVFull + s), C::kKvBytes);
-        for (int at = 0; at < C::kAtoms; ++at)
-          tma_load_4d(sV0 + s * C::kKvBytes + at * (kDqTileN * 128), &mV, bar(kDqBarVFull + s),
-                      at * 64, hkv, j * kDqTileN, b);
-        last_v[s] = j;
+      int last_q = -1;
+      int gj = 0;  // key tiles loaded so far, over all units
+      for (int ku = 0; ku < n_units && ok; ++ku) {
+        const Unit t = unit_info(u_of(ku));
+        // The previous unit's Q, dO must no longer be read: copied to TMEM
+        // (D = 64) or consumed by its S, dP MMAs (D = 128).
+        if (ku > 0 && !(ok = mbar_wait(bar(C::kQInTmem ? kDqBarQTmem : kDqBarQUsed), (ku - 1) & 1,
+                                       wait_ns)))
+          break;
+        mbar_arrive_expect_tx(bar(kDqBarQ), 2 * C::kQBytes);
+        for (int at = 0; at < C::kAtoms; ++at) {
+          tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kDqBarQ), at * 64, t.h, t.m0, t.b);
+          tma_load_4d(sdO + at * (kTileM * 128), &mdO, bar(kDqBarQ), at * 64, t.h, t.m0, t.b);
+        }
+        last_q = ku;
+        for (int j = 0; j < t.n_kv; ++j, ++gj) {
+          const int s = gj % NS;
+          const uint32_t ph = (gj / NS) & 1;
+          if (gj >= NS && !(ok = mbar_wait(bar(kDqBarKEmpty + s), ph ^ 1, wait_ns))) break;
+          mbar_arrive_expect_tx(bar(kDqBarKFull + s), C::kKvBytes);
+          for (int at = 0; at < C::kAtoms; ++at)
+            tma_load_4d(sK0 + s * C::kKvBytes + at * (kDqTileN * 128), &mK, bar(kDqBarKFull + s),
+                        at * 64, t.hkv, j * kDqTileN, t.b);
+          last_k[s] = gj;
+          if (gj >= NS && !(ok = mbar_wait(bar(kDqBarVEmpty + s), ph ^ 1, wait_ns))) break;
+          mbar_arrive_expect_tx(bar(kDqBarVFull + s), C::kKvBytes);
+          for (int at = 0; at < C::kAtoms; ++at)
+            tma_load_4d(sV0 + s * C::kKvBytes + at * (kDqTileN * 128), &mV, bar(kDqBarVFull + s),
+                        at * 64, t.hkv, j * kDqTileN, t.b);
+          last_v[s] = gj;
+        }
       }
       if (!ok) {
-        mbar_wait(bar(kDqBarQ), 0, wait_ns);
+        if (last_q >= 0) mbar_wait(bar(kDqBarQ), last_q & 1, wait_ns);
         for (int s = 0; s < NS; ++s) {
           if (last_k[s] >= 0) mbar_wait(bar(kDqBarKFull + s), (last_k[s] / NS) & 1, wait_ns);
           if (last_v[s] >= 0) mbar_wait(bar(kDqBarVFull + s), (last_v[s] / NS) & 1, wait_ns);
@@ -809,20 +856,22 @@ __global__ void __launch_bounds__(kDqThreads, 2)
   } else if (warp == 1) {
     // MMA issuer: the whole warp runs the loop (MMA issue is warp-collective);
     // every wait is made warp-uniform so the warp stays converged.
-    {
-      const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ;
-      constexpr uint32_t kIdS = idesc_bf16(kTileM, kDqTileN, false, false);
-      constexpr uint32_t kIdDQ = idesc_bf16(kTileM, D, false, true);
-      // Operand descriptors built once; the loops only add constant offsets.
-      const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), ddO = sdesc_sw128(sdO, 16, 1024);
-      const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024), dV0 = sdesc_sw128(sV0, 16, 1024);
-      const uint64_t dKm0 = sdesc_sw128(sK0, kDqTileN * 128, 1024);  // K as MN-major B
-      ok = warp_all(mbar_wait(bar(kDqBarQ), 0, wait_ns));
-      if (ok && C::kQInTmem) ok = warp_all(mbar_wait(bar(kDqBarQTmem), 0, wait_ns));
+    const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ;
+    constexpr uint32_t kIdS = idesc_bf16(kTileM, kDqTileN, false, false);
+    constexpr uint32_t kIdDQ = idesc_bf16(kTileM, D, false, true);
+    // Operand descriptors built once; the loops only add constant offsets.
+    const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), ddO = sdesc_sw128(sdO, 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024), dV0 = sdesc_sw128(sV0, 16, 1024);
+    const uint64_t dKm0 = sdesc_sw128(sK0, kDqTileN * 128, 1024);  // K as MN-major B
+    int gj = 0;
+    for (int ku = 0; ku < n_units && ok; ++ku) {
+      const Unit t = unit_info(u_of(ku));
+      if (!(ok = warp_all(mbar_wait(bar(kDqBarQ), ku & 1, wait_ns)))) break;
+      if (C::kQInTmem && !(ok = warp_all(mbar_wait(bar(kDqBarQTmem), ku & 1, wait_ns)))) break;
       tc_fence_after();
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int s = j % NS;
-        const uint32_t ph = (j / NS) & 1;
+      for (int j = 0; j < t.n_kv && ok; ++j, ++gj) {
+        const int s = gj % NS;
+        const uint32_t ph = (gj / NS) & 1;
         const uint64_t dK = desc_add(dK0, s * C::kKvBytes), dV = desc_add(dV0, s * C::kKvBytes);
         const uint64_t dKm = desc_add(dKm0, s * C::kKvBytes);
         if (!(ok = warp_all(mbar_wait(bar(kDqBarKFull + s), ph, wait_ns)))) break;
@@ -855,7 +904,13 @@ __global__ void __launch_bounds__(kDqThreads, 2)
         }
         mma_commit(bar(kDqBarS));
         mma_commit(bar(kDqBarVEmpty + s));
-        if (!(ok = warp_all(mbar_wait(bar(kDqBarDS), j & 1, wait_ns)))) break;
+        if (j + 1 == t.n_kv) mma_commit(bar(kDqBarQUsed));  // the unit's last S, dP
+        if (!(ok = warp_all(mbar_wait(bar(kDqBarDS), gj & 1, wait_ns)))) break;
+        // The previous unit's epilogue must have read dQ before this unit's
+        // first dQ MMA overwrites it.
+        if (j == 0 && ku > 0 &&
+            !(ok = warp_all(mbar_wait(bar(kDqBarAccFree), (ku - 1) & 1, wait_ns))))
+          break;
         tc_fence_after();
         // dS of keys 16ks..16ks+15: half ks/2 wrote its 32 keys as 16 packed
         // columns at the start of its own 32 S columns.
@@ -864,30 +919,33 @@ __global__ void __launch_bounds__(kDqThreads, 2)
                   desc_add(dKm, 6144), kIdDQ, j > 0 ? 1u : 0u);
         mma_commit(bar(kDqBarKEmpty + s));
       }
+      if (!ok) break;
       mma_commit(bar(kDqBarAcc));
-      mma_commit(bar(kDqBarDrain));
-      warp_all(mbar_wait(bar(kDqBarDrain), 0, wait_ns));
     }
+    mma_commit(bar(kDqBarDrain));
+    warp_all(mbar_wait(bar(kDqBarDrain), 0, wait_ns));
   } else {
-    // Eight warps: warps w and w+4 share TMEM lane quarter (w & 3), i.e. the
-    // same 32 query rows; half 0 takes key columns 0..31 of the tile, half 1
-    // columns 32..63.  Each half writes its dS (bf16 pairs) over the first 16
-    // of its own 32 S columns.
-    const int quarter = warp & 3;
+    // Eight warps: warps w and w+4 of a pipeline share a TMEM lane quarter,
+    // i.e. the same 32 query rows; half 0 takes key columns 0..31 of the tile,
+    // half 1 columns 32..63.  Each half writes its dS (bf16 pairs) over the
+    // first 16 of its own 32 S columns.
+    const int quarter = gwarp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
-    const int qrow = m0 + r;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const uint32_t tS = tl + C::kColS + half * 32, tDP = tl + C::kColDP + half * 32;
     const float sl2 = a.scale_log2;
-    // (-LSE*log2e, -Delta) of this row; rows past T read (-inf, -0): P = 0.
-    const float2 rstat = a.rowstats[(static_cast<size_t>(b) * a.Hq + h) * a.Tp + qrow];
-    if (C::kQInTmem) {
-      // Q and dO row r into TMEM as the A operands of S and dP: this warp
-      // copies elements 32 half..32 half+31 (four 16-byte chunks of the
-      // 128-byte-swizzled tile row) as 16 packed pairs.
-      ok = warp_all(mbar_wait(bar(kDqBarQ), 0, wait_ns));
-      if (ok) {
+    // Q and dO row r of unit ku into TMEM as the A operands of S and dP, once
+    // the previous unit's S, dP MMAs no longer read them: this warp copies
+    // elements 32 half..32 half+31 (four 16-byte chunks of the
+    // 128-byte-swizzled tile row) as 16 packed pairs.  Done for the next unit
+    // before this unit's epilogue, so its first S, dP overlap the epilogue.
+    auto copy_q = [&](int ku) -> bool {
+      bool good = true;
+      if (ku > 0) good = warp_all(mbar_wait(bar(kDqBarQUsed), (ku - 1) & 1, wait_ns));
+      if (good) good = warp_all(mbar_wait(bar(kDqBarQ), ku & 1, wait_ns));
+      if (good) {
+        tc_fence_after();
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           const uint32_t base = (which == 0 ? sQ : sdO) + r * 128;
@@ -907,71 +965,85 @@ __global__ void __launch_bounds__(kDqThreads, 2)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kDqBarQTmem));
-    }
-    for (int j = 0; j < n_kv && ok; ++j) {
-      ok = warp_all(mbar_wait(bar(kDqBarS), j & 1, wait_ns));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sv[32], dp[32];
-      tmem_ld32_nowait(tS, sv);
-      tmem_ld32_nowait(tDP, dp);
-      tmem_wait_ld();
-      reg_fence32(sv);
-      reg_fence32(dp);
-      const int kv0 = j * kDqTileN + half * 32;  // key of this half's first column
-      // key kv0 + c visible iff c <= lim
-      const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
-      uint32_t dsk[16];
-      const bool need_mask = a.causal ? (kv0 + 31 > m0) : (kv0 + 32 > a.T);
+      return good;
+    };
+    if (C::kQInTmem && n_units > 0) ok = copy_q(0);
+    int gj = 0;
+    for (int ku = 0; ku < n_units && ok; ++ku) {
+      const Unit t = unit_info(u_of(ku));
+      const int qrow = t.m0 + r;
+      // (-LSE*log2e, -Delta) of this row; rows past T read (-inf, -0): P = 0.
+      const float2 rstat = a.rowstats[(static_cast<size_t>(t.b) * a.Hq + t.h) * a.Tp + qrow];
+      for (int j = 0; j < t.n_kv; ++j, ++gj) {
+        ok = warp_all(mbar_wait(bar(kDqBarS), gj & 1, wait_ns));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[32], dp[32];
+        tmem_ld32_nowait(tS, sv);
+        tmem_ld32_nowait(tDP, dp);
+        tmem_wait_ld();
+        reg_fence32(sv);
+        reg_fence32(dp);
+        const int kv0 = j * kDqTileN + half * 32;  // key of this half's first column
+        // key kv0 + c visible iff c <= lim
+        const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
+        uint32_t dsk[16];
+        const bool need_mask = a.causal ? (kv0 + 31 > t.m0) : (kv0 + 32 > a.T);
 #pragma unroll
-      for (int c2 = 0; c2 < 16; ++c2) {
-        const int c = 2 * c2;
-        const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rstat.x);
-        const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rstat.x);
-        float p0, p1;
-        if ((c2 & 7) < kPolyOf8) {
-          p0 = exp2_poly(x0);
-          p1 = exp2_poly(x1);
-        } else {
-          p0 = ex2_approx(x0);
-          p1 = ex2_approx(x1);
+        for (int c2 = 0; c2 < 16; ++c2) {
+          const int c = 2 * c2;
+          const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rstat.x);
+          const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rstat.x);
+          float p0, p1;
+          if ((c2 & 7) < kPolyOf8) {
+            p0 = exp2_poly(x0);
+            p1 = exp2_poly(x1);
+          } else {
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+          }
+          if (need_mask) {
+            if (c > lim) p0 = 0.f;
+            if (c + 1 > lim) p1 = 0.f;
+          }
+          const float d0 = p0 * (__uint_as_float(dp[c]) + rstat.y);
+          const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rstat.y);
+          dsk[c2] = pack_bf16x2(d0, d1);
         }
-        if (need_mask) {
-          if (c > lim) p0 = 0.f;
-          if (c + 1 > lim) p1 = 0.f;
-        }
-        const float d0 = p0 * (__uint_as_float(dp[c]) + rstat.y);
-        const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rstat.y);
-        dsk[c2] = pack_bf16x2(d0, d1);
+        tmem_st16_nowait(tS, dsk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kDqBarDS));
       }
-      tmem_st16_nowait(tS, dsk);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDqBarDS));
-    }
-    if (ok) ok = warp_all(mbar_wait(bar(kDqBarAcc), 0, wait_ns));
-    if (ok) {
+      if (!ok) break;
+      if (C::kQInTmem && ku + 1 < n_units && !(ok = copy_q(ku + 1))) break;
+      ok = warp_all(mbar_wait(bar(kDqBarAcc), ku & 1, wait_ns));
+      if (!ok) break;
       tc_fence_after();
       const bool live = qrow < a.T;
       __nv_bfloat16* dqrow = static_cast<__nv_bfloat16*>(a.dq) +
-                             ((static_cast<size_t>(b) * a.T + qrow) * a.Hq + h) * D;
+                             ((static_cast<size_t>(t.b) * a.T + qrow) * a.Hq + t.h) * D;
+      uint32_t pkd[D / 4];
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
         const int c = half * (D / 64) + cc;  // this half's 32-column chunks of dQ
         uint32_t v[32];
         tmem_ld32(tl + C::kColDQ + c * 32, v);
-        uint32_t pkd[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pkd[i] = pack_bf16x2(__uint_as_float(v[2 * i]) * a.scale,
-                               __uint_as_float(v[2 * i + 1]) * a.scale);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(dqrow + c * 32);
+          pkd[16 * cc + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * a.scale,
+                                         __uint_as_float(v[2 * i + 1]) * a.scale);
+      }
+      // dQ is in registers: the next unit's first dQ MMA may overwrite it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDqBarAccFree));
+      if (live) {
+        uint4* dst = reinterpret_cast<uint4*>(dqrow + half * (D / 2));
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
-        }
+        for (int i = 0; i < D / 16; ++i)
+          dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
       }
     }
   }
@@ -979,10 +1051,9 @@ __global__ void __launch_bounds__(kDqThreads, 2)
   if (!ok) atomicOr(&g_bwd_status, 4u);
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
+  if (threadIdx.x < 32) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc(tmem_slot, NP * C::kTmemCols);
   }
 }
 
@@ -1061,11 +1132,12 @@ cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk
 template <int D>
 cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                        cudaStream_t st) {
+                        const QTileSched& sched, cudaStream_t st) {
   static bool done[64] = {};
   cudaError_t e = set_smem_once(attn_dq_kernel<D>, DqCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
-  attn_dq_kernel<D><<<grid, kDqThreads, DqCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
+  attn_dq_kernel<D><<<grid, kDqPipeThreads * DqCfg<D>::NP, DqCfg<D>::kSmemBytes, st>>>(
+      mq, mk, mv, mdo, a, sched);
   return cudaGetLastError();
 }
 
@@ -1098,9 +1170,9 @@ int dkdv_max_cluster_size(int D) { return D == 64 ? DkvCfg<64>::kMaxCluster : Dk
 
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                      cudaStream_t st) {
-  return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, a, st)
-                 : launch_dq_t<128>(grid, mq, mk, mv, mdo, a, st);
+                      const QTileSched& sched, cudaStream_t st) {
+  return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, a, sched, st)
+                 : launch_dq_t<128>(grid, mq, mk, mv, mdo, a, sched, st);
 }
 
 // Diagnostic: the kernels' 2^x forms on n inputs (polynomial scalar form,

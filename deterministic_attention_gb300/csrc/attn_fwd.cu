@@ -67,7 +67,7 @@ struct Cfg {
   static constexpr int kOffK = kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKvBytes;
   static constexpr int kPipeBytes = kOffV + kStages * kKvBytes;  // one pipeline (multiple of 1024)
-  static constexpr int NP = fwd_pipes_per_block(D);
+  static constexpr int NP = qtile_pipes_per_block(D);
   static constexpr int kSmemBytes = NP * kPipeBytes + 1024;     // + alignment slack
   static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;  // per pipeline
   static_assert(kPipeBytes % 1024 == 0, "pipelines keep the 1024-byte swizzle alignment");
@@ -100,10 +100,10 @@ __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffff
 
 
 template <int D>
-__global__ void __launch_bounds__(kPipeThreads * fwd_pipes_per_block(D), 1)
+__global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const FwdArgs a,
-                    const __grid_constant__ FwdSched sched) {
+                    const __grid_constant__ QTileSched sched) {
   using C = Cfg<D>;
   constexpr int NS = C::kStages;
   constexpr int NP = C::NP;
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kPipeThreads * fwd_pipes_per_block(D), 1)
 
 template <int D>
 cudaError_t launch_fwd_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                         const CUtensorMap& mv, const FwdArgs& a, const FwdSched& sched,
+                         const CUtensorMap& mv, const FwdArgs& a, const QTileSched& sched,
                          cudaStream_t st) {
   const int smem = Cfg<D>::kSmemBytes;
   static bool attr_set[64] = {};
@@ -504,7 +504,7 @@ cudaError_t launch_fwd_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
 }  // namespace
 
 cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const FwdArgs& a, const FwdSched& sched,
+                       const CUtensorMap& mv, const FwdArgs& a, const QTileSched& sched,
                        cudaStream_t st) {
   return D == 64 ? launch_fwd_t<64>(grid, mq, mk, mv, a, sched, st)
                  : launch_fwd_t<128>(grid, mq, mk, mv, a, sched, st);

@@ -16,21 +16,22 @@ constexpr int kDqTileN = 64;    // key rows per dQ-kernel KV tile
 // 64 at D = 128 (TMEM must also hold the larger dV, dK accumulators).
 constexpr int dkdv_tile_m(int D) { return D == 64 ? 128 : 64; }
 
-// Static deal of forward work units to persistent pipelines.  Unit u (in
-// heaviest-first order) is query tile n_m - 1 - u / BHq of (b, h) = u % BHq.
+// Static deal of query-tile work units (forward and dQ) to persistent
+// pipelines.  Unit u (in heaviest-first order) is query tile n_m - 1 - u / BHq
+// of (b, h) = u % BHq.
 // Pipeline i takes units unit[start[i]] .. unit[start[i + 1] - 1]; with
 // n_listed == 0 it takes units i, i + n_pipes, i + 2 n_pipes, ... instead.
-constexpr int kFwdMaxPipes = 320;
-constexpr int kFwdMaxListed = 1024;
-struct FwdSched {
+constexpr int kQTileMaxPipes = 320;
+constexpr int kQTileMaxListed = 1024;
+struct QTileSched {
   int n_pipes;
   int n_listed;
-  uint16_t start[kFwdMaxPipes + 1];
-  uint16_t unit[kFwdMaxListed];
+  uint16_t start[kQTileMaxPipes + 1];
+  uint16_t unit[kQTileMaxListed];
 };
-// Pipelines per forward block: two at D = 64 (256 TMEM columns each), one at
-// D = 128.
-constexpr int fwd_pipes_per_block(int D) { return D == 64 ? 2 : 1; }
+// Pipelines per forward / dQ block: two at D = 64 (256 TMEM columns each),
+// one at D = 128.
+constexpr int qtile_pipes_per_block(int D) { return D == 64 ? 2 : 1; }
 
 struct FwdArgs {
   void* o;               // bf16 [B, T, Hq, D]
@@ -76,7 +77,7 @@ struct BwdArgs {
 
 // Each returns the launch error (cudaSuccess when the kernel was queued).
 cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const FwdArgs& a, const FwdSched& sched,
+                       const CUtensorMap& mv, const FwdArgs& a, const QTileSched& sched,
                        cudaStream_t st);
 cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st);
 // Clusters of c blocks of the dK/dV kernel that can be resident at once on the
@@ -88,7 +89,7 @@ cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMa
                         cudaStream_t st);
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                      cudaStream_t st);
+                      const QTileSched& sched, cudaStream_t st);
 
 // Launches a one-thread kernel whose bounded wait on a never-completed
 // mbarrier runs out after limit_ns (sets the timeout bit, then returns).

@@ -133,26 +133,27 @@ float log2e_times(float scale) { return scale * 1.4426950408889634f; }
 
 int sm_count(int* out);
 
-// Deal of the forward's work units to persistent pipelines (see FwdSched).
+// Deal of the forward's work units to persistent pipelines (see QTileSched).
 // Heaviest first, each unit goes to the block with the least work so far and
 // within it to the pipeline with the least: the pipelines of one block share
 // an SM, so it is the block totals that must balance.  A unit's work counts
 // its key tiles plus two for its Q load and epilogue.  Beyond the size of the
 // listed form, units are dealt round-robin (many units balance by number).
 // Built on the host from the shape and the SM count only; cached.
-void fwd_schedule(int D, int B, int T, int Hq, int causal, int sms, FwdSched* out, int* grid) {
-  const int NP = fwd_pipes_per_block(D);
+void qtile_schedule(int D, int B, int T, int Hq, int causal, int sms, QTileSched* out, int* grid) {
+  const int NP = qtile_pipes_per_block(D);
   const int n_m = (T + kTileM - 1) / kTileM;
   const int BHq = B * Hq;
   const long units = static_cast<long>(n_m) * BHq;
   const int kv_tiles = (T + kFwdTileN - 1) / kFwdTileN;
-  long blocks = (units + NP - 1) / NP;
-  if (blocks > sms) blocks = sms;
+  // One block per SM while there are units for it: a second pipeline on an
+  // SM adds far less than a second SM does.
+  long blocks = units < sms ? units : sms;
   if (blocks < 1) blocks = 1;
   const int pipes = static_cast<int>(blocks) * NP;
   out->n_pipes = pipes;
   *grid = static_cast<int>(blocks);
-  if (units > kFwdMaxListed || pipes > kFwdMaxPipes) {
+  if (units > kQTileMaxListed || pipes > kQTileMaxPipes) {
     out->n_listed = 0;
     return;
   }
@@ -181,6 +182,24 @@ void fwd_schedule(int D, int B, int T, int Hq, int causal, int sms, FwdSched* ou
   out->n_listed = n;
 }
 
+// The schedule depends only on (D, B, T, Hq, causal, SMs): the last one is
+// kept (the forward and dQ of one layer share it).
+void cached_qtile_schedule(int D, int B, int T, int Hq, int causal, int sms, QTileSched* out,
+                           int* grid) {
+  static std::mutex mu;
+  static int key[6] = {-1, -1, -1, -1, -1, -1};
+  static QTileSched sched;
+  static int g = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  const int want[6] = {D, B, T, Hq, causal, sms};
+  if (!std::equal(want, want + 6, key)) {
+    qtile_schedule(D, B, T, Hq, causal, sms, &sched, &g);
+    std::copy(want, want + 6, key);
+  }
+  *out = sched;
+  *grid = g;
+}
+
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
              int Hq, int Hkv, int D, float scale, int causal, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
@@ -201,23 +220,9 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   a.wait_ns = g_wait_ns;
   int sms = 0;
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
-  // The schedule depends only on (D, B, T, Hq, causal, SMs): keep the last one.
-  static std::mutex mu;
-  static int key[6] = {-1, -1, -1, -1, -1, -1};
-  static FwdSched sched;
-  static int grid = 0;
-  FwdSched sc;
+  QTileSched sc;
   int g;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    const int want[6] = {D, B, T, Hq, causal, sms};
-    if (!std::equal(want, want + 6, key)) {
-      fwd_schedule(D, B, T, Hq, causal, sms, &sched, &grid);
-      std::copy(want, want + 6, key);
-    }
-    sc = sched;
-    g = grid;
-  }
+  cached_qtile_schedule(D, B, T, Hq, causal, sms, &sc, &g);
   return launched(launch_fwd(D, g, mq, mk, mv, a, sc, st), "attn_fwd");
 }
 
@@ -346,7 +351,13 @@ int dq_impl(const void* q, const void* k, const void* v, const void* dout, const
   a.dq = dq;
   a.n_tiles = (T + kTileM - 1) / kTileM;
   a.BH = B * Hq;
-  return launched(launch_dq(D, a.n_tiles * a.BH, mq, mk, mv, mdo, a, st), "attn_bwd_dq");
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
+  static_assert(kDqTileN == kFwdTileN, "the forward's schedule weights fit dQ");
+  QTileSched sc;
+  int g;
+  cached_qtile_schedule(D, B, T, Hq, causal, sms, &sc, &g);
+  return launched(launch_dq(D, g, mq, mk, mv, mdo, a, sc, st), "attn_bwd_dq");
 }
 
 size_t rowstat_bytes(int B, int T, int Hq) {
