@@ -48,42 +48,71 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
 }
 
 // ============================================================== Delta
-// One warp per (b, h, 32 consecutive positions).  Each row of D bf16 is split
-// in 16-byte chunks over D/8 lanes; a lane issues all its loads first, forms
-// its 8 products per chunk in order, the lanes of a row are combined by a
-// fixed xor-shuffle tree, and lane t stores the (-LSE*log2e, -Delta) pair of
-// position t (coalesced).  Positions T..Tp-1 get (-inf, -0).
+// Rows (b, t, h) in memory order: warp w takes rows 32 w .. 32 w + 31 of the
+// [B, T, Hq] row space, so each warp streams 32 contiguous rows of O and dO
+// (4 KB each at D = 64) -- whole DRAM pages, where one head's rows alone lie
+// Hq * D * 2 bytes apart.  Each row of D bf16 is split in 16-byte chunks over
+// D/8 lanes; a lane issues all its loads first, forms its 8 products per chunk
+// in order, and the lanes of a row are combined by a fixed xor-shuffle tree.
+// The first lane of a row reads that row's LSE and stores its
+// (-LSE*log2e, -Delta) pair.  Warps past the row space write (-inf, -0) to
+// the padding positions T..Tp-1 of every (b, h).
 template <int D>
 __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
   constexpr int kCpr = D / 8;        // 16-byte chunks per row
   constexpr int kRpi = 32 / kCpr;    // rows per warp iteration
   constexpr int kIters = 32 / kRpi;
   const int lane = threadIdx.x & 31;
-  const long unit = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int tchunks = a.Tp / 32;
-  const long units = static_cast<long>(a.B) * a.Hq * tchunks;
-  if (unit >= units) return;
-  const int tc = static_cast<int>(unit % tchunks);
-  const int bh = static_cast<int>(unit / tchunks);
-  const int b = bh / a.Hq, h = bh % a.Hq;
-  const int i0 = tc * 32;
+  const long warp_id = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const long rows = static_cast<long>(a.B) * a.T * a.Hq;
+  const long row_warps = (rows + 31) / 32;
+  if (warp_id >= row_warps) {
+    // Padding positions: (b, h, t) for t in [T, Tp), 32 per warp.
+    const int pad = a.Tp - a.T;
+    const long p = (warp_id - row_warps) * 32 + lane;
+    if (pad > 0 && p < static_cast<long>(a.B) * a.Hq * pad) {
+      const long bh = p / pad;
+      const int t = a.T + static_cast<int>(p % pad);
+      a.rowstats[bh * a.Tp + t] = make_float2(-INFINITY, -0.f);
+    }
+    return;
+  }
   const uint4* O = static_cast<const uint4*>(a.o);
   const uint4* dO = static_cast<const uint4*>(a.dout);
-  const int mine_i = i0 + lane;
-  const float lse = mine_i < a.T ? a.lse[static_cast<size_t>(bh) * a.T + mine_i] : 0.f;
+  const long r0 = warp_id * 32;
   uint4 xo[kIters], xd[kIters];
+  float lse[kIters];  // of this lane's row in each iteration (its first lane stores it)
+  size_t dst[kIters];
+  // (b, t, h) of this lane's row, decoded once and advanced by kRpi rows per
+  // iteration.
+  const long r_lane = r0 + lane / kCpr;
+  int h = static_cast<int>(r_lane % a.Hq);
+  const long bt0 = r_lane / a.Hq;
+  int b = static_cast<int>(bt0 / a.T), t = static_cast<int>(bt0 % a.T);
 #pragma unroll
   for (int it = 0; it < kIters; ++it) {
-    const int i = i0 + it * kRpi + lane / kCpr;
+    const long r = r_lane + it * kRpi;
     xo[it] = make_uint4(0u, 0u, 0u, 0u);
     xd[it] = xo[it];
-    if (i < a.T) {
-      const size_t off = ((static_cast<size_t>(b) * a.T + i) * a.Hq + h) * kCpr + lane % kCpr;
+    lse[it] = 0.f;
+    dst[it] = 0;
+    if (r < rows) {
+      const size_t off = static_cast<size_t>(r) * kCpr + lane % kCpr;
       xo[it] = O[off];
       xd[it] = dO[off];
+      const size_t bh = static_cast<size_t>(b) * a.Hq + h;
+      if (lane % kCpr == 0) lse[it] = a.lse[bh * a.T + t];
+      dst[it] = bh * a.Tp + t;
+    }
+    h += kRpi;
+    while (h >= a.Hq) {
+      h -= a.Hq;
+      if (++t == a.T) {
+        t = 0;
+        ++b;
+      }
     }
   }
-  float mine = 0.f;
 #pragma unroll
   for (int it = 0; it < kIters; ++it) {
     const uint32_t xs[4] = {xo[it].x, xo[it].y, xo[it].z, xo[it].w};
@@ -96,12 +125,10 @@ __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
       acc = fmaf(xf.y, yf.y, acc);
     }
 #pragma unroll
-    for (int s = kCpr / 2; s >= 1; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-    const float v = __shfl_sync(0xffffffffu, acc, (lane % kRpi) * kCpr);
-    if (lane / kRpi == it) mine = v;
+    for (int s2 = kCpr / 2; s2 >= 1; s2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s2);
+    const long r = r0 + it * kRpi + lane / kCpr;
+    if (lane % kCpr == 0 && r < rows) a.rowstats[dst[it]] = make_float2(-lse[it] * kLog2e, -acc);
   }
-  a.rowstats[static_cast<size_t>(bh) * a.Tp + mine_i] =
-      mine_i < a.T ? make_float2(-lse * kLog2e, -mine) : make_float2(-INFINITY, -0.f);
 }
 
 // ============================================================== dK / dV
@@ -1144,8 +1171,9 @@ cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
 }  // namespace
 
 cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st) {
-  const long units = static_cast<long>(a.B) * a.Hq * (a.Tp / 32);
-  const int grid = static_cast<int>((units + 7) / 8);
+  const long row_warps = (static_cast<long>(a.B) * a.T * a.Hq + 31) / 32;
+  const long pad_warps = (static_cast<long>(a.B) * a.Hq * (a.Tp - a.T) + 31) / 32;
+  const int grid = static_cast<int>((row_warps + pad_warps + 7) / 8);
   if (a.D == 64)
     attn_delta_kernel<64><<<grid, 256, 0, st>>>(a);
   else
