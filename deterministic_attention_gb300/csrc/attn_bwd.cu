@@ -22,6 +22,8 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
+#include <utility>
 
 #include "attn_launch.h"
 #include "exp2_poly.cuh"
@@ -42,6 +44,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kPolyOf8 = DETATTN_BWD_POLY_OF8;
 
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
+
+// f(std::integral_constant<int, i>{}) for i = 0 .. N-1, unrolled at compile
+// time (so i can be a template argument inside f).
+template <typename F, int... I>
+__device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, I...>) {
+  (f(std::integral_constant<int, I>{}), ...);
+}
+template <int N, typename F>
+__device__ __forceinline__ void static_for(F&& f) {
+  static_for_impl(f, std::make_integer_sequence<int, N>{});
+}
 
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
   return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
@@ -537,35 +550,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kDkvBarSFree));
-        // Causal: query i0 + c sees key krow iff c >= krow - i0.
+        // Causal: query i0 + c sees key krow iff c >= krow - i0.  Only a
+        // block on the diagonal needs the mask, and lane 0 holds the warp's
+        // smallest krow, so the test is made once for the whole warp and the
+        // unmasked items run a loop without it.
         const int cmin = a.causal ? (krow - i0) : -1;
-        const bool need_mask = cmin > 0;
+        const bool warp_masked = a.causal && (ti.n0 + quarter * 32 - i0) + 31 > 0;
         uint32_t pk[QG / 2], dk[QG / 2];
         // (-lse2, -delta) of this group's queries, two per float4.
         const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * QG * 8;
-#pragma unroll
-        for (int c2 = 0; c2 < QG / 2; ++c2) {
-          const int c = 2 * c2;
-          const float4 rs = ld_shared_f4(st4 + c2 * 16);  // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
-          const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rs.x);
-          const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rs.z);
-          float p0, p1;
-          if ((c2 & 7) < kPolyOf8) {
-            p0 = exp2_poly(x0);
-            p1 = exp2_poly(x1);
-          } else {
-            p0 = ex2_approx(x0);
-            p1 = ex2_approx(x1);
-          }
-          if (need_mask) {
-            if (c < cmin) p0 = 0.f;
-            if (c + 1 < cmin) p1 = 0.f;
-          }
-          const float d0 = p0 * (__uint_as_float(dp[c]) + rs.y);
-          const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rs.w);
-          pk[c2] = pack_bf16x2(p0, p1);
-          dk[c2] = pack_bf16x2(d0, d1);
-        }
+        auto element_loop = [&](auto masked) {
+          constexpr bool kMasked = decltype(masked)::value;
+          static_for<QG / 2>([&](auto ic) {
+              constexpr int c2 = decltype(ic)::value;
+              constexpr int c = 2 * c2;
+              // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1)
+              const float4 rs = ld_shared_f4_at<c2 * 16>(st4);
+              const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rs.x);
+              const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rs.z);
+              float p0, p1;
+              if constexpr ((c2 & 7) < kPolyOf8) {
+                p0 = exp2_poly(x0);
+                p1 = exp2_poly(x1);
+              } else {
+                p0 = ex2_approx(x0);
+                p1 = ex2_approx(x1);
+              }
+              if constexpr (kMasked) {
+                if (c < cmin) p0 = 0.f;
+                if (c + 1 < cmin) p1 = 0.f;
+              }
+              const float d0 = p0 * (__uint_as_float(dp[c]) + rs.y);
+              const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rs.w);
+              pk[c2] = pack_bf16x2(p0, p1);
+              dk[c2] = pack_bf16x2(d0, d1);
+          });
+        };
+        if (warp_masked)
+          element_loop(std::true_type{});
+        else
+          element_loop(std::false_type{});
         // P^T / dS^T buffer pb last held item gi - NPB: its dV, dK must have
         // read it.
         if (gi >= NPB) {

@@ -405,6 +405,17 @@ __device__ __forceinline__ void st_shared_cluster_f4(uint32_t addr, float4 v) {
                "f"(v.z), "f"(v.w)
                : "memory");
 }
+// Shared-memory load at base + OFF (a compile-time byte offset folded into
+// the instruction).  No memory clobber: callers order it after the mbarrier
+// wait that makes the data visible, which itself is a compiler barrier.
+template <int OFF>
+__device__ __forceinline__ float4 ld_shared_f4_at(uint32_t base) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4+%5];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(base), "n"(OFF));
+  return v;
+}
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
