@@ -1039,28 +1039,39 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         // key kv0 + c visible iff c <= lim
         const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
         uint32_t dsk[16];
-        const bool need_mask = a.causal ? (kv0 + 31 > t.m0) : (kv0 + 32 > a.T);
-#pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
-          const int c = 2 * c2;
-          const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rstat.x);
-          const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rstat.x);
-          float p0, p1;
-          if ((c2 & 7) < kPolyOf8) {
-            p0 = exp2_poly(x0);
-            p1 = exp2_poly(x1);
-          } else {
-            p0 = ex2_approx(x0);
-            p1 = ex2_approx(x1);
-          }
-          if (need_mask) {
-            if (c > lim) p0 = 0.f;
-            if (c + 1 > lim) p1 = 0.f;
-          }
-          const float d0 = p0 * (__uint_as_float(dp[c]) + rstat.y);
-          const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rstat.y);
-          dsk[c2] = pack_bf16x2(d0, d1);
-        }
+        // Masking is needed only where this warp's 32 rows meet the diagonal
+        // (or T), decided for the whole warp; other tiles run the loop
+        // without it.
+        const int row0 = t.m0 + quarter * 32;
+        const bool need_mask = (a.causal && kv0 + 31 > row0) || kv0 + 32 > a.T;
+        auto element_loop = [&](auto masked) {
+          constexpr bool kMasked = decltype(masked)::value;
+          static_for<16>([&](auto ic) {
+            constexpr int c2 = decltype(ic)::value;
+            constexpr int c = 2 * c2;
+            const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rstat.x);
+            const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rstat.x);
+            float p0, p1;
+            if constexpr ((c2 & 7) < kPolyOf8) {
+              p0 = exp2_poly(x0);
+              p1 = exp2_poly(x1);
+            } else {
+              p0 = ex2_approx(x0);
+              p1 = ex2_approx(x1);
+            }
+            if constexpr (kMasked) {
+              if (c > lim) p0 = 0.f;
+              if (c + 1 > lim) p1 = 0.f;
+            }
+            const float d0 = p0 * (__uint_as_float(dp[c]) + rstat.y);
+            const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rstat.y);
+            dsk[c2] = pack_bf16x2(d0, d1);
+          });
+        };
+        if (need_mask)
+          element_loop(std::true_type{});
+        else
+          element_loop(std::false_type{});
         tmem_st16_nowait(tS, dsk);
         tmem_wait_st();
         tc_fence_before();

@@ -31,6 +31,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "attn_launch.h"
 #include "exp2_poly.cuh"
@@ -351,50 +352,60 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
         reg_fence32(sr);
 
         const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
-        if (need_mask) {
-#pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (c > lim) sr[c] = __float_as_uint(-INFINITY);
-        }
-        // Maximum over this half's 32 columns in four independent chains.
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          mx4[c & 3] = fmax3(mx4[c & 3], __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        // A half-row may see no key in this tile (past its diagonal): mx = -inf
-        // leaves the running maximum alone and every P zero.
-        const float m_new = mx * sl2;
         float alpha = 1.f;
         bool moved = false;
-        if (m_new > m_run + kRescaleLog2) {
-          alpha = ex2_approx(m_run - m_new);
-          m_run = m_new;
-          moved = true;
-        }
-        const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-        const uint64_t sl2x2 = f2_make(sl2, sl2), neg_m = f2_make(-m_use, -m_use);
-        uint64_t sum2[2] = {f2_make(0.f, 0.f), f2_make(0.f, 0.f)};  // four partial sums
+        uint64_t sum2[2];  // four partial sums
         uint32_t pk[16];
+        // Masking is needed only where this warp's rows meet the diagonal (or
+        // T), decided for the whole warp; other tiles run the code without it.
+        auto softmax_tile = [&](auto masked) {
+          constexpr bool kMasked = decltype(masked)::value;
+          if constexpr (kMasked) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint64_t x = f2_fma(f2_make(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
-                                    sl2x2, neg_m);
-          float x0, x1, p0, p1;
-          f2_split(x, x0, x1);
-          if ((i & 7) < kPolyOf8) {
-            exp2_poly2(x0, x1, p0, p1);
-          } else {
-            p0 = ex2_approx(x0);
-            p1 = ex2_approx(x1);
+            for (int c = 0; c < 32; ++c)
+              if (c > lim) sr[c] = __float_as_uint(-INFINITY);
           }
-          if (need_mask) {  // masked keys contribute exactly zero
-            if (2 * i > lim) p0 = 0.f;
-            if (2 * i + 1 > lim) p1 = 0.f;
+          // Maximum over this half's 32 columns in four independent chains.
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            mx4[c & 3] = fmax3(mx4[c & 3], __uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          // A half-row may see no key in this tile (past its diagonal): mx =
+          // -inf leaves the running maximum alone and every P zero.
+          const float m_new = mx * sl2;
+          if (m_new > m_run + kRescaleLog2) {
+            alpha = ex2_approx(m_run - m_new);
+            m_run = m_new;
+            moved = true;
           }
-          sum2[i & 1] = f2_add(sum2[i & 1], f2_make(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
-        }
+          const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+          const uint64_t sl2x2 = f2_make(sl2, sl2), neg_m = f2_make(-m_use, -m_use);
+          sum2[0] = sum2[1] = f2_make(0.f, 0.f);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const uint64_t x = f2_fma(f2_make(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])),
+                                      sl2x2, neg_m);
+            float x0, x1, p0, p1;
+            f2_split(x, x0, x1);
+            if ((i & 7) < kPolyOf8) {
+              exp2_poly2(x0, x1, p0, p1);
+            } else {
+              p0 = ex2_approx(x0);
+              p1 = ex2_approx(x1);
+            }
+            if constexpr (kMasked) {  // masked keys contribute exactly zero
+              if (2 * i > lim) p0 = 0.f;
+              if (2 * i + 1 > lim) p1 = 0.f;
+            }
+            sum2[i & 1] = f2_add(sum2[i & 1], f2_make(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+        };
+        if (need_mask)
+          softmax_tile(std::true_type{});
+        else
+          softmax_tile(std::false_type{});
         tmem_st16_nowait(tS, pk);
         tmem_wait_st();
         if (j > 0 && __any_sync(0xffffffffu, moved)) {
