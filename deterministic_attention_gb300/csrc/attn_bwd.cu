@@ -193,7 +193,7 @@ struct DkvCfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kKvBytes = kTileN * 128 * kAtoms;  // 128 keys x D
   static constexpr int kQBytes = kTM * 128 * kAtoms;      // TM queries x D
-  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr int kStages = (D == 64) ? 6 : 2;
   static constexpr int kStageBytes = 2 * kQBytes + 1024;  // Q, dO, then TM row statistics
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kKvBytes;
@@ -205,30 +205,38 @@ struct DkvCfg {
   static constexpr int kRecvBytes = (kTileN - kTileN / kMaxCluster) * kRowBytes;
   static constexpr int kSmemBytes = kOffRecv + kRecvBytes + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  // S^T at 0 and dP^T at TM (TM fp32 columns each, one per query).  P^T and
-  // dS^T of item gi go to buffer gi % kNumPB at kColPB + TM * buffer: P^T as
-  // packed bf16 pairs over TM/2 columns (two queries per column), dS^T over
-  // the next TM/2; group g writes columns g*TM/8 .. of each.
+  // S^T and dP^T of item gi (TM fp32 columns each, one per query) go to score
+  // buffer gi % kNumSB: S^T at 2 TM b, dP^T at 2 TM b + TM.  With two buffers
+  // the issuer computes the next item's scores while the element-wise warps
+  // work on this one.  P^T and dS^T of item gi go to buffer gi % kNumPB at
+  // kColPB + TM * buffer: P^T as packed bf16 pairs over TM/2 columns (two
+  // queries per column), dS^T over the next TM/2; group g writes columns
+  // g*TM/8 .. of each.  At D = 64 the tile's K and V also live in TMEM as
+  // packed bf16 pairs (the A operands of S^T and dP^T, which then run with
+  // only Q / dO read from shared memory).
+  static constexpr int kNumSB = (D == 64) ? 2 : 1;
   static constexpr int kNumPB = (D == 64) ? 1 : 2;
-  static constexpr uint32_t kColS = 0;
-  static constexpr uint32_t kColDP = kTM;
-  static constexpr uint32_t kColPB = 2 * kTM;
+  static constexpr bool kKvInTmem = (D == 64);
+  static constexpr uint32_t kColPB = kNumSB * 2 * kTM;
   static constexpr uint32_t kColDV = kColPB + kNumPB * kTM;  // dV accumulator, D cols
   static constexpr uint32_t kColDK = kColDV + D;             // dK accumulator, D cols
-  static_assert(kColDK + D <= kTmemCols, "TMEM layout");
+  static constexpr uint32_t kColK = kColDK + D;              // K (D = 64), D/2 columns
+  static constexpr uint32_t kColV = kColK + D / 2;           // V (D = 64), D/2 columns
+  static_assert(kColDK + D + (kKvInTmem ? D : 0) <= kTmemCols, "TMEM layout");
   static_assert(kTM * 8 <= 1024, "row statistics fit their stage slot");
   static_assert(kSmemBytes + 512 <= 227 * 1024, "shared memory per block (with the static part)");
 };
 
-constexpr int kDkvMaxStages = 4;
+constexpr int kDkvMaxStages = 6;
 enum : int {
   kDkvBarKV = 0,                             // this tile's K, V landed
   kDkvBarKVFree = 1,                         // the previous tile's S^T MMAs are done with K, V
-  kDkvBarQFull = 2,
+  kDkvBarKvTmem = 2,                         // this tile's K, V copied into TMEM (D = 64)
+  kDkvBarQFull = 3,
   kDkvBarQEmpty = kDkvBarQFull + kDkvMaxStages,
-  kDkvBarS = kDkvBarQEmpty + kDkvMaxStages,  // S^T, dP^T of the current item landed
-  kDkvBarSFree = kDkvBarS + 1,               // element-wise warps hold them in registers
-  kDkvBarP = kDkvBarSFree + 1,               // [2] P^T, dS^T of the buffer's item written
+  kDkvBarS = kDkvBarQEmpty + kDkvMaxStages,  // [2] S^T, dP^T of the buffer's item landed
+  kDkvBarSFree = kDkvBarS + 2,               // [2] element-wise warps hold them in registers
+  kDkvBarP = kDkvBarSFree + 2,               // [2] P^T, dS^T of the buffer's item written
   kDkvBarFree = kDkvBarP + 2,                // [2] dV, dK of the buffer's item done
   kDkvBarAcc = kDkvBarFree + 2,              // this tile's dV, dK complete
   kDkvBarAccFree = kDkvBarAcc + 1,           // element-wise warps hold them in registers
@@ -275,6 +283,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int TM = Cf::kTM;
   constexpr int QG = Cf::kQG;
   constexpr int NPB = Cf::kNumPB;
+  constexpr int NSB = Cf::kNumSB;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t bars[kDkvNumBars];
   __shared__ uint32_t tmem_slot;
@@ -332,8 +341,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar(kDkvBarQFull + s), 1);
       mbar_init(bar(kDkvBarQEmpty + s), 1);
     }
-    mbar_init(bar(kDkvBarS), 1);
-    mbar_init(bar(kDkvBarSFree), kComputeWarps);
+    mbar_init(bar(kDkvBarKvTmem), kComputeWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kDkvBarS + i), 1);
+      mbar_init(bar(kDkvBarSFree + i), kComputeWarps);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kDkvBarP + i), kComputeWarps);
       mbar_init(bar(kDkvBarFree + i), 1);
@@ -374,8 +386,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int t = tile_of(kt);
         if (t < 0) break;
         const DkvTile ti = tile_info(t);
-        // K, V of the previous tile must no longer be read.
-        if (kt > 0 && !(ok = mbar_wait(bar(kDkvBarKVFree), (kt - 1) & 1, wait_ns))) break;
+        // K, V of the previous tile must no longer be read from shared
+        // memory: copied into TMEM (D = 64) or consumed by its S^T MMAs.
+        if (kt > 0 && !(ok = mbar_wait(bar(Cf::kKvInTmem ? kDkvBarKvTmem : kDkvBarKVFree),
+                                       (kt - 1) & 1, wait_ns)))
+          break;
         mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * Cf::kKvBytes);
         for (int at = 0; at < Cf::kAtoms; ++at) {
           tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, ti.g, ti.n0, ti.b);
@@ -421,37 +436,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Operand descriptors built once; the loop only adds constant offsets.
     const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
     const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);  // K-major B
-    const uint32_t tS = tmem + Cf::kColS, tDP = tmem + Cf::kColDP;
     int gi = 0;
     for (int kt = 0; ok; ++kt) {
       const int t = tile_of(kt);
       if (t < 0) break;
       const DkvTile ti = tile_info(t);
-      if (!(ok = warp_all(mbar_wait(bar(kDkvBarKV), kt & 1, wait_ns)))) break;
+      // The tile's K, V: in TMEM (D = 64, copied by the element-wise warps)
+      // or in shared memory.
+      if (!(ok = warp_all(mbar_wait(bar(Cf::kKvInTmem ? kDkvBarKvTmem : kDkvBarKV), kt & 1,
+                                    wait_ns))))
+        break;
       tc_fence_after();
       for (int li = 0; li < ti.n_it; ++li, ++gi) {
         const int s = gi % NS;
-        // The element-wise warps must hold S^T, dP^T of the previous item in
-        // registers before those of this one overwrite them.
-        if (gi >= 1 && !(ok = warp_all(mbar_wait(bar(kDkvBarSFree), (gi - 1) & 1, wait_ns)))) break;
+        const int sb = gi % NSB;
+        // The element-wise warps must hold S^T, dP^T of the buffer's previous
+        // item in registers before those of this one overwrite them.
+        if (gi >= NSB &&
+            !(ok = warp_all(mbar_wait(bar(kDkvBarSFree + sb), ((gi - NSB) / NSB) & 1, wait_ns))))
+          break;
         if (!(ok = warp_all(mbar_wait(bar(kDkvBarQFull + s), (gi / NS) & 1, wait_ns)))) break;
         tc_fence_after();
         const uint64_t dQk = desc_add(dQk0, s * Cf::kStageBytes);
         const uint64_t ddOk = desc_add(dQk, Cf::kQBytes);
-        // K = D in groups of 64 (one 128-byte swizzle atom): four 32-byte steps.
+        const uint32_t tS = tmem + sb * 2 * TM, tDP = tS + TM;
+        if constexpr (Cf::kKvInTmem) {
+          // K = D = 64: four steps over the packed K / V columns and the
+          // 32-byte K-major slices of Q / dO.
+          const uint32_t aK = tmem + Cf::kColK, aV = tmem + Cf::kColV;
+          mma_ts_x4(tS, aK, aK + 8, aK + 16, aK + 24, dQk, desc_add(dQk, 32), desc_add(dQk, 64),
+                    desc_add(dQk, 96), kIdS, 0u);
+          mma_ts_x4(tDP, aV, aV + 8, aV + 16, aV + 24, ddOk, desc_add(ddOk, 32), desc_add(ddOk, 64),
+                    desc_add(ddOk, 96), kIdS, 0u);
+        } else {
+          // K = D in groups of 64 (one 128-byte swizzle atom): four 32-byte steps.
 #pragma unroll
-        for (int at = 0; at < Cf::kAtoms; ++at) {
-          const uint64_t k = desc_add(dK, at * (kTileN * 128)), q = desc_add(dQk, at * (TM * 128));
-          mma_ss_x4(tS, k, desc_add(k, 32), desc_add(k, 64), desc_add(k, 96), q, desc_add(q, 32),
-                    desc_add(q, 64), desc_add(q, 96), kIdS, at > 0 ? 1u : 0u);
-        }
+          for (int at = 0; at < Cf::kAtoms; ++at) {
+            const uint64_t k = desc_add(dK, at * (kTileN * 128)), q = desc_add(dQk, at * (TM * 128));
+            mma_ss_x4(tS, k, desc_add(k, 32), desc_add(k, 64), desc_add(k, 96), q, desc_add(q, 32),
+                      desc_add(q, 64), desc_add(q, 96), kIdS, at > 0 ? 1u : 0u);
+          }
 #pragma unroll
-        for (int at = 0; at < Cf::kAtoms; ++at) {
-          const uint64_t v = desc_add(dV, at * (kTileN * 128)), o = desc_add(ddOk, at * (TM * 128));
-          mma_ss_x4(tDP, v, desc_add(v, 32), desc_add(v, 64), desc_add(v, 96), o, desc_add(o, 32),
-                    desc_add(o, 64), desc_add(o, 96), kIdS, at > 0 ? 1u : 0u);
+          for (int at = 0; at < Cf::kAtoms; ++at) {
+            const uint64_t v = desc_add(dV, at * (kTileN * 128)), o = desc_add(ddOk, at * (TM * 128));
+            mma_ss_x4(tDP, v, desc_add(v, 32), desc_add(v, 64), desc_add(v, 96), o, desc_add(o, 32),
+                      desc_add(o, 64), desc_add(o, 96), kIdS, at > 0 ? 1u : 0u);
+          }
         }
-        mma_commit(bar(kDkvBarS));
+        mma_commit(bar(kDkvBarS + sb));
       }
       if (!ok) break;
       // K, V of this tile are free once these MMAs complete.
@@ -525,6 +557,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
     const int owner = r / R;  // block of the cluster that stores key row r
+    // D = 64: K and V row r of tile kt into TMEM as the A operands of S^T and
+    // dP^T, once they have landed and the previous tile's S^T MMAs no longer
+    // read TMEM's copy; this thread copies elements 16 grp..16 grp+15 (two
+    // 16-byte chunks of the 128-byte-swizzled tile row) as 8 packed pairs.
+    // Done for the next tile before this tile's epilogue, so the next tile's
+    // first scores overlap the epilogue.
+    auto copy_kv = [&](int kt) -> bool {
+      bool good = warp_all(mbar_wait(bar(kDkvBarKV), kt & 1, wait_ns));
+      if (good && kt > 0) good = warp_all(mbar_wait(bar(kDkvBarKVFree), (kt - 1) & 1, wait_ns));
+      if (good) {
+        tc_fence_after();
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t base = (which == 0 ? sK : sV) + r * 128;
+          uint32_t v8[8];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const uint4 x = ld_shared_u4(base + (((2 * grp + c) ^ (r & 7)) * 16));
+            v8[4 * c] = x.x;
+            v8[4 * c + 1] = x.y;
+            v8[4 * c + 2] = x.z;
+            v8[4 * c + 3] = x.w;
+          }
+          tmem_st8_nowait(tl + (which == 0 ? Cf::kColK : Cf::kColV) + grp * 8, v8);
+        }
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDkvBarKvTmem));
+      return good;
+    };
+    if (Cf::kKvInTmem && tile_of(0) >= 0) ok = copy_kv(0);
     int gi = 0;
     for (int kt = 0; ok; ++kt) {
       const int t = tile_of(kt);
@@ -537,19 +602,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int pb = gi % NPB;
         const int i0 = (ti.m_begin + m_idx) * TM + grp * QG;  // this group's first query
         if (++m_idx == ti.per_head) m_idx = 0;
-        ok = warp_all(mbar_wait(bar(kDkvBarS), gi & 1, wait_ns));
+        const int sb = gi % NSB;
+        ok = warp_all(mbar_wait(bar(kDkvBarS + sb), (gi / NSB) & 1, wait_ns));
         if (!ok) break;
         tc_fence_after();
         uint32_t sv[QG], dp[QG];
-        tmem_ld_cols<QG>(tl + Cf::kColS + grp * QG, sv);
-        tmem_ld_cols<QG>(tl + Cf::kColDP + grp * QG, dp);
+        const uint32_t tSb = tl + sb * 2 * TM;
+        tmem_ld_cols<QG>(tSb + grp * QG, sv);
+        tmem_ld_cols<QG>(tSb + TM + grp * QG, dp);
         tmem_wait_ld();
         reg_fence_cols<QG>(sv);
         reg_fence_cols<QG>(dp);
-        // S^T, dP^T are in registers: the next item's may overwrite them.
+        // S^T, dP^T are in registers: a later item's may overwrite them.
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kDkvBarSFree));
+        if (lane == 0) mbar_arrive(bar(kDkvBarSFree + sb));
         // Causal: query i0 + c sees key krow iff c >= krow - i0.  Only a
         // block on the diagonal needs the mask, and lane 0 holds the warp's
         // smallest krow, so the test is made once for the whole warp and the
@@ -606,6 +673,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) mbar_arrive(bar(kDkvBarP + pb));
       }
       if (!ok) break;
+      if (Cf::kKvInTmem && tile_of(kt + 1) >= 0 && !(ok = copy_kv(kt + 1))) break;
 
       // ---------------------------------------------------------- tile epilogue
       // This thread's share of key row r: D/4 columns of dV and of dK (zero

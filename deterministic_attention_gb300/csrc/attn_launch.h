@@ -11,10 +11,9 @@ constexpr int kTileM = 128;     // query rows per forward / dQ tile
 constexpr int kTileN = 128;     // key rows per dK/dV tile
 constexpr int kFwdTileN = 64;   // key rows per forward KV tile
 constexpr int kDqTileN = 64;    // key rows per dQ-kernel KV tile
-// Query rows per dK/dV-kernel item: 128 at D = 64 (the S^T, dP^T MMAs then
-// run at N = 128 and the per-item fixed costs are shared by twice the work),
-// 64 at D = 128 (TMEM must also hold the larger dV, dK accumulators).
-constexpr int dkdv_tile_m(int D) { return D == 64 ? 128 : 64; }
+// Query rows per dK/dV-kernel item (64: two items' S^T, dP^T fit TMEM at
+// D = 64 beside the accumulators and K, V).
+constexpr int dkdv_tile_m(int) { return 64; }
 
 // Static deal of query-tile work units (forward and dQ) to persistent
 // pipelines.  Unit u (in heaviest-first order) is query tile n_m - 1 - u / BHq
