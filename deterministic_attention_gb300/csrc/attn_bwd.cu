@@ -72,6 +72,11 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
 // the padding positions T..Tp-1 of every (b, h).
 template <int D>
 __global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
+  // Launched as a dependent of whatever precedes it (the forward, in a
+  // training step): everything below reads that kernel's output.  Only after
+  // this wait may the next kernel (the dK/dV step) start its own prologue.
+  griddep_wait();
+  griddep_launch_dependents();
   constexpr int kCpr = D / 8;        // 16-byte chunks per row
   constexpr int kRpi = 32 / kCpr;    // rows per warp iteration
   constexpr int kIters = 32 / kRpi;
@@ -382,6 +387,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int s = 0; s < kDkvMaxStages; ++s) last[s] = -1;
       int last_kv = -1;
       int gi = 0;  // items loaded so far, over all tiles
+      bool waited = false;  // for the Delta step's row statistics (dependent launch)
       for (int kt = 0; ok; ++kt) {
         const int t = tile_of(kt);
         if (t < 0) break;
@@ -410,6 +416,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tma_load_4d(st + at * (TM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h, i0, ti.b);
             tma_load_4d(st + Cf::kQBytes + at * (TM * 128), &mdO, bar(kDkvBarQFull + s), at * 64,
                         h, i0, ti.b);
+          }
+          if (!waited) {
+            // Launched as a dependent of the Delta step: only the row
+            // statistics are its output, so everything up to here (setup,
+            // K, V, Q, dO loads) overlaps it.
+            griddep_wait();
+            waited = true;
           }
           bulk_load(st + 2 * Cf::kQBytes,
                     a.rowstats + (static_cast<size_t>(ti.b) * a.Hq + h) * a.Tp + i0, TM * 8,
@@ -1234,26 +1247,31 @@ cudaError_t dkdv_max_clusters_t(int c, int* out) {
 template <int D>
 cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                          cudaStream_t st) {
+                          bool dependent, cudaStream_t st) {
   static bool done[64] = {};
   cudaError_t e = set_smem_once(attn_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
-  if (a.cluster <= 1) {
-    attn_dkdv_kernel<D><<<grid, kBwdThreads, DkvCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kBwdThreads);
   cfg.dynamicSmemBytes = DkvCfg<D>::kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(a.cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (a.cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (dependent) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   e = cudaLaunchKernelEx(&cfg, attn_dkdv_kernel<D>, mq, mk, mv, mdo, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -1277,18 +1295,26 @@ cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st) {
   const long row_warps = (static_cast<long>(a.B) * a.T * a.Hq + 31) / 32;
   const long pad_warps = (static_cast<long>(a.B) * a.Hq * (a.Tp - a.T) + 31) / 32;
   const int grid = static_cast<int>((row_warps + pad_warps + 7) / 8);
-  if (a.D == 64)
-    attn_delta_kernel<64><<<grid, 256, 0, st>>>(a);
-  else
-    attn_delta_kernel<128><<<grid, 256, 0, st>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = a.D == 64 ? cudaLaunchKernelEx(&cfg, attn_delta_kernel<64>, a)
+                            : cudaLaunchKernelEx(&cfg, attn_delta_kernel<128>, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                        cudaStream_t st) {
-  return D == 64 ? launch_dkdv_t<64>(grid, mq, mk, mv, mdo, a, st)
-                 : launch_dkdv_t<128>(grid, mq, mk, mv, mdo, a, st);
+                        bool dependent, cudaStream_t st) {
+  return D == 64 ? launch_dkdv_t<64>(grid, mq, mk, mv, mdo, a, dependent, st)
+                 : launch_dkdv_t<128>(grid, mq, mk, mv, mdo, a, dependent, st);
 }
 
 cudaError_t dkdv_max_clusters(int D, int c, int* out) {

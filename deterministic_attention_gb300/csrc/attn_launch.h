@@ -83,9 +83,12 @@ cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st);
 // current device (c = 1: blocks), and the largest c the kernel supports.
 cudaError_t dkdv_max_clusters(int D, int c, int* out);
 int dkdv_max_cluster_size(int D);
+// `dependent`: launched as a programmatic dependent of the Delta step just
+// before it in `st` (the kernel waits for it only before reading the row
+// statistics; Q, K, V, dO must not be written by that step).
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                        cudaStream_t st);
+                        bool dependent, cudaStream_t st);
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                       const QTileSched& sched, cudaStream_t st);

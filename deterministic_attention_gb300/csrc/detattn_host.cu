@@ -318,7 +318,7 @@ int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int
 
 int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
               const void* workspace, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
-              float scale, int causal, cudaStream_t st) {
+              float scale, int causal, cudaStream_t st, bool after_delta = false) {
   CUtensorMap mq, mk, mv, mdo;
   int rc;
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, dkdv_tile_m(D), "q")) != DETATTN_OK) return rc;
@@ -335,7 +335,8 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
   if ((rc = dkdv_schedule(B, T, Hq, Hkv, D, causal, sms, g_dkdv_split, &a.cluster, &a.n_groups)) !=
       DETATTN_OK)
     return rc;
-  return launched(launch_dkdv(D, a.n_groups * a.cluster, mq, mk, mv, mdo, a, st), "attn_bwd_dkdv");
+  return launched(launch_dkdv(D, a.n_groups * a.cluster, mq, mk, mv, mdo, a, after_delta, st),
+                  "attn_bwd_dkdv");
 }
 
 int dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
@@ -419,8 +420,10 @@ int bwd_steps(const void* q, const void* k, const void* v, const void* o, const 
   if ((rc = dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, ss->stream)) !=
       DETATTN_OK)
     return rc;
-  if ((rc = dkdv_impl(q, k, v, dout, ws, dk, dv, B, T, Hq, Hkv, D, scale, causal, st)) !=
-      DETATTN_OK)
+  // dK/dV follows the Delta step directly in `st`: its prologue and
+  // operand loads overlap that step (it waits only for the row statistics).
+  if ((rc = dkdv_impl(q, k, v, dout, ws, dk, dv, B, T, Hq, Hkv, D, scale, causal, st,
+                      /*after_delta=*/true)) != DETATTN_OK)
     return rc;
   e = cudaEventRecord(ss->join, ss->stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->join, 0);
