@@ -570,8 +570,8 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
   if ((rc = noalloc_scratch(&ws)) != DETATTN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, st)) != DETATTN_OK) return rc;
-  if ((rc = dkdv_impl(q, k, v, dout, ws, dk, dv, B, T, Hq, Hkv, D, scale, causal, st)) !=
-      DETATTN_OK)
+  if ((rc = dkdv_impl(q, k, v, dout, ws, dk, dv, B, T, Hq, Hkv, D, scale, causal, st,
+                      /*after_delta=*/true)) != DETATTN_OK)
     return rc;
   return dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, st);
 }
