@@ -819,9 +819,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // NP pipelines (two at D = 64, one at D = 128), each with its own warps,
 // shared memory, mbarriers and TMEM columns, working through the units the
 // host dealt it.  Per pipeline, warp 0 loads each unit's Q, dO and the K, V
-// ring; warp 1 issues S = Q K^T, dP = dO V^T and dQ += dS K with dS read from
-// TMEM; warps 2..9 (two threads per query row, one per 32-key half) form P
-// and dS and, at the unit's end, write dQ.
+// ring; warp 1 issues S = Q K^T, dP = dO V^T and dQ += dS K; warps 2..9 (two
+// threads per query row, one per 32-key half) form P and dS and, at the
+// unit's end, write dQ.  At D = 64, dS goes to a shared-memory tile and the
+// element-wise warps release S, dP as soon as they hold them in registers, so
+// the next key tile's S, dP are computed while they work on this one; at
+// D = 128, dS is written over S in TMEM and the tiles run one after another.
 constexpr int kDqPipeWarps = 10;  // producer, MMA issuer, 8 compute warps
 constexpr int kDqPipeThreads = kDqPipeWarps * 32;
 template <int D>
@@ -834,11 +837,15 @@ struct DqCfg {
   static constexpr int kOffdO = kQBytes;
   static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKvBytes;
-  static constexpr int kPipeBytes = kOffV + kStages * kKvBytes;  // multiple of 1024
+  // D = 64: the dS tile [128 queries x 64 keys] bf16, 128-byte swizzled like a
+  // TMA-loaded tile, read by the dQ MMA from shared memory.
+  static constexpr bool kDsInSmem = (D == 64);
+  static constexpr int kOffDS = kOffV + kStages * kKvBytes;
+  static constexpr int kPipeBytes = kOffDS + (kDsInSmem ? kTileM * 128 : 0);  // multiple of 1024
   static constexpr int NP = qtile_pipes_per_block(D);
   static constexpr int kSmemBytes = NP * kPipeBytes + 1024;
   static constexpr uint32_t kTmemCols = 256;  // per pipeline (D = 64: 2 x 256)
-  static constexpr uint32_t kColS = 0;    // S fp32 [128 x 64]; dS bf16 over cols 0..31
+  static constexpr uint32_t kColS = 0;    // S fp32 [128 x 64]; dS bf16 over cols 0..31 (D = 128)
   static constexpr uint32_t kColDP = 64;  // dP fp32 [128 x 64]
   static constexpr uint32_t kColDQ = 128; // dQ accumulator, D cols
   // For D = 64 the unit's Q and dO tiles also live in TMEM (packed bf16
@@ -850,13 +857,17 @@ struct DqCfg {
   static constexpr uint32_t kColdO = 224;
   static_assert(kPipeBytes % 1024 == 0, "pipelines keep the 1024-byte swizzle alignment");
   static_assert(D == 64 || NP == 1, "D = 128 needs a block's whole TMEM");
+  static_assert(!kDsInSmem || kQInTmem, "the early release of S, dP assumes Q, dO in TMEM");
+  static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory per block");
 };
 
 enum : int { kDqBarQ = 0, kDqBarKFull = 1, kDqBarVFull = 4, kDqBarKEmpty = 7, kDqBarVEmpty = 10,
              kDqBarS = 13, kDqBarDS = 14, kDqBarAcc = 15, kDqBarDrain = 16, kDqBarQTmem = 17,
              kDqBarQUsed = 18,   // the unit's S, dP MMAs are done (Q, dO no longer read)
              kDqBarAccFree = 19, // the unit's epilogue has read dQ
-             kDqNumBars = 20 };
+             kDqBarSFree = 20,   // D = 64: element-wise warps hold this tile's S, dP in registers
+             kDqBarDSFree = 21,  // D = 64: the dQ MMAs are done with the dS tile
+             kDqNumBars = 22 };
 
 template <int D>
 __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
@@ -904,7 +915,7 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t s0 = smem_u32(smem) + pipe * C::kPipeBytes;
   const uint32_t sQ = s0 + C::kOffQ, sdO = s0 + C::kOffdO;
-  const uint32_t sK0 = s0 + C::kOffK, sV0 = s0 + C::kOffV;
+  const uint32_t sK0 = s0 + C::kOffK, sV0 = s0 + C::kOffV, sDS = s0 + C::kOffDS;
   uint64_t* bars = bars_all[pipe];
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
@@ -928,6 +939,8 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
     mbar_init(bar(kDqBarQTmem), 8);
     mbar_init(bar(kDqBarQUsed), 1);
     mbar_init(bar(kDqBarAccFree), 8);
+    mbar_init(bar(kDqBarSFree), 8);
+    mbar_init(bar(kDqBarDSFree), 1);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -996,7 +1009,64 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
     const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024), dV0 = sdesc_sw128(sV0, 16, 1024);
     const uint64_t dKm0 = sdesc_sw128(sK0, kDqTileN * 128, 1024);  // K as MN-major B
     int gj = 0;
-    for (int ku = 0; ku < n_units && ok; ++ku) {
+    if constexpr (C::kDsInSmem) {
+      const uint64_t dDS = sdesc_sw128(sDS, 16, 1024);  // dS as K-major A
+      const uint32_t aQ = tmem + C::kColQ, adO = tmem + C::kColdO;
+      // S, dP of tile j of unit ku (g-th over all units), once the element-wise
+      // warps hold the previous tile's in registers.
+      auto issue_sdp = [&](const Unit& t, int ku, int j, int g) -> bool {
+        const int s = g % NS;
+        const uint32_t ph = (g / NS) & 1;
+        if (j == 0 && !(warp_all(mbar_wait(bar(kDqBarQ), ku & 1, wait_ns)) &&
+                        warp_all(mbar_wait(bar(kDqBarQTmem), ku & 1, wait_ns))))
+          return false;
+        if (g > 0 && !warp_all(mbar_wait(bar(kDqBarSFree), (g - 1) & 1, wait_ns))) return false;
+        if (!warp_all(mbar_wait(bar(kDqBarKFull + s), ph, wait_ns))) return false;
+        tc_fence_after();
+        const uint64_t dK = desc_add(dK0, s * C::kKvBytes), dV = desc_add(dV0, s * C::kKvBytes);
+        mma_ts_x4(tS, aQ, aQ + 8, aQ + 16, aQ + 24, dK, desc_add(dK, 32), desc_add(dK, 64),
+                  desc_add(dK, 96), kIdS, 0u);
+        if (!warp_all(mbar_wait(bar(kDqBarVFull + s), ph, wait_ns))) return false;
+        tc_fence_after();
+        mma_ts_x4(tDP, adO, adO + 8, adO + 16, adO + 24, dV, desc_add(dV, 32), desc_add(dV, 64),
+                  desc_add(dV, 96), kIdS, 0u);
+        mma_commit(bar(kDqBarS));
+        mma_commit(bar(kDqBarVEmpty + s));
+        if (j + 1 == t.n_kv) mma_commit(bar(kDqBarQUsed));  // the unit's last S, dP
+        return true;
+      };
+      Unit t{};
+      if (n_units > 0) {
+        t = unit_info(u_of(0));
+        ok = issue_sdp(t, 0, 0, 0);
+      }
+      for (int ku = 0; ku < n_units && ok; ++ku) {
+        for (int j = 0; j < t.n_kv && ok; ++j, ++gj) {
+          const int s = gj % NS;
+          if (j + 1 < t.n_kv && !(ok = issue_sdp(t, ku, j + 1, gj + 1))) break;
+          if (!(ok = warp_all(mbar_wait(bar(kDqBarDS), gj & 1, wait_ns)))) break;
+          // The previous unit's epilogue must have read dQ before this unit's
+          // first dQ MMA overwrites it.
+          if (j == 0 && ku > 0 &&
+              !(ok = warp_all(mbar_wait(bar(kDqBarAccFree), (ku - 1) & 1, wait_ns))))
+            break;
+          tc_fence_after();
+          const uint64_t dKm = desc_add(dKm0, s * C::kKvBytes);
+          mma_ss_x4(tDQ, dDS, desc_add(dDS, 32), desc_add(dDS, 64), desc_add(dDS, 96), dKm,
+                    desc_add(dKm, 2048), desc_add(dKm, 4096), desc_add(dKm, 6144), kIdDQ,
+                    j > 0 ? 1u : 0u);
+          mma_commit(bar(kDqBarKEmpty + s));
+          mma_commit(bar(kDqBarDSFree));
+        }
+        if (!ok) break;
+        mma_commit(bar(kDqBarAcc));
+        if (ku + 1 < n_units) {
+          t = unit_info(u_of(ku + 1));
+          ok = issue_sdp(t, ku + 1, 0, gj);
+        }
+      }
+    }
+    for (int ku = 0; !C::kDsInSmem && ku < n_units && ok; ++ku) {
       const Unit t = unit_info(u_of(ku));
       if (!(ok = warp_all(mbar_wait(bar(kDqBarQ), ku & 1, wait_ns)))) break;
       if (C::kQInTmem && !(ok = warp_all(mbar_wait(bar(kDqBarQTmem), ku & 1, wait_ns)))) break;
@@ -1116,6 +1186,12 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         tmem_wait_ld();
         reg_fence32(sv);
         reg_fence32(dp);
+        if constexpr (C::kDsInSmem) {
+          // S, dP are in registers: the next tile's may overwrite them.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kDqBarSFree));
+        }
         const int kv0 = j * kDqTileN + half * 32;  // key of this half's first column
         // key kv0 + c visible iff c <= lim
         const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
@@ -1153,9 +1229,21 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
           element_loop(std::true_type{});
         else
           element_loop(std::false_type{});
-        tmem_st16_nowait(tS, dsk);
-        tmem_wait_st();
-        tc_fence_before();
+        if constexpr (C::kDsInSmem) {
+          // The previous tile's dQ MMAs must be done reading the dS tile.
+          if (gj > 0 && !(ok = warp_all(mbar_wait(bar(kDqBarDSFree), (gj - 1) & 1, wait_ns)))) break;
+          // Row r, keys 32 half .. 32 half + 31: 16-byte chunks 4 half .. 4 half + 3
+          // of the 128-byte-swizzled row.
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st_shared_u4(sDS + r * 128 + (((4 * half + i) ^ (r & 7)) * 16),
+                         make_uint4(dsk[4 * i], dsk[4 * i + 1], dsk[4 * i + 2], dsk[4 * i + 3]));
+          fence_proxy_async_smem();  // visible to the tensor core's reads
+        } else {
+          tmem_st16_nowait(tS, dsk);
+          tmem_wait_st();
+          tc_fence_before();
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kDqBarDS));
       }
