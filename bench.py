@@ -10,7 +10,9 @@ Prints one JSON line.  `value` is algorithmic causal fwd+bwd TFLOPS
 in HBM and rotate over enough sets that each step reads them from DRAM, not
 L2.  `e2e` is the same metric through the public API with host buffers
 (pinned host -> device copies of Q, K, V, dO and device -> host copies of O,
-LSE, dQ, dK, dV inside the timed region).
+LSE, dQ, dK, dV inside the timed region, every step), with consecutive steps
+overlapped as a stream of batches would be: the next step's inputs and the
+previous step's results move on two copy streams while a step computes.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload page3]
   python bench.py --impl reference ...   # the fp64 CPU oracle, timed on host cores
@@ -332,35 +334,60 @@ def run_gpu_arm(args, world, rank):
     kernel_rates = {n: (kflops[n] / (v * 1e-3) / 1e12 if n in kflops
                         else delta_bytes / (v * 1e-3) / 1e9) for n, v in per_kernel_ms.items()}
 
-    # End to end through the public API with host buffers.
+    # End to end through the public API with host buffers.  Every step copies
+    # its inputs from pinned host memory, runs attn_fwd + attn_bwd and reads
+    # all five results back into pinned host memory.  Consecutive steps
+    # overlap the way a stream of batches does: the inputs of step i + 1 go in
+    # and the results of step i - 1 come out (one copy stream each way) while
+    # step i computes, on up to three device sets used in turn.
     hin = P.host_in
-    ins, outs = P.sets[0]
-    houts = {n: torch.empty(outs[n].shape, dtype=outs[n].dtype, pin_memory=True)
-             for n in ("o", "lse", "dq", "dk", "dv")}
+    nb = min(3, len(P.sets))
+    houts = [{n: torch.empty(P.sets[k][1][n].shape, dtype=P.sets[k][1][n].dtype, pin_memory=True)
+              for n in ("o", "lse", "dq", "dk", "dv")} for k in range(nb)]
     n_e2e = max(3, min(K, 200))
     h2d = sum(t.numel() * t.element_size() for t in hin)
-    d2h = sum(t.numel() * t.element_size() for t in houts.values())
+    d2h = sum(t.numel() * t.element_size() for t in houts[0].values())
+    s_c = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {n: [torch.cuda.Event() for _ in range(nb)] for n in ("in", "done", "out")}
 
-    def e2e_step():
-        for dst, src in zip(ins, hin):
-            dst.copy_(src, non_blocking=True)
-        P.step_api(0)
-        for n, h in houts.items():
-            h.copy_(outs[n], non_blocking=True)
+    def e2e_run(n):
+        for i in range(n):
+            k = i % nb
+            ins, outs = P.sets[k]
+            with torch.cuda.stream(s_in):
+                if i >= nb:
+                    s_in.wait_event(ev["done"][k])  # step i - nb has read these inputs
+                for dst, src in zip(ins, hin):
+                    dst.copy_(src, non_blocking=True)
+                ev["in"][k].record(s_in)
+            s_c.wait_event(ev["in"][k])
+            if i >= nb:
+                s_c.wait_event(ev["out"][k])  # step i - nb's results have been read out
+            P.step_api(k)
+            ev["done"][k].record(s_c)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev["done"][k])
+                for name, h in houts[k].items():
+                    h.copy_(outs[name], non_blocking=True)
+                ev["out"][k].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    e2e_run(3)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n_e2e):
-        e2e_step()
-    b.record()
+    a.record(s_c)
+    s_in.wait_event(a)
+    s_out.wait_event(a)
+    e2e_run(n_e2e)
+    s_c.wait_stream(s_out)
+    b.record(s_c)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(a.elapsed_time(b) / n_e2e, world)
     e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
            "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "steps": n_e2e}
+           "steps": n_e2e,
+           "overlap": f"inputs of step i+1 and results of step i-1 copied on two copy streams "
+                      f"while step i computes ({nb} device sets)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
