@@ -821,10 +821,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // host dealt it.  Per pipeline, warp 0 loads each unit's Q, dO and the K, V
 // ring; warp 1 issues S = Q K^T, dP = dO V^T and dQ += dS K; warps 2..9 (two
 // threads per query row, one per 32-key half) form P and dS and, at the
-// unit's end, write dQ.  At D = 64, dS goes to a shared-memory tile and the
+// unit's end, write dQ.  The unit's Q and dO are copied into TMEM (the A
+// operands of S and dP), dS goes to a shared-memory tile, and the
 // element-wise warps release S, dP as soon as they hold them in registers, so
-// the next key tile's S, dP are computed while they work on this one; at
-// D = 128, dS is written over S in TMEM and the tiles run one after another.
+// the next key tile's S, dP are computed while they work on this one.
 constexpr int kDqPipeWarps = 10;  // producer, MMA issuer, 8 compute warps
 constexpr int kDqPipeThreads = kDqPipeWarps * 32;
 template <int D>
@@ -832,32 +832,30 @@ struct DqCfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kQBytes = kTileM * 128 * kAtoms;     // 128 queries x D
   static constexpr int kKvBytes = kDqTileN * 128 * kAtoms;  // 64 keys x D
-  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kStages = 3;
   static constexpr int kOffQ = 0;
   static constexpr int kOffdO = kQBytes;
   static constexpr int kOffK = 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKvBytes;
-  // D = 64: the dS tile [128 queries x 64 keys] bf16, 128-byte swizzled like a
+  // The dS tile [128 queries x 64 keys] bf16, 128-byte swizzled like a
   // TMA-loaded tile, read by the dQ MMA from shared memory.
-  static constexpr bool kDsInSmem = (D == 64);
   static constexpr int kOffDS = kOffV + kStages * kKvBytes;
-  static constexpr int kPipeBytes = kOffDS + (kDsInSmem ? kTileM * 128 : 0);  // multiple of 1024
+  static constexpr int kPipeBytes = kOffDS + kTileM * 128;  // multiple of 1024
   static constexpr int NP = qtile_pipes_per_block(D);
   static constexpr int kSmemBytes = NP * kPipeBytes + 1024;
-  static constexpr uint32_t kTmemCols = 256;  // per pipeline (D = 64: 2 x 256)
-  static constexpr uint32_t kColS = 0;    // S fp32 [128 x 64]; dS bf16 over cols 0..31 (D = 128)
+  static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;  // per pipeline
+  static constexpr uint32_t kColS = 0;    // S fp32 [128 x 64]
   static constexpr uint32_t kColDP = 64;  // dP fp32 [128 x 64]
   static constexpr uint32_t kColDQ = 128; // dQ accumulator, D cols
-  // For D = 64 the unit's Q and dO tiles also live in TMEM (packed bf16
-  // pairs, 32 columns each), so S = Q K^T and dP = dO V^T read only K / V from
-  // shared memory: an N = 64 MMA with both operands in shared memory is bound
-  // by shared-memory bandwidth (48 clocks against 32 for the math).
-  static constexpr bool kQInTmem = (D == 64);
-  static constexpr uint32_t kColQ = 192;
-  static constexpr uint32_t kColdO = 224;
+  // The unit's Q and dO tiles also live in TMEM (packed bf16 pairs, D/2
+  // columns each), so S = Q K^T and dP = dO V^T read only K / V from shared
+  // memory: an N = 64 MMA with both operands in shared memory is bound by
+  // shared-memory bandwidth (48 clocks against 32 for the math).
+  static constexpr uint32_t kColQ = kColDQ + D;
+  static constexpr uint32_t kColdO = kColQ + D / 2;
+  static_assert(kColdO + D / 2 <= kTmemCols, "TMEM layout");
   static_assert(kPipeBytes % 1024 == 0, "pipelines keep the 1024-byte swizzle alignment");
   static_assert(D == 64 || NP == 1, "D = 128 needs a block's whole TMEM");
-  static_assert(!kDsInSmem || kQInTmem, "the early release of S, dP assumes Q, dO in TMEM");
   static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory per block");
 };
 
@@ -865,8 +863,8 @@ enum : int { kDqBarQ = 0, kDqBarKFull = 1, kDqBarVFull = 4, kDqBarKEmpty = 7, kD
              kDqBarS = 13, kDqBarDS = 14, kDqBarAcc = 15, kDqBarDrain = 16, kDqBarQTmem = 17,
              kDqBarQUsed = 18,   // the unit's S, dP MMAs are done (Q, dO no longer read)
              kDqBarAccFree = 19, // the unit's epilogue has read dQ
-             kDqBarSFree = 20,   // D = 64: element-wise warps hold this tile's S, dP in registers
-             kDqBarDSFree = 21,  // D = 64: the dQ MMAs are done with the dS tile
+             kDqBarSFree = 20,   // element-wise warps hold this tile's S, dP in registers
+             kDqBarDSFree = 21,  // the dQ MMAs are done with the dS tile
              kDqNumBars = 22 };
 
 template <int D>
@@ -962,11 +960,8 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
       int gj = 0;  // key tiles loaded so far, over all units
       for (int ku = 0; ku < n_units && ok; ++ku) {
         const Unit t = unit_info(u_of(ku));
-        // The previous unit's Q, dO must no longer be read: copied to TMEM
-        // (D = 64) or consumed by its S, dP MMAs (D = 128).
-        if (ku > 0 && !(ok = mbar_wait(bar(C::kQInTmem ? kDqBarQTmem : kDqBarQUsed), (ku - 1) & 1,
-                                       wait_ns)))
-          break;
+        // The previous unit's Q, dO must no longer be read: copied to TMEM.
+        if (ku > 0 && !(ok = mbar_wait(bar(kDqBarQTmem), (ku - 1) & 1, wait_ns))) break;
         mbar_arrive_expect_tx(bar(kDqBarQ), 2 * C::kQBytes);
         for (int at = 0; at < C::kAtoms; ++at) {
           tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kDqBarQ), at * 64, t.h, t.m0, t.b);
@@ -1005,11 +1000,10 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
     constexpr uint32_t kIdS = idesc_bf16(kTileM, kDqTileN, false, false);
     constexpr uint32_t kIdDQ = idesc_bf16(kTileM, D, false, true);
     // Operand descriptors built once; the loops only add constant offsets.
-    const uint64_t dQ = sdesc_sw128(sQ, 16, 1024), ddO = sdesc_sw128(sdO, 16, 1024);
     const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024), dV0 = sdesc_sw128(sV0, 16, 1024);
     const uint64_t dKm0 = sdesc_sw128(sK0, kDqTileN * 128, 1024);  // K as MN-major B
     int gj = 0;
-    if constexpr (C::kDsInSmem) {
+    {
       const uint64_t dDS = sdesc_sw128(sDS, 16, 1024);  // dS as K-major A
       const uint32_t aQ = tmem + C::kColQ, adO = tmem + C::kColdO;
       // S, dP of tile j of unit ku (g-th over all units), once the element-wise
@@ -1023,13 +1017,25 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         if (g > 0 && !warp_all(mbar_wait(bar(kDqBarSFree), (g - 1) & 1, wait_ns))) return false;
         if (!warp_all(mbar_wait(bar(kDqBarKFull + s), ph, wait_ns))) return false;
         tc_fence_after();
+        // K = D in steps of 16: packed Q / dO columns 8 apart, K-major K / V
+        // slices of 32 bytes, 64-column atoms kDqTileN * 128 bytes apart.
         const uint64_t dK = desc_add(dK0, s * C::kKvBytes), dV = desc_add(dV0, s * C::kKvBytes);
-        mma_ts_x4(tS, aQ, aQ + 8, aQ + 16, aQ + 24, dK, desc_add(dK, 32), desc_add(dK, 64),
-                  desc_add(dK, 96), kIdS, 0u);
+#pragma unroll
+        for (int at = 0; at < C::kAtoms; ++at) {
+          const uint32_t a = aQ + 32 * at;
+          const uint64_t b = desc_add(dK, at * (kDqTileN * 128));
+          mma_ts_x4(tS, a, a + 8, a + 16, a + 24, b, desc_add(b, 32), desc_add(b, 64),
+                    desc_add(b, 96), kIdS, at > 0 ? 1u : 0u);
+        }
         if (!warp_all(mbar_wait(bar(kDqBarVFull + s), ph, wait_ns))) return false;
         tc_fence_after();
-        mma_ts_x4(tDP, adO, adO + 8, adO + 16, adO + 24, dV, desc_add(dV, 32), desc_add(dV, 64),
-                  desc_add(dV, 96), kIdS, 0u);
+#pragma unroll
+        for (int at = 0; at < C::kAtoms; ++at) {
+          const uint32_t a = adO + 32 * at;
+          const uint64_t b = desc_add(dV, at * (kDqTileN * 128));
+          mma_ts_x4(tDP, a, a + 8, a + 16, a + 24, b, desc_add(b, 32), desc_add(b, 64),
+                    desc_add(b, 96), kIdS, at > 0 ? 1u : 0u);
+        }
         mma_commit(bar(kDqBarS));
         mma_commit(bar(kDqBarVEmpty + s));
         if (j + 1 == t.n_kv) mma_commit(bar(kDqBarQUsed));  // the unit's last S, dP
@@ -1066,71 +1072,13 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         }
       }
     }
-    for (int ku = 0; !C::kDsInSmem && ku < n_units && ok; ++ku) {
-      const Unit t = unit_info(u_of(ku));
-      if (!(ok = warp_all(mbar_wait(bar(kDqBarQ), ku & 1, wait_ns)))) break;
-      if (C::kQInTmem && !(ok = warp_all(mbar_wait(bar(kDqBarQTmem), ku & 1, wait_ns)))) break;
-      tc_fence_after();
-      for (int j = 0; j < t.n_kv && ok; ++j, ++gj) {
-        const int s = gj % NS;
-        const uint32_t ph = (gj / NS) & 1;
-        const uint64_t dK = desc_add(dK0, s * C::kKvBytes), dV = desc_add(dV0, s * C::kKvBytes);
-        const uint64_t dKm = desc_add(dKm0, s * C::kKvBytes);
-        if (!(ok = warp_all(mbar_wait(bar(kDqBarKFull + s), ph, wait_ns)))) break;
-        tc_fence_after();
-        if (C::kQInTmem) {
-          const uint32_t aQ = tmem + C::kColQ;
-          mma_ts_x4(tS, aQ, aQ + 8, aQ + 16, aQ + 24, dK, desc_add(dK, 32), desc_add(dK, 64),
-                    desc_add(dK, 96), kIdS, 0u);
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
-            const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
-            mma_ss(tS, desc_add(dQ, oq), desc_add(dK, okv), kIdS, ks > 0);
-          }
-        }
-        if (!(ok = warp_all(mbar_wait(bar(kDqBarVFull + s), ph, wait_ns)))) break;
-        tc_fence_after();
-        if (C::kQInTmem) {
-          const uint32_t adO = tmem + C::kColdO;
-          mma_ts_x4(tDP, adO, adO + 8, adO + 16, adO + 24, dV, desc_add(dV, 32), desc_add(dV, 64),
-                    desc_add(dV, 96), kIdS, 0u);
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t oq = (ks >> 2) * (kTileM * 128) + (ks & 3) * 32;
-            const uint32_t okv = (ks >> 2) * (kDqTileN * 128) + (ks & 3) * 32;
-            mma_ss(tDP, desc_add(ddO, oq), desc_add(dV, okv), kIdS, ks > 0);
-          }
-        }
-        mma_commit(bar(kDqBarS));
-        mma_commit(bar(kDqBarVEmpty + s));
-        if (j + 1 == t.n_kv) mma_commit(bar(kDqBarQUsed));  // the unit's last S, dP
-        if (!(ok = warp_all(mbar_wait(bar(kDqBarDS), gj & 1, wait_ns)))) break;
-        // The previous unit's epilogue must have read dQ before this unit's
-        // first dQ MMA overwrites it.
-        if (j == 0 && ku > 0 &&
-            !(ok = warp_all(mbar_wait(bar(kDqBarAccFree), (ku - 1) & 1, wait_ns))))
-          break;
-        tc_fence_after();
-        // dS of keys 16ks..16ks+15: half ks/2 wrote its 32 keys as 16 packed
-        // columns at the start of its own 32 S columns.
-        static_assert(kDqTileN == 64, "the dQ issue below takes 4 key steps");
-        mma_ts_x4(tDQ, tS, tS + 8, tS + 32, tS + 40, dKm, desc_add(dKm, 2048), desc_add(dKm, 4096),
-                  desc_add(dKm, 6144), kIdDQ, j > 0 ? 1u : 0u);
-        mma_commit(bar(kDqBarKEmpty + s));
-      }
-      if (!ok) break;
-      mma_commit(bar(kDqBarAcc));
-    }
     mma_commit(bar(kDqBarDrain));
     warp_all(mbar_wait(bar(kDqBarDrain), 0, wait_ns));
   } else {
     // Eight warps: warps w and w+4 of a pipeline share a TMEM lane quarter,
     // i.e. the same 32 query rows; half 0 takes key columns 0..31 of the tile,
-    // half 1 columns 32..63.  Each half writes its dS (bf16 pairs) over the
-    // first 16 of its own 32 S columns.
+    // half 1 columns 32..63, and writes its dS (bf16) into those columns of the
+    // shared-memory dS tile.
     const int quarter = gwarp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
@@ -1139,9 +1087,10 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
     const float sl2 = a.scale_log2;
     // Q and dO row r of unit ku into TMEM as the A operands of S and dP, once
     // the previous unit's S, dP MMAs no longer read them: this warp copies
-    // elements 32 half..32 half+31 (four 16-byte chunks of the
-    // 128-byte-swizzled tile row) as 16 packed pairs.  Done for the next unit
-    // before this unit's epilogue, so its first S, dP overlap the epilogue.
+    // elements D/2 half .. D/2 half + D/2 - 1 (D/16 16-byte chunks of the
+    // 128-byte-swizzled tile row, 64-column atoms 128 * 128 bytes apart) as
+    // D/4 packed pairs.  Done for the next unit before this unit's epilogue,
+    // so its first S, dP overlap the epilogue.
     auto copy_q = [&](int ku) -> bool {
       bool good = true;
       if (ku > 0) good = warp_all(mbar_wait(bar(kDqBarQUsed), (ku - 1) & 1, wait_ns));
@@ -1150,17 +1099,22 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         tc_fence_after();
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
-          const uint32_t base = (which == 0 ? sQ : sdO) + r * 128;
-          uint32_t v16[16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 x = ld_shared_u4(base + (((4 * half + c) ^ (r & 7)) * 16));
-            v16[4 * c] = x.x;
-            v16[4 * c + 1] = x.y;
-            v16[4 * c + 2] = x.z;
-            v16[4 * c + 3] = x.w;
+          for (int g = 0; g < D / 64; ++g) {  // groups of four chunks (32 elements)
+            uint32_t v16[16];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int e = half * (D / 2) + 32 * g + 8 * c;  // first element of the chunk
+              const uint32_t base = (which == 0 ? sQ : sdO) + (e / 64) * (kTileM * 128) + r * 128;
+              const uint4 x = ld_shared_u4(base + ((((e % 64) / 8) ^ (r & 7)) * 16));
+              v16[4 * c] = x.x;
+              v16[4 * c + 1] = x.y;
+              v16[4 * c + 2] = x.z;
+              v16[4 * c + 3] = x.w;
+            }
+            tmem_st16_nowait(tl + (which == 0 ? C::kColQ : C::kColdO) + half * (D / 4) + 16 * g,
+                             v16);
           }
-          tmem_st16_nowait(tl + (which == 0 ? C::kColQ : C::kColdO) + half * 16, v16);
         }
         tmem_wait_st();
       }
@@ -1169,7 +1123,7 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
       if (lane == 0) mbar_arrive(bar(kDqBarQTmem));
       return good;
     };
-    if (C::kQInTmem && n_units > 0) ok = copy_q(0);
+    if (n_units > 0) ok = copy_q(0);
     int gj = 0;
     for (int ku = 0; ku < n_units && ok; ++ku) {
       const Unit t = unit_info(u_of(ku));
@@ -1186,12 +1140,10 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         tmem_wait_ld();
         reg_fence32(sv);
         reg_fence32(dp);
-        if constexpr (C::kDsInSmem) {
-          // S, dP are in registers: the next tile's may overwrite them.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kDqBarSFree));
-        }
+        // S, dP are in registers: the next tile's may overwrite them.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kDqBarSFree));
         const int kv0 = j * kDqTileN + half * 32;  // key of this half's first column
         // key kv0 + c visible iff c <= lim
         const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
@@ -1229,26 +1181,20 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
           element_loop(std::true_type{});
         else
           element_loop(std::false_type{});
-        if constexpr (C::kDsInSmem) {
-          // The previous tile's dQ MMAs must be done reading the dS tile.
-          if (gj > 0 && !(ok = warp_all(mbar_wait(bar(kDqBarDSFree), (gj - 1) & 1, wait_ns)))) break;
-          // Row r, keys 32 half .. 32 half + 31: 16-byte chunks 4 half .. 4 half + 3
-          // of the 128-byte-swizzled row.
+        // The previous tile's dQ MMAs must be done reading the dS tile.
+        if (gj > 0 && !(ok = warp_all(mbar_wait(bar(kDqBarDSFree), (gj - 1) & 1, wait_ns)))) break;
+        // Row r, keys 32 half .. 32 half + 31: 16-byte chunks 4 half .. 4 half + 3
+        // of the 128-byte-swizzled row.
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            st_shared_u4(sDS + r * 128 + (((4 * half + i) ^ (r & 7)) * 16),
-                         make_uint4(dsk[4 * i], dsk[4 * i + 1], dsk[4 * i + 2], dsk[4 * i + 3]));
-          fence_proxy_async_smem();  // visible to the tensor core's reads
-        } else {
-          tmem_st16_nowait(tS, dsk);
-          tmem_wait_st();
-          tc_fence_before();
-        }
+        for (int i = 0; i < 4; ++i)
+          st_shared_u4(sDS + r * 128 + (((4 * half + i) ^ (r & 7)) * 16),
+                       make_uint4(dsk[4 * i], dsk[4 * i + 1], dsk[4 * i + 2], dsk[4 * i + 3]));
+        fence_proxy_async_smem();  // visible to the tensor core's reads
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kDqBarDS));
       }
       if (!ok) break;
-      if (C::kQInTmem && ku + 1 < n_units && !(ok = copy_q(ku + 1))) break;
+      if (ku + 1 < n_units && !(ok = copy_q(ku + 1))) break;
       ok = warp_all(mbar_wait(bar(kDqBarAcc), ku & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
