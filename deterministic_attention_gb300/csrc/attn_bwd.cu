@@ -20,6 +20,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <type_traits>
@@ -61,91 +62,96 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
 }
 
 // ============================================================== Delta
-// Rows (b, t, h) in memory order: warp w takes rows 32 w .. 32 w + 31 of the
-// [B, T, Hq] row space, so each warp streams 32 contiguous rows of O and dO
-// (4 KB each at D = 64) -- whole DRAM pages, where one head's rows alone lie
-// Hq * D * 2 bytes apart.  Each row of D bf16 is split in 16-byte chunks over
-// D/8 lanes; a lane issues all its loads first, forms its 8 products per chunk
-// in order, and the lanes of a row are combined by a fixed xor-shuffle tree.
-// The first lane of a row reads that row's LSE and stores its
-// (-LSE*log2e, -Delta) pair.  Warps past the row space write (-inf, -0) to
-// the padding positions T..Tp-1 of every (b, h).
+// Rows (b, t, h) in memory order, so a run of rows is one contiguous stretch
+// of O and of dO (whole DRAM pages, where one head's rows alone lie
+// Hq * D * 2 bytes apart).  Each row of D bf16 is split in 16-byte chunks over
+// D/8 lanes, so one warp-wide load covers kRpi = 256 / D rows; a warp takes
+// batches of kBatch such loads (kBatch * kRpi contiguous rows, 2 KB of O and
+// 2 KB of dO per load step), batch index striding by the number of warps in
+// the grid, and issues all of a batch's loads before it uses any.  The grid
+// holds four blocks per SM, so every SM keeps about 128 KB of loads in flight
+// through the whole pass.  A lane forms its 8 products per chunk in order and
+// the lanes of a row are combined by a fixed xor-shuffle tree; the first lane
+// of a row reads that row's LSE and stores its (-LSE*log2e, -Delta) pair.
+// The padding positions T..Tp-1 of every (b, h) get (-inf, -0).
+constexpr int kDeltaBlocksPerSm = 4;
 template <int D>
-__global__ void __launch_bounds__(256) attn_delta_kernel(const DeltaArgs a) {
+__global__ void __launch_bounds__(256, kDeltaBlocksPerSm) attn_delta_kernel(const DeltaArgs a) {
   // Launched as a dependent of whatever precedes it (the forward, in a
   // training step): everything below reads that kernel's output.  Only after
   // this wait may the next kernel (the dK/dV step) start its own prologue.
   griddep_wait();
   griddep_launch_dependents();
-  constexpr int kCpr = D / 8;        // 16-byte chunks per row
-  constexpr int kRpi = 32 / kCpr;    // rows per warp iteration
-  constexpr int kIters = 32 / kRpi;
+  constexpr int kCpr = D / 8;          // 16-byte chunks per row
+  constexpr int kRpi = 32 / kCpr;      // rows per warp-wide load
+  constexpr int kBatch = 4;            // loads per operand per batch
+  constexpr int kRows = kBatch * kRpi; // rows per batch
   const int lane = threadIdx.x & 31;
-  const long warp_id = static_cast<long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const long n_warps = static_cast<long>(gridDim.x) * (blockDim.x / 32);
+  const long gw = static_cast<long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
   const long rows = static_cast<long>(a.B) * a.T * a.Hq;
-  const long row_warps = (rows + 31) / 32;
-  if (warp_id >= row_warps) {
-    // Padding positions: (b, h, t) for t in [T, Tp), 32 per warp.
-    const int pad = a.Tp - a.T;
-    const long p = (warp_id - row_warps) * 32 + lane;
-    if (pad > 0 && p < static_cast<long>(a.B) * a.Hq * pad) {
-      const long bh = p / pad;
-      const int t = a.T + static_cast<int>(p % pad);
-      a.rowstats[bh * a.Tp + t] = make_float2(-INFINITY, -0.f);
-    }
-    return;
-  }
+  const long n_batches = (rows + kRows - 1) / kRows;
   const uint4* O = static_cast<const uint4*>(a.o);
   const uint4* dO = static_cast<const uint4*>(a.dout);
-  const long r0 = warp_id * 32;
-  uint4 xo[kIters], xd[kIters];
-  float lse[kIters];  // of this lane's row in each iteration (its first lane stores it)
-  size_t dst[kIters];
-  // (b, t, h) of this lane's row, decoded once and advanced by kRpi rows per
-  // iteration.
-  const long r_lane = r0 + lane / kCpr;
-  int h = static_cast<int>(r_lane % a.Hq);
-  const long bt0 = r_lane / a.Hq;
-  int b = static_cast<int>(bt0 / a.T), t = static_cast<int>(bt0 % a.T);
+  for (long bi = gw; bi < n_batches; bi += n_warps) {
+    // (b, t, h) of this lane's row in load step 0, advanced by kRpi rows per
+    // step.
+    const long r_lane = bi * kRows + lane / kCpr;
+    int h = static_cast<int>(r_lane % a.Hq);
+    const long bt0 = r_lane / a.Hq;
+    int b = static_cast<int>(bt0 / a.T), t = static_cast<int>(bt0 % a.T);
+    uint4 xo[kBatch], xd[kBatch];
+    float lse[kBatch];
+    size_t dst[kBatch];
 #pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const long r = r_lane + it * kRpi;
-    xo[it] = make_uint4(0u, 0u, 0u, 0u);
-    xd[it] = xo[it];
-    lse[it] = 0.f;
-    dst[it] = 0;
-    if (r < rows) {
-      const size_t off = static_cast<size_t>(r) * kCpr + lane % kCpr;
-      xo[it] = O[off];
-      xd[it] = dO[off];
-      const size_t bh = static_cast<size_t>(b) * a.Hq + h;
-      if (lane % kCpr == 0) lse[it] = a.lse[bh * a.T + t];
-      dst[it] = bh * a.Tp + t;
-    }
-    h += kRpi;
-    while (h >= a.Hq) {
-      h -= a.Hq;
-      if (++t == a.T) {
-        t = 0;
-        ++b;
+    for (int it = 0; it < kBatch; ++it) {
+      const long r = r_lane + it * kRpi;
+      xo[it] = make_uint4(0u, 0u, 0u, 0u);
+      xd[it] = xo[it];
+      lse[it] = 0.f;
+      dst[it] = 0;
+      if (r < rows) {
+        const size_t off = static_cast<size_t>(r) * kCpr + lane % kCpr;
+        xo[it] = O[off];
+        xd[it] = dO[off];
+        const size_t bh = static_cast<size_t>(b) * a.Hq + h;
+        if (lane % kCpr == 0) lse[it] = a.lse[bh * a.T + t];
+        dst[it] = bh * a.Tp + t;
+      }
+      h += kRpi;
+      while (h >= a.Hq) {
+        h -= a.Hq;
+        if (++t == a.T) {
+          t = 0;
+          ++b;
+        }
       }
     }
-  }
 #pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const uint32_t xs[4] = {xo[it].x, xo[it].y, xo[it].z, xo[it].w};
-    const uint32_t ys[4] = {xd[it].x, xd[it].y, xd[it].z, xd[it].w};
-    float acc = 0.f;
+    for (int it = 0; it < kBatch; ++it) {
+      const uint32_t xs[4] = {xo[it].x, xo[it].y, xo[it].z, xo[it].w};
+      const uint32_t ys[4] = {xd[it].x, xd[it].y, xd[it].z, xd[it].w};
+      float acc = 0.f;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float2 xf = bf16x2_to_float2(xs[k]), yf = bf16x2_to_float2(ys[k]);
-      acc = fmaf(xf.x, yf.x, acc);
-      acc = fmaf(xf.y, yf.y, acc);
+      for (int k = 0; k < 4; ++k) {
+        const float2 xf = bf16x2_to_float2(xs[k]), yf = bf16x2_to_float2(ys[k]);
+        acc = fmaf(xf.x, yf.x, acc);
+        acc = fmaf(xf.y, yf.y, acc);
+      }
+#pragma unroll
+      for (int s2 = kCpr / 2; s2 >= 1; s2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s2);
+      const long r = r_lane + it * kRpi;
+      if (lane % kCpr == 0 && r < rows) a.rowstats[dst[it]] = make_float2(-lse[it] * kLog2e, -acc);
     }
-#pragma unroll
-    for (int s2 = kCpr / 2; s2 >= 1; s2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s2);
-    const long r = r0 + it * kRpi + lane / kCpr;
-    if (lane % kCpr == 0 && r < rows) a.rowstats[dst[it]] = make_float2(-lse[it] * kLog2e, -acc);
+  }
+  // Padding positions: (b, h, t) for t in [T, Tp).
+  const int pad = a.Tp - a.T;
+  const long n_pad = static_cast<long>(a.B) * a.Hq * pad;
+  for (long p = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; p < n_pad;
+       p += static_cast<long>(gridDim.x) * blockDim.x) {
+    const long bh = p / pad;
+    const int t = a.T + static_cast<int>(p % pad);
+    a.rowstats[bh * a.Tp + t] = make_float2(-INFINITY, -0.f);
   }
 }
 
@@ -1325,10 +1331,13 @@ cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
 
 }  // namespace
 
-cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st) {
-  const long row_warps = (static_cast<long>(a.B) * a.T * a.Hq + 31) / 32;
-  const long pad_warps = (static_cast<long>(a.B) * a.Hq * (a.Tp - a.T) + 31) / 32;
-  const int grid = static_cast<int>((row_warps + pad_warps + 7) / 8);
+cudaError_t launch_delta(const DeltaArgs& a, int sms, cudaStream_t st) {
+  // Persistent: kDeltaBlocksPerSm blocks per SM, fewer when there are fewer
+  // batches of rows than warps.
+  const int rows_per_batch = 4 * (256 / a.D);
+  const long batches = (static_cast<long>(a.B) * a.T * a.Hq + rows_per_batch - 1) / rows_per_batch;
+  const long want = std::max<long>(1, (batches + 7) / 8);
+  const int grid = static_cast<int>(std::min<long>(want, static_cast<long>(sms) * kDeltaBlocksPerSm));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(256);

@@ -78,7 +78,8 @@ struct BwdArgs {
 cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const FwdArgs& a, const QTileSched& sched,
                        cudaStream_t st);
-cudaError_t launch_delta(const DeltaArgs& a, cudaStream_t st);
+// `sms`: the current device's SM count (the grid is persistent).
+cudaError_t launch_delta(const DeltaArgs& a, int sms, cudaStream_t st);
 // Clusters of c blocks of the dK/dV kernel that can be resident at once on the
 // current device (c = 1: blocks), and the largest c the kernel supports.
 cudaError_t dkdv_max_clusters(int D, int c, int* out);

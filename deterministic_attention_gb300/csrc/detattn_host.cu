@@ -229,7 +229,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
 int delta_impl(const void* o, const void* dout, const float* lse, void* workspace, int B, int T,
                int Hq, int D, cudaStream_t st) {
   DeltaArgs a{o, dout, lse, static_cast<float2*>(workspace), B, T, padded_T(T), Hq, D};
-  return launched(launch_delta(a, st), "attn_bwd_delta");
+  int sms = 0;
+  int rc;
+  if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
+  return launched(launch_delta(a, sms, st), "attn_bwd_delta");
 }
 
 BwdArgs bwd_args(const void* workspace, int T, int Hq, int Hkv, float scale, int causal) {
