@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(256, kDeltaBlocksPerSm) attn_delta_kernel(cons
   // this wait may the next kernel (the dK/dV step) start its own prologue.
   griddep_wait();
   griddep_launch_dependents();
+  // The dQ step's unit counter (two words) starts each backward at zero.
+  if (a.unit_counter != nullptr && blockIdx.x == 0 && threadIdx.x < 2) a.unit_counter[threadIdx.x] = 0u;
   constexpr int kCpr = D / 8;          // 16-byte chunks per row
   constexpr int kRpi = 32 / kCpr;      // rows per warp-wide load
   constexpr int kBatch = 4;            // loads per operand per batch
@@ -871,7 +873,8 @@ enum : int { kDqBarQ = 0, kDqBarKFull = 1, kDqBarVFull = 4, kDqBarKEmpty = 7, kD
              kDqBarAccFree = 19, // the unit's epilogue has read dQ
              kDqBarSFree = 20,   // element-wise warps hold this tile's S, dP in registers
              kDqBarDSFree = 21,  // the dQ MMAs are done with the dS tile
-             kDqNumBars = 22 };
+             kDqBarUnit = 22,    // [4] unit k published in ring slot k % 4
+             kDqNumBars = 26 };
 
 template <int D>
 __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
@@ -902,6 +905,15 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
   auto u_of = [&](int k) {
     return sched.n_listed > 0 ? static_cast<int>(sched.unit[first + k]) : first + k * sched.n_pipes;
   };
+  // Units are numbered heaviest first.  With a.unit_counter, a pipeline's
+  // producer takes the next unit from that counter whenever it is ready for
+  // one, so pipelines that start early (on SMs another kernel frees first)
+  // take the heaviest units; otherwise it follows the host's deal.  Either
+  // way it passes unit k (or -1 after the last) to the pipeline's other warps
+  // in ring slot k % 4, published by mbarrier kDqBarUnit + k % 4.  Which
+  // pipeline computes a unit does not change any bit of its result.
+  const int n_all = a.n_tiles * a.BH;
+  __shared__ int unit_ring[NP][4];
   struct Unit { int b, h, hkv, m0, n_kv; };
   auto unit_info = [&](int u) {
     Unit t;
@@ -945,6 +957,7 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
     mbar_init(bar(kDqBarAccFree), 8);
     mbar_init(bar(kDqBarSFree), 8);
     mbar_init(bar(kDqBarDSFree), 1);
+    for (int k = 0; k < 4; ++k) mbar_init(bar(kDqBarUnit + k), 1);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -958,16 +971,43 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
   const uint32_t tmem = tmem_slot + pipe * C::kTmemCols;
   const uint64_t wait_ns = a.wait_ns;
   bool ok = true;
+  // Unit k of this pipeline, for the warps other than the producer (whole
+  // warp; -1 after the last unit, or when the wait runs out with ok false).
+  auto read_unit = [&](int k) -> int {
+    if (!(ok = warp_all(mbar_wait(bar(kDqBarUnit + (k & 3)), (k >> 2) & 1, wait_ns)))) return -1;
+    return unit_ring[pipe][k & 3];
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       int last_k[3] = {-1, -1, -1}, last_v[3] = {-1, -1, -1};
       int last_q = -1;
       int gj = 0;  // key tiles loaded so far, over all units
-      for (int ku = 0; ku < n_units && ok; ++ku) {
-        const Unit t = unit_info(u_of(ku));
+      for (int ku = 0; ok; ++ku) {
         // The previous unit's Q, dO must no longer be read: copied to TMEM.
         if (ku > 0 && !(ok = mbar_wait(bar(kDqBarQTmem), (ku - 1) & 1, wait_ns))) break;
+        int u;
+        if (a.unit_counter != nullptr) {
+          const unsigned v = atomicAdd(a.unit_counter, 1u);
+          u = v < static_cast<unsigned>(n_all) ? static_cast<int>(v) : -1;
+        } else {
+          u = ku < n_units ? u_of(ku) : -1;
+        }
+        unit_ring[pipe][ku & 3] = u;
+        mbar_arrive(bar(kDqBarUnit + (ku & 3)));
+        if (u < 0) {
+          if (a.unit_counter != nullptr) {
+            // Count this pipeline out (second word); the last one to finish
+            // taking units puts both words back to zero for the next launch.
+            __threadfence();
+            if (atomicAdd(a.unit_counter + 1, 1u) == gridDim.x * NP - 1) {
+              atomicExch(a.unit_counter, 0u);
+              atomicExch(a.unit_counter + 1, 0u);
+            }
+          }
+          break;
+        }
+        const Unit t = unit_info(u);
         mbar_arrive_expect_tx(bar(kDqBarQ), 2 * C::kQBytes);
         for (int at = 0; at < C::kAtoms; ++at) {
           tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kDqBarQ), at * 64, t.h, t.m0, t.b);
@@ -1048,11 +1088,12 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         return true;
       };
       Unit t{};
-      if (n_units > 0) {
-        t = unit_info(u_of(0));
+      int u = read_unit(0);
+      if (u >= 0) {
+        t = unit_info(u);
         ok = issue_sdp(t, 0, 0, 0);
       }
-      for (int ku = 0; ku < n_units && ok; ++ku) {
+      for (int ku = 0; u >= 0 && ok; ++ku) {
         for (int j = 0; j < t.n_kv && ok; ++j, ++gj) {
           const int s = gj % NS;
           if (j + 1 < t.n_kv && !(ok = issue_sdp(t, ku, j + 1, gj + 1))) break;
@@ -1072,8 +1113,9 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         }
         if (!ok) break;
         mma_commit(bar(kDqBarAcc));
-        if (ku + 1 < n_units) {
-          t = unit_info(u_of(ku + 1));
+        u = read_unit(ku + 1);
+        if (u >= 0) {
+          t = unit_info(u);
           ok = issue_sdp(t, ku + 1, 0, gj);
         }
       }
@@ -1129,10 +1171,11 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
       if (lane == 0) mbar_arrive(bar(kDqBarQTmem));
       return good;
     };
-    if (n_units > 0) ok = copy_q(0);
+    int u = read_unit(0);
+    if (u >= 0) ok = copy_q(0);
     int gj = 0;
-    for (int ku = 0; ku < n_units && ok; ++ku) {
-      const Unit t = unit_info(u_of(ku));
+    for (int ku = 0; u >= 0 && ok; ++ku) {
+      const Unit t = unit_info(u);
       const int qrow = t.m0 + r;
       // (-LSE*log2e, -Delta) of this row; rows past T read (-inf, -0): P = 0.
       const float2 rstat = a.rowstats[(static_cast<size_t>(t.b) * a.Hq + t.h) * a.Tp + qrow];
@@ -1200,7 +1243,9 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         if (lane == 0) mbar_arrive(bar(kDqBarDS));
       }
       if (!ok) break;
-      if (ku + 1 < n_units && !(ok = copy_q(ku + 1))) break;
+      const int u_next = read_unit(ku + 1);
+      if (!ok) break;
+      if (u_next >= 0 && !(ok = copy_q(ku + 1))) break;
       ok = warp_all(mbar_wait(bar(kDqBarAcc), ku & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
@@ -1228,6 +1273,7 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         for (int i = 0; i < D / 16; ++i)
           dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
       }
+      u = u_next;
     }
   }
 

@@ -56,6 +56,7 @@ struct DeltaArgs {
   const float* lse;      // fp32 [B, Hq, T]
   float2* rowstats;      // [B * Hq, Tp] pairs
   int B, T, Tp, Hq, D;
+  unsigned* unit_counter;  // the dQ step's unit counter, cleared here (may be null)
 };
 
 struct BwdArgs {
@@ -72,6 +73,9 @@ struct BwdArgs {
   float scale;
   float scale_log2;
   unsigned long long wait_ns;
+  // dQ: units are taken from this counter (zero at launch) instead of the
+  // static deal, when not null.
+  unsigned* unit_counter;
 };
 
 // Each returns the launch error (cudaSuccess when the kernel was queued).

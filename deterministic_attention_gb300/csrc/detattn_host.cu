@@ -226,9 +226,22 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   return launched(launch_fwd(D, g, mq, mk, mv, a, sc, st), "attn_fwd");
 }
 
+// Workspace: the row statistics, then (from a 256-byte boundary) the dQ
+// step's unit counter (two words: units taken, pipelines done).  A workspace too short for the counter runs the dQ
+// step on the host's static deal instead.
+size_t rowstat_bytes(int B, int T, int Hq) {
+  return static_cast<size_t>(B) * Hq * padded_T(T) * sizeof(float2);
+}
+size_t counter_offset(int B, int T, int Hq) { return (rowstat_bytes(B, T, Hq) + 255) / 256 * 256; }
+unsigned* unit_counter_ptr(const void* ws, size_t bytes, int B, int T, int Hq) {
+  if (bytes < counter_offset(B, T, Hq) + 2 * sizeof(unsigned)) return nullptr;
+  return reinterpret_cast<unsigned*>(static_cast<char*>(const_cast<void*>(ws)) +
+                                     counter_offset(B, T, Hq));
+}
+
 int delta_impl(const void* o, const void* dout, const float* lse, void* workspace, int B, int T,
-               int Hq, int D, cudaStream_t st) {
-  DeltaArgs a{o, dout, lse, static_cast<float2*>(workspace), B, T, padded_T(T), Hq, D};
+               int Hq, int D, unsigned* counter, cudaStream_t st) {
+  DeltaArgs a{o, dout, lse, static_cast<float2*>(workspace), B, T, padded_T(T), Hq, D, counter};
   int sms = 0;
   int rc;
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
@@ -344,7 +357,7 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
 
 int dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
             void* dq, int B, int T, int Hq, int Hkv, int D, float scale, int causal,
-            cudaStream_t st) {
+            unsigned* counter, cudaStream_t st) {
   CUtensorMap mq, mk, mv, mdo;
   int rc;
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
@@ -355,6 +368,7 @@ int dq_impl(const void* q, const void* k, const void* v, const void* dout, const
   a.dq = dq;
   a.n_tiles = (T + kTileM - 1) / kTileM;
   a.BH = B * Hq;
+  a.unit_counter = counter;
   int sms = 0;
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
   static_assert(kDqTileN == kFwdTileN, "the forward's schedule weights fit dQ");
@@ -362,10 +376,6 @@ int dq_impl(const void* q, const void* k, const void* v, const void* dout, const
   int g;
   cached_qtile_schedule(D, B, T, Hq, causal, sms, &sc, &g);
   return launched(launch_dq(D, g, mq, mk, mv, mdo, a, sc, st), "attn_bwd_dq");
-}
-
-size_t rowstat_bytes(int B, int T, int Hq) {
-  return static_cast<size_t>(B) * Hq * padded_T(T) * sizeof(float2);
 }
 
 int check_workspace(const void* ws, size_t bytes, int B, int T, int Hq) {
@@ -411,16 +421,18 @@ int side_stream(SideStream** out) {
 
 // Delta, then dK/dV on `st` and dQ on the side stream.
 int bwd_steps(const void* q, const void* k, const void* v, const void* o, const float* lse,
-              const void* dout, void* dq, void* dk, void* dv, void* ws, int B, int T, int Hq,
-              int Hkv, int D, float scale, int causal, cudaStream_t st) {
+              const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B,
+              int T, int Hq, int Hkv, int D, float scale, int causal, cudaStream_t st) {
   int rc;
-  if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, st)) != DETATTN_OK) return rc;
+  unsigned* counter = unit_counter_ptr(ws, ws_bytes, B, T, Hq);
+  if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, counter, st)) != DETATTN_OK) return rc;
   SideStream* ss = nullptr;
   if ((rc = side_stream(&ss)) != DETATTN_OK) return rc;
   cudaError_t e = cudaEventRecord(ss->fork, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->fork, 0);
   if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "fork: %s", cudaGetErrorString(e));
-  if ((rc = dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, ss->stream)) !=
+  if ((rc = dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, counter,
+                    ss->stream)) !=
       DETATTN_OK)
     return rc;
   // dK/dV follows the Delta step directly in `st`: its prologue and
@@ -485,7 +497,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
   bool empty = false;
   if (check_shape(B, T, Hq, Hkv, D, &empty) != DETATTN_OK || empty) return 0;
-  return rowstat_bytes(B, T, Hq);
+  return counter_offset(B, T, Hq) + 256;
 }
 
 int attn_bwd_delta(const void* o, const void* dout, const float* lse, void* workspace,
@@ -497,7 +509,9 @@ int attn_bwd_delta(const void* o, const void* dout, const float* lse, void* work
   if ((rc = check_ptrs({{o, "o"}, {dout, "dout"}, {lse, "lse"}})) != DETATTN_OK) return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, B, T, Hq)) != DETATTN_OK) return rc;
   if ((rc = check_device()) != DETATTN_OK) return rc;
-  return delta_impl(o, dout, lse, workspace, B, T, Hq, D, static_cast<cudaStream_t>(stream));
+  return delta_impl(o, dout, lse, workspace, B, T, Hq, D,
+                    unit_counter_ptr(workspace, workspace_bytes, B, T, Hq),
+                    static_cast<cudaStream_t>(stream));
 }
 
 int attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout,
@@ -530,6 +544,7 @@ int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout,
   if ((rc = check_workspace(workspace, workspace_bytes, B, T, Hq)) != DETATTN_OK) return rc;
   if ((rc = check_device()) != DETATTN_OK) return rc;
   return dq_impl(q, k, v, dout, workspace, dq, B, T, Hq, Hkv, D, scale, causal,
+                 unit_counter_ptr(workspace, workspace_bytes, B, T, Hq),
                  static_cast<cudaStream_t>(stream));
 }
 
@@ -547,7 +562,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
     return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, B, T, Hq)) != DETATTN_OK) return rc;
   if ((rc = check_device()) != DETATTN_OK) return rc;
-  return bwd_steps(q, k, v, o, lse, dout, dq, dk, dv, workspace, B, T, Hq, Hkv, D, scale, causal,
+  return bwd_steps(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, T, Hq, Hkv, D,
+                   scale, causal,
                    static_cast<cudaStream_t>(stream));
 }
 
@@ -572,11 +588,13 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
   void* ws = nullptr;
   if ((rc = noalloc_scratch(&ws)) != DETATTN_OK) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, st)) != DETATTN_OK) return rc;
+  // The built-in scratch holds the row statistics only: the dQ step follows
+  // the static deal.
+  if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, nullptr, st)) != DETATTN_OK) return rc;
   if ((rc = dkdv_impl(q, k, v, dout, ws, dk, dv, B, T, Hq, Hkv, D, scale, causal, st,
                       /*after_delta=*/true)) != DETATTN_OK)
     return rc;
-  return dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, st);
+  return dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, nullptr, st);
 }
 
 int detattn_check_status(void* stream) {

@@ -69,9 +69,10 @@ typedef enum {
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
              int Hq, int Hkv, int D, float scale, int causal, void* stream);
 
-/* Bytes of device workspace the backward needs: B * Hq * Tp * 8 with
- * Tp = T rounded up to a multiple of 128.  Returns 0 for an empty or invalid
- * shape.
+/* Bytes of device workspace the backward uses: R + 256, where
+ * R = B * Hq * Tp * 8 rounded up to a multiple of 256 and Tp = T rounded up to
+ * a multiple of 128.  Returns 0 for an empty or invalid shape.  Only the first
+ * B * Hq * Tp * 8 bytes are required; see the layout below for the rest.
  *
  * Workspace layout (written by attn_bwd_delta, read by attn_bwd_dkdv and
  * attn_bwd_dq): row statistics, one (float, float) pair per (b, h, t),
@@ -79,7 +80,14 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
  *   pair.x = -LSE[b,h,t] * log2(e),   pair.y = -Delta[b,h,t]
  *   Delta[b,h,t] = sum_d dout[b,t,h,d] * o[b,t,h,d]   (fp32, fixed order)
  * and (-inf, -0) for t >= T.  Stored negated and in base 2 because the
- * kernels add them: P = exp2(S*scale*log2(e) + pair.x), dS = P (dP + pair.y). */
+ * kernels add them: P = exp2(S*scale*log2(e) + pair.x), dS = P (dP + pair.y).
+ * At byte R: two unsigned words, a counter the dQ step takes its 128-query
+ * tiles from, heaviest first (so its blocks that start early, on SMs the
+ * concurrent dK/dV step frees first, take more of them), and a count of its
+ * pipelines done; the last pipeline puts both back to zero, and
+ * attn_bwd_delta clears them too.  Which block computes a tile changes none
+ * of its bits.  Without room for them (workspace_bytes < R + 8) the dQ step
+ * follows a static deal fixed by the shape and the SM count. */
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
 
 /* Backward.  Given q, k, v, the forward's o and lse, and dout, writes dq, dk,
@@ -135,7 +143,9 @@ int attn_bwd_dkdv(const void* q, const void* k, const void* v, const void* dout,
                   int Hq, int Hkv, int D, float scale, int causal, void* stream);
 
 /* Backward step 3 alone: dq, reduced over key tiles in ascending order by the
- * single block that owns the 128-query tile (no atomics). */
+ * single block that owns the 128-query tile (no atomics on the data).  Pass
+ * the workspace_bytes that attn_bwd_delta got on this workspace (that call
+ * cleared the tile counter; every dQ call leaves it cleared). */
 int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout,
                 const void* workspace, size_t workspace_bytes, void* dq, int B, int T, int Hq,
                 int Hkv, int D, float scale, int causal, void* stream);

@@ -63,9 +63,12 @@ def test_empty_problem_is_ok_without_device(L):
 
 
 def test_workspace_bytes(L):
-    assert L.attn_bwd_workspace_bytes(4, 1024, 12, 4, 64) == 4 * 12 * 1024 * 8
-    assert L.attn_bwd_workspace_bytes(1, 3, 1, 1, 64) == 128 * 8
-    assert L.attn_bwd_workspace_bytes(2, 129, 3, 1, 128) == 2 * 3 * 256 * 8
+    # Row statistics rounded up to 256 bytes, then 256 bytes for the dQ step's
+    # tile counter.
+    assert L.attn_bwd_workspace_bytes(4, 1024, 12, 4, 64) == 4 * 12 * 1024 * 8 + 256
+    assert L.attn_bwd_workspace_bytes(1, 3, 1, 1, 64) == 128 * 8 + 256
+    assert L.attn_bwd_workspace_bytes(2, 129, 3, 1, 128) == 2 * 3 * 256 * 8 + 256
+    assert L.attn_bwd_workspace_bytes(1, 1, 1, 1, 64) == 1024 + 256
     assert L.attn_bwd_workspace_bytes(1, 3, 3, 2, 64) == 0
     assert L.attn_bwd_workspace_bytes(0, 3, 2, 1, 64) == 0
 
