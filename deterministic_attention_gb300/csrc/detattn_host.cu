@@ -603,6 +603,10 @@ int detattn_check_status(void* stream) {
   cudaError_t e = take_fwd_status(st, &f);
   if (e == cudaSuccess) e = take_bwd_status(st, &b);
   if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (b & 16u)
+    return fail(DETATTN_ERR_WORKSPACE,
+                "the dQ step found its tile counter not cleared: run attn_bwd_delta on this "
+                "workspace (with the same workspace_bytes) first");
   if (f | b)
     return fail(DETATTN_ERR_DEVICE_TIMEOUT,
                 "a kernel gave up on a pipeline wait (fwd flags %u, bwd flags %u)", f, b);

@@ -152,8 +152,10 @@ int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout,
 
 /* Synchronises `stream`, then reads and clears the device-side status word
  * that kernels set when a pipeline wait runs out (a bounded wait, default
- * limit 1 s).  Returns DETATTN_OK, DETATTN_ERR_DEVICE_TIMEOUT or
- * DETATTN_ERR_CUDA. */
+ * limit 1 s).  Returns DETATTN_OK, DETATTN_ERR_DEVICE_TIMEOUT,
+ * DETATTN_ERR_WORKSPACE (a dQ step found the workspace's tile counter not
+ * cleared, i.e. attn_bwd_delta had not run on that workspace: that dQ
+ * step's dq is not valid) or DETATTN_ERR_CUDA. */
 int detattn_check_status(void* stream);
 
 /* Diagnostic for accuracy tests: evaluates on n device floats x the three

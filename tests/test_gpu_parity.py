@@ -253,3 +253,24 @@ def test_dq_dynamic_and_static_deal_agree_bitwise(name):
     _, _, dq_r = oracle.attn_rows(widen(q), widen(k), widen(v), widen(do), rows, w.softmax_scale, True)
     dq_g = np.stack([to_np(dq[b, i, h]) for b, h, i in rows])
     assert_bwd_close([("dQ", dq_g, dq_r)], f"{name} sampled rows")
+
+
+def test_dq_reports_a_counter_not_cleared():
+    """attn_bwd_dq on a workspace that attn_bwd_delta never touched (its tile
+    counter holds garbage) is reported through the status check; after
+    attn_bwd_delta the same workspace works."""
+    import deterministic_attention_gb300 as da
+    B, T, Hq, Hkv, D = 1, 384, 4, 2, 64
+    q, k, v, do = (t.cuda() for t in make_inputs(B, T, Hq, Hkv, D, seed=11))
+    o, lse = da.attn_fwd(q, k, v)
+    ws = torch.full((da.workspace_bytes(B, T, Hq, Hkv, D),), 0xFF, dtype=torch.uint8, device="cuda")
+    da.attn_bwd_dq(q, k, v, do, ws)
+    with pytest.raises(da.DetAttnError) as err:
+        da.check_status()
+    assert err.value.code == -9 and "not cleared" in str(err.value)
+    da.attn_bwd_delta(o, do, lse, ws)
+    dq = da.attn_bwd_dq(q, k, v, do, ws)
+    da.check_status()
+    dq_ref, _, _ = da.attn_bwd(q, k, v, o, lse, do)
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq_ref)
