@@ -825,8 +825,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // Work unit: one 128-query tile of one (b, query head), over 64-key tiles
 // 0..diagonal in ascending order.  Persistent like the forward: a block holds
 // NP pipelines (two at D = 64, one at D = 128), each with its own warps,
-// shared memory, mbarriers and TMEM columns, working through the units the
-// host dealt it.  Per pipeline, warp 0 loads each unit's Q, dO and the K, V
+// shared memory, mbarriers and TMEM columns, working through units it takes,
+// heaviest first, from a counter in the workspace (or, without one, the units
+// the host dealt it).  Per pipeline, warp 0 loads each unit's Q, dO and the K, V
 // ring; warp 1 issues S = Q K^T, dP = dO V^T and dQ += dS K; warps 2..9 (two
 // threads per query row, one per 32-key half) form P and dS and, at the
 // unit's end, write dQ.  The unit's Q and dO are copied into TMEM (the A
