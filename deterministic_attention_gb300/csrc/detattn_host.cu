@@ -316,7 +316,11 @@ int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int
         if (t >= total) break;
         const int nt = static_cast<int>(t / BH);
         const int items = G * (m_end - (causal ? nt * kTileN / tm : 0));
-        load += (items + c - 1) / c + 2;
+        // Per tile: its share of the items, one item's worth for writing the
+        // sums out, and two per peer for the partial-sum exchange (measured:
+        // distributed shared memory moves ~9 bytes per clock per SM, and an
+        // item takes ~1,500 clocks).
+        load += (items + c - 1) / c + 1.0 + 2.0 * (c - 1);
       }
       if (load > worst) worst = load;
     }
