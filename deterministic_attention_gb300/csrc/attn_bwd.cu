@@ -989,11 +989,18 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         if (ku > 0 && !(ok = mbar_wait(bar(kDqBarQTmem), (ku - 1) & 1, wait_ns))) break;
         int u;
         if (a.unit_counter != nullptr) {
-          const unsigned v = atomicAdd(a.unit_counter, 1u);
-          u = v < static_cast<unsigned>(n_all) ? static_cast<int>(v) : -1;
-          // A cleared counter never passes n_all plus one per pipeline: a
-          // larger value means it was not cleared before this launch.
-          if (v >= static_cast<unsigned>(n_all) + gridDim.x * NP) atomicOr(&g_bwd_status, 16u);
+          if (NP > 1 && pipe > 0 && n_all <= static_cast<int>(gridDim.x)) {
+            // No more units than blocks: the first pipeline of each block takes
+            // them, one unit per SM (the others would share SMs while blocks
+            // sit idle).
+            u = -1;
+          } else {
+            const unsigned v = atomicAdd(a.unit_counter, 1u);
+            u = v < static_cast<unsigned>(n_all) ? static_cast<int>(v) : -1;
+            // A cleared counter never passes n_all plus one per pipeline: a
+            // larger value means it was not cleared before this launch.
+            if (v >= static_cast<unsigned>(n_all) + gridDim.x * NP) atomicOr(&g_bwd_status, 16u);
+          }
         } else {
           u = ku < n_units ? u_of(ku) : -1;
         }
