@@ -33,8 +33,11 @@
  *   - Inputs are never written.  Outputs are fully overwritten (no zero-fill
  *     needed); rows t >= T are never touched.
  *   - Results are bitwise identical from call to call for identical inputs
- *     and shapes on the same GPU model: every output element is produced by
- *     one thread block in a fixed order, with no atomics.
+ *     and shapes on the same GPU model: every output element is produced in a
+ *     fixed order by one thread block (dk, dv: by the block that owns the
+ *     row, adding its cluster's partial sums in rank order), with no atomics
+ *     on the data.  The one atomic, the dQ step's tile counter, only deals out
+ *     work.
  *   - B == 0 or T == 0 is a valid empty problem: nothing is launched.
  *   - D must be 64 or 128; Hq must be a multiple of Hkv; scale must be finite
  *     and > 0; causal is 0 (full attention) or 1 (key j visible to query i iff
@@ -59,7 +62,9 @@ typedef enum {
   DETATTN_ERR_CUDA = -6,           /* a CUDA runtime / driver call failed */
   DETATTN_ERR_DEVICE_TIMEOUT = -7, /* a kernel gave up waiting on a pipeline barrier */
   DETATTN_ERR_ARCH = -8,           /* current device is not compute capability 10.3 */
-  DETATTN_ERR_WORKSPACE = -9       /* workspace NULL or too small */
+  DETATTN_ERR_WORKSPACE = -9       /* workspace NULL or too small; from detattn_check_status:
+                                      a dQ step ran on a workspace attn_bwd_delta had not
+                                      prepared */
 } detattn_status;
 
 /* Forward.  Writes o [B,T,Hq,D] (bf16) and lse [B,Hq,T] (fp32).
@@ -95,9 +100,10 @@ size_t attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
  * and attn_bwd_dq concurrently on a library-owned side stream (forked from
  * `stream` after the Delta step with an event and joined back before the call
  * returns; created on the first call per device), so all work is ordered
- * after earlier work on `stream` and later work on `stream` sees the results.  `workspace` (>= attn_bwd_workspace_bytes, 16-byte
- * aligned, caller-owned, contents on entry irrelevant) holds the row
- * statistics.  Passage: "Step 2: fused flash attention" and "Where the time
+ * after earlier work on `stream` and later work on `stream` sees the results.
+ * `workspace` (attn_bwd_workspace_bytes, at least the row statistics' share;
+ * 16-byte aligned, caller-owned, contents on entry irrelevant) holds the row
+ * statistics and the dQ step's tile counter (layout above).  Passage: "Step 2: fused flash attention" and "Where the time
  * goes now" (the flash_attention_dkv kernel) on the RustingBrain page. */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dout, void* dq, void* dk, void* dv, void* workspace,
