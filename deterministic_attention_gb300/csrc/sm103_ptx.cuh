@@ -81,14 +81,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int c0, int c1, int c2, int c3) {
   asm volatile(
@@ -136,33 +128,11 @@ __device__ __forceinline__ void tc_fence_after() {
 // same lane every time for a full, converged warp, so a commit tracks the
 // MMAs issued before it.
 //
-// D[tmem] (+)= A[smem] * B[smem]^T  (both operands described by descriptors)
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // Four MMAs under one elect.sync: D (+)= A_k * B_k for k = 0..3, the first
 // accumulating iff `accumulate` != 0 and the other three always -- one K = 64
-// product as four K = 16 steps.  Fewer instructions per MMA than four single
-// calls, which matters when the issuing warp shares its scheduler with busy
-// element-wise warps.
+// product as four K = 16 steps.  Fewer instructions per MMA than an
+// elect.sync block per MMA, which matters when the issuing warp shares its
+// scheduler with busy element-wise warps.
 __device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint64_t b0, uint64_t b1, uint64_t b2,
                                           uint64_t b3, uint32_t idesc, uint32_t accumulate) {
@@ -265,32 +235,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : DETATTN_R8(r, 0), DETATTN_R8(r, 8)
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      DETATTN_W8(r, 0), DETATTN_W8(r, 8), DETATTN_W8(r, 16), DETATTN_W8(r, 24)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
-      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
-      DETATTN_W8(r, 0), DETATTN_W8(r, 8)
-      : "memory");
-}
 
 // Split form: issue several loads, then one wait, then fence the registers
 // so the compiler cannot move a use of them above the wait.
@@ -362,26 +306,6 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// The two halves of a cluster barrier, for a wait placed long after the
-// arrival (all threads of every block of the cluster execute both).
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from
-// this block's shared memory to shared memory of a block of the cluster
-// (`dst`, `bar` from map_shared_rank); completes as transaction bytes on the
-// destination block's mbarrier `bar`.
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
-                                                  uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst),
-      "r"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
 // Asynchronous 16-byte store into shared memory of a block of the cluster
 // (`addr`, `bar` from map_shared_rank); completes as 16 transaction bytes on
 // that block's mbarrier `bar`, which also makes the data visible to it.
@@ -402,21 +326,6 @@ __device__ __forceinline__ uint32_t map_shared_rank(uint32_t saddr, uint32_t ran
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
-}
-__device__ __forceinline__ float4 ld_shared_cluster_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-// Store to shared memory of another block of the cluster (`addr` from
-// map_shared_rank).  Made visible to that block by the next cluster barrier.
-__device__ __forceinline__ void st_shared_cluster_f4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
-               "f"(v.z), "f"(v.w)
-               : "memory");
 }
 // Shared-memory load at base + OFF (a compile-time byte offset folded into
 // the instruction).  No memory clobber: callers order it after the mbarrier
@@ -454,11 +363,6 @@ __device__ __forceinline__ void st_shared_u4(uint32_t addr, uint4 v) {
 // async proxy (TMA, tcgen05.mma operands).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void st_shared_f4(uint32_t addr, float4 v) {
-  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
-               "f"(v.z), "f"(v.w)
-               : "memory");
 }
 
 // ---------------------------------------------------------------- misc
