@@ -424,15 +424,15 @@ def run_gpu_arm(args, world, rank):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def _oracle_sample(w, T_s, n_groups):
-    """fp64 inputs of a bounded sample: batch 0, KV groups 0..n_groups-1 (all
-    their query heads), the first T_s positions (a causal prefix is itself a
-    complete causal problem)."""
+def _oracle_sample(w, T_s, n_groups, n_batches=1):
+    """fp64 inputs of a bounded sample: batches 0..n_batches-1, KV groups
+    0..n_groups-1 (all their query heads), the first T_s positions (a causal
+    prefix is itself a complete causal problem)."""
     import oracle
     from deterministic_attention_gb300.inputs import bf16_bits
     q, k, v, do = workload_inputs(w)
     G = w.Hq // w.Hkv
-    sl = lambda t, hs: t[:1, :T_s, hs].contiguous()
+    sl = lambda t, hs: t[:n_batches, :T_s, hs].contiguous()
     qs = sl(q, slice(0, n_groups * G))
     ks, vs = sl(k, slice(0, n_groups)), sl(v, slice(0, n_groups))
     dos = sl(do, slice(0, n_groups * G))
@@ -448,23 +448,33 @@ def _oracle_step(w, xs):
 
 
 def cpu_baseline(w, budget_s=20.0):
-    """The oracle as it stands, on host cores, on a bounded sample."""
+    """The oracle as it stands, on host cores, on a bounded sample: whole KV
+    groups of the workload (batch 0 first, then further batches) as many as
+    about half the budget allows, run repeatedly for about half of it."""
     import oracle
     G = w.Hq // w.Hkv
     xs = _oracle_sample(w, w.T, 1)
     t0 = time.perf_counter()
     _oracle_step(w, xs)
     one = time.perf_counter() - t0
-    n_groups = max(1, min(w.Hkv, int(budget_s / max(one, 1e-3))))
-    xs = _oracle_sample(w, w.T, n_groups)
+    n_units = max(1, min(w.B * w.Hkv, int(0.5 * budget_s / max(one, 1e-3))))
+    n_batches = max(1, n_units // w.Hkv)
+    n_groups = w.Hkv if n_units >= w.Hkv else n_units
+    xs = _oracle_sample(w, w.T, n_groups, n_batches)
     t0 = time.perf_counter()
     _oracle_step(w, xs)
+    est = time.perf_counter() - t0
+    reps = max(1, int(0.5 * budget_s / max(est, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        _oracle_step(w, xs)
     dt = time.perf_counter() - t0
-    flops = 3.5 * 2.0 * n_groups * G * w.T * w.T * w.D
+    flops = reps * 3.5 * 2.0 * n_batches * n_groups * G * w.T * w.T * w.D
     return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": dt,
-            "sample": f"batch 0, KV heads 0..{n_groups - 1} with their {n_groups * G} query heads, "
-                      f"all T={w.T} positions: fwd + bwd in fp64"}
+            "sample": f"batches 0..{n_batches - 1} of {w.B}, KV heads 0..{n_groups - 1} of {w.Hkv} "
+                      f"with their {n_groups * G} query heads each, all T={w.T} positions: "
+                      f"fwd + bwd in fp64, run {reps} times"}
 
 
 def run_reference_arm(args, world, rank):
