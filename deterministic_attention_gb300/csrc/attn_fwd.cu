@@ -127,10 +127,11 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
     n_units = sched.start[pipe_id + 1] - first;
   } else {
     const int total = a.n_m * a.BHq;
-    n_units = pipe_id < total ? (total - 1 - pipe_id) / sched.n_pipes + 1 : 0;
+    n_units = qtile_snake_count(pipe_id, total, sched.n_pipes);
   }
   auto u_of = [&](int k) {
-    return sched.n_listed > 0 ? static_cast<int>(sched.unit[first + k]) : first + k * sched.n_pipes;
+    return sched.n_listed > 0 ? static_cast<int>(sched.unit[first + k])
+                              : qtile_snake_unit(pipe_id, k, sched.n_pipes);
   };
   struct Unit { int b, h, hkv, m0, n_kv; };
   auto unit_info = [&](int u) {

@@ -19,7 +19,8 @@ constexpr int dkdv_tile_m(int) { return 64; }
 // pipelines.  Unit u (in heaviest-first order) is query tile n_m - 1 - u / BHq
 // of (b, h) = u % BHq.
 // Pipeline i takes units unit[start[i]] .. unit[start[i + 1] - 1]; with
-// n_listed == 0 it takes units i, i + n_pipes, i + 2 n_pipes, ... instead.
+// n_listed == 0 it takes one unit per round of n_pipes units instead, rounds
+// dealt to the pipelines forward and backward in turn (qtile_snake_*).
 constexpr int kQTileMaxPipes = 320;
 constexpr int kQTileMaxListed = 1024;
 struct QTileSched {
@@ -28,6 +29,15 @@ struct QTileSched {
   uint16_t start[kQTileMaxPipes + 1];
   uint16_t unit[kQTileMaxListed];
 };
+// The unlisted deal: pipeline i's k-th unit, and how many it takes of `total`.
+// Alternating the direction of the rounds pairs heavy units with light ones.
+__host__ __device__ inline int qtile_snake_unit(int i, int k, int n_pipes) {
+  return k * n_pipes + ((k & 1) ? n_pipes - 1 - i : i);
+}
+__host__ __device__ inline int qtile_snake_count(int i, int total, int n_pipes) {
+  const int full = total / n_pipes, rem = total % n_pipes;
+  return full + (((full & 1) ? n_pipes - 1 - i : i) < rem ? 1 : 0);
+}
 // Pipelines per forward / dQ block: two at D = 64 (256 TMEM columns each),
 // one at D = 128.
 constexpr int qtile_pipes_per_block(int D) { return D == 64 ? 2 : 1; }
