@@ -216,25 +216,32 @@ def test_fma_pipe_exp2_error_bound():
     assert np.max(np.abs(yp[live] / ys[live] - 1.0)) <= 1e-4
 
 
-@pytest.mark.parametrize("name", ["small", "page3"])
+@pytest.mark.parametrize("name", ["small", "page3", "1152-units"])
 def test_dq_dynamic_and_static_deal_agree_bitwise(name):
     """With the full workspace the dQ step takes its query tiles from a counter
     (whichever block is ready first); with a workspace that holds only the row
-    statistics it follows the static deal.  A tile's arithmetic does not depend
-    on the block that computes it, so dq is bit-identical either way, and it
-    matches the oracle."""
+    statistics it follows the static deal (a host list up to 1,024 tiles, past
+    that rounds dealt forward and backward in turn: the 1152-unit case).  A
+    tile's arithmetic does not depend on the block that computes it, so dq is
+    bit-identical either way, and it matches the oracle."""
     import deterministic_attention_gb300 as da
     from helpers import sha256
-    w = WORKLOADS[name]
-    q, k, v, do = workload_inputs(w)
-    B, T, Hq, Hkv, D = w.shape
+    if name == "1152-units":
+        B, T, Hq, Hkv, D = 12, 1024, 12, 4, 64
+        q, k, v, do = make_inputs(B, T, Hq, Hkv, D, seed=13, dout_std=0.1)
+        scale = 1.0 / math.sqrt(D)
+    else:
+        w = WORKLOADS[name]
+        q, k, v, do = workload_inputs(w)
+        B, T, Hq, Hkv, D = w.shape
+        scale = w.softmax_scale
     tp = -(-T // 128) * 128
     qc, kc, vc, doc = (t.cuda() for t in (q, k, v, do))
-    o, lse = da.attn_fwd(qc, kc, vc, scale=w.softmax_scale)
+    o, lse = da.attn_fwd(qc, kc, vc, scale=scale)
     out = {}
     for label, nbytes in (("dynamic", da.workspace_bytes(B, T, Hq, Hkv, D)), ("static", B * Hq * tp * 8)):
         ws = torch.empty((nbytes,), dtype=torch.uint8, device="cuda")
-        res = [da.attn_bwd(qc, kc, vc, o, lse, doc, scale=w.softmax_scale, workspace=ws) for _ in range(2)]
+        res = [da.attn_bwd(qc, kc, vc, o, lse, doc, scale=scale, workspace=ws) for _ in range(2)]
         torch.cuda.synchronize()
         assert [sha256(t) for t in res[0]] == [sha256(t) for t in res[1]], label
         out[label] = res[0]
@@ -242,15 +249,15 @@ def test_dq_dynamic_and_static_deal_agree_bitwise(name):
     # workspace (each dQ call leaves the tile counter as it found it).
     ws = da.new_workspace(B, T, Hq, Hkv, D)
     da.attn_bwd_delta(o, doc, lse, ws)
-    dq_a = da.attn_bwd_dq(qc, kc, vc, doc, ws, scale=w.softmax_scale)
-    dq_b = da.attn_bwd_dq(qc, kc, vc, doc, ws, scale=w.softmax_scale)
+    dq_a = da.attn_bwd_dq(qc, kc, vc, doc, ws, scale=scale)
+    dq_b = da.attn_bwd_dq(qc, kc, vc, doc, ws, scale=scale)
     torch.cuda.synchronize()
     da.check_status()
     assert sha256(dq_a) == sha256(dq_b) == sha256(out["dynamic"][0])
     assert [sha256(t) for t in out["dynamic"]] == [sha256(t) for t in out["static"]]
     dq = out["dynamic"][0]
     rows = [(0, 0, T - 1), (B - 1, Hq - 1, T // 2), (0, Hq // 2, 0), (B - 1, 1, 129)]
-    _, _, dq_r = oracle.attn_rows(widen(q), widen(k), widen(v), widen(do), rows, w.softmax_scale, True)
+    _, _, dq_r = oracle.attn_rows(widen(q), widen(k), widen(v), widen(do), rows, scale, True)
     dq_g = np.stack([to_np(dq[b, i, h]) for b, h, i in rows])
     assert_bwd_close([("dQ", dq_g, dq_r)], f"{name} sampled rows")
 
