@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
     L.detattn_check_status.argtypes = [vp]
     L.detattn_diag_exp2.argtypes = [vp, vp, vp, vp, i, vp]
     L.detattn_diag_exp2.restype = i
+    L.detattn_diag_qtile_deal.argtypes = [i, i, i, i, i, i, vp, i]
+    L.detattn_diag_qtile_deal.restype = i
     L.detattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
     L.detattn_selftest_wait_timeout.restype = i
     L.detattn_set_dkdv_split.argtypes = [i]
@@ -221,6 +223,19 @@ def attn_bwd_dq(q, k, v, dout, workspace, scale=None, causal=True, dq=None):
 def check_status():
     """Synchronises the current stream and raises if a kernel timed out."""
     _check(lib().detattn_check_status(_stream()), "detattn_check_status")
+
+
+def diag_qtile_deal(D, B, T, Hq, causal, sms):
+    """(number of pipelines, numpy int32 pipeline of each unit) of the static
+    query-tile deal; host-only, no GPU needed."""
+    import numpy as np
+    n = B * Hq * -(-T // 128) if B > 0 and T > 0 else 0
+    out = np.empty(max(1, n), dtype=np.int32)
+    rc = lib().detattn_diag_qtile_deal(D, B, T, Hq, int(bool(causal)), sms,
+                                       ctypes.c_void_p(out.ctypes.data), n)
+    if rc < 0:
+        raise DetAttnError(rc, "detattn_diag_qtile_deal", last_error())
+    return rc, out[:n]
 
 
 def diag_exp2(x):

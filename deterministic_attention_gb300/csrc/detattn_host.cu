@@ -617,6 +617,33 @@ int detattn_check_status(void* stream) {
   return ok_status();
 }
 
+int detattn_diag_qtile_deal(int D, int B, int T, int Hq, int causal, int sms, int* pipe_of_unit,
+                            int n_units) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, 1, D, &empty)) != DETATTN_OK) return rc;
+  if (causal != 0 && causal != 1) return fail(DETATTN_ERR_SCALE, "causal must be 0 or 1");
+  if (sms < 1) return fail(DETATTN_ERR_SHAPE, "sms=%d", sms);
+  if (pipe_of_unit == nullptr) return fail(DETATTN_ERR_NULL, "pipe_of_unit is NULL");
+  const long units = empty ? 0 : static_cast<long>((T + kTileM - 1) / kTileM) * B * Hq;
+  if (n_units != units)
+    return fail(DETATTN_ERR_SHAPE, "n_units=%d, the shape has %ld units", n_units, units);
+  if (empty) return 0;
+  QTileSched sc;
+  int grid = 0;
+  qtile_schedule(D, B, T, Hq, causal, sms, &sc, &grid);
+  for (long u = 0; u < units; ++u) pipe_of_unit[u] = -1;
+  for (int i = 0; i < sc.n_pipes; ++i) {
+    if (sc.n_listed > 0) {
+      for (int k = sc.start[i]; k < sc.start[i + 1]; ++k) pipe_of_unit[sc.unit[k]] = i;
+    } else {
+      const int n = qtile_snake_count(i, static_cast<int>(units), sc.n_pipes);
+      for (int k = 0; k < n; ++k) pipe_of_unit[qtile_snake_unit(i, k, sc.n_pipes)] = i;
+    }
+  }
+  return sc.n_pipes;
+}
+
 int detattn_diag_exp2(const float* x, float* y_poly, float* y_pair, float* y_sfu, int n,
                       void* stream) {
   int rc;

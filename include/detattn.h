@@ -173,6 +173,17 @@ int detattn_check_status(void* stream);
 int detattn_diag_exp2(const float* x, float* y_poly, float* y_pair, float* y_sfu, int n,
                       void* stream);
 
+/* Diagnostic for host-side tests (no GPU needed): the static deal of
+ * 128-query tiles to persistent pipelines that the forward uses, and the dQ
+ * step without its tile counter, for a shape and an SM count.  Units are
+ * numbered heaviest first: unit u is query tile ceil(T/128) - 1 - u / (B*Hq)
+ * of (b, h) with b*Hq + h = u % (B*Hq).  Writes pipe_of_unit[u] for all
+ * n_units = B * Hq * ceil(T / 128) units (n_units must equal that) and returns
+ * the number of pipelines, 0 for an empty shape, or a negative status.  Not
+ * tied to a passage of the method. */
+int detattn_diag_qtile_deal(int D, int B, int T, int Hq, int causal, int sms, int* pipe_of_unit,
+                            int n_units);
+
 /* Failure-detection self-test.  Launches a one-thread kernel on `stream`
  * that waits, with the same bounded wait the attention kernels use, on a
  * barrier nothing ever completes; after `limit_ns` (clamped to [1 ms, 10 s])

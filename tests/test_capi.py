@@ -4,6 +4,7 @@ the documented status codes before any CUDA call (so no device is needed)."""
 import ctypes
 import math
 
+import numpy as np
 import pytest
 
 import deterministic_attention_gb300 as da
@@ -100,3 +101,41 @@ def test_python_binding_refuses_cpu_tensors(L):
     q = torch.zeros((1, 8, 2, 64), dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         da.attn_fwd(q, q[:, :, :1], q[:, :, :1])
+
+
+@pytest.mark.parametrize("D,B,T,Hq,causal,sms", [
+    (64, 4, 1024, 12, 1, 152),    # page3: the host's listed deal
+    (64, 32, 1024, 24, 1, 152),   # past the list: rounds dealt in alternating directions
+    (128, 1, 8192, 32, 1, 152),   # one pipeline per block, past the list
+    (64, 1, 512, 12, 1, 152),     # fewer units than SMs
+    (64, 2, 300, 3, 0, 8),        # full attention on few SMs
+    (128, 3, 1000, 5, 1, 132),
+])
+def test_qtile_deal(D, B, T, Hq, causal, sms):
+    """The static deal of 128-query tiles to pipelines (host logic, no GPU):
+    every unit goes to exactly one pipeline, and no pipeline's load exceeds
+    the mean by more than one unit; past the host list (1,024 units) the deal
+    is round k of the pipelines, forward in even rounds, backward in odd."""
+    n_pipes, pipe = da.diag_qtile_deal(D, B, T, Hq, causal, sms)
+    n_m = -(-T // 128)
+    units = B * Hq * n_m
+    per_block = 2 if D == 64 else 1
+    assert n_pipes == min(sms, units) * per_block
+    assert pipe.shape == (units,) and (pipe >= 0).all() and (pipe < n_pipes).all()
+    kv = -(-T // 64)
+    mt = n_m - 1 - np.arange(units) // (B * Hq)
+    n_kv = np.minimum(kv, (mt * 128 + 128) // 64) if causal else np.full(units, kv)
+    w = n_kv + 2.0
+    load = np.bincount(pipe, weights=w, minlength=n_pipes)
+    assert load.max() <= w.sum() / n_pipes + w.max()
+    if units > 1024:
+        k, i = np.divmod(np.arange(units), n_pipes)
+        assert (pipe == np.where(k % 2 == 0, i, n_pipes - 1 - i)).all()
+
+
+def test_qtile_deal_validates():
+    with pytest.raises(da.DetAttnError):
+        da.diag_qtile_deal(96, 1, 128, 2, 1, 152)  # head dim
+    with pytest.raises(da.DetAttnError):
+        da.diag_qtile_deal(64, 1, 128, 2, 1, 0)    # no SMs
+    assert da.diag_qtile_deal(64, 0, 128, 2, 1, 152)[0] == 0
