@@ -64,6 +64,9 @@ def _dist_init():
         import torch.distributed as dist
         backend = "nccl" if torch.cuda.is_available() else "gloo"
         if torch.cuda.is_available():
+            if local >= torch.cuda.device_count():
+                raise SystemExit(f"bench.py: LOCAL_RANK {local} but only "
+                                 f"{torch.cuda.device_count()} GPU(s) are visible")
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)
     elif torch.cuda.is_available():

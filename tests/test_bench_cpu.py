@@ -43,8 +43,10 @@ def test_reference_arm_two_ranks_gloo():
 
 
 def _worker(rank, world, port, out):
+    # The gloo path under test is the CPU one: hide any GPU of the host before
+    # the first CUDA query, so that each rank takes the CPU branch.
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
-                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
     sys.path.insert(0, ROOT)
     import bench
     w, r = bench._dist_init()
@@ -62,10 +64,19 @@ def test_max_over_ranks_gloo():
     mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     ctx = mp.get_context("spawn")
-    procs = [ctx.Process(target=_worker, args=(r, 2, 29541, out)) for r in range(2)]
-    for p in procs:
-        p.start()
-    for p in procs:
-        p.join(120)
-        assert p.exitcode == 0
-    assert out[0] == (2, 0, 3.0) and out[1] == (2, 1, 3.0)
+    procs = [ctx.Process(target=_worker, args=(r, 2, 29541, out), daemon=True)
+             for r in range(2)]
+    try:
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+        assert [p.exitcode for p in procs] == [0, 0]
+        assert out[0] == (2, 0, 3.0) and out[1] == (2, 1, 3.0)
+    finally:
+        # A rank left waiting for a peer that failed must not outlive the test.
+        for p in procs:
+            if p.is_alive():
+                p.kill()
+                p.join(10)
+        mgr.shutdown()
