@@ -443,6 +443,13 @@ def _oracle_sample(w, T_s, n_groups, n_batches=1):
     return tuple(f(t) for t in (qs, ks, vs, dos))
 
 
+def _oracle_cores(n_batches, n_groups):
+    """Host threads with work in the oracle's backward, which runs one
+    (batch, KV head) per thread and dominates its time."""
+    import oracle
+    return min(oracle.num_threads(), n_batches * n_groups)
+
+
 def _oracle_step(w, xs):
     import oracle
     q, k, v, do = xs
@@ -473,7 +480,8 @@ def cpu_baseline(w, budget_s=20.0):
         _oracle_step(w, xs)
     dt = time.perf_counter() - t0
     flops = reps * 3.5 * 2.0 * n_batches * n_groups * G * w.T * w.T * w.D
-    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(),
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS",
+            "cores": _oracle_cores(n_batches, n_groups),
             "kind": "oracle", "seconds": dt,
             "sample": f"batches 0..{n_batches - 1} of {w.B}, KV heads 0..{n_groups - 1} of {w.Hkv} "
                       f"with their {n_groups * G} query heads each, all T={w.T} positions: "
@@ -486,13 +494,13 @@ def run_reference_arm(args, world, rank):
     import oracle
     oracle.build()
     w = WORKLOADS[args.workload]
-    G = w.Hq // w.Hkv
-    # Size the per-step sample (a causal prefix of one KV group) so the whole
-    # run stays within a few minutes.
+    # Size the per-step sample (a causal prefix, over every batch and KV group
+    # so that every host thread has work) so the whole run stays within a few
+    # minutes.
     budget = 150.0 / max(1, args.steps + args.warmup)
     T_s = w.T
     while True:
-        xs = _oracle_sample(w, T_s, 1)
+        xs = _oracle_sample(w, T_s, w.Hkv, w.B)
         t0 = time.perf_counter()
         _oracle_step(w, xs)
         one = time.perf_counter() - t0
@@ -505,9 +513,9 @@ def run_reference_arm(args, world, rank):
     for _ in range(args.steps):
         _oracle_step(w, xs)
     dt = (time.perf_counter() - t0) / max(1, args.steps)
-    flops = 3.5 * 2.0 * G * T_s * T_s * w.D
+    flops = 3.5 * 2.0 * w.B * w.Hq * T_s * T_s * w.D
     value = flops / dt / 1e12
-    sample = (f"per step: batch 0, KV head 0 with its {G} query heads, causal prefix of "
+    sample = (f"per step: all {w.B} batches and {w.Hq} query heads, causal prefix of "
               f"T={T_s} of {w.T} positions, fwd + bwd in fp64")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
@@ -516,7 +524,7 @@ def run_reference_arm(args, world, rank):
         "data": "synthetic", "impl": "reference",
         "config": {"workload": w.name, "B": w.B, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
                    "causal": True},
-        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.num_threads(),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": _oracle_cores(w.B, w.Hkv),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},

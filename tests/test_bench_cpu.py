@@ -29,6 +29,9 @@ def test_reference_arm_single_process():
     assert d["impl"] == "reference" and d["unit"] == "TFLOPS" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["higher_is_better"] is True and d["steps"] == 2 and d["warmup"] == 3
+    # `tiny` has one (batch, KV head): the oracle's backward has work for one thread.
+    assert d["cpu_baseline"]["cores"] == 1
+    assert d["cpu_baseline"]["sample"].startswith("per step: all 1 batches and 2 query heads")
 
 
 def test_reference_arm_two_ranks_gloo():
