@@ -28,6 +28,16 @@ _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
 _lib = None
 
 
+def compile_library(src: str, out: str) -> str:
+    """Compile a C source of the oracle (``attn_oracle.c`` or a copy of it)
+    into the shared library ``out`` with the flags the oracle is built with."""
+    # -O2 without -ffast-math: the compiler keeps every sum in source order.
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-I", _HERE, src, "-o", out,
+           "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
 def build(force: bool = False) -> str:
     """Compile ``attn_oracle.c`` into ``_build/liboracle.so`` (gcc, -O2, OpenMP)."""
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
@@ -37,9 +47,7 @@ def build(force: bool = False) -> str:
     if fresh and not force:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    # -O2 without -ffast-math: the compiler keeps every sum in source order.
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
-    subprocess.run(cmd, check=True)
+    compile_library(_SRC, tmp)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -47,27 +55,33 @@ def build(force: bool = False) -> str:
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
-        dp = ctypes.POINTER(ctypes.c_double)
-        ip = ctypes.POINTER(ctypes.c_int)
-        i, d = ctypes.c_int, ctypes.c_double
-        lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, d, i]
-        lib.oracle_attn_fwd.restype = None
-        lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, d, i]
-        lib.oracle_attn_bwd.restype = d
-        lib.oracle_attn_probs.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, d, i]
-        lib.oracle_attn_probs.restype = None
-        lib.oracle_attn_rows.argtypes = [dp, dp, dp, dp, i, ip, ip, ip, dp, dp, dp,
-                                         i, i, i, i, i, d, i]
-        lib.oracle_attn_rows.restype = None
-        lib.oracle_kv_rows.argtypes = [dp, dp, dp, dp, i, i, i, ip, dp, dp, i, i, i, i, i, d, i]
-        lib.oracle_kv_rows.restype = None
-        lib.oracle_rowdot.argtypes = [dp, dp, dp, i, i, i, i]
-        lib.oracle_rowdot.restype = None
-        lib.oracle_num_threads.argtypes = []
-        lib.oracle_num_threads.restype = i
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def _bind(lib):
+    """Declare the C signatures on a loaded oracle library and return it.  The
+    tests bind copies built with planted mistakes this way, to show that the
+    pins catch them."""
+    dp = ctypes.POINTER(ctypes.c_double)
+    ip = ctypes.POINTER(ctypes.c_int)
+    i, d = ctypes.c_int, ctypes.c_double
+    lib.oracle_attn_fwd.argtypes = [dp, dp, dp, dp, dp, i, i, i, i, i, d, i]
+    lib.oracle_attn_fwd.restype = None
+    lib.oracle_attn_bwd.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, i, i, i, i, d, i]
+    lib.oracle_attn_bwd.restype = d
+    lib.oracle_attn_probs.argtypes = [dp, dp, dp, i, i, i, i, i, i, i, d, i]
+    lib.oracle_attn_probs.restype = None
+    lib.oracle_attn_rows.argtypes = [dp, dp, dp, dp, i, ip, ip, ip, dp, dp, dp,
+                                     i, i, i, i, i, d, i]
+    lib.oracle_attn_rows.restype = None
+    lib.oracle_kv_rows.argtypes = [dp, dp, dp, dp, i, i, i, ip, dp, dp, i, i, i, i, i, d, i]
+    lib.oracle_kv_rows.restype = None
+    lib.oracle_rowdot.argtypes = [dp, dp, dp, i, i, i, i]
+    lib.oracle_rowdot.restype = None
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i
+    return lib
 
 
 def _dp(a):

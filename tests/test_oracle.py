@@ -7,6 +7,7 @@ invariants (softmax rows sum to one, causality, GQA as repeated-KV MHA) and a
 library special case (PyTorch's fp64 CPU scaled_dot_product_attention with
 autograd).  Each test names the kind of mistake it is there to catch.
 """
+import ctypes
 import math
 
 import numpy as np
@@ -249,17 +250,19 @@ def test_sampled_rows_match_full_oracle():
     for causal in (True, False):
         o, lse = oracle.attn_fwd(q, k, v, 0.3, causal)
         dq, dk, dv, _, _ = oracle.attn_bwd(q, k, v, do, 0.3, causal)
-        rows = [(0, 0, 0), (1, 5, 39), (0, 3, 17), (1, 2, 1)]
+        # Heads 1 and 4 are where the group mapping h // G differs from h % Hkv.
+        rows = [(0, 0, 0), (1, 5, 39), (0, 3, 17), (1, 2, 1), (0, 1, 22), (1, 4, 30)]
         o_r, lse_r, dq_r = oracle.attn_rows(q, k, v, do, rows, 0.3, causal)
         for s, (b, h, i) in enumerate(rows):
             assert np.array_equal(o_r[s], o[b, i, h])
             assert lse_r[s] == lse[b, h, i]
             np.testing.assert_allclose(dq_r[s], dq[b, i, h], rtol=1e-12, atol=1e-15)
         js = [0, 7, 39]
-        dk_r, dv_r = oracle.kv_rows(q, k, v, do, 1, 1, js, 0.3, causal)
-        for s, j in enumerate(js):
-            np.testing.assert_allclose(dk_r[s], dk[1, j, 1], rtol=1e-12, atol=1e-15)
-            np.testing.assert_allclose(dv_r[s], dv[1, j, 1], rtol=1e-12, atol=1e-15)
+        for b, g in ((1, 1), (0, 0)):
+            dk_r, dv_r = oracle.kv_rows(q, k, v, do, b, g, js, 0.3, causal)
+            for s, j in enumerate(js):
+                np.testing.assert_allclose(dk_r[s], dk[b, j, g], rtol=1e-12, atol=1e-15)
+                np.testing.assert_allclose(dv_r[s], dv[b, j, g], rtol=1e-12, atol=1e-15)
 
 
 def test_oracle_is_deterministic():
@@ -270,9 +273,126 @@ def test_oracle_is_deterministic():
         assert x.tobytes() == y.tobytes()
 
 
+def test_oracle_reproduces_its_fixture():
+    """The stored outputs of tests/golden/make_oracle_fixture.py (written by
+    the oracle alone) are reproduced; tolerance for libm differences between
+    hosts only."""
+    import importlib.util
+    import os
+    golden = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+    spec = importlib.util.spec_from_file_location(
+        "make_oracle_fixture", os.path.join(golden, "make_oracle_fixture.py"))
+    fx = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(fx)
+    stored = {}
+    with open(os.path.join(golden, fx.NAME)) as f:
+        for line in f:
+            if line.startswith("#"):
+                continue
+            causal, name, *vals = line.split()
+            stored[(int(causal.split("=")[1]), name)] = np.array([float(x) for x in vals])
+    assert len(stored) == 10
+    for causal in (1, 0):
+        for name, x in fx.outputs(bool(causal)).items():
+            ref = stored[(causal, name)]
+            assert ref.size == x.size, (causal, name)
+            np.testing.assert_allclose(x.reshape(-1), ref, rtol=1e-13, atol=1e-15,
+                                       err_msg=f"causal={causal} {name}")
+
+
 def test_bf16_widening_is_exact():
     vals = torch.tensor([0.0, -0.0, 1.0, -2.5, 3.140625, 1e-30, 65280.0, float("inf")],
                         dtype=torch.bfloat16)
     bits = vals.view(torch.int16).numpy().view(np.uint16)
     got = oracle.bf16_bits_to_f64(bits)
     np.testing.assert_array_equal(got, vals.to(torch.float64).numpy())
+
+
+# ------------------------------------------------------------ the pins catch planted mistakes
+# Each entry plants one plausible mistake in a copy of the oracle's C source:
+# (name, text in the source, its replacement, how often the text occurs).  A
+# wrong sign, a dropped term or scale, a transposed operand, an off-by-one in
+# the mask or a wrong head index anywhere in the forward, the backward, the
+# row-sampling helpers or the standalone row dot must make at least one pin
+# above fail.  The text must occur exactly as often as stated, so an edit of
+# the oracle that moves a pattern fails here rather than testing nothing.
+_MUTANTS = [
+    ("mask_admits_next_key", "return causal ? i + 1 : T;",
+     "return causal ? (i + 2 < T ? i + 2 : T) : T;", 1),
+    ("causal_flag_ignored", "return causal ? i + 1 : T;", "return i + 1;", 1),
+    ("score_scale_dropped", "const double s = scale * dot(qi, k + row_off(b, j, g, T, Hkv, D), D);",
+     "const double s = dot(qi, k + row_off(b, j, g, T, Hkv, D), D);", 1),
+    ("lse_without_row_max", "const double l = m + log(sum);", "const double l = log(sum);", 1),
+    ("probs_from_max_not_lse", "p[j] = exp(p[j] - l);", "p[j] = exp(p[j] - m);", 1),
+    ("scores_head_interleaved", "const int g = h / (Hq / Hkv);", "const int g = h % Hkv;", 1),
+    ("fwd_values_head_interleaved", "weighted_values(p, v, b, h / G,",
+     "weighted_values(p, v, b, h % Hkv,", 1),
+    ("lse_in_base_2", "lse[((size_t)b * Hq + h) * T + i] = l;",
+     "lse[((size_t)b * Hq + h) * T + i] = l * 1.4426950408889634;", 1),
+    ("ds_sign_flipped", "const double ds = p[j] * (dp[j] - d1);",
+     "const double ds = p[j] * (d1 - dp[j]);", 1),
+    ("ds_delta_dropped", "const double ds = p[j] * (dp[j] - d1);", "const double ds = p[j] * dp[j];", 1),
+    ("dk_from_do_not_q", "dkj[d] += ds * qi[d];", "dkj[d] += ds * doi[d];", 2),
+    ("dv_weighted_by_ds", "dvj[d] += p[j] * doi[d];", "dvj[d] += ds * doi[d];", 1),
+    ("dq_scale_dropped", "for (int d = 0; d < D; ++d) dqi[d] *= scale;", "", 2),
+    ("dk_scale_dropped", "for (int d = 0; d < D; ++d) dkj[d] *= scale;", "", 2),
+    ("dp_reads_kv_head_0", "dp[j] = dot(doi, v + row_off(b, j, g, T, Hkv, D), D);",
+     "dp[j] = dot(doi, v + row_off(b, j, 0, T, Hkv, D), D);", 1),
+    ("group_sum_first_head_only", "for (int h = g * G; h < (g + 1) * G; ++h)",
+     "for (int h = g * G; h < g * G + 1; ++h)", 1),
+    ("delta_from_do_do", "const double d1 = dot(doi, oi, D);", "const double d1 = dot(doi, doi, D);", 2),
+    ("dq_weighted_by_p", "dqi[d] += ds * kj[d];", "dqi[d] += p[j] * kj[d];", 2),
+    ("rowdot_do_squared",
+     "dot(dout + row_off(b, i, h, T, H, D), o + row_off(b, i, h, T, H, D), D)",
+     "dot(dout + row_off(b, i, h, T, H, D), dout + row_off(b, i, h, T, H, D), D)", 1),
+    ("kv_rows_unscaled_score", "exp(scale * dot(qi, kj, D) - lse[(size_t)hh * T + i])",
+     "exp(dot(qi, kj, D) - lse[(size_t)hh * T + i])", 1),
+    ("kv_rows_range_starts_late", "for (int i = causal ? j : 0; i < T; ++i)",
+     "for (int i = causal ? j + 1 : 0; i < T; ++i)", 1),
+    ("rows_head_interleaved", "i = ri[s], g = h / G;", "i = ri[s], g = h % Hkv;", 1),
+]
+
+_SDPA_CASES = [(shape, causal) for shape in [(2, 37, 6, 2, 16), (1, 64, 4, 4, 32), (1, 1, 2, 1, 8)]
+               for causal in (True, False)]
+_PINS = [
+    ("hand_derived", test_hand_derived_two_tokens, ()),
+    ("uniform", test_uniform_attention_when_q_is_zero, ()),
+    ("single_token", test_single_token, ()),
+    ("constant_v", test_constant_v_rows, ()),
+    ("softmax_causal", test_softmax_rows_sum_to_one_and_mask, (True,)),
+    ("softmax_full", test_softmax_rows_sum_to_one_and_mask, (False,)),
+    ("causality", test_causality_is_exact, ()),
+    ("gqa2", test_gqa_is_repeated_kv_mha, (2,)),
+    ("gqa3", test_gqa_is_repeated_kv_mha, (3,)),
+    ("rowdot", test_rowdot_is_the_backward_delta, ()),
+    ("delta_forms", test_delta_forms_agree, ()),
+    ("fd_causal", test_finite_differences, (True,)),
+    ("fd_full", test_finite_differences, (False,)),
+    ("sdpa", lambda: [test_matches_torch_sdpa_fp64(s, c) for s, c in _SDPA_CASES], ()),
+    ("sampled_rows", test_sampled_rows_match_full_oracle, ()),
+]
+
+
+@pytest.mark.parametrize("name,old,new,count",
+                         [pytest.param(*m, id=m[0])
+                          for m in [("unchanged", None, None, 0)] + _MUTANTS])
+def test_pins_catch_planted_mistakes(name, old, new, count, tmp_path, monkeypatch):
+    with open(oracle._SRC) as f:
+        src = f.read()
+    if old is not None:
+        assert src.count(old) == count, name
+        src = src.replace(old, new)
+    c_path = tmp_path / f"{name}.c"
+    c_path.write_text(src)
+    lib = oracle._bind(ctypes.CDLL(oracle.compile_library(str(c_path), str(tmp_path / f"{name}.so"))))
+    monkeypatch.setattr(oracle, "_lib", lib)
+    caught = []
+    for pin, fn, args in _PINS:
+        try:
+            fn(*args)
+        except AssertionError:
+            caught.append(pin)
+    if old is None:
+        assert caught == [], f"the unchanged source, rebuilt, fails {caught}"
+    else:
+        assert caught, f"no pin catches the planted mistake {name}"
