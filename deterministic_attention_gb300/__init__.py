@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
     L.detattn_diag_exp2.restype = i
     L.detattn_diag_qtile_deal.argtypes = [i, i, i, i, i, i, vp, i]
     L.detattn_diag_qtile_deal.restype = i
+    L.detattn_diag_dkdv_split.argtypes = [i, i, i, i, i, i, vp, i, vp, vp]
+    L.detattn_diag_dkdv_split.restype = i
     L.detattn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
     L.detattn_selftest_wait_timeout.restype = i
     L.detattn_set_dkdv_split.argtypes = [i]
@@ -236,6 +238,21 @@ def diag_qtile_deal(D, B, T, Hq, causal, sms):
     if rc < 0:
         raise DetAttnError(rc, "detattn_diag_qtile_deal", last_error())
     return rc, out[:n]
+
+
+def diag_dkdv_split(B, T, Hq, Hkv, D, causal, resident, blocks_per_key_tile=0):
+    """(C, NG) the dK/dV step would choose on a device holding resident[i]
+    clusters of 2**i blocks (i = 0..3); host-only, no GPU needed."""
+    import numpy as np
+    res = np.zeros(4, dtype=np.int32)
+    res[:len(resident)] = resident
+    c, ng = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().detattn_diag_dkdv_split(B, T, Hq, Hkv, D, int(bool(causal)),
+                                       ctypes.c_void_p(res.ctypes.data), blocks_per_key_tile,
+                                       ctypes.byref(c), ctypes.byref(ng))
+    if rc < 0:
+        raise DetAttnError(rc, "detattn_diag_dkdv_split", last_error())
+    return c.value, ng.value
 
 
 def diag_exp2(x):

@@ -284,8 +284,10 @@ int sm_count(int* out) {
 // at once (at most one per tile).  Both depend only on the shape and the
 // device, so the summation order, and with it every output bit, is fixed for
 // a given problem and GPU.  `forced_c` > 0 takes that C (capped at the limit).
-int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int forced_c,
-                  int* c_out, int* ng_out) {
+// `resident[i]`: clusters of 2^i blocks the device holds at once (0: none).
+// Returns false when no allowed C can be resident.
+bool dkdv_choose(int B, int T, int Hq, int Hkv, int D, int causal, const int resident[4],
+                 int forced_c, int* c_out, int* ng_out) {
   const int G = Hq / Hkv;
   const int n_tiles = (T + kTileN - 1) / kTileN;
   const int BH = B * Hkv;
@@ -296,18 +298,10 @@ int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int
   double best = 0.0;
   *c_out = 0;
   *ng_out = 0;
-  for (int c = 1; c <= cmax; c *= 2) {
+  for (int c = 1, i = 0; c <= cmax && i < 4; c *= 2, ++i) {
     if (forced_c > 0 && c != (forced_c < cmax ? forced_c : cmax)) continue;
-    int resident = sms;
-    if (c > 1) {
-      cudaError_t e = dkdv_max_clusters(D, c, &resident);
-      if (e != cudaSuccess) {
-        return fail(DETATTN_ERR_CUDA, "attn_bwd_dkdv: cluster occupancy query: %s",
-                    cudaGetErrorString(e));
-      }
-    }
-    if (resident < 1) continue;
-    const long ng = total < resident ? total : resident;
+    if (resident[i] < 1) continue;
+    const long ng = total < resident[i] ? total : resident[i];
     double worst = 0.0;
     for (long k = 0; k < ng; ++k) {
       double load = 0.0;
@@ -330,7 +324,24 @@ int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int
       *ng_out = static_cast<int>(ng);
     }
   }
-  if (*c_out == 0) {
+  return *c_out != 0;
+}
+
+// dkdv_choose with the current device's residency: `sms` blocks alone, and
+// the cluster sizes it supports from the occupancy query.
+int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int forced_c,
+                  int* c_out, int* ng_out) {
+  const int cmax = dkdv_max_cluster_size(D);
+  int resident[4] = {sms, 0, 0, 0};
+  for (int c = 2, i = 1; c <= cmax && i < 4; c *= 2, ++i) {
+    if (forced_c > 0 && c != (forced_c < cmax ? forced_c : cmax)) continue;
+    cudaError_t e = dkdv_max_clusters(D, c, &resident[i]);
+    if (e != cudaSuccess) {
+      return fail(DETATTN_ERR_CUDA, "attn_bwd_dkdv: cluster occupancy query: %s",
+                  cudaGetErrorString(e));
+    }
+  }
+  if (!dkdv_choose(B, T, Hq, Hkv, D, causal, resident, forced_c, c_out, ng_out)) {
     return fail(DETATTN_ERR_CUDA, "attn_bwd_dkdv: no resident cluster shape for D = %d", D);
   }
   return DETATTN_OK;
@@ -642,6 +653,27 @@ int detattn_diag_qtile_deal(int D, int B, int T, int Hq, int causal, int sms, in
     }
   }
   return sc.n_pipes;
+}
+
+int detattn_diag_dkdv_split(int B, int T, int Hq, int Hkv, int D, int causal,
+                            const int* resident, int blocks_per_key_tile, int* c_out,
+                            int* ng_out) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, Hkv, D, &empty)) != DETATTN_OK) return rc;
+  if (causal != 0 && causal != 1) return fail(DETATTN_ERR_SHAPE, "causal=%d must be 0 or 1", causal);
+  if (resident == nullptr || c_out == nullptr || ng_out == nullptr)
+    return fail(DETATTN_ERR_NULL, "resident, c_out and ng_out must not be NULL");
+  if (blocks_per_key_tile != 0 && blocks_per_key_tile != 1 && blocks_per_key_tile != 2 &&
+      blocks_per_key_tile != 4 && blocks_per_key_tile != 8)
+    return fail(DETATTN_ERR_SHAPE, "dK/dV split %d: must be 0 (automatic), 1, 2, 4 or 8",
+                blocks_per_key_tile);
+  *c_out = 0;
+  *ng_out = 0;
+  if (empty) return ok_status();
+  if (!dkdv_choose(B, T, Hq, Hkv, D, causal, resident, blocks_per_key_tile, c_out, ng_out))
+    return fail(DETATTN_ERR_SHAPE, "no cluster size with resident clusters for D = %d", D);
+  return ok_status();
 }
 
 int detattn_diag_exp2(const float* x, float* y_poly, float* y_pair, float* y_sfu, int n,

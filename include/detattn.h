@@ -184,6 +184,22 @@ int detattn_diag_exp2(const float* x, float* y_poly, float* y_pair, float* y_sfu
 int detattn_diag_qtile_deal(int D, int B, int T, int Hq, int causal, int sms, int* pipe_of_unit,
                             int n_units);
 
+/* Diagnostic for host-side tests (no GPU needed): the dK/dV step's choice of
+ * C, the blocks that share one 128-key tile, and NG, the resident clusters of
+ * C blocks that walk the key tiles, for a shape and a device described by
+ * resident[0..3]: how many clusters of 1, 2, 4 and 8 blocks it holds at once
+ * (0 where that size cannot be resident; sizes above the kernel's limit for
+ * D are not considered).  blocks_per_key_tile: 0 for the automatic choice,
+ * else the C to take (as detattn_set_dkdv_split).  Writes *c_out and *ng_out
+ * (both 0 for an empty shape).  Returns DETATTN_OK, DETATTN_ERR_SHAPE /
+ * DETATTN_ERR_HEADDIM for a bad shape, split or a device with no usable size,
+ * DETATTN_ERR_NULL for a NULL pointer.  The attention calls make the same
+ * choice from the current device's occupancy.  Not tied to a passage of the
+ * method. */
+int detattn_diag_dkdv_split(int B, int T, int Hq, int Hkv, int D, int causal,
+                            const int* resident, int blocks_per_key_tile, int* c_out,
+                            int* ng_out);
+
 /* Failure-detection self-test.  Launches a one-thread kernel on `stream`
  * that waits, with the same bounded wait the attention kernels use, on a
  * barrier nothing ever completes; after `limit_ns` (clamped to [1 ms, 10 s])

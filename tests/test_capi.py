@@ -139,3 +139,53 @@ def test_qtile_deal_validates():
     with pytest.raises(da.DetAttnError):
         da.diag_qtile_deal(64, 1, 128, 2, 1, 0)    # no SMs
     assert da.diag_qtile_deal(64, 0, 128, 2, 1, 152)[0] == 0
+
+
+# A GB300-like device for the split model: 152 SMs, one dK/dV block per SM,
+# clusters placed without loss (152 / C of them).  Nominal, not queried.
+_RESIDENT = [152, 76, 38, 19]
+
+
+def test_dkdv_split_picks_the_measured_best():
+    """The cost model's automatic C at the three D = 64 shapes whose C was
+    measured on a GB300 at every value (fastest: C = 4 at 1x512x12/4,
+    C = 2 at 4x1024x12/4, C = 1 at 32x1024x24/24), and NG = min(key tiles,
+    resident clusters of that C)."""
+    assert da.diag_dkdv_split(1, 512, 12, 4, 64, True, _RESIDENT) == (4, 16)
+    assert da.diag_dkdv_split(4, 1024, 12, 4, 64, True, _RESIDENT) == (2, 76)
+    assert da.diag_dkdv_split(32, 1024, 24, 24, 64, True, _RESIDENT) == (1, 152)
+
+
+@pytest.mark.parametrize("shape", [(1, 128, 2, 1, 64), (4, 1024, 12, 4, 64),
+                                   (1, 8192, 32, 8, 128), (3, 777, 6, 2, 128)])
+def test_dkdv_split_invariants(shape):
+    B, T, Hq, Hkv, D = shape
+    tiles = B * Hkv * -(-T // 128)
+    limit = 8 if D == 64 else 2
+    c, ng = da.diag_dkdv_split(*shape, True, _RESIDENT)
+    assert c in (1, 2, 4, 8) and c <= limit
+    assert ng == min(tiles, _RESIDENT[c.bit_length() - 1])
+    for forced in (1, 2, 4, 8):
+        fc, fng = da.diag_dkdv_split(*shape, True, _RESIDENT, forced)
+        assert fc == min(forced, limit)
+        assert fng == min(tiles, _RESIDENT[fc.bit_length() - 1])
+    # A cluster size the device cannot hold is never chosen.
+    res = list(_RESIDENT)
+    res[c.bit_length() - 1] = 0
+    if any(res[: limit.bit_length()]):
+        assert da.diag_dkdv_split(*shape, True, res)[0] != c
+
+
+def test_dkdv_split_validates():
+    assert da.diag_dkdv_split(0, 128, 2, 1, 64, True, _RESIDENT) == (0, 0)
+    with pytest.raises(da.DetAttnError):
+        da.diag_dkdv_split(1, 128, 2, 1, 64, True, [0, 0, 0, 0])  # nothing resident
+    with pytest.raises(da.DetAttnError):
+        da.diag_dkdv_split(1, 128, 2, 1, 64, True, _RESIDENT, 3)  # not a power of two
+    with pytest.raises(da.DetAttnError):
+        da.diag_dkdv_split(1, 128, 3, 2, 64, True, _RESIDENT)     # Hq % Hkv
+    # D = 64 allows clusters of 8; at D = 128 a forced 8 acts as 2, which this
+    # device cannot hold.
+    assert da.diag_dkdv_split(1, 128, 2, 1, 64, True, [0, 0, 0, 5], 8) == (8, 1)
+    with pytest.raises(da.DetAttnError):
+        da.diag_dkdv_split(1, 128, 2, 1, 128, True, [152, 0, 0, 5], 8)
