@@ -53,6 +53,13 @@ int check_shape(int B, int T, int Hq, int Hkv, int D, bool* empty) {
   return DETATTN_OK;
 }
 
+// Blocks per dK/dV key tile: 0 (automatic) or a power of two up to 8.
+int check_split(int c) {
+  if (c != 0 && c != 1 && c != 2 && c != 4 && c != 8)
+    return fail(DETATTN_ERR_SHAPE, "dK/dV split %d: must be 0 (automatic), 1, 2, 4 or 8", c);
+  return DETATTN_OK;
+}
+
 int check_scale(float scale, int causal) {
   if (!std::isfinite(scale) || !(scale > 0.f))
     return fail(DETATTN_ERR_SCALE, "scale=%g must be finite and > 0", static_cast<double>(scale));
@@ -664,10 +671,7 @@ int detattn_diag_dkdv_split(int B, int T, int Hq, int Hkv, int D, int causal,
   if (causal != 0 && causal != 1) return fail(DETATTN_ERR_SHAPE, "causal=%d must be 0 or 1", causal);
   if (resident == nullptr || c_out == nullptr || ng_out == nullptr)
     return fail(DETATTN_ERR_NULL, "resident, c_out and ng_out must not be NULL");
-  if (blocks_per_key_tile != 0 && blocks_per_key_tile != 1 && blocks_per_key_tile != 2 &&
-      blocks_per_key_tile != 4 && blocks_per_key_tile != 8)
-    return fail(DETATTN_ERR_SHAPE, "dK/dV split %d: must be 0 (automatic), 1, 2, 4 or 8",
-                blocks_per_key_tile);
+  if ((rc = check_split(blocks_per_key_tile)) != DETATTN_OK) return rc;
   *c_out = 0;
   *ng_out = 0;
   if (empty) return ok_status();
@@ -699,10 +703,8 @@ int detattn_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
 }
 
 int detattn_set_dkdv_split(int blocks_per_key_tile) {
-  if (blocks_per_key_tile != 0 && blocks_per_key_tile != 1 && blocks_per_key_tile != 2 &&
-      blocks_per_key_tile != 4 && blocks_per_key_tile != 8)
-    return fail(DETATTN_ERR_SHAPE, "dK/dV split %d: must be 0 (automatic), 1, 2, 4 or 8",
-                blocks_per_key_tile);
+  int rc;
+  if ((rc = check_split(blocks_per_key_tile)) != DETATTN_OK) return rc;
   g_dkdv_split = blocks_per_key_tile;
   return ok_status();
 }
