@@ -4,6 +4,11 @@ TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
 the CPU-baseline leg of ``bench.py`` may import this package.  The attention
 library never imports, links or runs it, and the two share no code.
 
+Besides fixed-length batches [B, T, H, D] it covers packed variable-length
+batches with Tq != Tk (``attn_fwd_varlen``, ``attn_bwd_varlen``), which no page
+describes; the readings (bottom-right causal alignment, rows that see no key)
+are stated in ``attn_oracle.h``.
+
 The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over
 independent heads); this module compiles it with gcc, loads it with ctypes and
 marshals numpy arrays.  The only thing done here besides marshalling is the
@@ -79,6 +84,10 @@ def _bind(lib):
     lib.oracle_kv_rows.restype = None
     lib.oracle_rowdot.argtypes = [dp, dp, dp, i, i, i, i]
     lib.oracle_rowdot.restype = None
+    lib.oracle_attn_fwd_varlen.argtypes = [dp, dp, dp, dp, dp, i, ip, ip, i, i, i, d, i]
+    lib.oracle_attn_fwd_varlen.restype = None
+    lib.oracle_attn_bwd_varlen.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, ip, ip, i, i, i, d, i]
+    lib.oracle_attn_bwd_varlen.restype = d
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
     return lib
@@ -184,3 +193,49 @@ def kv_rows(q, k, v, dout, b: int, g: int, js, scale: float, causal: bool = True
     _load().oracle_kv_rows(_dp(q), _dp(k), _dp(v), _dp(dout), int(b), int(g), j.size, _ip(j),
                            _dp(dk), _dp(dv), B, T, Hq, Hkv, D, float(scale), int(bool(causal)))
     return dk, dv
+
+
+def _cu(cu, total, what):
+    c = np.ascontiguousarray(np.asarray(cu, dtype=np.int64).reshape(-1))
+    if c.size < 1 or c[0] != 0 or np.any(np.diff(c) < 0) or c[-1] != total:
+        raise ValueError(f"{what} must start at 0, not decrease and end at {total}: {c.tolist()}")
+    return np.ascontiguousarray(c.astype(np.int32))
+
+
+def _varlen_shape(q, k, cu_q, cu_k):
+    Nq, Hq, D = q.shape
+    Nk, Hkv, Dk = k.shape
+    if D != Dk or Hkv < 1 or Hq % Hkv:
+        raise ValueError(f"incompatible q {q.shape} / k {k.shape}")
+    cq, ck = _cu(cu_q, Nq, "cu_q"), _cu(cu_k, Nk, "cu_k")
+    if cq.size != ck.size:
+        raise ValueError("cu_q and cu_k must describe the same number of sequences")
+    return cq, ck, cq.size - 1, Hq, Hkv, D
+
+
+def attn_fwd_varlen(q, k, v, cu_q, cu_k, scale: float, causal: bool = True):
+    """Packed variable-length forward: q [total_q, Hq, D], k, v [total_k, Hkv,
+    D], sequence s in rows cu_q[s]..cu_q[s+1]-1 and cu_k[s]..cu_k[s+1]-1.
+    Returns O [total_q, Hq, D] and LSE [Hq, total_q]."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    cq, ck, n_seq, Hq, Hkv, D = _varlen_shape(q, k, cu_q, cu_k)
+    o = np.empty_like(q)
+    lse = np.empty((Hq, q.shape[0]), dtype=np.float64)
+    _load().oracle_attn_fwd_varlen(_dp(q), _dp(k), _dp(v), _dp(o), _dp(lse), n_seq, _ip(cq),
+                                   _ip(ck), Hq, Hkv, D, float(scale), int(bool(causal)))
+    return o, lse
+
+
+def attn_bwd_varlen(q, k, v, dout, cu_q, cu_k, scale: float, causal: bool = True):
+    """dQ, dK, dV, Delta [Hq, total_q] and the worst disagreement between the
+    two forms of Delta, for a packed variable-length batch."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    cq, ck, n_seq, Hq, Hkv, D = _varlen_shape(q, k, cu_q, cu_k)
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    delta = np.empty((Hq, q.shape[0]), dtype=np.float64)
+    worst = _load().oracle_attn_bwd_varlen(_dp(q), _dp(k), _dp(v), _dp(dout), _dp(dq), _dp(dk),
+                                           _dp(dv), _dp(delta), n_seq, _ip(cq), _ip(ck), Hq, Hkv,
+                                           D, float(scale), int(bool(causal)))
+    return dq, dk, dv, delta, worst

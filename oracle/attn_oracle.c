@@ -253,3 +253,152 @@ void oracle_kv_rows(const double* q, const double* k, const double* v, const dou
   free(lse);
   free(del);
 }
+
+/* ------------------------------------------------------------------------
+ * Packed variable-length batches, Tq != Tk allowed (see attn_oracle.h).
+ * Sequence s owns query rows cu_q[s] .. cu_q[s+1]-1 and key rows
+ * cu_k[s] .. cu_k[s+1]-1; nothing crosses a sequence boundary.  The loops
+ * follow the fixed-length functions above in the same order, so a batch of
+ * equal-length sequences gives the same bytes as those functions.
+ * ------------------------------------------------------------------------ */
+
+/* Keys 0 .. n-1 of its sequence that query i sees: all tk, or under the
+ * causal mask those with j <= i + (tk - tq) (the mask's diagonal ends in the
+ * bottom-right corner of the tq x tk score matrix), clamped to [0, tk]. */
+static int seq_visible(int i, int tq, int tk, int causal) {
+  if (!causal) return tk;
+  const int n = i + 1 + (tk - tq);
+  return n < 0 ? 0 : (n > tk ? tk : n);
+}
+
+static size_t packed_off(int row, int h, int H, int D) { return ((size_t)row * H + h) * (size_t)D; }
+
+/* Softmax row of packed query row `qrow` (head h) against the n keys from
+ * packed key row `k0` (KV head g): prob[j] for j < n, *lse_out.  n == 0 gives
+ * *lse_out = -inf and no probabilities. */
+static void seq_softmax_row(const double* q, const double* k, int qrow, int k0, int n, int h,
+                            int g, int Hq, int Hkv, int D, double scale, double* prob,
+                            double* lse_out) {
+  if (n == 0) {
+    *lse_out = -INFINITY;
+    return;
+  }
+  const double* qr = q + packed_off(qrow, h, Hq, D);
+  double mx = -INFINITY;
+  for (int j = 0; j < n; ++j) {
+    prob[j] = scale * dot(qr, k + packed_off(k0 + j, g, Hkv, D), D);
+    if (prob[j] > mx) mx = prob[j];
+  }
+  double tot = 0.0;
+  for (int j = 0; j < n; ++j) tot += exp(prob[j] - mx);
+  const double lrow = mx + log(tot);
+  for (int j = 0; j < n; ++j) prob[j] = exp(prob[j] - lrow);
+  *lse_out = lrow;
+}
+
+/* orow = sum_{j < n} prob[j] V[k0 + j, g, :]; zero when n == 0. */
+static void seq_weighted_values(const double* prob, const double* v, int k0, int n, int g, int Hkv,
+                                int D, double* orow) {
+  for (int d = 0; d < D; ++d) orow[d] = 0.0;
+  for (int j = 0; j < n; ++j) {
+    const double* vr = v + packed_off(k0 + j, g, Hkv, D);
+    for (int d = 0; d < D; ++d) orow[d] += prob[j] * vr[d];
+  }
+}
+
+static int max_len(int n_seq, const int* cu) {
+  int m = 1;
+  for (int s = 0; s < n_seq; ++s)
+    if (cu[s + 1] - cu[s] > m) m = cu[s + 1] - cu[s];
+  return m;
+}
+
+void oracle_attn_fwd_varlen(const double* q, const double* k, const double* v, double* o,
+                            double* lse, int n_seq, const int* cu_q, const int* cu_k, int Hq,
+                            int Hkv, int D, double scale, int causal) {
+  const int G = Hq / Hkv;
+  const int total_q = cu_q[n_seq];
+  const int tk_max = max_len(n_seq, cu_k);
+#pragma omp parallel
+  {
+    double* prob = (double*)malloc(sizeof(double) * (size_t)tk_max);
+#pragma omp for collapse(2) schedule(dynamic)
+    for (int s = 0; s < n_seq; ++s)
+      for (int h = 0; h < Hq; ++h) {
+        const int tq = cu_q[s + 1] - cu_q[s], tk = cu_k[s + 1] - cu_k[s];
+        for (int i = 0; i < tq; ++i) {
+          const int row = cu_q[s] + i, n = seq_visible(i, tq, tk, causal);
+          seq_softmax_row(q, k, row, cu_k[s], n, h, h / G, Hq, Hkv, D, scale, prob,
+                          &lse[(size_t)h * total_q + row]);
+          seq_weighted_values(prob, v, cu_k[s], n, h / G, Hkv, D, o + packed_off(row, h, Hq, D));
+        }
+      }
+    free(prob);
+  }
+}
+
+double oracle_attn_bwd_varlen(const double* q, const double* k, const double* v,
+                              const double* dout, double* dq, double* dk, double* dv,
+                              double* delta, int n_seq, const int* cu_q, const int* cu_k, int Hq,
+                              int Hkv, int D, double scale, int causal) {
+  const int G = Hq / Hkv;
+  const int total_q = cu_q[n_seq];
+  const int tk_max = max_len(n_seq, cu_k);
+  double worst = 0.0;
+#pragma omp parallel reduction(max : worst)
+  {
+    double* prob = (double*)malloc(sizeof(double) * (size_t)tk_max);
+    double* dprob = (double*)malloc(sizeof(double) * (size_t)tk_max);
+    double* orow = (double*)malloc(sizeof(double) * (size_t)D);
+#pragma omp for collapse(2) schedule(dynamic)
+    for (int s = 0; s < n_seq; ++s)
+      for (int g = 0; g < Hkv; ++g) {
+        /* This thread owns dK, dV of (s, g) and dQ of the group's query rows. */
+        const int tq = cu_q[s + 1] - cu_q[s], tk = cu_k[s + 1] - cu_k[s], k0 = cu_k[s];
+        for (int j = 0; j < tk; ++j) {
+          memset(dk + packed_off(k0 + j, g, Hkv, D), 0, sizeof(double) * (size_t)D);
+          memset(dv + packed_off(k0 + j, g, Hkv, D), 0, sizeof(double) * (size_t)D);
+        }
+        for (int h = g * G; h < g * G + G; ++h)
+          for (int i = 0; i < tq; ++i) {
+            const int row = cu_q[s] + i, n = seq_visible(i, tq, tk, causal);
+            const double* qr = q + packed_off(row, h, Hq, D);
+            const double* dor = dout + packed_off(row, h, Hq, D);
+            double* dqr = dq + packed_off(row, h, Hq, D);
+            double lrow;
+            seq_softmax_row(q, k, row, k0, n, h, g, Hq, Hkv, D, scale, prob, &lrow);
+            seq_weighted_values(prob, v, k0, n, g, Hkv, D, orow);
+            const double dl = dot(dor, orow, D);
+            double dl2 = 0.0;
+            for (int j = 0; j < n; ++j) {
+              dprob[j] = dot(dor, v + packed_off(k0 + j, g, Hkv, D), D);
+              dl2 += prob[j] * dprob[j];
+            }
+            const double gap = fabs(dl - dl2) / fmax(1.0, fabs(dl));
+            if (gap > worst) worst = gap;
+            delta[(size_t)h * total_q + row] = dl;
+            for (int d = 0; d < D; ++d) dqr[d] = 0.0;
+            for (int j = 0; j < n; ++j) {
+              const double dsc = prob[j] * (dprob[j] - dl);
+              const double* kr = k + packed_off(k0 + j, g, Hkv, D);
+              double* dkr = dk + packed_off(k0 + j, g, Hkv, D);
+              double* dvr = dv + packed_off(k0 + j, g, Hkv, D);
+              for (int d = 0; d < D; ++d) {
+                dqr[d] += dsc * kr[d];
+                dkr[d] += dsc * qr[d];
+                dvr[d] += prob[j] * dor[d];
+              }
+            }
+            for (int d = 0; d < D; ++d) dqr[d] = dqr[d] * scale;
+          }
+        for (int j = 0; j < tk; ++j) {
+          double* dkr = dk + packed_off(k0 + j, g, Hkv, D);
+          for (int d = 0; d < D; ++d) dkr[d] = dkr[d] * scale;
+        }
+      }
+    free(prob);
+    free(dprob);
+    free(orow);
+  }
+  return worst;
+}

@@ -75,6 +75,27 @@ void oracle_kv_rows(const double* q, const double* k, const double* v, const dou
  * (the rowsum that the backward's first step forms from the stored output). */
 void oracle_rowdot(const double* o, const double* dout, double* delta, int B, int T, int H, int D);
 
+/* Packed variable-length batches (no page describes them; the plainest
+ * extension of the definition above).  n_seq sequences; sequence s has the
+ * tq = cu_q[s+1] - cu_q[s] query rows from cu_q[s] and the tk = cu_k[s+1] -
+ * cu_k[s] key rows from cu_k[s] (cu_q[0] = cu_k[0] = 0, non-decreasing).
+ * Layouts: q, o, dout, dq [cu_q[n_seq], Hq, D]; k, v, dk, dv
+ * [cu_k[n_seq], Hkv, D]; lse, delta [Hq, cu_q[n_seq]].  Readings:
+ *   - the causal mask ends in the bottom-right corner of each sequence's
+ *     tq x tk score matrix: query i sees key j iff j <= i + (tk - tq), which
+ *     is j <= i when tq == tk;
+ *   - a query row that sees no key (tq > tk under the mask, or tk == 0) has
+ *     O = 0, LSE = -inf, dQ = 0 and delta = 0, and adds nothing to dK, dV.
+ * With every tq == tk == T these equal the fixed-length functions bit for bit
+ * (same operations in the same order). */
+void oracle_attn_fwd_varlen(const double* q, const double* k, const double* v, double* o,
+                            double* lse, int n_seq, const int* cu_q, const int* cu_k, int Hq,
+                            int Hkv, int D, double scale, int causal);
+double oracle_attn_bwd_varlen(const double* q, const double* k, const double* v,
+                              const double* dout, double* dq, double* dk, double* dv,
+                              double* delta, int n_seq, const int* cu_q, const int* cu_k, int Hq,
+                              int Hkv, int D, double scale, int causal);
+
 /* Number of OpenMP threads the oracle uses. */
 int oracle_num_threads(void);
 

@@ -308,6 +308,167 @@ def test_bf16_widening_is_exact():
     np.testing.assert_array_equal(got, vals.to(torch.float64).numpy())
 
 
+# ------------------------------------------------------------ packed variable-length batches
+def _packed(seed, tqs, tks, Hq, Hkv, D):
+    rng = np.random.default_rng(seed)
+    cu_q, cu_k = np.concatenate([[0], np.cumsum(tqs)]), np.concatenate([[0], np.cumsum(tks)])
+    return (_rand(rng, cu_q[-1], Hq, D), _rand(rng, cu_k[-1], Hkv, D), _rand(rng, cu_k[-1], Hkv, D),
+            _rand(rng, cu_q[-1], Hq, D), cu_q, cu_k)
+
+
+def test_varlen_equal_lengths_is_the_batched_oracle():
+    """B sequences of one length T, packed, give the fixed-length oracle's
+    bytes (same operations in the same order).  Catches a wrong packed offset
+    or LSE layout."""
+    B, T, Hq, Hkv, D = 3, 11, 6, 2, 5
+    q, k, v, do = _case(20, B, T, Hq, Hkv, D)
+    cu = np.arange(B + 1) * T
+    pk = lambda x: x.reshape(B * T, x.shape[2], D)
+    lse_layout = lambda x: x.transpose(1, 0, 2).reshape(x.shape[1], B * T)
+    for causal in (True, False):
+        o, lse = oracle.attn_fwd(q, k, v, 0.4, causal)
+        ov, lsev = oracle.attn_fwd_varlen(pk(q), pk(k), pk(v), cu, cu, 0.4, causal)
+        assert np.array_equal(pk(o), ov) and np.array_equal(lse_layout(lse), lsev)
+        dq, dk, dv, delta, _ = oracle.attn_bwd(q, k, v, do, 0.4, causal)
+        dqv, dkv, dvv, deltav, _ = oracle.attn_bwd_varlen(pk(q), pk(k), pk(v), pk(do), cu, cu, 0.4,
+                                                          causal)
+        assert np.array_equal(pk(dq), dqv) and np.array_equal(pk(dk), dkv)
+        assert np.array_equal(pk(dv), dvv) and np.array_equal(lse_layout(delta), deltav)
+
+
+def test_varlen_sequences_are_independent():
+    """Sequences of different lengths (one empty) each give exactly what the
+    fixed-length oracle gives for that sequence alone.  Catches attention
+    across a sequence boundary."""
+    tqs = [5, 0, 13, 1, 8]
+    Hq, Hkv, D = 4, 2, 6
+    q, k, v, do, cu, _ = _packed(21, tqs, tqs, Hq, Hkv, D)
+    for causal in (True, False):
+        o, lse = oracle.attn_fwd_varlen(q, k, v, cu, cu, 0.3, causal)
+        dq, dk, dv, _, _ = oracle.attn_bwd_varlen(q, k, v, do, cu, cu, 0.3, causal)
+        for s, T in enumerate(tqs):
+            if T == 0:
+                continue
+            sl = slice(cu[s], cu[s + 1])
+            one = lambda x: x[sl][None]
+            o1, lse1 = oracle.attn_fwd(one(q), one(k), one(v), 0.3, causal)
+            dq1, dk1, dv1, _, _ = oracle.attn_bwd(one(q), one(k), one(v), one(do), 0.3, causal)
+            assert np.array_equal(o[sl], o1[0]) and np.array_equal(lse[:, sl], lse1[0])
+            assert np.array_equal(dq[sl], dq1[0]) and np.array_equal(dk[sl], dk1[0])
+            assert np.array_equal(dv[sl], dv1[0])
+
+
+def _torch_seq(q, k, v, do, scale, causal):
+    """PyTorch fp64 SDPA with autograd for one sequence (q [tq, Hq, D],
+    k [tk, Hkv, D]) under the bottom-right causal mask.  Rows that see no key
+    are left out of the call (SDPA returns NaN for them) and returned as
+    O = 0, LSE = -inf, dQ = 0: they add nothing to dK, dV."""
+    tq, tk, Hq, Hkv = q.shape[0], k.shape[0], q.shape[1], k.shape[1]
+    G = Hq // Hkv
+    r0 = min(tq, max(0, tq - tk)) if causal else (tq if tk == 0 else 0)
+    o, lse = np.zeros_like(q), np.full((Hq, tq), -np.inf)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    if r0 == tq:
+        return o, lse, dq, dk, dv
+    tt = lambda x: torch.tensor(x, dtype=torch.float64).permute(1, 0, 2)[None].contiguous()
+    tq_, tk_, tv_ = (tt(x).requires_grad_(True) for x in (q[r0:], k, v))
+    kr, vr = tk_.repeat_interleave(G, dim=1), tv_.repeat_interleave(G, dim=1)
+    mask = None
+    if causal:
+        i = np.arange(r0, tq)[:, None]
+        mask = torch.tensor(np.arange(tk)[None, :] <= i + (tk - tq))
+    out = torch.nn.functional.scaled_dot_product_attention(tq_, kr, vr, attn_mask=mask,
+                                                           scale=scale)
+    out.backward(tt(do[r0:]))
+    sc = (tq_ @ kr.transpose(-1, -2)) * scale
+    if mask is not None:
+        sc = sc.masked_fill(~mask, float("-inf"))
+    back = lambda t: t.detach()[0].permute(1, 0, 2).numpy()
+    o[r0:], dq[r0:] = back(out), back(tq_.grad)
+    lse[:, r0:] = torch.logsumexp(sc, dim=-1).detach()[0].numpy()
+    return o, lse, dq, back(tk_.grad), back(tv_.grad)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_varlen_cross_attention_matches_torch(causal):
+    """Tq != Tk per sequence (more queries than keys, fewer, equal, no keys,
+    no queries) against PyTorch's fp64 scaled_dot_product_attention with the
+    bottom-right causal mask given explicitly.  Catches a wrong mask offset,
+    a wrong key offset or a wrong head mapping in the packed functions."""
+    tqs, tks = [7, 3, 12, 1, 5, 0], [4, 9, 12, 6, 0, 5]
+    Hq, Hkv, D = 4, 2, 8
+    q, k, v, do, cu_q, cu_k = _packed(22, tqs, tks, Hq, Hkv, D)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = oracle.attn_fwd_varlen(q, k, v, cu_q, cu_k, scale, causal)
+    dq, dk, dv, _, worst = oracle.attn_bwd_varlen(q, k, v, do, cu_q, cu_k, scale, causal)
+    assert worst <= 1e-12
+    for s in range(len(tqs)):
+        sq, sk = slice(cu_q[s], cu_q[s + 1]), slice(cu_k[s], cu_k[s + 1])
+        o_r, lse_r, dq_r, dk_r, dv_r = _torch_seq(q[sq], k[sk], v[sk], do[sq], scale, causal)
+        if tqs[s]:
+            assert _rel(o[sq], o_r, floor=1.0) <= 1e-12
+            fin = np.isfinite(lse_r)
+            assert np.array_equal(fin, np.isfinite(lse[:, sq]))
+            if fin.any():
+                assert _rel(lse[:, sq][fin], lse_r[fin], floor=1.0) <= 1e-12
+            assert _rel(dq[sq], dq_r, floor=1.0) <= 1e-12
+        if tks[s]:
+            assert _rel(dk[sk], dk_r, floor=1.0) <= 1e-12
+            assert _rel(dv[sk], dv_r, floor=1.0) <= 1e-12
+
+
+def test_varlen_rows_that_see_no_key():
+    """More queries than keys under the causal mask: the first tq - tk rows
+    see nothing, so O = 0, LSE = -inf, dQ = 0, Delta = 0; keys that no query
+    sees get dK = dV = 0."""
+    tqs, tks = [6, 3], [2, 0]
+    q, k, v, do, cu_q, cu_k = _packed(23, tqs, tks, 2, 1, 4)
+    o, lse = oracle.attn_fwd_varlen(q, k, v, cu_q, cu_k, 0.5, True)
+    dq, dk, dv, delta, _ = oracle.attn_bwd_varlen(q, k, v, do, cu_q, cu_k, 0.5, True)
+    blind = list(range(0, 4)) + list(range(6, 9))  # rows 0..3 of seq 0, all of seq 1
+    assert np.all(o[blind] == 0.0) and np.all(dq[blind] == 0.0) and np.all(delta[:, blind] == 0.0)
+    assert np.all(np.isneginf(lse[:, blind]))
+    assert np.all(np.isfinite(lse[:, 4:6])) and np.max(np.abs(o[4:6])) > 0.0
+    # Row 4 sees key 0 only, row 5 both: O_4 is V_0 exactly.
+    np.testing.assert_array_equal(o[4, 0], v[0, 0])
+    # Non-causal: every row of seq 0 sees both keys.
+    o_f, _ = oracle.attn_fwd_varlen(q, k, v, cu_q, cu_k, 0.5, False)
+    assert np.all(np.abs(o_f[0:6]).sum(axis=-1) > 0.0) and np.all(o_f[6:9] == 0.0)
+
+
+def test_varlen_finite_differences():
+    """Central differences of L = sum(dO * O) over every entry of Q, K, V of a
+    packed batch with a query row that sees no key and a key that no query
+    sees match the packed backward."""
+    tqs, tks = [3, 2], [2, 4]
+    q, k, v, do, cu_q, cu_k = _packed(24, tqs, tks, 2, 1, 2)
+    scale = 0.8
+    dq, dk, dv, _, _ = oracle.attn_bwd_varlen(q, k, v, do, cu_q, cu_k, scale, True)
+
+    def loss(args):
+        o, _ = oracle.attn_fwd_varlen(args["q"], args["k"], args["v"], cu_q, cu_k, scale, True)
+        return float(np.sum(do * o))
+
+    h = 1e-6
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            base = {"q": q, "k": k, "v": v}
+            fd[idx] = (loss({**base, name: xp}) - loss({**base, name: xm})) / (2 * h)
+        assert np.max(np.abs(fd - grad)) <= 1e-6 * max(1.0, np.max(np.abs(grad))), name
+
+
+def test_varlen_validates():
+    q, k, v, _, cu_q, cu_k = _packed(25, [2, 3], [2, 3], 2, 1, 4)
+    for bad_q, bad_k in (([1, 2, 5], cu_k), ([0, 3, 2, 5], [0, 2, 3, 5]), ([0, 2, 4], cu_k),
+                         (cu_q, [0, 5])):
+        with pytest.raises(ValueError):
+            oracle.attn_fwd_varlen(q, k, v, bad_q, bad_k, 0.5, True)
+
+
 # ------------------------------------------------------------ the pins catch planted mistakes
 # Each entry plants one plausible mistake in a copy of the oracle's C source:
 # (name, text in the source, its replacement, how often the text occurs).  A
@@ -350,6 +511,18 @@ _MUTANTS = [
     ("kv_rows_range_starts_late", "for (int i = causal ? j : 0; i < T; ++i)",
      "for (int i = causal ? j + 1 : 0; i < T; ++i)", 1),
     ("rows_head_interleaved", "i = ri[s], g = h / G;", "i = ri[s], g = h % Hkv;", 1),
+    ("varlen_mask_offset_flipped", "const int n = i + 1 + (tk - tq);",
+     "const int n = i + 1 + (tq - tk);", 1),
+    ("varlen_values_of_first_sequence",
+     "seq_weighted_values(prob, v, cu_k[s], n, h / G, Hkv, D, o + packed_off(row, h, Hq, D));",
+     "seq_weighted_values(prob, v, 0, n, h / G, Hkv, D, o + packed_off(row, h, Hq, D));", 1),
+    ("varlen_blind_row_lse_zero", "*lse_out = -INFINITY;\n    return;", "*lse_out = 0.0;\n    return;", 1),
+    ("varlen_group_interleaved", "for (int h = g * G; h < g * G + G; ++h)",
+     "for (int h = g; h < Hq; h += Hkv)", 1),
+    ("varlen_ds_sign_flipped", "const double dsc = prob[j] * (dprob[j] - dl);",
+     "const double dsc = prob[j] * (dl - dprob[j]);", 1),
+    ("varlen_dk_scale_dropped", "for (int d = 0; d < D; ++d) dkr[d] = dkr[d] * scale;", "", 1),
+    ("varlen_dq_scale_dropped", "for (int d = 0; d < D; ++d) dqr[d] = dqr[d] * scale;", "", 1),
 ]
 
 _SDPA_CASES = [(shape, causal) for shape in [(2, 37, 6, 2, 16), (1, 64, 4, 4, 32), (1, 1, 2, 1, 8)]
@@ -370,6 +543,12 @@ _PINS = [
     ("fd_full", test_finite_differences, (False,)),
     ("sdpa", lambda: [test_matches_torch_sdpa_fp64(s, c) for s, c in _SDPA_CASES], ()),
     ("sampled_rows", test_sampled_rows_match_full_oracle, ()),
+    ("varlen_batched", test_varlen_equal_lengths_is_the_batched_oracle, ()),
+    ("varlen_independent", test_varlen_sequences_are_independent, ()),
+    ("varlen_torch_causal", test_varlen_cross_attention_matches_torch, (True,)),
+    ("varlen_torch_full", test_varlen_cross_attention_matches_torch, (False,)),
+    ("varlen_blind_rows", test_varlen_rows_that_see_no_key, ()),
+    ("varlen_fd", test_varlen_finite_differences, ()),
 ]
 
 
