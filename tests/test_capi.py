@@ -189,3 +189,36 @@ def test_dkdv_split_validates():
     assert da.diag_dkdv_split(1, 128, 2, 1, 64, True, [0, 0, 0, 5], 8) == (8, 1)
     with pytest.raises(da.DetAttnError):
         da.diag_dkdv_split(1, 128, 2, 1, 128, True, [152, 0, 0, 5], 8)
+
+
+def test_size_limits_reject_before_any_device_call(L):
+    """Shapes beyond the kernels' index limits fail validation (no device is
+    needed to reach the answer)."""
+    assert _fwd(L, B=1 << 20, T=1 << 20, Hq=16, Hkv=1) == -3     # elements > 1e12
+    assert _fwd(L, B=1, T=(1 << 30) + 1, Hq=1, Hkv=1) == -3      # T > 2^30
+    assert "too large" in da.last_error()
+    assert L.attn_bwd_workspace_bytes(1 << 20, 1 << 20, 16, 1, 64) == 0
+
+
+def _has_gpu():
+    import torch
+    return torch.cuda.is_available()
+
+
+def test_noalloc_rejects(L):
+    def call(B=1, T=128, Hq=2, Hkv=1, D=64, ptr=P, scale=0.125):
+        return L.attn_bwd_noalloc(P, P, P, P, P, P, ptr, P, P, B, T, Hq, Hkv, D, scale, 1, None)
+    # B * Hq * Tp row-statistic pairs above the built-in 2^20: a workspace error.
+    assert call(B=4, T=1024, Hq=257) == -9                 # 4 * 257 * 1024 > 2^20
+    assert "exceeds the built-in scratch" in da.last_error()
+    assert call(B=16, T=1025, Hq=64, Hkv=8) == -9         # Tp = 1152: 1,179,648 pairs
+    if not _has_gpu():
+        # Just under the limit validation passes, and only the missing device
+        # stops the call.  (Never made where a GPU exists: the pointers here
+        # are stand-ins.)
+        assert call(B=8, T=1025, Hq=64, Hkv=8) == -6
+    assert call(ptr=None) == -1
+    assert call(ptr=BAD) == -2
+    assert call(D=96) == -4
+    assert call(scale=0.0) == -5
+    assert call(B=0, ptr=None) == 0                       # empty: nothing to do
