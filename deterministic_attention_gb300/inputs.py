@@ -86,6 +86,54 @@ def make_inputs(B: int, T: int, Hq: int, Hkv: int, D: int, seed: int, dout_std: 
     return q, k, v, dout
 
 
+def varlen_lengths(total: int, lo: int, hi: int, seed: int) -> list[int]:
+    """Sequence lengths that sum to `total`: each drawn uniformly from
+    [lo, hi] with ``torch.randint`` on a generator seeded with `seed`, the
+    last one cut to what is left (so it may be shorter than lo)."""
+    if not (0 < lo <= hi) or total < 0:
+        raise ValueError(f"need 0 < lo <= hi and total >= 0 (lo={lo}, hi={hi}, total={total})")
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    out, left = [], total
+    while left > 0:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g))
+        out.append(min(n, left))
+        left -= out[-1]
+    return out
+
+
+def make_varlen_inputs(tqs, tks, Hq: int, Hkv: int, D: int, seed: int, dout_std: float = 1.0):
+    """Packed bf16 CPU tensors q, dout [sum(tqs), Hq, D] and k, v [sum(tks), Hkv, D],
+    and the int32 offsets cu_q, cu_k (sequence s: rows cu[s] .. cu[s+1]-1).
+    Same draw order as make_inputs, so B sequences of length T give exactly
+    make_inputs' values in the packed layout."""
+    if len(tqs) != len(tks) or min(list(tqs) + list(tks) + [0]) < 0:
+        raise ValueError("tqs and tks must be equally long lists of lengths >= 0")
+    cu_q = torch.tensor([0] + list(tqs), dtype=torch.int64).cumsum(0).to(torch.int32)
+    cu_k = torch.tensor([0] + list(tks), dtype=torch.int64).cumsum(0).to(torch.int32)
+    nq, nk = int(cu_q[-1]), int(cu_k[-1])
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    q = torch.randn((nq, Hq, D), dtype=torch.float32, generator=g)
+    k = torch.randn((nk, Hkv, D), dtype=torch.float32, generator=g)
+    v = torch.randn((nk, Hkv, D), dtype=torch.float32, generator=g)
+    dout = torch.randn((nq, Hq, D), dtype=torch.float32, generator=g)
+    if dout_std != 1.0:
+        dout = dout * dout_std
+    q, k, v, dout = (t.to(torch.bfloat16) for t in (q, k, v, dout))
+    return q, k, v, dout, cu_q, cu_k
+
+
+# Packed variable-length workload next to page3 (no page describes one): the
+# same 4 x 1024 = 4,096 tokens per step and heads, cut into sequences of
+# 64..1,024 tokens (self-attention, Tq = Tk), seed 5, dO sigma 0.1.
+VARLEN_PAGE3 = dict(total=4096, lo=64, hi=1024, Hq=12, Hkv=4, D=64, seed=5, dout_std=0.1)
+
+
+def varlen_page3_inputs():
+    w = VARLEN_PAGE3
+    tqs = varlen_lengths(w["total"], w["lo"], w["hi"], w["seed"])
+    return make_varlen_inputs(tqs, tqs, w["Hq"], w["Hkv"], w["D"], w["seed"], w["dout_std"])
+
+
 def workload_inputs(w: Workload):
     return make_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, w.seed, w.dout_std, w.k_peak_frac)
 
