@@ -222,3 +222,28 @@ def test_noalloc_rejects(L):
     assert call(D=96) == -4
     assert call(scale=0.0) == -5
     assert call(B=0, ptr=None) == 0                       # empty: nothing to do
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library every call raises: there is no fallback."""
+    monkeypatch.setattr(da, "_lib", None)
+    monkeypatch.setattr(da, "_LIB_PATH", str(tmp_path / "libdetattn.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        da.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        da.last_error()
+
+
+def test_product_shares_nothing_with_the_oracle():
+    """The package (binding, build, kernels, host layer) never imports,
+    includes or links the oracle; only tests, smoke and the bench's CPU legs do."""
+    import glob
+    import os
+    pkg = os.path.dirname(da.__file__)
+    files = (glob.glob(os.path.join(pkg, "*.py")) + glob.glob(os.path.join(pkg, "csrc", "*")) +
+             glob.glob(os.path.join(os.path.dirname(pkg), "include", "*")))
+    assert len(files) >= 8
+    for f in files:
+        text = open(f, errors="replace").read()
+        for needle in ("import oracle", "from oracle", "attn_oracle", "liboracle"):
+            assert needle not in text, (f, needle)
