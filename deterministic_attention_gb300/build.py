@@ -37,8 +37,14 @@ def _inputs():
     return files
 
 
+def resource_report_path(src: str) -> str:
+    """ptxas's resource report (registers, spills, shared memory per kernel)
+    of one translation unit, kept from the last build."""
+    return os.path.join(BUILD, src.replace(".cu", ".ptxas.txt"))
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not os.path.exists(LIB) or not all(os.path.exists(resource_report_path(s)) for s in SOURCES):
         return False
     t = os.path.getmtime(LIB)
     return all(os.path.getmtime(f) <= t for f in _inputs())
@@ -53,25 +59,34 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     def compile_one(src: str) -> str:
         obj = os.path.join(BUILD, src.replace(".cu", f".{tag}.o"))
-        cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-I", INCLUDE, "-c",
+        cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-Xptxas", "-v", "-I", INCLUDE, "-c",
                os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        report = resource_report_path(src)
+        with open(report + f".tmp{tag}", "w") as f:
+            f.write(r.stdout + r.stderr)
+        os.replace(report + f".tmp{tag}", report)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{tag}"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    for o in objs:
-        os.remove(o)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    objs = [os.path.join(BUILD, src.replace(".cu", f".{tag}.o")) for src in SOURCES]
+    try:
+        with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+            list(ex.map(compile_one, SOURCES))
+        tmp = LIB + f".tmp{tag}"
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, LIB)
+    finally:
+        # This build's objects go whether it succeeded or not.
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB
 
 

@@ -247,3 +247,42 @@ def test_product_shares_nothing_with_the_oracle():
         text = open(f, errors="replace").read()
         for needle in ("import oracle", "from oracle", "attn_oracle", "liboracle"):
             assert needle not in text, (f, needle)
+
+
+# Threads that share one SM's 65,536 registers for each kernel: its block size
+# times the blocks it keeps per SM.
+_KERNEL_THREADS_PER_SM = {
+    "attn_fwd_kernelILi64E": 640, "attn_fwd_kernelILi128E": 320,
+    "attn_dq_kernelILi64E": 640, "attn_dq_kernelILi128E": 320,
+    "attn_dkdv_kernelILi64E": 608, "attn_dkdv_kernelILi128E": 608,
+    "attn_delta_kernelILi64E": 4 * 256, "attn_delta_kernelILi128E": 4 * 256,
+}
+
+
+def _ptxas_entries():
+    """(kernel, registers, spill store bytes, spill load bytes) from the
+    build's ptxas reports."""
+    import importlib
+    import re
+    b = importlib.import_module("deterministic_attention_gb300.build")
+    out = []
+    for src in b.SOURCES:
+        text = open(b.resource_report_path(src)).read()
+        for chunk in text.split("Compiling entry function '")[1:]:
+            name = chunk.split("'", 1)[0]
+            regs = int(re.search(r"Used (\d+) registers", chunk).group(1))
+            sp = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", chunk)
+            out.append((name, regs, int(sp.group(1)), int(sp.group(2))))
+    return out
+
+
+def test_kernels_fit_their_launch_without_spills(L):
+    entries = _ptxas_entries()
+    seen = set()
+    for name, regs, st, ld in entries:
+        assert st == 0 and ld == 0, f"{name} spills {st}/{ld} bytes"
+        for key, threads in _KERNEL_THREADS_PER_SM.items():
+            if key in name:
+                seen.add(key)
+                assert regs * threads <= 65536, f"{name}: {regs} registers x {threads} threads"
+    assert seen == set(_KERNEL_THREADS_PER_SM), f"kernels not found in the reports: {seen}"
