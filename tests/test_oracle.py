@@ -273,10 +273,7 @@ def test_oracle_is_deterministic():
         assert x.tobytes() == y.tobytes()
 
 
-def test_oracle_reproduces_its_fixture():
-    """The stored outputs of tests/golden/make_oracle_fixture.py (written by
-    the oracle alone) are reproduced; tolerance for libm differences between
-    hosts only."""
+def _fixture_module():
     import importlib.util
     import os
     golden = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
@@ -284,20 +281,32 @@ def test_oracle_reproduces_its_fixture():
         "make_oracle_fixture", os.path.join(golden, "make_oracle_fixture.py"))
     fx = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(fx)
+    return fx, golden
+
+
+@pytest.mark.parametrize("which", ["fixed", "varlen"])
+def test_oracle_reproduces_its_fixture(which):
+    """The stored outputs of tests/golden/make_oracle_fixture.py (written by
+    the oracle alone) are reproduced; tolerance for libm differences between
+    hosts only (-inf entries must match exactly)."""
+    import os
+    fx, golden = _fixture_module()
+    name, outputs = ((fx.NAME, fx.outputs) if which == "fixed"
+                     else (fx.VARLEN_NAME, fx.varlen_outputs))
     stored = {}
-    with open(os.path.join(golden, fx.NAME)) as f:
+    with open(os.path.join(golden, name)) as f:
         for line in f:
             if line.startswith("#"):
                 continue
-            causal, name, *vals = line.split()
-            stored[(int(causal.split("=")[1]), name)] = np.array([float(x) for x in vals])
+            causal, tensor, *vals = line.split()
+            stored[(int(causal.split("=")[1]), tensor)] = np.array([float(x) for x in vals])
     assert len(stored) == 10
     for causal in (1, 0):
-        for name, x in fx.outputs(bool(causal)).items():
-            ref = stored[(causal, name)]
-            assert ref.size == x.size, (causal, name)
+        for tensor, x in outputs(bool(causal)).items():
+            ref = stored[(causal, tensor)]
+            assert ref.size == x.size, (causal, tensor)
             np.testing.assert_allclose(x.reshape(-1), ref, rtol=1e-13, atol=1e-15,
-                                       err_msg=f"causal={causal} {name}")
+                                       err_msg=f"causal={causal} {tensor}")
 
 
 def test_bf16_widening_is_exact():
