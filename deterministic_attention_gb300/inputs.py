@@ -122,6 +122,27 @@ def make_varlen_inputs(tqs, tks, Hq: int, Hkv: int, D: int, seed: int, dout_std:
     return q, k, v, dout, cu_q, cu_k
 
 
+def visible_pairs(tq: int, tk: int, causal: bool) -> int:
+    """(query, key) pairs a sequence attends over: every pair, or under the
+    bottom-right causal mask (query i sees key j iff j <= i + tk - tq) the sum
+    over rows of clamp(i + 1 + tk - tq, 0, tk)."""
+    if not causal:
+        return tq * tk
+    off = tk - tq
+    # Rows with i + 1 + off <= 0 see nothing; rows with i + 1 + off >= tk see all.
+    lo = max(0, -off)                      # first row that sees a key
+    hi = min(tq, max(lo, tk - off - 1))    # first row that sees every key
+    partial = sum(range(lo + 1 + off, hi + 1 + off)) if hi > lo else 0
+    return partial + (tq - hi) * tk
+
+
+def varlen_fwd_flops(tqs, tks, Hq: int, D: int, causal: bool) -> float:
+    """Algorithmic forward FLOPs of a packed batch: 4 * Hq * D per visible
+    pair (Q K^T and P V).  With tq = tk = T causal this is the fixed-length
+    2 * Hq * T^2 * D plus its diagonal term 2 * Hq * T * D."""
+    return 4.0 * Hq * D * sum(visible_pairs(a, b, causal) for a, b in zip(tqs, tks))
+
+
 # Packed variable-length workload next to page3 (no page describes one): the
 # same 4 x 1024 = 4,096 tokens per step and heads, cut into sequences of
 # 64..1,024 tokens (self-attention, Tq = Tk), seed 5, dO sigma 0.1.

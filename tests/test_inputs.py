@@ -81,3 +81,17 @@ def test_named_workloads_are_the_documented_shapes():
     assert shapes == {"tiny": (1, 128, 2, 1, 64), "small": (1, 512, 12, 4, 64),
                       "page3": (4, 1024, 12, 4, 64), "wide": (32, 1024, 24, 24, 64),
                       "long": (1, 8192, 32, 8, 128)}
+
+
+def test_visible_pairs_count_the_mask():
+    """The closed-form pair count equals a count of the bottom-right causal
+    mask (and of the full matrix) for every tq, tk < 12."""
+    from deterministic_attention_gb300.inputs import varlen_fwd_flops, visible_pairs
+    for tq in range(12):
+        for tk in range(12):
+            i, j = np.arange(tq)[:, None], np.arange(tk)[None, :]
+            assert visible_pairs(tq, tk, True) == int((j <= i + (tk - tq)).sum()), (tq, tk)
+            assert visible_pairs(tq, tk, False) == tq * tk
+    # tq = tk = T, causal: 2 Hq T^2 D plus the diagonal's 2 Hq T D.
+    T, Hq, D = 1024, 12, 64
+    assert varlen_fwd_flops([T], [T], Hq, D, True) == 2 * Hq * T * T * D + 2 * Hq * T * D
