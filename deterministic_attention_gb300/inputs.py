@@ -155,6 +155,32 @@ def varlen_page3_inputs():
     return make_varlen_inputs(tqs, tqs, w["Hq"], w["Hkv"], w["D"], w["seed"], w["dout_std"])
 
 
+# Embedding-lookup gradient of the trainer the oxide-train README profiles
+# ("Full-step profiling": B = 32, T = 1024, a vocabulary of 50,257 padded to
+# 50,432, width 1536): N = 32,768 token ids and their gradient rows.
+EMBED_GRAD = dict(N=32 * 1024, V=50432, V_used=50257, E=1536, seed=6)
+
+
+def make_embed_grad_inputs(N: int, V_used: int, E: int, seed: int, dist: str = "uniform",
+                           zipf_s: float = 1.1):
+    """int32 token ids [N] in [0, V_used) and a bf16 gradient dY [N, E] ~ N(0, 1).
+
+    dist "uniform": ids from ``torch.randint`` (synthetic token IDs, as the
+    throughput runs use); "zipf": id r drawn with weight 1 / (r + 1)^zipf_s by
+    ``torch.multinomial`` (a natural-text stand-in, where a few ids take most
+    tokens and collide often).  Ids are drawn first, then dY."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    if dist == "uniform":
+        ids = torch.randint(0, V_used, (N,), generator=g, dtype=torch.int64)
+    elif dist == "zipf":
+        w = torch.arange(1, V_used + 1, dtype=torch.float64).pow(-zipf_s)
+        ids = torch.multinomial(w, N, replacement=True, generator=g)
+    else:
+        raise ValueError(f"dist must be 'uniform' or 'zipf', not {dist!r}")
+    dy = torch.randn((N, E), dtype=torch.float32, generator=g).to(torch.bfloat16)
+    return ids.to(torch.int32), dy
+
+
 def workload_inputs(w: Workload):
     return make_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, w.seed, w.dout_std, w.k_peak_frac)
 

@@ -7,7 +7,9 @@ library never imports, links or runs it, and the two share no code.
 Besides fixed-length batches [B, T, H, D] it covers packed variable-length
 batches with Tq != Tk (``attn_fwd_varlen``, ``attn_bwd_varlen``), which no page
 describes; the readings (bottom-right causal alignment, rows that see no key)
-are stated in ``attn_oracle.h``.
+are stated in ``attn_oracle.h``.  ``embed_grad`` (``embed_oracle.c``) is the
+gradient of an embedding lookup summed in ascending token order (oxide-train
+README, "The trainer is not bit-identical to itself after step 1").
 
 The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over
 independent heads); this module compiles it with gcc, loads it with ctypes and
@@ -29,30 +31,33 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "attn_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "embed_oracle.c")]
 _LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
 _lib = None
 
 
-def compile_library(src: str, out: str) -> str:
-    """Compile a C source of the oracle (``attn_oracle.c`` or a copy of it)
-    into the shared library ``out`` with the flags the oracle is built with."""
+def compile_library(srcs, out: str) -> str:
+    """Compile the oracle's C sources (the files in ``oracle/`` or copies of
+    them) into the shared library ``out`` with the flags the oracle is built
+    with."""
+    srcs = [srcs] if isinstance(srcs, str) else list(srcs)
     # -O2 without -ffast-math: the compiler keeps every sum in source order.
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-I", _HERE, src, "-o", out,
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-I", _HERE, *srcs, "-o", out,
            "-lm"]
     subprocess.run(cmd, check=True)
     return out
 
 
 def build(force: bool = False) -> str:
-    """Compile ``attn_oracle.c`` into ``_build/liboracle.so`` (gcc, -O2, OpenMP)."""
+    """Compile the oracle's C sources into ``_build/liboracle.so`` (gcc, -O2, OpenMP)."""
     os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
     fresh = os.path.exists(_LIB_PATH) and all(
         os.path.getmtime(_LIB_PATH) >= os.path.getmtime(os.path.join(_HERE, f))
-        for f in ("attn_oracle.c", "attn_oracle.h"))
+        for f in ("attn_oracle.c", "attn_oracle.h", "embed_oracle.c", "embed_oracle.h"))
     if fresh and not force:
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    compile_library(_SRC, tmp)
+    compile_library(_SRCS, tmp)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -88,6 +93,8 @@ def _bind(lib):
     lib.oracle_attn_fwd_varlen.restype = None
     lib.oracle_attn_bwd_varlen.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, i, ip, ip, i, i, i, d, i]
     lib.oracle_attn_bwd_varlen.restype = d
+    lib.oracle_embed_grad.argtypes = [ip, dp, dp, i, i, i]
+    lib.oracle_embed_grad.restype = i
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = i
     return lib
@@ -239,3 +246,17 @@ def attn_bwd_varlen(q, k, v, dout, cu_q, cu_k, scale: float, causal: bool = True
                                            _dp(dv), _dp(delta), n_seq, _ip(cq), _ip(ck), Hq, Hkv,
                                            D, float(scale), int(bool(causal)))
     return dq, dk, dv, delta, worst
+
+
+def embed_grad(ids, dy, V: int):
+    """dW [V, E] = sum over t with ids[t] == v of dy[t, :] (ascending t, fp64)
+    for ids [N] and dy [N, E]."""
+    ids = np.ascontiguousarray(np.asarray(ids).reshape(-1), dtype=np.int32)
+    dy = _f64(dy)
+    N, E = dy.shape
+    if ids.size != N:
+        raise ValueError(f"{ids.size} ids for {N} gradient rows")
+    dw = np.empty((V, E), dtype=np.float64)
+    if _load().oracle_embed_grad(_ip(ids), _dp(dy), _dp(dw), N, int(V), E) != 0:
+        raise ValueError(f"ids must lie in [0, {V})")
+    return dw

@@ -245,7 +245,7 @@ def test_product_shares_nothing_with_the_oracle():
     assert len(files) >= 8
     for f in files:
         text = open(f, errors="replace").read()
-        for needle in ("import oracle", "from oracle", "attn_oracle", "liboracle"):
+        for needle in ("import oracle", "from oracle", "attn_oracle", "embed_oracle", "liboracle"):
             assert needle not in text, (f, needle)
 
 

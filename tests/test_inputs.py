@@ -95,3 +95,32 @@ def test_visible_pairs_count_the_mask():
     # tq = tk = T, causal: 2 Hq T^2 D plus the diagonal's 2 Hq T D.
     T, Hq, D = 1024, 12, 64
     assert varlen_fwd_flops([T], [T], Hq, D, True) == 2 * Hq * T * T * D + 2 * Hq * T * D
+
+
+@pytest.mark.parametrize("dist", ["uniform", "zipf"])
+def test_embed_grad_inputs(dist):
+    from deterministic_attention_gb300.inputs import make_embed_grad_inputs
+    ids, dy = make_embed_grad_inputs(5000, 300, 7, seed=3, dist=dist)
+    ids2, dy2 = make_embed_grad_inputs(5000, 300, 7, seed=3, dist=dist)
+    assert torch.equal(ids, ids2) and torch.equal(dy, dy2)
+    assert ids.dtype == torch.int32 and dy.dtype == torch.bfloat16 and dy.shape == (5000, 7)
+    assert int(ids.min()) >= 0 and int(ids.max()) < 300
+    counts = torch.bincount(ids.long(), minlength=300)
+    if dist == "zipf":
+        # Id 0 takes the largest share, far above the uniform 1/300.
+        assert int(counts.argmax()) == 0 and counts[0] > 5000 / 30
+    else:
+        assert counts.max() < 5000 / 300 * 3
+
+
+def test_embed_grad_oracle_on_generated_inputs():
+    """The oracle on the generator's ids and exactly widened bf16 rows matches
+    the one-hot product."""
+    from deterministic_attention_gb300.inputs import make_embed_grad_inputs
+    ids, dy = make_embed_grad_inputs(2000, 120, 9, seed=4, dist="zipf")
+    dyf = oracle.bf16_bits_to_f64(bf16_bits(dy)).reshape(tuple(dy.shape))
+    dw = oracle.embed_grad(ids.numpy(), dyf, 120)
+    onehot = np.zeros((2000, 120))
+    onehot[np.arange(2000), ids.numpy()] = 1.0
+    ref = onehot.T @ dyf
+    assert np.max(np.abs(dw - ref)) <= 1e-12 * np.max(np.abs(ref))

@@ -478,6 +478,54 @@ def test_varlen_validates():
             oracle.attn_fwd_varlen(q, k, v, bad_q, bad_k, 0.5, True)
 
 
+# ------------------------------------------------------------ embedding-lookup gradient
+def test_embed_grad_hand_case():
+    """ids (2, 0, 2, 3): row 2 gets rows 0 and 2 of dY, row 0 gets row 1,
+    row 3 gets row 3, row 1 nothing (exactly zero)."""
+    ids = np.array([2, 0, 2, 3])
+    dy = np.array([[1.0, -2.0, 0.5], [3.0, 4.0, -1.0], [5.0, 6.0, 2.0], [-7.0, 0.25, 8.0]])
+    dw = oracle.embed_grad(ids, dy, 5)
+    np.testing.assert_array_equal(dw, [[3.0, 4.0, -1.0], [0.0, 0.0, 0.0], [6.0, 4.0, 2.5],
+                                       [-7.0, 0.25, 8.0], [0.0, 0.0, 0.0]])
+
+
+def test_embed_grad_is_the_one_hot_product():
+    """dW = onehot(ids)^T dY, the lookup's Jacobian transposed (a numpy fp64
+    matrix product), on skewed ids with many repeats."""
+    rng = np.random.default_rng(30)
+    N, V, E = 700, 97, 13
+    ids = np.minimum((rng.pareto(1.2, N) * 3).astype(np.int64), V - 1)
+    dy = rng.standard_normal((N, E))
+    onehot = np.zeros((N, V))
+    onehot[np.arange(N), ids] = 1.0
+    assert _rel(oracle.embed_grad(ids, dy, V), onehot.T @ dy) <= 1e-13
+    # Column totals are kept, and a row no token selects is exactly zero.
+    dw = oracle.embed_grad(ids, dy, V)
+    assert _rel(dw.sum(axis=0), dy.sum(axis=0)) <= 1e-12
+    unused = np.setdiff1d(np.arange(V), ids)
+    assert unused.size > 0 and np.all(dw[unused] == 0.0)
+
+
+def test_embed_grad_order_is_ascending_positions():
+    """Each row is summed over its tokens in ascending position: a sum that
+    rounds differently in another order shows which one was taken."""
+    ids = np.array([1, 1, 1])
+    dy = np.array([[1.0], [1e16], [-1e16]])
+    # Ascending: (1 + 1e16) - 1e16 = 0 in fp64; descending would give 1.
+    assert oracle.embed_grad(ids, dy, 2)[1, 0] == 0.0
+    assert oracle.embed_grad(ids[::-1], dy[::-1], 2)[1, 0] == 1.0
+
+
+def test_embed_grad_validates():
+    with pytest.raises(ValueError):
+        oracle.embed_grad([0, 5], np.zeros((2, 3)), 5)
+    with pytest.raises(ValueError):
+        oracle.embed_grad([-1, 0], np.zeros((2, 3)), 5)
+    with pytest.raises(ValueError):
+        oracle.embed_grad([0, 1, 2], np.zeros((2, 3)), 5)
+    assert oracle.embed_grad([], np.zeros((0, 3)), 4).tolist() == [[0.0] * 3] * 4
+
+
 # ------------------------------------------------------------ the pins catch planted mistakes
 # Each entry plants one plausible mistake in a copy of the oracle's C source:
 # (name, text in the source, its replacement, how often the text occurs).  A
@@ -534,6 +582,14 @@ _MUTANTS = [
     ("varlen_dq_scale_dropped", "for (int d = 0; d < D; ++d) dqr[d] = dqr[d] * scale;", "", 1),
 ]
 
+# Planted mistakes in embed_oracle.c (all stay in bounds).
+_EMBED_MUTANTS = [
+    ("embed_row_shifted", "dw[(size_t)ids[t] * E + col]", "dw[(size_t)((ids[t] + 1) % V) * E + col]", 1),
+    ("embed_rows_reversed", "dy[(size_t)t * E + col]", "dy[(size_t)(N - 1 - t) * E + col]", 1),
+    ("embed_columns_reversed", "dy[(size_t)t * E + col]", "dy[(size_t)t * E + (E - 1 - col)]", 1),
+    ("embed_last_token_dropped", "for (int t = 0; t < N; ++t) dw", "for (int t = 0; t + 1 < N; ++t) dw", 1),
+]
+
 _SDPA_CASES = [(shape, causal) for shape in [(2, 37, 6, 2, 16), (1, 64, 4, 4, 32), (1, 1, 2, 1, 8)]
                for causal in (True, False)]
 _PINS = [
@@ -558,21 +614,29 @@ _PINS = [
     ("varlen_torch_full", test_varlen_cross_attention_matches_torch, (False,)),
     ("varlen_blind_rows", test_varlen_rows_that_see_no_key, ()),
     ("varlen_fd", test_varlen_finite_differences, ()),
+    ("embed_hand", test_embed_grad_hand_case, ()),
+    ("embed_one_hot", test_embed_grad_is_the_one_hot_product, ()),
+    ("embed_order", test_embed_grad_order_is_ascending_positions, ()),
 ]
 
 
-@pytest.mark.parametrize("name,old,new,count",
-                         [pytest.param(*m, id=m[0])
-                          for m in [("unchanged", None, None, 0)] + _MUTANTS])
-def test_pins_catch_planted_mistakes(name, old, new, count, tmp_path, monkeypatch):
-    with open(oracle._SRC) as f:
-        src = f.read()
-    if old is not None:
-        assert src.count(old) == count, name
-        src = src.replace(old, new)
-    c_path = tmp_path / f"{name}.c"
-    c_path.write_text(src)
-    lib = oracle._bind(ctypes.CDLL(oracle.compile_library(str(c_path), str(tmp_path / f"{name}.so"))))
+@pytest.mark.parametrize("source,name,old,new,count",
+                         [pytest.param("attn_oracle.c", *m, id=m[0])
+                          for m in [("unchanged", None, None, 0)] + _MUTANTS] +
+                         [pytest.param("embed_oracle.c", *m, id=m[0]) for m in _EMBED_MUTANTS])
+def test_pins_catch_planted_mistakes(source, name, old, new, count, tmp_path, monkeypatch):
+    import os
+    paths = []
+    for src_path in oracle._SRCS:
+        with open(src_path) as f:
+            src = f.read()
+        if os.path.basename(src_path) == source and old is not None:
+            assert src.count(old) == count, name
+            src = src.replace(old, new)
+        paths.append(tmp_path / os.path.basename(src_path))
+        paths[-1].write_text(src)
+    lib = oracle._bind(ctypes.CDLL(oracle.compile_library([str(p) for p in paths],
+                                                          str(tmp_path / f"{name}.so"))))
     monkeypatch.setattr(oracle, "_lib", lib)
     caught = []
     for pin, fn, args in _PINS:
