@@ -181,6 +181,24 @@ def make_embed_grad_inputs(N: int, V_used: int, E: int, seed: int, dist: str = "
     return ids.to(torch.int32), dy
 
 
+# One attention layer of the page-3 model for the training micro-loop
+# (RustingBrain page, "The setup": d_model 768, 12 query heads over 4 KV
+# heads of head_dim 64, batch 4 x 1024 tokens).
+LAYER_PAGE3 = dict(B=4, T=1024, d=768, Hq=12, Hkv=4, D=64, seed=7, w_std=0.02, dy_std=0.1)
+
+
+def make_layer_inputs(B: int, T: int, d: int, Hq: int, Hkv: int, D: int, seed: int,
+                      w_std: float = 0.02, dy_std: float = 0.1):
+    """bf16 CPU tensors X [B, T, d], Wq [d, Hq*D], Wk, Wv [d, Hkv*D],
+    Wo [Hq*D, d] and dY [B, T, d], drawn in that order with ``torch.randn``:
+    X ~ N(0, 1), weights ~ N(0, w_std^2), dY ~ N(0, dy_std^2)."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    shapes = [((B, T, d), 1.0), ((d, Hq * D), w_std), ((d, Hkv * D), w_std),
+              ((d, Hkv * D), w_std), ((Hq * D, d), w_std), ((B, T, d), dy_std)]
+    return tuple((torch.randn(shp, dtype=torch.float32, generator=g) * sd).to(torch.bfloat16)
+                 for shp, sd in shapes)
+
+
 def workload_inputs(w: Workload):
     return make_inputs(w.B, w.T, w.Hq, w.Hkv, w.D, w.seed, w.dout_std, w.k_peak_frac)
 

@@ -10,6 +10,9 @@ describes; the readings (bottom-right causal alignment, rows that see no key)
 are stated in ``attn_oracle.h``.  ``embed_grad`` (``embed_oracle.c``) is the
 gradient of an embedding lookup summed in ascending token order (oxide-train
 README, "The trainer is not bit-identical to itself after step 1").
+``oracle.layer`` (numpy around the attention functions here) is one attention
+layer of a training step: QKV projection, rotary positions, attention, output
+projection, and its closed-form backward.
 
 The arithmetic lives in ``attn_oracle.c`` (plain C, fp64, OpenMP over
 independent heads); this module compiles it with gcc, loads it with ctypes and

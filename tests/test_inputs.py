@@ -124,3 +124,22 @@ def test_embed_grad_oracle_on_generated_inputs():
     onehot[np.arange(2000), ids.numpy()] = 1.0
     ref = onehot.T @ dyf
     assert np.max(np.abs(dw - ref)) <= 1e-12 * np.max(np.abs(ref))
+
+
+def test_layer_inputs_and_the_layer_oracle():
+    """The layer recipe's shapes and spreads, and the layer oracle on its
+    exactly widened bf16 values (a small copy of the page-3 layer)."""
+    from deterministic_attention_gb300.inputs import make_layer_inputs
+    from oracle import layer
+    B, T, d, Hq, Hkv, D = 2, 40, 48, 6, 2, 8
+    t = make_layer_inputs(B, T, d, Hq, Hkv, D, seed=3)
+    assert [tuple(a.shape) for a in t] == [(B, T, d), (d, Hq * D), (d, Hkv * D), (d, Hkv * D),
+                                           (Hq * D, d), (B, T, d)]
+    assert all(a.dtype == torch.bfloat16 for a in t)
+    assert 0.01 < float(t[1].float().std()) < 0.03 and 0.05 < float(t[5].float().std()) < 0.2
+    f = lambda a: oracle.bf16_bits_to_f64(bf16_bits(a)).reshape(tuple(a.shape))
+    x, wq, wk, wv, wo, dy = (f(a) for a in t)
+    y, _ = layer.layer_forward(x, wq, wk, wv, wo, Hq, Hkv, D)
+    grads = layer.layer_backward(x, wq, wk, wv, wo, dy, Hq, Hkv, D)
+    assert y.shape == (B, T, d) and all(np.all(np.isfinite(g)) for g in grads)
+    assert [g.shape for g in grads] == [x.shape, wq.shape, wk.shape, wv.shape, wo.shape]
