@@ -27,6 +27,14 @@ a head's first half and component i of its second half turn together by
 angle t * base^(-2i/D), base 10000.
 
 Matrix products use numpy (a library step); the attention is the C oracle.
+
+The training micro-loop around the layer updates its four weights with AdamW
+(oxide-train README: the trainer's step ends in AdamW, run with LR 3e-4 and
+weight decay 0.1).  The pages give neither betas nor epsilon; the reading
+takes 0.9, 0.999 and 1e-8, with decoupled weight decay:
+
+    m = b1 m + (1 - b1) g,   v = b2 v + (1 - b2) g^2
+    w = w - lr (m / (1 - b1^t) / (sqrt(v / (1 - b2^t)) + eps) + wd w)
 """
 from __future__ import annotations
 
@@ -88,3 +96,32 @@ def layer_backward(x, wq, wk, wv, wo, dy, Hq: int, Hkv: int, D: int, causal: boo
     dwq, dwk, dwv = xf.T @ dq, xf.T @ dk, xf.T @ dvf
     dx = (dq @ wq.T + dk @ wk.T + dvf @ wv.T).reshape(B, T, d)
     return dx, dwq, dwk, dwv, dwo
+
+
+def adamw_step(w, g, m, v, t: int, lr: float = 3e-4, wd: float = 0.1, b1: float = 0.9,
+               b2: float = 0.999, eps: float = 1e-8):
+    """One AdamW update of step t (1-based): returns (w, m, v), new arrays."""
+    w, g, m, v = (np.asarray(a, dtype=np.float64) for a in (w, g, m, v))
+    w = w * (1.0 - lr * wd)
+    m = b1 * m + (1.0 - b1) * g
+    v = b2 * v + (1.0 - b2) * g * g
+    mhat = m / (1.0 - b1 ** t)
+    vhat = v / (1.0 - b2 ** t)
+    return w - lr * mhat / (np.sqrt(vhat) + eps), m, v
+
+
+def train_steps(weights, xs, dys, Hq: int, Hkv: int, D: int, causal: bool = True,
+                lr: float = 3e-4, wd: float = 0.1):
+    """The micro-loop: for each (x, dy) in turn, the layer's weight gradients
+    at the current weights, then one AdamW update of (Wq, Wk, Wv, Wo).
+    Returns the final weights and every step's gradients."""
+    w = [np.asarray(a, dtype=np.float64) for a in weights]
+    m = [np.zeros_like(a) for a in w]
+    v = [np.zeros_like(a) for a in w]
+    grads = []
+    for t, (x, dy) in enumerate(zip(xs, dys), start=1):
+        g = layer_backward(x, *w, dy, Hq, Hkv, D, causal)[1:]
+        grads.append(g)
+        for i in range(4):
+            w[i], m[i], v[i] = adamw_step(w[i], g[i], m[i], v[i], t, lr, wd)
+    return w, grads

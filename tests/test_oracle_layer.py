@@ -124,6 +124,52 @@ def test_layer_matches_torch_autograd(shape):
         assert rel(g, g_t) <= 1e-12, name
 
 
+def test_adamw_matches_torch():
+    """Five AdamW steps on random gradients equal torch.optim.AdamW in fp64
+    (same defaults: betas 0.9, 0.999, eps 1e-8; lr 3e-4, weight decay 0.1)."""
+    w0, gs = _rand(40, 6, 5), [_rand(41 + i, 6, 5) for i in range(5)]
+    p = torch.tensor(w0, dtype=torch.float64, requires_grad=True)
+    opt = torch.optim.AdamW([p], lr=3e-4, weight_decay=0.1)
+    w, m, v = w0, np.zeros_like(w0), np.zeros_like(w0)
+    for t, g in enumerate(gs, start=1):
+        p.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+        w, m, v = layer.adamw_step(w, g, m, v, t)
+        np.testing.assert_allclose(w, p.detach().numpy(), rtol=1e-15, atol=1e-15)
+
+
+def test_adamw_first_step_closed_form():
+    """At t = 1 the corrected moments are g and g^2, so each weight moves by
+    lr * g / (|g| + eps) after its decay."""
+    w0, g = _rand(50, 4, 3), _rand(51, 4, 3)
+    w, _, _ = layer.adamw_step(w0, g, np.zeros_like(g), np.zeros_like(g), 1)
+    np.testing.assert_allclose(w, w0 * (1 - 3e-4 * 0.1) - 3e-4 * g / (np.abs(g) + 1e-8),
+                               rtol=1e-14)
+
+
+def test_train_steps_is_the_composition():
+    """Two micro-loop steps equal gradient, update, gradient, update done by
+    hand; with lr = 0 the weights stay and both steps' gradients are equal."""
+    B, T, d, Hq, Hkv, D = 1, 6, 8, 4, 2, 4
+    x, wq, wk, wv, wo, dy = _layer_case(60, B, T, d, Hq, Hkv, D)
+    x2, dy2 = _rand(70, B, T, d), _rand(71, B, T, d)
+    w, grads = layer.train_steps([wq, wk, wv, wo], [x, x2], [dy, dy2], Hq, Hkv, D)
+    ws = [wq, wk, wv, wo]
+    ms = [np.zeros_like(a) for a in ws]
+    vs = [np.zeros_like(a) for a in ws]
+    for t, (xx, dd) in enumerate(((x, dy), (x2, dy2)), start=1):
+        g = layer.layer_backward(xx, *ws, dd, Hq, Hkv, D)[1:]
+        for a, b in zip(g, grads[t - 1]):
+            assert np.array_equal(a, b)
+        for i in range(4):
+            ws[i], ms[i], vs[i] = layer.adamw_step(ws[i], g[i], ms[i], vs[i], t)
+    for a, b in zip(w, ws):
+        assert np.array_equal(a, b)
+    w0, g0 = layer.train_steps([wq, wk, wv, wo], [x, x], [dy, dy], Hq, Hkv, D, lr=0.0)
+    assert all(np.array_equal(a, b) for a, b in zip(w0, [wq, wk, wv, wo]))
+    assert all(np.array_equal(a, b) for a, b in zip(g0[0], g0[1]))
+
+
 # Planted mistakes in a copy of oracle/layer.py: (name, text, replacement,
 # occurrences).  Each must make at least one pin above fail.
 _LAYER_MUTANTS = [
@@ -137,6 +183,8 @@ _LAYER_MUTANTS = [
     ("dwv_from_dk", "xf.T @ dvf", "xf.T @ dk", 1),
     ("dx_without_v_term", " + dvf @ wv.T", "", 1),
     ("dk_rotated_forward", "dk = rope(dkr, inverse=True)", "dk = rope(dkr, inverse=False)", 1),
+    ("adamw_no_bias_correction", "mhat = m / (1.0 - b1 ** t)", "mhat = m", 1),
+    ("adamw_no_weight_decay", "    w = w * (1.0 - lr * wd)\n", "", 1),
 ]
 
 _LAYER_PINS = [
@@ -146,6 +194,9 @@ _LAYER_PINS = [
     ("fd", test_layer_finite_differences, ()),
     ("torch_a", test_layer_matches_torch_autograd, ((2, 9, 12, 4, 2, 8),)),
     ("torch_b", test_layer_matches_torch_autograd, ((1, 17, 10, 3, 3, 4),)),
+    ("adamw_torch", test_adamw_matches_torch, ()),
+    ("adamw_first", test_adamw_first_step_closed_form, ()),
+    ("loop", test_train_steps_is_the_composition, ()),
 ]
 
 
