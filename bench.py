@@ -219,14 +219,13 @@ def _kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def _graph_time(fn, n_calls, replays):
-    """Captures `n_calls` calls of fn(i) in one CUDA graph, replays it
-    `replays` times and returns the average device ms per call (CUDA events
-    on the replay stream)."""
+def _capture(fn, n_calls):
+    """A CUDA graph holding fn(0) .. fn(n_calls - 1), captured after one
+    uncaptured pass (kernel attributes, descriptors, the side stream)."""
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
-        for i in range(n_calls):  # warm up outside capture (kernel attributes, descriptors)
+        for i in range(n_calls):
             fn(i)
     torch.cuda.current_stream().wait_stream(stream)
     torch.cuda.synchronize()
@@ -234,16 +233,57 @@ def _graph_time(fn, n_calls, replays):
     with torch.cuda.graph(g):
         for i in range(n_calls):
             fn(i)
-    for _ in range(2):
-        g.replay()
+    g.replay()
     torch.cuda.synchronize()
+    return g
+
+
+class GraphRunner:
+    """Exactly `k` calls of fn(i) (i cycling over `n_sets` input sets) from
+    CUDA graphs: one graph of n_sets calls replayed k // n_sets times, then one
+    of the k % n_sets remaining calls."""
+
+    def __init__(self, fn, n_sets, k):
+        self.full, self.rem = divmod(k, n_sets)
+        self.g_full = _capture(fn, n_sets) if self.full else None
+        self.g_rem = _capture(fn, self.rem) if self.rem else None
+        self.k = k
+
+    def run(self):
+        for _ in range(self.full):
+            self.g_full.replay()
+        if self.g_rem is not None:
+            self.g_rem.replay()
+
+
+def _event_ms(run, world=1):
+    """Device time of run() in ms: CUDA events on the current stream, with a
+    barrier and a synchronize on both sides."""
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
     a.record()
-    for _ in range(replays):
-        g.replay()
+    run()
     b.record()
     torch.cuda.synchronize()
-    return a.elapsed_time(b) / (replays * n_calls), g
+    _barrier(world)
+    return a.elapsed_time(b)
+
+
+def _trials(run, k, n_trials=5, world=1, spread_limit=0.05):
+    """n_trials timings of run() (k steps each) as ms per step, max over
+    ranks per trial.  A set whose spread ((max - min) / median) exceeds
+    spread_limit is taken once more (shared GPU); the second set is kept."""
+    def one_set():
+        return [_max_over_ranks(_event_ms(run, world) / k, world) for _ in range(n_trials)]
+    ms = one_set()
+    repeated = False
+    med = sorted(ms)[len(ms) // 2]
+    if (max(ms) - min(ms)) / med > spread_limit:
+        ms, repeated = one_set(), True
+        med = sorted(ms)[len(ms) // 2]
+    return {"n": n_trials, "steps_each": k, "ms_per_step": ms, "median": med, "min": min(ms),
+            "max": max(ms), "spread": (max(ms) - min(ms)) / med, "repeated": repeated}
 
 
 def run_gpu_arm(args, world, rank):
@@ -278,39 +318,35 @@ def run_gpu_arm(args, world, rank):
         P.step(i)
     torch.cuda.synchronize()
 
-    # Timed region: the K steps (fwd + Delta + dK/dV + dQ) replayed from one
-    # CUDA graph holding one step per rotating input set.
-    replays = max(1, math.ceil(args.steps / n_sets))
-    K = replays * n_sets
+    # Timed region: exactly K steps (fwd + Delta + dK/dV + dQ each), replayed
+    # from CUDA graphs holding one step per rotating input set; five trials.
+    K = args.steps
+    runner = GraphRunner(P.step, n_sets, K)
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
     time.sleep(0.25)
-    _barrier(world)
-    torch.cuda.synchronize()
     t0 = time.perf_counter()
-    step_ms, graph = _graph_time(P.step, n_sets, replays)
+    trials = _trials(runner.run, K, world=world)
     wall = time.perf_counter() - t0
-    _barrier(world)
     clocks = sampler.stop()
     da.check_status()
-    ms_step = _max_over_ranks(step_ms, world)
+    ms_step = trials["median"]
 
-    # Each kernel alone, K launches from a graph, for the per-kernel roofline.
+    # Each kernel alone, K launches from graphs, for the per-kernel roofline.
     kernels = {"attn_fwd": lambda i: P.kernel("fwd", i), "attn_bwd_delta": lambda i: P.kernel("delta", i),
                "attn_bwd_dkdv": lambda i: P.kernel("dkdv", i), "attn_bwd_dq": lambda i: P.kernel("dq", i)}
     per_kernel_ms = {}
     for n, fn in kernels.items():
-        per_kernel_ms[n], _ = _graph_time(fn, n_sets, replays)
+        kr = GraphRunner(fn, n_sets, K)
+        per_kernel_ms[n] = _trials(kr.run, K, n_trials=3)["median"]
+        del kr
 
-    # The same steps launched one by one on the stream (no graph).
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-    torch.cuda.synchronize()
-    evs[0].record()
-    for i in range(K):
-        P.step_api(i)
-    evs[1].record()
-    torch.cuda.synchronize()
-    stream_ms = evs[0].elapsed_time(evs[1]) / K
+    # The same K steps launched one by one on the stream (no graph).
+    def stream_run():
+        for i in range(K):
+            P.step_api(i)
+    stream_trials = _trials(stream_run, K, world=world)
+    stream_ms = stream_trials["median"]
 
     flops = w.fwd_bwd_flops()
     value = world * flops / (ms_step * 1e-3) / 1e12
@@ -405,13 +441,19 @@ def run_gpu_arm(args, world, rank):
                    "dout_std": w.dout_std,
                    "l2": f"{n_sets} rotating input/output sets of {per_set / 2**20:.1f} MiB "
                          f"({n_sets * per_set / 2**20:.0f} MiB vs 129 MiB L2)",
-                   "launch": f"CUDA graph of {n_sets} steps (attn_fwd + attn_bwd, 4 kernels each), "
-                             f"replayed {replays}x",
+                   "launch": f"CUDA graphs: {n_sets} steps (attn_fwd + attn_bwd, 4 kernels each) "
+                             f"replayed {runner.full}x, then {runner.rem} steps; exactly {K} steps "
+                             f"per trial, median of {trials['n']} trials",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "flop_convention": "fwd 2*B*Hq*T^2*D (causal half), fwd+bwd 3.5x fwd"},
         "pct_of_peak": value / world / peak,
         "fwd_tflops": world * w.fwd_flops() / (per_kernel_ms["attn_fwd"] * 1e-3) / 1e12,
-        "stream_launch": {"value": world * flops / (stream_ms * 1e-3) / 1e12, "ms_per_step": stream_ms},
+        "trials": {**trials, "value_median": value,
+                   "value_min": world * flops / (trials["max"] * 1e-3) / 1e12,
+                   "value_max": world * flops / (trials["min"] * 1e-3) / 1e12},
+        "stream_launch": {"value": world * flops / (stream_ms * 1e-3) / 1e12, "ms_per_step": stream_ms,
+                          "trials": stream_trials,
+                          "note": "the same K steps launched one by one through attn_fwd + attn_bwd"},
         "kernels_ms": per_kernel_ms,
         "kernel_rates": kernel_rates,
         "roofline": roof,

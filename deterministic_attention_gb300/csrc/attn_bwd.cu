@@ -1310,22 +1310,26 @@ __global__ void wait_timeout_selftest_kernel(unsigned long long limit_ns) {
   if (!mbar_wait(smem_u32(&bar), 0, limit_ns)) atomicOr(&g_bwd_status, 8u);
 }
 
+// Sets the kernel's dynamic shared-memory limit once per device and context
+// (the attribute belongs to the context's copy of the kernel, so a re-created
+// context needs it again).  done[dev] holds the context id it was set for.
 template <typename K>
-cudaError_t set_smem_once(K kernel, int bytes, bool* done) {
+cudaError_t set_smem_once(K kernel, int bytes, unsigned long long* done) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !done[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (dev >= 64 || ctx == 0 || done[dev] != ctx) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
-    done[dev] = true;
+    if (dev < 64) done[dev] = current_context_id();
   }
   return cudaSuccess;
 }
 
 template <int D>
 cudaError_t dkdv_max_clusters_t(int c, int* out) {
-  static bool done[64] = {};
+  static unsigned long long done[64] = {};
   cudaError_t e = set_smem_once(attn_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1346,7 +1350,7 @@ template <int D>
 cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                           bool dependent, cudaStream_t st) {
-  static bool done[64] = {};
+  static unsigned long long done[64] = {};
   cudaError_t e = set_smem_once(attn_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1379,7 +1383,7 @@ template <int D>
 cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                         const QTileSched& sched, cudaStream_t st) {
-  static bool done[64] = {};
+  static unsigned long long done[64] = {};
   cudaError_t e = set_smem_once(attn_dq_kernel<D>, DqCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   attn_dq_kernel<D><<<grid, kDqPipeThreads * DqCfg<D>::NP, DqCfg<D>::kSmemBytes, st>>>(

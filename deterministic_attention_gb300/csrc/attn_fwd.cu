@@ -499,15 +499,17 @@ cudaError_t launch_fwd_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const FwdArgs& a, const QTileSched& sched,
                          cudaStream_t st) {
   const int smem = Cfg<D>::kSmemBytes;
-  static bool attr_set[64] = {};
+  // Once per device and context (holds the context id it was set for).
+  static unsigned long long attr_ctx[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 64 && !attr_set[dev]) {
+  const unsigned long long ctx = current_context_id();
+  if (dev >= 64 || ctx == 0 || attr_ctx[dev] != ctx) {
     e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (dev < 64) attr_ctx[dev] = current_context_id();
   }
   attn_fwd_kernel<D><<<grid, kPipeThreads * Cfg<D>::NP, smem, st>>>(mq, mk, mv, a, sched);
   return cudaGetLastError();

@@ -115,6 +115,13 @@ cudaError_t launch_wait_timeout_selftest(unsigned long long limit_ns, cudaStream
 cudaError_t launch_exp2_diag(const float* x, float* y_poly, float* y_pair, float* y_sfu, int n,
                              cudaStream_t st);
 
+// Unique id (cuCtxGetId) of the CUDA context current on the calling thread,
+// or 0 when none is current or the driver cannot say.  Per-device caches of
+// context-bound state (function attributes, streams, symbol addresses) are
+// keyed on it, so that they are rebuilt after the context is destroyed and
+// re-created (cudaDeviceReset, or a primary-context reset by another module).
+unsigned long long current_context_id();
+
 // Read-and-clear of the device status words the kernels set when a bounded
 // wait runs out (synchronous on `st`).  Returns the OR of the words.
 cudaError_t take_fwd_status(cudaStream_t st, unsigned* out);

@@ -417,6 +417,7 @@ int check_workspace(const void* ws, size_t bytes, int B, int T, int Hq) {
 struct SideStream {
   cudaStream_t stream = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
+  unsigned long long ctx = 0;  // id of the context the handles belong to
 };
 
 int side_stream(SideStream** out) {
@@ -428,6 +429,10 @@ int side_stream(SideStream** out) {
   if (dev >= 64) return fail(DETATTN_ERR_CUDA, "device index %d too large", dev);
   std::lock_guard<std::mutex> lock(mu);
   SideStream& ss = per_dev[dev];
+  // Handles of a context that has since been destroyed (device reset) are
+  // dropped, not destroyed: they went with it.
+  const unsigned long long ctx = current_context_id();
+  if (ss.stream != nullptr && ctx != 0 && ss.ctx != ctx) ss = SideStream{};
   if (ss.stream == nullptr) {
     e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
@@ -436,6 +441,7 @@ int side_stream(SideStream** out) {
       ss = SideStream{};
       return fail(DETATTN_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
     }
+    ss.ctx = current_context_id();
   }
   *out = &ss;
   return DETATTN_OK;
@@ -473,7 +479,10 @@ int bwd_steps(const void* q, const void* k, const void* v, const void* o, const 
 // that cannot allocate device memory still get the backward.  Every GPU that
 // loads this library holds it (8 MiB) until the process exits.  In host code
 // the name is only a host-side stand-in; its device address comes from
-// cudaGetSymbolAddress, looked up once per device with that device current.
+// cudaGetSymbolAddress, looked up once per device and context with that
+// device current.  The context is part of the key: after a device reset the
+// library's module is loaded again and the array may sit elsewhere, and an
+// address kept from the old context would send the kernels' stores there.
 constexpr size_t kNoallocMaxPairs = size_t(1) << 20;
 static __device__ __align__(256) float2 g_noalloc_rowstats[kNoallocMaxPairs];
 
@@ -481,11 +490,16 @@ int noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  static void* cached[64] = {};
+  struct Entry {
+    unsigned long long ctx;
+    void* ptr;
+  };
+  static Entry cached[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
-  if (dev < 64 && cached[dev] != nullptr) {
-    *out = cached[dev];
+  const unsigned long long ctx = current_context_id();
+  if (dev < 64 && ctx != 0 && cached[dev].ctx == ctx && cached[dev].ptr != nullptr) {
+    *out = cached[dev].ptr;
     return DETATTN_OK;
   }
   void* ptr = nullptr;
@@ -493,12 +507,40 @@ int noalloc_scratch(void** out) {
   if (e != cudaSuccess || ptr == nullptr)
     return fail(DETATTN_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch: %s",
                 cudaGetErrorString(e));
-  if (dev < 64) cached[dev] = ptr;
+  // The lookup made the device's context current if it was not yet.
+  if (dev < 64) cached[dev] = Entry{current_context_id(), ptr};
   *out = ptr;
   return DETATTN_OK;
 }
 
 }  // namespace
+
+namespace detattn {
+
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", reinterpret_cast<void**>(&get_current),
+                                         4000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      get_current = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", reinterpret_cast<void**>(&get_id), 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      get_id = nullptr;
+  });
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+}  // namespace detattn
 
 extern "C" {
 

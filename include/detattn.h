@@ -123,8 +123,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
  * B * Hq * Tp must not exceed 1,048,576 (Tp = T rounded up to 128); larger
  * problems return DETATTN_ERR_WORKSPACE without launching anything.  This
  * call never allocates memory.  Its first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every call shares the one
+ * array's device address (cudaGetSymbolAddress) with that device current,
+ * and so does the first call after that device's context was re-created
+ * (cudaDeviceReset loads the library's module anew, and the array may then
+ * sit elsewhere); make such a first call before any stream capture.  Every call shares the one
  * array: each call overwrites all the statistics it reads before reading
  * them, so nothing needs to start at zero, but calls that overlap on the GPU
  * (on different streams, or different host threads without ordering) race
