@@ -468,6 +468,255 @@ def run_gpu_arm(args, world, rank):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ embedding gradient
+EMBED_WORKLOADS = ("embed_uniform", "embed_zipf")
+
+
+def run_embed_arm(args, world, rank):
+    """The deterministic embedding-lookup gradient at the trainer's shape
+    (32 x 1024 tokens, 50,432 x 1536 table): HBM GB/s of its algorithmic bytes
+    (ids and dY read once, dW written once)."""
+    import deterministic_attention_gb300 as da
+    from deterministic_attention_gb300.inputs import EMBED_GRAD, make_embed_grad_inputs
+    da.build()
+    w = EMBED_GRAD
+    dist = args.workload.split("_", 1)[1]
+    N, V, E = w["N"], w["V"], w["E"]
+    ids_h, dy_h = make_embed_grad_inputs(N, w["V_used"], E, w["seed"], dist)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ids, dy = ids_h.to(dev), dy_h.to(dev)
+    dw = torch.empty((V, E), dtype=torch.float32, device=dev)
+    ws = torch.empty(da.embed_grad_workspace_bytes(N, V, E), dtype=torch.uint8, device=dev)
+    digests = set()
+    for _ in range(20):
+        da.embed_grad(ids, dy, V, dw=dw, workspace=ws)
+        torch.cuda.synchronize()
+        digests.add(hashlib.sha256(dw.view(torch.uint8).cpu().numpy().tobytes()).hexdigest())
+    da.check_status()
+    if len(digests) != 1:
+        raise SystemExit(json.dumps({"error": "embed_grad outputs differ between identical runs"}))
+    for _ in range(args.warmup):
+        da.embed_grad(ids, dy, V, dw=dw, workspace=ws)
+    torch.cuda.synchronize()
+    K = args.steps
+    runner = GraphRunner(lambda i: da.embed_grad(ids, dy, V, dw=dw, workspace=ws), 1, K)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.25)
+    trials = _trials(runner.run, K, world=world)
+    clocks = sampler.stop()
+    da.check_status()
+    ms = trials["median"]
+    algo_bytes = N * 4 + N * E * 2 + V * E * 4
+    gbs = world * algo_bytes / (ms * 1e-3) / 1e9
+    peaks = _peaks()
+    # End to end: ids and dY copied in from pinned host memory, dW read back.
+    ids_p, dy_p = ids_h.pin_memory(), dy_h.pin_memory()
+    dw_p = torch.empty((V, E), dtype=torch.float32, pin_memory=True)
+    n_e2e = max(3, min(K, 50))
+
+    def e2e_run():
+        for _ in range(n_e2e):
+            ids.copy_(ids_p, non_blocking=True)
+            dy.copy_(dy_p, non_blocking=True)
+            da.embed_grad(ids, dy, V, dw=dw, workspace=ws)
+            dw_p.copy_(dw, non_blocking=True)
+    e2e_run()
+    e2e_ms = _max_over_ranks(_event_ms(e2e_run, world) / n_e2e, world)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        from deterministic_attention_gb300.inputs import bf16_bits
+        dyf = oracle.bf16_bits_to_f64(bf16_bits(dy_h)).reshape(N, E)
+        idn = ids_h.numpy()
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < args.cpu_budget / 2 or reps == 0:
+            oracle.embed_grad(idn, dyf, V)
+            reps += 1
+        dt = (time.perf_counter() - t0) / reps
+        cpu = {"value": algo_bytes / dt / 1e9, "unit": "GB/s", "cores": oracle.num_threads(),
+               "kind": "oracle", "sample": f"the whole workload in fp64, run {reps} times"}
+    line = {
+        "metric": "deterministic embedding-lookup gradient, algorithmic HBM GB/s; bitwise run-to-run repro",
+        "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 (bf16 dY)", "data": "synthetic",
+        "config": {"workload": f"embed_grad_n{N}_v{V}_e{E}_{dist}", "N": N, "V": V,
+                   "V_used": w["V_used"], "E": E, "ids": dist, "seed": w["seed"],
+                   "l2": f"{(N * E * 2 + V * E * 4) / 2**20:.0f} MiB of dY and dW per call vs 129 MiB L2",
+                   "launch": "CUDA graph of one call (a memset and 6 kernels), replayed; "
+                             f"exactly {K} calls per trial, median of {trials['n']} trials"},
+        "trials": trials,
+        "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": gbs / world / peaks["hbm_gbs"], "kernel": "embed_grad (whole call)",
+                     "peak_source": f"{peaks['source']} (copy)", "traffic": None,
+                     "algorithmic_bytes": algo_bytes},
+        "repro": {"runs": 20, "sha256_identical": True},
+        "e2e": {"value": world * algo_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": N * 4 + N * E * 2,
+                "d2h_bytes_per_step": V * E * 4, "steps": n_e2e},
+        "cpu_baseline": cpu, "clocks": clocks, "gpu_launches": 6 * K,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ packed varlen batch
+def run_varlen_arm(args, world, rank):
+    """attn_fwd_varlen + attn_bwd_varlen on the 4,096-token packed batch next
+    to page3 (sequences of 64..1,024 tokens, seed 5): TFLOPS over the exact
+    visible (query, key) pairs, fwd + bwd = 3.5 x fwd."""
+    import deterministic_attention_gb300 as da
+    from deterministic_attention_gb300.inputs import (VARLEN_PAGE3, varlen_fwd_flops,
+                                                      varlen_page3_inputs)
+    da.build()
+    w = VARLEN_PAGE3
+    q, k, v, do, cu_q, cu_k = varlen_page3_inputs()
+    tqs = [int(cu_q[i + 1] - cu_q[i]) for i in range(len(cu_q) - 1)]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    per_set = 2 * (3 * q.numel() + 3 * k.numel()) * 2 + 4 * q.shape[0] * q.shape[1]
+    n_sets = max(1, math.ceil(1.5 * L2_BYTES / per_set))
+    sets = []
+    for _ in range(n_sets):
+        ins = [t.to(dev) for t in (q, k, v, do)]
+        outs = [torch.empty_like(ins[0]), torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32,
+                                                      device=dev),
+                torch.empty_like(ins[0]), torch.empty_like(ins[1]), torch.empty_like(ins[2]),
+                torch.empty(da.varlen_workspace_bytes(cu_q, cu_k, w["Hq"], w["Hkv"], w["D"]),
+                            dtype=torch.uint8, device=dev)]
+        sets.append((ins, outs))
+
+    def step(i):
+        (qd, kd, vd, dod), (o, lse, dq, dk, dv, ws) = sets[i % n_sets]
+        da.attn_fwd_varlen(qd, kd, vd, cu_q, cu_k, out=o, lse=lse)
+        da.attn_bwd_varlen(qd, kd, vd, o, lse, dod, cu_q, cu_k, dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    digests = set()
+    for _ in range(20):
+        step(0)
+        torch.cuda.synchronize()
+        digests.add(tuple(hashlib.sha256(t.contiguous().view(torch.uint8).cpu().numpy().tobytes())
+                          .hexdigest() for t in sets[0][1][:5]))
+    da.check_status()
+    if len(digests) != 1:
+        raise SystemExit(json.dumps({"error": "varlen outputs differ between identical runs"}))
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    K = args.steps
+    runner = GraphRunner(step, n_sets, K)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.25)
+    trials = _trials(runner.run, K, world=world)
+    clocks = sampler.stop()
+    da.check_status()
+    fwd = varlen_fwd_flops(tqs, tqs, w["Hq"], w["D"], True)
+    flops = 3.5 * fwd
+    ms = trials["median"]
+    value = world * flops / (ms * 1e-3) / 1e12
+    peaks = _peaks()
+    line = {
+        "metric": "packed varlen causal attn fwd+bwd TFLOPS (exact visible pairs); bitwise run-to-run repro",
+        "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"varlen_page3_{w['total']}tok_{len(tqs)}seq", "lengths": tqs,
+                   "Hq": w["Hq"], "Hkv": w["Hkv"], "D": w["D"], "causal": True, "seed": w["seed"],
+                   "flop_convention": "4*Hq*D per visible (query, key) pair forward, fwd+bwd 3.5x",
+                   "l2": f"{n_sets} rotating sets of {per_set / 2**20:.1f} MiB",
+                   "launch": f"CUDA graphs, exactly {K} steps per trial, median of {trials['n']}"},
+        "trials": trials, "pct_of_peak": value / world / peaks["bf16_tflops"],
+        "roofline": {"bound": "tensor", "achieved": value / world, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": value / world / peaks["bf16_tflops"],
+                     "kernel": "whole step (fwd + Delta + dK/dV + dQ)", "traffic": None,
+                     "peak_source": f"{peaks['source']} (burst)"},
+        "repro": {"runs": 20, "sha256_identical": True}, "clocks": clocks, "gpu_launches": 4 * K,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ training micro-loop
+def run_layer_arm(args, world, rank):
+    """One attention layer of the page-3 model trained with AdamW:
+    layer_train_step (six GEMMs, rotary positions, attention fwd + bwd,
+    AdamW) at B = 4, T = 1024, d = 768.  Tokens per second, and TFLOPS of
+    its algorithmic work (GEMMs 2 M N K each, attention 3.5 x 2 B Hq T^2 D)."""
+    import deterministic_attention_gb300 as da
+    from deterministic_attention_gb300.inputs import LAYER_PAGE3, make_layer_inputs
+    da.build()
+    w = LAYER_PAGE3
+    B, T, d, Hq, Hkv, D = (w[k] for k in ("B", "T", "d", "Hq", "Hkv", "D"))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    n_sets = 4
+    xs, dys = [], []
+    for s in range(n_sets):
+        x, wq, wk, wv, wo, dy = make_layer_inputs(B, T, d, Hq, Hkv, D, seed=w["seed"] + 1 + s)
+        xs.append(x.to(dev))
+        dys.append(dy.to(dev))
+    _, wq, wk, wv, wo, _ = make_layer_inputs(B, T, d, Hq, Hkv, D, seed=w["seed"])
+
+    def run_steps(n, st):
+        for i in range(n):
+            da.layer_train_step(st, xs[i % n_sets], dys[i % n_sets])
+
+    ref = None
+    for _ in range(2):
+        st = da.LayerState(wq, wk, wv, wo, B, T, Hq, Hkv, D, device=dev)
+        digests = []
+        for i in range(5):
+            g_qkv, g_o = da.layer_train_step(st, xs[i % n_sets], dys[i % n_sets])
+            torch.cuda.synchronize()
+            digests.append((hashlib.sha256(g_qkv.view(torch.uint8).cpu().numpy().tobytes()).hexdigest(),
+                            hashlib.sha256(g_o.view(torch.uint8).cpu().numpy().tobytes()).hexdigest()))
+        ref = ref or digests
+        if digests != ref:
+            raise SystemExit(json.dumps({"error": "layer gradients differ between identical runs"}))
+    da.check_status()
+    st = da.LayerState(wq, wk, wv, wo, B, T, Hq, Hkv, D, device=dev)
+    run_steps(args.warmup, st)
+    torch.cuda.synchronize()
+    K = args.steps
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.25)
+    trials = _trials(lambda: run_steps(K, st), K, world=world)
+    clocks = sampler.stop()
+    da.check_status()
+    ms = trials["median"]
+    BT, N3, HqD = B * T, (Hq + 2 * Hkv) * D, Hq * D
+    gemm_flops = 2.0 * (BT * N3 * d + BT * d * HqD + BT * HqD * d + HqD * d * BT + d * N3 * BT
+                        + BT * d * N3)
+    attn_flops = 3.5 * 2.0 * B * Hq * T * T * D
+    flops = gemm_flops + attn_flops
+    peaks = _peaks()
+    tflops = world * flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "one-layer training step (QKV proj, RoPE, causal GQA attn fwd+bwd, out proj, "
+                  "AdamW) tokens/s; bitwise run-to-run repro of the weight gradients",
+        "value": world * BT / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (fp32 master weights)", "data": "synthetic",
+        "config": {"workload": f"layer_page3_b{B}_t{T}_d{d}_hq{Hq}_hkv{Hkv}_d{D}", "B": B, "T": T,
+                   "d": d, "Hq": Hq, "Hkv": Hkv, "D": D, "lr": 3e-4, "weight_decay": 0.1,
+                   "l2": f"{n_sets} rotating (x, dy) sets of {2 * BT * d * 2 / 2**20:.1f} MiB; weights "
+                         "and intermediates stay resident (a training step reads them hot)",
+                   "launch": f"stream launches, exactly {K} steps per trial, median of {trials['n']}"},
+        "tflops": tflops, "flops_per_step": {"gemm": gemm_flops, "attention": attn_flops},
+        "trials": trials,
+        "roofline": {"bound": "tensor", "achieved": tflops / world, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": tflops / world / peaks["bf16_tflops"],
+                     "kernel": "whole step", "traffic": None,
+                     "peak_source": f"{peaks['source']} (burst)"},
+        "repro": {"steps": 5, "runs": 2, "sha256_identical": True}, "clocks": clocks,
+        "gpu_launches": 15 * K,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ CPU oracle
 def _oracle_sample(w, T_s, n_groups, n_batches=1):
     """fp64 inputs of a bounded sample: batches 0..n_batches-1, KV groups
@@ -530,11 +779,98 @@ def cpu_baseline(w, budget_s=20.0):
                       f"fwd + bwd in fp64, run {reps} times"}
 
 
+def run_embed_reference_arm(args, world):
+    """The fp64 oracle of the embedding-lookup gradient on the host cores, on
+    the whole workload each step."""
+    import oracle
+    from deterministic_attention_gb300.inputs import EMBED_GRAD, bf16_bits, make_embed_grad_inputs
+    oracle.build()
+    w = EMBED_GRAD
+    dist = args.workload.split("_", 1)[1]
+    N, V, E = w["N"], w["V"], w["E"]
+    ids, dy = make_embed_grad_inputs(N, w["V_used"], E, w["seed"], dist)
+    dyf = oracle.bf16_bits_to_f64(bf16_bits(dy)).reshape(N, E)
+    idn = ids.numpy()
+    for _ in range(args.warmup):
+        oracle.embed_grad(idn, dyf, V)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.embed_grad(idn, dyf, V)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    algo_bytes = N * 4 + N * E * 2 + V * E * 4
+    value = algo_bytes / dt / 1e9
+    line = {
+        "metric": "deterministic embedding-lookup gradient, algorithmic HBM GB/s; bitwise run-to-run repro",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": f"embed_grad_n{N}_v{V}_e{E}_{dist}", "N": N, "V": V, "E": E},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": "the whole workload in fp64 per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_other_reference_arm(args, world):
+    """The oracle of the packed varlen step or of the layer step on the host
+    cores, on the whole workload each step."""
+    import oracle
+    from deterministic_attention_gb300.inputs import (LAYER_PAGE3, VARLEN_PAGE3, bf16_bits,
+                                                      make_layer_inputs, varlen_fwd_flops,
+                                                      varlen_page3_inputs)
+    f = lambda t: oracle.bf16_bits_to_f64(bf16_bits(t)).reshape(tuple(t.shape))
+    if args.workload == "varlen":
+        w = VARLEN_PAGE3
+        q, k, v, do, cu_q, cu_k = varlen_page3_inputs()
+        tqs = [int(cu_q[i + 1] - cu_q[i]) for i in range(len(cu_q) - 1)]
+        qf, kf, vf, dof = (f(t) for t in (q, k, v, do))
+        scale = 1.0 / math.sqrt(w["D"])
+
+        def step():
+            oracle.attn_fwd_varlen(qf, kf, vf, cu_q, cu_k, scale, True)
+            oracle.attn_bwd_varlen(qf, kf, vf, dof, cu_q, cu_k, scale, True)
+        work, unit = 3.5 * varlen_fwd_flops(tqs, tqs, w["Hq"], w["D"], True) / 1e12, "TFLOPS"
+        name = f"varlen_page3_{w['total']}tok_{len(tqs)}seq"
+    else:
+        from oracle import layer
+        w = LAYER_PAGE3
+        B, T, d, Hq, Hkv, D = (w[k] for k in ("B", "T", "d", "Hq", "Hkv", "D"))
+        x, wq, wk, wv, wo, dy = (f(t) for t in make_layer_inputs(B, T, d, Hq, Hkv, D, w["seed"]))
+
+        def step():
+            layer.train_steps([wq, wk, wv, wo], [x], [dy], Hq, Hkv, D)
+        work, unit = B * T, "tokens/s"
+        name = f"layer_page3_b{B}_t{T}_d{d}_hq{Hq}_hkv{Hkv}_d{D}"
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    value = work / dt
+    line = {"metric": f"oracle {args.workload} step", "value": value, "unit": unit,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference", "config": {"workload": name},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": "the whole workload in fp64 per step"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference_arm(args, world, rank):
     if rank != 0:
         return
     import oracle
     oracle.build()
+    if args.workload in EMBED_WORKLOADS:
+        run_embed_reference_arm(args, world)
+        return
+    if args.workload in ("varlen", "layer"):
+        run_other_reference_arm(args, world)
+        return
     w = WORKLOADS[args.workload]
     # Size the per-step sample (a causal prefix, over every batch and KV group
     # so that every host thread has work) so the whole run stays within a few
@@ -579,7 +915,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="page3", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="page3",
+                    choices=sorted(WORKLOADS) + list(EMBED_WORKLOADS) + ["varlen", "layer"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -590,6 +927,12 @@ def main():
     try:
         if args.impl == "reference":
             run_reference_arm(args, world, rank)
+        elif args.workload in EMBED_WORKLOADS:
+            run_embed_arm(args, world, rank)
+        elif args.workload == "varlen":
+            run_varlen_arm(args, world, rank)
+        elif args.workload == "layer":
+            run_layer_arm(args, world, rank)
         else:
             run_gpu_arm(args, world, rank)
     finally:

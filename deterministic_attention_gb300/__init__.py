@@ -23,12 +23,15 @@ from .build import LIB as _LIB_PATH, build  # noqa: F401
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_delta", "attn_bwd_dkdv", "attn_bwd_dq",
            "workspace_bytes", "check_status", "set_wait_limit_ns", "selftest_wait_timeout",
            "set_dkdv_split", "new_workspace", "rowstats_view", "last_error", "lib",
-           "DetAttnError", "STATUS", "header_symbols", "build"]
+           "DetAttnError", "STATUS", "header_symbols", "build", "embed_grad",
+           "embed_grad_workspace_bytes", "attn_fwd_varlen", "attn_bwd_varlen",
+           "varlen_workspace_bytes", "layer_gemm", "layer_workspace_bytes", "LayerState",
+           "layer_train_step"]
 
 STATUS = {0: "DETATTN_OK", -1: "DETATTN_ERR_NULL", -2: "DETATTN_ERR_ALIGN",
           -3: "DETATTN_ERR_SHAPE", -4: "DETATTN_ERR_HEADDIM", -5: "DETATTN_ERR_SCALE",
           -6: "DETATTN_ERR_CUDA", -7: "DETATTN_ERR_DEVICE_TIMEOUT", -8: "DETATTN_ERR_ARCH",
-          -9: "DETATTN_ERR_WORKSPACE"}
+          -9: "DETATTN_ERR_WORKSPACE", -10: "DETATTN_ERR_INDEX"}
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                       "include", "detattn.h")
@@ -61,6 +64,23 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd_delta.argtypes = [vp, vp, fp, vp, sz, i, i, i, i, vp]
     L.attn_bwd_dkdv.argtypes = [vp, vp, vp, vp, vp, sz, vp, vp, i, i, i, i, i, f, i, vp]
     L.attn_bwd_dq.argtypes = [vp, vp, vp, vp, vp, sz, vp, i, i, i, i, i, f, i, vp]
+    L.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, fp, vp, vp, i, i, i, i, f, i, vp]
+    L.attn_fwd_varlen.restype = i
+    L.attn_bwd_varlen_workspace_bytes.argtypes = [vp, vp, i, i, i, i]
+    L.attn_bwd_varlen_workspace_bytes.restype = sz
+    L.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, sz, vp, vp, i, i, i, i, f,
+                                  i, vp]
+    L.attn_bwd_varlen.restype = i
+    L.layer_gemm.argtypes = [vp, i, i, vp, i, i, vp, i, i, i, i, i, f, vp]
+    L.layer_gemm.restype = i
+    L.layer_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    L.layer_workspace_bytes.restype = sz
+    L.layer_train_step.argtypes = [vp] * 15 + [sz] + [i] * 7 + [f] * 5 + [vp]
+    L.layer_train_step.restype = i
+    L.embed_grad_workspace_bytes.argtypes = [i, i, i]
+    L.embed_grad_workspace_bytes.restype = sz
+    L.embed_grad.argtypes = [vp, vp, vp, vp, sz, i, i, i, vp]
+    L.embed_grad.restype = i
     L.detattn_check_status.argtypes = [vp]
     L.detattn_diag_exp2.argtypes = [vp, vp, vp, vp, i, vp]
     L.detattn_diag_exp2.restype = i
@@ -220,6 +240,158 @@ def attn_bwd_dq(q, k, v, dout, workspace, scale=None, causal=True, dq=None):
                              workspace.numel(), _ptr(dq), B, T, Hq, Hkv, D, _scale(scale, D),
                              int(bool(causal)), _stream()), "attn_bwd_dq")
     return dq
+
+
+def _host_cu(cu):
+    """Offsets as a contiguous host int32 array (kept alive by the caller)."""
+    import numpy as np
+    if isinstance(cu, torch.Tensor):
+        cu = cu.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(cu, dtype=np.int32).reshape(-1))
+
+
+def varlen_workspace_bytes(cu_q, cu_k, Hq, Hkv, D) -> int:
+    cq, ck = _host_cu(cu_q), _host_cu(cu_k)
+    return int(lib().attn_bwd_varlen_workspace_bytes(ctypes.c_void_p(cq.ctypes.data),
+                                                     ctypes.c_void_p(ck.ctypes.data),
+                                                     cq.size - 1, Hq, Hkv, D))
+
+
+def attn_fwd_varlen(q, k, v, cu_q, cu_k, scale=None, causal=True, out=None, lse=None):
+    """Packed variable-length forward: q [total_q, Hq, D], k, v [total_k, Hkv,
+    D]; sequence s is query rows cu_q[s]..cu_q[s+1]-1 and key rows
+    cu_k[s]..cu_k[s+1]-1 (cu_q, cu_k on the host).  Returns o [total_q, Hq,
+    D] and lse fp32 [Hq, total_q] (-inf for rows that see no key)."""
+    Nq, Hq, D = q.shape
+    Nk, Hkv = k.shape[0], k.shape[1]
+    bf = torch.bfloat16
+    _need(q, "q", bf, (Nq, Hq, D))
+    _need(k, "k", bf, (Nk, Hkv, D))
+    _need(v, "v", bf, (Nk, Hkv, D))
+    o = torch.empty_like(q) if out is None else out
+    l = torch.empty((Hq, Nq), dtype=torch.float32, device=q.device) if lse is None else lse
+    _need(o, "o", bf, (Nq, Hq, D))
+    _need(l, "lse", torch.float32, (Hq, Nq))
+    cq, ck = _host_cu(cu_q), _host_cu(cu_k)
+    rc = lib().attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(l),
+                               ctypes.c_void_p(cq.ctypes.data), ctypes.c_void_p(ck.ctypes.data),
+                               cq.size - 1, Hq, Hkv, D, _scale(scale, D), int(bool(causal)),
+                               _stream())
+    _check(rc, "attn_fwd_varlen")
+    return o, l
+
+
+def attn_bwd_varlen(q, k, v, o, lse, dout, cu_q, cu_k, scale=None, causal=True, dq=None,
+                    dk=None, dv=None, workspace=None):
+    """Packed variable-length backward: (dq, dk, dv) in the layouts of q, k, v."""
+    Nq, Hq, D = q.shape
+    Nk, Hkv = k.shape[0], k.shape[1]
+    bf = torch.bfloat16
+    for t, n, shp in ((q, "q", (Nq, Hq, D)), (k, "k", (Nk, Hkv, D)), (v, "v", (Nk, Hkv, D)),
+                      (o, "o", (Nq, Hq, D)), (dout, "dout", (Nq, Hq, D))):
+        _need(t, n, bf, shp)
+    _need(lse, "lse", torch.float32, (Hq, Nq))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    cq, ck = _host_cu(cu_q), _host_cu(cu_k)
+    if workspace is None:
+        workspace = torch.empty((max(16, varlen_workspace_bytes(cq, ck, Hq, Hkv, D)),),
+                                dtype=torch.uint8, device=q.device)
+    rc = lib().attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                               _ptr(dk), _ptr(dv), _ptr(workspace), workspace.numel(),
+                               ctypes.c_void_p(cq.ctypes.data), ctypes.c_void_p(ck.ctypes.data),
+                               cq.size - 1, Hq, Hkv, D, _scale(scale, D), int(bool(causal)),
+                               _stream())
+    _check(rc, "attn_bwd_varlen")
+    return dq, dk, dv
+
+
+def layer_gemm(a, b, a_mn_major=False, b_mn_major=True, out=None, out_fp32=False, alpha=1.0):
+    """C = alpha A B on the tensor cores (bf16 in, fp32 accumulation).  a is
+    [M, K] (or, with a_mn_major, stored transposed as [K, M]); b is [K, N]
+    with b_mn_major (the default, row-major B) or stored transposed [N, K]."""
+    M, K = (a.shape[1], a.shape[0]) if a_mn_major else tuple(a.shape)
+    N = b.shape[1] if b_mn_major else b.shape[0]
+    if (b.shape[0] if b_mn_major else b.shape[1]) != K:
+        raise ValueError(f"inner dimensions differ: a {tuple(a.shape)}, b {tuple(b.shape)}")
+    _need(a, "a", torch.bfloat16, tuple(a.shape))
+    _need(b, "b", torch.bfloat16, tuple(b.shape))
+    dt = torch.float32 if out_fp32 else torch.bfloat16
+    c = torch.empty((M, N), dtype=dt, device=a.device) if out is None else out
+    _need(c, "c", dt, (M, N))
+    _check(lib().layer_gemm(_ptr(a), int(a_mn_major), a.shape[1], _ptr(b), int(b_mn_major),
+                            b.shape[1], _ptr(c), int(out_fp32), N, M, N, K, float(alpha),
+                            _stream()), "layer_gemm")
+    return c
+
+
+def layer_workspace_bytes(B, T, d, Hq, Hkv, D) -> int:
+    return int(lib().layer_workspace_bytes(B, T, d, Hq, Hkv, D))
+
+
+class LayerState:
+    """Device state of one attention layer under AdamW: fp32 master weights
+    w_qkv [d, (Hq + 2 Hkv) D] (= [Wq | Wk | Wv]) and w_o [Hq D, d], their
+    moments, bf16 copies, gradient buffers and the step workspace."""
+
+    def __init__(self, wq, wk, wv, wo, B, T, Hq, Hkv, D, device="cuda"):
+        d = wq.shape[0]
+        self.dims = (B, T, d, Hq, Hkv, D)
+        f32 = dict(dtype=torch.float32, device=device)
+        self.w_qkv = torch.cat([wq, wk, wv], dim=1).to(**f32).contiguous()
+        self.w_o = wo.to(**f32).contiguous()
+        self.m_qkv, self.v_qkv = torch.zeros_like(self.w_qkv), torch.zeros_like(self.w_qkv)
+        self.m_o, self.v_o = torch.zeros_like(self.w_o), torch.zeros_like(self.w_o)
+        self.w_qkv_bf16 = self.w_qkv.to(torch.bfloat16)
+        self.w_o_bf16 = self.w_o.to(torch.bfloat16)
+        self.g_qkv, self.g_o = torch.empty_like(self.w_qkv), torch.empty_like(self.w_o)
+        self.y = torch.empty((B, T, d), dtype=torch.bfloat16, device=device)
+        self.dx = torch.empty((B, T, d), dtype=torch.bfloat16, device=device)
+        self.workspace = torch.empty((layer_workspace_bytes(*self.dims),), dtype=torch.uint8,
+                                     device=device)
+        self.step = 0
+
+
+def layer_train_step(state, x, dy, lr=3e-4, weight_decay=0.1, beta1=0.9, beta2=0.999, eps=1e-8,
+                     with_dx=True):
+    """One training step of the layer on (x, dy), then AdamW; returns
+    (g_qkv, g_o) of this step (the state's buffers)."""
+    B, T, d, Hq, Hkv, D = state.dims
+    _need(x, "x", torch.bfloat16, (B, T, d))
+    _need(dy, "dy", torch.bfloat16, (B, T, d))
+    state.step += 1
+    s = state
+    _check(lib().layer_train_step(_ptr(x), _ptr(dy), _ptr(s.w_qkv), _ptr(s.w_o), _ptr(s.m_qkv),
+                                  _ptr(s.v_qkv), _ptr(s.m_o), _ptr(s.v_o), _ptr(s.w_qkv_bf16),
+                                  _ptr(s.w_o_bf16), _ptr(s.g_qkv), _ptr(s.g_o), _ptr(s.y),
+                                  _ptr(s.dx) if with_dx else None, _ptr(s.workspace),
+                                  s.workspace.numel(), B, T, d, Hq, Hkv, D, s.step, float(lr),
+                                  float(weight_decay), float(beta1), float(beta2), float(eps),
+                                  _stream()), "layer_train_step")
+    return s.g_qkv, s.g_o
+
+
+def embed_grad_workspace_bytes(N, V, E) -> int:
+    return int(lib().embed_grad_workspace_bytes(N, V, E))
+
+
+def embed_grad(ids, dy, V, dw=None, workspace=None):
+    """Deterministic embedding-lookup gradient: dw fp32 [V, E] with
+    dw[v] = sum of dy[t] over tokens t with ids[t] == v (include/detattn.h)."""
+    if ids.dim() != 1 or dy.dim() != 2:
+        raise ValueError("ids must be [N] and dy [N, E]")
+    N, E = dy.shape
+    _need(ids, "ids", torch.int32, (N,))
+    _need(dy, "dy", torch.bfloat16, (N, E))
+    dw = torch.empty((V, E), dtype=torch.float32, device=dy.device) if dw is None else dw
+    _need(dw, "dw", torch.float32, (V, E))
+    if workspace is None:
+        workspace = torch.empty((max(16, embed_grad_workspace_bytes(N, V, E)),), dtype=torch.uint8,
+                                device=dy.device)
+    _check(lib().embed_grad(_ptr(ids), _ptr(dy), _ptr(dw), _ptr(workspace), workspace.numel(), N,
+                            V, E, _stream()), "embed_grad")
+    return dw
 
 
 def check_status():

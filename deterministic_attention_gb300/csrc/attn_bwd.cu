@@ -75,8 +75,24 @@ __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
 // of a row reads that row's LSE and stores its (-LSE*log2e, -Delta) pair.
 // The padding positions T..Tp-1 of every (b, h) get (-inf, -0).
 constexpr int kDeltaBlocksPerSm = 4;
-template <int D>
-__global__ void __launch_bounds__(256, kDeltaBlocksPerSm) attn_delta_kernel(const DeltaArgs a) {
+// Packed batches (VL): B = 1 and T = total_q; the row statistics of query
+// row t of sequence s go to position ps[s] + t - cu_q[s] (sequence found by a
+// binary search of cu_q), and each sequence's padding positions up to the
+// next multiple of 128 get (-inf, -0).  Rows whose LSE is -inf (packed rows
+// that see no key) store -inf, so every P formed from them is 0.
+__device__ __forceinline__ int seq_of_row(const VarlenTable& vt, int t) {
+  int lo = 0, hi = vt.n_seq - 1;
+  while (lo < hi) {  // last s with cu_q[s] <= t
+    const int mid = (lo + hi + 1) >> 1;
+    if (vt.cu_q[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int D, class VT>
+__global__ void __launch_bounds__(256, kDeltaBlocksPerSm) attn_delta_kernel(const DeltaArgs a,
+                                                                             const __grid_constant__ VT vt) {
+  constexpr bool VL = std::is_same<VT, VarlenTable>::value;
   // Launched as a dependent of whatever precedes it (the forward, in a
   // training step): everything below reads that kernel's output.  Only after
   // this wait may the next kernel (the dK/dV step) start its own prologue.
@@ -118,7 +134,14 @@ __global__ void __launch_bounds__(256, kDeltaBlocksPerSm) attn_delta_kernel(cons
         xd[it] = dO[off];
         const size_t bh = static_cast<size_t>(b) * a.Hq + h;
         if (lane % kCpr == 0) lse[it] = a.lse[bh * a.T + t];
-        dst[it] = bh * a.Tp + t;
+        if constexpr (VL) {
+          if (lane % kCpr == 0) {
+            const int sq = seq_of_row(vt, t);
+            dst[it] = bh * a.Tp + vt.ps[sq] + (t - vt.cu_q[sq]);
+          }
+        } else {
+          dst[it] = bh * a.Tp + t;
+        }
       }
       h += kRpi;
       while (h >= a.Hq) {
@@ -143,17 +166,35 @@ __global__ void __launch_bounds__(256, kDeltaBlocksPerSm) attn_delta_kernel(cons
 #pragma unroll
       for (int s2 = kCpr / 2; s2 >= 1; s2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s2);
       const long r = r_lane + it * kRpi;
-      if (lane % kCpr == 0 && r < rows) a.rowstats[dst[it]] = make_float2(-lse[it] * kLog2e, -acc);
+      if (lane % kCpr == 0 && r < rows)
+        a.rowstats[dst[it]] = make_float2(lse[it] > -INFINITY ? -lse[it] * kLog2e : -INFINITY, -acc);
     }
   }
-  // Padding positions: (b, h, t) for t in [T, Tp).
-  const int pad = a.Tp - a.T;
-  const long n_pad = static_cast<long>(a.B) * a.Hq * pad;
-  for (long p = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; p < n_pad;
-       p += static_cast<long>(gridDim.x) * blockDim.x) {
-    const long bh = p / pad;
-    const int t = a.T + static_cast<int>(p % pad);
-    a.rowstats[bh * a.Tp + t] = make_float2(-INFINITY, -0.f);
+  if constexpr (VL) {
+    // Padding positions: for every (h, s), [ps[s] + tq_s, ps[s + 1]).  Each
+    // thread walks position slots of the whole padded row and writes those
+    // that no query row of their sequence fills.
+    const long n_all = static_cast<long>(a.Hq) * a.Tp;
+    for (long p = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; p < n_all;
+         p += static_cast<long>(gridDim.x) * blockDim.x) {
+      const int pos = static_cast<int>(p % a.Tp);
+      int lo = 0, hi = vt.n_seq - 1;  // last s with ps[s] <= pos
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (vt.ps[mid] <= pos) lo = mid; else hi = mid - 1;
+      }
+      if (pos - vt.ps[lo] >= vt.cu_q[lo + 1] - vt.cu_q[lo]) a.rowstats[p] = make_float2(-INFINITY, -0.f);
+    }
+  } else {
+    // Padding positions: (b, h, t) for t in [T, Tp).
+    const int pad = a.Tp - a.T;
+    const long n_pad = static_cast<long>(a.B) * a.Hq * pad;
+    for (long p = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; p < n_pad;
+         p += static_cast<long>(gridDim.x) * blockDim.x) {
+      const long bh = p / pad;
+      const int t = a.T + static_cast<int>(p % pad);
+      a.rowstats[bh * a.Tp + t] = make_float2(-INFINITY, -0.f);
+    }
   }
 }
 
@@ -280,18 +321,24 @@ __device__ __forceinline__ void reg_fence_cols(uint32_t (&v)[N]) {
 }
 
 // One key tile of the dK/dV work, as one block of its cluster sees it.
+// Rows are relative to the tile's sequence: its keys start at row kbase of
+// the K, V maps, its queries at qbase of the Q, dO maps, and their row
+// statistics at rbase of each head's row; query i sees key j iff
+// j <= i + off under the causal mask (off = 0, bases 0 unless packed).
 struct DkvTile {
   int b, g, n0;
   int m_begin, per_head;  // first query tile, query tiles per head
   int it_lo, n_it;        // this block's chunk of the tile's G * per_head items
+  int qbase, kbase, rbase, tk, off;
 };
 
-template <int D>
+template <int D, class VT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                      const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
-                     const BwdArgs a) {
+                     const BwdArgs a, const __grid_constant__ VT vt) {
   using Cf = DkvCfg<D>;
+  constexpr bool VL = std::is_same<VT, VarlenTable>::value;
   constexpr int NS = Cf::kStages;
   constexpr int TM = Cf::kTM;
   constexpr int QG = Cf::kQG;
@@ -306,7 +353,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int crank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const int group = static_cast<int>(blockIdx.x) / C;
   const int NG = a.n_groups;
-  const int n_tiles_all = a.n_tiles * a.BH;
+  const int n_tiles_all = (VL ? vt_tiles(vt) : a.n_tiles) * a.BH;
   const int G = a.Hq / a.Hkv;
   const int m_end = (a.T + TM - 1) / TM;
   const int R = kTileN / C;
@@ -317,12 +364,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   };
   auto tile_info = [&](int t) {
     DkvTile ti;
-    const int nt = t / a.BH, bg = t % a.BH;
-    ti.b = bg / a.Hkv;
-    ti.g = bg % a.Hkv;
-    ti.n0 = nt * kTileN;
-    ti.m_begin = a.causal ? ti.n0 / TM : 0;
-    ti.per_head = m_end - ti.m_begin;
+    if constexpr (VL) {
+      const uint32_t e = vt_tile(vt, t / a.BH);
+      const int s = static_cast<int>(e >> 16);
+      ti.b = 0;
+      ti.g = t % a.BH;
+      ti.n0 = static_cast<int>(e & 0xFFFFu) * kTileN;
+      ti.qbase = vt_cu_q(vt, s);
+      const int tq = vt_cu_q(vt, s + 1) - ti.qbase;
+      ti.kbase = vt_cu_k(vt, s);
+      ti.tk = vt_cu_k(vt, s + 1) - ti.kbase;
+      ti.rbase = vt_ps(vt, s);
+      ti.off = ti.tk - tq;
+      // Query tiles whose last row sees the tile's first key.
+      const int first_q = ti.n0 - ti.off;  // first query that sees key n0
+      const int mq_end = (tq + TM - 1) / TM;
+      ti.m_begin = a.causal ? min(mq_end, max(0, first_q) / TM) : 0;
+      ti.per_head = mq_end - ti.m_begin;
+    } else {
+      const int nt = t / a.BH, bg = t % a.BH;
+      ti.b = bg / a.Hkv;
+      ti.g = bg % a.Hkv;
+      ti.n0 = nt * kTileN;
+      ti.m_begin = a.causal ? ti.n0 / TM : 0;
+      ti.per_head = m_end - ti.m_begin;
+      ti.qbase = ti.kbase = ti.rbase = 0;
+      ti.tk = a.T;
+      ti.off = 0;
+    }
     const int n_all = G * ti.per_head;
     ti.it_lo = static_cast<int>(static_cast<long>(crank) * n_all / C);
     ti.n_it = static_cast<int>(static_cast<long>(crank + 1) * n_all / C) - ti.it_lo;
@@ -407,8 +476,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * Cf::kKvBytes);
         for (int at = 0; at < Cf::kAtoms; ++at) {
-          tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, ti.g, ti.n0, ti.b);
-          tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, ti.g, ti.n0, ti.b);
+          tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, ti.g,
+                      ti.kbase + ti.n0, ti.b);
+          tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, ti.g,
+                      ti.kbase + ti.n0, ti.b);
         }
         last_kv = kt;
         int h = ti.g * G + (ti.n_it > 0 ? ti.it_lo / ti.per_head : 0);
@@ -421,9 +492,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t st = stage_base(s);
           mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + TM * 8);
           for (int at = 0; at < Cf::kAtoms; ++at) {
-            tma_load_4d(st + at * (TM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h, i0, ti.b);
+            tma_load_4d(st + at * (TM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h,
+                        ti.qbase + i0, ti.b);
             tma_load_4d(st + Cf::kQBytes + at * (TM * 128), &mdO, bar(kDkvBarQFull + s), at * 64,
-                        h, i0, ti.b);
+                        h, ti.qbase + i0, ti.b);
           }
           if (!waited) {
             // Launched as a dependent of the Delta step: only the row
@@ -433,8 +505,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             waited = true;
           }
           bulk_load(st + 2 * Cf::kQBytes,
-                    a.rowstats + (static_cast<size_t>(ti.b) * a.Hq + h) * a.Tp + i0, TM * 8,
-                    bar(kDkvBarQFull + s));
+                    a.rowstats + (static_cast<size_t>(ti.b) * a.Hq + h) * a.Tp + ti.rbase + i0,
+                    TM * 8, bar(kDkvBarQFull + s));
           last[s] = gi;
           if (++m_idx == ti.per_head) {
             m_idx = 0;
@@ -642,8 +714,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // block on the diagonal needs the mask, and lane 0 holds the warp's
         // smallest krow, so the test is made once for the whole warp and the
         // unmasked items run a loop without it.
-        const int cmin = a.causal ? (krow - i0) : -1;
-        const bool warp_masked = a.causal && (ti.n0 + quarter * 32 - i0) + 31 > 0;
+        const int cmin = a.causal ? (krow - ti.off - i0) : -1;
+        const bool warp_masked = a.causal && (ti.n0 + quarter * 32 - ti.off - i0) + 31 > 0;
         uint32_t pk[QG / 2], dk[QG / 2];
         // (-lse2, -delta) of this group's queries, two per float4.
         const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * QG * 8;
@@ -783,9 +855,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mbar_arrive_remote(map_shared_rank(bar(kDkvBarRegionFree), static_cast<uint32_t>(p)));
         }
       }
-      if (owner == crank && krow < a.T) {
+      if (owner == crank && krow < ti.tk) {
         const size_t rbase =
-            ((static_cast<size_t>(ti.b) * a.T + krow) * a.Hkv + ti.g) * D + grp * (D / 4);
+            ((static_cast<size_t>(ti.b) * a.Tk + ti.kbase + krow) * a.Hkv + ti.g) * D +
+            grp * (D / 4);
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           const uint32_t* v = which == 0 ? part_v : part_k;
@@ -877,12 +950,14 @@ enum : int { kDqBarQ = 0, kDqBarKFull = 1, kDqBarVFull = 4, kDqBarKEmpty = 7, kD
              kDqBarUnit = 22,    // [4] unit k published in ring slot k % 4
              kDqNumBars = 26 };
 
-template <int D>
+template <int D, class VT>
 __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
-                   const BwdArgs a, const __grid_constant__ QTileSched sched) {
+                   const BwdArgs a, const __grid_constant__ QTileSched sched,
+                   const __grid_constant__ VT vt) {
   using C = DqCfg<D>;
+  constexpr bool VL = std::is_same<VT, VarlenTable>::value;
   constexpr int NS = C::kStages;
   constexpr int NP = C::NP;
   extern __shared__ uint8_t smem_raw[];
@@ -900,7 +975,7 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
     first = sched.start[pipe_id];
     n_units = sched.start[pipe_id + 1] - first;
   } else {
-    const int total = a.n_tiles * a.BH;
+    const int total = (VL ? vt_tiles(vt) : a.n_tiles) * a.BH;
     n_units = qtile_snake_count(pipe_id, total, sched.n_pipes);
   }
   auto u_of = [&](int k) {
@@ -914,18 +989,41 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
   // way it passes unit k (or -1 after the last) to the pipeline's other warps
   // in ring slot k % 4, published by mbarrier kDqBarUnit + k % 4.  Which
   // pipeline computes a unit does not change any bit of its result.
-  const int n_all = a.n_tiles * a.BH;
+  const int n_all = (VL ? vt_tiles(vt) : a.n_tiles) * a.BH;
   __shared__ int unit_ring[NP][4];
-  struct Unit { int b, h, hkv, m0, n_kv; };
+  // Rows relative to the unit's sequence, as in the forward: queries from row
+  // qbase, keys from kbase, row statistics from rbase; key j visible to
+  // query i iff j < tk and (causal) j <= i + off.
+  struct Unit { int b, h, hkv, m0, n_kv, qbase, kbase, rbase, tq, tk, off; };
   auto unit_info = [&](int u) {
     Unit t;
-    const int mt = a.n_tiles - 1 - u / a.BH;
-    const int bh = u % a.BH;
-    t.b = bh / a.Hq;
-    t.h = bh % a.Hq;
+    if constexpr (VL) {
+      const uint32_t e = vt_tile(vt, u / a.BH);
+      const int s = static_cast<int>(e >> 16);
+      t.b = 0;
+      t.h = u % a.BH;
+      t.m0 = static_cast<int>(e & 0xFFFFu) * kTileM;
+      t.qbase = vt_cu_q(vt, s);
+      t.tq = vt_cu_q(vt, s + 1) - t.qbase;
+      t.kbase = vt_cu_k(vt, s);
+      t.tk = vt_cu_k(vt, s + 1) - t.kbase;
+      t.rbase = vt_ps(vt, s);
+      t.off = t.tk - t.tq;
+      const int tiles = (t.tk + kDqTileN - 1) / kDqTileN;
+      const int last = min(t.m0 + kTileM - 1, t.tq - 1) + t.off;
+      t.n_kv = a.causal ? (last < 0 ? 0 : min(tiles, last / kDqTileN + 1)) : tiles;
+    } else {
+      const int mt = a.n_tiles - 1 - u / a.BH;
+      const int bh = u % a.BH;
+      t.b = bh / a.Hq;
+      t.h = bh % a.Hq;
+      t.m0 = mt * kTileM;
+      t.n_kv = a.causal ? min(kv_tiles, (t.m0 + kTileM) / kDqTileN) : kv_tiles;
+      t.qbase = t.kbase = t.rbase = 0;
+      t.tq = t.tk = a.T;
+      t.off = 0;
+    }
     t.hkv = t.h / (a.Hq / a.Hkv);
-    t.m0 = mt * kTileM;
-    t.n_kv = a.causal ? min(kv_tiles, (t.m0 + kTileM) / kDqTileN) : kv_tiles;
     return t;
   };
 
@@ -1022,8 +1120,10 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         const Unit t = unit_info(u);
         mbar_arrive_expect_tx(bar(kDqBarQ), 2 * C::kQBytes);
         for (int at = 0; at < C::kAtoms; ++at) {
-          tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kDqBarQ), at * 64, t.h, t.m0, t.b);
-          tma_load_4d(sdO + at * (kTileM * 128), &mdO, bar(kDqBarQ), at * 64, t.h, t.m0, t.b);
+          tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kDqBarQ), at * 64, t.h, t.qbase + t.m0,
+                      t.b);
+          tma_load_4d(sdO + at * (kTileM * 128), &mdO, bar(kDqBarQ), at * 64, t.h,
+                      t.qbase + t.m0, t.b);
         }
         last_q = ku;
         for (int j = 0; j < t.n_kv; ++j, ++gj) {
@@ -1033,13 +1133,13 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
           mbar_arrive_expect_tx(bar(kDqBarKFull + s), C::kKvBytes);
           for (int at = 0; at < C::kAtoms; ++at)
             tma_load_4d(sK0 + s * C::kKvBytes + at * (kDqTileN * 128), &mK, bar(kDqBarKFull + s),
-                        at * 64, t.hkv, j * kDqTileN, t.b);
+                        at * 64, t.hkv, t.kbase + j * kDqTileN, t.b);
           last_k[s] = gj;
           if (gj >= NS && !(ok = mbar_wait(bar(kDqBarVEmpty + s), ph ^ 1, wait_ns))) break;
           mbar_arrive_expect_tx(bar(kDqBarVFull + s), C::kKvBytes);
           for (int at = 0; at < C::kAtoms; ++at)
             tma_load_4d(sV0 + s * C::kKvBytes + at * (kDqTileN * 128), &mV, bar(kDqBarVFull + s),
-                        at * 64, t.hkv, j * kDqTileN, t.b);
+                        at * 64, t.hkv, t.kbase + j * kDqTileN, t.b);
           last_v[s] = gj;
         }
       }
@@ -1072,6 +1172,15 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         if (j == 0 && !(warp_all(mbar_wait(bar(kDqBarQ), ku & 1, wait_ns)) &&
                         warp_all(mbar_wait(bar(kDqBarQTmem), ku & 1, wait_ns))))
           return false;
+        if constexpr (VL) {
+          if (t.n_kv == 0) {
+            // A packed unit whose rows see no key: no products, but the same
+            // hand-offs as any unit (its Q copy is released at once).
+            tc_fence_after();
+            mma_commit(bar(kDqBarQUsed));
+            return true;
+          }
+        }
         if (g > 0 && !warp_all(mbar_wait(bar(kDqBarSFree), (g - 1) & 1, wait_ns))) return false;
         if (!warp_all(mbar_wait(bar(kDqBarKFull + s), ph, wait_ns))) return false;
         tc_fence_after();
@@ -1190,7 +1299,8 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
       const Unit t = unit_info(u);
       const int qrow = t.m0 + r;
       // (-LSE*log2e, -Delta) of this row; rows past T read (-inf, -0): P = 0.
-      const float2 rstat = a.rowstats[(static_cast<size_t>(t.b) * a.Hq + t.h) * a.Tp + qrow];
+      const float2 rstat =
+          a.rowstats[(static_cast<size_t>(t.b) * a.Hq + t.h) * a.Tp + t.rbase + qrow];
       for (int j = 0; j < t.n_kv; ++j, ++gj) {
         ok = warp_all(mbar_wait(bar(kDqBarS), gj & 1, wait_ns));
         if (!ok) break;
@@ -1207,13 +1317,13 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         if (lane == 0) mbar_arrive(bar(kDqBarSFree));
         const int kv0 = j * kDqTileN + half * 32;  // key of this half's first column
         // key kv0 + c visible iff c <= lim
-        const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
+        const int lim = a.causal ? min(qrow + t.off - kv0, t.tk - 1 - kv0) : (t.tk - 1 - kv0);
         uint32_t dsk[16];
         // Masking is needed only where this warp's 32 rows meet the diagonal
         // (or T), decided for the whole warp; other tiles run the loop
         // without it.
-        const int row0 = t.m0 + quarter * 32;
-        const bool need_mask = (a.causal && kv0 + 31 > row0) || kv0 + 32 > a.T;
+        const int row0 = t.m0 + quarter * 32 + t.off;  // last visible key of the warp's first row
+        const bool need_mask = (a.causal && kv0 + 31 > row0) || kv0 + 32 > t.tk;
         auto element_loop = [&](auto masked) {
           constexpr bool kMasked = decltype(masked)::value;
           static_for<16>([&](auto ic) {
@@ -1261,9 +1371,9 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
       ok = warp_all(mbar_wait(bar(kDqBarAcc), ku & 1, wait_ns));
       if (!ok) break;
       tc_fence_after();
-      const bool live = qrow < a.T;
+      const bool live = qrow < t.tq;
       __nv_bfloat16* dqrow = static_cast<__nv_bfloat16*>(a.dq) +
-                             ((static_cast<size_t>(t.b) * a.T + qrow) * a.Hq + t.h) * D;
+                             ((static_cast<size_t>(t.b) * a.T + t.qbase + qrow) * a.Hq + t.h) * D;
       uint32_t pkd[D / 4];
 #pragma unroll
       for (int cc = 0; cc < D / 64; ++cc) {
@@ -1274,6 +1384,13 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
         for (int i = 0; i < 16; ++i)
           pkd[16 * cc + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * a.scale,
                                          __uint_as_float(v[2 * i + 1]) * a.scale);
+      }
+      if constexpr (VL) {
+        // No key tile: the accumulator still holds an earlier unit's sums.
+        if (t.n_kv == 0) {
+#pragma unroll
+          for (int i = 0; i < D / 4; ++i) pkd[i] = 0u;
+        }
       }
       // dQ is in registers: the next unit's first dQ MMA may overwrite it.
       tc_fence_before();
@@ -1330,7 +1447,7 @@ cudaError_t set_smem_once(K kernel, int bytes, unsigned long long* done) {
 template <int D>
 cudaError_t dkdv_max_clusters_t(int c, int* out) {
   static unsigned long long done[64] = {};
-  cudaError_t e = set_smem_once(attn_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, done);
+  cudaError_t e = set_smem_once(attn_dkdv_kernel<D, NoVarlen>, DkvCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(c));
@@ -1343,15 +1460,15 @@ cudaError_t dkdv_max_clusters_t(int c, int* out) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, attn_dkdv_kernel<D>, &cfg);
+  return cudaOccupancyMaxActiveClusters(out, attn_dkdv_kernel<D, NoVarlen>, &cfg);
 }
 
-template <int D>
+template <int D, class VT>
 cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                          bool dependent, cudaStream_t st) {
+                          bool dependent, const VT& vt, cudaStream_t st) {
   static unsigned long long done[64] = {};
-  cudaError_t e = set_smem_once(attn_dkdv_kernel<D>, DkvCfg<D>::kSmemBytes, done);
+  cudaError_t e = set_smem_once(attn_dkdv_kernel<D, VT>, DkvCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -1374,26 +1491,26 @@ cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  e = cudaLaunchKernelEx(&cfg, attn_dkdv_kernel<D>, mq, mk, mv, mdo, a);
+  e = cudaLaunchKernelEx(&cfg, attn_dkdv_kernel<D, VT>, mq, mk, mv, mdo, a, vt);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, class VT>
 cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                        const QTileSched& sched, cudaStream_t st) {
+                        const QTileSched& sched, const VT& vt, cudaStream_t st) {
   static unsigned long long done[64] = {};
-  cudaError_t e = set_smem_once(attn_dq_kernel<D>, DqCfg<D>::kSmemBytes, done);
+  cudaError_t e = set_smem_once(attn_dq_kernel<D, VT>, DqCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
-  attn_dq_kernel<D><<<grid, kDqPipeThreads * DqCfg<D>::NP, DqCfg<D>::kSmemBytes, st>>>(
-      mq, mk, mv, mdo, a, sched);
+  attn_dq_kernel<D, VT><<<grid, kDqPipeThreads * DqCfg<D>::NP, DqCfg<D>::kSmemBytes, st>>>(
+      mq, mk, mv, mdo, a, sched, vt);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_delta(const DeltaArgs& a, int sms, cudaStream_t st) {
+cudaError_t launch_delta(const DeltaArgs& a, int sms, const VarlenTable* vt, cudaStream_t st) {
   // Persistent: kDeltaBlocksPerSm blocks per SM, fewer when there are fewer
   // batches of rows than warps.
   const int rows_per_batch = 4 * (256 / a.D);
@@ -1409,17 +1526,28 @@ cudaError_t launch_delta(const DeltaArgs& a, int sms, cudaStream_t st) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = a.D == 64 ? cudaLaunchKernelEx(&cfg, attn_delta_kernel<64>, a)
-                            : cudaLaunchKernelEx(&cfg, attn_delta_kernel<128>, a);
+  cudaError_t e;
+  if (vt != nullptr) {
+    e = a.D == 64 ? cudaLaunchKernelEx(&cfg, attn_delta_kernel<64, VarlenTable>, a, *vt)
+                  : cudaLaunchKernelEx(&cfg, attn_delta_kernel<128, VarlenTable>, a, *vt);
+  } else {
+    const NoVarlen none{};
+    e = a.D == 64 ? cudaLaunchKernelEx(&cfg, attn_delta_kernel<64, NoVarlen>, a, none)
+                  : cudaLaunchKernelEx(&cfg, attn_delta_kernel<128, NoVarlen>, a, none);
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                        bool dependent, cudaStream_t st) {
-  return D == 64 ? launch_dkdv_t<64>(grid, mq, mk, mv, mdo, a, dependent, st)
-                 : launch_dkdv_t<128>(grid, mq, mk, mv, mdo, a, dependent, st);
+                        bool dependent, const VarlenTable* vt, cudaStream_t st) {
+  if (vt != nullptr)
+    return D == 64 ? launch_dkdv_t<64>(grid, mq, mk, mv, mdo, a, dependent, *vt, st)
+                   : launch_dkdv_t<128>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
+  const NoVarlen none{};
+  return D == 64 ? launch_dkdv_t<64>(grid, mq, mk, mv, mdo, a, dependent, none, st)
+                 : launch_dkdv_t<128>(grid, mq, mk, mv, mdo, a, dependent, none, st);
 }
 
 cudaError_t dkdv_max_clusters(int D, int c, int* out) {
@@ -1432,9 +1560,13 @@ int dkdv_max_cluster_size(int D) { return D == 64 ? DkvCfg<64>::kMaxCluster : Dk
 
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                      const QTileSched& sched, cudaStream_t st) {
-  return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, a, sched, st)
-                 : launch_dq_t<128>(grid, mq, mk, mv, mdo, a, sched, st);
+                      const QTileSched& sched, const VarlenTable* vt, cudaStream_t st) {
+  if (vt != nullptr)
+    return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, a, sched, *vt, st)
+                   : launch_dq_t<128>(grid, mq, mk, mv, mdo, a, sched, *vt, st);
+  const NoVarlen none{};
+  return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, a, sched, none, st)
+                 : launch_dq_t<128>(grid, mq, mk, mv, mdo, a, sched, none, st);
 }
 
 // Diagnostic: the kernels' 2^x forms on n inputs (polynomial scalar form,

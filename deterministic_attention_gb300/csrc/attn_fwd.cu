@@ -100,12 +100,13 @@ enum : int {
 __device__ __forceinline__ bool warp_all(bool ok) { return __all_sync(0xffffffffu, ok); }
 
 
-template <int D>
+template <int D, class VT>
 __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                     const __grid_constant__ CUtensorMap mV, const FwdArgs a,
-                    const __grid_constant__ QTileSched sched) {
+                    const __grid_constant__ QTileSched sched, const __grid_constant__ VT vt) {
   using C = Cfg<D>;
+  constexpr bool VL = std::is_same<VT, VarlenTable>::value;
   constexpr int NS = C::kStages;
   constexpr int NP = C::NP;
   extern __shared__ uint8_t smem_raw[];
@@ -126,23 +127,46 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
     first = sched.start[pipe_id];
     n_units = sched.start[pipe_id + 1] - first;
   } else {
-    const int total = a.n_m * a.BHq;
+    const int total = (VL ? vt_tiles(vt) : a.n_m) * a.BHq;
     n_units = qtile_snake_count(pipe_id, total, sched.n_pipes);
   }
   auto u_of = [&](int k) {
     return sched.n_listed > 0 ? static_cast<int>(sched.unit[first + k])
                               : qtile_snake_unit(pipe_id, k, sched.n_pipes);
   };
-  struct Unit { int b, h, hkv, m0, n_kv; };
+  // A unit's query tile starts at row qbase + m0 of the tensor maps and its
+  // keys at row kbase; it has tq query and tk key rows, and with the causal
+  // mask query i sees key j iff j <= i + off, off = tk - tq (0 unless packed).
+  struct Unit { int b, h, hkv, m0, n_kv, qbase, kbase, tq, tk, off; };
   auto unit_info = [&](int u) {
     Unit t;
-    const int mt = a.n_m - 1 - u / a.BHq;
-    const int bh = u % a.BHq;
-    t.b = bh / a.Hq;
-    t.h = bh % a.Hq;
+    if constexpr (VL) {
+      const uint32_t e = vt_tile(vt, u / a.Hq);
+      const int s = static_cast<int>(e >> 16);
+      t.b = 0;
+      t.h = u % a.Hq;
+      t.m0 = static_cast<int>(e & 0xFFFFu) * kTileM;
+      t.qbase = vt_cu_q(vt, s);
+      t.tq = vt_cu_q(vt, s + 1) - t.qbase;
+      t.kbase = vt_cu_k(vt, s);
+      t.tk = vt_cu_k(vt, s + 1) - t.kbase;
+      t.off = t.tk - t.tq;
+      const int tiles = (t.tk + kBN - 1) / kBN;
+      // Keys up to the last visible one of the tile's last row.
+      const int last = min(t.m0 + kTileM - 1, t.tq - 1) + t.off;
+      t.n_kv = a.causal ? (last < 0 ? 0 : min(tiles, last / kBN + 1)) : tiles;
+    } else {
+      const int mt = a.n_m - 1 - u / a.BHq;
+      const int bh = u % a.BHq;
+      t.b = bh / a.Hq;
+      t.h = bh % a.Hq;
+      t.m0 = mt * kTileM;
+      t.n_kv = a.causal ? min(kv_tiles, (t.m0 + kTileM) / kBN) : kv_tiles;
+      t.qbase = t.kbase = 0;
+      t.tq = t.tk = a.T;
+      t.off = 0;
+    }
     t.hkv = t.h / (a.Hq / a.Hkv);
-    t.m0 = mt * kTileM;
-    t.n_kv = a.causal ? min(kv_tiles, (t.m0 + kTileM) / kBN) : kv_tiles;
     return t;
   };
 
@@ -206,7 +230,7 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
         if (ku > 0 && !(ok = mbar_wait(bar(kBarQFree), (ku - 1) & 1, wait_ns))) break;
         mbar_arrive_expect_tx(bar(kBarQ), C::kQBytes);
         for (int at = 0; at < C::kAtoms; ++at)
-          tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kBarQ), at * 64, t.h, t.m0, t.b);
+          tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kBarQ), at * 64, t.h, t.qbase + t.m0, t.b);
         last_q = ku;
         for (int j = 0; j < t.n_kv; ++j, ++gj) {
           const int s = gj % NS;
@@ -215,13 +239,13 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
           mbar_arrive_expect_tx(bar(kBarKFull + s), C::kKvBytes);
           for (int at = 0; at < C::kAtoms; ++at)
             tma_load_4d(sK0 + s * C::kKvBytes + at * (kBN * 128), &mK, bar(kBarKFull + s), at * 64,
-                        t.hkv, j * kBN, t.b);
+                        t.hkv, t.kbase + j * kBN, t.b);
           last_k[s] = gj;
           if (gj >= NS && !(ok = mbar_wait(bar(kBarVEmpty + s), ph ^ 1, wait_ns))) break;
           mbar_arrive_expect_tx(bar(kBarVFull + s), C::kKvBytes);
           for (int at = 0; at < C::kAtoms; ++at)
             tma_load_4d(sV0 + s * C::kKvBytes + at * (kBN * 128), &mV, bar(kBarVFull + s), at * 64,
-                        t.hkv, j * kBN, t.b);
+                        t.hkv, t.kbase + j * kBN, t.b);
           last_v[s] = gj;
         }
       }
@@ -320,10 +344,17 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
     const uint32_t pair_bar = bar(kBarPair + quarter);  // the two halves of these rows
     int gj = 0;
     for (int ku = 0; ku < n_units && ok; ++ku) {
-      const Unit t = unit_info(u_of(ku));
-      const int qrow = t.m0 + r;
+      int qlast, wlast, tk, n_kv;
+      {
+        const Unit t0 = unit_info(u_of(ku));
+        // Last key visible to this row and to the warp's first row (causal).
+        qlast = t0.m0 + r + t0.off;
+        wlast = t0.m0 + quarter * 32 + t0.off;
+        tk = t0.tk;
+        n_kv = t0.n_kv;
+      }
       float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < t.n_kv; ++j, ++gj) {
+      for (int j = 0; j < n_kv; ++j, ++gj) {
         ok = warp_all(mbar_wait(bar(kBarS + (gj & 1)), (gj >> 1) & 1, wait_ns));
         if (!ok) break;
         tc_fence_after();
@@ -333,9 +364,8 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
         // whole warp: every key after every row (or past T) -- P is zero and
         // the running maximum and sum stay as they are; every key visible --
         // no mask.
-        const int row0 = t.m0 + quarter * 32;
-        const bool all_masked = (a.causal && row0 + 31 < kv0) || kv0 >= a.T;
-        const bool need_mask = (a.causal && kv0 + 31 > row0) || kv0 + 32 > a.T;
+        const bool all_masked = (a.causal && wlast + 31 < kv0) || kv0 >= tk;
+        const bool need_mask = (a.causal && kv0 + 31 > wlast) || kv0 + 32 > tk;
         if (all_masked) {
           uint32_t pk[16];
 #pragma unroll
@@ -352,7 +382,7 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
         tmem_wait_ld();
         reg_fence32(sr);
 
-        const int lim = a.causal ? min(qrow - kv0, a.T - 1 - kv0) : (a.T - 1 - kv0);
+        const int lim = a.causal ? min(qlast - kv0, tk - 1 - kv0) : (tk - 1 - kv0);
         float alpha = 1.f;
         bool moved = false;
         uint64_t sum2[2];  // four partial sums
@@ -439,6 +469,10 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
       if (!ok) break;
       ok = warp_all(mbar_wait(bar(kBarOFinal), ku & 1, wait_ns));
       if (!ok) break;
+      // The unit again, for its epilogue (looked up anew rather than kept in
+      // registers through the key loop).
+      const Unit t = unit_info(u_of(ku));
+      const int qrow = t.m0 + r;
       // Merge the two halves: M = max(m_0, m_1), f_h = 2^(m_h - M),
       // L = l_0 f_0 + l_1 f_1 (half 0 first), O = (O_0 f_0 + O_1 f_1) / L.
       red_m[half][r] = m_run;
@@ -448,14 +482,23 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
       if (!ok) break;
       tc_fence_after();
       const float m0v = red_m[0][r], m1v = red_m[1][r];
-      const float M = fmaxf(m0v, m1v);  // finite: key 0 is visible to every row
+      // Finite in the fixed-length form (key 0 is visible to every row).  A
+      // packed sequence with more queries than keys has rows that see no key:
+      // M = -inf there, and the row gets O = 0 and LSE = -inf.
+      float M = fmaxf(m0v, m1v);
+      bool blind = false;
+      if constexpr (VL) {
+        blind = !(M > -INFINITY);
+        if (blind) M = 0.f;
+      }
       const float f0 = ex2_approx(m0v - M), f1 = ex2_approx(m1v - M);
       const float l_tot = red_l[0][r] * f0 + red_l[1][r] * f1;
-      const float inv_l = 1.f / l_tot;
-      const float w0 = f0 * inv_l, w1 = f1 * inv_l;
-      const bool live = qrow < a.T;
+      const float inv_l = blind ? 0.f : 1.f / l_tot;
+      const float w0 = blind ? 0.f : f0 * inv_l, w1 = blind ? 0.f : f1 * inv_l;
+      const bool live = qrow < t.tq;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.o) +
-                            ((static_cast<size_t>(t.b) * a.T + qrow) * a.Hq + t.h) * D + half * (D / 2);
+                            ((static_cast<size_t>(t.b) * a.T + t.qbase + qrow) * a.Hq + t.h) * D +
+                            half * (D / 2);
       uint32_t pkd[D / 4];
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
@@ -469,6 +512,14 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
               fmaf(__uint_as_float(o0[2 * i]), w0, __uint_as_float(o1[2 * i]) * w1),
               fmaf(__uint_as_float(o0[2 * i + 1]), w0, __uint_as_float(o1[2 * i + 1]) * w1));
       }
+      if constexpr (VL) {
+        // A unit without key tiles never wrote its accumulators: they hold an
+        // earlier unit's sums (which times 0 could still be NaN).
+        if (blind) {
+#pragma unroll
+          for (int i = 0; i < D / 4; ++i) pkd[i] = 0u;
+        }
+      }
       // O is in registers: the next unit's first P V may overwrite it.
       tc_fence_before();
       __syncwarp();
@@ -479,8 +530,8 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
         for (int i = 0; i < D / 16; ++i)
           dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
         if (half == 0)
-          a.lse[(static_cast<size_t>(t.b) * a.Hq + t.h) * a.T + qrow] =
-              (M + log2f(l_tot)) * 0.69314718055994530942f;
+          a.lse[(static_cast<size_t>(t.b) * a.Hq + t.h) * a.T + t.qbase + qrow] =
+              blind ? -INFINITY : (M + log2f(l_tot)) * 0.69314718055994530942f;
       }
     }
   }
@@ -494,10 +545,10 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
   }
 }
 
-template <int D>
+template <int D, class VT>
 cudaError_t launch_fwd_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const FwdArgs& a, const QTileSched& sched,
-                         cudaStream_t st) {
+                         const VT& vt, cudaStream_t st) {
   const int smem = Cfg<D>::kSmemBytes;
   // Once per device and context (holds the context id it was set for).
   static unsigned long long attr_ctx[64] = {};
@@ -506,12 +557,12 @@ cudaError_t launch_fwd_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
   if (e != cudaSuccess) return e;
   const unsigned long long ctx = current_context_id();
   if (dev >= 64 || ctx == 0 || attr_ctx[dev] != ctx) {
-    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D, VT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_ctx[dev] = current_context_id();
   }
-  attn_fwd_kernel<D><<<grid, kPipeThreads * Cfg<D>::NP, smem, st>>>(mq, mk, mv, a, sched);
+  attn_fwd_kernel<D, VT><<<grid, kPipeThreads * Cfg<D>::NP, smem, st>>>(mq, mk, mv, a, sched, vt);
   return cudaGetLastError();
 }
 
@@ -519,9 +570,13 @@ cudaError_t launch_fwd_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
 
 cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const FwdArgs& a, const QTileSched& sched,
-                       cudaStream_t st) {
-  return D == 64 ? launch_fwd_t<64>(grid, mq, mk, mv, a, sched, st)
-                 : launch_fwd_t<128>(grid, mq, mk, mv, a, sched, st);
+                       const VarlenTable* vt, cudaStream_t st) {
+  if (vt != nullptr)
+    return D == 64 ? launch_fwd_t<64>(grid, mq, mk, mv, a, sched, *vt, st)
+                   : launch_fwd_t<128>(grid, mq, mk, mv, a, sched, *vt, st);
+  const NoVarlen none{};
+  return D == 64 ? launch_fwd_t<64>(grid, mq, mk, mv, a, sched, none, st)
+                 : launch_fwd_t<128>(grid, mq, mk, mv, a, sched, none, st);
 }
 
 cudaError_t take_fwd_status(cudaStream_t st, unsigned* out) {

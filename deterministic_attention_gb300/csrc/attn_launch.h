@@ -42,6 +42,41 @@ __host__ __device__ inline int qtile_snake_count(int i, int total, int n_pipes) 
 // one at D = 128.
 constexpr int qtile_pipes_per_block(int D) { return D == 64 ? 2 : 1; }
 
+// Packed variable-length batches: sequence s holds query rows cu_q[s] ..
+// cu_q[s + 1] - 1 of the packed [total_q, Hq, D] tensors and key rows
+// cu_k[s] .. cu_k[s + 1] - 1 of the [total_k, Hkv, D] ones.  Under the
+// causal mask query i of s sees key j of s iff j <= i + tk - tq (the mask
+// ends in the bottom-right corner of the tq x tk score matrix).  The table
+// travels as a __grid_constant__ kernel parameter; `tile` lists the work
+// tiles heaviest first as (s << 16) | tile index within s: 128-query tiles
+// for the forward and dQ steps, 128-key tiles for the dK/dV step.  The
+// backward's row statistics of sequence s start at position ps[s] (a
+// multiple of 128) of each query head's row, so every tile of them is
+// aligned and positions past tq hold (-inf, -0).
+constexpr int kVarlenMaxSeqs = 256;
+constexpr int kVarlenMaxTiles = 2048;
+struct VarlenTable {
+  int n_seq;
+  int n_tiles;
+  int cu_q[kVarlenMaxSeqs + 1];
+  int cu_k[kVarlenMaxSeqs + 1];
+  int ps[kVarlenMaxSeqs + 1];
+  uint32_t tile[kVarlenMaxTiles];
+};
+// The fixed-length kernels take this empty parameter in its place.
+struct NoVarlen {};
+// Table accessors that also compile (and are never called) for NoVarlen.
+__host__ __device__ inline int vt_tiles(const VarlenTable& v) { return v.n_tiles; }
+__host__ __device__ inline int vt_tiles(const NoVarlen&) { return 0; }
+__host__ __device__ inline uint32_t vt_tile(const VarlenTable& v, int i) { return v.tile[i]; }
+__host__ __device__ inline uint32_t vt_tile(const NoVarlen&, int) { return 0u; }
+__host__ __device__ inline int vt_cu_q(const VarlenTable& v, int s) { return v.cu_q[s]; }
+__host__ __device__ inline int vt_cu_q(const NoVarlen&, int) { return 0; }
+__host__ __device__ inline int vt_cu_k(const VarlenTable& v, int s) { return v.cu_k[s]; }
+__host__ __device__ inline int vt_cu_k(const NoVarlen&, int) { return 0; }
+__host__ __device__ inline int vt_ps(const VarlenTable& v, int s) { return v.ps[s]; }
+__host__ __device__ inline int vt_ps(const NoVarlen&, int) { return 0; }
+
 struct FwdArgs {
   void* o;               // bf16 [B, T, Hq, D]
   float* lse;            // fp32 [B, Hq, T]
@@ -72,9 +107,10 @@ struct DeltaArgs {
 struct BwdArgs {
   const float2* rowstats;  // [B * Hq, Tp] pairs written by the Delta step
   void* dq;              // bf16 [B, T, Hq, D]   (dQ kernel)
-  void* dk;              // bf16 [B, T, Hkv, D]  (dK/dV kernel)
+  void* dk;              // bf16 [B, Tk, Hkv, D]  (dK/dV kernel)
   void* dv;
   int T, Tp, Hq, Hkv;
+  int Tk;                // key rows per batch: T, or total_k when packed
   int n_tiles;           // tiles per (b, head) along T
   int BH;                // B * Hq (dQ) or B * Hkv (dK/dV)
   int cluster;           // dK/dV: blocks sharing one key tile (1, 2, 4 or 8)
@@ -89,11 +125,14 @@ struct BwdArgs {
 };
 
 // Each returns the launch error (cudaSuccess when the kernel was queued).
+// `vt` (not null) selects the packed variable-length form: the tensor maps
+// then cover the packed rows with B = 1, FwdArgs::T / BwdArgs::T is the
+// number of packed query rows, and units / tiles come from the table.
 cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const FwdArgs& a, const QTileSched& sched,
-                       cudaStream_t st);
+                       const VarlenTable* vt, cudaStream_t st);
 // `sms`: the current device's SM count (the grid is persistent).
-cudaError_t launch_delta(const DeltaArgs& a, int sms, cudaStream_t st);
+cudaError_t launch_delta(const DeltaArgs& a, int sms, const VarlenTable* vt, cudaStream_t st);
 // Clusters of c blocks of the dK/dV kernel that can be resident at once on the
 // current device (c = 1: blocks), and the largest c the kernel supports.
 cudaError_t dkdv_max_clusters(int D, int c, int* out);
@@ -103,10 +142,10 @@ int dkdv_max_cluster_size(int D);
 // statistics; Q, K, V, dO must not be written by that step).
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                        bool dependent, cudaStream_t st);
+                        bool dependent, const VarlenTable* vt, cudaStream_t st);
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                      const QTileSched& sched, cudaStream_t st);
+                      const QTileSched& sched, const VarlenTable* vt, cudaStream_t st);
 
 // Launches a one-thread kernel whose bounded wait on a never-completed
 // mbarrier runs out after limit_ns (sets the timeout bit, then returns).

@@ -14,6 +14,8 @@
 
 #include "../../include/detattn.h"
 #include "attn_launch.h"
+#include "embed_launch.h"
+#include "layer_launch.h"
 
 using namespace detattn;
 
@@ -147,12 +149,14 @@ int sm_count(int* out);
 // its key tiles plus two for its Q load and epilogue.  Beyond the size of the
 // listed form, units are dealt round-robin (many units balance by number).
 // Built on the host from the shape and the SM count only; cached.
-void qtile_schedule(int D, int B, int T, int Hq, int causal, int sms, QTileSched* out, int* grid) {
+//
+// Units are numbered heaviest first in groups of `per_group` equal units
+// (the heads, or batches and heads, of one query tile): unit u weighs
+// group_w[u / per_group].
+void qtile_schedule_w(int D, const std::vector<double>& group_w, int per_group, int sms,
+                      QTileSched* out, int* grid) {
   const int NP = qtile_pipes_per_block(D);
-  const int n_m = (T + kTileM - 1) / kTileM;
-  const int BHq = B * Hq;
-  const long units = static_cast<long>(n_m) * BHq;
-  const int kv_tiles = (T + kFwdTileN - 1) / kFwdTileN;
+  const long units = static_cast<long>(group_w.size()) * per_group;
   // One block per SM while there are units for it: a second pipeline on an
   // SM adds far less than a second SM does.
   long blocks = units < sms ? units : sms;
@@ -167,9 +171,7 @@ void qtile_schedule(int D, int B, int T, int Hq, int causal, int sms, QTileSched
   std::vector<double> block_load(blocks, 0.0), pipe_load(pipes, 0.0);
   std::vector<std::vector<uint16_t>> lists(pipes);
   for (long u = 0; u < units; ++u) {
-    const int mt = n_m - 1 - static_cast<int>(u / BHq);
-    const int n_kv = causal ? std::min(kv_tiles, (mt * kTileM + kTileM) / kFwdTileN) : kv_tiles;
-    const double w = n_kv + 2.0;
+    const double w = group_w[u / per_group];
     long bi = 0;
     for (long i = 1; i < blocks; ++i)
       if (block_load[i] < block_load[bi]) bi = i;
@@ -187,6 +189,18 @@ void qtile_schedule(int D, int B, int T, int Hq, int causal, int sms, QTileSched
   }
   out->start[pipes] = static_cast<uint16_t>(n);
   out->n_listed = n;
+}
+
+void qtile_schedule(int D, int B, int T, int Hq, int causal, int sms, QTileSched* out, int* grid) {
+  const int n_m = (T + kTileM - 1) / kTileM;
+  const int kv_tiles = (T + kFwdTileN - 1) / kFwdTileN;
+  std::vector<double> w(n_m);
+  for (int g = 0; g < n_m; ++g) {
+    const int mt = n_m - 1 - g;
+    const int n_kv = causal ? std::min(kv_tiles, (mt * kTileM + kTileM) / kFwdTileN) : kv_tiles;
+    w[g] = n_kv + 2.0;
+  }
+  qtile_schedule_w(D, w, B * Hq, sms, out, grid);
 }
 
 // The schedule depends only on (D, B, T, Hq, causal, SMs): the last one is
@@ -230,7 +244,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   QTileSched sc;
   int g;
   cached_qtile_schedule(D, B, T, Hq, causal, sms, &sc, &g);
-  return launched(launch_fwd(D, g, mq, mk, mv, a, sc, st), "attn_fwd");
+  return launched(launch_fwd(D, g, mq, mk, mv, a, sc, nullptr, st), "attn_fwd");
 }
 
 // Workspace: the row statistics, then (from a 256-byte boundary) the dQ
@@ -252,13 +266,14 @@ int delta_impl(const void* o, const void* dout, const float* lse, void* workspac
   int sms = 0;
   int rc;
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
-  return launched(launch_delta(a, sms, st), "attn_bwd_delta");
+  return launched(launch_delta(a, sms, nullptr, st), "attn_bwd_delta");
 }
 
 BwdArgs bwd_args(const void* workspace, int T, int Hq, int Hkv, float scale, int causal) {
   BwdArgs a{};
   a.rowstats = static_cast<const float2*>(workspace);
   a.T = T;
+  a.Tk = T;
   a.Tp = padded_T(T);
   a.Hq = Hq;
   a.Hkv = Hkv;
@@ -293,14 +308,12 @@ int sm_count(int* out) {
 // a given problem and GPU.  `forced_c` > 0 takes that C (capped at the limit).
 // `resident[i]`: clusters of 2^i blocks the device holds at once (0: none).
 // Returns false when no allowed C can be resident.
-bool dkdv_choose(int B, int T, int Hq, int Hkv, int D, int causal, const int resident[4],
-                 int forced_c, int* c_out, int* ng_out) {
-  const int G = Hq / Hkv;
-  const int n_tiles = (T + kTileN - 1) / kTileN;
-  const int BH = B * Hkv;
-  const int tm = dkdv_tile_m(D);
-  const int m_end = (T + tm - 1) / tm;
-  const long total = static_cast<long>(n_tiles) * BH;
+// The choice over key tiles numbered heaviest first in groups of `per_group`
+// (the KV heads, or batches and KV heads, of one key position): tile t
+// carries items[t / per_group] items.
+bool dkdv_choose_items(const std::vector<int>& items_per_group, int per_group, int D,
+                       const int resident[4], int forced_c, int* c_out, int* ng_out) {
+  const long total = static_cast<long>(items_per_group.size()) * per_group;
   const int cmax = dkdv_max_cluster_size(D);
   double best = 0.0;
   *c_out = 0;
@@ -315,8 +328,7 @@ bool dkdv_choose(int B, int T, int Hq, int Hkv, int D, int causal, const int res
       for (long kt = 0;; ++kt) {
         const long t = kt * ng + ((kt & 1) ? ng - 1 - k : k);
         if (t >= total) break;
-        const int nt = static_cast<int>(t / BH);
-        const int items = G * (m_end - (causal ? nt * kTileN / tm : 0));
+        const int items = items_per_group[t / per_group];
         // Per tile: its share of the items, one item's worth for writing the
         // sums out, and two per peer for the partial-sum exchange (measured:
         // distributed shared memory moves ~9 bytes per clock per SM, and an
@@ -332,6 +344,18 @@ bool dkdv_choose(int B, int T, int Hq, int Hkv, int D, int causal, const int res
     }
   }
   return *c_out != 0;
+}
+
+bool dkdv_choose(int B, int T, int Hq, int Hkv, int D, int causal, const int resident[4],
+                 int forced_c, int* c_out, int* ng_out) {
+  const int G = Hq / Hkv;
+  const int n_tiles = (T + kTileN - 1) / kTileN;
+  const int tm = dkdv_tile_m(D);
+  const int m_end = (T + tm - 1) / tm;
+  std::vector<int> items(n_tiles);
+  for (int nt = 0; nt < n_tiles; ++nt)
+    items[nt] = G * (m_end - (causal ? nt * kTileN / tm : 0));
+  return dkdv_choose_items(items, B * Hkv, D, resident, forced_c, c_out, ng_out);
 }
 
 // dkdv_choose with the current device's residency: `sms` blocks alone, and
@@ -373,8 +397,9 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
   if ((rc = dkdv_schedule(B, T, Hq, Hkv, D, causal, sms, g_dkdv_split, &a.cluster, &a.n_groups)) !=
       DETATTN_OK)
     return rc;
-  return launched(launch_dkdv(D, a.n_groups * a.cluster, mq, mk, mv, mdo, a, after_delta, st),
-                  "attn_bwd_dkdv");
+  return launched(
+      launch_dkdv(D, a.n_groups * a.cluster, mq, mk, mv, mdo, a, after_delta, nullptr, st),
+      "attn_bwd_dkdv");
 }
 
 int dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
@@ -397,7 +422,7 @@ int dq_impl(const void* q, const void* k, const void* v, const void* dout, const
   QTileSched sc;
   int g;
   cached_qtile_schedule(D, B, T, Hq, causal, sms, &sc, &g);
-  return launched(launch_dq(D, g, mq, mk, mv, mdo, a, sc, st), "attn_bwd_dq");
+  return launched(launch_dq(D, g, mq, mk, mv, mdo, a, sc, nullptr, st), "attn_bwd_dq");
 }
 
 int check_workspace(const void* ws, size_t bytes, int B, int T, int Hq) {
@@ -474,6 +499,327 @@ int bwd_steps(const void* q, const void* k, const void* v, const void* o, const 
   return ok_status();
 }
 
+// ------------------------------------------------------------ packed variable-length batches
+// Host form of a packed batch: the kernel tables (query tiles for the
+// forward and dQ steps, key tiles for the dK/dV step) and the per-group work
+// the deals weigh.  Built from the host arrays cu_q, cu_k on every call.
+struct Packed {
+  int n_seq = 0, total_q = 0, total_k = 0, Tp = 0;
+  VarlenTable qt{}, kt{};
+  std::vector<double> q_weight;  // per q-table entry: visible 64-key tiles + 2
+  std::vector<int> k_items;      // per k-table entry: items of one KV head
+};
+
+int check_packed(const int* cu_q, const int* cu_k, int n_seq, int Hq, int Hkv, int D, int causal,
+                 Packed* pk) {
+  if (n_seq < 0 || n_seq > kVarlenMaxSeqs)
+    return fail(DETATTN_ERR_SHAPE, "n_seq=%d: must be in [0, %d]", n_seq, kVarlenMaxSeqs);
+  if (n_seq > 0 && (cu_q == nullptr || cu_k == nullptr))
+    return fail(DETATTN_ERR_NULL, "cu_q and cu_k must not be NULL");
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv != 0)
+    return fail(DETATTN_ERR_SHAPE, "Hq=%d must be a positive multiple of Hkv=%d", Hq, Hkv);
+  if (D != 64 && D != 128) return fail(DETATTN_ERR_HEADDIM, "D=%d: only 64 and 128", D);
+  pk->n_seq = n_seq;
+  if (n_seq == 0) return DETATTN_OK;
+  if (cu_q[0] != 0 || cu_k[0] != 0) return fail(DETATTN_ERR_SHAPE, "cu_q[0] and cu_k[0] must be 0");
+  long ps = 0;
+  for (int s = 0; s < n_seq; ++s) {
+    const long tq = static_cast<long>(cu_q[s + 1]) - cu_q[s];
+    const long tk = static_cast<long>(cu_k[s + 1]) - cu_k[s];
+    if (tq < 0 || tk < 0)
+      return fail(DETATTN_ERR_SHAPE, "sequence %d: cu_q / cu_k must not decrease", s);
+    if (tq > (1L << 22) || tk > (1L << 22))
+      return fail(DETATTN_ERR_SHAPE, "sequence %d longer than 2^22 rows", s);
+    ps += (tq + 127) / 128 * 128;
+  }
+  const double elems = static_cast<double>(cu_q[n_seq]) * Hq * D + static_cast<double>(cu_k[n_seq]) * Hkv * D;
+  if (ps > (1L << 30) || static_cast<double>(ps) * Hq > 1.0e11 || elems > 1.0e12)
+    return fail(DETATTN_ERR_SHAPE, "packed problem too large");
+  pk->total_q = cu_q[n_seq];
+  pk->total_k = cu_k[n_seq];
+  pk->Tp = static_cast<int>(ps);
+  for (VarlenTable* t : {&pk->qt, &pk->kt}) {
+    t->n_seq = n_seq;
+    int p = 0;
+    for (int s = 0; s <= n_seq; ++s) {
+      t->cu_q[s] = cu_q[s];
+      t->cu_k[s] = cu_k[s];
+      t->ps[s] = p;
+      if (s < n_seq) p += (cu_q[s + 1] - cu_q[s] + 127) / 128 * 128;
+    }
+  }
+  // Query tiles, heaviest first (visible 64-key tiles of the tile's last row).
+  struct QE { double w; int s, mt; };
+  std::vector<QE> qe;
+  for (int s = 0; s < n_seq; ++s) {
+    const int tq = cu_q[s + 1] - cu_q[s], tk = cu_k[s + 1] - cu_k[s], off = tk - tq;
+    const int tiles = (tk + kFwdTileN - 1) / kFwdTileN;
+    for (int mt = 0; mt * kTileM < tq; ++mt) {
+      const int last = std::min(mt * kTileM + kTileM - 1, tq - 1) + off;
+      const int n_kv = causal ? (last < 0 ? 0 : std::min(tiles, last / kFwdTileN + 1)) : tiles;
+      qe.push_back({n_kv + 2.0, s, mt});
+    }
+  }
+  // Key tiles, heaviest first (items: query tiles of TM rows that see them).
+  const int tm = dkdv_tile_m(D), G = Hq / Hkv;
+  struct KE { int items, s, nt; };
+  std::vector<KE> ke;
+  for (int s = 0; s < n_seq; ++s) {
+    const int tq = cu_q[s + 1] - cu_q[s], tk = cu_k[s + 1] - cu_k[s], off = tk - tq;
+    const int mq_end = (tq + tm - 1) / tm;
+    for (int nt = 0; nt * kTileN < tk; ++nt) {
+      const int first_q = nt * kTileN - off;
+      const int m_begin = causal ? std::min(mq_end, std::max(0, first_q) / tm) : 0;
+      ke.push_back({G * (mq_end - m_begin), s, nt});
+    }
+  }
+  if (qe.size() > static_cast<size_t>(kVarlenMaxTiles) ||
+      ke.size() > static_cast<size_t>(kVarlenMaxTiles))
+    return fail(DETATTN_ERR_SHAPE, "packed batch has %zu query / %zu key tiles of 128; at most %d",
+                qe.size(), ke.size(), kVarlenMaxTiles);
+  std::stable_sort(qe.begin(), qe.end(), [](const QE& x, const QE& y) { return x.w > y.w; });
+  std::stable_sort(ke.begin(), ke.end(), [](const KE& x, const KE& y) { return x.items > y.items; });
+  pk->qt.n_tiles = static_cast<int>(qe.size());
+  pk->kt.n_tiles = static_cast<int>(ke.size());
+  for (size_t i = 0; i < qe.size(); ++i) {
+    pk->qt.tile[i] = (static_cast<uint32_t>(qe[i].s) << 16) | static_cast<uint32_t>(qe[i].mt);
+    pk->q_weight.push_back(qe[i].w);
+  }
+  for (size_t i = 0; i < ke.size(); ++i) {
+    pk->kt.tile[i] = (static_cast<uint32_t>(ke[i].s) << 16) | static_cast<uint32_t>(ke[i].nt);
+    pk->k_items.push_back(ke[i].items);
+  }
+  return DETATTN_OK;
+}
+
+size_t packed_rowstat_bytes(const Packed& pk, int Hq) {
+  return static_cast<size_t>(Hq) * pk.Tp * sizeof(float2);
+}
+size_t packed_counter_offset(const Packed& pk, int Hq) {
+  return (packed_rowstat_bytes(pk, Hq) + 255) / 256 * 256;
+}
+
+int fwd_varlen_impl(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const Packed& pk, int Hq, int Hkv, int D, float scale, int causal,
+                    cudaStream_t st) {
+  if (pk.qt.n_tiles == 0) return ok_status();
+  CUtensorMap mq, mk, mv;
+  int rc;
+  // Without any key rows the kernels never load K, V, but the tensor maps
+  // still need an address: q stands in.
+  const int tk_rows = pk.total_k > 0 ? pk.total_k : 1;
+  const void* kk = pk.total_k > 0 ? k : q;
+  const void* vv = pk.total_k > 0 ? v : q;
+  if ((rc = encode_rows(&mq, q, 1, pk.total_q, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mk, kk, 1, tk_rows, Hkv, D, kFwdTileN, "k")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mv, vv, 1, tk_rows, Hkv, D, kFwdTileN, "v")) != DETATTN_OK) return rc;
+  FwdArgs a{};
+  a.o = o;
+  a.lse = lse;
+  a.T = pk.total_q;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.n_m = 0;
+  a.BHq = Hq;
+  a.causal = causal;
+  a.scale_log2 = log2e_times(scale);
+  a.wait_ns = g_wait_ns;
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
+  QTileSched sc;
+  int g;
+  qtile_schedule_w(D, pk.q_weight, Hq, sms, &sc, &g);
+  return launched(launch_fwd(D, g, mq, mk, mv, a, sc, &pk.qt, st), "attn_fwd_varlen");
+}
+
+int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes,
+                    const Packed& pk, int Hq, int Hkv, int D, float scale, int causal,
+                    cudaStream_t st) {
+  int rc;
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
+  unsigned* counter = nullptr;
+  if (ws_bytes >= packed_counter_offset(pk, Hq) + 2 * sizeof(unsigned))
+    counter = reinterpret_cast<unsigned*>(static_cast<char*>(ws) + packed_counter_offset(pk, Hq));
+  if (pk.total_q > 0) {
+    DeltaArgs da{o, dout, lse, static_cast<float2*>(ws), 1, pk.total_q, pk.Tp, Hq, D, counter};
+    if ((rc = launched(launch_delta(da, sms, &pk.qt, st), "attn_bwd_varlen (Delta)")) != DETATTN_OK)
+      return rc;
+  }
+  BwdArgs a{};
+  a.rowstats = static_cast<const float2*>(ws);
+  a.T = pk.total_q;
+  a.Tk = pk.total_k;
+  a.Tp = pk.Tp;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.causal = causal;
+  a.scale = scale;
+  a.scale_log2 = log2e_times(scale);
+  a.wait_ns = g_wait_ns;
+  // Maps over rows that no kernel will load (no query rows, or no key rows)
+  // still need an address: the other side's tensor stands in.
+  const int tq_rows = pk.total_q > 0 ? pk.total_q : 1, tk_rows = pk.total_k > 0 ? pk.total_k : 1;
+  const void* qq = pk.total_q > 0 ? q : k;
+  const void* dd = pk.total_q > 0 ? dout : k;
+  const void* kk = pk.total_k > 0 ? k : q;
+  const void* vv = pk.total_k > 0 ? v : q;
+  if (pk.kt.n_tiles > 0) {
+    // dK/dV (every key row belongs to some key tile, so all of dk, dv is written).
+    CUtensorMap mq, mk, mv, mdo;
+    if ((rc = encode_rows(&mq, qq, 1, tq_rows, Hq, D, dkdv_tile_m(D), "q")) != DETATTN_OK) return rc;
+    if ((rc = encode_rows(&mdo, dd, 1, tq_rows, Hq, D, dkdv_tile_m(D), "dout")) != DETATTN_OK)
+      return rc;
+    if ((rc = encode_rows(&mk, kk, 1, tk_rows, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
+    if ((rc = encode_rows(&mv, vv, 1, tk_rows, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
+    BwdArgs b = a;
+    b.dk = dk;
+    b.dv = dv;
+    b.BH = Hkv;
+    const int cmax = dkdv_max_cluster_size(D);
+    int resident[4] = {sms, 0, 0, 0};
+    for (int c = 2, i = 1; c <= cmax && i < 4; c *= 2, ++i) {
+      if (g_dkdv_split > 0 && c != (g_dkdv_split < cmax ? g_dkdv_split : cmax)) continue;
+      cudaError_t e = dkdv_max_clusters(D, c, &resident[i]);
+      if (e != cudaSuccess)
+        return fail(DETATTN_ERR_CUDA, "attn_bwd_varlen: cluster occupancy query: %s",
+                    cudaGetErrorString(e));
+    }
+    if (!dkdv_choose_items(pk.k_items, Hkv, D, resident, g_dkdv_split, &b.cluster, &b.n_groups))
+      return fail(DETATTN_ERR_CUDA, "attn_bwd_varlen: no resident cluster shape for D = %d", D);
+    if ((rc = launched(launch_dkdv(D, b.n_groups * b.cluster, mq, mk, mv, mdo, b, pk.total_q > 0,
+                                   &pk.kt, st),
+                       "attn_bwd_varlen (dK/dV)")) != DETATTN_OK)
+      return rc;
+  }
+  if (pk.qt.n_tiles > 0) {
+    CUtensorMap mq, mk, mv, mdo;
+    if ((rc = encode_rows(&mq, qq, 1, tq_rows, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
+    if ((rc = encode_rows(&mdo, dd, 1, tq_rows, Hq, D, kTileM, "dout")) != DETATTN_OK) return rc;
+    if ((rc = encode_rows(&mk, kk, 1, tk_rows, Hkv, D, kDqTileN, "k")) != DETATTN_OK) return rc;
+    if ((rc = encode_rows(&mv, vv, 1, tk_rows, Hkv, D, kDqTileN, "v")) != DETATTN_OK) return rc;
+    BwdArgs b = a;
+    b.dq = dq;
+    b.BH = Hq;
+    b.unit_counter = counter;
+    QTileSched sc;
+    int g;
+    qtile_schedule_w(D, pk.q_weight, Hq, sms, &sc, &g);
+    if ((rc = launched(launch_dq(D, g, mq, mk, mv, mdo, b, sc, &pk.qt, st),
+                       "attn_bwd_varlen (dQ)")) != DETATTN_OK)
+      return rc;
+  }
+  return ok_status();
+}
+
+// ------------------------------------------------------------ layer GEMM and training step
+// 2-D bf16 tensor map of a row-major matrix with `outer` rows of `inner`
+// contiguous elements (row stride ld elements), box {box_inner, box_outer},
+// 128-byte swizzle.
+int encode_2d(CUtensorMap* m, const void* ptr, long inner, long outer, long ld, int box_inner,
+              int box_outer, const char* what) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_outer)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DETATTN_ERR_CUDA, "tensor map for %s: CUresult %d", what, (int)r);
+  return DETATTN_OK;
+}
+
+int check_gemm(const void* a, int a_mn, long lda, const void* b, int b_mn, long ldb, const void* c,
+               int c_f32, long ldc, int M, int N, int K) {
+  int rc;
+  if ((rc = check_ptrs({{a, "a"}, {b, "b"}, {c, "c"}})) != DETATTN_OK) return rc;
+  if (M < kTileM || N < kGemmBN || K < 64 || M % kTileM || N % kGemmBN || K % 64)
+    return fail(DETATTN_ERR_SHAPE, "GEMM M=%d N=%d K=%d: need multiples of 128, %d and 64", M, N,
+                K, kGemmBN);
+  if (static_cast<double>(M) * N > 4.0e9 || static_cast<double>(M) * K > 4.0e9 ||
+      static_cast<double>(K) * N > 4.0e9 || M > (1 << 24) || N > (1 << 24) || K > (1 << 24))
+    return fail(DETATTN_ERR_SHAPE, "GEMM too large (M=%d N=%d K=%d)", M, N, K);
+  if (a_mn < 0 || a_mn > 1 || b_mn < 0 || b_mn > 1 || c_f32 < 0 || c_f32 > 1)
+    return fail(DETATTN_ERR_SHAPE, "GEMM layout flags must be 0 or 1");
+  if (lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldc < N || lda % 8 || ldb % 8 ||
+      ldc % (c_f32 ? 4 : 8))
+    return fail(DETATTN_ERR_SHAPE,
+                "GEMM leading dimensions lda=%ld ldb=%ld ldc=%ld: too short or not 16-byte rows",
+                lda, ldb, ldc);
+  return DETATTN_OK;
+}
+
+int gemm_impl(const void* a, int a_mn, long lda, const void* b, int b_mn, long ldb, void* c,
+              int c_f32, long ldc, int M, int N, int K, float alpha, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  int rc;
+  if (a_mn)
+    rc = encode_2d(&ma, a, M, K, lda, 64, 64, "a");
+  else
+    rc = encode_2d(&ma, a, K, M, lda, 64, kTileM, "a");
+  if (rc != DETATTN_OK) return rc;
+  if (b_mn)
+    rc = encode_2d(&mb, b, N, K, ldb, 64, 64, "b");
+  else
+    rc = encode_2d(&mb, b, K, N, ldb, 64, kGemmBN, "b");
+  if (rc != DETATTN_OK) return rc;
+  GemmArgs g{};
+  g.c = c;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.ldc = ldc;
+  g.alpha = alpha;
+  g.wait_ns = g_wait_ns;
+  return launched(launch_gemm(a_mn != 0, b_mn != 0, c_f32 != 0, ma, mb, g, st), "layer_gemm");
+}
+
+// Workspace of layer_train_step: the step's intermediates, each 256-byte
+// aligned.  N3 = (Hq + 2 Hkv) D columns of the joined projection.
+struct LayerLayout {
+  size_t qkv, q, k, v, o, lse, dout, dq, dk, dv, dqkv, attn, attn_bytes, total;
+};
+LayerLayout layer_layout(int B, int T, int d, int Hq, int Hkv, int D) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t BT = static_cast<size_t>(B) * T;
+  const size_t N3 = static_cast<size_t>(Hq + 2 * Hkv) * D;
+  LayerLayout l{};
+  size_t at = 0;
+  l.qkv = at;  at += up(BT * N3 * 2);
+  l.q = at;    at += up(BT * Hq * D * 2);
+  l.k = at;    at += up(BT * Hkv * D * 2);
+  l.v = at;    at += up(BT * Hkv * D * 2);
+  l.o = at;    at += up(BT * Hq * D * 2);
+  l.lse = at;  at += up(static_cast<size_t>(B) * Hq * T * 4);
+  l.dout = at; at += up(BT * Hq * D * 2);
+  l.dq = at;   at += up(BT * Hq * D * 2);
+  l.dk = at;   at += up(BT * Hkv * D * 2);
+  l.dv = at;   at += up(BT * Hkv * D * 2);
+  l.dqkv = at; at += up(BT * N3 * 2);
+  l.attn_bytes = counter_offset(B, T, Hq) + 256;
+  l.attn = at; at += up(l.attn_bytes);
+  l.total = at;
+  (void)d;
+  return l;
+}
+
+int check_layer(int B, int T, int d, int Hq, int Hkv, int D) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, Hkv, D, &empty)) != DETATTN_OK) return rc;
+  if (empty) return fail(DETATTN_ERR_SHAPE, "layer step needs B, T >= 1");
+  const long BT = static_cast<long>(B) * T;
+  if (BT % kTileM || d % kTileM || d % kGemmBN || (Hq * D) % kGemmBN ||
+      ((Hq + 2 * Hkv) * D) % kGemmBN)
+    return fail(DETATTN_ERR_SHAPE,
+                "layer step: B*T=%ld, d=%d, Hq*D=%d and (Hq+2Hkv)*D=%d must be multiples of 128", BT,
+                d, Hq * D, (Hq + 2 * Hkv) * D);
+  if (BT > (1 << 24) || d > (1 << 16)) return fail(DETATTN_ERR_SHAPE, "layer step too large");
+  return DETATTN_OK;
+}
+
 // ------------------------------------------------------------ built-in scratch
 // Row statistics for attn_bwd_noalloc: a file-scope device array, so callers
 // that cannot allocate device memory still get the backward.  Every GPU that
@@ -510,6 +856,40 @@ int noalloc_scratch(void** out) {
   // The lookup made the device's context current if it was not yet.
   if (dev < 64) cached[dev] = Entry{current_context_id(), ptr};
   *out = ptr;
+  return DETATTN_OK;
+}
+
+// ------------------------------------------------------------ embedding gradient
+// Workspace of embed_grad: counts [V], offsets [V + 1], cursor [V], unsorted
+// [N], sorted [N] (int32), then the head and tail partial rows, fp32
+// [ceil(N / 32), E] each; every part starts on a 256-byte boundary.
+struct EmbedLayout {
+  size_t counts, offsets, cursor, unsorted, sorted, head, tail, total;
+};
+EmbedLayout embed_layout(int N, int V, int E) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  EmbedLayout l{};
+  size_t at = 0;
+  l.counts = at;   at += up(sizeof(int) * static_cast<size_t>(V));
+  l.offsets = at;  at += up(sizeof(int) * (static_cast<size_t>(V) + 1));
+  l.cursor = at;   at += up(sizeof(int) * static_cast<size_t>(V));
+  l.unsorted = at; at += up(sizeof(int) * static_cast<size_t>(N));
+  l.sorted = at;   at += up(sizeof(int) * static_cast<size_t>(N));
+  const size_t runs = (static_cast<size_t>(N) + 31) / 32;
+  l.head = at;     at += up(sizeof(float) * runs * static_cast<size_t>(E));
+  l.tail = at;     at += up(sizeof(float) * runs * static_cast<size_t>(E));
+  l.total = at;
+  return l;
+}
+
+int check_embed_shape(int N, int V, int E) {
+  if (N < 0 || N > (1 << 30))
+    return fail(DETATTN_ERR_SHAPE, "N=%d tokens: must be in [0, 2^30]", N);
+  if (V < 1 || V > (1 << 30)) return fail(DETATTN_ERR_SHAPE, "V=%d rows: must be in [1, 2^30]", V);
+  if (E < 4 || E % 4 != 0 || E > (1 << 20))
+    return fail(DETATTN_ERR_SHAPE, "E=%d columns: must be a positive multiple of 4 up to 2^20", E);
+  if (static_cast<double>(V) * E > 4.0e11 || static_cast<double>(N) * E > 4.0e11)
+    return fail(DETATTN_ERR_SHAPE, "embedding problem too large (N=%d V=%d E=%d)", N, V, E);
   return DETATTN_OK;
 }
 
@@ -661,19 +1041,194 @@ int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
   return dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, nullptr, st);
 }
 
+size_t embed_grad_workspace_bytes(int N, int V, int E) {
+  if (check_embed_shape(N, V, E) != DETATTN_OK) return 0;
+  return embed_layout(N, V, E).total;
+}
+
+int embed_grad(const int* ids, const void* dy, float* dw, void* workspace, size_t workspace_bytes,
+               int N, int V, int E, void* stream) {
+  int rc;
+  if ((rc = check_embed_shape(N, V, E)) != DETATTN_OK) return rc;
+  if (N > 0 && (rc = check_ptrs({{ids, "ids"}, {dy, "dy"}})) != DETATTN_OK) return rc;
+  if ((rc = check_ptrs({{dw, "dw"}, {workspace, "workspace"}})) != DETATTN_OK) return rc;
+  const EmbedLayout l = embed_layout(N, V, E);
+  if (workspace_bytes < l.total)
+    return fail(DETATTN_ERR_WORKSPACE, "embed_grad workspace needs %zu bytes, got %zu", l.total,
+                workspace_bytes);
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
+  char* w = static_cast<char*>(workspace);
+  EmbedArgs a{};
+  a.ids = ids;
+  a.dy = dy;
+  a.dw = dw;
+  a.N = N;
+  a.V = V;
+  a.E = E;
+  a.counts = reinterpret_cast<int*>(w + l.counts);
+  a.offsets = reinterpret_cast<int*>(w + l.offsets);
+  a.cursor = reinterpret_cast<int*>(w + l.cursor);
+  a.unsorted = reinterpret_cast<int*>(w + l.unsorted);
+  a.sorted = reinterpret_cast<int*>(w + l.sorted);
+  a.head = reinterpret_cast<float*>(w + l.head);
+  a.tail = reinterpret_cast<float*>(w + l.tail);
+  return launched(launch_embed_grad(a, sms, static_cast<cudaStream_t>(stream)), "embed_grad");
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_q, const int* cu_k, int n_seq, int Hq, int Hkv, int D,
+                    float scale, int causal, void* stream) {
+  int rc;
+  static thread_local Packed pk;
+  pk = Packed{};
+  if ((rc = check_packed(cu_q, cu_k, n_seq, Hq, Hkv, D, causal, &pk)) != DETATTN_OK) return rc;
+  if ((rc = check_scale(scale, causal)) != DETATTN_OK) return rc;
+  if (pk.total_q == 0) return ok_status();
+  if ((rc = check_ptrs({{q, "q"}, {o, "o"}, {lse, "lse"}})) != DETATTN_OK) return rc;
+  if (pk.total_k > 0 && (rc = check_ptrs({{k, "k"}, {v, "v"}})) != DETATTN_OK) return rc;
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  return fwd_varlen_impl(q, k, v, o, lse, pk, Hq, Hkv, D, scale, causal,
+                         static_cast<cudaStream_t>(stream));
+}
+
+size_t attn_bwd_varlen_workspace_bytes(const int* cu_q, const int* cu_k, int n_seq, int Hq,
+                                       int Hkv, int D) {
+  static thread_local Packed pk;
+  pk = Packed{};
+  if (check_packed(cu_q, cu_k, n_seq, Hq, Hkv, D, 1, &pk) != DETATTN_OK || pk.total_q == 0)
+    return 0;
+  return packed_counter_offset(pk, Hq) + 256;
+}
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                    size_t workspace_bytes, const int* cu_q, const int* cu_k, int n_seq, int Hq,
+                    int Hkv, int D, float scale, int causal, void* stream) {
+  int rc;
+  static thread_local Packed pk;
+  pk = Packed{};
+  if ((rc = check_packed(cu_q, cu_k, n_seq, Hq, Hkv, D, causal, &pk)) != DETATTN_OK) return rc;
+  if ((rc = check_scale(scale, causal)) != DETATTN_OK) return rc;
+  if (pk.total_q == 0 && pk.total_k == 0) return ok_status();
+  if (pk.total_q > 0 &&
+      (rc = check_ptrs({{q, "q"}, {o, "o"}, {lse, "lse"}, {dout, "dout"}, {dq, "dq"}})) != DETATTN_OK)
+    return rc;
+  if (pk.total_k > 0 && (rc = check_ptrs({{k, "k"}, {v, "v"}, {dk, "dk"}, {dv, "dv"}})) != DETATTN_OK)
+    return rc;
+  if (pk.total_q > 0) {
+    if (workspace == nullptr || workspace_bytes < packed_rowstat_bytes(pk, Hq))
+      return fail(DETATTN_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu%s",
+                  packed_rowstat_bytes(pk, Hq), workspace_bytes, workspace ? "" : " (NULL)");
+    if (!aligned16(workspace)) return fail(DETATTN_ERR_ALIGN, "workspace is not 16-byte aligned");
+  }
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  return bwd_varlen_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, pk, Hq, Hkv,
+                         D, scale, causal, static_cast<cudaStream_t>(stream));
+}
+
+int layer_gemm(const void* a, int a_mn_major, int lda, const void* b, int b_mn_major, int ldb,
+               void* c, int c_fp32, int ldc, int M, int N, int K, float alpha, void* stream) {
+  int rc;
+  if ((rc = check_gemm(a, a_mn_major, lda, b, b_mn_major, ldb, c, c_fp32, ldc, M, N, K)) !=
+      DETATTN_OK)
+    return rc;
+  if (!std::isfinite(alpha)) return fail(DETATTN_ERR_SCALE, "alpha must be finite");
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  return gemm_impl(a, a_mn_major, lda, b, b_mn_major, ldb, c, c_fp32, ldc, M, N, K, alpha,
+                   static_cast<cudaStream_t>(stream));
+}
+
+size_t layer_workspace_bytes(int B, int T, int d, int Hq, int Hkv, int D) {
+  if (check_layer(B, T, d, Hq, Hkv, D) != DETATTN_OK) return 0;
+  return layer_layout(B, T, d, Hq, Hkv, D).total;
+}
+
+int layer_train_step(const void* x, const void* dy, float* w_qkv, float* w_o, float* m_qkv,
+                     float* v_qkv, float* m_o, float* v_o, void* w_qkv_bf16, void* w_o_bf16,
+                     float* g_qkv, float* g_o, void* y, void* dx, void* workspace,
+                     size_t workspace_bytes, int B, int T, int d, int Hq, int Hkv, int D, int step,
+                     float lr, float weight_decay, float beta1, float beta2, float eps,
+                     void* stream) {
+  int rc;
+  if ((rc = check_layer(B, T, d, Hq, Hkv, D)) != DETATTN_OK) return rc;
+  if ((rc = check_ptrs({{x, "x"}, {dy, "dy"}, {w_qkv, "w_qkv"}, {w_o, "w_o"}, {m_qkv, "m_qkv"},
+                        {v_qkv, "v_qkv"}, {m_o, "m_o"}, {v_o, "v_o"}, {w_qkv_bf16, "w_qkv_bf16"},
+                        {w_o_bf16, "w_o_bf16"}, {g_qkv, "g_qkv"}, {g_o, "g_o"}, {y, "y"},
+                        {workspace, "workspace"}})) != DETATTN_OK)
+    return rc;
+  if (dx != nullptr && !aligned16(dx)) return fail(DETATTN_ERR_ALIGN, "dx is not 16-byte aligned");
+  if (step < 1) return fail(DETATTN_ERR_SHAPE, "step=%d: AdamW steps count from 1", step);
+  for (float f : {lr, weight_decay, beta1, beta2, eps})
+    if (!std::isfinite(f) || f < 0.f) return fail(DETATTN_ERR_SCALE, "AdamW settings must be finite and >= 0");
+  if (!(beta1 < 1.f) || !(beta2 < 1.f)) return fail(DETATTN_ERR_SCALE, "AdamW betas must be < 1");
+  const LayerLayout l = layer_layout(B, T, d, Hq, Hkv, D);
+  if (workspace_bytes < l.total)
+    return fail(DETATTN_ERR_WORKSPACE, "layer workspace needs %zu bytes, got %zu", l.total,
+                workspace_bytes);
+  if ((rc = check_device()) != DETATTN_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
+  char* w = static_cast<char*>(workspace);
+  void *qkv = w + l.qkv, *q = w + l.q, *k = w + l.k, *v = w + l.v, *o = w + l.o, *dout = w + l.dout;
+  void *dq = w + l.dq, *dk = w + l.dk, *dv = w + l.dv, *dqkv = w + l.dqkv, *aws = w + l.attn;
+  float* lse = reinterpret_cast<float*>(w + l.lse);
+  const int BT = B * T, HqD = Hq * D, N3 = (Hq + 2 * Hkv) * D;
+  const float scale = 1.0f / std::sqrt(static_cast<float>(D));
+  RopeArgs ra{B, T, Hq, Hkv, D, 13.287712379549449f /* log2(10000) */};
+  // Forward: projection, rotary positions, attention, output projection.
+  if ((rc = gemm_impl(x, 0, d, w_qkv_bf16, 1, N3, qkv, 0, N3, BT, N3, d, 1.f, st)) != DETATTN_OK)
+    return rc;
+  if ((rc = launched(launch_rope_split(qkv, q, k, v, ra, sms, st), "rope")) != DETATTN_OK) return rc;
+  if ((rc = fwd_impl(q, k, v, o, lse, B, T, Hq, Hkv, D, scale, 1, st)) != DETATTN_OK) return rc;
+  if ((rc = gemm_impl(o, 0, HqD, w_o_bf16, 1, d, y, 0, d, BT, d, HqD, 1.f, st)) != DETATTN_OK)
+    return rc;
+  // Backward: dO = dY Wo^T, attention backward, rotary transpose, weight
+  // gradients, input gradient.
+  if ((rc = gemm_impl(dy, 0, d, w_o_bf16, 0, d, dout, 0, HqD, BT, HqD, d, 1.f, st)) != DETATTN_OK)
+    return rc;
+  if ((rc = bwd_steps(q, k, v, o, lse, dout, dq, dk, dv, aws, l.attn_bytes, B, T, Hq, Hkv, D, scale,
+                      1, st)) != DETATTN_OK)
+    return rc;
+  if ((rc = launched(launch_rope_merge(dq, dk, dv, dqkv, ra, sms, st), "rope")) != DETATTN_OK)
+    return rc;
+  if ((rc = gemm_impl(o, 1, HqD, dy, 1, d, g_o, 1, d, HqD, d, BT, 1.f, st)) != DETATTN_OK) return rc;
+  if ((rc = gemm_impl(x, 1, d, dqkv, 1, N3, g_qkv, 1, N3, d, N3, BT, 1.f, st)) != DETATTN_OK)
+    return rc;
+  if (dx != nullptr &&
+      (rc = gemm_impl(dqkv, 0, N3, w_qkv_bf16, 0, N3, dx, 0, d, BT, d, N3, 1.f, st)) != DETATTN_OK)
+    return rc;
+  // AdamW on both weights (fp32 master copies and moments; new bf16 copies).
+  AdamArgs aa{lr, weight_decay, beta1, beta2, eps, step};
+  if ((rc = launched(launch_adamw(w_qkv, m_qkv, v_qkv, g_qkv, w_qkv_bf16,
+                                  static_cast<long>(d) * N3, aa, sms, st),
+                     "adamw")) != DETATTN_OK)
+    return rc;
+  return launched(launch_adamw(w_o, m_o, v_o, g_o, w_o_bf16, static_cast<long>(HqD) * d, aa, sms, st),
+                  "adamw");
+}
+
 int detattn_check_status(void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  unsigned f = 0, b = 0;
+  unsigned f = 0, b = 0, em = 0, ly = 0;
   cudaError_t e = take_fwd_status(st, &f);
   if (e == cudaSuccess) e = take_bwd_status(st, &b);
+  if (e == cudaSuccess) e = take_embed_status(st, &em);
+  if (e == cudaSuccess) e = take_layer_status(st, &ly);
   if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (em & 1u)
+    return fail(DETATTN_ERR_INDEX,
+                "embed_grad found token ids outside [0, V); those tokens were left out of dw");
   if (b & 16u)
     return fail(DETATTN_ERR_WORKSPACE,
                 "the dQ step found its tile counter not cleared: run attn_bwd_delta on this "
                 "workspace (with the same workspace_bytes) first");
-  if (f | b)
+  if (f | b | ly)
     return fail(DETATTN_ERR_DEVICE_TIMEOUT,
-                "a kernel gave up on a pipeline wait (fwd flags %u, bwd flags %u)", f, b);
+                "a kernel gave up on a pipeline wait (fwd flags %u, bwd flags %u, layer flags %u)",
+                f, b, ly);
   return ok_status();
 }
 

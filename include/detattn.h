@@ -62,9 +62,11 @@ typedef enum {
   DETATTN_ERR_CUDA = -6,           /* a CUDA runtime / driver call failed */
   DETATTN_ERR_DEVICE_TIMEOUT = -7, /* a kernel gave up waiting on a pipeline barrier */
   DETATTN_ERR_ARCH = -8,           /* current device is not compute capability 10.3 */
-  DETATTN_ERR_WORKSPACE = -9       /* workspace NULL or too small; from detattn_check_status:
+  DETATTN_ERR_WORKSPACE = -9,      /* workspace NULL or too small; from detattn_check_status:
                                       a dQ step ran on a workspace attn_bwd_delta had not
                                       prepared */
+  DETATTN_ERR_INDEX = -10          /* from detattn_check_status: embed_grad met token ids
+                                      outside [0, V) (it left those tokens out) */
 } detattn_status;
 
 /* Forward.  Writes o [B,T,Hq,D] (bf16) and lse [B,Hq,T] (fp32).
@@ -158,12 +160,149 @@ int attn_bwd_dq(const void* q, const void* k, const void* v, const void* dout,
                 const void* workspace, size_t workspace_bytes, void* dq, int B, int T, int Hq,
                 int Hkv, int D, float scale, int causal, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Packed variable-length batches (several sequences of their own lengths in
+ * one call, and cross-attention with Tq != Tk).  No page describes them; they
+ * are the same computation per sequence (the operation above, with the
+ * RustingBrain page's fused kernels) over packed rows:
+ *
+ *   q, o, dout, dq : bf16 [total_q, Hq, D]    k, v, dk, dv : bf16 [total_k, Hkv, D]
+ *   lse            : fp32 [Hq, total_q]
+ *   cu_q, cu_k     : HOST int32 arrays of n_seq + 1 nondecreasing offsets,
+ *                    cu[0] = 0, total = cu[n_seq]; sequence s owns query rows
+ *                    cu_q[s] .. cu_q[s+1]-1 and key rows cu_k[s] .. cu_k[s+1]-1
+ *
+ * With tq = cu_q[s+1] - cu_q[s] and tk likewise, query i of s sees key j of
+ * s iff j <= i + tk - tq when causal (the mask ends in the bottom-right
+ * corner, which is j <= i when tq == tk), every key of s otherwise.  A query
+ * row that sees no key (causal, tq > tk) gets o = 0, lse = -inf and dq = 0;
+ * a key no query sees gets dk = dv = 0.  Empty sequences are allowed.
+ * Limits: n_seq <= 256; each sequence <= 2^22 rows; at most 2048 tiles of
+ * 128 query rows and 2048 of 128 key rows over the batch (DETATTN_ERR_SHAPE
+ * beyond).  Results are deterministic like the fixed-length calls.  The
+ * tile tables are built on the host from cu_q, cu_k at every call and passed
+ * as kernel parameters, so nothing is allocated. */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_q, const int* cu_k, int n_seq, int Hq, int Hkv, int D,
+                    float scale, int causal, void* stream);
+
+/* Workspace bytes of attn_bwd_varlen: R + 256, with R = Hq * Tp * 8 rounded
+ * up to 256 and Tp = the sum over sequences of tq rounded up to 128 (row
+ * statistics per query head, each sequence's starting at a multiple of 128,
+ * then the dQ step's two counter words).  0 for an invalid or query-less
+ * batch. */
+size_t attn_bwd_varlen_workspace_bytes(const int* cu_q, const int* cu_k, int n_seq, int Hq,
+                                       int Hkv, int D);
+
+/* Packed variable-length backward: writes dq, dk, dv.  Runs the Delta,
+ * dK/dV and dQ steps on `stream` in that order. */
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                    const void* dout, void* dq, void* dk, void* dv, void* workspace,
+                    size_t workspace_bytes, const int* cu_q, const int* cu_k, int n_seq, int Hq,
+                    int Hkv, int D, float scale, int causal, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Deterministic embedding-lookup gradient (oxide-train README, "The trainer
+ * is not bit-identical to itself after step 1": its embedding gradient is
+ * summed with atomics, so two runs of one binary disagree from step 2 on;
+ * "Full-step profiling": B = 32, T = 1024, vocabulary 50,257 padded to
+ * 50,432, width 1536).  For the lookup X[t,:] = W[ids[t],:]:
+ *
+ *   dw[v,:] = sum over t with ids[t] == v of dy[t,:]
+ *
+ * Every element is one fp32 sum whose order depends on the ids only: the
+ * tokens of an id are taken in ascending position, in runs of 32 entries of
+ * the id-sorted token list; an id whose tokens span several runs has one
+ * partial sum per run, added in run order.  Integer atomics only count
+ * tokens and hand out slots, which changes no bit of dw, so repeated calls
+ * give identical bytes.
+ *
+ * Layout: ids int32 [N]; dy bf16 [N, E] (row-major); dw fp32 [V, E]
+ * (row-major, fully overwritten: rows no token selects are zero).  E must be
+ * a multiple of 4 (up to 2^20), N in [0, 2^30], V in [1, 2^30].  Pointers are
+ * device pointers, 16-byte aligned; ids and dy may be NULL when N == 0.
+ * Tokens whose id lies outside [0, V) are left out of dw and reported by
+ * detattn_check_status (DETATTN_ERR_INDEX); they are never used as an index.
+ * The call queues one memset and up to six kernels on `stream`.
+ */
+
+/* Bytes of workspace embed_grad needs: int32 counts [V], offsets [V + 1],
+ * cursor [V], two token lists [N], and two fp32 [ceil(N / 32), E] blocks of
+ * partial rows, each part 256-byte aligned.  0 for an invalid shape. */
+size_t embed_grad_workspace_bytes(int N, int V, int E);
+
+/* Writes dw from ids and dy (see above).  `workspace` is caller-owned device
+ * memory of embed_grad_workspace_bytes(N, V, E) bytes, contents on entry
+ * irrelevant.  Returns DETATTN_OK or DETATTN_ERR_SHAPE / _NULL / _ALIGN /
+ * _WORKSPACE / _ARCH / _CUDA (nothing launched on an error). */
+int embed_grad(const int* ids, const void* dy, float* dw, void* workspace, size_t workspace_bytes,
+               int N, int V, int E, void* stream);
+
+/* ------------------------------------------------------------------------
+ * One attention layer of a training step, and its AdamW update (RustingBrain
+ * vs PyTorch/TensorFlow page, "The setup": d_model 768, 12 query heads over 4
+ * KV heads of head_dim 64, rotary positions; "Where the time goes now":
+ * GEMMs are most of the step; oxide-train README: the step ends in AdamW
+ * with LR 3e-4 and weight decay 0.1, and "The trainer is not bit-identical
+ * to itself after step 1").  Every kernel writes each output element once in
+ * a fixed order, with no atomics on data, so repeated steps give identical
+ * gradients and weights.
+ */
+
+/* C[M, N] = alpha * A[M, K] B[K, N] on the tensor cores: bf16 A and B, fp32
+ * accumulation, C bf16 (c_fp32 = 0) or fp32 (c_fp32 = 1), row-major with row
+ * stride ldc elements.  a_mn_major = 0: A is stored [M rows, K] (row stride
+ * lda); 1: A is stored transposed, [K rows, M] (row stride lda).  Likewise
+ * b_mn_major = 1: B stored [K rows, N]; 0: stored transposed, [N rows, K].
+ * M must be a multiple of 128, N of 128 and K of 64; row strides hold whole
+ * rows and make 16-byte rows.  Every element of C is one block's sum over K
+ * in ascending order.  Device pointers, 16-byte aligned. */
+int layer_gemm(const void* a, int a_mn_major, int lda, const void* b, int b_mn_major, int ldb,
+               void* c, int c_fp32, int ldc, int M, int N, int K, float alpha, void* stream);
+
+/* Workspace bytes of layer_train_step (its intermediates: the joined QKV
+ * projection, the rotated Q, K and V, O, LSE, dO, dQ, dK, dV, the joined
+ * gradient of the projection, and the attention backward's workspace).  0
+ * for an invalid shape. */
+size_t layer_workspace_bytes(int B, int T, int d, int Hq, int Hkv, int D);
+
+/* One training step of one attention layer at the current weights, then one
+ * AdamW update of them:
+ *
+ *   QKV = X Wqkv  (Wqkv = [Wq | Wk | Wv], [d, (Hq + 2 Hkv) D])
+ *   Q, K = rope(Q, K), V      (rotate-half: component i of a head's first
+ *                              half turns with component i of its second half
+ *                              by t * 10000^(-2i/D), t = position in the
+ *                              sequence; the pages name rotary positions
+ *                              without a convention)
+ *   O = causal GQA attention (attn_fwd), Y = O Wo
+ *   dO = dY Wo^T, (dQ, dK, dV) = attn_bwd, dQ, dK = rope^T(dQ, dK)
+ *   g_o = O^T dY, g_qkv = X^T [dQ | dK | dV], dX = [dQ | dK | dV] Wqkv^T
+ *   AdamW (decoupled decay):  w *= 1 - lr wd; m = b1 m + (1 - b1) g;
+ *     v = b2 v + (1 - b2) g^2; w -= lr (m / (1 - b1^step)) / (sqrt(v / (1 - b2^step)) + eps)
+ *
+ * x, dy, y, dx: bf16 [B, T, d]; w_qkv, m_qkv, v_qkv, g_qkv: fp32 [d, (Hq +
+ * 2 Hkv) D]; w_o, m_o, v_o, g_o: fp32 [Hq D, d]; w_qkv_bf16, w_o_bf16: the
+ * bf16 copies the GEMMs read (the caller sets them from the fp32 weights
+ * before the first step; each step rewrites them after the update).  g_qkv
+ * and g_o receive this step's gradients (at the weights before the update);
+ * dx may be NULL.  The scale is 1/sqrt(D) and the attention is causal.
+ * B*T, d, Hq*D and (Hq + 2 Hkv)*D must be multiples of 128, D 64 or 128.
+ * step counts from 1.  All on `stream`. */
+int layer_train_step(const void* x, const void* dy, float* w_qkv, float* w_o, float* m_qkv,
+                     float* v_qkv, float* m_o, float* v_o, void* w_qkv_bf16, void* w_o_bf16,
+                     float* g_qkv, float* g_o, void* y, void* dx, void* workspace,
+                     size_t workspace_bytes, int B, int T, int d, int Hq, int Hkv, int D, int step,
+                     float lr, float weight_decay, float beta1, float beta2, float eps,
+                     void* stream);
+
 /* Synchronises `stream`, then reads and clears the device-side status word
  * that kernels set when a pipeline wait runs out (a bounded wait, default
  * limit 1 s).  Returns DETATTN_OK, DETATTN_ERR_DEVICE_TIMEOUT,
  * DETATTN_ERR_WORKSPACE (a dQ step found the workspace's tile counter not
  * cleared, i.e. attn_bwd_delta had not run on that workspace: that dQ
- * step's dq is not valid) or DETATTN_ERR_CUDA. */
+ * step's dq is not valid), DETATTN_ERR_INDEX (embed_grad met ids outside
+ * [0, V)) or DETATTN_ERR_CUDA. */
 int detattn_check_status(void* stream);
 
 /* Diagnostic for accuracy tests: evaluates on n device floats x the three

@@ -286,3 +286,77 @@ def test_kernels_fit_their_launch_without_spills(L):
                 seen.add(key)
                 assert regs * threads <= 65536, f"{name}: {regs} registers x {threads} threads"
     assert seen == set(_KERNEL_THREADS_PER_SM), f"kernels not found in the reports: {seen}"
+
+
+def test_embed_grad_rejects_before_any_device_call(L):
+    """embed_grad validates shapes, pointers and the workspace on the host."""
+    def call(N=64, V=100, E=128, ids=P, dy=P, dw=P, ws=P, wsb=1 << 30):
+        return L.embed_grad(ids, dy, dw, ws, wsb, N, V, E, None)
+    assert call(N=-1) == -3
+    assert call(V=0) == -3
+    assert call(E=6) == -3                       # not a multiple of 4
+    assert call(E=0) == -3
+    assert call(ids=None) == -1
+    assert call(dw=None) == -1
+    assert call(ws=None) == -1
+    assert call(dy=BAD) == -2
+    assert call(wsb=16) == -9
+    assert "workspace needs" in da.last_error()
+    assert L.embed_grad_workspace_bytes(-1, 5, 8) == 0
+    # counts, offsets, cursor (V, V + 1, V ints), two token lists (N ints) and
+    # two partial-row blocks of ceil(N / 32) x E floats, each 256-aligned.
+    up = lambda x: (x + 255) // 256 * 256
+    N, V, E = 1000, 50432, 1536
+    want = (up(4 * V) + up(4 * (V + 1)) + up(4 * V) + 2 * up(4 * N)
+            + 2 * up(4 * ((N + 31) // 32) * E))
+    assert L.embed_grad_workspace_bytes(N, V, E) == want
+    if not _has_gpu():
+        assert call() == -6                     # valid: only the missing device stops it
+        assert call(N=0, ids=None, dy=None) == -6
+
+
+def test_varlen_rejects_before_any_device_call(L):
+    """attn_fwd_varlen / attn_bwd_varlen validate the host offsets first."""
+    def fwd(cu_q, cu_k, n_seq=None, Hq=4, Hkv=2, D=64, ptr=P):
+        cq = np.asarray(cu_q, dtype=np.int32)
+        ck = np.asarray(cu_k, dtype=np.int32)
+        n = len(cq) - 1 if n_seq is None else n_seq
+        return L.attn_fwd_varlen(P, P, P, ptr, P, ctypes.c_void_p(cq.ctypes.data),
+                                 ctypes.c_void_p(ck.ctypes.data), n, Hq, Hkv, D, 0.125, 1, None)
+    assert fwd([1, 5], [0, 5]) == -3                 # does not start at 0
+    assert fwd([0, 5, 3], [0, 5, 9]) == -3           # decreases
+    assert fwd([0, 5], [0, 5], n_seq=257) == -3      # too many sequences
+    assert fwd([0, 5], [0, 5], Hq=3) == -3
+    assert fwd([0, 5], [0, 5], D=32) == -4
+    assert fwd([0, 5], [0, 5], ptr=None) == -1
+    assert fwd([0, 0, 0], [0, 4, 9]) == 0            # no query rows: nothing to do
+    # More than 2048 query tiles of 128 rows over the batch: 9 x 65,536 rows.
+    big = [65536 * i for i in range(10)]
+    assert fwd(big, big) == -3
+    assert "tiles" in da.last_error()
+    assert L.attn_bwd_varlen_workspace_bytes(None, None, 1, 4, 2, 64) == 0
+    cq = np.asarray([0, 100, 300], dtype=np.int32)
+    ws = L.attn_bwd_varlen_workspace_bytes(ctypes.c_void_p(cq.ctypes.data),
+                                           ctypes.c_void_p(cq.ctypes.data), 2, 4, 2, 64)
+    # Row statistics: Hq * (128 + 256) pairs of 8 bytes, rounded to 256, + 256.
+    assert ws == (4 * 384 * 8 + 255) // 256 * 256 + 256
+    if not _has_gpu():
+        assert fwd([0, 100, 300], [0, 100, 300]) == -6
+
+
+def test_layer_calls_reject_before_any_device_call(L):
+    def gemm(M=128, N=128, K=64, lda=64, ldb=128, ldc=128, a=P, a_mn=0, b_mn=1, c_f32=0):
+        return L.layer_gemm(a, a_mn, lda, P, b_mn, ldb, P, c_f32, ldc, M, N, K, 1.0, None)
+    assert gemm(M=100) == -3
+    assert gemm(N=96) == -3
+    assert gemm(K=32) == -3
+    assert gemm(lda=32) == -3           # shorter than K
+    assert gemm(ldc=100) == -3
+    assert gemm(a=None) == -1
+    assert gemm(a=BAD) == -2
+    assert gemm(a_mn=2) == -3
+    assert L.layer_workspace_bytes(4, 1024, 768, 12, 4, 64) > 0
+    assert L.layer_workspace_bytes(4, 1000, 768, 12, 4, 64) == 0   # B*T not a multiple of 128
+    assert L.layer_workspace_bytes(4, 1024, 700, 12, 4, 64) == 0
+    if not _has_gpu():
+        assert gemm() == -6
