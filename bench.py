@@ -138,7 +138,7 @@ class ClockSampler:
 class Problem:
     """One replica's device buffers (several rotating sets) and the step."""
 
-    def __init__(self, w, n_sets, device):
+    def __init__(self, w, n_sets, device, stored_ds=False):
         import deterministic_attention_gb300 as da
         self.da, self.w = da, w
         B, T, Hq, Hkv, D = w.shape
@@ -150,7 +150,7 @@ class Problem:
             outs = dict(o=torch.empty_like(ins[0]), dq=torch.empty_like(ins[0]),
                         dk=torch.empty_like(ins[1]), dv=torch.empty_like(ins[2]),
                         lse=torch.empty((B, Hq, T), dtype=torch.float32, device=device),
-                        ws=da.new_workspace(*w.shape, device=device))
+                        ws=da.new_workspace(*w.shape, device=device, stored_ds=stored_ds))
             self.sets.append((ins, outs))
         self.scale = w.softmax_scale
 
@@ -292,11 +292,11 @@ def run_gpu_arm(args, world, rank):
     w = WORKLOADS[args.workload]
     B, T, Hq, Hkv, D = w.shape
     dev = torch.device("cuda", torch.cuda.current_device())
-    probe = Problem(w, 1, dev)
+    probe = Problem(w, 1, dev, stored_ds=args.stored_ds)
     per_set = probe.set_bytes()
     del probe
     n_sets = max(1, math.ceil(1.5 * L2_BYTES / per_set))
-    P = Problem(w, n_sets, dev)
+    P = Problem(w, n_sets, dev, stored_ds=args.stored_ds)
 
     # Gate: finite outputs and bitwise-identical repeats before anything is timed.
     ref = None
@@ -445,6 +445,8 @@ def run_gpu_arm(args, world, rank):
                              f"replayed {runner.full}x, then {runner.rem} steps; exactly {K} steps "
                              f"per trial, median of {trials['n']} trials",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "backward": "stored dS (dQ = scale dS K)" if args.stored_ds
+                               else "dQ recomputes S and dP",
                    "flop_convention": "fwd 2*B*Hq*T^2*D (causal half), fwd+bwd 3.5x fwd"},
         "pct_of_peak": value / world / peak,
         "fwd_tflops": world * w.fwd_flops() / (per_kernel_ms["attn_fwd"] * 1e-3) / 1e12,
@@ -920,6 +922,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stored-ds", action="store_true",
+                    help="give attn_bwd the workspace of the stored-dS backward")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -26,7 +26,7 @@ __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_delta", "attn_bwd_dkdv", "attn_bwd_
            "DetAttnError", "STATUS", "header_symbols", "build", "embed_grad",
            "embed_grad_workspace_bytes", "attn_fwd_varlen", "attn_bwd_varlen",
            "varlen_workspace_bytes", "layer_gemm", "layer_workspace_bytes", "LayerState",
-           "layer_train_step"]
+           "layer_train_step", "ds_workspace_bytes", "set_bwd_dq_mode"]
 
 STATUS = {0: "DETATTN_OK", -1: "DETATTN_ERR_NULL", -2: "DETATTN_ERR_ALIGN",
           -3: "DETATTN_ERR_SHAPE", -4: "DETATTN_ERR_HEADDIM", -5: "DETATTN_ERR_SCALE",
@@ -71,6 +71,10 @@ def lib() -> ctypes.CDLL:
     L.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, fp, vp, vp, vp, vp, vp, sz, vp, vp, i, i, i, i, f,
                                   i, vp]
     L.attn_bwd_varlen.restype = i
+    L.attn_bwd_ds_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    L.attn_bwd_ds_workspace_bytes.restype = sz
+    L.detattn_set_bwd_dq_mode.argtypes = [i]
+    L.detattn_set_bwd_dq_mode.restype = i
     L.layer_gemm.argtypes = [vp, i, i, vp, i, i, vp, i, i, i, i, i, f, vp]
     L.layer_gemm.restype = i
     L.layer_workspace_bytes.argtypes = [i, i, i, i, i, i]
@@ -197,10 +201,22 @@ def attn_bwd(q, k, v, o, lse, dout, scale=None, causal=True, dq=None, dk=None, d
     return dq, dk, dv
 
 
-def new_workspace(B, T, Hq, Hkv, D, device="cuda"):
-    """A device workspace of attn_bwd_workspace_bytes (uint8)."""
-    return torch.empty((max(16, workspace_bytes(B, T, Hq, Hkv, D)),), dtype=torch.uint8,
-                       device=device)
+def ds_workspace_bytes(B, T, Hq, Hkv, D, causal=True) -> int:
+    return int(lib().attn_bwd_ds_workspace_bytes(B, T, Hq, Hkv, D, int(bool(causal))))
+
+
+def new_workspace(B, T, Hq, Hkv, D, device="cuda", stored_ds=False, causal=True):
+    """A device workspace (uint8) of attn_bwd_workspace_bytes, or with
+    stored_ds of attn_bwd_ds_workspace_bytes (the stored-dS backward)."""
+    n = ds_workspace_bytes(B, T, Hq, Hkv, D, causal) if stored_ds else 0
+    if n == 0:
+        n = workspace_bytes(B, T, Hq, Hkv, D)
+    return torch.empty((max(16, n),), dtype=torch.uint8, device=device)
+
+
+def set_bwd_dq_mode(mode: int):
+    """0: stored-dS backward whenever the workspace holds it (default); 1: never."""
+    _check(lib().detattn_set_bwd_dq_mode(int(mode)), "detattn_set_bwd_dq_mode")
 
 
 def rowstats_view(workspace, B, T, Hq):

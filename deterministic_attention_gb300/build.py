@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libdetattn.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "embed_grad.cu", "layer_ops.cu", "detattn_host.cu"]
+SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "attn_dq_ds.cu", "embed_grad.cu", "layer_ops.cu",
+           "detattn_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

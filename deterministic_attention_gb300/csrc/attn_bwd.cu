@@ -757,6 +757,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           tc_fence_after();
         }
+        if constexpr (!VL) {
+          if (a.ds != nullptr) {
+            // Stored-dS backward: this item's dS^T rows also go to the
+            // workspace, for the dQ step to read instead of recomputing them.
+            const int it = ti.it_lo + li;
+            const int h = ti.g * G + it / ti.per_head;
+            const int m = ti.m_begin + it % ti.per_head;
+            const int mt = m >> 1, kt = ti.n0 / kTileN;
+            const long pr = a.causal ? static_cast<long>(mt) * (mt + 1) / 2 + kt
+                                     : static_cast<long>(mt) * a.n_tiles + kt;
+            const size_t row =
+                (((static_cast<size_t>(ti.b) * a.Hq + h) * a.ds_pairs + pr) * 2 + (m & 1)) * kTileN + r;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ds) + row * TM +
+                                                  grp * QG);
+            static_assert(QG == 16, "two 16-byte stores per thread");
+            dst[0] = make_uint4(dk[0], dk[1], dk[2], dk[3]);
+            dst[1] = make_uint4(dk[4], dk[5], dk[6], dk[7]);
+          }
+        }
         const uint32_t tP = tl + Cf::kColPB + pb * TM + grp * (QG / 2);
         tmem_st_cols<QG / 2>(tP, pk);
         tmem_st_cols<QG / 2>(tP + TM / 2, dk);

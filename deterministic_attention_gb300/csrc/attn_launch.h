@@ -122,7 +122,22 @@ struct BwdArgs {
   // dQ: units are taken from this counter (zero at launch) instead of the
   // static deal, when not null.
   unsigned* unit_counter;
+  // Stored-dS backward (fixed-length only): when not null the dK/dV step
+  // also writes every item's dS^T (bf16) here, pairs (128-query tile mt,
+  // 128-key tile kt) of each (b, h) in the order kt <= mt, mt(mt+1)/2 + kt
+  // (causal) or mt * n_tiles + kt (full); per pair two halves of 64 queries,
+  // each [128 keys][64 queries].  attn_dq_from_ds reads them back.
+  void* ds;
+  long ds_pairs;         // pairs per (b, h)
 };
+
+// dQ from the stored dS: for each 128-query tile, dQ = scale * sum over its
+// key tiles (ascending) of dS K, on the tensor cores.  `mds` is a 2-D map
+// over the dS rows ({64, rows}, box {64, 64}); `mk` maps K with 64-row
+// boxes.  Units (b, h, query tile) heaviest first, one block each.
+cudaError_t launch_dq_from_ds(int D, const CUtensorMap& mds, const CUtensorMap& mk,
+                              const BwdArgs& a, int n_units, cudaStream_t st);
+cudaError_t take_ds_status(cudaStream_t st, unsigned* out);
 
 // Each returns the launch error (cudaSuccess when the kernel was queued).
 // `vt` (not null) selects the packed variable-length form: the tensor maps

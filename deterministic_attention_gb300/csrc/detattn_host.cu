@@ -133,6 +133,21 @@ int encode_rows(CUtensorMap* m, const void* ptr, int B, int T, int H, int D, int
   return DETATTN_OK;
 }
 
+// Tensor map over the stored dS tiles: bf16 rows of 64 (one 128-byte
+// swizzle atom), boxes of 64 rows.
+int encode_2d_rows64(CUtensorMap* m, const void* ptr, long rows) {
+  cuuint64_t dims[2] = {64, static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {64, 64};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DETATTN_ERR_CUDA, "tensor map for dS: CUresult %d", (int)r);
+  return DETATTN_OK;
+}
+
 int launched(cudaError_t e, const char* what) {
   if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
   return ok_status();
@@ -380,7 +395,8 @@ int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int
 
 int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
               const void* workspace, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
-              float scale, int causal, cudaStream_t st, bool after_delta = false) {
+              float scale, int causal, cudaStream_t st, bool after_delta = false,
+              void* ds = nullptr, long ds_pairs = 0) {
   CUtensorMap mq, mk, mv, mdo;
   int rc;
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, dkdv_tile_m(D), "q")) != DETATTN_OK) return rc;
@@ -392,6 +408,8 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
   a.dv = dv;
   a.n_tiles = (T + kTileN - 1) / kTileN;
   a.BH = B * Hkv;
+  a.ds = ds;
+  a.ds_pairs = ds_pairs;
   int sms = 0;
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
   if ((rc = dkdv_schedule(B, T, Hq, Hkv, D, causal, sms, g_dkdv_split, &a.cluster, &a.n_groups)) !=
@@ -472,12 +490,56 @@ int side_stream(SideStream** out) {
   return DETATTN_OK;
 }
 
-// Delta, then dK/dV on `st` and dQ on the side stream.
+// ------------------------------------------------------------ stored-dS backward
+// With a workspace long enough, the dK/dV step also stores each dS tile it
+// forms and the dQ step becomes a plain product dQ = scale dS K (no
+// recomputed S, P, dP): pairs (query tile, key tile) of 128 x 128, two bf16
+// halves of 128 x 64 each, after the row statistics and the counter.
+int g_bwd_dq_mode = 0;  // 0: stored dS whenever the workspace holds it; 1: never
+
+long ds_pairs(int T, int causal) {
+  const long n = (T + kTileM - 1) / kTileM;
+  return causal ? n * (n + 1) / 2 : n * n;
+}
+size_t ds_offset(int B, int T, int Hq) { return counter_offset(B, T, Hq) + 256; }
+size_t ds_region_bytes(int B, int T, int Hq, int causal) {
+  return static_cast<size_t>(B) * Hq * ds_pairs(T, causal) * 2 * kTileN * 64 * 2;
+}
+
+int dq_from_ds_impl(const void* k, const void* ds, void* dq, long pairs, int B, int T, int Hq,
+                    int Hkv, int D, float scale, int causal, cudaStream_t st) {
+  CUtensorMap mds, mk;
+  int rc;
+  const long rows = static_cast<long>(B) * Hq * pairs * 2 * kTileN;
+  if ((rc = encode_2d_rows64(&mds, ds, rows)) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mk, k, B, T, Hkv, D, 64, "k")) != DETATTN_OK) return rc;
+  BwdArgs a = bwd_args(nullptr, T, Hq, Hkv, scale, causal);
+  a.dq = dq;
+  a.n_tiles = (T + kTileM - 1) / kTileM;
+  a.BH = B * Hq;
+  a.ds_pairs = pairs;
+  return launched(launch_dq_from_ds(D, mds, mk, a, a.n_tiles * a.BH, st), "attn_bwd dQ from dS");
+}
+
+// Delta, then dK/dV on `st` and dQ on the side stream (or, with a workspace
+// that holds the dS tiles, dK/dV then dQ from dS, both on `st`).
 int bwd_steps(const void* q, const void* k, const void* v, const void* o, const float* lse,
               const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B,
               int T, int Hq, int Hkv, int D, float scale, int causal, cudaStream_t st) {
   int rc;
   unsigned* counter = unit_counter_ptr(ws, ws_bytes, B, T, Hq);
+  if (g_bwd_dq_mode == 0 && ws_bytes >= ds_offset(B, T, Hq) + ds_region_bytes(B, T, Hq, causal) &&
+      static_cast<double>(B) * Hq * ds_pairs(T, causal) * 2 * kTileN < 2.0e9) {
+    void* ds = static_cast<char*>(ws) + ds_offset(B, T, Hq);
+    const long pairs = ds_pairs(T, causal);
+    if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, counter, st)) != DETATTN_OK) return rc;
+    if ((rc = dkdv_impl(q, k, v, dout, ws, dk, dv, B, T, Hq, Hkv, D, scale, causal, st,
+                        /*after_delta=*/true, ds, pairs)) != DETATTN_OK)
+      return rc;
+    if ((rc = dq_from_ds_impl(k, ds, dq, pairs, B, T, Hq, Hkv, D, scale, causal, st)) != DETATTN_OK)
+      return rc;
+    return ok_status();
+  }
   if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, counter, st)) != DETATTN_OK) return rc;
   SideStream* ss = nullptr;
   if ((rc = side_stream(&ss)) != DETATTN_OK) return rc;
@@ -944,6 +1006,20 @@ size_t attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D) {
   return counter_offset(B, T, Hq) + 256;
 }
 
+size_t attn_bwd_ds_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int causal) {
+  bool empty = false;
+  if (check_shape(B, T, Hq, Hkv, D, &empty) != DETATTN_OK || empty) return 0;
+  if (causal != 0 && causal != 1) return 0;
+  if (static_cast<double>(B) * Hq * ds_pairs(T, causal) * 2 * kTileN >= 2.0e9) return 0;
+  return ds_offset(B, T, Hq) + ds_region_bytes(B, T, Hq, causal);
+}
+
+int detattn_set_bwd_dq_mode(int mode) {
+  if (mode != 0 && mode != 1) return fail(DETATTN_ERR_SHAPE, "dQ mode %d: must be 0 or 1", mode);
+  g_bwd_dq_mode = mode;
+  return ok_status();
+}
+
 int attn_bwd_delta(const void* o, const void* dout, const float* lse, void* workspace,
                    size_t workspace_bytes, int B, int T, int Hq, int D, void* stream) {
   bool empty = false;
@@ -1217,6 +1293,9 @@ int detattn_check_status(void* stream) {
   if (e == cudaSuccess) e = take_bwd_status(st, &b);
   if (e == cudaSuccess) e = take_embed_status(st, &em);
   if (e == cudaSuccess) e = take_layer_status(st, &ly);
+  unsigned dsf = 0;
+  if (e == cudaSuccess) e = take_ds_status(st, &dsf);
+  if (dsf) b |= 32u;
   if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
   if (em & 1u)
     return fail(DETATTN_ERR_INDEX,

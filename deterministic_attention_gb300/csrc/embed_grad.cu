@@ -22,9 +22,10 @@
 //                ascending token order.  An id whose tokens lie inside one
 //                run is final and stored in dW; an id that crosses runs
 //                leaves one partial row per run it touches
-//   6. rows      one warp per (row v, 128 columns): rows no token selects are
-//                written as zeros; rows that crossed runs add their partials
-//                in run order
+//   6. rows      rows no token selects are written as zeros (right after
+//                step 2); rows that crossed runs add their partials in run
+//                order, one warp per (first crossed run boundary, 128
+//                columns)
 // The work is bound by HBM: dY is read once and every row of dW is written
 // once (zero rows included), plus the partial rows of ids that cross runs.
 #include <cuda_bf16.h>
@@ -41,22 +42,27 @@ __device__ unsigned int g_embed_status;
 namespace {
 
 constexpr int kRun = 32;        // sorted entries per run (one per lane)
-constexpr int kSlabF4 = 128;    // float4 column groups per slab (512 columns)
+constexpr int kSlabF4 = 64;     // float4 column groups per slab (256 columns)
 constexpr int kF4PerLane = kSlabF4 / 32;
-constexpr int kAhead = 8;       // dY rows loaded ahead in the sum
+constexpr int kAhead = 16;      // dY rows loaded ahead in the sum
 
 __device__ __forceinline__ bool id_ok(int v, int V) { return v >= 0 && v < V; }
 
 // 1. counts[v] += 1 per valid token; invalid ids are skipped here and in
 // every later step, and flagged.
+// Lanes of a warp holding the same id add once, through their lowest lane
+// (frequent ids would otherwise queue many atomics on one address).
 __global__ void embed_count_kernel(const int* __restrict__ ids, int* __restrict__ counts, int N,
                                    int V) {
-  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < N; t += gridDim.x * blockDim.x) {
-    const int v = ids[t];
-    if (id_ok(v, V))
-      atomicAdd(counts + v, 1);
-    else
-      atomicOr(&g_embed_status, 1u);
+  const int lane = threadIdx.x & 31;
+  for (int t0 = (blockIdx.x * blockDim.x + threadIdx.x) & ~31; t0 < N;
+       t0 += gridDim.x * blockDim.x) {
+    const int t = t0 + lane;
+    const int v = t < N ? ids[t] : -1;
+    const bool good = t < N && id_ok(v, V);
+    if (t < N && !good) atomicOr(&g_embed_status, 1u);
+    const unsigned same = __match_any_sync(0xffffffffu, good ? v : -1);
+    if (good && (same & ((1u << lane) - 1u)) == 0u) atomicAdd(counts + v, __popc(same));
   }
 }
 
@@ -121,62 +127,56 @@ __global__ void __launch_bounds__(1024) embed_scan_kernel(const int* __restrict_
 }
 
 // 3. Each valid token takes a slot of its id's segment.
+// Lanes with the same id take consecutive slots from one atomic.
 __global__ void embed_fill_kernel(const int* __restrict__ ids, const int* __restrict__ offsets,
                                   int* __restrict__ cursor, int* __restrict__ unsorted, int N,
                                   int V) {
-  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < N; t += gridDim.x * blockDim.x) {
-    const int v = ids[t];
-    if (!id_ok(v, V)) continue;
-    unsorted[offsets[v] + atomicAdd(cursor + v, 1)] = t;
+  const int lane = threadIdx.x & 31;
+  for (int t0 = (blockIdx.x * blockDim.x + threadIdx.x) & ~31; t0 < N;
+       t0 += gridDim.x * blockDim.x) {
+    const int t = t0 + lane;
+    const int v = t < N ? ids[t] : -1;
+    const bool good = t < N && id_ok(v, V);
+    const unsigned same = __match_any_sync(0xffffffffu, good ? v : -1);
+    const int leader = __ffs(same) - 1;
+    int base = 0;
+    if (good && lane == leader) base = atomicAdd(cursor + v, __popc(same));
+    base = __shfl_sync(0xffffffffu, base, leader);
+    if (good) unsorted[offsets[v] + base + __popc(same & ((1u << lane) - 1u))] = t;
   }
 }
 
 // 4. Token t's place in its segment is the number of the segment's tokens
 // before it.  Tokens are distinct, so the places are a permutation.  One
 // thread per entry of `unsorted`, which step 3 grouped by id, 256 entries
-// per block.  A block whose entries all belong to one long segment (a
-// frequent id) stages that segment through shared memory in tiles and every
-// thread counts against the tile; other blocks walk their short segments in
-// global memory.
+// per block.  Short segments (up to 64 tokens) are counted by each thread
+// alone in global memory.  Each long segment (a frequent id) that the block
+// touches is staged through shared memory in tiles, and the block's threads
+// of that segment count against each tile.
 constexpr int kOrderBlock = 256;
 constexpr int kOrderTile = 4096;
+constexpr int kOrderShort = 64;
 __global__ void __launch_bounds__(kOrderBlock) embed_order_kernel(
     const int* __restrict__ ids, const int* __restrict__ offsets, const int* __restrict__ unsorted,
     int* __restrict__ sorted, int V) {
   __shared__ __align__(16) int tile[kOrderTile];
+  __shared__ int long_seg[kOrderBlock];
+  __shared__ int n_long;
   const int n_valid = offsets[V];
   const int e0 = blockIdx.x * kOrderBlock;
   if (e0 >= n_valid) return;
+  if (threadIdx.x == 0) n_long = 0;
+  __syncthreads();
   const int e = e0 + threadIdx.x;
   const bool live = e < n_valid;
   const int t = live ? unsorted[e] : 0;
   const int v = live ? ids[t] : 0;
   const int o = live ? offsets[v] : 0, n = live ? offsets[v + 1] - o : 0;
-  // The block's first and last entries share a segment: every entry does.
-  const int e_last = min(e0 + kOrderBlock, n_valid) - 1;
-  const int v_first = ids[unsorted[e0]], v_last = ids[unsorted[e_last]];
+  // The first entry of each long segment in this block lists it (the list's
+  // order is irrelevant: each segment's counts are its own).
+  if (live && n > kOrderShort && e == max(o, e0)) long_seg[atomicAdd(&n_long, 1)] = v;
   int rank = 0;
-  if (v_first == v_last && offsets[v_first + 1] - offsets[v_first] > kOrderBlock) {
-    const int so = offsets[v_first], sn = offsets[v_first + 1] - so;
-    for (int b0 = 0; b0 < sn; b0 += kOrderTile) {
-      const int nb = min(kOrderTile, sn - b0);
-      __syncthreads();
-      for (int j = threadIdx.x; j < kOrderTile; j += kOrderBlock)
-        tile[j] = j < nb ? unsorted[so + b0 + j] : 0x7FFFFFFF;
-      __syncthreads();
-      const int4* t4 = reinterpret_cast<const int4*>(tile);
-      int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-#pragma unroll 8
-      for (int j = 0; j < (nb + 3) / 4; ++j) {
-        const int4 x = t4[j];
-        r0 += x.x < t;
-        r1 += x.y < t;
-        r2 += x.z < t;
-        r3 += x.w < t;
-      }
-      rank += (r0 + r1) + (r2 + r3);
-    }
-  } else if (live) {
+  if (live && n <= kOrderShort) {
     int j = 0;
     for (; j + 4 <= n; j += 4) {
       const int a0 = unsorted[o + j], a1 = unsorted[o + j + 1], a2 = unsorted[o + j + 2],
@@ -184,6 +184,33 @@ __global__ void __launch_bounds__(kOrderBlock) embed_order_kernel(
       rank += (a0 < t) + (a1 < t) + (a2 < t) + (a3 < t);
     }
     for (; j < n; ++j) rank += unsorted[o + j] < t ? 1 : 0;
+  }
+  __syncthreads();
+  const int nl = n_long;
+  for (int li = 0; li < nl; ++li) {
+    const int vs = long_seg[li];
+    const int so = offsets[vs], sn = offsets[vs + 1] - so;
+    const bool mine = live && v == vs;
+    for (int b0 = 0; b0 < sn; b0 += kOrderTile) {
+      const int nb = min(kOrderTile, sn - b0);
+      __syncthreads();
+      for (int j = threadIdx.x; j < kOrderTile; j += kOrderBlock)
+        tile[j] = j < nb ? unsorted[so + b0 + j] : 0x7FFFFFFF;
+      __syncthreads();
+      if (mine) {
+        const int4* t4 = reinterpret_cast<const int4*>(tile);
+        int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
+#pragma unroll 8
+        for (int j = 0; j < (nb + 3) / 4; ++j) {
+          const int4 x = t4[j];
+          r0 += x.x < t;
+          r1 += x.y < t;
+          r2 += x.z < t;
+          r3 += x.w < t;
+        }
+        rank += (r0 + r1) + (r2 + r3);
+      }
+    }
   }
   if (live) sorted[o + rank] = t;
 }
@@ -195,14 +222,14 @@ __device__ __forceinline__ void add_bf16x4(float (&acc)[4], uint2 x) {
   acc[3] += __uint_as_float(x.y & 0xFFFF0000u);
 }
 
-// 5. One warp per (run of 32 sorted entries, slab of 512 columns).  Lane l
-// owns column groups slab*128 + l + 32k (k = 0..3) of 4 floats each; entry j
+// 5. One warp per (run of 32 sorted entries, slab of 256 columns).  Lane l
+// owns column groups slab*64 + l + 32k (k = 0, 1) of 4 floats each; entry j
 // of the run is token sorted[32 r + j], read by all lanes.  The rows of one
 // id are added in entry order.  Where an id's segment lies wholly inside the
 // run its sum is final and goes to dW; otherwise it goes to the run's head
 // partial (the segment began in an earlier run) or tail partial (it began in
 // this run and goes on past it).
-__global__ void __launch_bounds__(256) embed_sum_kernel(EmbedArgs a) {
+__global__ void __launch_bounds__(256, 2) embed_sum_kernel(EmbedArgs a) {
   const int lane = threadIdx.x & 31;
   const int n_valid = a.offsets[a.V];
   const int n_runs = (n_valid + kRun - 1) / kRun;
@@ -269,44 +296,68 @@ __global__ void __launch_bounds__(256) embed_sum_kernel(EmbedArgs a) {
   }
 }
 
-// 6. One warp per (row, 128-column slab): zeros for rows no token selects;
-// for rows whose segment crosses runs, the tail partial of its first run,
-// then the head partials of the runs after it, in run order.  Each lane owns
-// one float4 of the slab; the partials of up to 16 runs are loaded before
-// they are added, so a long segment keeps many loads in flight.
-constexpr int kRowsAhead = 16;
-__global__ void __launch_bounds__(256) embed_rows_kernel(EmbedArgs a) {
+// 6a. Rows no token selects are zero: one warp per 8 consecutive rows (their
+// offsets come in with one load per lane), each zero row written whole with
+// lane-strided float4 stores.  Depends only on the offsets.
+constexpr int kZeroRows = 8;
+__global__ void __launch_bounds__(256) embed_zero_kernel(EmbedArgs a) {
   const int lane = threadIdx.x & 31;
   const int n_f4 = a.E / 4;
+  const int n_blocks = (a.V + kZeroRows - 1) / kZeroRows;
+  const int warps = gridDim.x * (blockDim.x / 32);
+  for (int rb = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); rb < n_blocks; rb += warps) {
+    const int v_l = rb * kZeroRows + (lane & (kZeroRows - 1));
+    const int cnt_l = v_l < a.V ? a.offsets[v_l + 1] - a.offsets[v_l] : 1;
+    for (int j = 0; j < kZeroRows; ++j) {
+      const int v = rb * kZeroRows + j;
+      if (v >= a.V || __shfl_sync(0xffffffffu, cnt_l, j) != 0) continue;
+      float4* d4 = reinterpret_cast<float4*>(a.dw + static_cast<size_t>(v) * a.E);
+      for (int g = lane; g < n_f4; g += 32) d4[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+// 6b. Ids whose tokens cross runs.  Such an id crosses the boundary after its
+// first run first; the item (that boundary, 128-column slab) owns its sum:
+// the tail partial of the first run, then the head partials of the runs
+// after it, in run order, one float4 per lane, with the partials of up to 16
+// runs loaded before they are added.  A frequent id spreads over 12 such
+// warps (one per slab at width 1536).
+constexpr int kFixAhead = 16;
+__global__ void __launch_bounds__(256) embed_fixup_kernel(EmbedArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int n_valid = a.offsets[a.V];
+  const int n_runs = (n_valid + kRun - 1) / kRun;
+  const int n_f4 = a.E / 4;
   const int n_slabs = (n_f4 + 31) / 32;
-  const long items = static_cast<long>(a.V) * n_slabs;
+  const long items = static_cast<long>(n_runs > 0 ? n_runs - 1 : 0) * n_slabs;
   const long warps = static_cast<long>(gridDim.x) * (blockDim.x / 32);
   for (long it = static_cast<long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5); it < items;
        it += warps) {
-    const int v = static_cast<int>(it / n_slabs), slab = static_cast<int>(it % n_slabs);
+    const int rb = static_cast<int>(it / n_slabs), slab = static_cast<int>(it % n_slabs);
+    // The id of the last entry of run rb, and whether it starts in rb and
+    // goes on past it.
+    const int v = a.ids[a.sorted[(rb + 1) * kRun - 1]];
     const int so = a.offsets[v], se = a.offsets[v + 1];
-    const int rs = so / kRun, re = (se - 1) / kRun;
-    if (se > so && rs == re) continue;  // final already
+    if (so / kRun != rb || se <= (rb + 1) * kRun) continue;
+    const int re = (se - 1) / kRun;
     const int g = slab * 32 + lane;
     if (g >= n_f4) continue;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (se > so) {
-      acc = reinterpret_cast<const float4*>(a.tail + static_cast<size_t>(rs) * a.E)[g];
-      for (int r0 = rs + 1; r0 <= re; r0 += kRowsAhead) {
-        float4 x[kRowsAhead];
+    float4 acc = reinterpret_cast<const float4*>(a.tail + static_cast<size_t>(rb) * a.E)[g];
+    for (int r0 = rb + 1; r0 <= re; r0 += kFixAhead) {
+      float4 x[kFixAhead];
 #pragma unroll
-        for (int k = 0; k < kRowsAhead; ++k)
-          x[k] = r0 + k <= re
-                     ? reinterpret_cast<const float4*>(a.head + static_cast<size_t>(r0 + k) * a.E)[g]
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < kFixAhead; ++k)
+        x[k] = r0 + k <= re
+                   ? reinterpret_cast<const float4*>(a.head + static_cast<size_t>(r0 + k) * a.E)[g]
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < kRowsAhead; ++k) {
-          if (r0 + k > re) break;
-          acc.x += x[k].x;
-          acc.y += x[k].y;
-          acc.z += x[k].z;
-          acc.w += x[k].w;
-        }
+      for (int k = 0; k < kFixAhead; ++k) {
+        if (r0 + k > re) break;
+        acc.x += x[k].x;
+        acc.y += x[k].y;
+        acc.z += x[k].z;
+        acc.w += x[k].w;
       }
     }
     reinterpret_cast<float4*>(a.dw + static_cast<size_t>(v) * a.E)[g] = acc;
@@ -329,24 +380,24 @@ cudaError_t launch_embed_grad(const EmbedArgs& a, int sms, cudaStream_t st) {
   }
   embed_scan_kernel<<<(a.V + kScanTile - 1) / kScanTile, 1024, 0, st>>>(a.counts, a.offsets,
                                                                           a.cursor, a.V);
+  {
+    const long warps = (static_cast<long>(a.V) + kZeroRows - 1) / kZeroRows;
+    embed_zero_kernel<<<grid_for(warps * 32, 256, sms, 8), 256, 0, st>>>(a);
+  }
   if (a.N > 0) {
     embed_fill_kernel<<<grid_for(a.N, 256, sms, 8), 256, 0, st>>>(a.ids, a.offsets, a.cursor,
                                                                   a.unsorted, a.N, a.V);
     embed_order_kernel<<<(a.N + kOrderBlock - 1) / kOrderBlock, kOrderBlock, 0, st>>>(
         a.ids, a.offsets, a.unsorted, a.sorted, a.V);
-    const long n_slabs = (a.E / 4 + kSlabF4 - 1) / kSlabF4;
-    const long warps = (static_cast<long>(a.N) + kRun - 1) / kRun * n_slabs;
-    embed_sum_kernel<<<grid_for(warps * 32, 256, sms, 8), 256, 0, st>>>(a);
-  }
-  {
+    embed_sum_kernel<<<sms * 2, 256, 0, st>>>(a);
     const long n_slabs = (a.E / 4 + 31) / 32;
-    const long warps = static_cast<long>(a.V) * n_slabs;
-    embed_rows_kernel<<<grid_for(warps * 32, 256, sms, 8), 256, 0, st>>>(a);
+    const long warps = ((static_cast<long>(a.N) + kRun - 1) / kRun) * n_slabs;
+    embed_fixup_kernel<<<grid_for(warps * 32, 256, sms, 8), 256, 0, st>>>(a);
   }
   return cudaGetLastError();
 }
 
-int embed_grad_launches(int N) { return N > 0 ? 6 : 2; }
+int embed_grad_launches(int N) { return N > 0 ? 7 : 2; }
 
 cudaError_t take_embed_status(cudaStream_t st, unsigned* out) {
   unsigned v = 0, zero = 0;
