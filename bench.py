@@ -292,6 +292,8 @@ def run_gpu_arm(args, world, rank):
     w = WORKLOADS[args.workload]
     B, T, Hq, Hkv, D = w.shape
     dev = torch.device("cuda", torch.cuda.current_device())
+    if args.stored_ds:
+        da.set_bwd_dq_mode(1)
     probe = Problem(w, 1, dev, stored_ds=args.stored_ds)
     per_set = probe.set_bytes()
     del probe

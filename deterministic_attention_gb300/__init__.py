@@ -215,7 +215,8 @@ def new_workspace(B, T, Hq, Hkv, D, device="cuda", stored_ds=False, causal=True)
 
 
 def set_bwd_dq_mode(mode: int):
-    """0: stored-dS backward whenever the workspace holds it (default); 1: never."""
+    """0 (default): the dQ step recomputes S and dP; 1: stored-dS backward
+    whenever the workspace holds it (new_workspace(..., stored_ds=True))."""
     _check(lib().detattn_set_bwd_dq_mode(int(mode)), "detattn_set_bwd_dq_mode")
 
 

@@ -332,13 +332,19 @@ struct DkvTile {
   int qbase, kbase, rbase, tk, off;
 };
 
-template <int D, class VT>
+// MODE bit 0: the chunked tile walk (BwdArgs::bg_chunk); bit 1: store every
+// item's dS^T (BwdArgs::ds).  Separate instantiations keep the plain walk
+// free of both (each measured to cost about a microsecond at page3 as a
+// run-time branch).
+constexpr int kDkvChunked = 1, kDkvStoreDs = 2;
+template <int D, class VT, int MODE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                      const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
                      const BwdArgs a, const __grid_constant__ VT vt) {
   using Cf = DkvCfg<D>;
   constexpr bool VL = std::is_same<VT, VarlenTable>::value;
+  static_assert(!VL || MODE == 0, "the packed form walks its own table");
   constexpr int NS = Cf::kStages;
   constexpr int TM = Cf::kTM;
   constexpr int QG = Cf::kQG;
@@ -382,7 +388,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ti.m_begin = a.causal ? min(mq_end, max(0, first_q) / TM) : 0;
       ti.per_head = mq_end - ti.m_begin;
     } else {
-      const int nt = t / a.BH, bg = t % a.BH;
+      int nt, bg;
+      if constexpr ((MODE & kDkvChunked) != 0) {
+        dkdv_tile_coords(t, a.n_tiles, a.BH, a.bg_chunk, &nt, &bg);
+      } else {
+        nt = t / a.BH;
+        bg = t % a.BH;
+      }
       ti.b = bg / a.Hkv;
       ti.g = bg % a.Hkv;
       ti.n0 = nt * kTileN;
@@ -757,8 +769,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!ok) break;
           tc_fence_after();
         }
-        if constexpr (!VL) {
-          if (a.ds != nullptr) {
+        if constexpr ((MODE & kDkvStoreDs) != 0) {
+          {
             // Stored-dS backward: this item's dS^T rows also go to the
             // workspace, for the dQ step to read instead of recomputing them.
             const int it = ti.it_lo + li;
@@ -1466,7 +1478,7 @@ cudaError_t set_smem_once(K kernel, int bytes, unsigned long long* done) {
 template <int D>
 cudaError_t dkdv_max_clusters_t(int c, int* out) {
   static unsigned long long done[64] = {};
-  cudaError_t e = set_smem_once(attn_dkdv_kernel<D, NoVarlen>, DkvCfg<D>::kSmemBytes, done);
+  cudaError_t e = set_smem_once(attn_dkdv_kernel<D, NoVarlen, 0>, DkvCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(c));
@@ -1479,15 +1491,15 @@ cudaError_t dkdv_max_clusters_t(int c, int* out) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, attn_dkdv_kernel<D, NoVarlen>, &cfg);
+  return cudaOccupancyMaxActiveClusters(out, attn_dkdv_kernel<D, NoVarlen, 0>, &cfg);
 }
 
-template <int D, class VT>
+template <int D, class VT, int MODE>
 cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                           bool dependent, const VT& vt, cudaStream_t st) {
   static unsigned long long done[64] = {};
-  cudaError_t e = set_smem_once(attn_dkdv_kernel<D, VT>, DkvCfg<D>::kSmemBytes, done);
+  cudaError_t e = set_smem_once(attn_dkdv_kernel<D, VT, MODE>, DkvCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
@@ -1510,7 +1522,7 @@ cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  e = cudaLaunchKernelEx(&cfg, attn_dkdv_kernel<D, VT>, mq, mk, mv, mdo, a, vt);
+  e = cudaLaunchKernelEx(&cfg, attn_dkdv_kernel<D, VT, MODE>, mq, mk, mv, mdo, a, vt);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1562,11 +1574,22 @@ cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMa
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                         bool dependent, const VarlenTable* vt, cudaStream_t st) {
   if (vt != nullptr)
-    return D == 64 ? launch_dkdv_t<64>(grid, mq, mk, mv, mdo, a, dependent, *vt, st)
-                   : launch_dkdv_t<128>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
+    return D == 64 ? launch_dkdv_t<64, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st)
+                   : launch_dkdv_t<128, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
   const NoVarlen none{};
-  return D == 64 ? launch_dkdv_t<64>(grid, mq, mk, mv, mdo, a, dependent, none, st)
-                 : launch_dkdv_t<128>(grid, mq, mk, mv, mdo, a, dependent, none, st);
+  const int mode = (a.bg_chunk > 0 ? kDkvChunked : 0) | (a.ds != nullptr ? kDkvStoreDs : 0);
+  auto go = [&](auto d, auto m) {
+    return launch_dkdv_t<decltype(d)::value, NoVarlen, decltype(m)::value>(grid, mq, mk, mv, mdo, a,
+                                                                           dependent, none, st);
+  };
+  using I64 = std::integral_constant<int, 64>;
+  using I128 = std::integral_constant<int, 128>;
+  switch (mode) {
+    case 0: return D == 64 ? go(I64{}, std::integral_constant<int, 0>{}) : go(I128{}, std::integral_constant<int, 0>{});
+    case 1: return D == 64 ? go(I64{}, std::integral_constant<int, 1>{}) : go(I128{}, std::integral_constant<int, 1>{});
+    case 2: return D == 64 ? go(I64{}, std::integral_constant<int, 2>{}) : go(I128{}, std::integral_constant<int, 2>{});
+    default: return D == 64 ? go(I64{}, std::integral_constant<int, 3>{}) : go(I128{}, std::integral_constant<int, 3>{});
+  }
 }
 
 cudaError_t dkdv_max_clusters(int D, int c, int* out) {

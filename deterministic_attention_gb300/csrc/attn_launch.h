@@ -115,6 +115,11 @@ struct BwdArgs {
   int BH;                // B * Hq (dQ) or B * Hkv (dK/dV)
   int cluster;           // dK/dV: blocks sharing one key tile (1, 2, 4 or 8)
   int n_groups;          // dK/dV: resident clusters (persistent), each walking its key tiles
+  // dK/dV tile order: 0 walks every (b, KV head)'s tile nt before any tile
+  // nt + 1 (heaviest first); g > 0 does so within chunks of g (b, KV head)
+  // pairs, one chunk after the other, so the queries the clusters read at
+  // once (those of g KV groups) stay in L2 on long sequences.
+  int bg_chunk;
   int causal;
   float scale;
   float scale_log2;
@@ -138,6 +143,20 @@ struct BwdArgs {
 cudaError_t launch_dq_from_ds(int D, const CUtensorMap& mds, const CUtensorMap& mk,
                               const BwdArgs& a, int n_units, cudaStream_t st);
 cudaError_t take_ds_status(cudaStream_t st, unsigned* out);
+
+// Key tile t of the dK/dV walk as (nt, bg): position nt along T, bg = b Hkv + g.
+__host__ __device__ inline void dkdv_tile_coords(int t, int n_tiles, int BH, int bg_chunk, int* nt,
+                                                 int* bg) {
+  if (bg_chunk <= 0 || bg_chunk >= BH) {
+    *nt = t / BH;
+    *bg = t % BH;
+    return;
+  }
+  const int per = n_tiles * bg_chunk;
+  const int chunk = t / per, r = t % per;
+  *nt = r / bg_chunk;
+  *bg = chunk * bg_chunk + r % bg_chunk;
+}
 
 // Each returns the launch error (cudaSuccess when the kernel was queued).
 // `vt` (not null) selects the packed variable-length form: the tensor maps

@@ -323,9 +323,8 @@ int sm_count(int* out) {
 // a given problem and GPU.  `forced_c` > 0 takes that C (capped at the limit).
 // `resident[i]`: clusters of 2^i blocks the device holds at once (0: none).
 // Returns false when no allowed C can be resident.
-// The choice over key tiles numbered heaviest first in groups of `per_group`
-// (the KV heads, or batches and KV heads, of one key position): tile t
-// carries items[t / per_group] items.
+// The choice over key tiles in walk order: tile t carries items[t / per_group]
+// items (per_group = 1: one entry per tile).
 bool dkdv_choose_items(const std::vector<int>& items_per_group, int per_group, int D,
                        const int resident[4], int forced_c, int* c_out, int* ng_out) {
   const long total = static_cast<long>(items_per_group.size()) * per_group;
@@ -361,16 +360,34 @@ bool dkdv_choose_items(const std::vector<int>& items_per_group, int per_group, i
   return *c_out != 0;
 }
 
+// (b, KV head) pairs per chunk of the dK/dV walk (0: no chunks): chunks keep
+// the queries and output gradients the clusters read at once to about 32 MB
+// (they stay in L2) when all of them together would not fit.
+int dkdv_bg_chunk(int B, int T, int Hq, int Hkv, int D) {
+  const double group_bytes = static_cast<double>(T) * (Hq / Hkv) * D * 2 * 2;  // Q and dO
+  const int BH = B * Hkv;
+  if (group_bytes * BH <= 48.0 * (1 << 20)) return 0;
+  int g = static_cast<int>(32.0 * (1 << 20) / group_bytes);
+  if (g < 1) g = 1;
+  while (g > 1 && BH % g != 0) --g;  // whole chunks
+  return g >= BH ? 0 : g;
+}
+
 bool dkdv_choose(int B, int T, int Hq, int Hkv, int D, int causal, const int resident[4],
                  int forced_c, int* c_out, int* ng_out) {
   const int G = Hq / Hkv;
   const int n_tiles = (T + kTileN - 1) / kTileN;
   const int tm = dkdv_tile_m(D);
   const int m_end = (T + tm - 1) / tm;
-  std::vector<int> items(n_tiles);
-  for (int nt = 0; nt < n_tiles; ++nt)
-    items[nt] = G * (m_end - (causal ? nt * kTileN / tm : 0));
-  return dkdv_choose_items(items, B * Hkv, D, resident, forced_c, c_out, ng_out);
+  const int BH = B * Hkv;
+  const int chunk = dkdv_bg_chunk(B, T, Hq, Hkv, D);
+  std::vector<int> items(static_cast<size_t>(n_tiles) * BH);
+  for (long t = 0; t < static_cast<long>(items.size()); ++t) {
+    int nt, bg;
+    dkdv_tile_coords(static_cast<int>(t), n_tiles, BH, chunk, &nt, &bg);
+    items[t] = G * (m_end - (causal ? nt * kTileN / tm : 0));
+  }
+  return dkdv_choose_items(items, 1, D, resident, forced_c, c_out, ng_out);
 }
 
 // dkdv_choose with the current device's residency: `sms` blocks alone, and
@@ -410,6 +427,7 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
   a.BH = B * Hkv;
   a.ds = ds;
   a.ds_pairs = ds_pairs;
+  a.bg_chunk = dkdv_bg_chunk(B, T, Hq, Hkv, D);
   int sms = 0;
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
   if ((rc = dkdv_schedule(B, T, Hq, Hkv, D, causal, sms, g_dkdv_split, &a.cluster, &a.n_groups)) !=
@@ -495,7 +513,7 @@ int side_stream(SideStream** out) {
 // forms and the dQ step becomes a plain product dQ = scale dS K (no
 // recomputed S, P, dP): pairs (query tile, key tile) of 128 x 128, two bf16
 // halves of 128 x 64 each, after the row statistics and the counter.
-int g_bwd_dq_mode = 0;  // 0: stored dS whenever the workspace holds it; 1: never
+int g_bwd_dq_mode = 0;  // 0: recompute in the dQ step; 1: stored dS when the workspace holds it
 
 long ds_pairs(int T, int causal) {
   const long n = (T + kTileM - 1) / kTileM;
@@ -528,7 +546,7 @@ int bwd_steps(const void* q, const void* k, const void* v, const void* o, const 
               int T, int Hq, int Hkv, int D, float scale, int causal, cudaStream_t st) {
   int rc;
   unsigned* counter = unit_counter_ptr(ws, ws_bytes, B, T, Hq);
-  if (g_bwd_dq_mode == 0 && ws_bytes >= ds_offset(B, T, Hq) + ds_region_bytes(B, T, Hq, causal) &&
+  if (g_bwd_dq_mode == 1 && ws_bytes >= ds_offset(B, T, Hq) + ds_region_bytes(B, T, Hq, causal) &&
       static_cast<double>(B) * Hq * ds_pairs(T, causal) * 2 * kTileN < 2.0e9) {
     void* ds = static_cast<char*>(ws) + ds_offset(B, T, Hq);
     const long pairs = ds_pairs(T, causal);
@@ -814,7 +832,8 @@ int check_gemm(const void* a, int a_mn, long lda, const void* b, int b_mn, long 
 }
 
 int gemm_impl(const void* a, int a_mn, long lda, const void* b, int b_mn, long ldb, void* c,
-              int c_f32, long ldc, int M, int N, int K, float alpha, cudaStream_t st) {
+              int c_f32, long ldc, int M, int N, int K, float alpha, cudaStream_t st,
+              int k_splits = 1, float* partial = nullptr) {
   CUtensorMap ma, mb;
   int rc;
   if (a_mn)
@@ -835,14 +854,26 @@ int gemm_impl(const void* a, int a_mn, long lda, const void* b, int b_mn, long l
   g.ldc = ldc;
   g.alpha = alpha;
   g.wait_ns = g_wait_ns;
-  return launched(launch_gemm(a_mn != 0, b_mn != 0, c_f32 != 0, ma, mb, g, st), "layer_gemm");
+  g.k_splits = (k_splits > 1 && partial != nullptr && (K / 64) % k_splits == 0) ? k_splits : 1;
+  g.partial = partial;
+  if ((rc = launched(launch_gemm(a_mn != 0, b_mn != 0, c_f32 != 0, ma, mb, g, st),
+                     "layer_gemm")) != DETATTN_OK)
+    return rc;
+  if (g.k_splits == 1) return DETATTN_OK;
+  int sms = 0;
+  if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
+  return launched(launch_gemm_reduce(g, c_f32 != 0, sms, st), "layer_gemm (split-K sum)");
 }
 
 // Workspace of layer_train_step: the step's intermediates, each 256-byte
 // aligned.  N3 = (Hq + 2 Hkv) D columns of the joined projection.
 struct LayerLayout {
-  size_t qkv, q, k, v, o, lse, dout, dq, dk, dv, dqkv, attn, attn_bytes, total;
+  size_t qkv, q, k, v, o, lse, dout, dq, dk, dv, dqkv, attn, attn_bytes, partial, total;
 };
+// The weight-gradient products (M = d or Hq D, K = B T) have few output
+// tiles and a long K: they split K in kWgradSplits blocks, whose fp32
+// partials a second kernel adds in a fixed order.
+constexpr int kWgradSplits = 4;
 LayerLayout layer_layout(int B, int T, int d, int Hq, int Hkv, int D) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t BT = static_cast<size_t>(B) * T;
@@ -862,8 +893,8 @@ LayerLayout layer_layout(int B, int T, int d, int Hq, int Hkv, int D) {
   l.dqkv = at; at += up(BT * N3 * 2);
   l.attn_bytes = counter_offset(B, T, Hq) + 256;
   l.attn = at; at += up(l.attn_bytes);
+  l.partial = at; at += up(static_cast<size_t>(kWgradSplits) * d * std::max<size_t>(N3, d) * 4);
   l.total = at;
-  (void)d;
   return l;
 }
 
@@ -1270,8 +1301,12 @@ int layer_train_step(const void* x, const void* dy, float* w_qkv, float* w_o, fl
     return rc;
   if ((rc = launched(launch_rope_merge(dq, dk, dv, dqkv, ra, sms, st), "rope")) != DETATTN_OK)
     return rc;
-  if ((rc = gemm_impl(o, 1, HqD, dy, 1, d, g_o, 1, d, HqD, d, BT, 1.f, st)) != DETATTN_OK) return rc;
-  if ((rc = gemm_impl(x, 1, d, dqkv, 1, N3, g_qkv, 1, N3, d, N3, BT, 1.f, st)) != DETATTN_OK)
+  float* part = reinterpret_cast<float*>(w + l.partial);
+  if ((rc = gemm_impl(o, 1, HqD, dy, 1, d, g_o, 1, d, HqD, d, BT, 1.f, st, kWgradSplits, part)) !=
+      DETATTN_OK)
+    return rc;
+  if ((rc = gemm_impl(x, 1, d, dqkv, 1, N3, g_qkv, 1, N3, d, N3, BT, 1.f, st, kWgradSplits,
+                      part)) != DETATTN_OK)
     return rc;
   if (dx != nullptr &&
       (rc = gemm_impl(dqkv, 0, N3, w_qkv_bf16, 0, N3, dx, 0, d, BT, d, N3, 1.f, st)) != DETATTN_OK)

@@ -14,7 +14,13 @@ struct GemmArgs {
   long ldc;
   float alpha;
   unsigned long long wait_ns;
+  // Split K (k_splits > 1): block z of the grid's third dimension sums K
+  // rows [z K / k_splits, (z + 1) K / k_splits) into fp32 partial[z] [M, N];
+  // launch_gemm_reduce then adds the partials in ascending z into C.
+  int k_splits;
+  float* partial;
 };
+cudaError_t launch_gemm_reduce(const GemmArgs& g, bool out_f32, int sms, cudaStream_t st);
 
 struct RopeArgs {
   int B, T, Hq, Hkv, D;

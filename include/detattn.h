@@ -117,20 +117,22 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
  * step forms, bf16: per (b, h) the pairs (128-query tile mt, 128-key tile
  * kt) visible under the mask (kt <= mt when causal, in the order
  * mt (mt + 1) / 2 + kt; all pairs mt * n + kt otherwise), each pair two
- * halves of 64 queries stored [128 keys][64 queries] (32 KiB a pair).  An
- * attn_bwd call whose workspace_bytes reaches this size stores dS in the
- * dK/dV step and forms dQ = scale * dS K with one tensor-core product per
- * tile instead of recomputing S, P and dP (RustingBrain page, "Where the time
- * goes now": the backward's time is in the kernels that recompute the
- * probabilities); both forms are deterministic, and dk, dv are the same bits
- * in both.  Returns 0 for an invalid shape or one whose dS rows would exceed
- * 2^31. */
+ * halves of 64 queries stored [128 keys][64 queries] (32 KiB a pair).  With
+ * detattn_set_bwd_dq_mode(1), an attn_bwd call whose workspace_bytes reaches
+ * this size stores dS in the dK/dV step and forms dQ = scale * dS K with one
+ * tensor-core product per tile instead of recomputing S, P and dP
+ * (RustingBrain page, "Where the time goes now": the backward's time is in
+ * the kernels that recompute the probabilities); both forms are
+ * deterministic, and dk, dv are the same bits in both.  Measured on GB300 the
+ * recompute form is the faster at every benchmarked shape (it runs dQ beside
+ * dK/dV; the stored form must run after it), so it is the default.  Returns
+ * 0 for an invalid shape or one whose dS rows would exceed 2^31. */
 size_t attn_bwd_ds_workspace_bytes(int B, int T, int Hq, int Hkv, int D, int causal);
 
-/* 0 (default): attn_bwd takes the stored-dS form whenever its workspace is
- * long enough for it; 1: it always recomputes in the dQ step.  Host-side,
- * per process.  Returns DETATTN_OK or DETATTN_ERR_SHAPE.  Not tied to a
- * passage of the method. */
+/* 0 (default): attn_bwd recomputes S and dP in its dQ step; 1: it takes the
+ * stored-dS form whenever its workspace is long enough for it
+ * (attn_bwd_ds_workspace_bytes).  Host-side, per process.  Returns
+ * DETATTN_OK or DETATTN_ERR_SHAPE.  Not tied to a passage of the method. */
 int detattn_set_bwd_dq_mode(int mode);
 
 /* Backward without a caller workspace, for callers that cannot allocate

@@ -16,6 +16,13 @@ from helpers import assert_bwd_close, sha256, to_np, widen
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True)
+def stored_mode():
+    da.set_bwd_dq_mode(1)
+    yield
+    da.set_bwd_dq_mode(0)
+
+
 def _both(q, k, v, do, scale, causal):
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
@@ -24,8 +31,9 @@ def _both(q, k, v, do, scale, causal):
     ws_ds = da.new_workspace(B, T, Hq, Hkv, D, stored_ds=True, causal=causal)
     assert ws_ds.numel() == da.ds_workspace_bytes(B, T, Hq, Hkv, D, causal)
     stored = da.attn_bwd(qd, kd, vd, o, lse, dod, scale=scale, causal=causal, workspace=ws_ds)
-    plain = da.attn_bwd(qd, kd, vd, o, lse, dod, scale=scale, causal=causal,
-                        workspace=da.new_workspace(B, T, Hq, Hkv, D))
+    da.set_bwd_dq_mode(0)
+    plain = da.attn_bwd(qd, kd, vd, o, lse, dod, scale=scale, causal=causal, workspace=ws_ds)
+    da.set_bwd_dq_mode(1)
     torch.cuda.synchronize()
     da.check_status()
     return [t.cpu() for t in stored], [t.cpu() for t in plain]
