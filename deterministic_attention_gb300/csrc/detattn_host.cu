@@ -329,6 +329,7 @@ bool dkdv_choose_items(const std::vector<int>& items_per_group, int per_group, i
                        const int resident[4], int forced_c, int* c_out, int* ng_out) {
   const long total = static_cast<long>(items_per_group.size()) * per_group;
   const int cmax = dkdv_max_cluster_size(D);
+  const double per_item64 = 64.0 / dkdv_tile_m(D);  // fixed costs in this kernel's items
   double best = 0.0;
   *c_out = 0;
   *ng_out = 0;
@@ -343,11 +344,12 @@ bool dkdv_choose_items(const std::vector<int>& items_per_group, int per_group, i
         const long t = kt * ng + ((kt & 1) ? ng - 1 - k : k);
         if (t >= total) break;
         const int items = items_per_group[t / per_group];
-        // Per tile: its share of the items, one item's worth for writing the
-        // sums out, and two per peer for the partial-sum exchange (measured:
-        // distributed shared memory moves ~9 bytes per clock per SM, and an
-        // item takes ~1,500 clocks).
-        load += (items + c - 1) / c + 1.0 + 2.0 * (c - 1);
+        // Per tile: its share of the items, one 64-query item's worth for
+        // writing the sums out, and two per peer for the partial-sum exchange
+        // (measured: distributed shared memory moves ~9 bytes per clock per
+        // SM, and a 64-query item takes ~1,500 clocks); items of TM queries
+        // count TM / 64 such items.
+        load += (items + c - 1) / c + (1.0 + 2.0 * (c - 1)) * per_item64;
       }
       if (load > worst) worst = load;
     }
