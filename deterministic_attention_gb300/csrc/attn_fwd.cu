@@ -213,6 +213,12 @@ __global__ void __launch_bounds__(kPipeThreads * qtile_pipes_per_block(D), 1)
   }
   __syncthreads();
   tc_fence_after();
+  // A kernel launched after this one as a programmatic dependent (the
+  // backward's Delta step) may be scheduled now: it takes SMs as this grid's
+  // blocks leave them and waits (griddepcontrol.wait) for this grid to
+  // finish before it reads anything, so its launch latency hides under this
+  // grid's tail.
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const uint32_t tmem = tmem_slot + pipe * C::kTmemCols;
   const uint64_t wait_ns = a.wait_ns;
   bool ok = true;
