@@ -870,7 +870,7 @@ int gemm_impl(const void* a, int a_mn, long lda, const void* b, int b_mn, long l
 // Workspace of layer_train_step: the step's intermediates, each 256-byte
 // aligned.  N3 = (Hq + 2 Hkv) D columns of the joined projection.
 struct LayerLayout {
-  size_t qkv, q, k, v, o, lse, dout, dq, dk, dv, dqkv, attn, attn_bytes, partial, total;
+  size_t qkv, q, k, v, o, lse, dout, dq, dk, dv, dqkv, attn, attn_bytes, partial, partial_o, total;
 };
 // The weight-gradient products (M = d or Hq D, K = B T) have few output
 // tiles and a long K: they split K in kWgradSplits blocks, whose fp32
@@ -895,9 +895,44 @@ LayerLayout layer_layout(int B, int T, int d, int Hq, int Hkv, int D) {
   l.dqkv = at; at += up(BT * N3 * 2);
   l.attn_bytes = counter_offset(B, T, Hq) + 256;
   l.attn = at; at += up(l.attn_bytes);
-  l.partial = at; at += up(static_cast<size_t>(kWgradSplits) * d * std::max<size_t>(N3, d) * 4);
+  l.partial = at; at += up(static_cast<size_t>(kWgradSplits) * d * N3 * 4);
+  l.partial_o = at; at += up(static_cast<size_t>(kWgradSplits) * Hq * D * d * 4);
   l.total = at;
   return l;
+}
+
+// The layer step's second stream: the products that do not wait on the
+// attention (dO = dY Wo^T during the forward, the Wo gradient and its AdamW
+// update during the attention backward) run there.  Per device and context,
+// created on first use; fork and join are events.
+struct LayerStreams {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, dout = nullptr, o = nullptr, y = nullptr, done = nullptr;
+  unsigned long long ctx = 0;
+};
+int layer_streams(LayerStreams** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev >= 64) return fail(DETATTN_ERR_CUDA, "device index %d too large", dev);
+  static LayerStreams per_dev[64];
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  LayerStreams& ls = per_dev[dev];
+  const unsigned long long ctx = current_context_id();
+  if (ls.side != nullptr && ctx != 0 && ls.ctx != ctx) ls = LayerStreams{};
+  if (ls.side == nullptr) {
+    e = cudaStreamCreateWithFlags(&ls.side, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&ls.fork, &ls.dout, &ls.o, &ls.y, &ls.done})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      ls = LayerStreams{};
+      return fail(DETATTN_ERR_CUDA, "layer side stream: %s", cudaGetErrorString(e));
+    }
+    ls.ctx = current_context_id();
+  }
+  *out = &ls;
+  return DETATTN_OK;
 }
 
 int check_layer(int B, int T, int d, int Hq, int Hkv, int D) {
@@ -1287,40 +1322,71 @@ int layer_train_step(const void* x, const void* dy, float* w_qkv, float* w_o, fl
   const int BT = B * T, HqD = Hq * D, N3 = (Hq + 2 * Hkv) * D;
   const float scale = 1.0f / std::sqrt(static_cast<float>(D));
   RopeArgs ra{B, T, Hq, Hkv, D, 13.287712379549449f /* log2(10000) */};
-  // Forward: projection, rotary positions, attention, output projection.
-  if ((rc = gemm_impl(x, 0, d, w_qkv_bf16, 1, N3, qkv, 0, N3, BT, N3, d, 1.f, st)) != DETATTN_OK)
-    return rc;
-  if ((rc = launched(launch_rope_split(qkv, q, k, v, ra, sms, st), "rope")) != DETATTN_OK) return rc;
-  if ((rc = fwd_impl(q, k, v, o, lse, B, T, Hq, Hkv, D, scale, 1, st)) != DETATTN_OK) return rc;
-  if ((rc = gemm_impl(o, 0, HqD, w_o_bf16, 1, d, y, 0, d, BT, d, HqD, 1.f, st)) != DETATTN_OK)
-    return rc;
-  // Backward: dO = dY Wo^T, attention backward, rotary transpose, weight
-  // gradients, input gradient.
-  if ((rc = gemm_impl(dy, 0, d, w_o_bf16, 0, d, dout, 0, HqD, BT, HqD, d, 1.f, st)) != DETATTN_OK)
-    return rc;
-  if ((rc = bwd_steps(q, k, v, o, lse, dout, dq, dk, dv, aws, l.attn_bytes, B, T, Hq, Hkv, D, scale,
-                      1, st)) != DETATTN_OK)
-    return rc;
-  if ((rc = launched(launch_rope_merge(dq, dk, dv, dqkv, ra, sms, st), "rope")) != DETATTN_OK)
-    return rc;
+  // One enqueue at a time: the side stream and its events are shared by all
+  // callers on a device.
+  static std::mutex enqueue_mu;
+  std::lock_guard<std::mutex> enqueue_lock(enqueue_mu);
+  LayerStreams* ls = nullptr;
+  if ((rc = layer_streams(&ls)) != DETATTN_OK) return rc;
+  cudaStream_t s2 = ls->side;
+  auto ev = [&](cudaError_t e, const char* what) {
+    return e == cudaSuccess ? DETATTN_OK : fail(DETATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  };
   float* part = reinterpret_cast<float*>(w + l.partial);
-  if ((rc = gemm_impl(o, 1, HqD, dy, 1, d, g_o, 1, d, HqD, d, BT, 1.f, st, kWgradSplits, part)) !=
-      DETATTN_OK)
-    return rc;
-  if ((rc = gemm_impl(x, 1, d, dqkv, 1, N3, g_qkv, 1, N3, d, N3, BT, 1.f, st, kWgradSplits,
-                      part)) != DETATTN_OK)
-    return rc;
-  if (dx != nullptr &&
-      (rc = gemm_impl(dqkv, 0, N3, w_qkv_bf16, 0, N3, dx, 0, d, BT, d, N3, 1.f, st)) != DETATTN_OK)
-    return rc;
-  // AdamW on both weights (fp32 master copies and moments; new bf16 copies).
+  float* part_o = reinterpret_cast<float*>(w + l.partial_o);
   AdamArgs aa{lr, weight_decay, beta1, beta2, eps, step};
-  if ((rc = launched(launch_adamw(w_qkv, m_qkv, v_qkv, g_qkv, w_qkv_bf16,
-                                  static_cast<long>(d) * N3, aa, sms, st),
-                     "adamw")) != DETATTN_OK)
-    return rc;
-  return launched(launch_adamw(w_o, m_o, v_o, g_o, w_o_bf16, static_cast<long>(HqD) * d, aa, sms, st),
-                  "adamw");
+  // Fork: the side stream follows everything queued on `stream` so far.
+  if ((rc = ev(cudaEventRecord(ls->fork, st), "fork")) != DETATTN_OK) return rc;
+  if ((rc = ev(cudaStreamWaitEvent(s2, ls->fork, 0), "fork")) != DETATTN_OK) return rc;
+  rc = [&]() -> int {
+    int r;
+    // Side: dO = dY Wo^T (needs only dY and Wo), during the forward.
+    if ((r = gemm_impl(dy, 0, d, w_o_bf16, 0, d, dout, 0, HqD, BT, HqD, d, 1.f, s2)) != DETATTN_OK)
+      return r;
+    if ((r = ev(cudaEventRecord(ls->dout, s2), "dO event")) != DETATTN_OK) return r;
+    // Forward: projection, rotary positions, attention, output projection.
+    if ((r = gemm_impl(x, 0, d, w_qkv_bf16, 1, N3, qkv, 0, N3, BT, N3, d, 1.f, st)) != DETATTN_OK)
+      return r;
+    if ((r = launched(launch_rope_split(qkv, q, k, v, ra, sms, st), "rope")) != DETATTN_OK) return r;
+    if ((r = fwd_impl(q, k, v, o, lse, B, T, Hq, Hkv, D, scale, 1, st)) != DETATTN_OK) return r;
+    if ((r = ev(cudaEventRecord(ls->o, st), "O event")) != DETATTN_OK) return r;
+    if ((r = gemm_impl(o, 0, HqD, w_o_bf16, 1, d, y, 0, d, BT, d, HqD, 1.f, st)) != DETATTN_OK)
+      return r;
+    if ((r = ev(cudaEventRecord(ls->y, st), "Y event")) != DETATTN_OK) return r;
+    // Side: the Wo gradient (needs O and dY), then, once the Y product has
+    // read the old bf16 Wo, its AdamW update -- during the attention backward.
+    if ((r = ev(cudaStreamWaitEvent(s2, ls->o, 0), "O wait")) != DETATTN_OK) return r;
+    if ((r = gemm_impl(o, 1, HqD, dy, 1, d, g_o, 1, d, HqD, d, BT, 1.f, s2, kWgradSplits,
+                       part_o)) != DETATTN_OK)
+      return r;
+    if ((r = ev(cudaStreamWaitEvent(s2, ls->y, 0), "Y wait")) != DETATTN_OK) return r;
+    if ((r = launched(launch_adamw(w_o, m_o, v_o, g_o, w_o_bf16, static_cast<long>(HqD) * d, aa,
+                                   sms, s2),
+                      "adamw")) != DETATTN_OK)
+      return r;
+    // Backward: attention backward (after dO), rotary transpose, the Wqkv
+    // gradient, the input gradient, AdamW on Wqkv.
+    if ((r = ev(cudaStreamWaitEvent(st, ls->dout, 0), "dO wait")) != DETATTN_OK) return r;
+    if ((r = bwd_steps(q, k, v, o, lse, dout, dq, dk, dv, aws, l.attn_bytes, B, T, Hq, Hkv, D,
+                       scale, 1, st)) != DETATTN_OK)
+      return r;
+    if ((r = launched(launch_rope_merge(dq, dk, dv, dqkv, ra, sms, st), "rope")) != DETATTN_OK)
+      return r;
+    if ((r = gemm_impl(x, 1, d, dqkv, 1, N3, g_qkv, 1, N3, d, N3, BT, 1.f, st, kWgradSplits,
+                       part)) != DETATTN_OK)
+      return r;
+    if (dx != nullptr &&
+        (r = gemm_impl(dqkv, 0, N3, w_qkv_bf16, 0, N3, dx, 0, d, BT, d, N3, 1.f, st)) != DETATTN_OK)
+      return r;
+    return launched(launch_adamw(w_qkv, m_qkv, v_qkv, g_qkv, w_qkv_bf16,
+                                 static_cast<long>(d) * N3, aa, sms, st),
+                    "adamw");
+  }();
+  // Join, on success and on failure alike: later work on `stream` follows the
+  // side stream, and a stream capture in progress stays closed over both.
+  const int jr = ev(cudaEventRecord(ls->done, s2), "join");
+  const int jw = jr == DETATTN_OK ? ev(cudaStreamWaitEvent(st, ls->done, 0), "join") : jr;
+  return rc != DETATTN_OK ? rc : jw;
 }
 
 int detattn_check_status(void* stream) {

@@ -285,8 +285,9 @@ int layer_gemm(const void* a, int a_mn_major, int lda, const void* b, int b_mn_m
 
 /* Workspace bytes of layer_train_step (its intermediates: the joined QKV
  * projection, the rotated Q, K and V, O, LSE, dO, dQ, dK, dV, the joined
- * gradient of the projection, and the attention backward's workspace).  0
- * for an invalid shape. */
+ * gradient of the projection, the attention backward's workspace, and the
+ * fp32 partial sums of the two split-K weight-gradient products).  0 for an
+ * invalid shape. */
 size_t layer_workspace_bytes(int B, int T, int d, int Hq, int Hkv, int D);
 
 /* One training step of one attention layer at the current weights, then one
@@ -311,7 +312,12 @@ size_t layer_workspace_bytes(int B, int T, int d, int Hq, int Hkv, int D);
  * and g_o receive this step's gradients (at the weights before the update);
  * dx may be NULL.  The scale is 1/sqrt(D) and the attention is causal.
  * B*T, d, Hq*D and (Hq + 2 Hkv)*D must be multiples of 128, D 64 or 128.
- * step counts from 1.  All on `stream`. */
+ * step counts from 1.  Stream-ordered on `stream`: the call forks a
+ * library-owned second stream from it (dO = dY Wo^T during the forward; g_o
+ * and the Wo update during the attention backward) and joins it back before
+ * returning, so work queued on `stream` afterwards sees every result, and a
+ * stream capture of the call closes over both streams.  Calls from several
+ * host threads are serialised while they enqueue. */
 int layer_train_step(const void* x, const void* dy, float* w_qkv, float* w_o, float* m_qkv,
                      float* v_qkv, float* m_o, float* v_o, void* w_qkv_bf16, void* w_o_bf16,
                      float* g_qkv, float* g_o, void* y, void* dx, void* workspace,
