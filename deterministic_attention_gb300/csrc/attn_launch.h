@@ -9,7 +9,7 @@ namespace detattn {
 
 constexpr int kTileM = 128;     // query rows per forward / dQ tile
 constexpr int kTileN = 128;     // key rows per dK/dV tile
-constexpr int kFwdTileN = 64;   // key rows per forward KV tile
+constexpr int kFwdTileN = 128;  // key rows per forward KV tile
 constexpr int kDqTileN = 64;    // key rows per dQ-kernel KV tile
 // Query rows per dK/dV-kernel item (64: two items' S^T, dP^T fit TMEM at
 // D = 64 beside the accumulators and K, V).
@@ -41,6 +41,11 @@ __host__ __device__ inline int qtile_snake_count(int i, int total, int n_pipes) 
 // Pipelines per forward / dQ block: two at D = 64 (256 TMEM columns each),
 // one at D = 128.
 constexpr int qtile_pipes_per_block(int D) { return D == 64 ? 2 : 1; }
+// Pipelines per forward block.
+#ifndef DETATTN_FWD_NP64
+#define DETATTN_FWD_NP64 2
+#endif
+constexpr int fwd_pipes_per_block(int D) { return D == 64 ? DETATTN_FWD_NP64 : 1; }
 
 // Packed variable-length batches: sequence s holds query rows cu_q[s] ..
 // cu_q[s + 1] - 1 of the packed [total_q, Hq, D] tensors and key rows
@@ -162,9 +167,12 @@ __host__ __device__ inline void dkdv_tile_coords(int t, int n_tiles, int BH, int
 // `vt` (not null) selects the packed variable-length form: the tensor maps
 // then cover the packed rows with B = 1, FwdArgs::T / BwdArgs::T is the
 // number of packed query rows, and units / tiles come from the table.
+// The forward's `mo` map covers O ([B, T, Hq, D], or the packed rows) with
+// boxes of 32 rows x 64 columns: each softmax warp stores its rows of a tile.
+constexpr int kFwdStoreRows = 32;
 cudaError_t launch_fwd(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const FwdArgs& a, const QTileSched& sched,
-                       const VarlenTable* vt, cudaStream_t st);
+                       const CUtensorMap& mv, const CUtensorMap& mo, const FwdArgs& a,
+                       const QTileSched& sched, const VarlenTable* vt, cudaStream_t st);
 // `sms`: the current device's SM count (the grid is persistent).
 cudaError_t launch_delta(const DeltaArgs& a, int sms, const VarlenTable* vt, cudaStream_t st);
 // Clusters of c blocks of the dK/dV kernel that can be resident at once on the

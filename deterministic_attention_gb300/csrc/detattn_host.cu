@@ -168,9 +168,8 @@ int sm_count(int* out);
 // Units are numbered heaviest first in groups of `per_group` equal units
 // (the heads, or batches and heads, of one query tile): unit u weighs
 // group_w[u / per_group].
-void qtile_schedule_w(int D, const std::vector<double>& group_w, int per_group, int sms,
+void qtile_schedule_w(int NP, const std::vector<double>& group_w, int per_group, int sms,
                       QTileSched* out, int* grid) {
-  const int NP = qtile_pipes_per_block(D);
   const long units = static_cast<long>(group_w.size()) * per_group;
   // One block per SM while there are units for it: a second pipeline on an
   // SM adds far less than a second SM does.
@@ -206,43 +205,46 @@ void qtile_schedule_w(int D, const std::vector<double>& group_w, int per_group, 
   out->n_listed = n;
 }
 
-void qtile_schedule(int D, int B, int T, int Hq, int causal, int sms, QTileSched* out, int* grid) {
+void qtile_schedule(int NP, int B, int T, int Hq, int causal, int sms, QTileSched* out, int* grid) {
   const int n_m = (T + kTileM - 1) / kTileM;
-  const int kv_tiles = (T + kFwdTileN - 1) / kFwdTileN;
+  const int kv_tiles = (T + kDqTileN - 1) / kDqTileN;
   std::vector<double> w(n_m);
   for (int g = 0; g < n_m; ++g) {
     const int mt = n_m - 1 - g;
-    const int n_kv = causal ? std::min(kv_tiles, (mt * kTileM + kTileM) / kFwdTileN) : kv_tiles;
+    const int n_kv = causal ? std::min(kv_tiles, (mt * kTileM + kTileM) / kDqTileN) : kv_tiles;
     w[g] = n_kv + 2.0;
   }
-  qtile_schedule_w(D, w, B * Hq, sms, out, grid);
+  qtile_schedule_w(NP, w, B * Hq, sms, out, grid);
 }
 
-// The schedule depends only on (D, B, T, Hq, causal, SMs): the last one is
-// kept (the forward and dQ of one layer share it).
-void cached_qtile_schedule(int D, int B, int T, int Hq, int causal, int sms, QTileSched* out,
+// The schedule depends only on (pipelines per block, B, T, Hq, causal, SMs):
+// the last one for each pipeline count is kept (the forward and dQ of one
+// layer each reuse theirs).
+void cached_qtile_schedule(int NP, int B, int T, int Hq, int causal, int sms, QTileSched* out,
                            int* grid) {
   static std::mutex mu;
-  static int key[6] = {-1, -1, -1, -1, -1, -1};
-  static QTileSched sched;
-  static int g = 0;
+  static int key[2][6] = {{-1, -1, -1, -1, -1, -1}, {-1, -1, -1, -1, -1, -1}};
+  static QTileSched sched[2];
+  static int g[2] = {0, 0};
   std::lock_guard<std::mutex> lock(mu);
-  const int want[6] = {D, B, T, Hq, causal, sms};
-  if (!std::equal(want, want + 6, key)) {
-    qtile_schedule(D, B, T, Hq, causal, sms, &sched, &g);
-    std::copy(want, want + 6, key);
+  const int slot = NP > 1 ? 1 : 0;
+  const int want[6] = {NP, B, T, Hq, causal, sms};
+  if (!std::equal(want, want + 6, key[slot])) {
+    qtile_schedule(NP, B, T, Hq, causal, sms, &sched[slot], &g[slot]);
+    std::copy(want, want + 6, key[slot]);
   }
-  *out = sched;
-  *grid = g;
+  *out = sched[slot];
+  *grid = g[slot];
 }
 
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int T,
              int Hq, int Hkv, int D, float scale, int causal, cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   int rc;
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kFwdTileN, "k")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kFwdTileN, "v")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mo, o, B, T, Hq, D, kFwdStoreRows, "o")) != DETATTN_OK) return rc;
   FwdArgs a{};
   a.o = o;
   a.lse = lse;
@@ -258,8 +260,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
   QTileSched sc;
   int g;
-  cached_qtile_schedule(D, B, T, Hq, causal, sms, &sc, &g);
-  return launched(launch_fwd(D, g, mq, mk, mv, a, sc, nullptr, st), "attn_fwd");
+  cached_qtile_schedule(fwd_pipes_per_block(D), B, T, Hq, causal, sms, &sc, &g);
+  return launched(launch_fwd(D, g, mq, mk, mv, mo, a, sc, nullptr, st), "attn_fwd");
 }
 
 // Workspace: the row statistics, then (from a 256-byte boundary) the dQ
@@ -456,10 +458,9 @@ int dq_impl(const void* q, const void* k, const void* v, const void* dout, const
   a.unit_counter = counter;
   int sms = 0;
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
-  static_assert(kDqTileN == kFwdTileN, "the forward's schedule weights fit dQ");
   QTileSched sc;
   int g;
-  cached_qtile_schedule(D, B, T, Hq, causal, sms, &sc, &g);
+  cached_qtile_schedule(qtile_pipes_per_block(D), B, T, Hq, causal, sms, &sc, &g);
   return launched(launch_dq(D, g, mq, mk, mv, mdo, a, sc, nullptr, st), "attn_bwd_dq");
 }
 
@@ -635,10 +636,10 @@ int check_packed(const int* cu_q, const int* cu_k, int n_seq, int Hq, int Hkv, i
   std::vector<QE> qe;
   for (int s = 0; s < n_seq; ++s) {
     const int tq = cu_q[s + 1] - cu_q[s], tk = cu_k[s + 1] - cu_k[s], off = tk - tq;
-    const int tiles = (tk + kFwdTileN - 1) / kFwdTileN;
+    const int tiles = (tk + kDqTileN - 1) / kDqTileN;
     for (int mt = 0; mt * kTileM < tq; ++mt) {
       const int last = std::min(mt * kTileM + kTileM - 1, tq - 1) + off;
-      const int n_kv = causal ? (last < 0 ? 0 : std::min(tiles, last / kFwdTileN + 1)) : tiles;
+      const int n_kv = causal ? (last < 0 ? 0 : std::min(tiles, last / kDqTileN + 1)) : tiles;
       qe.push_back({n_kv + 2.0, s, mt});
     }
   }
@@ -685,7 +686,7 @@ int fwd_varlen_impl(const void* q, const void* k, const void* v, void* o, float*
                     const Packed& pk, int Hq, int Hkv, int D, float scale, int causal,
                     cudaStream_t st) {
   if (pk.qt.n_tiles == 0) return ok_status();
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   int rc;
   // Without any key rows the kernels never load K, V, but the tensor maps
   // still need an address: q stands in.
@@ -695,6 +696,7 @@ int fwd_varlen_impl(const void* q, const void* k, const void* v, void* o, float*
   if ((rc = encode_rows(&mq, q, 1, pk.total_q, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mk, kk, 1, tk_rows, Hkv, D, kFwdTileN, "k")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mv, vv, 1, tk_rows, Hkv, D, kFwdTileN, "v")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mo, o, 1, pk.total_q, Hq, D, kFwdStoreRows, "o")) != DETATTN_OK) return rc;
   FwdArgs a{};
   a.o = o;
   a.lse = lse;
@@ -710,8 +712,8 @@ int fwd_varlen_impl(const void* q, const void* k, const void* v, void* o, float*
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
   QTileSched sc;
   int g;
-  qtile_schedule_w(D, pk.q_weight, Hq, sms, &sc, &g);
-  return launched(launch_fwd(D, g, mq, mk, mv, a, sc, &pk.qt, st), "attn_fwd_varlen");
+  qtile_schedule_w(fwd_pipes_per_block(D), pk.q_weight, Hq, sms, &sc, &g);
+  return launched(launch_fwd(D, g, mq, mk, mv, mo, a, sc, &pk.qt, st), "attn_fwd_varlen");
 }
 
 int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -787,7 +789,7 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, 
     b.unit_counter = counter;
     QTileSched sc;
     int g;
-    qtile_schedule_w(D, pk.q_weight, Hq, sms, &sc, &g);
+    qtile_schedule_w(qtile_pipes_per_block(D), pk.q_weight, Hq, sms, &sc, &g);
     if ((rc = launched(launch_dq(D, g, mq, mk, mv, mdo, b, sc, &pk.qt, st),
                        "attn_bwd_varlen (dQ)")) != DETATTN_OK)
       return rc;
@@ -1428,7 +1430,7 @@ int detattn_diag_qtile_deal(int D, int B, int T, int Hq, int causal, int sms, in
   if (empty) return 0;
   QTileSched sc;
   int grid = 0;
-  qtile_schedule(D, B, T, Hq, causal, sms, &sc, &grid);
+  qtile_schedule(qtile_pipes_per_block(D), B, T, Hq, causal, sms, &sc, &grid);
   for (long u = 0; u < units; ++u) pipe_of_unit[u] = -1;
   for (int i = 0; i < sc.n_pipes; ++i) {
     if (sc.n_listed > 0) {
