@@ -926,80 +926,82 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ============================================================== dQ
-// Work unit: one 128-query tile of one (b, query head), over 64-key tiles
-// 0..diagonal in ascending order.  Persistent like the forward: a block holds
-// NP pipelines (two at D = 64, one at D = 128), each with its own warps,
-// shared memory, mbarriers and TMEM columns, working through units it takes,
-// heaviest first, from a counter in the workspace (or, without one, the units
-// the host dealt it).  Per pipeline, warp 0 loads each unit's Q, dO and the K, V
-// ring; warp 1 issues S = Q K^T, dP = dO V^T and dQ += dS K; warps 2..9 (two
-// threads per query row, one per 32-key half) form P and dS and, at the
-// unit's end, write dQ.  The unit's Q and dO are copied into TMEM (the A
-// operands of S and dP), dS goes to a shared-memory tile, and the
-// element-wise warps release S, dP as soon as they hold them in registers, so
-// the next key tile's S, dP are computed while they work on this one.
-constexpr int kDqPipeWarps = 10;  // producer, MMA issuer, 8 compute warps
-constexpr int kDqPipeThreads = kDqPipeWarps * 32;
+// Work unit: one 128-query tile of one (b, query head), over 128-key tiles
+// 0..diagonal in ascending order.  Persistent, one pipeline per SM, working
+// through units it takes, heaviest first, from a counter in the workspace (or,
+// without one, the units the host dealt it):
+//   warp 0      TMA producer: each unit's Q and dO (two slots at D = 64, so
+//               the next unit's load runs ahead), K_j and V_j into a ring
+//   warp 1      tcgen05 issuer: S_j = Q K_j^T and dP_j = dO V_j^T (both
+//               operands in shared memory, N = 128) as soon as the
+//               element-wise warps hold S_{j-1}, dP_{j-1} in registers; then
+//               dQ += dS_{j-1} K_{j-1} with dS read from TMEM
+//   warps 4..11 element-wise, two threads per query row (TMEM lane), one per
+//               64-key half: P = 2^(S scale log2e - LSE log2e), dS = P (dP -
+//               Delta) as packed bf16 into TMEM columns of their own; at the
+//               unit's end dQ = scale * (sum over key tiles) to bf16.
+// TMEM: S [128 fp32 columns], dP [128], dS [64 columns of bf16 pairs], dQ [D].
+// Every dQ row is summed by one block over its key tiles in ascending order.
+// Warps 0..3 (one warpgroup): producer, MMA issuer, two idle; warps 4..11 (two
+// warpgroups): element-wise.  The first warpgroup hands registers to the
+// other two, whose threads each hold 64 scores and 64 dP values.
+constexpr int kDqWarps = 12;
+constexpr int kDqThreads = kDqWarps * 32;
+constexpr uint32_t kDqCtrlRegs = 88, kDqElemRegs = 192;
+constexpr int kDqRegBudget = 128 * kDqCtrlRegs + 256 * kDqElemRegs;
 template <int D>
 struct DqCfg {
   static constexpr int kAtoms = D / 64;
   static constexpr int kQBytes = kTileM * 128 * kAtoms;     // 128 queries x D
-  static constexpr int kKvBytes = kDqTileN * 128 * kAtoms;  // 64 keys x D
-  static constexpr int kStages = 3;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffdO = kQBytes;
-  static constexpr int kOffK = 2 * kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKvBytes;
-  // The dS tile [128 queries x 64 keys] bf16, 128-byte swizzled like a
-  // TMA-loaded tile, read by the dQ MMA from shared memory.
-  static constexpr int kOffDS = kOffV + kStages * kKvBytes;
-  static constexpr int kPipeBytes = kOffDS + kTileM * 128;  // multiple of 1024
-  static constexpr int NP = qtile_pipes_per_block(D);
-  static constexpr int kSmemBytes = NP * kPipeBytes + 1024;
-  static constexpr uint32_t kTmemCols = (D == 64) ? 256 : 512;  // per pipeline
-  static constexpr uint32_t kColS = 0;    // S fp32 [128 x 64]
-  static constexpr uint32_t kColDP = 64;  // dP fp32 [128 x 64]
-  static constexpr uint32_t kColDQ = 128; // dQ accumulator, D cols
-  // The unit's Q and dO tiles also live in TMEM (packed bf16 pairs, D/2
-  // columns each), so S = Q K^T and dP = dO V^T read only K / V from shared
-  // memory: an N = 64 MMA with both operands in shared memory is bound by
-  // shared-memory bandwidth (48 clocks against 32 for the math).
-  static constexpr uint32_t kColQ = kColDQ + D;
-  static constexpr uint32_t kColdO = kColQ + D / 2;
-  static_assert(kColdO + D / 2 <= kTmemCols, "TMEM layout");
-  static_assert(kPipeBytes % 1024 == 0, "pipelines keep the 1024-byte swizzle alignment");
-  static_assert(D == 64 || NP == 1, "D = 128 needs a block's whole TMEM");
-  static_assert(kSmemBytes + 1024 <= 227 * 1024, "shared memory per block");
+  static constexpr int kKvBytes = kDqTileN * 128 * kAtoms;  // 128 keys x D
+  static constexpr int kQSlots = (D == 64) ? 2 : 1;         // Q, dO pairs
+  // K stays until its tile's dQ MMA (late), V only until dP: K gets the
+  // deeper ring.
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = (D == 64) ? 3 : 2;
+  static constexpr int kOffQ = 0;  // slot i: Q at 2 i kQBytes, dO at (2 i + 1) kQBytes
+  static constexpr int kOffK = 2 * kQSlots * kQBytes;
+  static constexpr int kOffV = kOffK + kKStages * kKvBytes;
+  static constexpr int kSmemBytes = kOffV + kVStages * kKvBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 320;
+  static_assert(kColDQ + D <= kTmemCols, "TMEM layout");
+  static_assert(kSmemBytes + 512 <= 227 * 1024, "shared memory per block");
 };
+constexpr int kDqMaxStages = 3;
 
-enum : int { kDqBarQ = 0, kDqBarKFull = 1, kDqBarVFull = 4, kDqBarKEmpty = 7, kDqBarVEmpty = 10,
-             kDqBarS = 13, kDqBarDS = 14, kDqBarAcc = 15, kDqBarDrain = 16, kDqBarQTmem = 17,
-             kDqBarQUsed = 18,   // the unit's S, dP MMAs are done (Q, dO no longer read)
-             kDqBarAccFree = 19, // the unit's epilogue has read dQ
-             kDqBarSFree = 20,   // element-wise warps hold this tile's S, dP in registers
-             kDqBarDSFree = 21,  // the dQ MMAs are done with the dS tile
-             kDqBarUnit = 22,    // [4] unit k published in ring slot k % 4
-             kDqNumBars = 26 };
+enum : int { kDqBarQFull = 0,                       // [2] Q, dO slot loaded
+             kDqBarQFree = 2,                       // [2] the unit's S, dP MMAs are done with the slot
+             kDqBarKFull = 4, kDqBarKEmpty = 7,     // [3]
+             kDqBarVFull = 10, kDqBarVEmpty = 13,   // [3]
+             kDqBarS = 16,        // S_j, dP_j are in TMEM
+             kDqBarSFree = 17,    // element-wise warps hold S_j, dP_j in registers (8)
+             kDqBarDS = 18,       // dS_j is in TMEM (8)
+             kDqBarDSFree = 19,   // the dQ MMAs of tile j are done with dS
+             kDqBarAcc = 20,      // the unit's last dQ MMA has finished
+             kDqBarDrain = 21,
+             kDqBarUnit = 22,     // [4] unit k published in ring slot k % 4
+             kDqBarUnitFree = 26, // [4] ring slot k % 4 read by the MMA and element-wise warps (9)
+             kDqNumBars = 30 };
 
 template <int D, class VT>
-__global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
                    const BwdArgs a, const __grid_constant__ QTileSched sched,
                    const __grid_constant__ VT vt) {
   using C = DqCfg<D>;
   constexpr bool VL = std::is_same<VT, VarlenTable>::value;
-  constexpr int NS = C::kStages;
-  constexpr int NP = C::NP;
+  constexpr int NK = C::kKStages, NV = C::kVStages;
+  constexpr int NQ = C::kQSlots;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t bars_all[NP][kDqNumBars];
+  __shared__ __align__(8) uint64_t bars[kDqNumBars];
   __shared__ uint32_t tmem_slot;
+  __shared__ int unit_ring[4];
 
-  const int pipe = static_cast<int>(threadIdx.x) / kDqPipeThreads;
-  const int warp = (static_cast<int>(threadIdx.x) >> 5) % kDqPipeWarps;  // role within the pipeline
+  const int warp = static_cast<int>(threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  const int gwarp = static_cast<int>(threadIdx.x) >> 5;                  // TMEM lane quarter: gwarp & 3
-  const int pipe_id = static_cast<int>(blockIdx.x) * NP + pipe;
+  const int pipe_id = static_cast<int>(blockIdx.x);
   const int kv_tiles = (a.T + kDqTileN - 1) / kDqTileN;
   int first = pipe_id, n_units;
   if (sched.n_listed > 0) {
@@ -1013,15 +1015,13 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
     return sched.n_listed > 0 ? static_cast<int>(sched.unit[first + k])
                               : qtile_snake_unit(pipe_id, k, sched.n_pipes);
   };
-  // Units are numbered heaviest first.  With a.unit_counter, a pipeline's
-  // producer takes the next unit from that counter whenever it is ready for
-  // one, so pipelines that start early (on SMs another kernel frees first)
-  // take the heaviest units; otherwise it follows the host's deal.  Either
-  // way it passes unit k (or -1 after the last) to the pipeline's other warps
-  // in ring slot k % 4, published by mbarrier kDqBarUnit + k % 4.  Which
-  // pipeline computes a unit does not change any bit of its result.
+  // Units are numbered heaviest first.  With a.unit_counter, the producer
+  // takes the next unit from that counter whenever it is ready for one, so
+  // blocks that start early (on SMs another kernel frees first) take the
+  // heaviest units; otherwise it follows the host's deal.  Either way it
+  // passes unit k (or -1 after the last) to the other warps in ring slot
+  // k % 4.  Which block computes a unit does not change any bit of its result.
   const int n_all = (VL ? vt_tiles(vt) : a.n_tiles) * a.BH;
-  __shared__ int unit_ring[NP][4];
   // Rows relative to the unit's sequence, as in the forward: queries from row
   // qbase, keys from kbase, row statistics from rbase; key j visible to
   // query i iff j < tk and (causal) j <= i + off.
@@ -1060,35 +1060,36 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t s0 = smem_u32(smem) + pipe * C::kPipeBytes;
-  const uint32_t sQ = s0 + C::kOffQ, sdO = s0 + C::kOffdO;
-  const uint32_t sK0 = s0 + C::kOffK, sV0 = s0 + C::kOffV, sDS = s0 + C::kOffDS;
-  uint64_t* bars = bars_all[pipe];
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sQ0 = s0 + C::kOffQ, sK0 = s0 + C::kOffK, sV0 = s0 + C::kOffV;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
-  if (threadIdx.x < 32) {
-    tmem_alloc(smem_u32(&tmem_slot), NP * C::kTmemCols);
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_slot), C::kTmemCols);
     tmem_relinquish();
     tc_fence_before();
   }
-  if (warp == 1 && lane == 0) {  // each pipeline's MMA warp sets up its own barriers
-    mbar_init(bar(kDqBarQ), 1);
-    for (int s = 0; s < 3; ++s) {
+  if (warp == 1 && lane == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kDqBarQFull + i), 1);
+      mbar_init(bar(kDqBarQFree + i), 1);
+    }
+    for (int s = 0; s < kDqMaxStages; ++s) {
       mbar_init(bar(kDqBarKFull + s), 1);
-      mbar_init(bar(kDqBarVFull + s), 1);
       mbar_init(bar(kDqBarKEmpty + s), 1);
+      mbar_init(bar(kDqBarVFull + s), 1);
       mbar_init(bar(kDqBarVEmpty + s), 1);
     }
     mbar_init(bar(kDqBarS), 1);
+    mbar_init(bar(kDqBarSFree), 8);
     mbar_init(bar(kDqBarDS), 8);
+    mbar_init(bar(kDqBarDSFree), 1);
     mbar_init(bar(kDqBarAcc), 1);
     mbar_init(bar(kDqBarDrain), 1);
-    mbar_init(bar(kDqBarQTmem), 8);
-    mbar_init(bar(kDqBarQUsed), 1);
-    mbar_init(bar(kDqBarAccFree), 8);
-    mbar_init(bar(kDqBarSFree), 8);
-    mbar_init(bar(kDqBarDSFree), 1);
-    for (int k = 0; k < 4; ++k) mbar_init(bar(kDqBarUnit + k), 1);
+    for (int k = 0; k < 4; ++k) {
+      mbar_init(bar(kDqBarUnit + k), 1);
+      mbar_init(bar(kDqBarUnitFree + k), 9);
+    }
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -1099,49 +1100,52 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_slot + pipe * C::kTmemCols;
+  const uint32_t tmem = tmem_slot;
   const uint64_t wait_ns = a.wait_ns;
   bool ok = true;
-  // Unit k of this pipeline, for the warps other than the producer (whole
-  // warp; -1 after the last unit, or when the wait runs out with ok false).
+  // Unit k, for the MMA and element-wise warps (whole warp; -1 after the
+  // last unit, or when the wait runs out with ok false).  The slot is handed
+  // back once read.
   auto read_unit = [&](int k) -> int {
     if (!(ok = warp_all(mbar_wait(bar(kDqBarUnit + (k & 3)), (k >> 2) & 1, wait_ns)))) return -1;
-    return unit_ring[pipe][k & 3];
+    const int u = unit_ring[k & 3];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kDqBarUnitFree + (k & 3)));
+    return u;
   };
 
+  if (warp < 4) {
+  // Each warpgroup changes its register count at the top of its own branch,
+  // so the code after it is compiled for the new count.
+  setmaxnreg_dec<kDqCtrlRegs>();
   if (warp == 0) {
     if (lane == 0) {
-      int last_k[3] = {-1, -1, -1}, last_v[3] = {-1, -1, -1};
-      int last_q = -1;
+      int last_k[kDqMaxStages] = {-1, -1, -1}, last_v[kDqMaxStages] = {-1, -1, -1};
+      int last_q[2] = {-1, -1};
       int gj = 0;  // key tiles loaded so far, over all units
+      int ne = 0;  // units with key tiles so far
       for (int ku = 0; ok; ++ku) {
-        // The previous unit's Q, dO must no longer be read: copied to TMEM.
-        if (ku > 0 && !(ok = mbar_wait(bar(kDqBarQTmem), (ku - 1) & 1, wait_ns))) break;
+        // Ring slot ku % 4 must have been read for unit ku - 4.
+        if (ku >= 4 && !(ok = mbar_wait(bar(kDqBarUnitFree + (ku & 3)), ((ku >> 2) - 1) & 1, wait_ns)))
+          break;
         int u;
         if (a.unit_counter != nullptr) {
-          if (NP > 1 && pipe > 0 && n_all <= static_cast<int>(gridDim.x)) {
-            // No more units than blocks: the first pipeline of each block takes
-            // them, one unit per SM (the others would share SMs while blocks
-            // sit idle).
-            u = -1;
-          } else {
-            const unsigned v = atomicAdd(a.unit_counter, 1u);
-            u = v < static_cast<unsigned>(n_all) ? static_cast<int>(v) : -1;
-            // A cleared counter never passes n_all plus one per pipeline: a
-            // larger value means it was not cleared before this launch.
-            if (v >= static_cast<unsigned>(n_all) + gridDim.x * NP) atomicOr(&g_bwd_status, 16u);
-          }
+          const unsigned v = atomicAdd(a.unit_counter, 1u);
+          u = v < static_cast<unsigned>(n_all) ? static_cast<int>(v) : -1;
+          // A cleared counter never passes n_all plus one per block: a larger
+          // value means it was not cleared before this launch.
+          if (v >= static_cast<unsigned>(n_all) + gridDim.x) atomicOr(&g_bwd_status, 16u);
         } else {
           u = ku < n_units ? u_of(ku) : -1;
         }
-        unit_ring[pipe][ku & 3] = u;
+        unit_ring[ku & 3] = u;
         mbar_arrive(bar(kDqBarUnit + (ku & 3)));
         if (u < 0) {
           if (a.unit_counter != nullptr) {
-            // Count this pipeline out (second word); the last one to finish
+            // Count this block out (second word); the last one to finish
             // taking units puts both words back to zero for the next launch.
             __threadfence();
-            if (atomicAdd(a.unit_counter + 1, 1u) == gridDim.x * NP - 1) {
+            if (atomicAdd(a.unit_counter + 1, 1u) == gridDim.x - 1) {
               atomicExch(a.unit_counter, 0u);
               atomicExch(a.unit_counter + 1, 0u);
             }
@@ -1149,300 +1153,274 @@ __global__ void __launch_bounds__(kDqPipeThreads * qtile_pipes_per_block(D), 1)
           break;
         }
         const Unit t = unit_info(u);
-        mbar_arrive_expect_tx(bar(kDqBarQ), 2 * C::kQBytes);
+        if (t.n_kv == 0) continue;  // a packed unit whose rows see no key: nothing to load
+        const int slot = ne % NQ, use = ne / NQ;
+        // The unit that last used this slot must be done with it.
+        if (use > 0 && !(ok = mbar_wait(bar(kDqBarQFree + slot), (use - 1) & 1, wait_ns))) break;
+        mbar_arrive_expect_tx(bar(kDqBarQFull + slot), 2 * C::kQBytes);
+        const uint32_t sq = sQ0 + 2 * slot * C::kQBytes;
         for (int at = 0; at < C::kAtoms; ++at) {
-          tma_load_4d(sQ + at * (kTileM * 128), &mQ, bar(kDqBarQ), at * 64, t.h, t.qbase + t.m0,
-                      t.b);
-          tma_load_4d(sdO + at * (kTileM * 128), &mdO, bar(kDqBarQ), at * 64, t.h,
+          tma_load_4d(sq + at * (kTileM * 128), &mQ, bar(kDqBarQFull + slot), at * 64, t.h,
                       t.qbase + t.m0, t.b);
+          tma_load_4d(sq + C::kQBytes + at * (kTileM * 128), &mdO, bar(kDqBarQFull + slot), at * 64,
+                      t.h, t.qbase + t.m0, t.b);
         }
-        last_q = ku;
+        last_q[slot] = ne;
         for (int j = 0; j < t.n_kv; ++j, ++gj) {
-          const int s = gj % NS;
-          const uint32_t ph = (gj / NS) & 1;
-          if (gj >= NS && !(ok = mbar_wait(bar(kDqBarKEmpty + s), ph ^ 1, wait_ns))) break;
-          mbar_arrive_expect_tx(bar(kDqBarKFull + s), C::kKvBytes);
+          const int sk = gj % NK, sv = gj % NV;
+          if (gj >= NK && !(ok = mbar_wait(bar(kDqBarKEmpty + sk), ((gj / NK) & 1) ^ 1, wait_ns))) break;
+          mbar_arrive_expect_tx(bar(kDqBarKFull + sk), C::kKvBytes);
           for (int at = 0; at < C::kAtoms; ++at)
-            tma_load_4d(sK0 + s * C::kKvBytes + at * (kDqTileN * 128), &mK, bar(kDqBarKFull + s),
+            tma_load_4d(sK0 + sk * C::kKvBytes + at * (kDqTileN * 128), &mK, bar(kDqBarKFull + sk),
                         at * 64, t.hkv, t.kbase + j * kDqTileN, t.b);
-          last_k[s] = gj;
-          if (gj >= NS && !(ok = mbar_wait(bar(kDqBarVEmpty + s), ph ^ 1, wait_ns))) break;
-          mbar_arrive_expect_tx(bar(kDqBarVFull + s), C::kKvBytes);
+          last_k[sk] = gj;
+          if (gj >= NV && !(ok = mbar_wait(bar(kDqBarVEmpty + sv), ((gj / NV) & 1) ^ 1, wait_ns))) break;
+          mbar_arrive_expect_tx(bar(kDqBarVFull + sv), C::kKvBytes);
           for (int at = 0; at < C::kAtoms; ++at)
-            tma_load_4d(sV0 + s * C::kKvBytes + at * (kDqTileN * 128), &mV, bar(kDqBarVFull + s),
+            tma_load_4d(sV0 + sv * C::kKvBytes + at * (kDqTileN * 128), &mV, bar(kDqBarVFull + sv),
                         at * 64, t.hkv, t.kbase + j * kDqTileN, t.b);
-          last_v[s] = gj;
+          last_v[sv] = gj;
         }
+        ++ne;
       }
       if (!ok) {
-        if (last_q >= 0) mbar_wait(bar(kDqBarQ), last_q & 1, wait_ns);
-        for (int s = 0; s < NS; ++s) {
-          if (last_k[s] >= 0) mbar_wait(bar(kDqBarKFull + s), (last_k[s] / NS) & 1, wait_ns);
-          if (last_v[s] >= 0) mbar_wait(bar(kDqBarVFull + s), (last_v[s] / NS) & 1, wait_ns);
-        }
+        // Let every copy already issued land before the block's shared memory goes away.
+        for (int i = 0; i < NQ; ++i)
+          if (last_q[i] >= 0) mbar_wait(bar(kDqBarQFull + i), (last_q[i] / NQ) & 1, wait_ns);
+        for (int s = 0; s < NK; ++s)
+          if (last_k[s] >= 0) mbar_wait(bar(kDqBarKFull + s), (last_k[s] / NK) & 1, wait_ns);
+        for (int s = 0; s < NV; ++s)
+          if (last_v[s] >= 0) mbar_wait(bar(kDqBarVFull + s), (last_v[s] / NV) & 1, wait_ns);
       }
     }
+    __syncwarp();
   } else if (warp == 1) {
     // MMA issuer: the whole warp runs the loop (MMA issue is warp-collective);
     // every wait is made warp-uniform so the warp stays converged.
-    const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDQ = tmem + C::kColDQ;
+    const uint32_t tS = tmem + C::kColS, tDP = tmem + C::kColDP, tDS = tmem + C::kColDS,
+                   tDQ = tmem + C::kColDQ;
     constexpr uint32_t kIdS = idesc_bf16(kTileM, kDqTileN, false, false);
     constexpr uint32_t kIdDQ = idesc_bf16(kTileM, D, false, true);
     // Operand descriptors built once; the loops only add constant offsets.
+    const uint64_t dQ0 = sdesc_sw128(sQ0, 16, 1024);
     const uint64_t dK0 = sdesc_sw128(sK0, 16, 1024), dV0 = sdesc_sw128(sV0, 16, 1024);
     const uint64_t dKm0 = sdesc_sw128(sK0, kDqTileN * 128, 1024);  // K as MN-major B
-    int gj = 0;
-    {
-      const uint64_t dDS = sdesc_sw128(sDS, 16, 1024);  // dS as K-major A
-      const uint32_t aQ = tmem + C::kColQ, adO = tmem + C::kColdO;
-      // S, dP of tile j of unit ku (g-th over all units), once the element-wise
-      // warps hold the previous tile's in registers.
-      auto issue_sdp = [&](const Unit& t, int ku, int j, int g) -> bool {
-        const int s = g % NS;
-        const uint32_t ph = (g / NS) & 1;
-        if (j == 0 && !(warp_all(mbar_wait(bar(kDqBarQ), ku & 1, wait_ns)) &&
-                        warp_all(mbar_wait(bar(kDqBarQTmem), ku & 1, wait_ns))))
-          return false;
-        if constexpr (VL) {
-          if (t.n_kv == 0) {
-            // A packed unit whose rows see no key: no products, but the same
-            // hand-offs as any unit (its Q copy is released at once).
-            tc_fence_after();
-            mma_commit(bar(kDqBarQUsed));
-            return true;
-          }
-        }
-        if (g > 0 && !warp_all(mbar_wait(bar(kDqBarSFree), (g - 1) & 1, wait_ns))) return false;
-        if (!warp_all(mbar_wait(bar(kDqBarKFull + s), ph, wait_ns))) return false;
-        tc_fence_after();
-        // K = D in steps of 16: packed Q / dO columns 8 apart, K-major K / V
-        // slices of 32 bytes, 64-column atoms kDqTileN * 128 bytes apart.
-        const uint64_t dK = desc_add(dK0, s * C::kKvBytes), dV = desc_add(dV0, s * C::kKvBytes);
+    // S_g = Q K_g^T and dP_g = dO V_g^T, Q / dO from slot `slot`.
+    auto issue_sdp = [&](int g, int slot) -> bool {
+      const int sk = g % NK, sv = g % NV;
+      if (!warp_all(mbar_wait(bar(kDqBarKFull + sk), (g / NK) & 1, wait_ns))) return false;
+      tc_fence_after();
+      const uint64_t dq = desc_add(dQ0, 2 * slot * C::kQBytes), ddo = desc_add(dq, C::kQBytes);
+      const uint64_t dK = desc_add(dK0, sk * C::kKvBytes), dV = desc_add(dV0, sv * C::kKvBytes);
 #pragma unroll
-        for (int at = 0; at < C::kAtoms; ++at) {
-          const uint32_t a = aQ + 32 * at;
-          const uint64_t b = desc_add(dK, at * (kDqTileN * 128));
-          mma_ts_x4(tS, a, a + 8, a + 16, a + 24, b, desc_add(b, 32), desc_add(b, 64),
-                    desc_add(b, 96), kIdS, at > 0 ? 1u : 0u);
-        }
-        if (!warp_all(mbar_wait(bar(kDqBarVFull + s), ph, wait_ns))) return false;
-        tc_fence_after();
+      for (int at = 0; at < C::kAtoms; ++at) {
+        const uint64_t aq = desc_add(dq, at * (kTileM * 128)), b = desc_add(dK, at * (kDqTileN * 128));
+        mma_ss_x4(tS, aq, desc_add(aq, 32), desc_add(aq, 64), desc_add(aq, 96), b, desc_add(b, 32),
+                  desc_add(b, 64), desc_add(b, 96), kIdS, at > 0 ? 1u : 0u);
+      }
+      if (!warp_all(mbar_wait(bar(kDqBarVFull + sv), (g / NV) & 1, wait_ns))) return false;
+      tc_fence_after();
 #pragma unroll
-        for (int at = 0; at < C::kAtoms; ++at) {
-          const uint32_t a = adO + 32 * at;
-          const uint64_t b = desc_add(dV, at * (kDqTileN * 128));
-          mma_ts_x4(tDP, a, a + 8, a + 16, a + 24, b, desc_add(b, 32), desc_add(b, 64),
-                    desc_add(b, 96), kIdS, at > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(kDqBarS));
-        mma_commit(bar(kDqBarVEmpty + s));
-        if (j + 1 == t.n_kv) mma_commit(bar(kDqBarQUsed));  // the unit's last S, dP
-        return true;
-      };
-      Unit t{};
-      int u = read_unit(0);
-      if (u >= 0) {
-        t = unit_info(u);
-        ok = issue_sdp(t, 0, 0, 0);
+      for (int at = 0; at < C::kAtoms; ++at) {
+        const uint64_t ad = desc_add(ddo, at * (kTileM * 128)), b = desc_add(dV, at * (kDqTileN * 128));
+        mma_ss_x4(tDP, ad, desc_add(ad, 32), desc_add(ad, 64), desc_add(ad, 96), b, desc_add(b, 32),
+                  desc_add(b, 64), desc_add(b, 96), kIdS, at > 0 ? 1u : 0u);
       }
-      for (int ku = 0; u >= 0 && ok; ++ku) {
-        for (int j = 0; j < t.n_kv && ok; ++j, ++gj) {
-          const int s = gj % NS;
-          if (j + 1 < t.n_kv && !(ok = issue_sdp(t, ku, j + 1, gj + 1))) break;
-          if (!(ok = warp_all(mbar_wait(bar(kDqBarDS), gj & 1, wait_ns)))) break;
-          // The previous unit's epilogue must have read dQ before this unit's
-          // first dQ MMA overwrites it.
-          if (j == 0 && ku > 0 &&
-              !(ok = warp_all(mbar_wait(bar(kDqBarAccFree), (ku - 1) & 1, wait_ns))))
-            break;
-          tc_fence_after();
-          const uint64_t dKm = desc_add(dKm0, s * C::kKvBytes);
-          mma_ss_x4(tDQ, dDS, desc_add(dDS, 32), desc_add(dDS, 64), desc_add(dDS, 96), dKm,
-                    desc_add(dKm, 2048), desc_add(dKm, 4096), desc_add(dKm, 6144), kIdDQ,
-                    j > 0 ? 1u : 0u);
-          mma_commit(bar(kDqBarKEmpty + s));
-          mma_commit(bar(kDqBarDSFree));
-        }
-        if (!ok) break;
-        mma_commit(bar(kDqBarAcc));
-        u = read_unit(ku + 1);
-        if (u >= 0) {
-          t = unit_info(u);
-          ok = issue_sdp(t, ku + 1, 0, gj);
-        }
+      mma_commit(bar(kDqBarS));
+      mma_commit(bar(kDqBarVEmpty + sv));
+      return true;
+    };
+    // dQ (+)= dS_g K_g: dS of key pair (2c, 2c + 1) in TMEM column c; K step
+    // k (16 keys) reads columns 8k .. 8k + 7 and K rows 16k .. 16k + 15.
+    auto issue_dq = [&](int g, bool first, bool last) -> bool {
+      const int s = g % NK;
+      if (!warp_all(mbar_wait(bar(kDqBarDS), g & 1, wait_ns))) return false;
+      tc_fence_after();
+      const uint64_t dKm = desc_add(dKm0, s * C::kKvBytes);
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        mma_ts_x4(tDQ, tDS + 32 * h, tDS + 32 * h + 8, tDS + 32 * h + 16, tDS + 32 * h + 24,
+                  desc_add(dKm, (4 * h) * 2048), desc_add(dKm, (4 * h + 1) * 2048),
+                  desc_add(dKm, (4 * h + 2) * 2048), desc_add(dKm, (4 * h + 3) * 2048), kIdDQ,
+                  (first && h == 0) ? 0u : 1u);
+      mma_commit(bar(kDqBarKEmpty + s));
+      mma_commit(bar(kDqBarDSFree));
+      if (last) mma_commit(bar(kDqBarAcc));
+      return true;
+    };
+    int gj = 0, ne = 0;
+    int pend = -1;  // the key tile whose dQ MMA is still to be issued
+    bool pend_first = false, pend_last = false;
+    for (int ku = 0; ok; ++ku) {
+      const int u = read_unit(ku);
+      if (u < 0) break;
+      const Unit t = unit_info(u);
+      if (t.n_kv == 0) continue;
+      const int slot = ne % NQ;
+      // With one Q slot the next unit's Q cannot arrive before this one's
+      // last S, dP: finish the previous unit's dQ first, so its epilogue
+      // does not wait behind that load.
+      if (NQ == 1 && pend >= 0) {
+        if (!(ok = issue_dq(pend, pend_first, pend_last))) break;
+        pend = -1;
       }
+      if (!(ok = warp_all(mbar_wait(bar(kDqBarQFull + slot), (ne / NQ) & 1, wait_ns)))) break;
+      for (int j = 0; j < t.n_kv; ++j, ++gj) {
+        // The score columns are free once the element-wise warps hold S, dP
+        // of the previous tile.
+        if (gj > 0 && !(ok = warp_all(mbar_wait(bar(kDqBarSFree), (gj - 1) & 1, wait_ns)))) break;
+        if (!(ok = issue_sdp(gj, slot))) break;
+        if (j + 1 == t.n_kv) mma_commit(bar(kDqBarQFree + slot));
+        if (pend >= 0 && !(ok = issue_dq(pend, pend_first, pend_last))) break;
+        pend = gj;
+        pend_first = (j == 0);
+        pend_last = (j + 1 == t.n_kv);
+      }
+      ++ne;
     }
+    if (ok && pend >= 0) ok = issue_dq(pend, pend_first, pend_last);
     mma_commit(bar(kDqBarDrain));
     warp_all(mbar_wait(bar(kDqBarDrain), 0, wait_ns));
+  }
   } else {
-    // Eight warps: warps w and w+4 of a pipeline share a TMEM lane quarter,
-    // i.e. the same 32 query rows; half 0 takes key columns 0..31 of the tile,
-    // half 1 columns 32..63, and writes its dS (bf16) into those columns of the
-    // shared-memory dS tile.
-    const int quarter = gwarp & 3;
-    const int half = (warp - 2) >> 2;
+    setmaxnreg_inc<kDqElemRegs>();
+    // Element-wise warps: warps w and w + 4 share a TMEM lane quarter, i.e.
+    // the same 32 query rows; half 0 takes keys 0..63 of each tile, half 1
+    // keys 64..127.
+    const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;
     const int r = quarter * 32 + lane;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t tS = tl + C::kColS + half * 32, tDP = tl + C::kColDP + half * 32;
+    const uint32_t tS = tl + C::kColS + 64 * half, tDP = tl + C::kColDP + 64 * half;
+    const uint32_t tDS = tl + C::kColDS + 32 * half;
     const float sl2 = a.scale_log2;
-    // Q and dO row r of unit ku into TMEM as the A operands of S and dP, once
-    // the previous unit's S, dP MMAs no longer read them: this warp copies
-    // elements D/2 half .. D/2 half + D/2 - 1 (D/16 16-byte chunks of the
-    // 128-byte-swizzled tile row, 64-column atoms 128 * 128 bytes apart) as
-    // D/4 packed pairs.  Done for the next unit before this unit's epilogue,
-    // so its first S, dP overlap the epilogue.
-    auto copy_q = [&](int ku) -> bool {
-      bool good = true;
-      if (ku > 0) good = warp_all(mbar_wait(bar(kDqBarQUsed), (ku - 1) & 1, wait_ns));
-      if (good) good = warp_all(mbar_wait(bar(kDqBarQ), ku & 1, wait_ns));
-      if (good) {
-        tc_fence_after();
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-#pragma unroll
-          for (int g = 0; g < D / 64; ++g) {  // groups of four chunks (32 elements)
-            uint32_t v16[16];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int e = half * (D / 2) + 32 * g + 8 * c;  // first element of the chunk
-              const uint32_t base = (which == 0 ? sQ : sdO) + (e / 64) * (kTileM * 128) + r * 128;
-              const uint4 x = ld_shared_u4(base + ((((e % 64) / 8) ^ (r & 7)) * 16));
-              v16[4 * c] = x.x;
-              v16[4 * c + 1] = x.y;
-              v16[4 * c + 2] = x.z;
-              v16[4 * c + 3] = x.w;
-            }
-            tmem_st16_nowait(tl + (which == 0 ? C::kColQ : C::kColdO) + half * (D / 4) + 16 * g,
-                             v16);
-          }
-        }
-        tmem_wait_st();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDqBarQTmem));
-      return good;
-    };
-    int u = read_unit(0);
-    if (u >= 0) ok = copy_q(0);
-    int gj = 0;
-    for (int ku = 0; u >= 0 && ok; ++ku) {
+    int gj = 0, ne = 0;
+    for (int ku = 0; ok; ++ku) {
+      const int u = read_unit(ku);
+      if (u < 0) break;
       const Unit t = unit_info(u);
       const int qrow = t.m0 + r;
       // (-LSE*log2e, -Delta) of this row; rows past T read (-inf, -0): P = 0.
       const float2 rstat =
           a.rowstats[(static_cast<size_t>(t.b) * a.Hq + t.h) * a.Tp + t.rbase + qrow];
+      const int wlast = t.m0 + quarter * 32 + 31 + t.off;  // last key any row of the warp sees
       for (int j = 0; j < t.n_kv; ++j, ++gj) {
         ok = warp_all(mbar_wait(bar(kDqBarS), gj & 1, wait_ns));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sv[32], dp[32];
-        tmem_ld32_nowait(tS, sv);
-        tmem_ld32_nowait(tDP, dp);
+        uint32_t sv[2][32], dp[2][32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32_nowait(tS + 32 * c, sv[c]);
+          tmem_ld32_nowait(tDP + 32 * c, dp[c]);
+        }
         tmem_wait_ld();
-        reg_fence32(sv);
-        reg_fence32(dp);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          reg_fence32(sv[c]);
+          reg_fence32(dp[c]);
+        }
         // S, dP are in registers: the next tile's may overwrite them.
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kDqBarSFree));
-        const int kv0 = j * kDqTileN + half * 32;  // key of this half's first column
+        const int kv0 = j * kDqTileN + 64 * half;  // key of this half's first column
         // key kv0 + c visible iff c <= lim
         const int lim = a.causal ? min(qrow + t.off - kv0, t.tk - 1 - kv0) : (t.tk - 1 - kv0);
-        uint32_t dsk[16];
-        // Masking is needed only where this warp's 32 rows meet the diagonal
-        // (or T), decided for the whole warp; other tiles run the loop
-        // without it.
-        const int row0 = t.m0 + quarter * 32 + t.off;  // last visible key of the warp's first row
-        const bool need_mask = (a.causal && kv0 + 31 > row0) || kv0 + 32 > t.tk;
+        // Masking only where the warp's rows meet the diagonal (or tk),
+        // decided for the whole warp; 32-key chunks past every row of the
+        // warp (or past tk) are all zeros.
+        const bool need_mask = (a.causal && kv0 + 63 > wlast - 31) || kv0 + 64 > t.tk;
+        const int last_key = a.causal ? min(wlast, t.tk - 1) : t.tk - 1;
+        const int live = last_key < kv0 ? 0 : min(2, (last_key - kv0) / 32 + 1);
+        uint32_t dsk[32];
         auto element_loop = [&](auto masked) {
           constexpr bool kMasked = decltype(masked)::value;
-          static_for<16>([&](auto ic) {
-            constexpr int c2 = decltype(ic)::value;
-            constexpr int c = 2 * c2;
-            const float x0 = fmaf(__uint_as_float(sv[c]), sl2, rstat.x);
-            const float x1 = fmaf(__uint_as_float(sv[c + 1]), sl2, rstat.x);
-            float p0, p1;
-            if constexpr ((c2 & 7) < kPolyOf8) {
-              p0 = exp2_poly(x0);
-              p1 = exp2_poly(x1);
-            } else {
-              p0 = ex2_approx(x0);
-              p1 = ex2_approx(x1);
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            if (kMasked && ch >= live) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) dsk[16 * ch + i] = 0u;
+              continue;
             }
-            if constexpr (kMasked) {
-              if (c > lim) p0 = 0.f;
-              if (c + 1 > lim) p1 = 0.f;
-            }
-            const float d0 = p0 * (__uint_as_float(dp[c]) + rstat.y);
-            const float d1 = p1 * (__uint_as_float(dp[c + 1]) + rstat.y);
-            dsk[c2] = pack_bf16x2(d0, d1);
-          });
+            static_for<16>([&](auto ic) {
+              constexpr int i = decltype(ic)::value;
+              constexpr int c = 2 * i;  // column within the chunk
+              const float x0 = fmaf(__uint_as_float(sv[ch][c]), sl2, rstat.x);
+              const float x1 = fmaf(__uint_as_float(sv[ch][c + 1]), sl2, rstat.x);
+              float p0, p1;
+              if constexpr ((i & 7) < kPolyOf8) {
+                p0 = exp2_poly(x0);
+                p1 = exp2_poly(x1);
+              } else {
+                p0 = ex2_approx(x0);
+                p1 = ex2_approx(x1);
+              }
+              if constexpr (kMasked) {
+                if (32 * ch + c > lim) p0 = 0.f;
+                if (32 * ch + c + 1 > lim) p1 = 0.f;
+              }
+              const float d0 = p0 * (__uint_as_float(dp[ch][c]) + rstat.y);
+              const float d1 = p1 * (__uint_as_float(dp[ch][c + 1]) + rstat.y);
+              dsk[16 * ch + i] = pack_bf16x2(d0, d1);
+            });
+          }
         };
         if (need_mask)
           element_loop(std::true_type{});
         else
           element_loop(std::false_type{});
-        // The previous tile's dQ MMAs must be done reading the dS tile.
+        // The previous tile's dQ MMAs must be done reading the dS columns.
         if (gj > 0 && !(ok = warp_all(mbar_wait(bar(kDqBarDSFree), (gj - 1) & 1, wait_ns)))) break;
-        // Row r, keys 32 half .. 32 half + 31: 16-byte chunks 4 half .. 4 half + 3
-        // of the 128-byte-swizzled row.
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          st_shared_u4(sDS + r * 128 + (((4 * half + i) ^ (r & 7)) * 16),
-                       make_uint4(dsk[4 * i], dsk[4 * i + 1], dsk[4 * i + 2], dsk[4 * i + 3]));
-        fence_proxy_async_smem();  // visible to the tensor core's reads
+        tmem_st32_nowait(tDS, dsk);
+        tmem_wait_st();
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kDqBarDS));
       }
       if (!ok) break;
-      const int u_next = read_unit(ku + 1);
-      if (!ok) break;
-      if (u_next >= 0 && !(ok = copy_q(ku + 1))) break;
-      ok = warp_all(mbar_wait(bar(kDqBarAcc), ku & 1, wait_ns));
-      if (!ok) break;
-      tc_fence_after();
-      const bool live = qrow < t.tq;
-      __nv_bfloat16* dqrow = static_cast<__nv_bfloat16*>(a.dq) +
-                             ((static_cast<size_t>(t.b) * a.T + t.qbase + qrow) * a.Hq + t.h) * D;
+      const bool live_row = qrow < t.tq;
       uint32_t pkd[D / 4];
+      if (t.n_kv > 0) {
+        ok = warp_all(mbar_wait(bar(kDqBarAcc), ne & 1, wait_ns));
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = half * (D / 64) + cc;  // this half's 32-column chunks of dQ
-        uint32_t v[32];
-        tmem_ld32(tl + C::kColDQ + c * 32, v);
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const int c = half * (D / 64) + cc;  // this half's 32-column chunks of dQ
+          uint32_t v[32];
+          tmem_ld32(tl + C::kColDQ + c * 32, v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pkd[16 * cc + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * a.scale,
-                                         __uint_as_float(v[2 * i + 1]) * a.scale);
-      }
-      if constexpr (VL) {
-        // No key tile: the accumulator still holds an earlier unit's sums.
-        if (t.n_kv == 0) {
-#pragma unroll
-          for (int i = 0; i < D / 4; ++i) pkd[i] = 0u;
+          for (int i = 0; i < 16; ++i)
+            pkd[16 * cc + i] = pack_bf16x2(__uint_as_float(v[2 * i]) * a.scale,
+                                           __uint_as_float(v[2 * i + 1]) * a.scale);
         }
+        // dQ is in registers: the next unit's first dQ MMA (issued after this
+        // warp's next dS arrival) may overwrite it.
+        tc_fence_before();
+        ++ne;
+      } else {
+        // A packed unit whose rows see no key: dQ = 0.
+#pragma unroll
+        for (int i = 0; i < D / 4; ++i) pkd[i] = 0u;
       }
-      // dQ is in registers: the next unit's first dQ MMA may overwrite it.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kDqBarAccFree));
-      if (live) {
-        uint4* dst = reinterpret_cast<uint4*>(dqrow + half * (D / 2));
+      if (live_row) {
+        uint4* dst = reinterpret_cast<uint4*>(
+            static_cast<__nv_bfloat16*>(a.dq) +
+            ((static_cast<size_t>(t.b) * a.T + t.qbase + qrow) * a.Hq + t.h) * D + half * (D / 2));
 #pragma unroll
         for (int i = 0; i < D / 16; ++i)
           dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
       }
-      u = u_next;
     }
   }
 
   if (!ok) atomicOr(&g_bwd_status, 4u);
   tc_fence_before();
   __syncthreads();
-  if (threadIdx.x < 32) {
+  if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem_slot, NP * C::kTmemCols);
+    tmem_dealloc(tmem_slot, C::kTmemCols);
   }
 }
 
@@ -1534,8 +1512,17 @@ cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
   static unsigned long long done[64] = {};
   cudaError_t e = set_smem_once(attn_dq_kernel<D, VT>, DqCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
-  attn_dq_kernel<D, VT><<<grid, kDqPipeThreads * DqCfg<D>::NP, DqCfg<D>::kSmemBytes, st>>>(
-      mq, mk, mv, mdo, a, sched, vt);
+  // The block's registers at launch must cover the warpgroups' shares after
+  // reallocation, or the element-wise warpgroups' increase never completes.
+  static int regs_ok[2] = {0, 0};
+  if (!regs_ok[D == 64 ? 0 : 1]) {
+    cudaFuncAttributes fa{};
+    if ((e = cudaFuncGetAttributes(&fa, attn_dq_kernel<D, VT>)) != cudaSuccess) return e;
+    if (fa.numRegs * kDqThreads < kDqRegBudget) return cudaErrorInvalidConfiguration;
+    regs_ok[D == 64 ? 0 : 1] = 1;
+  }
+  attn_dq_kernel<D, VT><<<grid, kDqThreads, DqCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a, sched,
+                                                                       vt);
   return cudaGetLastError();
 }
 

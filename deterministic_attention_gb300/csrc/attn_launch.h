@@ -10,7 +10,7 @@ namespace detattn {
 constexpr int kTileM = 128;     // query rows per forward / dQ tile
 constexpr int kTileN = 128;     // key rows per dK/dV tile
 constexpr int kFwdTileN = 128;  // key rows per forward KV tile
-constexpr int kDqTileN = 64;    // key rows per dQ-kernel KV tile
+constexpr int kDqTileN = 128;   // key rows per dQ-kernel KV tile
 // Query rows per dK/dV-kernel item (64: two items' S^T, dP^T fit TMEM at
 // D = 64 beside the accumulators and K, V).
 constexpr int dkdv_tile_m(int) { return 64; }
@@ -38,14 +38,11 @@ __host__ __device__ inline int qtile_snake_count(int i, int total, int n_pipes) 
   const int full = total / n_pipes, rem = total % n_pipes;
   return full + (((full & 1) ? n_pipes - 1 - i : i) < rem ? 1 : 0);
 }
-// Pipelines per forward / dQ block: two at D = 64 (256 TMEM columns each),
-// one at D = 128.
-constexpr int qtile_pipes_per_block(int D) { return D == 64 ? 2 : 1; }
-// Pipelines per forward block.
-#ifndef DETATTN_FWD_NP64
-#define DETATTN_FWD_NP64 2
-#endif
-constexpr int fwd_pipes_per_block(int D) { return D == 64 ? DETATTN_FWD_NP64 : 1; }
+// Pipelines per dQ block (one: S, dP, dS and dQ take most of TMEM).
+constexpr int dq_pipes_per_block(int) { return 1; }
+// Pipelines per forward block: two at D = 64 (256 TMEM columns each), one
+// at D = 128.
+constexpr int fwd_pipes_per_block(int D) { return D == 64 ? 2 : 1; }
 
 // Packed variable-length batches: sequence s holds query rows cu_q[s] ..
 // cu_q[s + 1] - 1 of the packed [total_q, Hq, D] tensors and key rows

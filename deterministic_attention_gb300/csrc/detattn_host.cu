@@ -460,7 +460,7 @@ int dq_impl(const void* q, const void* k, const void* v, const void* dout, const
   if ((rc = sm_count(&sms)) != DETATTN_OK) return rc;
   QTileSched sc;
   int g;
-  cached_qtile_schedule(qtile_pipes_per_block(D), B, T, Hq, causal, sms, &sc, &g);
+  cached_qtile_schedule(dq_pipes_per_block(D), B, T, Hq, causal, sms, &sc, &g);
   return launched(launch_dq(D, g, mq, mk, mv, mdo, a, sc, nullptr, st), "attn_bwd_dq");
 }
 
@@ -789,7 +789,7 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, 
     b.unit_counter = counter;
     QTileSched sc;
     int g;
-    qtile_schedule_w(qtile_pipes_per_block(D), pk.q_weight, Hq, sms, &sc, &g);
+    qtile_schedule_w(dq_pipes_per_block(D), pk.q_weight, Hq, sms, &sc, &g);
     if ((rc = launched(launch_dq(D, g, mq, mk, mv, mdo, b, sc, &pk.qt, st),
                        "attn_bwd_varlen (dQ)")) != DETATTN_OK)
       return rc;
@@ -1430,7 +1430,7 @@ int detattn_diag_qtile_deal(int D, int B, int T, int Hq, int causal, int sms, in
   if (empty) return 0;
   QTileSched sc;
   int grid = 0;
-  qtile_schedule(qtile_pipes_per_block(D), B, T, Hq, causal, sms, &sc, &grid);
+  qtile_schedule(dq_pipes_per_block(D), B, T, Hq, causal, sms, &sc, &grid);
   for (long u = 0; u < units; ++u) pipe_of_unit[u] = -1;
   for (int i = 0; i < sc.n_pipes; ++i) {
     if (sc.n_listed > 0) {

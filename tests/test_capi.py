@@ -112,19 +112,20 @@ def test_python_binding_refuses_cpu_tensors(L):
     (128, 3, 1000, 5, 1, 132),
 ])
 def test_qtile_deal(D, B, T, Hq, causal, sms):
-    """The static deal of 128-query tiles to pipelines (host logic, no GPU):
-    every unit goes to exactly one pipeline, and no pipeline's load exceeds
-    the mean by more than one unit; past the host list (1,024 units) the deal
-    is round k of the pipelines, forward in even rounds, backward in odd."""
+    """The dQ step's static deal of 128-query tiles to its blocks (one
+    pipeline each; host logic, no GPU): every unit goes to exactly one
+    pipeline, and no pipeline's load exceeds the mean by more than one unit;
+    past the host list (1,024 units) the deal is round k of the pipelines,
+    forward in even rounds, backward in odd.  A unit weighs its 128-key tiles
+    plus two."""
     n_pipes, pipe = da.diag_qtile_deal(D, B, T, Hq, causal, sms)
     n_m = -(-T // 128)
     units = B * Hq * n_m
-    per_block = 2 if D == 64 else 1
-    assert n_pipes == min(sms, units) * per_block
+    assert n_pipes == min(sms, units)
     assert pipe.shape == (units,) and (pipe >= 0).all() and (pipe < n_pipes).all()
-    kv = -(-T // 64)
+    kv = -(-T // 128)
     mt = n_m - 1 - np.arange(units) // (B * Hq)
-    n_kv = np.minimum(kv, (mt * 128 + 128) // 64) if causal else np.full(units, kv)
+    n_kv = np.minimum(kv, (mt * 128 + 128) // 128) if causal else np.full(units, kv)
     w = n_kv + 2.0
     load = np.bincount(pipe, weights=w, minlength=n_pipes)
     assert load.max() <= w.sum() / n_pipes + w.max()
@@ -253,7 +254,7 @@ def test_product_shares_nothing_with_the_oracle():
 # times the blocks it keeps per SM.
 _KERNEL_THREADS_PER_SM = {
     "attn_fwd_kernelILi64E": 384, "attn_fwd_kernelILi128E": 256,
-    "attn_dq_kernelILi64E": 640, "attn_dq_kernelILi128E": 320,
+    "attn_dq_kernelILi64E": 384, "attn_dq_kernelILi128E": 384,
     "attn_dkdv_kernelILi64E": 608, "attn_dkdv_kernelILi128E": 608,
     "attn_delta_kernelILi64E": 4 * 256, "attn_delta_kernelILi128E": 4 * 256,
 }
