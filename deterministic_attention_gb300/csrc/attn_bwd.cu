@@ -962,7 +962,14 @@ struct DqCfg {
   static constexpr int kOffQ = 0;  // slot i: Q at 2 i kQBytes, dO at (2 i + 1) kQBytes
   static constexpr int kOffK = 2 * kQSlots * kQBytes;
   static constexpr int kOffV = kOffK + kKStages * kKvBytes;
-  static constexpr int kSmemBytes = kOffV + kVStages * kKvBytes + 1024;  // + alignment slack
+  // The unit's 128 row statistics (-LSE log2e, -Delta), one KB per slot,
+  // loaded with its Q and dO.
+  static constexpr int kOffRs = kOffV + kVStages * kKvBytes;
+  // At D = 64, each element-wise warp's 32 rows x 32 columns of dQ are staged
+  // here (2 KB per warp) for one TMA store.
+  static constexpr bool kStageDq = (D == 64);
+  static constexpr int kOffStage = kOffRs + kQSlots * 1024;
+  static constexpr int kSmemBytes = kOffStage + (kStageDq ? 8 * 2048 : 0) + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0, kColDP = 128, kColDS = 256, kColDQ = 320;
   static_assert(kColDQ + D <= kTmemCols, "TMEM layout");
@@ -982,14 +989,15 @@ enum : int { kDqBarQFull = 0,                       // [2] Q, dO slot loaded
              kDqBarDrain = 21,
              kDqBarUnit = 22,     // [4] unit k published in ring slot k % 4
              kDqBarUnitFree = 26, // [4] ring slot k % 4 read by the MMA and element-wise warps (9)
-             kDqNumBars = 30 };
+             kDqBarRsRead = 30,   // [2] the element-wise warps hold the slot's row statistics (8)
+             kDqNumBars = 32 };
 
 template <int D, class VT>
 __global__ void __launch_bounds__(kDqThreads, 1)
     attn_dq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
-                   const BwdArgs a, const __grid_constant__ QTileSched sched,
-                   const __grid_constant__ VT vt) {
+                   const __grid_constant__ CUtensorMap mdQ, const BwdArgs a,
+                   const __grid_constant__ QTileSched sched, const __grid_constant__ VT vt) {
   using C = DqCfg<D>;
   constexpr bool VL = std::is_same<VT, VarlenTable>::value;
   constexpr int NK = C::kKStages, NV = C::kVStages;
@@ -1062,6 +1070,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t s0 = smem_u32(smem);
   const uint32_t sQ0 = s0 + C::kOffQ, sK0 = s0 + C::kOffK, sV0 = s0 + C::kOffV;
+  const uint32_t sRs = s0 + C::kOffRs, sStage = s0 + C::kOffStage;
   auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
   if (warp == 0) {
@@ -1073,6 +1082,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kDqBarQFull + i), 1);
       mbar_init(bar(kDqBarQFree + i), 1);
+      mbar_init(bar(kDqBarRsRead + i), 8);
     }
     for (int s = 0; s < kDqMaxStages; ++s) {
       mbar_init(bar(kDqBarKFull + s), 1);
@@ -1097,6 +1107,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     tma_prefetch_desc(&mK);
     tma_prefetch_desc(&mV);
     tma_prefetch_desc(&mdO);
+    tma_prefetch_desc(&mdQ);
   }
   __syncthreads();
   tc_fence_after();
@@ -1122,12 +1133,13 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     if (lane == 0) {
       int last_k[kDqMaxStages] = {-1, -1, -1}, last_v[kDqMaxStages] = {-1, -1, -1};
       int last_q[2] = {-1, -1};
-      int gj = 0;  // key tiles loaded so far, over all units
-      int ne = 0;  // units with key tiles so far
-      for (int ku = 0; ok; ++ku) {
-        // Ring slot ku % 4 must have been read for unit ku - 4.
+      int ku = 0;  // units published so far
+      // Takes the next unit (from the counter or the host's deal) and
+      // publishes it in ring slot ku % 4 once that slot has been read for
+      // unit ku - 4; -1 after the last.
+      auto take = [&]() -> int {
         if (ku >= 4 && !(ok = mbar_wait(bar(kDqBarUnitFree + (ku & 3)), ((ku >> 2) - 1) & 1, wait_ns)))
-          break;
+          return -1;
         int u;
         if (a.unit_counter != nullptr) {
           const unsigned v = atomicAdd(a.unit_counter, 1u);
@@ -1140,24 +1152,30 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         }
         unit_ring[ku & 3] = u;
         mbar_arrive(bar(kDqBarUnit + (ku & 3)));
-        if (u < 0) {
-          if (a.unit_counter != nullptr) {
-            // Count this block out (second word); the last one to finish
-            // taking units puts both words back to zero for the next launch.
-            __threadfence();
-            if (atomicAdd(a.unit_counter + 1, 1u) == gridDim.x - 1) {
-              atomicExch(a.unit_counter, 0u);
-              atomicExch(a.unit_counter + 1, 0u);
-            }
+        ++ku;
+        if (u < 0 && a.unit_counter != nullptr) {
+          // Count this block out (second word); the last one to finish
+          // taking units puts both words back to zero for the next launch.
+          __threadfence();
+          if (atomicAdd(a.unit_counter + 1, 1u) == gridDim.x - 1) {
+            atomicExch(a.unit_counter, 0u);
+            atomicExch(a.unit_counter + 1, 0u);
           }
-          break;
         }
-        const Unit t = unit_info(u);
-        if (t.n_kv == 0) continue;  // a packed unit whose rows see no key: nothing to load
+        return u;
+      };
+      // Q, dO and the row statistics of the ne-th unit with key tiles into
+      // slot ne % NQ, once the unit that last used the slot is done with it:
+      // its S, dP products have read Q and dO, and the element-wise warps
+      // hold its row statistics (they wait on the slot's barrier later than
+      // the MMA warp does; without this the barrier could complete twice
+      // before their wait).
+      auto issue_q = [&](const Unit& t, int ne) -> bool {
         const int slot = ne % NQ, use = ne / NQ;
-        // The unit that last used this slot must be done with it.
-        if (use > 0 && !(ok = mbar_wait(bar(kDqBarQFree + slot), (use - 1) & 1, wait_ns))) break;
-        mbar_arrive_expect_tx(bar(kDqBarQFull + slot), 2 * C::kQBytes);
+        if (use > 0 && !(mbar_wait(bar(kDqBarQFree + slot), (use - 1) & 1, wait_ns) &&
+                         mbar_wait(bar(kDqBarRsRead + slot), (use - 1) & 1, wait_ns)))
+          return false;
+        mbar_arrive_expect_tx(bar(kDqBarQFull + slot), 2 * C::kQBytes + 1024);
         const uint32_t sq = sQ0 + 2 * slot * C::kQBytes;
         for (int at = 0; at < C::kAtoms; ++at) {
           tma_load_4d(sq + at * (kTileM * 128), &mQ, bar(kDqBarQFull + slot), at * 64, t.h,
@@ -1165,7 +1183,25 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           tma_load_4d(sq + C::kQBytes + at * (kTileM * 128), &mdO, bar(kDqBarQFull + slot), at * 64,
                       t.h, t.qbase + t.m0, t.b);
         }
+        bulk_load(sRs + slot * 1024,
+                  a.rowstats + (static_cast<size_t>(t.b) * a.Hq + t.h) * a.Tp + t.rbase + t.m0, 1024,
+                  bar(kDqBarQFull + slot));
         last_q[slot] = ne;
+        return true;
+      };
+      int gj = 0;  // key tiles loaded so far, over all units
+      int ne = 0;  // units with key tiles so far
+      bool q_ahead = false;  // the current unit's Q was issued while the previous one loaded
+      int u_next = take();
+      while (ok && u_next >= 0) {
+        const int u = u_next;
+        const Unit t = unit_info(u);
+        if (t.n_kv == 0) {  // a packed unit whose rows see no key: nothing to load
+          u_next = take();
+          continue;
+        }
+        if (!q_ahead && !(ok = issue_q(t, ne))) break;
+        q_ahead = false;
         for (int j = 0; j < t.n_kv; ++j, ++gj) {
           const int sk = gj % NK, sv = gj % NV;
           if (gj >= NK && !(ok = mbar_wait(bar(kDqBarKEmpty + sk), ((gj / NK) & 1) ^ 1, wait_ns))) break;
@@ -1180,6 +1216,21 @@ __global__ void __launch_bounds__(kDqThreads, 1)
             tma_load_4d(sV0 + sv * C::kKvBytes + at * (kDqTileN * 128), &mV, bar(kDqBarVFull + sv),
                         at * 64, t.hkv, t.kbase + j * kDqTileN, t.b);
           last_v[sv] = gj;
+          if (j + 1 == t.n_kv) {
+            // The next unit, taken once this unit's loads are all issued (a
+            // block does not reserve work it cannot start soon: the counter
+            // keeps dealing the heaviest units to whichever block is free
+            // first); with two slots its Q, dO and row statistics load now.
+            u_next = take();
+            if (!ok) break;
+            if (NQ == 2 && u_next >= 0) {
+              const Unit tn = unit_info(u_next);
+              if (tn.n_kv > 0) {
+                if (!(ok = issue_q(tn, ne + 1))) break;
+                q_ahead = true;
+              }
+            }
+          }
         }
         ++ne;
       }
@@ -1300,9 +1351,17 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       if (u < 0) break;
       const Unit t = unit_info(u);
       const int qrow = t.m0 + r;
-      // (-LSE*log2e, -Delta) of this row; rows past T read (-inf, -0): P = 0.
-      const float2 rstat =
-          a.rowstats[(static_cast<size_t>(t.b) * a.Hq + t.h) * a.Tp + t.rbase + qrow];
+      // (-LSE*log2e, -Delta) of this row, loaded with the unit's Q and dO;
+      // rows past T hold (-inf, -0): P = 0.
+      float2 rstat = make_float2(0.f, 0.f);
+      if (t.n_kv > 0) {
+        const int slot = ne % NQ;
+        ok = warp_all(mbar_wait(bar(kDqBarQFull + slot), (ne / NQ) & 1, wait_ns));
+        if (!ok) break;
+        rstat = ld_shared_f2(sRs + slot * 1024 + r * 8);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kDqBarRsRead + slot));
+      }
       const int wlast = t.m0 + quarter * 32 + 31 + t.off;  // last key any row of the warp sees
       for (int j = 0; j < t.n_kv; ++j, ++gj) {
         ok = warp_all(mbar_wait(bar(kDqBarS), gj & 1, wait_ns));
@@ -1404,7 +1463,25 @@ __global__ void __launch_bounds__(kDqThreads, 1)
 #pragma unroll
         for (int i = 0; i < D / 4; ++i) pkd[i] = 0u;
       }
-      if (live_row) {
+      // At D = 64 the warp's 32 rows x 32 columns go out through one TMA
+      // store (rows past T are clipped by the map) unless they run past a
+      // packed sequence's end, where the rows beyond belong to the next one.
+      if (C::kStageDq && (!VL || t.m0 + quarter * 32 + 32 <= t.tq)) {
+        const uint32_t stage = sStage + (warp - 4) * 2048;
+        // The warp's previous store must have read the staging rows first.
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i)
+          st_shared_u4(stage + lane * (D / 2) * 2 + 16 * i,
+                       make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_4d(&mdQ, stage, half * (D / 2), t.h, t.qbase + t.m0 + quarter * 32, t.b);
+          bulk_commit_group();
+        }
+      } else if (live_row) {
         uint4* dst = reinterpret_cast<uint4*>(
             static_cast<__nv_bfloat16*>(a.dq) +
             ((static_cast<size_t>(t.b) * a.T + t.qbase + qrow) * a.Hq + t.h) * D + half * (D / 2));
@@ -1413,6 +1490,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
       }
     }
+    // Every store of dQ must be complete before the block (and its shared
+    // memory) goes away.
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 
   if (!ok) atomicOr(&g_bwd_status, 4u);
@@ -1507,8 +1588,8 @@ cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk
 
 template <int D, class VT>
 cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                        const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                        const QTileSched& sched, const VT& vt, cudaStream_t st) {
+                        const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
+                        const BwdArgs& a, const QTileSched& sched, const VT& vt, cudaStream_t st) {
   static unsigned long long done[64] = {};
   cudaError_t e = set_smem_once(attn_dq_kernel<D, VT>, DqCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
@@ -1521,8 +1602,8 @@ cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
     if (fa.numRegs * kDqThreads < kDqRegBudget) return cudaErrorInvalidConfiguration;
     regs_ok[D == 64 ? 0 : 1] = 1;
   }
-  attn_dq_kernel<D, VT><<<grid, kDqThreads, DqCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, a, sched,
-                                                                       vt);
+  attn_dq_kernel<D, VT><<<grid, kDqThreads, DqCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, mdq, a,
+                                                                       sched, vt);
   return cudaGetLastError();
 }
 
@@ -1588,14 +1669,15 @@ cudaError_t dkdv_max_clusters(int D, int c, int* out) {
 int dkdv_max_cluster_size(int D) { return D == 64 ? DkvCfg<64>::kMaxCluster : DkvCfg<128>::kMaxCluster; }
 
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                      const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                      const QTileSched& sched, const VarlenTable* vt, cudaStream_t st) {
+                      const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
+                      const BwdArgs& a, const QTileSched& sched, const VarlenTable* vt,
+                      cudaStream_t st) {
   if (vt != nullptr)
-    return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, a, sched, *vt, st)
-                   : launch_dq_t<128>(grid, mq, mk, mv, mdo, a, sched, *vt, st);
+    return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, mdq, a, sched, *vt, st)
+                   : launch_dq_t<128>(grid, mq, mk, mv, mdo, mdq, a, sched, *vt, st);
   const NoVarlen none{};
-  return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, a, sched, none, st)
-                 : launch_dq_t<128>(grid, mq, mk, mv, mdo, a, sched, none, st);
+  return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, mdq, a, sched, none, st)
+                 : launch_dq_t<128>(grid, mq, mk, mv, mdo, mdq, a, sched, none, st);
 }
 
 // Diagnostic: the kernels' 2^x forms on n inputs (polynomial scalar form,

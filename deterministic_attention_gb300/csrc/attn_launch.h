@@ -182,9 +182,13 @@ int dkdv_max_cluster_size(int D);
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                         bool dependent, const VarlenTable* vt, cudaStream_t st);
+// `mdq` covers dQ with boxes of 32 rows x D/2 columns, unswizzled: each
+// element-wise warp of the dQ step stores its rows of a tile (D = 64).
+constexpr int kDqStoreRows = 32;
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                      const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                      const QTileSched& sched, const VarlenTable* vt, cudaStream_t st);
+                      const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
+                      const BwdArgs& a, const QTileSched& sched, const VarlenTable* vt,
+                      cudaStream_t st);
 
 // Launches a one-thread kernel whose bounded wait on a never-completed
 // mbarrier runs out after limit_ns (sets the timeout bit, then returns).

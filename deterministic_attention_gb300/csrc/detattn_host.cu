@@ -133,6 +133,24 @@ int encode_rows(CUtensorMap* m, const void* ptr, int B, int T, int H, int D, int
   return DETATTN_OK;
 }
 
+// Tensor map over a [B, T, H, D] bf16 tensor for unswizzled stores of boxes
+// `inner` columns x `rows` rows (inner * 2 a multiple of 16 bytes).
+int encode_rows_store(CUtensorMap* m, const void* ptr, int B, int T, int H, int D, int inner,
+                      int rows, const char* what) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(H) * D * 2,
+                           static_cast<cuuint64_t>(T) * H * D * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(inner), 1, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(DETATTN_ERR_CUDA, "tensor map for %s: CUresult %d", what, (int)r);
+  return DETATTN_OK;
+}
+
 // Tensor map over the stored dS tiles: bf16 rows of 64 (one 128-byte
 // swizzle atom), boxes of 64 rows.
 int encode_2d_rows64(CUtensorMap* m, const void* ptr, long rows) {
@@ -445,12 +463,14 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
 int dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
             void* dq, int B, int T, int Hq, int Hkv, int D, float scale, int causal,
             unsigned* counter, cudaStream_t st) {
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   int rc;
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mdo, dout, B, T, Hq, D, kTileM, "dout")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kDqTileN, "k")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kDqTileN, "v")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows_store(&mdq, dq, B, T, Hq, D, D / 2, kDqStoreRows, "dq")) != DETATTN_OK)
+    return rc;
   BwdArgs a = bwd_args(workspace, T, Hq, Hkv, scale, causal);
   a.dq = dq;
   a.n_tiles = (T + kTileM - 1) / kTileM;
@@ -461,7 +481,7 @@ int dq_impl(const void* q, const void* k, const void* v, const void* dout, const
   QTileSched sc;
   int g;
   cached_qtile_schedule(dq_pipes_per_block(D), B, T, Hq, causal, sms, &sc, &g);
-  return launched(launch_dq(D, g, mq, mk, mv, mdo, a, sc, nullptr, st), "attn_bwd_dq");
+  return launched(launch_dq(D, g, mq, mk, mv, mdo, mdq, a, sc, nullptr, st), "attn_bwd_dq");
 }
 
 int check_workspace(const void* ws, size_t bytes, int B, int T, int Hq) {
@@ -778,11 +798,14 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, 
       return rc;
   }
   if (pk.qt.n_tiles > 0) {
-    CUtensorMap mq, mk, mv, mdo;
+    CUtensorMap mq, mk, mv, mdo, mdq;
     if ((rc = encode_rows(&mq, qq, 1, tq_rows, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
     if ((rc = encode_rows(&mdo, dd, 1, tq_rows, Hq, D, kTileM, "dout")) != DETATTN_OK) return rc;
     if ((rc = encode_rows(&mk, kk, 1, tk_rows, Hkv, D, kDqTileN, "k")) != DETATTN_OK) return rc;
     if ((rc = encode_rows(&mv, vv, 1, tk_rows, Hkv, D, kDqTileN, "v")) != DETATTN_OK) return rc;
+    if ((rc = encode_rows_store(&mdq, dq, 1, pk.total_q, Hq, D, D / 2, kDqStoreRows, "dq")) !=
+        DETATTN_OK)
+      return rc;
     BwdArgs b = a;
     b.dq = dq;
     b.BH = Hq;
@@ -790,7 +813,7 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, 
     QTileSched sc;
     int g;
     qtile_schedule_w(dq_pipes_per_block(D), pk.q_weight, Hq, sms, &sc, &g);
-    if ((rc = launched(launch_dq(D, g, mq, mk, mv, mdo, b, sc, &pk.qt, st),
+    if ((rc = launched(launch_dq(D, g, mq, mk, mv, mdo, mdq, b, sc, &pk.qt, st),
                        "attn_bwd_varlen (dQ)")) != DETATTN_OK)
       return rc;
   }
