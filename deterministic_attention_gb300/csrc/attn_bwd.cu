@@ -925,6 +925,567 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// ============================================================== dK / dV, D = 64
+// The same tile walk, cluster split and partial-sum exchange as above, with
+// items of 128 queries and fewer, fuller element-wise threads:
+//   warp 0      producer: each tile's K, V; each item's Q, dO and row
+//               statistics into a ring of stages
+//   warp 1      S^T = K Q^T and dP^T = V dO^T (both operands in shared
+//               memory, M = 128 keys, N = 128 queries) as soon as the
+//               element-wise warps hold the previous item's in registers
+//   warp 2      dV += P^T dO and dK += dS^T Q, P^T and dS^T read from TMEM
+//   warps 4..11 element-wise, two threads per key row (TMEM lane), one per
+//               64-query half of the item: P^T, dS^T as packed bf16 into TMEM
+//               columns of their own; at the tile's end D/2 columns each of
+//               dV and dK for the exchange and the store
+// TMEM: S^T [128 fp32 columns], dP^T [128], P^T [64 columns of bf16 pairs],
+// dS^T [64], dV [64], dK [64].
+constexpr int kDkw = 64;                   // head dimension of this kernel
+constexpr int kDkwTM = 128;                // queries per item
+constexpr int kDkwWarps = 12;
+constexpr int kDkwThreads = kDkwWarps * 32;
+constexpr uint32_t kDkwCtrlRegs = 104, kDkwElemRegs = 192;
+constexpr int kDkwRegBudget = 128 * kDkwCtrlRegs + 256 * kDkwElemRegs;
+struct DkwCfg {
+  static constexpr int kKvBytes = kTileN * 128;            // 128 keys x 64
+  static constexpr int kQBytes = kDkwTM * 128;             // 128 queries x 64
+  static constexpr int kStages = 3;
+  static constexpr int kStageBytes = 2 * kQBytes + 1024;   // Q, dO, then 128 row statistics
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kKvBytes;
+  static constexpr int kOffStage = 2 * kKvBytes;
+  static constexpr int kMaxCluster = 8;
+  static constexpr int kRowBytes = 2 * kDkw * 4;           // [dV | dK] fp32
+  static constexpr int kOffRecv = kOffStage + kStages * kStageBytes;
+  static constexpr int kRecvBytes = (kTileN - kTileN / kMaxCluster) * kRowBytes;
+  static constexpr int kSmemBytes = kOffRecv + kRecvBytes + 1024;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDS = 320, kColDV = 384,
+                            kColDK = 448;
+  static_assert(kSmemBytes + 512 <= 227 * 1024, "shared memory per block (with the static part)");
+  static_assert(kStageBytes % 1024 == 0, "stages keep the swizzle alignment");
+};
+
+template <class VT, int MODE>
+__global__ void __launch_bounds__(kDkwThreads, 1)
+    attn_dkdv64_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                       const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
+                       const BwdArgs a, const __grid_constant__ VT vt) {
+  using Cf = DkwCfg;
+  constexpr int D = kDkw;
+  constexpr bool VL = std::is_same<VT, VarlenTable>::value;
+  static_assert(!VL || MODE == 0, "the packed form walks its own table");
+  constexpr int NS = Cf::kStages;
+  constexpr int TM = kDkwTM;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t bars[kDkvNumBars];
+  __shared__ uint32_t tmem_slot;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = a.cluster;
+  const int crank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int group = static_cast<int>(blockIdx.x) / C;
+  const int NG = a.n_groups;
+  const int n_tiles_all = (VL ? vt_tiles(vt) : a.n_tiles) * a.BH;
+  const int G = a.Hq / a.Hkv;
+  const int m_end = (a.T + TM - 1) / TM;
+  const int R = kTileN / C;
+  // Tile of this cluster's kt-th turn, or -1 past its last.
+  auto tile_of = [&](int kt) {
+    const int t = kt * NG + ((kt & 1) ? NG - 1 - group : group);
+    return t < n_tiles_all ? t : -1;
+  };
+  auto tile_info = [&](int t) {
+    DkvTile ti;
+    if constexpr (VL) {
+      const uint32_t e = vt_tile(vt, t / a.BH);
+      const int s = static_cast<int>(e >> 16);
+      ti.b = 0;
+      ti.g = t % a.BH;
+      ti.n0 = static_cast<int>(e & 0xFFFFu) * kTileN;
+      ti.qbase = vt_cu_q(vt, s);
+      const int tq = vt_cu_q(vt, s + 1) - ti.qbase;
+      ti.kbase = vt_cu_k(vt, s);
+      ti.tk = vt_cu_k(vt, s + 1) - ti.kbase;
+      ti.rbase = vt_ps(vt, s);
+      ti.off = ti.tk - tq;
+      // Query tiles whose last row sees the tile's first key.
+      const int first_q = ti.n0 - ti.off;  // first query that sees key n0
+      const int mq_end = (tq + TM - 1) / TM;
+      ti.m_begin = a.causal ? min(mq_end, max(0, first_q) / TM) : 0;
+      ti.per_head = mq_end - ti.m_begin;
+    } else {
+      int nt, bg;
+      if constexpr ((MODE & kDkvChunked) != 0) {
+        dkdv_tile_coords(t, a.n_tiles, a.BH, a.bg_chunk, &nt, &bg);
+      } else {
+        nt = t / a.BH;
+        bg = t % a.BH;
+      }
+      ti.b = bg / a.Hkv;
+      ti.g = bg % a.Hkv;
+      ti.n0 = nt * kTileN;
+      ti.m_begin = a.causal ? ti.n0 / TM : 0;
+      ti.per_head = m_end - ti.m_begin;
+      ti.qbase = ti.kbase = ti.rbase = 0;
+      ti.tk = a.T;
+      ti.off = 0;
+    }
+    const int n_all = G * ti.per_head;
+    ti.it_lo = static_cast<int>(static_cast<long>(crank) * n_all / C);
+    ti.n_it = static_cast<int>(static_cast<long>(crank + 1) * n_all / C) - ti.it_lo;
+    return ti;
+  };
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t s0 = smem_u32(smem);
+  const uint32_t sK = s0 + Cf::kOffK, sV = s0 + Cf::kOffV;
+  auto stage_base = [&](int s) { return s0 + Cf::kOffStage + s * Cf::kStageBytes; };
+  auto bar = [&](int i) { return smem_u32(&bars[i]); };
+  // Byte offset of 16-byte chunk `chunk` of row `row` of a receive slot
+  // ([dV | dK] fp32 per row, chunks XOR-swizzled by row % 8).
+  auto slot_off = [](int row, int chunk) {
+    return static_cast<uint32_t>(row * Cf::kRowBytes + ((chunk ^ (row & 7)) * 16));
+  };
+  const uint32_t recv_bytes = static_cast<uint32_t>((C - 1) * R * Cf::kRowBytes);
+
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kDkvBarKV), 1);
+    mbar_init(bar(kDkvBarKVFree), 1);
+    for (int s = 0; s < kDkvMaxStages; ++s) {
+      mbar_init(bar(kDkvBarQFull + s), 1);
+      mbar_init(bar(kDkvBarQEmpty + s), 1);
+    }
+    mbar_init(bar(kDkvBarS), 1);
+    mbar_init(bar(kDkvBarSFree), 8);
+    mbar_init(bar(kDkvBarP), 8);
+    mbar_init(bar(kDkvBarFree), 1);
+    mbar_init(bar(kDkvBarAcc), 1);
+    mbar_init(bar(kDkvBarAccFree), 8);
+    mbar_init(bar(kDkvBarDrain), 1);
+    mbar_init(bar(kDkvBarDrainAcc), 1);
+    mbar_init(bar(kDkvBarRecv), 1);
+    mbar_init(bar(kDkvBarRegionFree), 8 * (C > 1 ? C - 1 : 1));
+    // The first tile's partial sums may arrive any time from now on.
+    if (C > 1) mbar_arrive_expect_tx(bar(kDkvBarRecv), recv_bytes);
+    fence_barrier_init();
+  }
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&mQ);
+    tma_prefetch_desc(&mK);
+    tma_prefetch_desc(&mV);
+    tma_prefetch_desc(&mdO);
+  }
+  __syncthreads();
+  // Peers' remote stores and arrivals target this block's mbarriers: they must
+  // be initialised first.
+  if (C > 1) cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint64_t wait_ns = a.wait_ns;
+  bool ok = true;
+
+  if (warp < 4) {
+  // Each warpgroup changes its register count at the top of its own branch,
+  // so the code after it is compiled for the new count.
+  setmaxnreg_dec<kDkwCtrlRegs>();
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int last[kDkvMaxStages];
+      for (int s = 0; s < kDkvMaxStages; ++s) last[s] = -1;
+      int last_kv = -1;
+      int gi = 0;  // items loaded so far, over all tiles
+      bool waited = false;  // for the Delta step's row statistics (dependent launch)
+      for (int kt = 0; ok; ++kt) {
+        const int t = tile_of(kt);
+        if (t < 0) break;
+        const DkvTile ti = tile_info(t);
+        // The previous tile's S^T, dP^T MMAs must be done with K, V.
+        if (kt > 0 && !(ok = mbar_wait(bar(kDkvBarKVFree), (kt - 1) & 1, wait_ns))) break;
+        mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * Cf::kKvBytes);
+        tma_load_4d(sK, &mK, bar(kDkvBarKV), 0, ti.g, ti.kbase + ti.n0, ti.b);
+        tma_load_4d(sV, &mV, bar(kDkvBarKV), 0, ti.g, ti.kbase + ti.n0, ti.b);
+        last_kv = kt;
+        int h = ti.g * G + (ti.n_it > 0 ? ti.it_lo / ti.per_head : 0);
+        int m_idx = ti.n_it > 0 ? ti.it_lo % ti.per_head : 0;
+        for (int li = 0; li < ti.n_it; ++li, ++gi) {
+          const int s = gi % NS;
+          const uint32_t ph = (gi / NS) & 1;
+          const int i0 = (ti.m_begin + m_idx) * TM;
+          if (gi >= NS && !(ok = mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns))) break;
+          const uint32_t st = stage_base(s);
+          mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + TM * 8);
+          tma_load_4d(st, &mQ, bar(kDkvBarQFull + s), 0, h, ti.qbase + i0, ti.b);
+          tma_load_4d(st + Cf::kQBytes, &mdO, bar(kDkvBarQFull + s), 0, h, ti.qbase + i0, ti.b);
+          if (!waited) {
+            // Launched as a dependent of the Delta step: only the row
+            // statistics are its output, so everything up to here (setup,
+            // K, V, Q, dO loads) overlaps it.
+            griddep_wait();
+            waited = true;
+          }
+          bulk_load(st + 2 * Cf::kQBytes,
+                    a.rowstats + (static_cast<size_t>(ti.b) * a.Hq + h) * a.Tp + ti.rbase + i0,
+                    TM * 8, bar(kDkvBarQFull + s));
+          last[s] = gi;
+          if (++m_idx == ti.per_head) {
+            m_idx = 0;
+            ++h;
+          }
+        }
+      }
+      if (!ok) {
+        // Copies still in flight must land before the block may exit.
+        if (last_kv >= 0) mbar_wait(bar(kDkvBarKV), last_kv & 1, wait_ns);
+        for (int s = 0; s < NS; ++s)
+          if (last[s] >= 0) mbar_wait(bar(kDkvBarQFull + s), (last[s] / NS) & 1, wait_ns);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ S^T / dP^T issuer
+    // The whole warp runs this loop (MMA issue is warp-collective); every
+    // wait is made warp-uniform so the warp stays converged.
+    constexpr uint32_t kIdS = idesc_bf16(kTileN, TM, false, false);
+    const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
+    const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);  // K-major B
+    const uint32_t tS = tmem + Cf::kColS, tDP = tmem + Cf::kColDP;
+    int gi = 0;
+    for (int kt = 0; ok; ++kt) {
+      const int t = tile_of(kt);
+      if (t < 0) break;
+      const DkvTile ti = tile_info(t);
+      if (!(ok = warp_all(mbar_wait(bar(kDkvBarKV), kt & 1, wait_ns)))) break;
+      tc_fence_after();
+      for (int li = 0; li < ti.n_it; ++li, ++gi) {
+        const int s = gi % NS;
+        // The element-wise warps must hold the previous item's S^T, dP^T in
+        // registers before this item's overwrite them.
+        if (gi > 0 && !(ok = warp_all(mbar_wait(bar(kDkvBarSFree), (gi - 1) & 1, wait_ns)))) break;
+        if (!(ok = warp_all(mbar_wait(bar(kDkvBarQFull + s), (gi / NS) & 1, wait_ns)))) break;
+        tc_fence_after();
+        const uint64_t q = desc_add(dQk0, s * Cf::kStageBytes), o = desc_add(q, Cf::kQBytes);
+        mma_ss_x4(tS, dK, desc_add(dK, 32), desc_add(dK, 64), desc_add(dK, 96), q, desc_add(q, 32),
+                  desc_add(q, 64), desc_add(q, 96), kIdS, 0u);
+        mma_ss_x4(tDP, dV, desc_add(dV, 32), desc_add(dV, 64), desc_add(dV, 96), o, desc_add(o, 32),
+                  desc_add(o, 64), desc_add(o, 96), kIdS, 0u);
+        mma_commit(bar(kDkvBarS));
+      }
+      if (!ok) break;
+      // K, V of this tile are free once these MMAs complete.
+      mma_commit(bar(kDkvBarKVFree));
+    }
+    // Every issued MMA must finish before TMEM is released.
+    mma_commit(bar(kDkvBarDrain));
+    warp_all(mbar_wait(bar(kDkvBarDrain), 0, wait_ns));
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ dV / dK issuer
+    constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
+    const uint32_t tDV = tmem + Cf::kColDV, tDK = tmem + Cf::kColDK;
+    const uint32_t tP = tmem + Cf::kColP, tDS = tmem + Cf::kColDS;
+    // Q, dO as MN-major B operands: 16 queries per 2048-byte step.
+    const uint64_t dQm0 = sdesc_sw128(stage_base(0), TM * 128, 1024);
+    int gi = 0;
+    for (int kt = 0; ok; ++kt) {
+      const int t = tile_of(kt);
+      if (t < 0) break;
+      const DkvTile ti = tile_info(t);
+      // The element-wise warps must have read the previous tile's sums before
+      // this tile's first MMA overwrites them -- and before this tile's
+      // completion is signalled at all: a tile without items here signals at
+      // once, and two completions ahead of the readers would alias the
+      // parity they wait on.
+      if (kt > 0 && !(ok = warp_all(mbar_wait(bar(kDkvBarAccFree), (kt - 1) & 1, wait_ns)))) break;
+      for (int li = 0; li < ti.n_it; ++li, ++gi) {
+        const int s = gi % NS;
+        if (!(ok = warp_all(mbar_wait(bar(kDkvBarP), gi & 1, wait_ns)))) break;
+        tc_fence_after();
+        const uint64_t qm = desc_add(dQm0, s * Cf::kStageBytes), om = desc_add(qm, Cf::kQBytes);
+        // P^T / dS^T of queries 16k..16k+15: 8 packed columns at 8k.
+#pragma unroll
+        for (int q4 = 0; q4 < TM / 64; ++q4) {
+          const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
+          const uint32_t p = tP + q4 * 32;
+          const uint64_t b = desc_add(om, q4 * 8192);
+          mma_ts_x4(tDV, p, p + 8, p + 16, p + 24, b, desc_add(b, 2048), desc_add(b, 4096),
+                    desc_add(b, 6144), kIdAcc, acc);
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < TM / 64; ++q4) {
+          const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
+          const uint32_t p = tDS + q4 * 32;
+          const uint64_t b = desc_add(qm, q4 * 8192);
+          mma_ts_x4(tDK, p, p + 8, p + 16, p + 24, b, desc_add(b, 2048), desc_add(b, 4096),
+                    desc_add(b, 6144), kIdAcc, acc);
+        }
+        // Both MMA streams of item gi have read stage s (the S^T stream
+        // finished before the element-wise warps released P): free it, and the
+        // P^T / dS^T columns.
+        mma_commit(bar(kDkvBarQEmpty + s));
+        mma_commit(bar(kDkvBarFree));
+      }
+      if (!ok) break;
+      mma_commit(bar(kDkvBarAcc));  // this tile's sums (at once when it has no items)
+    }
+    mma_commit(bar(kDkvBarDrainAcc));
+    warp_all(mbar_wait(bar(kDkvBarDrainAcc), 0, wait_ns));
+  }
+  } else {
+    setmaxnreg_inc<kDkwElemRegs>();
+    // ------------------------------------------------------------ P^T / dS^T warps
+    // Warps w and w + 4 share TMEM lane quarter (w & 3), i.e. the same 32 key
+    // rows; group grp = (w - 4) / 4 takes queries 64 grp .. 64 grp + 63 of
+    // each item, and columns 32 grp .. of dV, dK in the tile epilogue.
+    const int quarter = warp & 3;
+    const int grp = (warp - 4) >> 2;
+    const int r = quarter * 32 + lane;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const float sl2 = a.scale_log2;
+    const int owner = r / R;  // block of the cluster that stores key row r
+    int gi = 0;
+    for (int kt = 0; ok; ++kt) {
+      const int t = tile_of(kt);
+      if (t < 0) break;
+      const DkvTile ti = tile_info(t);
+      const int krow = ti.n0 + r;
+      int m_idx = ti.n_it > 0 ? ti.it_lo % ti.per_head : 0;  // query tile of the item in its head
+      for (int li = 0; li < ti.n_it && ok; ++li, ++gi) {
+        const int s = gi % NS;
+        const int i0 = (ti.m_begin + m_idx) * TM + grp * 64;  // this group's first query
+        if (++m_idx == ti.per_head) m_idx = 0;
+        ok = warp_all(mbar_wait(bar(kDkvBarS), gi & 1, wait_ns));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sv[2][32], dp[2][32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld32_nowait(tl + Cf::kColS + grp * 64 + 32 * c, sv[c]);
+          tmem_ld32_nowait(tl + Cf::kColDP + grp * 64 + 32 * c, dp[c]);
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          reg_fence32(sv[c]);
+          reg_fence32(dp[c]);
+        }
+        // S^T, dP^T are in registers: the next item's may overwrite them.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kDkvBarSFree));
+        // Causal: query i0 + c sees key krow iff c >= krow - off - i0.  The
+        // warp's rows span 32 keys: columns below the smallest row's bound
+        // need no mask, chunks of 32 columns below the largest row's bound
+        // are all zero.
+        const int cmin = a.causal ? (krow - ti.off - i0) : -1;
+        const int wmin = ti.n0 + quarter * 32 - ti.off - i0;  // smallest row's bound
+        const bool warp_masked = a.causal && wmin + 31 > 0;
+        // (-lse2, -delta) of this group's queries, two per float4.
+        const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * 64 * 8;
+        // The previous item's dV, dK MMAs must be done with the P^T, dS^T
+        // columns before this item's go there.
+        bool freed = gi == 0;
+        auto chunk = [&](auto ch_c, auto masked) -> bool {
+          constexpr int ch = decltype(ch_c)::value;
+          constexpr bool kMasked = decltype(masked)::value;
+          uint32_t pk[16], dk[16];
+          if (kMasked && a.causal && 32 * ch + 31 < wmin) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[i] = dk[i] = 0u;
+          } else {
+            static_for<16>([&](auto ic) {
+              constexpr int c2 = decltype(ic)::value;
+              constexpr int c = 2 * c2;
+              // (-lse2_c, -delta_c, -lse2_c+1, -delta_c+1), the same for the whole warp
+              const float4 rs = ld_shared_f4_at<(32 * ch + c) * 8>(st4);
+              const float x0 = fmaf(__uint_as_float(sv[ch][c]), sl2, rs.x);
+              const float x1 = fmaf(__uint_as_float(sv[ch][c + 1]), sl2, rs.z);
+              float p0, p1;
+              if constexpr ((c2 & 7) < kPolyOf8) {
+                p0 = exp2_poly(x0);
+                p1 = exp2_poly(x1);
+              } else {
+                p0 = ex2_approx(x0);
+                p1 = ex2_approx(x1);
+              }
+              if constexpr (kMasked) {
+                if (32 * ch + c < cmin) p0 = 0.f;
+                if (32 * ch + c + 1 < cmin) p1 = 0.f;
+              }
+              const float d0 = p0 * (__uint_as_float(dp[ch][c]) + rs.y);
+              const float d1 = p1 * (__uint_as_float(dp[ch][c + 1]) + rs.w);
+              pk[c2] = pack_bf16x2(p0, p1);
+              dk[c2] = pack_bf16x2(d0, d1);
+            });
+          }
+          if constexpr ((MODE & kDkvStoreDs) != 0) {
+            // Stored-dS backward: this item's dS^T rows also go to the
+            // workspace, for the dQ step to read instead of recomputing them
+            // (row = 64 queries of one half of the 128-query tile).
+            const int it = ti.it_lo + li;
+            const int h = ti.g * G + it / ti.per_head;
+            const int mt = ti.m_begin + it % ti.per_head, kt2 = ti.n0 / kTileN;
+            const long pr = a.causal ? static_cast<long>(mt) * (mt + 1) / 2 + kt2
+                                     : static_cast<long>(mt) * a.n_tiles + kt2;
+            const size_t row =
+                (((static_cast<size_t>(ti.b) * a.Hq + h) * a.ds_pairs + pr) * 2 + grp) * kTileN + r;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.ds) + row * 64 + 32 * ch);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(dk[4 * i], dk[4 * i + 1], dk[4 * i + 2], dk[4 * i + 3]);
+          }
+          if (!freed) {
+            if (!warp_all(mbar_wait(bar(kDkvBarFree), (gi - 1) & 1, wait_ns))) return false;
+            tc_fence_after();
+            freed = true;
+          }
+          tmem_st16_nowait(tl + Cf::kColP + grp * 32 + 16 * ch, pk);
+          tmem_st16_nowait(tl + Cf::kColDS + grp * 32 + 16 * ch, dk);
+          return true;
+        };
+        if (warp_masked)
+          ok = chunk(std::integral_constant<int, 0>{}, std::true_type{}) &&
+               chunk(std::integral_constant<int, 1>{}, std::true_type{});
+        else
+          ok = chunk(std::integral_constant<int, 0>{}, std::false_type{}) &&
+               chunk(std::integral_constant<int, 1>{}, std::false_type{});
+        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kDkvBarP));
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- tile epilogue
+      // This thread's share of key row r: D/2 columns of dV and of dK (zero
+      // for a block without items in the tile).
+      ok = warp_all(mbar_wait(bar(kDkvBarAcc), kt & 1, wait_ns));
+      if (!ok) break;
+      uint32_t part_v[D / 2], part_k[D / 2];
+      if (ti.n_it > 0) {
+        tc_fence_after();
+        tmem_ld32_nowait(tl + Cf::kColDV + grp * (D / 2), part_v);
+        tmem_ld32_nowait(tl + Cf::kColDK + grp * (D / 2), part_k);
+        tmem_wait_ld();
+        reg_fence32(part_v);
+        reg_fence32(part_k);
+      } else {
+#pragma unroll
+        for (int i = 0; i < D / 2; ++i) part_v[i] = part_k[i] = 0u;
+      }
+      // The next tile's first dV, dK MMA may overwrite the accumulators.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kDkvBarAccFree));
+
+      if (C > 1) {
+        // Rows another block owns: to its receive region, once it has read
+        // the previous tile's.
+        if (kt > 0) {
+          ok = warp_all(mbar_wait(bar(kDkvBarRegionFree), (kt - 1) & 1, wait_ns));
+          if (!ok) break;
+        }
+        if (owner != crank) {
+          const int j = crank < owner ? crank : crank - 1;
+          const int row = j * R + (r - owner * R);
+          const uint32_t dst = map_shared_rank(s0 + Cf::kOffRecv, static_cast<uint32_t>(owner));
+          const uint32_t rbar = map_shared_rank(bar(kDkvBarRecv), static_cast<uint32_t>(owner));
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t* v = which == 0 ? part_v : part_k;
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+              const int chunk16 = (which * D + grp * (D / 2)) / 4 + i;
+              st_async_f4(dst + slot_off(row, chunk16),
+                          make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])),
+                          rbar);
+            }
+          }
+        }
+        // Own rows: this block's sums, then the peers' in rank order.
+        ok = warp_all(mbar_wait(bar(kDkvBarRecv), kt & 1, wait_ns));
+        if (!ok) break;
+        // Arm the receive mbarrier for the next tile's sums.  Peers send them
+        // only after every warp here has signalled (below, after this arm in
+        // program order), and until then the barrier cannot move past the
+        // phase the other warps are still checking.
+        if (warp == 4 && lane == 0 && tile_of(kt + 1) >= 0)
+          mbar_arrive_expect_tx(bar(kDkvBarRecv), recv_bytes);
+        if (owner == crank) {
+          const int rl = r - crank * R;
+          for (int src = 0; src < C; ++src) {
+            if (src == crank) continue;
+            const int j = src < crank ? src : src - 1;
+            const uint32_t slot = s0 + Cf::kOffRecv;
+            const int row = j * R + rl;
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+              const float4 x = ld_shared_f4(slot + slot_off(row, (grp * (D / 2)) / 4 + i));
+              const float4 y = ld_shared_f4(slot + slot_off(row, (D + grp * (D / 2)) / 4 + i));
+              part_v[4 * i] = __float_as_uint(__uint_as_float(part_v[4 * i]) + x.x);
+              part_v[4 * i + 1] = __float_as_uint(__uint_as_float(part_v[4 * i + 1]) + x.y);
+              part_v[4 * i + 2] = __float_as_uint(__uint_as_float(part_v[4 * i + 2]) + x.z);
+              part_v[4 * i + 3] = __float_as_uint(__uint_as_float(part_v[4 * i + 3]) + x.w);
+              part_k[4 * i] = __float_as_uint(__uint_as_float(part_k[4 * i]) + y.x);
+              part_k[4 * i + 1] = __float_as_uint(__uint_as_float(part_k[4 * i + 1]) + y.y);
+              part_k[4 * i + 2] = __float_as_uint(__uint_as_float(part_k[4 * i + 2]) + y.z);
+              part_k[4 * i + 3] = __float_as_uint(__uint_as_float(part_k[4 * i + 3]) + y.w);
+            }
+          }
+        }
+        // This block's receive region is read: the peers may send the next
+        // tile's sums.
+        __syncwarp();
+        if (lane == 0) {
+          for (int p = 0; p < C; ++p)
+            if (p != crank)
+              mbar_arrive_remote(map_shared_rank(bar(kDkvBarRegionFree), static_cast<uint32_t>(p)));
+        }
+      }
+      if (owner == crank && krow < ti.tk) {
+        const size_t rbase =
+            ((static_cast<size_t>(ti.b) * a.Tk + ti.kbase + krow) * a.Hkv + ti.g) * D + grp * (D / 2);
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t* v = which == 0 ? part_v : part_k;
+          const float mul = which == 0 ? 1.f : a.scale;
+          uint4* dst = reinterpret_cast<uint4*>(
+              static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + rbase);
+          auto f = [&](int i) { return __uint_as_float(v[i]) * mul; };
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i)
+            dst[i] = make_uint4(pack_bf16x2(f(8 * i), f(8 * i + 1)), pack_bf16x2(f(8 * i + 2), f(8 * i + 3)),
+                                pack_bf16x2(f(8 * i + 4), f(8 * i + 5)),
+                                pack_bf16x2(f(8 * i + 6), f(8 * i + 7)));
+        }
+      }
+    }
+  }
+
+  // No block may exit while a peer can still store into its shared memory or
+  // arrive on its mbarriers: every block reaches this barrier (no early exit;
+  // all waits above are bounded).
+  if (C > 1) {
+    __syncwarp();
+    cluster_sync();
+  }
+
+  if (!ok) atomicOr(&g_bwd_status, 2u);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ============================================================== dQ
 // Work unit: one 128-query tile of one (b, query head), over 128-key tiles
 // 0..diagonal in ascending order.  Persistent, one pipeline per SM, working
@@ -1553,6 +2114,66 @@ cudaError_t dkdv_max_clusters_t(int c, int* out) {
   return cudaOccupancyMaxActiveClusters(out, attn_dkdv_kernel<D, NoVarlen, 0>, &cfg);
 }
 
+cudaError_t dkdv64_max_clusters(int c, int* out) {
+  static unsigned long long done[64] = {};
+  cudaError_t e = set_smem_once(attn_dkdv64_kernel<NoVarlen, 0>, DkwCfg::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(c));
+  cfg.blockDim = dim3(kDkwThreads);
+  cfg.dynamicSmemBytes = DkwCfg::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(c);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(out, attn_dkdv64_kernel<NoVarlen, 0>, &cfg);
+}
+
+template <class VT, int MODE>
+cudaError_t launch_dkdv64_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
+                            bool dependent, const VT& vt, cudaStream_t st) {
+  static unsigned long long done[64] = {};
+  cudaError_t e = set_smem_once(attn_dkdv64_kernel<VT, MODE>, DkwCfg::kSmemBytes, done);
+  if (e != cudaSuccess) return e;
+  // The block's registers at launch must cover the warpgroups' shares after
+  // reallocation, or the element-wise warpgroups' increase never completes.
+  static int regs_ok = 0;
+  if (!regs_ok) {
+    cudaFuncAttributes fa{};
+    if ((e = cudaFuncGetAttributes(&fa, attn_dkdv64_kernel<VT, MODE>)) != cudaSuccess) return e;
+    if (fa.numRegs * kDkwThreads < kDkwRegBudget) return cudaErrorInvalidConfiguration;
+    regs_ok = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kDkwThreads);
+  cfg.dynamicSmemBytes = DkwCfg::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (a.cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(a.cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (dependent) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  e = cudaLaunchKernelEx(&cfg, attn_dkdv64_kernel<VT, MODE>, mq, mk, mv, mdo, a, vt);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int D, class VT, int MODE>
 cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
@@ -1642,31 +2263,30 @@ cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMa
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                         bool dependent, const VarlenTable* vt, cudaStream_t st) {
   if (vt != nullptr)
-    return D == 64 ? launch_dkdv_t<64, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st)
+    return D == 64 ? launch_dkdv64_t<VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st)
                    : launch_dkdv_t<128, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
   const NoVarlen none{};
   const int mode = (a.bg_chunk > 0 ? kDkvChunked : 0) | (a.ds != nullptr ? kDkvStoreDs : 0);
-  auto go = [&](auto d, auto m) {
-    return launch_dkdv_t<decltype(d)::value, NoVarlen, decltype(m)::value>(grid, mq, mk, mv, mdo, a,
-                                                                           dependent, none, st);
+  auto go = [&](auto m) {
+    constexpr int M = decltype(m)::value;
+    return D == 64 ? launch_dkdv64_t<NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st)
+                   : launch_dkdv_t<128, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st);
   };
-  using I64 = std::integral_constant<int, 64>;
-  using I128 = std::integral_constant<int, 128>;
   switch (mode) {
-    case 0: return D == 64 ? go(I64{}, std::integral_constant<int, 0>{}) : go(I128{}, std::integral_constant<int, 0>{});
-    case 1: return D == 64 ? go(I64{}, std::integral_constant<int, 1>{}) : go(I128{}, std::integral_constant<int, 1>{});
-    case 2: return D == 64 ? go(I64{}, std::integral_constant<int, 2>{}) : go(I128{}, std::integral_constant<int, 2>{});
-    default: return D == 64 ? go(I64{}, std::integral_constant<int, 3>{}) : go(I128{}, std::integral_constant<int, 3>{});
+    case 0: return go(std::integral_constant<int, 0>{});
+    case 1: return go(std::integral_constant<int, 1>{});
+    case 2: return go(std::integral_constant<int, 2>{});
+    default: return go(std::integral_constant<int, 3>{});
   }
 }
 
 cudaError_t dkdv_max_clusters(int D, int c, int* out) {
   *out = 0;
-  if (D == 64) return dkdv_max_clusters_t<64>(c, out);
+  if (D == 64) return dkdv64_max_clusters(c, out);
   if (D == 128) return dkdv_max_clusters_t<128>(c, out);
   return cudaErrorInvalidValue;
 }
-int dkdv_max_cluster_size(int D) { return D == 64 ? DkvCfg<64>::kMaxCluster : DkvCfg<128>::kMaxCluster; }
+int dkdv_max_cluster_size(int D) { return D == 64 ? DkwCfg::kMaxCluster : DkvCfg<128>::kMaxCluster; }
 
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,

@@ -11,9 +11,10 @@ constexpr int kTileM = 128;     // query rows per forward / dQ tile
 constexpr int kTileN = 128;     // key rows per dK/dV tile
 constexpr int kFwdTileN = 128;  // key rows per forward KV tile
 constexpr int kDqTileN = 128;   // key rows per dQ-kernel KV tile
-// Query rows per dK/dV-kernel item (64: two items' S^T, dP^T fit TMEM at
-// D = 64 beside the accumulators and K, V).
-constexpr int dkdv_tile_m(int) { return 64; }
+// Query rows per dK/dV-kernel item: 128 at D = 64 (S^T, dP^T, P^T, dS^T and
+// both accumulators fill TMEM), 64 at D = 128 (the accumulators take twice
+// the columns).
+constexpr int dkdv_tile_m(int D) { return D == 64 ? 128 : 64; }
 
 // Static deal of query-tile work units (forward and dQ) to persistent
 // pipelines.  Unit u (in heaviest-first order) is query tile n_m - 1 - u / BHq

@@ -255,7 +255,7 @@ def test_product_shares_nothing_with_the_oracle():
 _KERNEL_THREADS_PER_SM = {
     "attn_fwd_kernelILi64E": 384, "attn_fwd_kernelILi128E": 256,
     "attn_dq_kernelILi64E": 384, "attn_dq_kernelILi128E": 384,
-    "attn_dkdv_kernelILi64E": 608, "attn_dkdv_kernelILi128E": 608,
+    "attn_dkdv64_kernel": 384, "attn_dkdv_kernelILi128E": 608,
     "attn_delta_kernelILi64E": 4 * 256, "attn_delta_kernelILi128E": 4 * 256,
 }
 
