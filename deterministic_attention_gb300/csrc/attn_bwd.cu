@@ -533,6 +533,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (last[s] >= 0) mbar_wait(bar(kDkvBarQFull + s), (last[s] / NS) & 1, wait_ns);
       }
     }
+    // The warp meets again before the block-wide barriers below (lanes 1-31
+    // skipped the producer loop).
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ S^T / dP^T issuer
     // The whole warp runs this loop (MMA issue is warp-collective); every

@@ -122,6 +122,8 @@ __global__ void __launch_bounds__(kDsThreads, 1)
         for (int s = 0; s < NS; ++s)
           if (last[s] >= 0) mbar_wait(bar(kSBarFull + s), (last[s] / NS) & 1, wait_ns);
     }
+    // The warp meets again before the block-wide barrier below.
+    __syncwarp();
   } else if (warp == 1) {
     // A: dS with queries (M) contiguous, two 64-query atoms 8 KB apart; B: K
     // with the head dimension (N) contiguous, 64-column atoms 8 KB apart.

@@ -132,6 +132,8 @@ __global__ void __launch_bounds__(kGemmThreads, GemmCfg<BN>::kBlocksPerSm)
         for (int s = 0; s < NS; ++s)
           if (last[s] >= 0) mbar_wait(bar(kGBarFull + s), (last[s] / NS) & 1, g.wait_ns);
     }
+    // The warp meets again before the block-wide barrier below.
+    __syncwarp();
   } else if (warp == 1) {
     constexpr uint32_t kId = idesc_bf16(kGemmBM, BN, A_MN, B_MN);
     // K-major tiles step K by 32 bytes inside the swizzled row; MN-major
