@@ -1872,10 +1872,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
       const Unit t = unit_info(u);
       if (t.n_kv == 0) continue;
       const int slot = ne % NQ;
-      // With one Q slot the next unit's Q cannot arrive before this one's
-      // last S, dP: finish the previous unit's dQ first, so its epilogue
-      // does not wait behind that load.
-      if (NQ == 1 && pend >= 0) {
+      // The previous unit's last dQ product goes first, so its epilogue never
+      // waits behind this unit's Q load (with one Q slot that load cannot
+      // even start before the previous unit's last S, dP).
+      if (pend >= 0) {
         if (!(ok = issue_dq(pend, pend_first, pend_last))) break;
         pend = -1;
       }
