@@ -298,7 +298,8 @@ enum : int {
   kDkvBarDrainAcc = kDkvBarDrain + 1,
   kDkvBarRecv = kDkvBarDrainAcc + 1,         // the peers' partial sums of this tile landed
   kDkvBarRegionFree = kDkvBarRecv + 1,       // every peer has read this block's previous sums
-  kDkvNumBars = kDkvBarRegionFree + 1
+  kDkvBarRecvRead = kDkvBarRegionFree + 1,   // (D = 64) this block has read the peers' sums
+  kDkvNumBars = kDkvBarRecvRead + 1
 };
 
 // TMEM columns [taddr, taddr + N) of this warp's 32 lanes into v (N = 16, 32).
@@ -881,9 +882,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         // This block's receive region is read: the peers may send the next
-        // tile's sums.
+        // tile's sums (after the last tile nothing more is sent).
         __syncwarp();
-        if (lane == 0) {
+        if (lane == 0 && tile_of(kt + 1) >= 0) {
           for (int p = 0; p < C; ++p)
             if (p != crank)
               mbar_arrive_remote(map_shared_rank(bar(kDkvBarRegionFree), static_cast<uint32_t>(p)));
@@ -1073,7 +1074,8 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
     mbar_init(bar(kDkvBarDrain), 1);
     mbar_init(bar(kDkvBarDrainAcc), 1);
     mbar_init(bar(kDkvBarRecv), 1);
-    mbar_init(bar(kDkvBarRegionFree), 8 * (C > 1 ? C - 1 : 1));
+    mbar_init(bar(kDkvBarRegionFree), C > 1 ? C - 1 : 1);
+    mbar_init(bar(kDkvBarRecvRead), 8);
     // The first tile's partial sums may arrive any time from now on.
     if (C > 1) mbar_arrive_expect_tx(bar(kDkvBarRecv), recv_bytes);
     fence_barrier_init();
@@ -1238,6 +1240,22 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
     }
     mma_commit(bar(kDkvBarDrainAcc));
     warp_all(mbar_wait(bar(kDkvBarDrainAcc), 0, wait_ns));
+  } else if (C > 1) {
+    // ------------------------------------------------------------ receive-region release
+    // After every tile but the last, once the element-wise warps have read
+    // the peers' sums, each peer is told it may send the next tile's: a
+    // remote arrival holds the issuing warp for about half a microsecond.
+    for (int kt = 0; ok; ++kt) {
+      const int t = tile_of(kt);
+      if (t < 0 || tile_of(kt + 1) < 0) break;
+      if (!(ok = warp_all(mbar_wait(bar(kDkvBarRecvRead), kt & 1, wait_ns)))) break;
+      if (lane == 0) {
+        for (int p = 0; p < C; ++p)
+          if (p != crank)
+            mbar_arrive_remote(map_shared_rank(bar(kDkvBarRegionFree), static_cast<uint32_t>(p)));
+      }
+      __syncwarp();
+    }
   }
   } else {
     setmaxnreg_inc<kDkwElemRegs>();
@@ -1443,13 +1461,10 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
           }
         }
         // This block's receive region is read: the peers may send the next
-        // tile's sums.
+        // tile's sums (warp 3 tells them, off these warps' path; after the
+        // last tile nothing more is sent).
         __syncwarp();
-        if (lane == 0) {
-          for (int p = 0; p < C; ++p)
-            if (p != crank)
-              mbar_arrive_remote(map_shared_rank(bar(kDkvBarRegionFree), static_cast<uint32_t>(p)));
-        }
+        if (lane == 0 && tile_of(kt + 1) >= 0) mbar_arrive(bar(kDkvBarRecvRead));
       }
       if (owner == crank && krow < ti.tk) {
         const size_t rbase =
@@ -1473,10 +1488,13 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
 
   // No block may exit while a peer can still store into its shared memory or
   // arrive on its mbarriers: every block reaches this barrier (no early exit;
-  // all waits above are bounded).
+  // all waits above are bounded).  Every such store and arrival has landed
+  // before its target block arrives here (its waits on them come first), so
+  // the barrier orders nothing else: its arrival is relaxed and need not wait
+  // for this block's dV, dK stores.
   if (C > 1) {
     __syncwarp();
-    cluster_sync();
+    cluster_sync_relaxed();
   }
 
   if (!ok) atomicOr(&g_bwd_status, 2u);

@@ -314,6 +314,13 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The same barrier without ordering this thread's earlier memory operations
+// for the other blocks (for a barrier that only keeps every block resident
+// until all have arrived).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+               "barrier.cluster.wait.aligned;" ::: "memory");
+}
 // Asynchronous 16-byte store into shared memory of a block of the cluster
 // (`addr`, `bar` from map_shared_rank); completes as 16 transaction bytes on
 // that block's mbarrier `bar`, which also makes the data visible to it.
