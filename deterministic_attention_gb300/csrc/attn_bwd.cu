@@ -1167,6 +1167,14 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       if (t < 0) break;
       const DkvTile ti = tile_info(t);
       if (!(ok = warp_all(mbar_wait(bar(kDkvBarKV), kt & 1, wait_ns)))) break;
+      // The previous tile's last dV, dK products go first: its epilogue waits
+      // for them, while this tile's first scores are not needed before that
+      // epilogue ends.  (Only before items of this block: with none, this
+      // tile's sums are signalled at once and could complete the barrier's
+      // next phase before this wait, which would then look for the wrong one.)
+      if (kt > 0 && ti.n_it > 0 &&
+          !(ok = warp_all(mbar_wait(bar(kDkvBarAcc), (kt - 1) & 1, wait_ns))))
+        break;
       tc_fence_after();
       for (int li = 0; li < ti.n_it; ++li, ++gi) {
         const int s = gi % NS;
