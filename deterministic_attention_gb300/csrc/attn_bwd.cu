@@ -944,40 +944,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //               dV and dK for the exchange and the store
 // TMEM: S^T [128 fp32 columns], dP^T [128], P^T [64 columns of bf16 pairs],
 // dS^T [64], dV [64], dK [64].
-constexpr int kDkw = 64;                   // head dimension of this kernel
+//
+// At D = 128 the same kernel runs with one block per key tile (no cluster)
+// and two stages; dV and dK take 256 TMEM columns, so P^T and dS^T go into
+// the S^T and dP^T columns their own threads have just read, and the next
+// item's S^T, dP^T wait for this item's dV, dK products.
 constexpr int kDkwTM = 128;                // queries per item
 constexpr int kDkwWarps = 12;
 constexpr int kDkwThreads = kDkwWarps * 32;
 constexpr uint32_t kDkwCtrlRegs = 104, kDkwElemRegs = 192;
 constexpr int kDkwRegBudget = 128 * kDkwCtrlRegs + 256 * kDkwElemRegs;
+template <int D>
 struct DkwCfg {
-  static constexpr int kKvBytes = kTileN * 128;            // 128 keys x 64
-  static constexpr int kQBytes = kDkwTM * 128;             // 128 queries x 64
-  static constexpr int kStages = 3;
+  static constexpr int kAtoms = D / 64;                    // 128-byte swizzle atoms per row
+  static constexpr int kKvBytes = kTileN * 128 * kAtoms;   // 128 keys x D
+  static constexpr int kQBytes = kDkwTM * 128 * kAtoms;    // 128 queries x D
+  static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kStageBytes = 2 * kQBytes + 1024;   // Q, dO, then 128 row statistics
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kKvBytes;
   static constexpr int kOffStage = 2 * kKvBytes;
-  static constexpr int kMaxCluster = 8;
-  static constexpr int kRowBytes = 2 * kDkw * 4;           // [dV | dK] fp32
+  static constexpr int kMaxCluster = D == 64 ? 8 : 1;
+  static constexpr int kRowBytes = 2 * D * 4;              // [dV | dK] fp32
   static constexpr int kOffRecv = kOffStage + kStages * kStageBytes;
   static constexpr int kRecvBytes = (kTileN - kTileN / kMaxCluster) * kRowBytes;
   static constexpr int kSmemBytes = kOffRecv + kRecvBytes + 1024;
-  static constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDS = 320, kColDV = 384,
-                            kColDK = 448;
+  // P^T and dS^T of query group g (64 queries, 32 packed columns) start at
+  // kColP + g kGrp and kColDS + g kGrp.
+  static constexpr uint32_t kColS = 0, kColDP = 128;
+  static constexpr uint32_t kColP = D == 64 ? 256 : kColS, kColDS = D == 64 ? 320 : kColDP;
+  static constexpr uint32_t kGrp = D == 64 ? 32 : 64;
+  static constexpr uint32_t kColDV = D == 64 ? 384 : 256, kColDK = kColDV + D;
+  static_assert(kColDK + D <= 512, "TMEM layout");
   static_assert(kSmemBytes + 512 <= 227 * 1024, "shared memory per block (with the static part)");
   static_assert(kStageBytes % 1024 == 0, "stages keep the swizzle alignment");
 };
 
-template <class VT, int MODE>
+template <int D, class VT, int MODE>
 __global__ void __launch_bounds__(kDkwThreads, 1)
-    attn_dkdv64_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-                       const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
-                       const BwdArgs a, const __grid_constant__ VT vt) {
-  using Cf = DkwCfg;
-  constexpr int D = kDkw;
+    attn_dkdvq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                      const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
+                      const BwdArgs a, const __grid_constant__ VT vt) {
+  using Cf = DkwCfg<D>;
   constexpr bool VL = std::is_same<VT, VarlenTable>::value;
   static_assert(!VL || MODE == 0, "the packed form walks its own table");
+  static_assert(D == 64 || (MODE & kDkvStoreDs) == 0, "dS^T stored at D = 64 only");
   constexpr int NS = Cf::kStages;
   constexpr int TM = kDkwTM;
   extern __shared__ uint8_t smem_raw[];
@@ -1114,8 +1125,12 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
         // The previous tile's S^T, dP^T MMAs must be done with K, V.
         if (kt > 0 && !(ok = mbar_wait(bar(kDkvBarKVFree), (kt - 1) & 1, wait_ns))) break;
         mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * Cf::kKvBytes);
-        tma_load_4d(sK, &mK, bar(kDkvBarKV), 0, ti.g, ti.kbase + ti.n0, ti.b);
-        tma_load_4d(sV, &mV, bar(kDkvBarKV), 0, ti.g, ti.kbase + ti.n0, ti.b);
+        for (int at = 0; at < Cf::kAtoms; ++at) {
+          tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, ti.g,
+                      ti.kbase + ti.n0, ti.b);
+          tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, ti.g,
+                      ti.kbase + ti.n0, ti.b);
+        }
         last_kv = kt;
         int h = ti.g * G + (ti.n_it > 0 ? ti.it_lo / ti.per_head : 0);
         int m_idx = ti.n_it > 0 ? ti.it_lo % ti.per_head : 0;
@@ -1126,8 +1141,12 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
           if (gi >= NS && !(ok = mbar_wait(bar(kDkvBarQEmpty + s), ph ^ 1, wait_ns))) break;
           const uint32_t st = stage_base(s);
           mbar_arrive_expect_tx(bar(kDkvBarQFull + s), 2 * Cf::kQBytes + TM * 8);
-          tma_load_4d(st, &mQ, bar(kDkvBarQFull + s), 0, h, ti.qbase + i0, ti.b);
-          tma_load_4d(st + Cf::kQBytes, &mdO, bar(kDkvBarQFull + s), 0, h, ti.qbase + i0, ti.b);
+          for (int at = 0; at < Cf::kAtoms; ++at) {
+            tma_load_4d(st + at * (TM * 128), &mQ, bar(kDkvBarQFull + s), at * 64, h,
+                        ti.qbase + i0, ti.b);
+            tma_load_4d(st + Cf::kQBytes + at * (TM * 128), &mdO, bar(kDkvBarQFull + s), at * 64,
+                        h, ti.qbase + i0, ti.b);
+          }
           if (!waited) {
             // Launched as a dependent of the Delta step: only the row
             // statistics are its output, so everything up to here (setup,
@@ -1179,15 +1198,27 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       for (int li = 0; li < ti.n_it; ++li, ++gi) {
         const int s = gi % NS;
         // The element-wise warps must hold the previous item's S^T, dP^T in
-        // registers before this item's overwrite them.
-        if (gi > 0 && !(ok = warp_all(mbar_wait(bar(kDkvBarSFree), (gi - 1) & 1, wait_ns)))) break;
+        // registers before this item's overwrite them; at D = 128 its dV, dK
+        // products must also have read the P^T, dS^T written over them.
+        if (gi > 0 && !(ok = warp_all(mbar_wait(bar(D == 64 ? kDkvBarSFree : kDkvBarFree),
+                                                (gi - 1) & 1, wait_ns))))
+          break;
         if (!(ok = warp_all(mbar_wait(bar(kDkvBarQFull + s), (gi / NS) & 1, wait_ns)))) break;
         tc_fence_after();
-        const uint64_t q = desc_add(dQk0, s * Cf::kStageBytes), o = desc_add(q, Cf::kQBytes);
-        mma_ss_x4(tS, dK, desc_add(dK, 32), desc_add(dK, 64), desc_add(dK, 96), q, desc_add(q, 32),
-                  desc_add(q, 64), desc_add(q, 96), kIdS, 0u);
-        mma_ss_x4(tDP, dV, desc_add(dV, 32), desc_add(dV, 64), desc_add(dV, 96), o, desc_add(o, 32),
-                  desc_add(o, 64), desc_add(o, 96), kIdS, 0u);
+        const uint64_t q0 = desc_add(dQk0, s * Cf::kStageBytes), o0 = desc_add(q0, Cf::kQBytes);
+        // K = D in groups of 64 (one 128-byte swizzle atom): four 32-byte steps.
+#pragma unroll
+        for (int at = 0; at < Cf::kAtoms; ++at) {
+          const uint64_t k = desc_add(dK, at * (kTileN * 128)), q = desc_add(q0, at * (TM * 128));
+          mma_ss_x4(tS, k, desc_add(k, 32), desc_add(k, 64), desc_add(k, 96), q, desc_add(q, 32),
+                    desc_add(q, 64), desc_add(q, 96), kIdS, at > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int at = 0; at < Cf::kAtoms; ++at) {
+          const uint64_t v = desc_add(dV, at * (kTileN * 128)), o = desc_add(o0, at * (TM * 128));
+          mma_ss_x4(tDP, v, desc_add(v, 32), desc_add(v, 64), desc_add(v, 96), o, desc_add(o, 32),
+                    desc_add(o, 64), desc_add(o, 96), kIdS, at > 0 ? 1u : 0u);
+        }
         mma_commit(bar(kDkvBarS));
       }
       if (!ok) break;
@@ -1202,7 +1233,8 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
     constexpr uint32_t kIdAcc = idesc_bf16(kTileN, D, false, true);
     const uint32_t tDV = tmem + Cf::kColDV, tDK = tmem + Cf::kColDK;
     const uint32_t tP = tmem + Cf::kColP, tDS = tmem + Cf::kColDS;
-    // Q, dO as MN-major B operands: 16 queries per 2048-byte step.
+    // Q, dO as MN-major B operands: 16 queries per 2048-byte step, the
+    // 64-column blocks of D = 128 TM * 128 bytes apart.
     const uint64_t dQm0 = sdesc_sw128(stage_base(0), TM * 128, 1024);
     int gi = 0;
     for (int kt = 0; ok; ++kt) {
@@ -1224,7 +1256,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
 #pragma unroll
         for (int q4 = 0; q4 < TM / 64; ++q4) {
           const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
-          const uint32_t p = tP + q4 * 32;
+          const uint32_t p = tP + q4 * Cf::kGrp;
           const uint64_t b = desc_add(om, q4 * 8192);
           mma_ts_x4(tDV, p, p + 8, p + 16, p + 24, b, desc_add(b, 2048), desc_add(b, 4096),
                     desc_add(b, 6144), kIdAcc, acc);
@@ -1232,7 +1264,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
 #pragma unroll
         for (int q4 = 0; q4 < TM / 64; ++q4) {
           const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
-          const uint32_t p = tDS + q4 * 32;
+          const uint32_t p = tDS + q4 * Cf::kGrp;
           const uint64_t b = desc_add(qm, q4 * 8192);
           mma_ts_x4(tDK, p, p + 8, p + 16, p + 24, b, desc_add(b, 2048), desc_add(b, 4096),
                     desc_add(b, 6144), kIdAcc, acc);
@@ -1303,10 +1335,12 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
           reg_fence32(sv[c]);
           reg_fence32(dp[c]);
         }
-        // S^T, dP^T are in registers: the next item's may overwrite them.
+        // S^T, dP^T are in registers: the next item's may overwrite them (at
+        // D = 128 only after this item's dV, dK products, which its issuer
+        // waits for).
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kDkvBarSFree));
+        if (D == 64 && lane == 0) mbar_arrive(bar(kDkvBarSFree));
         // Causal: query i0 + c sees key krow iff c >= krow - off - i0.  The
         // warp's rows span 32 keys: columns below the smallest row's bound
         // need no mask, chunks of 32 columns below the largest row's bound
@@ -1317,8 +1351,9 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
         // (-lse2, -delta) of this group's queries, two per float4.
         const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * 64 * 8;
         // The previous item's dV, dK MMAs must be done with the P^T, dS^T
-        // columns before this item's go there.
-        bool freed = gi == 0;
+        // columns before this item's go there (at D = 128 they are, as this
+        // item's S^T waited for them).
+        bool freed = gi == 0 || D != 64;
         auto chunk = [&](auto ch_c, auto masked) -> bool {
           constexpr int ch = decltype(ch_c)::value;
           constexpr bool kMasked = decltype(masked)::value;
@@ -1372,8 +1407,8 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
             tc_fence_after();
             freed = true;
           }
-          tmem_st16_nowait(tl + Cf::kColP + grp * 32 + 16 * ch, pk);
-          tmem_st16_nowait(tl + Cf::kColDS + grp * 32 + 16 * ch, dk);
+          tmem_st16_nowait(tl + Cf::kColP + grp * Cf::kGrp + 16 * ch, pk);
+          tmem_st16_nowait(tl + Cf::kColDS + grp * Cf::kGrp + 16 * ch, dk);
           return true;
         };
         if (warp_masked)
@@ -1398,11 +1433,19 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       uint32_t part_v[D / 2], part_k[D / 2];
       if (ti.n_it > 0) {
         tc_fence_after();
-        tmem_ld32_nowait(tl + Cf::kColDV + grp * (D / 2), part_v);
-        tmem_ld32_nowait(tl + Cf::kColDK + grp * (D / 2), part_k);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tmem_ld32_nowait(tl + Cf::kColDV + grp * (D / 2) + 32 * c,
+                           *reinterpret_cast<uint32_t(*)[32]>(part_v + 32 * c));
+          tmem_ld32_nowait(tl + Cf::kColDK + grp * (D / 2) + 32 * c,
+                           *reinterpret_cast<uint32_t(*)[32]>(part_k + 32 * c));
+        }
         tmem_wait_ld();
-        reg_fence32(part_v);
-        reg_fence32(part_k);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(part_v + 32 * c));
+          reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(part_k + 32 * c));
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < D / 2; ++i) part_v[i] = part_k[i] = 0u;
@@ -1412,7 +1455,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kDkvBarAccFree));
 
-      if (C > 1) {
+      if (Cf::kMaxCluster > 1 && C > 1) {
         // Rows another block owns: to its receive region, once it has read
         // the previous tile's.
         if (kt > 0) {
@@ -2145,12 +2188,12 @@ cudaError_t dkdv_max_clusters_t(int c, int* out) {
 
 cudaError_t dkdv64_max_clusters(int c, int* out) {
   static unsigned long long done[64] = {};
-  cudaError_t e = set_smem_once(attn_dkdv64_kernel<NoVarlen, 0>, DkwCfg::kSmemBytes, done);
+  cudaError_t e = set_smem_once(attn_dkdvq_kernel<64, NoVarlen, 0>, DkwCfg<64>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(c));
   cfg.blockDim = dim3(kDkwThreads);
-  cfg.dynamicSmemBytes = DkwCfg::kSmemBytes;
+  cfg.dynamicSmemBytes = DkwCfg<64>::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(c);
@@ -2158,29 +2201,29 @@ cudaError_t dkdv64_max_clusters(int c, int* out) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, attn_dkdv64_kernel<NoVarlen, 0>, &cfg);
+  return cudaOccupancyMaxActiveClusters(out, attn_dkdvq_kernel<64, NoVarlen, 0>, &cfg);
 }
 
-template <class VT, int MODE>
-cudaError_t launch_dkdv64_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
-                            const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                            bool dependent, const VT& vt, cudaStream_t st) {
+template <int D, class VT, int MODE>
+cudaError_t launch_dkdvq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
+                           const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
+                           bool dependent, const VT& vt, cudaStream_t st) {
   static unsigned long long done[64] = {};
-  cudaError_t e = set_smem_once(attn_dkdv64_kernel<VT, MODE>, DkwCfg::kSmemBytes, done);
+  cudaError_t e = set_smem_once(attn_dkdvq_kernel<D, VT, MODE>, DkwCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
   // The block's registers at launch must cover the warpgroups' shares after
   // reallocation, or the element-wise warpgroups' increase never completes.
   static int regs_ok = 0;
   if (!regs_ok) {
     cudaFuncAttributes fa{};
-    if ((e = cudaFuncGetAttributes(&fa, attn_dkdv64_kernel<VT, MODE>)) != cudaSuccess) return e;
+    if ((e = cudaFuncGetAttributes(&fa, attn_dkdvq_kernel<D, VT, MODE>)) != cudaSuccess) return e;
     if (fa.numRegs * kDkwThreads < kDkwRegBudget) return cudaErrorInvalidConfiguration;
     regs_ok = 1;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kDkwThreads);
-  cfg.dynamicSmemBytes = DkwCfg::kSmemBytes;
+  cfg.dynamicSmemBytes = DkwCfg<D>::kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   unsigned n = 0;
@@ -2198,7 +2241,7 @@ cudaError_t launch_dkdv64_t(int grid, const CUtensorMap& mq, const CUtensorMap& 
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  e = cudaLaunchKernelEx(&cfg, attn_dkdv64_kernel<VT, MODE>, mq, mk, mv, mdo, a, vt);
+  e = cudaLaunchKernelEx(&cfg, attn_dkdvq_kernel<D, VT, MODE>, mq, mk, mv, mdo, a, vt);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -2291,15 +2334,24 @@ cudaError_t launch_delta(const DeltaArgs& a, int sms, const VarlenTable* vt, cud
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                         bool dependent, const VarlenTable* vt, cudaStream_t st) {
-  if (vt != nullptr)
-    return D == 64 ? launch_dkdv64_t<VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st)
-                   : launch_dkdv_t<128, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
+  // D = 128: items of 128 queries with one block per key tile, items of 64
+  // queries when a tile is split over a cluster.
+  if (vt != nullptr) {
+    if (D == 64) return launch_dkdvq_t<64, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
+    if (a.cluster == 1)
+      return launch_dkdvq_t<128, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
+    return launch_dkdv_t<128, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
+  }
   const NoVarlen none{};
   const int mode = (a.bg_chunk > 0 ? kDkvChunked : 0) | (a.ds != nullptr ? kDkvStoreDs : 0);
   auto go = [&](auto m) {
     constexpr int M = decltype(m)::value;
-    return D == 64 ? launch_dkdv64_t<NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st)
-                   : launch_dkdv_t<128, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st);
+    if (D == 64) return launch_dkdvq_t<64, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st);
+    if constexpr ((M & kDkvStoreDs) == 0) {
+      if (a.cluster == 1)
+        return launch_dkdvq_t<128, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st);
+    }
+    return launch_dkdv_t<128, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st);
   };
   switch (mode) {
     case 0: return go(std::integral_constant<int, 0>{});
@@ -2315,7 +2367,7 @@ cudaError_t dkdv_max_clusters(int D, int c, int* out) {
   if (D == 128) return dkdv_max_clusters_t<128>(c, out);
   return cudaErrorInvalidValue;
 }
-int dkdv_max_cluster_size(int D) { return D == 64 ? DkwCfg::kMaxCluster : DkvCfg<128>::kMaxCluster; }
+int dkdv_max_cluster_size(int D) { return D == 64 ? DkwCfg<64>::kMaxCluster : DkvCfg<128>::kMaxCluster; }
 
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,

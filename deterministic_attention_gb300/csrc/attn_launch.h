@@ -15,6 +15,10 @@ constexpr int kDqTileN = 128;   // key rows per dQ-kernel KV tile
 // both accumulators fill TMEM), 64 at D = 128 (the accumulators take twice
 // the columns).
 constexpr int dkdv_tile_m(int D) { return D == 64 ? 128 : 64; }
+// Query rows the dK/dV kernel that runs with C blocks per key tile loads per
+// item (the rows of its Q, dO tensor-map boxes): 128, except at D = 128 with
+// a tile split over a cluster, which runs the 64-query kernel.
+constexpr int dkdv_item_rows(int D, int C) { return D == 64 || C == 1 ? 128 : 64; }
 
 // Static deal of query-tile work units (forward and dQ) to persistent
 // pipelines.  Unit u (in heaviest-first order) is query tile n_m - 1 - u / BHq

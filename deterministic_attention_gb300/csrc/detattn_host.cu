@@ -345,9 +345,16 @@ int sm_count(int* out) {
 // Returns false when no allowed C can be resident.
 // The choice over key tiles in walk order: tile t carries items[t / per_group]
 // items (per_group = 1: one entry per tile).
-bool dkdv_choose_items(const std::vector<int>& items_per_group, int per_group, int D,
-                       const int resident[4], int forced_c, int* c_out, int* ng_out) {
-  const long total = static_cast<long>(items_per_group.size()) * per_group;
+// At D = 128 with one block per tile the 128-query kernel runs: `items_one`
+// (tiles in that walk's order) then holds its 64-query halves, each weighted
+// kQ128Weight of a 64-query item of the clustered kernel (measured at B = 1,
+// T = 8192, Hq = 32, Hkv = 8: 2.13 us per 128 queries against 1.22 us per
+// 64); `items_split` is the walk of C > 1.
+constexpr double kQ128Weight = 0.875;
+bool dkdv_choose_items(const std::vector<int>& items_one, const std::vector<int>& items_split,
+                       int per_group, int D, const int resident[4], int forced_c, int* c_out,
+                       int* ng_out) {
+  const long total = static_cast<long>(items_split.size()) * per_group;
   const int cmax = dkdv_max_cluster_size(D);
   const double per_item64 = 64.0 / dkdv_tile_m(D);  // fixed costs in this kernel's items
   double best = 0.0;
@@ -357,6 +364,8 @@ bool dkdv_choose_items(const std::vector<int>& items_per_group, int per_group, i
     if (forced_c > 0 && c != (forced_c < cmax ? forced_c : cmax)) continue;
     if (resident[i] < 1) continue;
     const long ng = total < resident[i] ? total : resident[i];
+    const std::vector<int>& items_per_group = c == 1 ? items_one : items_split;
+    const double w = (c == 1 && D == 128) ? kQ128Weight : 1.0;
     double worst = 0.0;
     for (long k = 0; k < ng; ++k) {
       double load = 0.0;
@@ -369,7 +378,7 @@ bool dkdv_choose_items(const std::vector<int>& items_per_group, int per_group, i
         // (measured: distributed shared memory moves ~9 bytes per clock per
         // SM, and a 64-query item takes ~1,500 clocks); items of TM queries
         // count TM / 64 such items.
-        load += (items + c - 1) / c + (1.0 + 2.0 * (c - 1)) * per_item64;
+        load += w * ((items + c - 1) / c) + (1.0 + 2.0 * (c - 1)) * per_item64;
       }
       if (load > worst) worst = load;
     }
@@ -395,6 +404,9 @@ int dkdv_bg_chunk(int B, int T, int Hq, int Hkv, int D) {
   return g >= BH ? 0 : g;
 }
 
+// The chunk of the walk with one block per tile: none at D = 128.
+int dkdv_bg_chunk_one(int D, int chunk) { return D == 128 ? 0 : chunk; }
+
 bool dkdv_choose(int B, int T, int Hq, int Hkv, int D, int causal, const int resident[4],
                  int forced_c, int* c_out, int* ng_out) {
   const int G = Hq / Hkv;
@@ -403,13 +415,19 @@ bool dkdv_choose(int B, int T, int Hq, int Hkv, int D, int causal, const int res
   const int m_end = (T + tm - 1) / tm;
   const int BH = B * Hkv;
   const int chunk = dkdv_bg_chunk(B, T, Hq, Hkv, D);
-  std::vector<int> items(static_cast<size_t>(n_tiles) * BH);
+  // The walk with clusters (chunked when Q and dO do not fit in L2 at once)
+  // and the walk of one block per tile, which at D = 128 takes the tiles
+  // heaviest first without chunks (measured: the chunked walk of that kernel
+  // left blocks idle for up to 40 % of the step).
+  std::vector<int> items(static_cast<size_t>(n_tiles) * BH), items_one(items.size());
   for (long t = 0; t < static_cast<long>(items.size()); ++t) {
     int nt, bg;
     dkdv_tile_coords(static_cast<int>(t), n_tiles, BH, chunk, &nt, &bg);
     items[t] = G * (m_end - (causal ? nt * kTileN / tm : 0));
+    dkdv_tile_coords(static_cast<int>(t), n_tiles, BH, dkdv_bg_chunk_one(D, chunk), &nt, &bg);
+    items_one[t] = G * (m_end - (causal ? nt * kTileN / tm : 0));
   }
-  return dkdv_choose_items(items, 1, D, resident, forced_c, c_out, ng_out);
+  return dkdv_choose_items(items_one, items, 1, D, resident, forced_c, c_out, ng_out);
 }
 
 // dkdv_choose with the current device's residency: `sms` blocks alone, and
@@ -438,10 +456,6 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
               void* ds = nullptr, long ds_pairs = 0) {
   CUtensorMap mq, mk, mv, mdo;
   int rc;
-  if ((rc = encode_rows(&mq, q, B, T, Hq, D, dkdv_tile_m(D), "q")) != DETATTN_OK) return rc;
-  if ((rc = encode_rows(&mdo, dout, B, T, Hq, D, dkdv_tile_m(D), "dout")) != DETATTN_OK) return rc;
-  if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
-  if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
   BwdArgs a = bwd_args(workspace, T, Hq, Hkv, scale, causal);
   a.dk = dk;
   a.dv = dv;
@@ -455,6 +469,13 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
   if ((rc = dkdv_schedule(B, T, Hq, Hkv, D, causal, sms, g_dkdv_split, &a.cluster, &a.n_groups)) !=
       DETATTN_OK)
     return rc;
+  if (a.cluster == 1 && ds == nullptr) a.bg_chunk = dkdv_bg_chunk_one(D, a.bg_chunk);
+  // The stored-dS form keeps 64-query items at D = 128.
+  const int rows = ds != nullptr && D == 128 ? 64 : dkdv_item_rows(D, a.cluster);
+  if ((rc = encode_rows(&mq, q, B, T, Hq, D, rows, "q")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mdo, dout, B, T, Hq, D, rows, "dout")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
+  if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
   return launched(
       launch_dkdv(D, a.n_groups * a.cluster, mq, mk, mv, mdo, a, after_delta, nullptr, st),
       "attn_bwd_dkdv");
@@ -772,11 +793,6 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, 
   if (pk.kt.n_tiles > 0) {
     // dK/dV (every key row belongs to some key tile, so all of dk, dv is written).
     CUtensorMap mq, mk, mv, mdo;
-    if ((rc = encode_rows(&mq, qq, 1, tq_rows, Hq, D, dkdv_tile_m(D), "q")) != DETATTN_OK) return rc;
-    if ((rc = encode_rows(&mdo, dd, 1, tq_rows, Hq, D, dkdv_tile_m(D), "dout")) != DETATTN_OK)
-      return rc;
-    if ((rc = encode_rows(&mk, kk, 1, tk_rows, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
-    if ((rc = encode_rows(&mv, vv, 1, tk_rows, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
     BwdArgs b = a;
     b.dk = dk;
     b.dv = dv;
@@ -790,8 +806,14 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, 
         return fail(DETATTN_ERR_CUDA, "attn_bwd_varlen: cluster occupancy query: %s",
                     cudaGetErrorString(e));
     }
-    if (!dkdv_choose_items(pk.k_items, Hkv, D, resident, g_dkdv_split, &b.cluster, &b.n_groups))
+    if (!dkdv_choose_items(pk.k_items, pk.k_items, Hkv, D, resident, g_dkdv_split, &b.cluster,
+                           &b.n_groups))
       return fail(DETATTN_ERR_CUDA, "attn_bwd_varlen: no resident cluster shape for D = %d", D);
+    const int rows = dkdv_item_rows(D, b.cluster);
+    if ((rc = encode_rows(&mq, qq, 1, tq_rows, Hq, D, rows, "q")) != DETATTN_OK) return rc;
+    if ((rc = encode_rows(&mdo, dd, 1, tq_rows, Hq, D, rows, "dout")) != DETATTN_OK) return rc;
+    if ((rc = encode_rows(&mk, kk, 1, tk_rows, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
+    if ((rc = encode_rows(&mv, vv, 1, tk_rows, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
     if ((rc = launched(launch_dkdv(D, b.n_groups * b.cluster, mq, mk, mv, mdo, b, pk.total_q > 0,
                                    &pk.kt, st),
                        "attn_bwd_varlen (dK/dV)")) != DETATTN_OK)
