@@ -1076,10 +1076,15 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       mbar_init(bar(kDkvBarQFull + s), 1);
       mbar_init(bar(kDkvBarQEmpty + s), 1);
     }
-    mbar_init(bar(kDkvBarS), 1);
+    // D = 128 uses the second entries as well: S^T and dP^T land (S, S + 1),
+    // P^T and dS^T are written (P, P + 1), dV and dK products done (Free,
+    // Free + 1).
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kDkvBarS + i), 1);
+      mbar_init(bar(kDkvBarP + i), 8);
+      mbar_init(bar(kDkvBarFree + i), 1);
+    }
     mbar_init(bar(kDkvBarSFree), 8);
-    mbar_init(bar(kDkvBarP), 8);
-    mbar_init(bar(kDkvBarFree), 1);
     mbar_init(bar(kDkvBarAcc), 1);
     mbar_init(bar(kDkvBarAccFree), 8);
     mbar_init(bar(kDkvBarDrain), 1);
@@ -1197,12 +1202,37 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       tc_fence_after();
       for (int li = 0; li < ti.n_it; ++li, ++gi) {
         const int s = gi % NS;
+        if constexpr (D == 128) {
+          // S^T and dP^T separately: S^T once the previous item's dV product
+          // has read the P^T written over its columns, dP^T once its dK
+          // product has read dS^T; each lands on a barrier of its own, so the
+          // element-wise warps start on P^T while dP^T is computed.
+          if (!(ok = warp_all(mbar_wait(bar(kDkvBarQFull + s), (gi / NS) & 1, wait_ns)))) break;
+          const uint64_t q0 = desc_add(dQk0, s * Cf::kStageBytes), o0 = desc_add(q0, Cf::kQBytes);
+          if (gi > 0 && !(ok = warp_all(mbar_wait(bar(kDkvBarFree), (gi - 1) & 1, wait_ns)))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int at = 0; at < Cf::kAtoms; ++at) {
+            const uint64_t k = desc_add(dK, at * (kTileN * 128)), q = desc_add(q0, at * (TM * 128));
+            mma_ss_x4(tS, k, desc_add(k, 32), desc_add(k, 64), desc_add(k, 96), q, desc_add(q, 32),
+                      desc_add(q, 64), desc_add(q, 96), kIdS, at > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(kDkvBarS));
+          if (gi > 0 && !(ok = warp_all(mbar_wait(bar(kDkvBarFree + 1), (gi - 1) & 1, wait_ns))))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int at = 0; at < Cf::kAtoms; ++at) {
+            const uint64_t v = desc_add(dV, at * (kTileN * 128)), o = desc_add(o0, at * (TM * 128));
+            mma_ss_x4(tDP, v, desc_add(v, 32), desc_add(v, 64), desc_add(v, 96), o, desc_add(o, 32),
+                      desc_add(o, 64), desc_add(o, 96), kIdS, at > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(kDkvBarS + 1));
+          continue;
+        }
         // The element-wise warps must hold the previous item's S^T, dP^T in
-        // registers before this item's overwrite them; at D = 128 its dV, dK
-        // products must also have read the P^T, dS^T written over them.
-        if (gi > 0 && !(ok = warp_all(mbar_wait(bar(D == 64 ? kDkvBarSFree : kDkvBarFree),
-                                                (gi - 1) & 1, wait_ns))))
-          break;
+        // registers before this item's overwrite them.
+        if (gi > 0 && !(ok = warp_all(mbar_wait(bar(kDkvBarSFree), (gi - 1) & 1, wait_ns)))) break;
         if (!(ok = warp_all(mbar_wait(bar(kDkvBarQFull + s), (gi / NS) & 1, wait_ns)))) break;
         tc_fence_after();
         const uint64_t q0 = desc_add(dQk0, s * Cf::kStageBytes), o0 = desc_add(q0, Cf::kQBytes);
@@ -1261,6 +1291,13 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
           mma_ts_x4(tDV, p, p + 8, p + 16, p + 24, b, desc_add(b, 2048), desc_add(b, 4096),
                     desc_add(b, 6144), kIdAcc, acc);
         }
+        if constexpr (D == 128) {
+          // dV has read P^T (the next S^T may go there); dS^T is written
+          // separately, after P^T.
+          mma_commit(bar(kDkvBarFree));
+          if (!(ok = warp_all(mbar_wait(bar(kDkvBarP + 1), gi & 1, wait_ns)))) break;
+          tc_fence_after();
+        }
 #pragma unroll
         for (int q4 = 0; q4 < TM / 64; ++q4) {
           const uint32_t acc = (li > 0 || q4 > 0) ? 1u : 0u;
@@ -1271,9 +1308,9 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
         }
         // Both MMA streams of item gi have read stage s (the S^T stream
         // finished before the element-wise warps released P): free it, and the
-        // P^T / dS^T columns.
+        // P^T / dS^T columns (D = 128: the dS^T ones, where dP^T goes next).
         mma_commit(bar(kDkvBarQEmpty + s));
-        mma_commit(bar(kDkvBarFree));
+        mma_commit(bar(D == 64 ? kDkvBarFree : kDkvBarFree + 1));
       }
       if (!ok) break;
       mma_commit(bar(kDkvBarAcc));  // this tile's sums (at once when it has no items)
@@ -1320,6 +1357,113 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
         const int s = gi % NS;
         const int i0 = (ti.m_begin + m_idx) * TM + grp * 64;  // this group's first query
         if (++m_idx == ti.per_head) m_idx = 0;
+        // Causal: query i0 + c sees key krow iff c >= krow - off - i0.  The
+        // warp's rows span 32 keys: columns below the smallest row's bound
+        // need no mask, chunks of 32 columns below the largest row's bound
+        // are all zero.  (-lse2, -delta) of this group's queries: two per
+        // float4 at st4.
+        auto cmin_of = [&] { return a.causal ? (krow - ti.off - i0) : -1; };
+        auto wmin_of = [&] { return ti.n0 + quarter * 32 - ti.off - i0; };  // smallest row's bound
+        auto st4_of = [&] { return stage_base(s) + 2 * Cf::kQBytes + grp * 64 * 8; };
+        if constexpr (D == 128) {
+          // P^T first, from S^T alone, written over the S^T columns this
+          // thread has read (the dV product starts on it); then dS^T, once
+          // dP^T has landed, over the dP^T columns.  P stays in registers
+          // (fp32) for dS.
+          ok = warp_all(mbar_wait(bar(kDkvBarS), gi & 1, wait_ns));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t pv[2][32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) tmem_ld32_nowait(tl + Cf::kColS + grp * 64 + 32 * c, pv[c]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) reg_fence32(pv[c]);
+          const int cmin = cmin_of(), wmin = wmin_of();
+          const bool warp_masked = a.causal && wmin + 31 > 0;
+          const uint32_t st4 = st4_of();
+          auto p_chunk = [&](auto ch_c, auto masked) {
+            constexpr int ch = decltype(ch_c)::value;
+            constexpr bool kMasked = decltype(masked)::value;
+            uint32_t pk[16];
+            if (kMasked && a.causal && 32 * ch + 31 < wmin) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) pk[i] = 0u;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) pv[ch][i] = 0u;
+            } else {
+              static_for<16>([&](auto ic) {
+                constexpr int c2 = decltype(ic)::value;
+                constexpr int c = 2 * c2;
+                const float4 rs = ld_shared_f4_at<(32 * ch + c) * 8>(st4);
+                const float x0 = fmaf(__uint_as_float(pv[ch][c]), sl2, rs.x);
+                const float x1 = fmaf(__uint_as_float(pv[ch][c + 1]), sl2, rs.z);
+                float p0, p1;
+                if constexpr ((c2 & 7) < kPolyOf8) {
+                  p0 = exp2_poly(x0);
+                  p1 = exp2_poly(x1);
+                } else {
+                  p0 = ex2_approx(x0);
+                  p1 = ex2_approx(x1);
+                }
+                if constexpr (kMasked) {
+                  if (32 * ch + c < cmin) p0 = 0.f;
+                  if (32 * ch + c + 1 < cmin) p1 = 0.f;
+                }
+                pv[ch][c] = __float_as_uint(p0);
+                pv[ch][c + 1] = __float_as_uint(p1);
+                pk[c2] = pack_bf16x2(p0, p1);
+              });
+            }
+            tmem_st16_nowait(tl + Cf::kColP + grp * Cf::kGrp + 16 * ch, pk);
+          };
+          if (warp_masked) {
+            p_chunk(std::integral_constant<int, 0>{}, std::true_type{});
+            p_chunk(std::integral_constant<int, 1>{}, std::true_type{});
+          } else {
+            p_chunk(std::integral_constant<int, 0>{}, std::false_type{});
+            p_chunk(std::integral_constant<int, 1>{}, std::false_type{});
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kDkvBarP));
+          ok = warp_all(mbar_wait(bar(kDkvBarS + 1), gi & 1, wait_ns));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t dp[2][32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) tmem_ld32_nowait(tl + Cf::kColDP + grp * 64 + 32 * c, dp[c]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 2; ++c) reg_fence32(dp[c]);
+          auto ds_chunk = [&](auto ch_c) {
+            constexpr int ch = decltype(ch_c)::value;
+            uint32_t dk[16];
+            if (warp_masked && 32 * ch + 31 < wmin) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) dk[i] = 0u;
+            } else {
+              static_for<16>([&](auto ic) {
+                constexpr int c2 = decltype(ic)::value;
+                constexpr int c = 2 * c2;
+                const float4 rs = ld_shared_f4_at<(32 * ch + c) * 8>(st4);
+                const float d0 = __uint_as_float(pv[ch][c]) * (__uint_as_float(dp[ch][c]) + rs.y);
+                const float d1 =
+                    __uint_as_float(pv[ch][c + 1]) * (__uint_as_float(dp[ch][c + 1]) + rs.w);
+                dk[c2] = pack_bf16x2(d0, d1);
+              });
+            }
+            tmem_st16_nowait(tl + Cf::kColDS + grp * Cf::kGrp + 16 * ch, dk);
+          };
+          ds_chunk(std::integral_constant<int, 0>{});
+          ds_chunk(std::integral_constant<int, 1>{});
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kDkvBarP + 1));
+          continue;
+        }
         ok = warp_all(mbar_wait(bar(kDkvBarS), gi & 1, wait_ns));
         if (!ok) break;
         tc_fence_after();
@@ -1341,19 +1485,12 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (D == 64 && lane == 0) mbar_arrive(bar(kDkvBarSFree));
-        // Causal: query i0 + c sees key krow iff c >= krow - off - i0.  The
-        // warp's rows span 32 keys: columns below the smallest row's bound
-        // need no mask, chunks of 32 columns below the largest row's bound
-        // are all zero.
-        const int cmin = a.causal ? (krow - ti.off - i0) : -1;
-        const int wmin = ti.n0 + quarter * 32 - ti.off - i0;  // smallest row's bound
+        const int cmin = cmin_of(), wmin = wmin_of();
         const bool warp_masked = a.causal && wmin + 31 > 0;
-        // (-lse2, -delta) of this group's queries, two per float4.
-        const uint32_t st4 = stage_base(s) + 2 * Cf::kQBytes + grp * 64 * 8;
+        const uint32_t st4 = st4_of();
         // The previous item's dV, dK MMAs must be done with the P^T, dS^T
-        // columns before this item's go there (at D = 128 they are, as this
-        // item's S^T waited for them).
-        bool freed = gi == 0 || D != 64;
+        // columns before this item's go there.
+        bool freed = gi == 0;
         auto chunk = [&](auto ch_c, auto masked) -> bool {
           constexpr int ch = decltype(ch_c)::value;
           constexpr bool kMasked = decltype(masked)::value;
@@ -1430,6 +1567,45 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       // for a block without items in the tile).
       ok = warp_all(mbar_wait(bar(kDkvBarAcc), kt & 1, wait_ns));
       if (!ok) break;
+      if constexpr (D == 128) {
+        // One block per tile: dV, then dK, from TMEM straight to memory.
+        tc_fence_after();
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          uint32_t part[2][32];
+          if (ti.n_it > 0) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              tmem_ld32_nowait(tl + (which == 0 ? Cf::kColDV : Cf::kColDK) + grp * 64 + 32 * c, part[c]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) reg_fence32(part[c]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) part[i >> 5][i & 31] = 0u;
+          }
+          if (which == 1) {
+            // The next tile's first dV, dK MMA may overwrite the accumulators.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kDkvBarAccFree));
+          }
+          if (krow < ti.tk) {
+            const size_t rbase =
+                ((static_cast<size_t>(ti.b) * a.Tk + ti.kbase + krow) * a.Hkv + ti.g) * D + grp * 64;
+            const float mul = which == 0 ? 1.f : a.scale;
+            uint4* dst =
+                reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(which == 0 ? a.dv : a.dk) + rbase);
+            auto f = [&](int i) { return __uint_as_float(part[i >> 5][i & 31]) * mul; };
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_uint4(pack_bf16x2(f(8 * i), f(8 * i + 1)), pack_bf16x2(f(8 * i + 2), f(8 * i + 3)),
+                                  pack_bf16x2(f(8 * i + 4), f(8 * i + 5)),
+                                  pack_bf16x2(f(8 * i + 6), f(8 * i + 7)));
+          }
+        }
+        continue;
+      }
       uint32_t part_v[D / 2], part_k[D / 2];
       if (ti.n_it > 0) {
         tc_fence_after();
