@@ -513,8 +513,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!waited) {
             // Launched as a dependent of the Delta step: only the row
             // statistics are its output, so everything up to here (setup,
-            // K, V, Q, dO loads) overlaps it.
+            // K, V, Q, dO loads) overlaps it.  Once it is complete, the dQ
+            // step (a programmatic dependent of this grid, reading only the
+            // Delta step's results) may start on the SMs this grid frees.
             griddep_wait();
+            griddep_launch_dependents();
             waited = true;
           }
           bulk_load(st + 2 * Cf::kQBytes,
@@ -532,6 +535,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (last_kv >= 0) mbar_wait(bar(kDkvBarKV), last_kv & 1, wait_ns);
         for (int s = 0; s < NS; ++s)
           if (last[s] >= 0) mbar_wait(bar(kDkvBarQFull + s), (last[s] / NS) & 1, wait_ns);
+      }
+      // A block without items still lets the dQ step start only after the
+      // Delta step is complete.
+      if (!waited) {
+        griddep_wait();
+        griddep_launch_dependents();
       }
     }
     // The warp meets again before the block-wide barriers below (lanes 1-31
@@ -1155,8 +1164,11 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
           if (!waited) {
             // Launched as a dependent of the Delta step: only the row
             // statistics are its output, so everything up to here (setup,
-            // K, V, Q, dO loads) overlaps it.
+            // K, V, Q, dO loads) overlaps it.  Once it is complete, the dQ
+            // step (a programmatic dependent of this grid, reading only the
+            // Delta step's results) may start on the SMs this grid frees.
             griddep_wait();
+            griddep_launch_dependents();
             waited = true;
           }
           bulk_load(st + 2 * Cf::kQBytes,
@@ -1174,6 +1186,12 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
         if (last_kv >= 0) mbar_wait(bar(kDkvBarKV), last_kv & 1, wait_ns);
         for (int s = 0; s < NS; ++s)
           if (last[s] >= 0) mbar_wait(bar(kDkvBarQFull + s), (last[s] / NS) & 1, wait_ns);
+      }
+      // A block without items still lets the dQ step start only after the
+      // Delta step is complete.
+      if (!waited) {
+        griddep_wait();
+        griddep_launch_dependents();
       }
     }
     __syncwarp();
@@ -2305,6 +2323,10 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     __syncwarp();
   }
 
+  // Launched as a programmatic dependent of the dK/dV step, this grid may run
+  // beside it (it reads only the Delta step's results); it does not complete
+  // before that grid has, so later work on the stream sees dk and dv too.
+  if (threadIdx.x == 0) griddep_wait();
   if (!ok) atomicOr(&g_bwd_status, 4u);
   tc_fence_before();
   __syncthreads();
@@ -2458,7 +2480,8 @@ cudaError_t launch_dkdv_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk
 template <int D, class VT>
 cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
-                        const BwdArgs& a, const QTileSched& sched, const VT& vt, cudaStream_t st) {
+                        const BwdArgs& a, const QTileSched& sched, const VT& vt, bool dependent,
+                        cudaStream_t st) {
   static unsigned long long done[64] = {};
   cudaError_t e = set_smem_once(attn_dq_kernel<D, VT>, DqCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
@@ -2471,8 +2494,18 @@ cudaError_t launch_dq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
     if (fa.numRegs * kDqThreads < kDqRegBudget) return cudaErrorInvalidConfiguration;
     regs_ok[D == 64 ? 0 : 1] = 1;
   }
-  attn_dq_kernel<D, VT><<<grid, kDqThreads, DqCfg<D>::kSmemBytes, st>>>(mq, mk, mv, mdo, mdq, a,
-                                                                       sched, vt);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kDqThreads);
+  cfg.dynamicSmemBytes = DqCfg<D>::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, attn_dq_kernel<D, VT>, mq, mk, mv, mdo, mdq, a, sched, vt);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -2548,13 +2581,13 @@ int dkdv_max_cluster_size(int D) { return D == 64 ? DkwCfg<64>::kMaxCluster : Dk
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
                       const BwdArgs& a, const QTileSched& sched, const VarlenTable* vt,
-                      cudaStream_t st) {
+                      bool after_dkdv, cudaStream_t st) {
   if (vt != nullptr)
-    return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, mdq, a, sched, *vt, st)
-                   : launch_dq_t<128>(grid, mq, mk, mv, mdo, mdq, a, sched, *vt, st);
+    return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, mdq, a, sched, *vt, after_dkdv, st)
+                   : launch_dq_t<128>(grid, mq, mk, mv, mdo, mdq, a, sched, *vt, after_dkdv, st);
   const NoVarlen none{};
-  return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, mdq, a, sched, none, st)
-                 : launch_dq_t<128>(grid, mq, mk, mv, mdo, mdq, a, sched, none, st);
+  return D == 64 ? launch_dq_t<64>(grid, mq, mk, mv, mdo, mdq, a, sched, none, after_dkdv, st)
+                 : launch_dq_t<128>(grid, mq, mk, mv, mdo, mdq, a, sched, none, after_dkdv, st);
 }
 
 // Diagnostic: the kernels' 2^x forms on n inputs (polynomial scalar form,

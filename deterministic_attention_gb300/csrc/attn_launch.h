@@ -189,11 +189,15 @@ cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMa
                         bool dependent, const VarlenTable* vt, cudaStream_t st);
 // `mdq` covers dQ with boxes of 32 rows x D/2 columns, unswizzled: each
 // element-wise warp of the dQ step stores its rows of a tile (D = 64).
+// `after_dkdv`: launched as a programmatic dependent of the dK/dV step just
+// before it in `st`, which lets it start once every dK/dV block has seen the
+// Delta step complete; it then runs beside that step, and completes only
+// after it.
 constexpr int kDqStoreRows = 32;
 cudaError_t launch_dq(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                       const CUtensorMap& mv, const CUtensorMap& mdo, const CUtensorMap& mdq,
                       const BwdArgs& a, const QTileSched& sched, const VarlenTable* vt,
-                      cudaStream_t st);
+                      bool after_dkdv, cudaStream_t st);
 
 // Launches a one-thread kernel whose bounded wait on a never-completed
 // mbarrier runs out after limit_ns (sets the timeout bit, then returns).

@@ -483,7 +483,7 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
 
 int dq_impl(const void* q, const void* k, const void* v, const void* dout, const void* workspace,
             void* dq, int B, int T, int Hq, int Hkv, int D, float scale, int causal,
-            unsigned* counter, cudaStream_t st) {
+            unsigned* counter, cudaStream_t st, bool after_dkdv = false) {
   CUtensorMap mq, mk, mv, mdo, mdq;
   int rc;
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, kTileM, "q")) != DETATTN_OK) return rc;
@@ -502,7 +502,8 @@ int dq_impl(const void* q, const void* k, const void* v, const void* dout, const
   QTileSched sc;
   int g;
   cached_qtile_schedule(dq_pipes_per_block(D), B, T, Hq, causal, sms, &sc, &g);
-  return launched(launch_dq(D, g, mq, mk, mv, mdo, mdq, a, sc, nullptr, st), "attn_bwd_dq");
+  return launched(launch_dq(D, g, mq, mk, mv, mdo, mdq, a, sc, nullptr, after_dkdv, st),
+                  "attn_bwd_dq");
 }
 
 int check_workspace(const void* ws, size_t bytes, int B, int T, int Hq) {
@@ -510,45 +511,6 @@ int check_workspace(const void* ws, size_t bytes, int B, int T, int Hq) {
     return fail(DETATTN_ERR_WORKSPACE, "workspace needs %zu bytes, got %zu%s",
                 rowstat_bytes(B, T, Hq), bytes, ws ? "" : " (NULL)");
   if (!aligned16(ws)) return fail(DETATTN_ERR_ALIGN, "workspace is not 16-byte aligned");
-  return DETATTN_OK;
-}
-
-// ------------------------------------------------------------ side stream
-// attn_bwd runs dK/dV and dQ, which both need only the Delta step's output,
-// on two streams: dQ on a per-device side stream forked from the caller's
-// stream after Delta and joined back before attn_bwd returns.  The two grids
-// then fill each other's idle SMs.  Stream capture records the fork and join
-// as graph edges.  The side stream and events are created on first use.
-struct SideStream {
-  cudaStream_t stream = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  unsigned long long ctx = 0;  // id of the context the handles belong to
-};
-
-int side_stream(SideStream** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  static SideStream per_dev[64];
-  static std::mutex mu;
-  if (dev >= 64) return fail(DETATTN_ERR_CUDA, "device index %d too large", dev);
-  std::lock_guard<std::mutex> lock(mu);
-  SideStream& ss = per_dev[dev];
-  // Handles of a context that has since been destroyed (device reset) are
-  // dropped, not destroyed: they went with it.
-  const unsigned long long ctx = current_context_id();
-  if (ss.stream != nullptr && ctx != 0 && ss.ctx != ctx) ss = SideStream{};
-  if (ss.stream == nullptr) {
-    e = cudaStreamCreateWithFlags(&ss.stream, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
-    if (e != cudaSuccess) {
-      ss = SideStream{};
-      return fail(DETATTN_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
-    }
-    ss.ctx = current_context_id();
-  }
-  *out = &ss;
   return DETATTN_OK;
 }
 
@@ -583,8 +545,11 @@ int dq_from_ds_impl(const void* k, const void* ds, void* dq, long pairs, int B, 
   return launched(launch_dq_from_ds(D, mds, mk, a, a.n_tiles * a.BH, st), "attn_bwd dQ from dS");
 }
 
-// Delta, then dK/dV on `st` and dQ on the side stream (or, with a workspace
-// that holds the dS tiles, dK/dV then dQ from dS, both on `st`).
+// Delta, dK/dV and dQ on `st`, each a programmatic dependent of the one
+// before: dK/dV loads its operands while Delta runs, and dQ, which needs only
+// Delta's results, starts once every dK/dV block is past Delta and takes the
+// SMs the dK/dV grid frees (or, with a workspace that holds the dS tiles,
+// dK/dV then dQ from dS).
 int bwd_steps(const void* q, const void* k, const void* v, const void* o, const float* lse,
               const void* dout, void* dq, void* dk, void* dv, void* ws, size_t ws_bytes, int B,
               int T, int Hq, int Hkv, int D, float scale, int causal, cudaStream_t st) {
@@ -603,23 +568,12 @@ int bwd_steps(const void* q, const void* k, const void* v, const void* o, const 
     return ok_status();
   }
   if ((rc = delta_impl(o, dout, lse, ws, B, T, Hq, D, counter, st)) != DETATTN_OK) return rc;
-  SideStream* ss = nullptr;
-  if ((rc = side_stream(&ss)) != DETATTN_OK) return rc;
-  cudaError_t e = cudaEventRecord(ss->fork, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(ss->stream, ss->fork, 0);
-  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "fork: %s", cudaGetErrorString(e));
-  if ((rc = dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, counter,
-                    ss->stream)) !=
-      DETATTN_OK)
-    return rc;
-  // dK/dV follows the Delta step directly in `st`: its prologue and
-  // operand loads overlap that step (it waits only for the row statistics).
   if ((rc = dkdv_impl(q, k, v, dout, ws, dk, dv, B, T, Hq, Hkv, D, scale, causal, st,
                       /*after_delta=*/true)) != DETATTN_OK)
     return rc;
-  e = cudaEventRecord(ss->join, ss->stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ss->join, 0);
-  if (e != cudaSuccess) return fail(DETATTN_ERR_CUDA, "join: %s", cudaGetErrorString(e));
+  if ((rc = dq_impl(q, k, v, dout, ws, dq, B, T, Hq, Hkv, D, scale, causal, counter, st,
+                    /*after_dkdv=*/true)) != DETATTN_OK)
+    return rc;
   return ok_status();
 }
 
@@ -835,8 +789,11 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, 
     QTileSched sc;
     int g;
     qtile_schedule_w(dq_pipes_per_block(D), pk.q_weight, Hq, sms, &sc, &g);
-    if ((rc = launched(launch_dq(D, g, mq, mk, mv, mdo, mdq, b, sc, &pk.qt, st),
-                       "attn_bwd_varlen (dQ)")) != DETATTN_OK)
+    // A programmatic dependent of the dK/dV step when it was launched just
+    // before (not of the Delta step, which lets its dependents start early).
+    if ((rc = launched(
+             launch_dq(D, g, mq, mk, mv, mdo, mdq, b, sc, &pk.qt, pk.kt.n_tiles > 0, st),
+             "attn_bwd_varlen (dQ)")) != DETATTN_OK)
       return rc;
   }
   return ok_status();

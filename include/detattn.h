@@ -98,11 +98,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 size_t attn_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int D);
 
 /* Backward.  Given q, k, v, the forward's o and lse, and dout, writes dq, dk,
- * dv (bf16).  Runs attn_bwd_delta on `stream`, then attn_bwd_dkdv on `stream`
- * and attn_bwd_dq concurrently on a library-owned side stream (forked from
- * `stream` after the Delta step with an event and joined back before the call
- * returns; created on the first call per device), so all work is ordered
- * after earlier work on `stream` and later work on `stream` sees the results.
+ * dv (bf16).  Runs attn_bwd_delta, attn_bwd_dkdv and attn_bwd_dq on `stream`,
+ * the last two as programmatic dependents of the step before: the dQ step
+ * starts once every dK/dV block has seen the Delta step complete and runs on
+ * the SMs the dK/dV step frees, and it completes only after the dK/dV step
+ * has, so all work is ordered after earlier work on `stream` and later work
+ * on `stream` sees the results.
  * `workspace` (attn_bwd_workspace_bytes, at least the row statistics' share;
  * 16-byte aligned, caller-owned, contents on entry irrelevant) holds the row
  * statistics and the dQ step's tile counter (layout above).  Passage: "Step 2: fused flash attention" and "Where the time
