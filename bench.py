@@ -160,7 +160,7 @@ class Problem:
 
     def step(self, s):
         """fwd + bwd on set s through the public API: attn_fwd, then attn_bwd
-        (Delta, then dK/dV and dQ on two streams)."""
+        (Delta, then dK/dV with dQ taking the SMs it frees)."""
         self.step_api(s)
 
     def kernel(self, which, s):
@@ -221,7 +221,7 @@ def _kernel_source_sha() -> str:
 
 def _capture(fn, n_calls):
     """A CUDA graph holding fn(0) .. fn(n_calls - 1), captured after one
-    uncaptured pass (kernel attributes, descriptors, the side stream)."""
+    uncaptured pass (kernel attributes, descriptors)."""
     stream = torch.cuda.Stream()
     stream.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(stream):
