@@ -168,7 +168,7 @@ def test_dkdv_split_sizes(split, B, T, Hq, Hkv, D, causal):
     assert_bwd_close([("dK", to_np(dk), dk_r), ("dV", to_np(dv), dv_r)], f"split {split}")
 
 
-@pytest.mark.parametrize("split,D", [(1, 64), (2, 64), (4, 64), (8, 64), (2, 128)])
+@pytest.mark.parametrize("split,D", [(1, 64), (2, 64), (4, 64), (8, 64), (1, 128), (2, 128)])
 def test_dkdv_clusters_walk_several_tiles(split, D):
     """The persistent dK/dV launch with more key tiles than resident clusters:
     every cluster walks several tiles, the last ones small enough that some

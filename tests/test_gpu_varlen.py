@@ -84,6 +84,20 @@ def test_varlen_edge_cases(tqs, tks, Hq, Hkv, D, causal):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("split", [1, 2])
+def test_varlen_d128_both_dkdv_kernels(split):
+    """D = 128 packed batches through both dK/dV kernels: one block per key
+    tile (128-query items, P^T and dS^T over the score columns) and a key tile
+    split over two blocks (64-query items, partial sums exchanged)."""
+    da.set_dkdv_split(split)
+    try:
+        _check([130, 260, 77, 0], [300, 10, 200, 64], 4, 2, 128, True)
+        _check([257, 64], [90, 500], 2, 2, 128, False)
+    finally:
+        da.set_dkdv_split(0)
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("D", [64, 128])
 def test_varlen_equal_lengths_match_fixed_length_kernels(D):
     """B sequences of length T packed: O, LSE and dQ are the fixed-length
