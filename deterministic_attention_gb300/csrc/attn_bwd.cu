@@ -299,7 +299,9 @@ enum : int {
   kDkvBarRecv = kDkvBarDrainAcc + 1,         // the peers' partial sums of this tile landed
   kDkvBarRegionFree = kDkvBarRecv + 1,       // every peer has read this block's previous sums
   kDkvBarRecvRead = kDkvBarRegionFree + 1,   // (D = 64) this block has read the peers' sums
-  kDkvNumBars = kDkvBarRecvRead + 1
+  kDkvBarKV2 = kDkvBarRecvRead + 1,          // (D = 64) K, V landed in the second buffer
+  kDkvBarKVFree2 = kDkvBarKV2 + 1,           // (D = 64) the second buffer's S^T MMAs are done
+  kDkvNumBars = kDkvBarKVFree2 + 1
 };
 
 // TMEM columns [taddr, taddr + N) of this warp's 32 lanes into v (N = 16, 32).
@@ -970,9 +972,12 @@ struct DkwCfg {
   static constexpr int kQBytes = kDkwTM * 128 * kAtoms;    // 128 queries x D
   static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kStageBytes = 2 * kQBytes + 1024;   // Q, dO, then 128 row statistics
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = kKvBytes;
-  static constexpr int kOffStage = 2 * kKvBytes;
+  // K, V buffers: at D = 64 two, so the next tile's K, V load while this
+  // tile's items run (tile kt in buffer kt % 2).
+  static constexpr int kKvBufs = D == 64 ? 2 : 1;
+  static constexpr int kOffK = 0;                          // buffer b: K at 2 b kKvBytes
+  static constexpr int kOffV = kKvBytes;                   // V right after it
+  static constexpr int kOffStage = 2 * kKvBufs * kKvBytes;
   static constexpr int kMaxCluster = D == 64 ? 8 : 1;
   static constexpr int kRowBytes = 2 * D * 4;              // [dV | dK] fp32
   static constexpr int kOffRecv = kOffStage + kStages * kStageBytes;
@@ -1081,6 +1086,8 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(kDkvBarKV), 1);
     mbar_init(bar(kDkvBarKVFree), 1);
+    mbar_init(bar(kDkvBarKV2), 1);
+    mbar_init(bar(kDkvBarKVFree2), 1);
     for (int s = 0; s < kDkvMaxStages; ++s) {
       mbar_init(bar(kDkvBarQFull + s), 1);
       mbar_init(bar(kDkvBarQEmpty + s), 1);
@@ -1136,14 +1143,19 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
         const int t = tile_of(kt);
         if (t < 0) break;
         const DkvTile ti = tile_info(t);
-        // The previous tile's S^T, dP^T MMAs must be done with K, V.
-        if (kt > 0 && !(ok = mbar_wait(bar(kDkvBarKVFree), (kt - 1) & 1, wait_ns))) break;
-        mbar_arrive_expect_tx(bar(kDkvBarKV), 2 * Cf::kKvBytes);
+        // The S^T, dP^T MMAs of the tile that last used this K, V buffer
+        // must be done with it.
+        const int kb = kt % Cf::kKvBufs, kuse = kt / Cf::kKvBufs;
+        if (kuse > 0 && !(ok = mbar_wait(bar(kb == 0 ? kDkvBarKVFree : kDkvBarKVFree2),
+                                         (kuse - 1) & 1, wait_ns)))
+          break;
+        const int kvbar = kb == 0 ? kDkvBarKV : kDkvBarKV2;
+        mbar_arrive_expect_tx(bar(kvbar), 2 * Cf::kKvBytes);
         for (int at = 0; at < Cf::kAtoms; ++at) {
-          tma_load_4d(sK + at * (kTileN * 128), &mK, bar(kDkvBarKV), at * 64, ti.g,
-                      ti.kbase + ti.n0, ti.b);
-          tma_load_4d(sV + at * (kTileN * 128), &mV, bar(kDkvBarKV), at * 64, ti.g,
-                      ti.kbase + ti.n0, ti.b);
+          tma_load_4d(sK + kb * 2 * Cf::kKvBytes + at * (kTileN * 128), &mK, bar(kvbar), at * 64,
+                      ti.g, ti.kbase + ti.n0, ti.b);
+          tma_load_4d(sV + kb * 2 * Cf::kKvBytes + at * (kTileN * 128), &mV, bar(kvbar), at * 64,
+                      ti.g, ti.kbase + ti.n0, ti.b);
         }
         last_kv = kt;
         int h = ti.g * G + (ti.n_it > 0 ? ti.it_lo / ti.per_head : 0);
@@ -1183,7 +1195,9 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       }
       if (!ok) {
         // Copies still in flight must land before the block may exit.
-        if (last_kv >= 0) mbar_wait(bar(kDkvBarKV), last_kv & 1, wait_ns);
+        if (last_kv >= 0)
+          mbar_wait(bar(last_kv % Cf::kKvBufs == 0 ? kDkvBarKV : kDkvBarKV2),
+                    (last_kv / Cf::kKvBufs) & 1, wait_ns);
         for (int s = 0; s < NS; ++s)
           if (last[s] >= 0) mbar_wait(bar(kDkvBarQFull + s), (last[s] / NS) & 1, wait_ns);
       }
@@ -1200,7 +1214,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
     // The whole warp runs this loop (MMA issue is warp-collective); every
     // wait is made warp-uniform so the warp stays converged.
     constexpr uint32_t kIdS = idesc_bf16(kTileN, TM, false, false);
-    const uint64_t dK = sdesc_sw128(sK, 16, 1024), dV = sdesc_sw128(sV, 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(sK, 16, 1024), dV0 = sdesc_sw128(sV, 16, 1024);
     const uint64_t dQk0 = sdesc_sw128(stage_base(0), 16, 1024);  // K-major B
     const uint32_t tS = tmem + Cf::kColS, tDP = tmem + Cf::kColDP;
     int gi = 0;
@@ -1208,7 +1222,11 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       const int t = tile_of(kt);
       if (t < 0) break;
       const DkvTile ti = tile_info(t);
-      if (!(ok = warp_all(mbar_wait(bar(kDkvBarKV), kt & 1, wait_ns)))) break;
+      const int kb = kt % Cf::kKvBufs;
+      if (!(ok = warp_all(mbar_wait(bar(kb == 0 ? kDkvBarKV : kDkvBarKV2), (kt / Cf::kKvBufs) & 1,
+                                    wait_ns))))
+        break;
+      const uint64_t dK = desc_add(dK0, kb * 2 * Cf::kKvBytes), dV = desc_add(dV0, kb * 2 * Cf::kKvBytes);
       // The previous tile's last dV, dK products go first: its epilogue waits
       // for them, while this tile's first scores are not needed before that
       // epilogue ends.  (Only before items of this block: with none, this
@@ -1271,7 +1289,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       }
       if (!ok) break;
       // K, V of this tile are free once these MMAs complete.
-      mma_commit(bar(kDkvBarKVFree));
+      mma_commit(bar(kb == 0 ? kDkvBarKVFree : kDkvBarKVFree2));
     }
     // Every issued MMA must finish before TMEM is released.
     mma_commit(bar(kDkvBarDrain));
