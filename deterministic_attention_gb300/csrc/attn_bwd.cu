@@ -2335,6 +2335,9 @@ __global__ void __launch_bounds__(kDqThreads, 1)
           dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
       }
     }
+    // This block's units are done: whatever follows on the stream may start
+    // its set-up (it waits for this grid to complete before reading).
+    if (warp == 4 && lane == 0) griddep_launch_dependents();
     // Every store of dQ must be complete before the block (and its shared
     // memory) goes away.
     if (lane == 0) bulk_wait_group0();
