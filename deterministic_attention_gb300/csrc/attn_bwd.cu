@@ -199,13 +199,17 @@ __global__ void __launch_bounds__(256, kDeltaBlocksPerSm) attn_delta_kernel(cons
 }
 
 // ============================================================== dK / dV
+// This kernel (64-query items) runs at D = 128 when a key tile is split over
+// a cluster of two blocks, and for the stored-dS form at D = 128; every other
+// dK/dV launch runs attn_dkdvq_kernel below.  (Its D = 64 configuration, with
+// K and V copied into TMEM, is no longer instantiated.)
 // Persistent: the grid is n_groups clusters of C blocks, all resident.  Key
 // tiles (b, KV head, 128 keys), heaviest first under the causal mask, are
 // dealt to the clusters in snake order (round r: tiles r*NG .. r*NG + NG - 1,
 // reversed in odd rounds), and a cluster's C blocks split each of its tiles:
 // the tile's items -- one per (query head of the group, query tile of TM rows
-// at or after the key tile), TM = 128 for D = 64 and 64 for D = 128 -- are cut
-// into C contiguous chunks, and block r sums chunk r.  The split and the deal
+// at or after the key tile) -- are cut into C contiguous chunks, and block r
+// sums chunk r.  The split and the deal
 // depend only on the shape and the SM count, so every output bit is fixed for
 // a given problem and GPU.
 //   warp 0     loads each tile's K, V (once the previous tile's S^T MMAs are
