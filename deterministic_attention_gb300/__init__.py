@@ -22,7 +22,7 @@ from .build import LIB as _LIB_PATH, build  # noqa: F401
 
 __all__ = ["attn_fwd", "attn_bwd", "attn_bwd_delta", "attn_bwd_dkdv", "attn_bwd_dq",
            "workspace_bytes", "check_status", "set_wait_limit_ns", "selftest_wait_timeout",
-           "set_dkdv_split", "new_workspace", "rowstats_view", "last_error", "lib",
+           "set_dkdv_split", "set_dkdv_deal", "new_workspace", "rowstats_view", "last_error", "lib",
            "DetAttnError", "STATUS", "header_symbols", "build", "embed_grad",
            "embed_grad_workspace_bytes", "attn_fwd_varlen", "attn_bwd_varlen",
            "varlen_workspace_bytes", "layer_gemm", "layer_workspace_bytes", "LayerState",
@@ -96,6 +96,10 @@ def lib() -> ctypes.CDLL:
     L.detattn_selftest_wait_timeout.restype = i
     L.detattn_set_dkdv_split.argtypes = [i]
     L.detattn_set_dkdv_split.restype = i
+    L.detattn_diag_dkdv_list.argtypes = [i, i, i, i, i, i, i, i, vp, vp, i]
+    L.detattn_diag_dkdv_list.restype = i
+    L.detattn_set_dkdv_deal.argtypes = [i]
+    L.detattn_set_dkdv_deal.restype = i
     L.detattn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     L.detattn_set_wait_limit_ns.restype = None
     L.detattn_last_error.argtypes = []
@@ -444,6 +448,25 @@ def diag_dkdv_split(B, T, Hq, Hkv, D, causal, resident, blocks_per_key_tile=0):
     return c.value, ng.value
 
 
+def diag_dkdv_list(B, T, Hq, Hkv, causal, c, ng, force=False):
+    """The listed deal of the 64-dim dK/dV step's key tiles over ng clusters
+    of c blocks: a list, per block, of (tile, shared) pairs, or None where
+    the plain walk is used (see include/detattn.h); host-only."""
+    import numpy as np
+    nb = ng * c
+    start = np.zeros(nb + 1, dtype=np.int32)
+    cap = 4096
+    entry = np.zeros(cap, dtype=np.int32)
+    rc = lib().detattn_diag_dkdv_list(B, T, Hq, Hkv, int(bool(causal)), c, ng, int(bool(force)),
+                                      ctypes.c_void_p(start.ctypes.data),
+                                      ctypes.c_void_p(entry.ctypes.data), cap)
+    if rc < 0:
+        raise DetAttnError(rc, "detattn_diag_dkdv_list", last_error())
+    if rc == 0:
+        return None
+    return [[(int(e) >> 1, bool(e & 1)) for e in entry[start[i]:start[i + 1]]] for i in range(nb)]
+
+
 def diag_exp2(x):
     """(poly, poly pair form, special-function unit) 2^x of a float32 CUDA tensor."""
     _need(x, "x", torch.float32, tuple(x.shape))
@@ -462,6 +485,11 @@ def selftest_wait_timeout(limit_ns: int = 50_000_000):
 def set_dkdv_split(blocks_per_key_tile: int):
     """Forces the dK/dV split (1, 2, 4, 8) or restores automatic (0)."""
     _check(lib().detattn_set_dkdv_split(int(blocks_per_key_tile)), "detattn_set_dkdv_split")
+
+
+def set_dkdv_deal(mode: int):
+    """dK/dV key-tile deal at D = 64: 0 automatic, 1 plain walk, 2 listed deal."""
+    _check(lib().detattn_set_dkdv_deal(int(mode)), "detattn_set_dkdv_deal")
 
 
 def set_wait_limit_ns(ns: int):

@@ -21,8 +21,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <type_traits>
 #include <utility>
 
@@ -959,6 +961,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 //               dV and dK for the exchange and the store
 // TMEM: S^T [128 fp32 columns], dP^T [128], P^T [64 columns of bf16 pairs],
 // dS^T [64], dV [64], dK [64].
+// With a listed deal (DkvList) a block walks its own tiles: first those its
+// cluster shares (items split, partial sums exchanged, as in the snake
+// walk), then tiles of its own, whose rows it stores alone.
 //
 // At D = 128 the same kernel runs with one block per key tile (no cluster)
 // and two stages; dV and dK take 256 TMEM columns, so P^T and dS^T go into
@@ -1002,7 +1007,8 @@ template <int D, class VT, int MODE>
 __global__ void __launch_bounds__(kDkwThreads, 1)
     attn_dkdvq_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                       const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mdO,
-                      const BwdArgs a, const __grid_constant__ VT vt) {
+                      const BwdArgs a, const __grid_constant__ VT vt,
+                      const __grid_constant__ DkvList lst) {
   using Cf = DkwCfg<D>;
   constexpr bool VL = std::is_same<VT, VarlenTable>::value;
   static_assert(!VL || MODE == 0, "the packed form walks its own table");
@@ -1022,12 +1028,27 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
   const int G = a.Hq / a.Hkv;
   const int m_end = (a.T + TM - 1) / TM;
   const int R = kTileN / C;
-  // Tile of this cluster's kt-th turn, or -1 past its last.
+  // This block's turns: kt < n_sh are tiles the cluster shares (the exchange
+  // counts its phases by kt), the others tiles of this block alone.
+  // Only the 64-dim fixed-length walk without chunks is ever listed.
+  constexpr bool kListable = D == 64 && !VL && (MODE & kDkvChunked) == 0;
+  const bool listed = kListable && lst.n_blocks > 0;
+  const int l0 = listed ? lst.start[blockIdx.x] : 0;
+  const int l_n = listed ? lst.start[blockIdx.x + 1] - l0 : 0;
+  int n_sh = C > 1 ? INT_MAX : 0;
+  if (listed) {
+    n_sh = 0;
+    while (n_sh < l_n && (lst.entry[l0 + n_sh] & 1u) != 0) ++n_sh;
+  }
+  // Tile of this block's kt-th turn, or -1 past its last.
   auto tile_of = [&](int kt) {
+    if (listed) return kt < l_n ? static_cast<int>(lst.entry[l0 + kt] >> 1) : -1;
     const int t = kt * NG + ((kt & 1) ? NG - 1 - group : group);
     return t < n_tiles_all ? t : -1;
   };
-  auto tile_info = [&](int t) {
+  // Whether turn kt + 1 is shared as well (the exchange goes on).
+  auto shared_next = [&](int kt) { return kt + 1 < n_sh && tile_of(kt + 1) >= 0; };
+  auto tile_info = [&](int t, bool shared) {
     DkvTile ti;
     if constexpr (VL) {
       const uint32_t e = vt_tile(vt, t / a.BH);
@@ -1064,8 +1085,9 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       ti.off = 0;
     }
     const int n_all = G * ti.per_head;
-    ti.it_lo = static_cast<int>(static_cast<long>(crank) * n_all / C);
-    ti.n_it = static_cast<int>(static_cast<long>(crank + 1) * n_all / C) - ti.it_lo;
+    const int cs = shared ? C : 1, cr = shared ? crank : 0;
+    ti.it_lo = static_cast<int>(static_cast<long>(cr) * n_all / cs);
+    ti.n_it = static_cast<int>(static_cast<long>(cr + 1) * n_all / cs) - ti.it_lo;
     return ti;
   };
 
@@ -1113,7 +1135,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
     mbar_init(bar(kDkvBarRegionFree), C > 1 ? C - 1 : 1);
     mbar_init(bar(kDkvBarRecvRead), 8);
     // The first tile's partial sums may arrive any time from now on.
-    if (C > 1) mbar_arrive_expect_tx(bar(kDkvBarRecv), recv_bytes);
+    if (C > 1 && n_sh > 0) mbar_arrive_expect_tx(bar(kDkvBarRecv), recv_bytes);
     fence_barrier_init();
   }
   if (threadIdx.x == 32) {
@@ -1146,7 +1168,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       for (int kt = 0; ok; ++kt) {
         const int t = tile_of(kt);
         if (t < 0) break;
-        const DkvTile ti = tile_info(t);
+        const DkvTile ti = tile_info(t, kt < n_sh);
         // The S^T, dP^T MMAs of the tile that last used this K, V buffer
         // must be done with it.
         const int kb = kt % Cf::kKvBufs, kuse = kt / Cf::kKvBufs;
@@ -1225,7 +1247,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
     for (int kt = 0; ok; ++kt) {
       const int t = tile_of(kt);
       if (t < 0) break;
-      const DkvTile ti = tile_info(t);
+      const DkvTile ti = tile_info(t, kt < n_sh);
       const int kb = kt % Cf::kKvBufs;
       if (!(ok = warp_all(mbar_wait(bar(kb == 0 ? kDkvBarKV : kDkvBarKV2), (kt / Cf::kKvBufs) & 1,
                                     wait_ns))))
@@ -1310,7 +1332,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
     for (int kt = 0; ok; ++kt) {
       const int t = tile_of(kt);
       if (t < 0) break;
-      const DkvTile ti = tile_info(t);
+      const DkvTile ti = tile_info(t, kt < n_sh);
       // The element-wise warps must have read the previous tile's sums before
       // this tile's first MMA overwrites them -- and before this tile's
       // completion is signalled at all: a tile without items here signals at
@@ -1363,8 +1385,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
     // the peers' sums, each peer is told it may send the next tile's: a
     // remote arrival holds the issuing warp for about half a microsecond.
     for (int kt = 0; ok; ++kt) {
-      const int t = tile_of(kt);
-      if (t < 0 || tile_of(kt + 1) < 0) break;
+      if (tile_of(kt) < 0 || !shared_next(kt)) break;
       if (!(ok = warp_all(mbar_wait(bar(kDkvBarRecvRead), kt & 1, wait_ns)))) break;
       if (lane == 0) {
         for (int p = 0; p < C; ++p)
@@ -1390,7 +1411,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
     for (int kt = 0; ok; ++kt) {
       const int t = tile_of(kt);
       if (t < 0) break;
-      const DkvTile ti = tile_info(t);
+      const DkvTile ti = tile_info(t, kt < n_sh);
       const int krow = ti.n0 + r;
       int m_idx = ti.n_it > 0 ? ti.it_lo % ti.per_head : 0;  // query tile of the item in its head
       for (int li = 0; li < ti.n_it && ok; ++li, ++gi) {
@@ -1671,7 +1692,8 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kDkvBarAccFree));
 
-      if (Cf::kMaxCluster > 1 && C > 1) {
+      const bool sh = kt < n_sh;
+      if (Cf::kMaxCluster > 1 && C > 1 && sh) {
         // Rows another block owns: to its receive region, once it has read
         // the previous tile's.
         if (kt > 0) {
@@ -1703,7 +1725,7 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
         // only after every warp here has signalled (below, after this arm in
         // program order), and until then the barrier cannot move past the
         // phase the other warps are still checking.
-        if (warp == 4 && lane == 0 && tile_of(kt + 1) >= 0)
+        if (warp == 4 && lane == 0 && shared_next(kt))
           mbar_arrive_expect_tx(bar(kDkvBarRecv), recv_bytes);
         if (owner == crank) {
           const int rl = r - crank * R;
@@ -1731,9 +1753,9 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
         // tile's sums (warp 3 tells them, off these warps' path; after the
         // last tile nothing more is sent).
         __syncwarp();
-        if (lane == 0 && tile_of(kt + 1) >= 0) mbar_arrive(bar(kDkvBarRecvRead));
+        if (lane == 0 && shared_next(kt)) mbar_arrive(bar(kDkvBarRecvRead));
       }
-      if (owner == crank && krow < ti.tk) {
+      if ((owner == crank || !sh) && krow < ti.tk) {
         const size_t rbase =
             ((static_cast<size_t>(ti.b) * a.Tk + ti.kbase + krow) * a.Hkv + ti.g) * D + grp * (D / 2);
 #pragma unroll
@@ -2427,10 +2449,20 @@ cudaError_t dkdv64_max_clusters(int c, int* out) {
   return cudaOccupancyMaxActiveClusters(out, attn_dkdvq_kernel<64, NoVarlen, 0>, &cfg);
 }
 
+// The deal every launch without a list passes (n_blocks 0: the snake walk).
+const DkvList& no_dkv_list() {
+  static const DkvList none = [] {
+    DkvList l;
+    std::memset(&l, 0, sizeof(l));
+    return l;
+  }();
+  return none;
+}
+
 template <int D, class VT, int MODE>
 cudaError_t launch_dkdvq_t(int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                            const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                           bool dependent, const VT& vt, cudaStream_t st) {
+                           bool dependent, const VT& vt, const DkvList& lst, cudaStream_t st) {
   static unsigned long long done[64] = {};
   cudaError_t e = set_smem_once(attn_dkdvq_kernel<D, VT, MODE>, DkwCfg<D>::kSmemBytes, done);
   if (e != cudaSuccess) return e;
@@ -2464,7 +2496,7 @@ cudaError_t launch_dkdvq_t(int grid, const CUtensorMap& mq, const CUtensorMap& m
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  e = cudaLaunchKernelEx(&cfg, attn_dkdvq_kernel<D, VT, MODE>, mq, mk, mv, mdo, a, vt);
+  e = cudaLaunchKernelEx(&cfg, attn_dkdvq_kernel<D, VT, MODE>, mq, mk, mv, mdo, a, vt, lst);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -2567,23 +2599,37 @@ cudaError_t launch_delta(const DeltaArgs& a, int sms, const VarlenTable* vt, cud
 
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                        bool dependent, const VarlenTable* vt, cudaStream_t st) {
+                        bool dependent, const VarlenTable* vt, const DkvList* list,
+                        cudaStream_t st) {
   // D = 128: items of 128 queries with one block per key tile, items of 64
   // queries when a tile is split over a cluster.
+  const DkvList& nl = no_dkv_list();
+  if (list != nullptr) {
+    // Only the fixed-length walk of the 64-dim kernel without chunks takes a list.
+    if (D != 64 || vt != nullptr || a.bg_chunk > 0 || list->n_blocks != grid ||
+        grid > kDkvListMaxBlocks)
+      return cudaErrorInvalidValue;
+    if (a.ds != nullptr)
+      return launch_dkdvq_t<64, NoVarlen, kDkvStoreDs>(grid, mq, mk, mv, mdo, a, dependent, NoVarlen{},
+                                                       *list, st);
+    return launch_dkdvq_t<64, NoVarlen, 0>(grid, mq, mk, mv, mdo, a, dependent, NoVarlen{}, *list, st);
+  }
   if (vt != nullptr) {
-    if (D == 64) return launch_dkdvq_t<64, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
+    if (D == 64)
+      return launch_dkdvq_t<64, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, nl, st);
     if (a.cluster == 1)
-      return launch_dkdvq_t<128, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
+      return launch_dkdvq_t<128, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, nl, st);
     return launch_dkdv_t<128, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, st);
   }
   const NoVarlen none{};
   const int mode = (a.bg_chunk > 0 ? kDkvChunked : 0) | (a.ds != nullptr ? kDkvStoreDs : 0);
   auto go = [&](auto m) {
     constexpr int M = decltype(m)::value;
-    if (D == 64) return launch_dkdvq_t<64, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st);
+    if (D == 64)
+      return launch_dkdvq_t<64, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, nl, st);
     if constexpr ((M & kDkvStoreDs) == 0) {
       if (a.cluster == 1)
-        return launch_dkdvq_t<128, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st);
+        return launch_dkdvq_t<128, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, nl, st);
     }
     return launch_dkdv_t<128, NoVarlen, M>(grid, mq, mk, mv, mdo, a, dependent, none, st);
   };

@@ -151,6 +151,21 @@ cudaError_t launch_dq_from_ds(int D, const CUtensorMap& mds, const CUtensorMap& 
                               const BwdArgs& a, int n_units, cudaStream_t st);
 cudaError_t take_ds_status(cudaStream_t st, unsigned* out);
 
+// Listed deal of the dK/dV key tiles (the 128-query kernel, fixed length):
+// block i walks entries start[i] .. start[i + 1] - 1, each (tile << 1) |
+// shared.  A shared tile is taken by every block of the cluster (its items
+// split by rank, the partial sums exchanged); any other goes whole to one
+// block, which stores all its rows.  Every block lists its shared tiles
+// first, and the blocks of a cluster list the same ones in the same order.
+// n_blocks == 0: the snake walk of the tiles over the clusters instead.
+constexpr int kDkvListMaxBlocks = 256;
+constexpr int kDkvListMaxEntries = 1024;
+struct DkvList {
+  int n_blocks;
+  uint16_t start[kDkvListMaxBlocks + 1];
+  uint16_t entry[kDkvListMaxEntries];
+};
+
 // Key tile t of the dK/dV walk as (nt, bg): position nt along T, bg = b Hkv + g.
 __host__ __device__ inline void dkdv_tile_coords(int t, int n_tiles, int BH, int bg_chunk, int* nt,
                                                  int* bg) {
@@ -183,10 +198,13 @@ cudaError_t dkdv_max_clusters(int D, int c, int* out);
 int dkdv_max_cluster_size(int D);
 // `dependent`: launched as a programmatic dependent of the Delta step just
 // before it in `st` (the kernel waits for it only before reading the row
-// statistics; Q, K, V, dO must not be written by that step).
+// statistics; Q, K, V, dO must not be written by that step).  `list` (not
+// null, n_blocks == grid) deals the tiles by that list: D = 64, fixed length,
+// without the chunked walk.
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
-                        bool dependent, const VarlenTable* vt, cudaStream_t st);
+                        bool dependent, const VarlenTable* vt, const DkvList* list,
+                        cudaStream_t st);
 // `mdq` covers dQ with boxes of 32 rows x D/2 columns, unswizzled: each
 // element-wise warp of the dQ step stores its rows of a tile (D = 64).
 // `after_dkdv`: launched as a programmatic dependent of the dK/dV step just

@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <memory>
 #include <mutex>
 #include <vector>
 
@@ -25,6 +26,7 @@ constexpr int kVersion = 10000;  // 1.0.0
 thread_local char g_err[512] = "";
 unsigned long long g_wait_ns = 1000000000ull;  // 1 s per bounded wait
 int g_dkdv_split = 0;                           // 0: automatic
+int g_dkdv_deal = 0;  // 0: listed deal when its model beats the snake walk; 1: never; 2: always
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -450,6 +452,118 @@ int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int
   return DETATTN_OK;
 }
 
+// Listed deal of the 64-dim dK/dV kernel's key tiles over NG clusters of C
+// blocks (fixed length, the plain walk; see DkvList).  Tiles with at least x
+// items are shared by a cluster, lighter ones go whole to single blocks.
+// Heaviest first, a shared tile goes to the cluster whose blocks carry the
+// least and adds its share of the items to each of them, a whole tile to the
+// block with the least.  Besides its items a tile costs its end: reading the
+// sums, and when shared sending the peers' rows and waiting for theirs
+// (measured at page3: a shared tile's end and the next tile's start take
+// 4.3-5 us, about four 1.1 us items; a whole tile's about one and a half).
+// x is the item count that minimises the largest block load; the list is
+// kept when that load is below the snake walk's under the same costs (always
+// with `force`).  Returns false without a list, or when it does not fit.
+// Depends only on the tile loads, C and NG, so the sums' order is fixed for a
+// problem and a device.
+constexpr double kDkvSharedEnd = 4.0, kDkvOwnEnd = 1.5;
+bool dkdv_mixed_list(const std::vector<int>& items, int C, int NG, bool force, DkvList* out) {
+  const int n = static_cast<int>(items.size());
+  const int nb = NG * C;
+  if (C < 2 || NG < 1 || nb > kDkvListMaxBlocks || n < 1 || n >= 32768) return false;
+  double snake = 0.0;
+  for (int k = 0; k < NG; ++k) {
+    double load = 0.0;
+    for (int kt = 0;; ++kt) {
+      const int t = kt * NG + ((kt & 1) ? NG - 1 - k : k);
+      if (t >= n) break;
+      load += (items[t] + C - 1) / C + kDkvSharedEnd;
+    }
+    snake = std::max(snake, load);
+  }
+  std::vector<int> order(n);
+  for (int t = 0; t < n; ++t) order[t] = t;
+  std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return items[x] > items[y]; });
+  std::vector<int> xs;
+  for (int t : order)
+    if (xs.empty() || items[t] != xs.back()) xs.push_back(items[t]);
+  xs.push_back(INT32_MAX);  // nothing shared
+  double best = 0.0;
+  std::vector<std::vector<uint16_t>> best_lists;
+  for (int x : xs) {
+    std::vector<double> load(nb, 0.0);
+    std::vector<std::vector<uint16_t>> lists(nb);
+    long entries = 0;
+    for (int t : order) {
+      if (items[t] < x) continue;
+      int ci = 0;
+      double cl = 0.0;
+      for (int c = 0; c < NG; ++c) {
+        double m = 0.0;
+        for (int j = 0; j < C; ++j) m = std::max(m, load[c * C + j]);
+        if (c == 0 || m < cl) {
+          cl = m;
+          ci = c;
+        }
+      }
+      for (int j = 0; j < C; ++j) {
+        load[ci * C + j] += (items[t] + C - 1) / C + kDkvSharedEnd;
+        lists[ci * C + j].push_back(static_cast<uint16_t>((t << 1) | 1));
+      }
+      entries += C;
+    }
+    for (int t : order) {
+      if (items[t] >= x) continue;
+      int bi = 0;
+      for (int j = 1; j < nb; ++j)
+        if (load[j] < load[bi]) bi = j;
+      load[bi] += items[t] + kDkvOwnEnd;
+      lists[bi].push_back(static_cast<uint16_t>(t << 1));
+      ++entries;
+    }
+    if (entries > kDkvListMaxEntries) continue;
+    const double m = *std::max_element(load.begin(), load.end());
+    if (best_lists.empty() || m < best - 1e-9) {
+      best = m;
+      best_lists = std::move(lists);
+    }
+  }
+  if (best_lists.empty() || (!force && !(best < snake - 1e-9))) return false;
+  out->n_blocks = nb;
+  int e = 0;
+  for (int i = 0; i < nb; ++i) {
+    out->start[i] = static_cast<uint16_t>(e);
+    for (uint16_t v : best_lists[i]) out->entry[e++] = v;
+  }
+  out->start[nb] = static_cast<uint16_t>(e);
+  return true;
+}
+
+// dkdv_mixed_list for a fixed-length shape (tiles in the unchunked walk's
+// order), the last result kept: one layer's backward asks again every step.
+const DkvList* cached_dkdv_list(int B, int T, int Hq, int Hkv, int causal, int C, int NG,
+                                int deal) {
+  static std::mutex mu;
+  static int key[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+  static DkvList list;
+  static bool have = false;
+  std::lock_guard<std::mutex> lock(mu);
+  const int want[8] = {B, T, Hq, Hkv, causal, C, NG, deal};
+  if (!std::equal(want, want + 8, key)) {
+    const int G = Hq / Hkv, BH = B * Hkv;
+    const int tm = dkdv_tile_m(64);
+    const int n_tiles = (T + kTileN - 1) / kTileN, m_end = (T + tm - 1) / tm;
+    std::vector<int> items(static_cast<size_t>(n_tiles) * BH);
+    for (size_t t = 0; t < items.size(); ++t) {
+      const int nt = static_cast<int>(t) / BH;
+      items[t] = G * (m_end - (causal ? nt * kTileN / tm : 0));
+    }
+    have = dkdv_mixed_list(items, C, NG, deal == 2, &list);
+    std::copy(want, want + 8, key);
+  }
+  return have ? &list : nullptr;
+}
+
 int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
               const void* workspace, void* dk, void* dv, int B, int T, int Hq, int Hkv, int D,
               float scale, int causal, cudaStream_t st, bool after_delta = false,
@@ -470,6 +584,10 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
       DETATTN_OK)
     return rc;
   if (a.cluster == 1 && ds == nullptr) a.bg_chunk = dkdv_bg_chunk_one(D, a.bg_chunk);
+  const DkvList* list = nullptr;
+  // (The stored-dS form takes the same deal, so both forms give the same dK, dV.)
+  if (D == 64 && a.bg_chunk == 0 && a.cluster > 1 && g_dkdv_deal != 1)
+    list = cached_dkdv_list(B, T, Hq, Hkv, causal, a.cluster, a.n_groups, g_dkdv_deal);
   // The stored-dS form keeps 64-query items at D = 128.
   const int rows = ds != nullptr && D == 128 ? 64 : dkdv_item_rows(D, a.cluster);
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, rows, "q")) != DETATTN_OK) return rc;
@@ -477,7 +595,7 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
   if ((rc = encode_rows(&mk, k, B, T, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
   if ((rc = encode_rows(&mv, v, B, T, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
   return launched(
-      launch_dkdv(D, a.n_groups * a.cluster, mq, mk, mv, mdo, a, after_delta, nullptr, st),
+      launch_dkdv(D, a.n_groups * a.cluster, mq, mk, mv, mdo, a, after_delta, nullptr, list, st),
       "attn_bwd_dkdv");
 }
 
@@ -769,7 +887,7 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, 
     if ((rc = encode_rows(&mk, kk, 1, tk_rows, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
     if ((rc = encode_rows(&mv, vv, 1, tk_rows, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
     if ((rc = launched(launch_dkdv(D, b.n_groups * b.cluster, mq, mk, mv, mdo, b, pk.total_q > 0,
-                                   &pk.kt, st),
+                                   &pk.kt, nullptr, st),
                        "attn_bwd_varlen (dK/dV)")) != DETATTN_OK)
       return rc;
   }
@@ -1483,6 +1601,41 @@ int detattn_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
   if (limit_ns > 10000000000ull) limit_ns = 10000000000ull;
   return launched(launch_wait_timeout_selftest(limit_ns, static_cast<cudaStream_t>(stream)),
                   "detattn_selftest_wait_timeout");
+}
+
+int detattn_diag_dkdv_list(int B, int T, int Hq, int Hkv, int causal, int c, int ng, int force,
+                           int* start, int* entry, int max_entries) {
+  bool empty = false;
+  int rc;
+  if ((rc = check_shape(B, T, Hq, Hkv, 64, &empty)) != DETATTN_OK) return rc;
+  if (causal != 0 && causal != 1) return fail(DETATTN_ERR_SHAPE, "causal=%d must be 0 or 1", causal);
+  if (force != 0 && force != 1) return fail(DETATTN_ERR_SHAPE, "force=%d must be 0 or 1", force);
+  if (c < 2 || c > dkdv_max_cluster_size(64) || (c & (c - 1)) != 0 || ng < 1)
+    return fail(DETATTN_ERR_SHAPE, "c=%d, ng=%d", c, ng);
+  if (start == nullptr || entry == nullptr) return fail(DETATTN_ERR_NULL, "start and entry must not be NULL");
+  if (empty) return ok_status();
+  std::unique_ptr<DkvList> list(new DkvList());
+  const int G = Hq / Hkv, BH = B * Hkv, tm = dkdv_tile_m(64);
+  const int n_tiles = (T + kTileN - 1) / kTileN, m_end = (T + tm - 1) / tm;
+  std::vector<int> items(static_cast<size_t>(n_tiles) * BH);
+  for (size_t t = 0; t < items.size(); ++t)
+    items[t] = G * (m_end - (causal ? static_cast<int>(t) / BH * kTileN / tm : 0));
+  if (!dkdv_mixed_list(items, c, ng, force == 1, list.get())) {
+    ok_status();
+    return 0;
+  }
+  const int n = list->start[list->n_blocks];
+  if (n > max_entries) return fail(DETATTN_ERR_SHAPE, "the list holds %d entries, max_entries=%d", n, max_entries);
+  for (int i = 0; i <= list->n_blocks; ++i) start[i] = list->start[i];
+  for (int i = 0; i < n; ++i) entry[i] = list->entry[i];
+  ok_status();
+  return n;
+}
+
+int detattn_set_dkdv_deal(int mode) {
+  if (mode < 0 || mode > 2) return fail(DETATTN_ERR_SHAPE, "dkdv deal mode %d (0, 1 or 2)", mode);
+  g_dkdv_deal = mode;
+  return ok_status();
 }
 
 int detattn_set_dkdv_split(int blocks_per_key_tile) {

@@ -371,6 +371,33 @@ int detattn_diag_dkdv_split(int B, int T, int Hq, int Hkv, int D, int causal,
                             const int* resident, int blocks_per_key_tile, int* c_out,
                             int* ng_out);
 
+/* Diagnostic for host-side tests (no GPU needed): the listed deal of the
+ * dK/dV step's 128-key tiles at D = 64 (fixed length) over ng clusters of c
+ * blocks (c >= 2).  Tiles are numbered in walk order, t = nt * B*Hkv + b*Hkv
+ * + g (nt the tile's position along T).  A tile is either shared by all c
+ * blocks of one cluster (each takes a contiguous chunk of its items and the
+ * partial sums are added in rank order) or taken whole by one block.  Block
+ * i's tiles are entry[start[i] .. start[i + 1] - 1], each t * 2 + 1 when
+ * shared and t * 2 when whole; shared ones come first.  force = 0 builds the
+ * list only where its load model beats the plain walk, as attn_bwd does;
+ * force = 1 whenever it fits.  start must hold ng * c + 1 ints and entry
+ * max_entries.  Returns the number of entries, 0 when no list is used
+ * (the plain walk), or a negative status (DETATTN_ERR_SHAPE for a bad
+ * shape or c, ng; DETATTN_ERR_NULL for a NULL pointer).  Not tied to a
+ * passage of the method. */
+int detattn_diag_dkdv_list(int B, int T, int Hq, int Hkv, int causal, int c, int ng, int force,
+                           int* start, int* entry, int max_entries);
+
+/* Tuning knob: how the dK/dV step at D = 64 deals its key tiles when C > 1
+ * blocks share one (fixed-length inputs, either backward form).
+ * 0 (default): the listed deal of detattn_diag_dkdv_list where its load
+ * model beats the plain walk; 1: always the plain walk (every tile shared,
+ * tiles dealt to the clusters in alternating order); 2: the listed deal
+ * whenever it fits.  Results are bitwise reproducible for a given setting;
+ * different settings round dK, dV differently.  Host-side, per process.
+ * Returns DETATTN_OK or DETATTN_ERR_SHAPE for another value. */
+int detattn_set_dkdv_deal(int mode);
+
 /* Failure-detection self-test.  Launches a one-thread kernel on `stream`
  * that waits, with the same bounded wait the attention kernels use, on a
  * barrier nothing ever completes; after `limit_ns` (clamped to [1 ms, 10 s])

@@ -195,6 +195,71 @@ def test_dkdv_split_validates():
         da.diag_dkdv_split(1, 128, 2, 1, 128, True, [152, 0, 0, 5], 8)
 
 
+def _check_dkdv_list(lists, B, T, Hq, Hkv, c, ng):
+    """Every key tile is dealt once: whole to one block, or shared by all c
+    blocks of one cluster, which list it among their shared tiles in the
+    same order; each block's shared tiles come first."""
+    n_tiles = B * Hkv * -(-T // 128)
+    assert len(lists) == c * ng
+    seen = {}
+    for i, lst in enumerate(lists):
+        flags = [sh for _, sh in lst]
+        assert flags == sorted(flags, reverse=True), f"block {i}: shared tiles not first"
+        for t, sh in lst:
+            assert 0 <= t < n_tiles
+            seen.setdefault(t, []).append((i, sh))
+    assert sorted(seen) == list(range(n_tiles))
+    for t, holders in seen.items():
+        if holders[0][1]:
+            blocks = sorted(i for i, _ in holders)
+            assert all(sh for _, sh in holders) and len(blocks) == c
+            assert blocks == list(range(blocks[0], blocks[0] + c)) and blocks[0] % c == 0
+        else:
+            assert len(holders) == 1
+    for g in range(ng):
+        shared = [[t for t, sh in lists[g * c + j] if sh] for j in range(c)]
+        assert all(x == shared[0] for x in shared), f"cluster {g}: peers disagree"
+
+
+def test_dkdv_list_at_page3():
+    """At 4x1024x12/4 (C = 2 over 76 clusters) the automatic deal lists the
+    tiles: the three heaviest tile rows (24, 21, 18 items) shared, the rest
+    whole, so no block waits on a peer for a light tile."""
+    lists = da.diag_dkdv_list(4, 1024, 12, 4, True, 2, 76)
+    assert lists is not None
+    _check_dkdv_list(lists, 4, 1024, 12, 4, 2, 76)
+    BH = 4 * 4
+    for lst in lists:
+        for t, sh in lst:
+            assert sh == (t // BH < 3), (t, sh)
+    assert max(len(lst) for lst in lists) == 2
+
+
+@pytest.mark.parametrize("shape,c,ng", [((2, 520, 6, 2), 2, 3), ((1, 1024, 3, 1), 4, 2),
+                                        ((6, 1024, 3, 1), 8, 19), ((24, 1024, 3, 1), 2, 76),
+                                        ((3, 700, 8, 2), 2, 76)])
+def test_dkdv_list_invariants(shape, c, ng):
+    forced = da.diag_dkdv_list(*shape, True, c, ng, force=True)
+    assert forced is not None
+    _check_dkdv_list(forced, *shape, c, ng)
+    auto = da.diag_dkdv_list(*shape, True, c, ng)
+    if auto is not None:
+        assert auto == forced
+    assert da.diag_dkdv_list(*shape, False, c, ng, force=True) is not None
+
+
+def test_dkdv_list_validates():
+    assert da.diag_dkdv_list(0, 128, 2, 1, True, 2, 1) is None
+    for c, ng in ((1, 4), (3, 4), (16, 1), (2, 0)):
+        with pytest.raises(da.DetAttnError):
+            da.diag_dkdv_list(1, 1024, 2, 1, True, c, ng)
+    # More blocks than a list holds: the plain walk.
+    assert da.diag_dkdv_list(64, 1024, 2, 2, True, 2, 200, force=True) is None
+    da.set_dkdv_deal(0)
+    with pytest.raises(da.DetAttnError):
+        da.set_dkdv_deal(3)
+
+
 def test_size_limits_reject_before_any_device_call(L):
     """Shapes beyond the kernels' index limits fail validation (no device is
     needed to reach the answer)."""

@@ -171,9 +171,10 @@ def test_dkdv_split_sizes(split, B, T, Hq, Hkv, D, causal):
 @pytest.mark.parametrize("split,D", [(1, 64), (2, 64), (4, 64), (8, 64), (1, 128), (2, 128)])
 def test_dkdv_clusters_walk_several_tiles(split, D):
     """The persistent dK/dV launch with more key tiles than resident clusters:
-    every cluster walks several tiles, the last ones small enough that some
-    blocks of a cluster get no items of them.  Sampled key rows of early and
-    late tiles match the oracle, and the whole result repeats bit for bit."""
+    every cluster walks several tiles (the plain walk: every tile shared by
+    its cluster), the last ones small enough that some blocks of a cluster
+    get no items of them.  Sampled key rows of early and late tiles match the
+    oracle, and the whole result repeats bit for bit."""
     import deterministic_attention_gb300 as da
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     T, Hq, Hkv = 1024, 3, 1
@@ -181,11 +182,13 @@ def test_dkdv_clusters_walk_several_tiles(split, D):
     q, k, v, do = make_inputs(B, T, Hq, Hkv, D, seed=77 + split + D, dout_std=0.2)
     scale = 1.0 / math.sqrt(D)
     da.set_dkdv_split(split)
+    da.set_dkdv_deal(1)
     try:
         _, _, _, dk, dv = run_gpu(q, k, v, do, scale, True)
         _, _, _, dk2, dv2 = run_gpu(q, k, v, do, scale, True)
     finally:
         da.set_dkdv_split(0)
+        da.set_dkdv_deal(0)
     assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
     js = [0, 131, 640, 897, 1023]
     for b in (0, B - 1):
@@ -194,6 +197,46 @@ def test_dkdv_clusters_walk_several_tiles(split, D):
         got_k = to_np(dk[b:b + 1, js, 0])[0]
         got_v = to_np(dv[b:b + 1, js, 0])[0]
         assert_bwd_close([("dK", got_k, dk_r), ("dV", got_v, dv_r)], f"split {split} D {D} b {b}")
+
+
+@pytest.mark.parametrize("split", [2, 4, 8])
+def test_dkdv_listed_deal(split):
+    """The listed dK/dV deal (D = 64): the heaviest key tiles shared by a
+    cluster, lighter ones taken whole by single blocks that store all their
+    rows.  Sampled key rows of shared and whole tiles match the oracle, the
+    result repeats bit for bit, and the plain walk of the same tiles agrees
+    within the same tolerance."""
+    import deterministic_attention_gb300 as da
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    T, Hq, Hkv, D = 1024, 3, 1, 64
+    B = max(2, -(-5 * sms // (2 * split * (T // 128))))
+    q, k, v, do = make_inputs(B, T, Hq, Hkv, D, seed=91 + split, dout_std=0.2)
+    scale = 1.0 / math.sqrt(D)
+    ng = min(B * Hkv * (T // 128), sms // split)
+    lists = da.diag_dkdv_list(B, T, Hq, Hkv, True, split, ng, force=True)
+    assert lists is not None
+    kinds = {sh for lst in lists for _, sh in lst}
+    assert kinds == {True, False}, kinds
+    da.set_dkdv_split(split)
+    try:
+        da.set_dkdv_deal(2)
+        _, _, _, dk, dv = run_gpu(q, k, v, do, scale, True)
+        _, _, _, dk2, dv2 = run_gpu(q, k, v, do, scale, True)
+        da.set_dkdv_deal(1)
+        _, _, _, dk3, dv3 = run_gpu(q, k, v, do, scale, True)
+    finally:
+        da.set_dkdv_split(0)
+        da.set_dkdv_deal(0)
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert_bwd_close([("dK", to_np(dk), to_np(dk3)), ("dV", to_np(dv), to_np(dv3))],
+                     f"listed vs plain, split {split}")
+    js = [0, 131, 640, 897, 1023]
+    for b in (0, B - 1):
+        qf, kf, vf, dof = (widen(t[b:b + 1]) for t in (q, k, v, do))
+        dk_r, dv_r = oracle.kv_rows(qf, kf, vf, dof, 0, 0, js, scale, True)
+        got_k = to_np(dk[b:b + 1, js, 0])[0]
+        got_v = to_np(dv[b:b + 1, js, 0])[0]
+        assert_bwd_close([("dK", got_k, dk_r), ("dV", got_v, dv_r)], f"listed, split {split} b {b}")
 
 
 def test_fma_pipe_exp2_error_bound():
