@@ -1030,8 +1030,8 @@ __global__ void __launch_bounds__(kDkwThreads, 1)
   const int R = kTileN / C;
   // This block's turns: kt < n_sh are tiles the cluster shares (the exchange
   // counts its phases by kt), the others tiles of this block alone.
-  // Only the 64-dim fixed-length walk without chunks is ever listed.
-  constexpr bool kListable = D == 64 && !VL && (MODE & kDkvChunked) == 0;
+  // Only the 64-dim walk without chunks is ever listed.
+  constexpr bool kListable = D == 64 && (MODE & kDkvChunked) == 0;
   const bool listed = kListable && lst.n_blocks > 0;
   const int l0 = listed ? lst.start[blockIdx.x] : 0;
   const int l_n = listed ? lst.start[blockIdx.x + 1] - l0 : 0;
@@ -2605,10 +2605,12 @@ cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMa
   // queries when a tile is split over a cluster.
   const DkvList& nl = no_dkv_list();
   if (list != nullptr) {
-    // Only the fixed-length walk of the 64-dim kernel without chunks takes a list.
-    if (D != 64 || vt != nullptr || a.bg_chunk > 0 || list->n_blocks != grid ||
-        grid > kDkvListMaxBlocks)
+    // Only the walk of the 64-dim kernel without chunks takes a list.
+    if (D != 64 || a.bg_chunk > 0 || list->n_blocks != grid || grid > kDkvListMaxBlocks ||
+        (vt != nullptr && a.ds != nullptr))
       return cudaErrorInvalidValue;
+    if (vt != nullptr)
+      return launch_dkdvq_t<64, VarlenTable, 0>(grid, mq, mk, mv, mdo, a, dependent, *vt, *list, st);
     if (a.ds != nullptr)
       return launch_dkdvq_t<64, NoVarlen, kDkvStoreDs>(grid, mq, mk, mv, mdo, a, dependent, NoVarlen{},
                                                        *list, st);

@@ -151,7 +151,7 @@ cudaError_t launch_dq_from_ds(int D, const CUtensorMap& mds, const CUtensorMap& 
                               const BwdArgs& a, int n_units, cudaStream_t st);
 cudaError_t take_ds_status(cudaStream_t st, unsigned* out);
 
-// Listed deal of the dK/dV key tiles (the 128-query kernel, fixed length):
+// Listed deal of the dK/dV key tiles (the 128-query kernel at D = 64):
 // block i walks entries start[i] .. start[i + 1] - 1, each (tile << 1) |
 // shared.  A shared tile is taken by every block of the cluster (its items
 // split by rank, the partial sums exchanged); any other goes whole to one
@@ -199,8 +199,8 @@ int dkdv_max_cluster_size(int D);
 // `dependent`: launched as a programmatic dependent of the Delta step just
 // before it in `st` (the kernel waits for it only before reading the row
 // statistics; Q, K, V, dO must not be written by that step).  `list` (not
-// null, n_blocks == grid) deals the tiles by that list: D = 64, fixed length,
-// without the chunked walk.
+// null, n_blocks == grid) deals the tiles by that list: D = 64, without the
+// chunked walk (tile t of a packed batch: table entry t / Hkv, KV head t % Hkv).
 cudaError_t launch_dkdv(int D, int grid, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const CUtensorMap& mdo, const BwdArgs& a,
                         bool dependent, const VarlenTable* vt, const DkvList* list,

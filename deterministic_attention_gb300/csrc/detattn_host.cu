@@ -9,8 +9,10 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <functional>
 #include <memory>
 #include <mutex>
+#include <queue>
 #include <vector>
 
 #include "../../include/detattn.h"
@@ -490,35 +492,38 @@ bool dkdv_mixed_list(const std::vector<int>& items, int C, int NG, bool force, D
   xs.push_back(INT32_MAX);  // nothing shared
   double best = 0.0;
   std::vector<std::vector<uint16_t>> best_lists;
+  // Loads are sums of whole items and the two end costs (exact in double);
+  // each pick takes the least load, the lowest index among equals.
+  using Slot = std::pair<double, int>;
+  using MinHeap = std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>>;
   for (int x : xs) {
     std::vector<double> load(nb, 0.0);
     std::vector<std::vector<uint16_t>> lists(nb);
     long entries = 0;
+    // Shared tiles first: a cluster's blocks carry equal loads until then.
+    MinHeap clusters;
+    for (int c = 0; c < NG; ++c) clusters.push({0.0, c});
     for (int t : order) {
       if (items[t] < x) continue;
-      int ci = 0;
-      double cl = 0.0;
-      for (int c = 0; c < NG; ++c) {
-        double m = 0.0;
-        for (int j = 0; j < C; ++j) m = std::max(m, load[c * C + j]);
-        if (c == 0 || m < cl) {
-          cl = m;
-          ci = c;
-        }
-      }
+      const Slot top = clusters.top();
+      clusters.pop();
+      const double add = (items[t] + C - 1) / C + kDkvSharedEnd;
       for (int j = 0; j < C; ++j) {
-        load[ci * C + j] += (items[t] + C - 1) / C + kDkvSharedEnd;
-        lists[ci * C + j].push_back(static_cast<uint16_t>((t << 1) | 1));
+        load[top.second * C + j] += add;
+        lists[top.second * C + j].push_back(static_cast<uint16_t>((t << 1) | 1));
       }
+      clusters.push({top.first + add, top.second});
       entries += C;
     }
+    MinHeap blocks;
+    for (int j = 0; j < nb; ++j) blocks.push({load[j], j});
     for (int t : order) {
       if (items[t] >= x) continue;
-      int bi = 0;
-      for (int j = 1; j < nb; ++j)
-        if (load[j] < load[bi]) bi = j;
-      load[bi] += items[t] + kDkvOwnEnd;
-      lists[bi].push_back(static_cast<uint16_t>(t << 1));
+      const Slot top = blocks.top();
+      blocks.pop();
+      load[top.second] += items[t] + kDkvOwnEnd;
+      lists[top.second].push_back(static_cast<uint16_t>(t << 1));
+      blocks.push({load[top.second], top.second});
       ++entries;
     }
     if (entries > kDkvListMaxEntries) continue;
@@ -881,13 +886,22 @@ int bwd_varlen_impl(const void* q, const void* k, const void* v, const void* o, 
     if (!dkdv_choose_items(pk.k_items, pk.k_items, Hkv, D, resident, g_dkdv_split, &b.cluster,
                            &b.n_groups))
       return fail(DETATTN_ERR_CUDA, "attn_bwd_varlen: no resident cluster shape for D = %d", D);
+    // The listed deal as for fixed lengths, over the table's tiles (the
+    // items of tile t are those of its entry t / Hkv).
+    DkvList list;
+    bool listed = false;
+    if (D == 64 && b.cluster > 1 && g_dkdv_deal != 1) {
+      std::vector<int> items(pk.k_items.size() * static_cast<size_t>(Hkv));
+      for (size_t t = 0; t < items.size(); ++t) items[t] = pk.k_items[t / Hkv];
+      listed = dkdv_mixed_list(items, b.cluster, b.n_groups, g_dkdv_deal == 2, &list);
+    }
     const int rows = dkdv_item_rows(D, b.cluster);
     if ((rc = encode_rows(&mq, qq, 1, tq_rows, Hq, D, rows, "q")) != DETATTN_OK) return rc;
     if ((rc = encode_rows(&mdo, dd, 1, tq_rows, Hq, D, rows, "dout")) != DETATTN_OK) return rc;
     if ((rc = encode_rows(&mk, kk, 1, tk_rows, Hkv, D, kTileN, "k")) != DETATTN_OK) return rc;
     if ((rc = encode_rows(&mv, vv, 1, tk_rows, Hkv, D, kTileN, "v")) != DETATTN_OK) return rc;
     if ((rc = launched(launch_dkdv(D, b.n_groups * b.cluster, mq, mk, mv, mdo, b, pk.total_q > 0,
-                                   &pk.kt, nullptr, st),
+                                   &pk.kt, listed ? &list : nullptr, st),
                        "attn_bwd_varlen (dK/dV)")) != DETATTN_OK)
       return rc;
   }

@@ -389,7 +389,8 @@ int detattn_diag_dkdv_list(int B, int T, int Hq, int Hkv, int causal, int c, int
                            int* start, int* entry, int max_entries);
 
 /* Tuning knob: how the dK/dV step at D = 64 deals its key tiles when C > 1
- * blocks share one (fixed-length inputs, either backward form).
+ * blocks share one (fixed-length inputs with either backward form, and
+ * packed batches, whose list is built the same way over their key tiles).
  * 0 (default): the listed deal of detattn_diag_dkdv_list where its load
  * model beats the plain walk; 1: always the plain walk (every tile shared,
  * tiles dealt to the clusters in alternating order); 2: the listed deal
