@@ -135,23 +135,43 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU arm
+def _packed(like, device, pin=False):
+    """One uint8 buffer holding tensors of the shapes and dtypes of `like`
+    back to back (each at a 16-byte aligned offset), and views of it."""
+    sizes = [t.numel() * t.element_size() for t in like]
+    offs, total = [], 0
+    for n in sizes:
+        offs.append(total)
+        total += (n + 15) // 16 * 16
+    buf = torch.empty(total, dtype=torch.uint8, device=device, pin_memory=pin)
+    return buf, [buf[o:o + n].view(t.dtype).view(t.shape) for o, n, t in zip(offs, sizes, like)]
+
+
 class Problem:
-    """One replica's device buffers (several rotating sets) and the step."""
+    """One replica's device buffers (several rotating sets) and the step.
+    Each set keeps its inputs (Q, K, V, dO) in one buffer and its results
+    (O, LSE, dQ, dK, dV) in another, so that the end-to-end measurement moves
+    a step's data each way with one copy."""
 
     def __init__(self, w, n_sets, device, stored_ds=False):
         import deterministic_attention_gb300 as da
         self.da, self.w = da, w
         B, T, Hq, Hkv, D = w.shape
         q, k, v, do = workload_inputs(w)
-        self.host_in = [t.pin_memory() for t in (q, k, v, do)]
-        self.sets = []
+        self.host_in_buf, self.host_in = _packed((q, k, v, do), "cpu", pin=True)
+        for dst, src in zip(self.host_in, (q, k, v, do)):
+            dst.copy_(src)
+        out_like = [torch.empty(t.shape, dtype=t.dtype, device="meta") for t in (q, q, k, v)]
+        out_like.append(torch.empty((B, Hq, T), dtype=torch.float32, device="meta"))
+        self.sets, self.bufs = [], []
         for s in range(n_sets):
-            ins = [t.to(device) for t in (q, k, v, do)]
-            outs = dict(o=torch.empty_like(ins[0]), dq=torch.empty_like(ins[0]),
-                        dk=torch.empty_like(ins[1]), dv=torch.empty_like(ins[2]),
-                        lse=torch.empty((B, Hq, T), dtype=torch.float32, device=device),
+            in_buf, ins = _packed((q, k, v, do), device)
+            in_buf.copy_(self.host_in_buf)
+            out_buf, (o, dq, dk, dv, lse) = _packed(out_like, device)
+            outs = dict(o=o, dq=dq, dk=dk, dv=dv, lse=lse,
                         ws=da.new_workspace(*w.shape, device=device, stored_ds=stored_ds))
             self.sets.append((ins, outs))
+            self.bufs.append((in_buf, out_buf))
         self.scale = w.softmax_scale
 
     def set_bytes(self):
@@ -376,18 +396,18 @@ def run_gpu_arm(args, world, rank):
                         else delta_bytes / (v * 1e-3) / 1e9) for n, v in per_kernel_ms.items()}
 
     # End to end through the public API with host buffers.  Every step copies
-    # its inputs from pinned host memory, runs attn_fwd + attn_bwd and reads
-    # all five results back into pinned host memory.  Consecutive steps
-    # overlap the way a stream of batches does: the inputs of step i + 1 go in
-    # and the results of step i - 1 come out (one copy stream each way) while
-    # step i computes, on up to three device sets used in turn.
-    hin = P.host_in
+    # its inputs (one buffer) from pinned host memory, runs attn_fwd + attn_bwd
+    # and reads all five results (one buffer) back into pinned host memory.
+    # Consecutive steps overlap the way a stream of batches does: the inputs
+    # of step i + 1 go in and the results of step i - 1 come out (one copy
+    # stream each way) while step i computes, on up to three device sets used
+    # in turn.
+    hin = P.host_in_buf
     nb = min(3, len(P.sets))
-    houts = [{n: torch.empty(P.sets[k][1][n].shape, dtype=P.sets[k][1][n].dtype, pin_memory=True)
-              for n in ("o", "lse", "dq", "dk", "dv")} for k in range(nb)]
+    houts = [torch.empty(P.bufs[k][1].numel(), dtype=torch.uint8, pin_memory=True) for k in range(nb)]
     n_e2e = max(3, min(K, 200))
-    h2d = sum(t.numel() * t.element_size() for t in hin)
-    d2h = sum(t.numel() * t.element_size() for t in houts[0].values())
+    h2d = hin.numel()
+    d2h = houts[0].numel()
     s_c = torch.cuda.current_stream()
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     ev = {n: [torch.cuda.Event() for _ in range(nb)] for n in ("in", "done", "out")}
@@ -395,12 +415,11 @@ def run_gpu_arm(args, world, rank):
     def e2e_run(n):
         for i in range(n):
             k = i % nb
-            ins, outs = P.sets[k]
+            in_buf, out_buf = P.bufs[k]
             with torch.cuda.stream(s_in):
                 if i >= nb:
                     s_in.wait_event(ev["done"][k])  # step i - nb has read these inputs
-                for dst, src in zip(ins, hin):
-                    dst.copy_(src, non_blocking=True)
+                in_buf.copy_(hin, non_blocking=True)
                 ev["in"][k].record(s_in)
             s_c.wait_event(ev["in"][k])
             if i >= nb:
@@ -409,8 +428,7 @@ def run_gpu_arm(args, world, rank):
             ev["done"][k].record(s_c)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(ev["done"][k])
-                for name, h in houts[k].items():
-                    h.copy_(outs[name], non_blocking=True)
+                houts[k].copy_(out_buf, non_blocking=True)
                 ev["out"][k].record(s_out)
 
     e2e_run(3)
@@ -428,7 +446,9 @@ def run_gpu_arm(args, world, rank):
            "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "steps": n_e2e,
            "overlap": f"inputs of step i+1 and results of step i-1 copied on two copy streams "
-                      f"while step i computes ({nb} device sets)"}
+                      f"while step i computes ({nb} device sets)",
+           "copies": "one host-to-device copy of Q, K, V, dO and one device-to-host copy of "
+                     "O, LSE, dQ, dK, dV per step (each set packs them in one buffer)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
