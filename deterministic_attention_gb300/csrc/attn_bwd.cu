@@ -95,13 +95,6 @@ template <int D, class VT>
 __global__ void __launch_bounds__(256, kDeltaBlocksPerSm) attn_delta_kernel(const DeltaArgs a,
                                                                              const __grid_constant__ VT vt) {
   constexpr bool VL = std::is_same<VT, VarlenTable>::value;
-  // Launched as a dependent of whatever precedes it (the forward, in a
-  // training step): everything below reads that kernel's output.  Only after
-  // this wait may the next kernel (the dK/dV step) start its own prologue.
-  griddep_wait();
-  griddep_launch_dependents();
-  // The dQ step's unit counter (two words) starts each backward at zero.
-  if (a.unit_counter != nullptr && blockIdx.x == 0 && threadIdx.x < 2) a.unit_counter[threadIdx.x] = 0u;
   constexpr int kCpr = D / 8;          // 16-byte chunks per row
   constexpr int kRpi = 32 / kCpr;      // rows per warp-wide load
   constexpr int kBatch = 4;            // loads per operand per batch
@@ -113,6 +106,21 @@ __global__ void __launch_bounds__(256, kDeltaBlocksPerSm) attn_delta_kernel(cons
   const long n_batches = (rows + kRows - 1) / kRows;
   const uint4* O = static_cast<const uint4*>(a.o);
   const uint4* dO = static_cast<const uint4*>(a.dout);
+  // This warp's first batch of dO into L2 while the kernel before this one
+  // (the forward, in a training step) may still run; the loads below come
+  // after the wait, so they see the final values either way.
+  if (lane == 0 && gw < n_batches) {
+    const long r0 = gw * kRows;
+    const long nr = rows - r0 < kRows ? rows - r0 : kRows;
+    bulk_prefetch_l2(dO + r0 * kCpr, static_cast<uint32_t>(nr * kCpr * 16));
+  }
+  // Launched as a dependent of whatever precedes it (the forward, in a
+  // training step): everything below reads that kernel's output.  Only after
+  // this wait may the next kernel (the dK/dV step) start its own prologue.
+  griddep_wait();
+  griddep_launch_dependents();
+  // The dQ step's unit counter (two words) starts each backward at zero.
+  if (a.unit_counter != nullptr && blockIdx.x == 0 && threadIdx.x < 2) a.unit_counter[threadIdx.x] = 0u;
   for (long bi = gw; bi < n_batches; bi += n_warps) {
     // (b, t, h) of this lane's row in load step 0, advanced by kRpi rows per
     // step.
