@@ -455,14 +455,16 @@ int dkdv_schedule(int B, int T, int Hq, int Hkv, int D, int causal, int sms, int
 }
 
 // Listed deal of the 64-dim dK/dV kernel's key tiles over NG clusters of C
-// blocks (fixed length, the plain walk; see DkvList).  Tiles with at least x
-// items are shared by a cluster, lighter ones go whole to single blocks.
-// Heaviest first, a shared tile goes to the cluster whose blocks carry the
-// least and adds its share of the items to each of them, a whole tile to the
-// block with the least.  Besides its items a tile costs its end: reading the
-// sums, and when shared sending the peers' rows and waiting for theirs
-// (measured at page3: a shared tile's end and the next tile's start take
-// 4.3-5 us, about four 1.1 us items; a whole tile's about one and a half).
+// blocks (the walk without chunks; see DkvList).  `items[t]`: the items of
+// tile t in walk order.  Tiles with at least x items are shared by a
+// cluster, lighter ones go whole to single blocks.  Heaviest first, a shared
+// tile goes to the cluster whose blocks carry the least and adds its share
+// of the items to each of them, a whole tile to the block with the least.
+// Besides its items a tile costs its end: reading the sums, and when shared
+// sending the peers' rows and waiting for theirs (measured at B = 4, T =
+// 1024, 12 query and 4 KV heads of 64: a shared tile's end and the next
+// tile's start take 4.3-5 us, about four 1.1 us items; a whole tile's end,
+// without the exchange, is taken as one and a half).
 // x is the item count that minimises the largest block load; the list is
 // kept when that load is below the snake walk's under the same costs (always
 // with `force`).  Returns false without a list, or when it does not fit.
