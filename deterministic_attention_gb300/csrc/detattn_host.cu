@@ -9,6 +9,7 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <functional>
 #include <memory>
 #include <mutex>
@@ -548,8 +549,9 @@ bool dkdv_mixed_list(const std::vector<int>& items, int C, int NG, bool force, D
 
 // dkdv_mixed_list for a fixed-length shape (tiles in the unchunked walk's
 // order), the last result kept: one layer's backward asks again every step.
-const DkvList* cached_dkdv_list(int B, int T, int Hq, int Hkv, int causal, int C, int NG,
-                                int deal) {
+// Copied into *out under the lock (another thread may replace the kept one).
+bool cached_dkdv_list(int B, int T, int Hq, int Hkv, int causal, int C, int NG, int deal,
+                      DkvList* out) {
   static std::mutex mu;
   static int key[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
   static DkvList list;
@@ -568,7 +570,8 @@ const DkvList* cached_dkdv_list(int B, int T, int Hq, int Hkv, int causal, int C
     have = dkdv_mixed_list(items, C, NG, deal == 2, &list);
     std::copy(want, want + 8, key);
   }
-  return have ? &list : nullptr;
+  if (have) std::memcpy(out, &list, sizeof(DkvList));
+  return have;
 }
 
 int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
@@ -591,10 +594,13 @@ int dkdv_impl(const void* q, const void* k, const void* v, const void* dout,
       DETATTN_OK)
     return rc;
   if (a.cluster == 1 && ds == nullptr) a.bg_chunk = dkdv_bg_chunk_one(D, a.bg_chunk);
+  DkvList own;
   const DkvList* list = nullptr;
   // (The stored-dS form takes the same deal, so both forms give the same dK, dV.)
   if (D == 64 && a.bg_chunk == 0 && a.cluster > 1 && g_dkdv_deal != 1)
-    list = cached_dkdv_list(B, T, Hq, Hkv, causal, a.cluster, a.n_groups, g_dkdv_deal);
+    list = cached_dkdv_list(B, T, Hq, Hkv, causal, a.cluster, a.n_groups, g_dkdv_deal, &own)
+               ? &own
+               : nullptr;
   // The stored-dS form keeps 64-query items at D = 128.
   const int rows = ds != nullptr && D == 128 ? 64 : dkdv_item_rows(D, a.cluster);
   if ((rc = encode_rows(&mq, q, B, T, Hq, D, rows, "q")) != DETATTN_OK) return rc;
