@@ -1,4 +1,5 @@
-"""bench.py host logic without a GPU: the reference arm's JSON line, and the
+"""bench.py host logic without a GPU: the reference arm's JSON line, the packed
+end-to-end buffers, and the
 multi-process path (world size 2 over gloo, launched by torchrun): rank 0
 alone prints, the max-over-ranks reduction, and clean exits."""
 import json
@@ -83,3 +84,26 @@ def test_max_over_ranks_gloo():
                 p.kill()
                 p.join(10)
         mgr.shutdown()
+
+
+def test_packed_buffers_hold_each_tensor_aligned():
+    """The end-to-end measurement's packed buffers: every view starts on a
+    16-byte boundary (the kernels' TMA maps need it), keeps its shape and
+    dtype, and the views cover the buffer in order without overlap."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    like = [torch.empty((2, 33, 3, 64), dtype=torch.bfloat16), torch.empty((2, 3, 33), dtype=torch.float32),
+            torch.empty((2, 33, 1, 64), dtype=torch.bfloat16), torch.empty((5,), dtype=torch.float32)]
+    buf, views = bench._packed(like, "cpu")
+    assert buf.dtype == torch.uint8
+    end = buf.data_ptr()
+    for v, t in zip(views, like):
+        assert v.shape == t.shape and v.dtype == t.dtype and v.is_contiguous()
+        assert v.data_ptr() % 16 == 0 and v.data_ptr() >= end
+        end = v.data_ptr() + v.numel() * v.element_size()
+    assert end <= buf.data_ptr() + buf.numel()
+    for i, v in enumerate(views):
+        v.fill_(i + 1)
+    for i, v in enumerate(views):
+        assert bool((v == i + 1).all())
