@@ -1,7 +1,7 @@
-"""bench.py host logic without a GPU: the reference arm's JSON line, the packed
-end-to-end buffers, and the
-multi-process path (world size 2 over gloo, launched by torchrun): rank 0
-alone prints, the max-over-ranks reduction, and clean exits."""
+"""bench.py host logic without a GPU: the reference arm's JSON line, the
+packed end-to-end buffers, and the multi-process path (world size 2 over
+gloo, launched by torchrun): rank 0 alone prints, the max-over-ranks
+reduction, and clean exits."""
 import json
 import os
 import subprocess
